@@ -1,0 +1,329 @@
+"""Throughput of one Transformer layer forward (Llama-3-8B-shaped, seq 4096) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference] [--workload NAME]
+
+A step is one call of mt_layer_forward (all nine steps of the layer: norm, QKV GEMM + RoPE,
+causal GQA flash attention, output projection + residual, norm, fc1 + SwiGLU, fc2 + residual)
+on inputs already resident in HBM.  L2 is flushed (a 256 MiB write) between steps, outside the
+timed spans; each step is timed with CUDA events on the launching stream.  `e2e` repeats the
+measurement through mt_layer_forward_host with pinned host buffers (x copied in and y copied out
+inside every step).  With N > 1 (torchrun) every rank runs an independent replica -- the layer
+forward of one data-parallel replica needs no collective -- and the slowest rank's time counts.
+
+--impl reference times the float64 CPU oracle (the "reference" arm of this build) on the host
+cores: each step is a bounded sample of the same workload (K and V of every token plus the whole
+layer for the last rows of the sequence), reported in the same unit.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "Layer fwd TFLOP/s & MFU vs GB300 bf16 dense peak; tokens/s per layer (1 GPU)"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def workload_desc(cfg) -> str:
+    return (f"{cfg.name}: batch {cfg.batch}, seq {cfg.seq}, hidden {cfg.hidden}, {cfg.heads} heads x {cfg.head_dim}, "
+            f"{cfg.groups} query groups, {'SwiGLU' if cfg.act == 'swiglu' else 'GeLU-tanh'} ffn {cfg.ffn}, "
+            f"{'RMSNorm' if cfg.norm == 'rms' else 'LayerNorm'}, RoPE base {cfg.rope_base:g}, causal, "
+            f"TP {cfg.tp} (one rank)")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def sample_flops(cfg, rows) -> float:
+    """Algorithmic FLOPs of the oracle's row-sampled pass: K and V of every token, then the whole
+    layer for `rows` (causal attention over positions 0..s of each sampled row)."""
+    T, H, d = cfg.tokens, cfg.hidden, cfg.head_dim
+    qw, kvw, f = cfg.heads * d, cfg.groups * d, cfg.ffn
+    f1 = 2 * f if cfg.act == "swiglu" else f
+    pos = np.asarray(rows) // cfg.batch
+    per_row = 2.0 * H * qw + 2.0 * qw * H + 2.0 * H * f1 + 2.0 * f * H
+    attn = float(np.sum(4.0 * d * (pos + 1) * cfg.heads))
+    return 2.0 * T * H * 2 * kvw + per_row * len(rows) + attn
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def oracle_sample(cfg, inp, n_rows):
+    import oracle
+    rows = np.arange(cfg.tokens - n_rows, cfg.tokens)
+    t0 = time.perf_counter()
+    oracle.layer_forward(cfg, inp, rows=rows)
+    dt = time.perf_counter() - t0
+    return sample_flops(cfg, rows), dt
+
+
+# ------------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms while a region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.index), "-lms", "100"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self._t.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------ native arm
+def run_native(args):
+    import torch
+    import torch.distributed as dist
+
+    from megatron_tensor_transformer_gpt_gb300 import mt_layer as ml
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    cfg = synth.CONFIGS[args.workload]
+    inp = synth.make_inputs(cfg, seed=rank)
+
+    def to_dev(bits):
+        return None if bits is None else torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    shards = inp if cfg.tp == 1 else synth.shard_weights(cfg, inp, cfg.tp, 0)
+    tens = {k: to_dev(v) for k, v in shards.items()}
+    x = tens.pop("x").reshape(cfg.tokens, cfg.hidden)
+    layer = ml.Layer.from_config(cfg, tp_rank=0)
+    w = layer.weights(tens)
+    y = torch.empty(cfg.tokens, cfg.hidden, dtype=torch.bfloat16, device=dev)
+    layer.workspace(cfg.seq, cfg.batch, dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    flops = cfg.flops()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # warm-up, extended to about half a second of load so the clock samples see a busy GPU
+    for _ in range(args.warmup):
+        layer.forward(x, cfg.seq, cfg.batch, w, y)
+    torch.cuda.synchronize()
+    layer.status()
+
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    smi_index = int(vis.split(",")[local]) if vis and vis.split(",")[local].strip().isdigit() else local
+    clocks = ClockSampler(smi_index)
+    clocks.start()
+    t_end = time.perf_counter() + 0.5
+    while time.perf_counter() < t_end:
+        layer.forward(x, cfg.seq, cfg.batch, w, y)
+        torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ml.mt_layer_profile_enable(layer.handle, True)
+    ml.mt_layer_profile_read(layer.handle)
+    torch.cuda.synchronize()
+    barrier()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        layer.forward(x, cfg.seq, cfg.batch, w, y)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    prof = ml.mt_layer_profile_read(layer.handle)
+    ml.mt_layer_profile_enable(layer.handle, False)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+
+    # end to end through the host-buffer entry point
+    xh = x.cpu().pin_memory()
+    yh = torch.empty(cfg.tokens, cfg.hidden, dtype=torch.bfloat16).pin_memory()
+    for _ in range(2):
+        layer.forward_host(xh, cfg.seq, cfg.batch, w, yh)
+    torch.cuda.synchronize()
+    ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        ev2[i][0].record(stream)
+        layer.forward_host(xh, cfg.seq, cfg.batch, w, yh)
+        ev2[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    layer.status()
+    e2e_ms = [a.elapsed_time(b) for a, b in ev2]
+
+    total_ms = sum(step_ms)
+    total_e2e = sum(e2e_ms)
+    if world > 1:
+        t = torch.tensor([total_ms, total_e2e], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, total_e2e = t.tolist()
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    e2e_value = world * flops * args.steps / (total_e2e * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    peak_tf = peaks["bf16_tflops"]
+    launches, fc1_ms = prof["gemm_fc1"]
+    fc1_avg = fc1_ms / max(1, launches)
+    f1 = cfg.fc1_out // cfg.tp
+    fc1_flops = 2.0 * cfg.tokens * cfg.hidden * f1
+    achieved = fc1_flops / (fc1_avg * 1e-3) / 1e12
+    kernel_launches = sum(n for n, _ in prof.values())
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        n_rows = 256
+        sf, dt = oracle_sample(cfg, inp, n_rows)
+        cpu = {"value": sf / dt / 1e12, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+               "sample": f"float64 NumPy oracle: K/V of all {cfg.tokens} tokens + the whole layer for the last "
+                         f"{n_rows} rows ({sf / 1e9:.1f} GFLOP algorithmic, {dt:.1f} s)"}
+
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights)",
+        "config": {"workload": workload_desc(cfg), "seq": cfg.seq, "batch": cfg.batch, "tokens": cfg.tokens,
+                   "gflop_per_step": flops / 1e9, "l2": "flushed by a 256 MiB write between timed steps",
+                   "parallelism": f"replicas x{world}"},
+        "mfu": value / peak_tf, "mfu_vs_sustained": value / peaks["bf16_tflops_sustained"],
+        "peak_source": f"{peak_src}: bf16 {peak_tf} TF/s burst, {peaks['bf16_tflops_sustained']} sustained",
+        "tokens_per_s": world * cfg.tokens * args.steps / (total_ms * 1e-3),
+        "per_kernel_ms": {k: (ms / n if n else 0.0) for k, (n, ms) in prof.items()},
+        "roofline": {"kernel": "gemm_fc1 (fc1 GEMM + SwiGLU epilogue)", "bound": "tensor", "achieved": achieved,
+                     "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": None,
+                     "peak_note": f"{peak_src} cuBLAS bf16 burst"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": cfg.tokens * cfg.hidden * 2,
+                "d2h_bytes_per_step": cfg.tokens * cfg.hidden * 2, "ms_per_step": total_e2e / args.steps},
+        "gpu_launches": kernel_launches,
+        "clocks": clk,
+    }
+    print(json.dumps(out))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------------ reference arm
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cfg = synth.CONFIGS[args.workload]
+    inp = synth.make_inputs(cfg, seed=0)
+    n_rows = 16
+    for _ in range(args.warmup):
+        oracle_sample(cfg, inp, n_rows)
+    fl, tt = 0.0, 0.0
+    for _ in range(args.steps):
+        f, dt = oracle_sample(cfg, inp, n_rows)
+        fl += f
+        tt += dt
+    value = fl / tt / 1e12
+    sample = (f"float64 NumPy oracle per step: K/V of all {cfg.tokens} tokens + the whole layer for the last "
+              f"{n_rows} rows ({fl / args.steps / 1e9:.1f} GFLOP algorithmic)")
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": tt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": workload_desc(cfg), "seq": cfg.seq, "batch": cfg.batch,
+                      "parallelism": "host cores"},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("native", "reference"), default="native")
+    ap.add_argument("--workload", default="llama8b", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

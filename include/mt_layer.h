@@ -1,0 +1,165 @@
+/*
+ * mt_layer.h -- C ABI of a GB300 (sm_103a) forward pass of one GPT/Llama Transformer layer,
+ * as one tensor-parallel (TP) rank computes it.
+ *
+ * What is computed (page titles and sections of the Megatron pages this follows):
+ *   "快速入门 / Pai-Megatron-Patch 项目深度学习总结文档" §3.1, layer tree and layer spec:
+ *       input_layernorm -> SelfAttention(linear_qkv, core_attention [causal], linear_proj)
+ *       -> bias-dropout-add -> pre_mlp_layernorm -> MLP(linear_fc1, linear_fc2) -> bias-dropout-add.
+ *   "Megatron-LM 深度学习与源码分析文档" Part 2 §2 (Tensor Parallel):
+ *       Y = XW; column-parallel W=[W_1..W_p], Y_i = X W_i; row-parallel W=[W_1;..;W_p],
+ *       Y_i = X_i W_i, Y = sum_i Y_i; QKV is column-parallel with heads/TP heads per rank;
+ *       MLP Z = phi(X W_1), Y = Z W_2 with fc1 column- and fc2 row-parallel (SwiGLU widens fc1).
+ *   "ai阅读megatron", TransformerConfig (num_query_groups => GQA) and the Llama flag sets
+ *       (--swiglu, --normalization RMSNorm, rotary position embeddings).
+ *   Dropout is the identity (rate 0.0 in the launch flags of "快速入门" §6.1); the softmax
+ *   scale is 1/sqrt(head_dim) (query-key layer scaling disabled, same flags).
+ *
+ * Notation: T = seq*batch tokens, H = hidden, d = head_dim, nh_r = heads/tp, ng_r = groups/tp,
+ * q_w = nh_r*d, kv_w = ng_r*d, f_r = ffn/tp, f1_r = 2*f_r (SwiGLU) or f_r (GeLU).
+ *
+ * Layouts.  All tensors are bfloat16, row-major.  Activations use the [seq, batch, hidden]
+ * order, i.e. a [T, H] matrix whose row t = s*batch + b.  Weights are [out, in] (rows are
+ * output features, the F.linear convention):
+ *   w_qkv [q_w + 2*kv_w, H] rows = [this rank's q heads | its k groups | its v groups],
+ *         each head d consecutive rows;  w_o [H, q_w];  w_fc1 [f1_r, H] rows = [gate | up]
+ *         for SwiGLU;  w_fc2 [H, f_r];  norm gains/shifts [H];  biases [out].
+ *   RoPE: rotate-half pairs (i, i+d/2), angle = s * rope_base^(-2i/d), on q and k after the bias.
+ *   GQA: q head h (within the rank) reads kv group h / (nh_r/ng_r).
+ *
+ * Ownership.  The caller owns x, the weights, every output and the workspace (all device
+ * memory unless stated).  The library owns the handle and a 4-byte device error word,
+ * allocated in mt_layer_create and freed in mt_layer_destroy.  Calls that take a stream are
+ * asynchronous on it; a handle must not be used from two host threads at once.
+ *
+ * Errors.  Every call returns an mt_status; on failure no kernel is launched and
+ * mt_last_error() describes the problem (thread-local string, valid until the next call on the
+ * same thread).  A kernel that stops waiting (bounded waits on barriers; it never hangs)
+ * records MT_ERR_DEVICE_TIMEOUT in the error word; mt_layer_status reports and clears it.
+ */
+#ifndef MT_LAYER_H
+#define MT_LAYER_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct mt_layer mt_layer; /* opaque, library-owned */
+
+enum { MT_NORM_RMS = 0, MT_NORM_LAYER = 1 };
+enum { MT_ACT_SWIGLU = 0, MT_ACT_GELU_TANH = 1 };
+
+typedef enum {
+  MT_OK = 0,
+  MT_ERR_INVALID_ARG = 1,     /* null/misaligned pointer, non-positive size, bad enum        */
+  MT_ERR_UNSUPPORTED = 2,     /* well-formed but outside the supported shapes (see create)   */
+  MT_ERR_NO_WORKSPACE = 3,    /* no workspace set, or smaller than mt_layer_workspace_bytes  */
+  MT_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed (message has the detail)  */
+  MT_ERR_DEVICE_TIMEOUT = 5,  /* a kernel gave up on a barrier wait; its outputs are invalid */
+  MT_ERR_UNIMPLEMENTED = 6
+} mt_status;
+
+/* One rank's weights.  Device pointers to bf16, 16-byte aligned.  Norm shifts are ignored
+ * for RMSNorm and required for LayerNorm.  A NULL bias means "no bias".  Row-parallel biases
+ * (b_o, b_fc2) are added once, after the partial sums (bias-dropout-add). */
+typedef struct {
+  const void *norm1_w, *norm1_b; /* [H]                 */
+  const void *w_qkv, *b_qkv;     /* [q_w + 2 kv_w, H]   */
+  const void *w_o, *b_o;         /* [H, q_w], [H]       */
+  const void *norm2_w, *norm2_b; /* [H]                 */
+  const void *w_fc1, *b_fc1;     /* [f1_r, H]           */
+  const void *w_fc2, *b_fc2;     /* [H, f_r], [H]       */
+} mt_weights;
+
+/* Create a handle for one rank (tp_rank of tp_size) of a layer with the given full-model
+ * shape ("ai阅读megatron", TransformerConfig fields hidden_size, num_attention_heads,
+ * num_query_groups, kv_channels, ffn_hidden_size).  rope_base == 0 disables RoPE.
+ * Supported: head_dim in {64, 128}; heads % query_groups == 0; heads, query_groups and ffn
+ * divisible by tp_size; hidden % 8 == 0, hidden <= 8192; (ffn/tp_size) % 8 == 0.
+ * Needs the current CUDA device to be sm_103 (GB300).  Host call; allocates 4 bytes of
+ * device memory.  Returns MT_ERR_UNSUPPORTED / MT_ERR_INVALID_ARG otherwise. */
+int mt_layer_create(int hidden, int heads, int query_groups, int head_dim, int ffn, int norm, int act,
+                    float rope_base, int tp_size, int tp_rank, mt_layer** out);
+
+/* Norm epsilon (inside the square root); default 1e-5. */
+int mt_layer_set_eps(mt_layer* L, float eps);
+
+/* Device workspace needed for a call with this seq and batch (intermediates: normed input,
+ * q/k/v in attention layout, attention output, h, normed h, MLP hidden, RoPE table, and
+ * host-path staging for x and y). */
+int mt_layer_workspace_bytes(const mt_layer* L, int seq, int batch, size_t* bytes);
+
+/* Lend the library a device buffer of `bytes` (256-byte aligned) for the calls that follow.
+ * The caller keeps ownership and must keep it alive while calls using it are in flight. */
+int mt_layer_set_workspace(mt_layer* L, void* dev_ptr, size_t bytes);
+
+/* Whole layer.  x [T, H] -> y_partial [T, H].
+ *   tp_size == 1: y = h + fc2(act(fc1(norm2(h)))) + b_fc2, with h = x + o_proj(attn(norm1(x))) + b_o.
+ *   tp_size  > 1: the all-reduce between the two blocks is replaced by the identity,
+ *                 h = x + Y_attn,i + b_o, and y_partial = Y_mlp,i(h) is this rank's
+ *                 pre-reduce row-parallel partial (no bias, no residual).
+ * 8 kernel launches on `cuda_stream` (a cudaStream_t; NULL = legacy default stream). */
+int mt_layer_forward(mt_layer* L, const void* x, int seq, int batch, const mt_weights* w, void* y_partial,
+                     void* cuda_stream);
+
+/* Attention block only: attn_out [T, H] = Y_attn,i, this rank's pre-reduce partial of the
+ * output projection (no bias, no residual).  The caller sums the partials over ranks and
+ * forms h = x + sum_i Y_attn,i + b_o ("Megatron-LM 深度学习与源码分析文档" Part 2 §2, Row Parallel). */
+int mt_layer_forward_attn(mt_layer* L, const void* x, int seq, int batch, const mt_weights* w, void* attn_out,
+                          void* cuda_stream);
+
+/* MLP block only: y_partial [T, H] = Y_mlp,i(h), this rank's pre-reduce fc2 partial
+ * (no bias, no residual); the caller forms y = h + sum_i Y_mlp,i + b_fc2. */
+int mt_layer_forward_mlp(mt_layer* L, const void* h, int seq, int batch, const mt_weights* w, void* y_partial,
+                         void* cuda_stream);
+
+/* mt_layer_forward with x and y in HOST memory (pinned for asynchronous copies): copies x
+ * into the workspace, runs the layer, copies y back, all on `cuda_stream`; the host buffers
+ * must stay valid until the stream reaches this point. */
+int mt_layer_forward_host(mt_layer* L, const void* x_host, int seq, int batch, const mt_weights* w,
+                          void* y_host, void* cuda_stream);
+
+/* Where an intermediate lives inside the workspace (for inspection in tests).  `which`:
+ * 0 norm1 out [T,H]; 1 q [batch, nh_r, seq, d] after RoPE; 2 k [batch, ng_r, seq, d] after RoPE;
+ * 3 v transposed [batch, ng_r, d, seq_pad] (seq_pad = seq rounded up to 8);
+ * 4 attention out [T, q_w]; 5 h [T,H]; 6 norm2 out [T,H]; 7 MLP hidden [T, f_r];
+ * 8 RoPE table [seq, d/2] float2 (cos, sin). */
+int mt_layer_workspace_region(const mt_layer* L, int seq, int batch, int which, size_t* offset, size_t* bytes);
+
+/* Synchronise with the work queued by this handle (all streams) and report a device-side
+ * failure recorded since the last call (MT_ERR_DEVICE_TIMEOUT), clearing it. */
+int mt_layer_status(mt_layer* L);
+
+/* Thread-local description of the last failure on this thread ("" after success). */
+const char* mt_last_error(void);
+
+void mt_layer_destroy(mt_layer* L);
+
+/* Per-kernel timing.  While enabled, every kernel this handle launches is bracketed by a pair of
+ * CUDA events on its stream.  Kernel slots: 0 RoPE table, 1 norm1, 2 QKV GEMM, 3 attention,
+ * 4 output-projection GEMM, 5 norm2, 6 fc1 GEMM, 7 fc2 GEMM (MT_PROFILE_SLOTS).  Up to 8192
+ * launches are kept.  mt_layer_profile_read waits for the recorded events, writes per slot the
+ * number of launches and their summed milliseconds into the caller's arrays (MT_PROFILE_SLOTS
+ * entries each) and clears the record. */
+#define MT_PROFILE_SLOTS 8
+int mt_layer_profile_enable(mt_layer* L, int enable);
+int mt_layer_profile_read(mt_layer* L, int* launches, double* total_ms);
+
+/* ---- utility entry points (kernel-level; used by the parity tests) -------------------- */
+
+/* C[M, N] = A[M, K] * B[N, K]^T in bf16 with fp32 accumulation, on the layer's tcgen05 GEMM
+ * ("Megatron-LM 深度学习与源码分析文档" Part 2 §2, Y = XW with W stored [out, in]).
+ * Device pointers, 16-byte aligned; K % 8 == 0 and N % 8 == 0. */
+int mt_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, void* cuda_stream);
+
+/* Fault-detection self test: launches one CTA that waits on a barrier nothing will complete,
+ * giving up after `limit_us` microseconds (1..1000000).  Returns MT_ERR_DEVICE_TIMEOUT when the
+ * bounded wait fired and reported itself (the expected outcome), MT_OK if it did not fire. */
+int mt_selftest_bounded_wait(int limit_us);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MT_LAYER_H */

@@ -1,0 +1,623 @@
+// C ABI of the layer library: handle, argument checks, workspace layout, TMA descriptors and
+// the kernel sequence of one layer forward on the caller's stream.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/mt_layer.h"
+#include "internal.h"
+
+using mt::bf16;
+
+struct mt_layer {
+  int hidden, heads, groups, head_dim, ffn, norm, act, tp, rank;
+  float rope_base, eps;
+  int nh_r, ng_r, f_r, f1_r, q_w, kv_w;
+  int device;
+  int* d_err;       // device error word (mt_status code of the first device-side failure)
+  double* d_theta;  // [head_dim/2] RoPE frequencies base^(-2i/d), or null
+  void* ws;
+  size_t ws_bytes;
+  // per-kernel timing (mt_layer_profile_*)
+  bool profiling;
+  struct Rec {
+    int slot;
+    cudaEvent_t a, b;
+  };
+  std::vector<Rec> recs;
+  std::vector<cudaEvent_t> pool;
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int ok() {
+  g_last_error.clear();
+  return MT_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(MT_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+enum Slot { kSlotRope = 0, kSlotNorm1, kSlotQkv, kSlotAttn, kSlotO, kSlotNorm2, kSlotFc1, kSlotFc2 };
+constexpr size_t kMaxRecords = 8192;
+
+cudaEvent_t pool_event(mt_layer* L) {
+  if (!L->pool.empty()) {
+    cudaEvent_t e = L->pool.back();
+    L->pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Brackets one kernel launch with events when the handle is profiling.
+struct Timed {
+  mt_layer* L;
+  cudaStream_t st;
+  bool on;
+  cudaEvent_t a = nullptr;
+  int slot;
+  Timed(mt_layer* l, int s, cudaStream_t stream)
+      : L(l), st(stream), on(l != nullptr && l->profiling && l->recs.size() < kMaxRecords), slot(s) {
+    if (on) {
+      a = pool_event(L);
+      cudaEventRecord(a, st);
+    }
+  }
+  ~Timed() {
+    if (on) {
+      cudaEvent_t b = pool_event(L);
+      cudaEventRecord(b, st);
+      L->recs.push_back({slot, a, b});
+    }
+  }
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------------------ workspace layout
+enum Region { kXn = 0, kQ, kK, kVt, kO, kH, kHn, kA, kRope, kXStage, kYStage, kNumRegions };
+
+struct Layout {
+  size_t off[kNumRegions];
+  size_t size[kNumRegions];
+  size_t total;
+  int seq_pad;
+};
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+Layout layout_for(const mt_layer* L, int S, int B) {
+  Layout lay{};
+  const size_t T = static_cast<size_t>(S) * B;
+  const size_t d = L->head_dim;
+  lay.seq_pad = static_cast<int>(round_up(S, 8));
+  lay.size[kXn] = T * L->hidden * 2;
+  lay.size[kQ] = static_cast<size_t>(B) * L->nh_r * S * d * 2;
+  lay.size[kK] = static_cast<size_t>(B) * L->ng_r * S * d * 2;
+  lay.size[kVt] = static_cast<size_t>(B) * L->ng_r * d * lay.seq_pad * 2;
+  lay.size[kO] = T * L->q_w * 2;
+  lay.size[kH] = T * L->hidden * 2;
+  lay.size[kHn] = T * L->hidden * 2;
+  lay.size[kA] = T * L->f_r * 2;
+  lay.size[kRope] = L->rope_base > 0.f ? static_cast<size_t>(S) * (d / 2) * sizeof(float2) : 0;
+  lay.size[kXStage] = T * L->hidden * 2;
+  lay.size[kYStage] = T * L->hidden * 2;
+  size_t o = 0;
+  for (int r = 0; r < kNumRegions; ++r) {
+    lay.off[r] = o;
+    o = round_up(o + lay.size[r], 1024);
+  }
+  lay.total = o;
+  return lay;
+}
+
+template <typename T>
+T* region(const mt_layer* L, const Layout& lay, Region r) {
+  return reinterpret_cast<T*>(static_cast<char*>(L->ws) + lay.off[r]);
+}
+
+// ------------------------------------------------------------------ TMA descriptors
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// Row-major bf16 matrix [rows, cols] with `pitch` elements per row; box = 64 columns x box_rows.
+int map_2d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint64_t pitch, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return fail(MT_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {pitch * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MT_ERR_CUDA, "cuTensorMapEncodeTiled (2d %llu x %llu) failed: %d",
+                                     (unsigned long long)rows, (unsigned long long)cols, (int)r);
+  return MT_OK;
+}
+
+// bf16 tensor [d2][d1][d0] with element pitches p1 (between d1 rows) and p2 (between d2 slabs);
+// box = 64 x box1 x 1.
+int map_3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t p1, uint64_t p2,
+           uint32_t box1) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return fail(MT_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {p1 * 2, p2 * 2};
+  const cuuint32_t box[3] = {64, box1, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MT_ERR_CUDA, "cuTensorMapEncodeTiled (3d) failed: %d", (int)r);
+  return MT_OK;
+}
+
+mt::GemmParams gemm_params(int M, int N, int K, bool swiglu, int* err) {
+  mt::GemmParams p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.tiles_m = (M + 127) / 128;
+  p.tiles_n = swiglu ? (N + 127) / 128 : (N + 255) / 256;
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  p.b_row_step = swiglu ? N : 128;
+  p.err = err;
+  return p;
+}
+
+// One GEMM: A [M, K] (pitch lda) x W [rows_w, K]^T with the given epilogue.
+int run_gemm(mt_layer* L, int slot, int mode, const void* A, int lda, const void* W, int rows_w, int M, int N, int K,
+             mt::GemmParams p, cudaStream_t st) {
+  CUtensorMap ta, tb;
+  int rc = map_2d(&ta, A, K, M, lda, 128);
+  if (rc) return rc;
+  rc = map_2d(&tb, W, K, rows_w, K, 128);
+  if (rc) return rc;
+  cudaError_t e;
+  {
+    Timed t(L, slot, st);
+    e = mt::launch_gemm(mode, ta, tb, p, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
+  return MT_OK;
+}
+
+int check_weights(const mt_layer* L, const mt_weights* w, bool attn, bool mlp) {
+  if (w == nullptr) return fail(MT_ERR_INVALID_ARG, "weights struct is NULL");
+  struct {
+    const void* p;
+    const char* name;
+    bool required;
+  } items[] = {
+      {w->norm1_w, "norm1_w", attn},
+      {w->norm1_b, "norm1_b", attn && L->norm == MT_NORM_LAYER},
+      {w->w_qkv, "w_qkv", attn},
+      {w->b_qkv, "b_qkv", false},
+      {w->w_o, "w_o", attn},
+      {w->b_o, "b_o", false},
+      {w->norm2_w, "norm2_w", mlp},
+      {w->norm2_b, "norm2_b", mlp && L->norm == MT_NORM_LAYER},
+      {w->w_fc1, "w_fc1", mlp},
+      {w->b_fc1, "b_fc1", false},
+      {w->w_fc2, "w_fc2", mlp},
+      {w->b_fc2, "b_fc2", false},
+  };
+  for (auto& it : items) {
+    if (it.required && it.p == nullptr) return fail(MT_ERR_INVALID_ARG, "weight %s is NULL", it.name);
+    if (it.p != nullptr && !aligned16(it.p)) return fail(MT_ERR_INVALID_ARG, "weight %s is not 16-byte aligned", it.name);
+  }
+  return MT_OK;
+}
+
+int check_call(const mt_layer* L, const void* in, const void* out, int S, int B, Layout* lay) {
+  if (L == nullptr) return fail(MT_ERR_INVALID_ARG, "handle is NULL");
+  if (in == nullptr || out == nullptr) return fail(MT_ERR_INVALID_ARG, "input or output pointer is NULL");
+  if (!aligned16(in) || !aligned16(out)) return fail(MT_ERR_INVALID_ARG, "input/output must be 16-byte aligned");
+  if (S <= 0 || B <= 0) return fail(MT_ERR_INVALID_ARG, "seq and batch must be positive (got %d, %d)", S, B);
+  if (static_cast<long long>(S) * B > (1LL << 30)) return fail(MT_ERR_UNSUPPORTED, "seq*batch too large");
+  *lay = layout_for(L, S, B);
+  if (L->ws == nullptr) return fail(MT_ERR_NO_WORKSPACE, "no workspace set (need %zu bytes)", lay->total);
+  if (L->ws_bytes < lay->total)
+    return fail(MT_ERR_NO_WORKSPACE, "workspace has %zu bytes, this call needs %zu", L->ws_bytes, lay->total);
+  return MT_OK;
+}
+
+// ------------------------------------------------------------------ the two blocks
+// Attention block: norm1 -> QKV GEMM (+bias, RoPE, scatter) -> flash attention -> output projection.
+// out_mode kEpiStore writes the rank's partial; kEpiResid writes h = x + Y + b_o.
+int run_attention_block(mt_layer* L, const Layout& lay, const void* x, int S, int B, const mt_weights* w, void* out,
+                        int out_mode, cudaStream_t st) {
+  const int T = S * B, H = L->hidden, d = L->head_dim;
+  cudaError_t e;
+  float2* rope = nullptr;
+  if (L->rope_base > 0.f) {
+    rope = region<float2>(L, lay, kRope);
+    Timed t(L, kSlotRope, st);
+    e = mt::launch_rope_table(rope, L->d_theta, S, d / 2, st);
+    if (e != cudaSuccess) return cuda_fail(e, "RoPE table launch");
+  }
+  bf16* xn = region<bf16>(L, lay, kXn);
+  {
+    Timed t(L, kSlotNorm1, st);
+    e = mt::launch_norm(L->norm == MT_NORM_LAYER, static_cast<const bf16*>(x), static_cast<const bf16*>(w->norm1_w),
+                      static_cast<const bf16*>(w->norm1_b), xn, T, H, L->eps, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "norm1 launch");
+
+  bf16 *q = region<bf16>(L, lay, kQ), *k = region<bf16>(L, lay, kK), *vt = region<bf16>(L, lay, kVt);
+  const int nqkv = L->q_w + 2 * L->kv_w;
+  mt::GemmParams p = gemm_params(T, nqkv, H, false, L->d_err);
+  p.bias = static_cast<const bf16*>(w->b_qkv);
+  p.q = q;
+  p.k = k;
+  p.vt = vt;
+  p.rope = rope;
+  p.seq = S;
+  p.batch = B;
+  p.head_dim = d;
+  p.q_w = L->q_w;
+  p.kv_w = L->kv_w;
+  p.nh = L->nh_r;
+  p.ng = L->ng_r;
+  p.seq_pad = lay.seq_pad;
+  int rc = run_gemm(L, kSlotQkv, mt::kEpiQkv, xn, H, w->w_qkv, nqkv, T, nqkv, H, p, st);
+  if (rc) return rc;
+
+  CUtensorMap tq, tk, tv;
+  if ((rc = map_3d(&tq, q, d, S, static_cast<uint64_t>(B) * L->nh_r, d, static_cast<uint64_t>(S) * d, 128))) return rc;
+  if ((rc = map_3d(&tk, k, d, S, static_cast<uint64_t>(B) * L->ng_r, d, static_cast<uint64_t>(S) * d, 128))) return rc;
+  if ((rc = map_3d(&tv, vt, S, d, static_cast<uint64_t>(B) * L->ng_r, lay.seq_pad,
+                   static_cast<uint64_t>(d) * lay.seq_pad, static_cast<uint32_t>(d))))
+    return rc;
+  bf16* o = region<bf16>(L, lay, kO);
+  mt::AttnParams ap{};
+  ap.seq = S;
+  ap.batch = B;
+  ap.nh = L->nh_r;
+  ap.ng = L->ng_r;
+  ap.num_qb = (S + 127) / 128;
+  ap.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+  ap.o = o;
+  ap.ldo = L->q_w;
+  ap.err = L->d_err;
+  {
+    Timed t(L, kSlotAttn, st);
+    e = mt::launch_attention(d, tq, tk, tv, ap, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+
+  p = gemm_params(T, H, L->q_w, false, L->d_err);
+  p.out = static_cast<bf16*>(out);
+  p.ldo = H;
+  if (out_mode == mt::kEpiResid) {
+    p.bias = static_cast<const bf16*>(w->b_o);
+    p.resid = static_cast<const bf16*>(x);
+    p.ldr = H;
+  }
+  return run_gemm(L, kSlotO, out_mode, o, L->q_w, w->w_o, H, T, H, L->q_w, p, st);
+}
+
+// MLP block: norm2 -> fc1 GEMM (+bias, SwiGLU / GeLU) -> fc2 GEMM.
+// out_mode kEpiStore writes the rank's partial; kEpiResid writes y = h + Y + b_fc2.
+int run_mlp_block(mt_layer* L, const Layout& lay, const void* h, int S, int B, const mt_weights* w, void* out,
+                  int out_mode, cudaStream_t st) {
+  const int T = S * B, H = L->hidden;
+  bf16* hn = region<bf16>(L, lay, kHn);
+  cudaError_t e;
+  {
+    Timed t(L, kSlotNorm2, st);
+    e = mt::launch_norm(L->norm == MT_NORM_LAYER, static_cast<const bf16*>(h),
+                                  static_cast<const bf16*>(w->norm2_w), static_cast<const bf16*>(w->norm2_b), hn, T,
+                                  H, L->eps, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "norm2 launch");
+  bf16* a = region<bf16>(L, lay, kA);
+  const bool swiglu = L->act == MT_ACT_SWIGLU;
+  mt::GemmParams p = gemm_params(T, L->f_r, H, swiglu, L->d_err);
+  p.out = a;
+  p.ldo = L->f_r;
+  p.bias = static_cast<const bf16*>(w->b_fc1);
+  int rc = run_gemm(L, kSlotFc1, swiglu ? mt::kEpiSwiglu : mt::kEpiGelu, hn, H, w->w_fc1, L->f1_r, T, L->f_r, H, p, st);
+  if (rc) return rc;
+  p = gemm_params(T, H, L->f_r, false, L->d_err);
+  p.out = static_cast<bf16*>(out);
+  p.ldo = H;
+  if (out_mode == mt::kEpiResid) {
+    p.bias = static_cast<const bf16*>(w->b_fc2);
+    p.resid = static_cast<const bf16*>(h);
+    p.ldr = H;
+  }
+  return run_gemm(L, kSlotFc2, out_mode, a, L->f_r, w->w_fc2, H, T, H, L->f_r, p, st);
+}
+
+int forward_device(mt_layer* L, const Layout& lay, const void* x, int S, int B, const mt_weights* w, void* y,
+                   cudaStream_t st) {
+  bf16* h = region<bf16>(L, lay, kH);
+  int rc = run_attention_block(L, lay, x, S, B, w, h, mt::kEpiResid, st);
+  if (rc) return rc;
+  return run_mlp_block(L, lay, h, S, B, w, y, L->tp == 1 ? mt::kEpiResid : mt::kEpiStore, st);
+}
+
+}  // namespace
+
+namespace mt {
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+}  // namespace mt
+
+// ====================================================================== exported C ABI
+extern "C" {
+
+int mt_layer_create(int hidden, int heads, int query_groups, int head_dim, int ffn, int norm, int act,
+                    float rope_base, int tp_size, int tp_rank, mt_layer** out) {
+  if (out == nullptr) return fail(MT_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (hidden <= 0 || heads <= 0 || query_groups <= 0 || head_dim <= 0 || ffn <= 0 || tp_size <= 0)
+    return fail(MT_ERR_INVALID_ARG, "sizes must be positive");
+  if (tp_rank < 0 || tp_rank >= tp_size) return fail(MT_ERR_INVALID_ARG, "tp_rank %d outside [0, %d)", tp_rank, tp_size);
+  if (norm != MT_NORM_RMS && norm != MT_NORM_LAYER) return fail(MT_ERR_INVALID_ARG, "unknown norm %d", norm);
+  if (act != MT_ACT_SWIGLU && act != MT_ACT_GELU_TANH) return fail(MT_ERR_INVALID_ARG, "unknown activation %d", act);
+  if (!(rope_base >= 0.f) || std::isinf(rope_base)) return fail(MT_ERR_INVALID_ARG, "rope_base must be finite and >= 0");
+  if (head_dim != 64 && head_dim != 128) return fail(MT_ERR_UNSUPPORTED, "head_dim must be 64 or 128 (got %d)", head_dim);
+  if (heads % query_groups) return fail(MT_ERR_UNSUPPORTED, "heads %% query_groups != 0");
+  if (heads % tp_size || query_groups % tp_size || ffn % tp_size)
+    return fail(MT_ERR_UNSUPPORTED, "heads, query_groups and ffn must be divisible by tp_size");
+  if (hidden % 8 || hidden > 8192) return fail(MT_ERR_UNSUPPORTED, "hidden must be a multiple of 8 and <= 8192");
+  if ((ffn / tp_size) % 8) return fail(MT_ERR_UNSUPPORTED, "ffn/tp_size must be a multiple of 8");
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3)
+    return fail(MT_ERR_UNSUPPORTED, "this library is built for sm_103 (GB300); device %d is sm_%d%d", dev, major, minor);
+
+  mt_layer* L = new mt_layer{};
+  L->hidden = hidden;
+  L->heads = heads;
+  L->groups = query_groups;
+  L->head_dim = head_dim;
+  L->ffn = ffn;
+  L->norm = norm;
+  L->act = act;
+  L->tp = tp_size;
+  L->rank = tp_rank;
+  L->rope_base = rope_base;
+  L->eps = 1e-5f;
+  L->nh_r = heads / tp_size;
+  L->ng_r = query_groups / tp_size;
+  L->f_r = ffn / tp_size;
+  L->f1_r = act == MT_ACT_SWIGLU ? 2 * L->f_r : L->f_r;
+  L->q_w = L->nh_r * head_dim;
+  L->kv_w = L->ng_r * head_dim;
+  L->device = dev;
+  e = cudaMalloc(&L->d_err, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(L->d_err, 0, sizeof(int));
+  if (e == cudaSuccess && rope_base > 0.f) {
+    const int half = head_dim / 2;
+    double theta[64];
+    for (int i = 0; i < half; ++i) theta[i] = std::pow(static_cast<double>(rope_base), -2.0 * i / head_dim);
+    e = cudaMalloc(&L->d_theta, half * sizeof(double));
+    if (e == cudaSuccess) e = cudaMemcpy(L->d_theta, theta, half * sizeof(double), cudaMemcpyHostToDevice);
+  }
+  if (e != cudaSuccess) {
+    mt_layer_destroy(L);
+    return cuda_fail(e, "mt_layer_create allocation");
+  }
+  *out = L;
+  return ok();
+}
+
+int mt_layer_set_eps(mt_layer* L, float eps) {
+  if (L == nullptr) return fail(MT_ERR_INVALID_ARG, "handle is NULL");
+  if (!(eps > 0.f) || std::isinf(eps)) return fail(MT_ERR_INVALID_ARG, "eps must be positive and finite");
+  L->eps = eps;
+  return ok();
+}
+
+int mt_layer_workspace_bytes(const mt_layer* L, int seq, int batch, size_t* bytes) {
+  if (L == nullptr || bytes == nullptr) return fail(MT_ERR_INVALID_ARG, "handle or bytes is NULL");
+  if (seq <= 0 || batch <= 0) return fail(MT_ERR_INVALID_ARG, "seq and batch must be positive");
+  *bytes = layout_for(L, seq, batch).total;
+  return ok();
+}
+
+int mt_layer_set_workspace(mt_layer* L, void* dev_ptr, size_t bytes) {
+  if (L == nullptr) return fail(MT_ERR_INVALID_ARG, "handle is NULL");
+  if (dev_ptr != nullptr && (reinterpret_cast<uintptr_t>(dev_ptr) & 255u))
+    return fail(MT_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  L->ws = dev_ptr;
+  L->ws_bytes = dev_ptr ? bytes : 0;
+  return ok();
+}
+
+int mt_layer_workspace_region(const mt_layer* L, int seq, int batch, int which, size_t* offset, size_t* bytes) {
+  if (L == nullptr || offset == nullptr || bytes == nullptr) return fail(MT_ERR_INVALID_ARG, "NULL argument");
+  if (seq <= 0 || batch <= 0) return fail(MT_ERR_INVALID_ARG, "seq and batch must be positive");
+  if (which < 0 || which > kRope) return fail(MT_ERR_INVALID_ARG, "unknown region %d", which);
+  const Layout lay = layout_for(L, seq, batch);
+  *offset = lay.off[which];
+  *bytes = lay.size[which];
+  return ok();
+}
+
+int mt_layer_forward(mt_layer* L, const void* x, int seq, int batch, const mt_weights* w, void* y_partial,
+                     void* cuda_stream) {
+  Layout lay;
+  int rc = check_call(L, x, y_partial, seq, batch, &lay);
+  if (rc) return rc;
+  if ((rc = check_weights(L, w, true, true))) return rc;
+  rc = forward_device(L, lay, x, seq, batch, w, y_partial, static_cast<cudaStream_t>(cuda_stream));
+  return rc ? rc : ok();
+}
+
+int mt_layer_forward_attn(mt_layer* L, const void* x, int seq, int batch, const mt_weights* w, void* attn_out,
+                          void* cuda_stream) {
+  Layout lay;
+  int rc = check_call(L, x, attn_out, seq, batch, &lay);
+  if (rc) return rc;
+  if ((rc = check_weights(L, w, true, false))) return rc;
+  rc = run_attention_block(L, lay, x, seq, batch, w, attn_out, mt::kEpiStore, static_cast<cudaStream_t>(cuda_stream));
+  return rc ? rc : ok();
+}
+
+int mt_layer_forward_mlp(mt_layer* L, const void* h, int seq, int batch, const mt_weights* w, void* y_partial,
+                         void* cuda_stream) {
+  Layout lay;
+  int rc = check_call(L, h, y_partial, seq, batch, &lay);
+  if (rc) return rc;
+  if ((rc = check_weights(L, w, false, true))) return rc;
+  rc = run_mlp_block(L, lay, h, seq, batch, w, y_partial, mt::kEpiStore, static_cast<cudaStream_t>(cuda_stream));
+  return rc ? rc : ok();
+}
+
+int mt_layer_forward_host(mt_layer* L, const void* x_host, int seq, int batch, const mt_weights* w, void* y_host,
+                          void* cuda_stream) {
+  if (L == nullptr) return fail(MT_ERR_INVALID_ARG, "handle is NULL");
+  if (x_host == nullptr || y_host == nullptr) return fail(MT_ERR_INVALID_ARG, "host buffers must not be NULL");
+  if (seq <= 0 || batch <= 0) return fail(MT_ERR_INVALID_ARG, "seq and batch must be positive");
+  Layout lay = layout_for(L, seq, batch);
+  if (L->ws == nullptr || L->ws_bytes < lay.total)
+    return fail(MT_ERR_NO_WORKSPACE, "workspace missing or smaller than %zu bytes", lay.total);
+  int rc = check_weights(L, w, true, true);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  void* xd = region<void>(L, lay, kXStage);
+  void* yd = region<void>(L, lay, kYStage);
+  const size_t bytes = lay.size[kXStage];
+  cudaError_t e = cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy of x");
+  rc = forward_device(L, lay, xd, seq, batch, w, yd, st);
+  if (rc) return rc;
+  e = cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy of y");
+  return ok();
+}
+
+int mt_layer_status(mt_layer* L) {
+  if (L == nullptr) return fail(MT_ERR_INVALID_ARG, "handle is NULL");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  int code = 0;
+  e = cudaMemcpy(&code, L->d_err, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  if (code != 0) {
+    cudaMemset(L->d_err, 0, sizeof(int));
+    return fail(MT_ERR_DEVICE_TIMEOUT, "a kernel stopped waiting on a barrier (device code %d); outputs are invalid",
+                code);
+  }
+  return ok();
+}
+
+const char* mt_last_error(void) { return g_last_error.c_str(); }
+
+void mt_layer_destroy(mt_layer* L) {
+  if (L == nullptr) return;
+  if (L->d_err) cudaFree(L->d_err);
+  if (L->d_theta) cudaFree(L->d_theta);
+  for (auto& r : L->recs) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  for (auto e : L->pool) cudaEventDestroy(e);
+  delete L;
+}
+
+int mt_layer_profile_enable(mt_layer* L, int enable) {
+  if (L == nullptr) return fail(MT_ERR_INVALID_ARG, "handle is NULL");
+  L->profiling = enable != 0;
+  return ok();
+}
+
+int mt_layer_profile_read(mt_layer* L, int* launches, double* total_ms) {
+  if (L == nullptr || launches == nullptr || total_ms == nullptr) return fail(MT_ERR_INVALID_ARG, "NULL argument");
+  for (int i = 0; i < MT_PROFILE_SLOTS; ++i) {
+    launches[i] = 0;
+    total_ms[i] = 0.0;
+  }
+  int rc = MT_OK;
+  for (auto& r : L->recs) {
+    float ms = 0.f;
+    cudaError_t e = cudaEventSynchronize(r.b);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.a, r.b);
+    if (e != cudaSuccess && rc == MT_OK) rc = cuda_fail(e, "reading profile events");
+    launches[r.slot] += 1;
+    total_ms[r.slot] += ms;
+    L->pool.push_back(r.a);
+    L->pool.push_back(r.b);
+  }
+  L->recs.clear();
+  return rc ? rc : ok();
+}
+
+int mt_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, void* cuda_stream) {
+  if (A == nullptr || B == nullptr || C == nullptr) return fail(MT_ERR_INVALID_ARG, "NULL operand");
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return fail(MT_ERR_INVALID_ARG, "operands must be 16-byte aligned");
+  if (M <= 0 || N <= 0 || K <= 0) return fail(MT_ERR_INVALID_ARG, "M, N, K must be positive");
+  if (K % 8 || N % 8) return fail(MT_ERR_UNSUPPORTED, "K and N must be multiples of 8");
+  mt::GemmParams p = gemm_params(M, N, K, false, nullptr);
+  p.out = static_cast<bf16*>(C);
+  p.ldo = N;
+  int rc = run_gemm(nullptr, 0, mt::kEpiStore, A, K, B, N, M, N, K, p, static_cast<cudaStream_t>(cuda_stream));
+  return rc ? rc : ok();
+}
+
+int mt_selftest_bounded_wait(int limit_us) {
+  if (limit_us < 1 || limit_us > 1000000) return fail(MT_ERR_INVALID_ARG, "limit_us must be in [1, 1e6]");
+  int* d = nullptr;
+  cudaError_t e = cudaMalloc(&d, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+  cudaMemset(d, 0, sizeof(int));
+  e = mt::launch_wait_selftest(d, static_cast<unsigned long long>(limit_us) * 1000ull, nullptr);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  int code = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&code, d, sizeof(int), cudaMemcpyDeviceToHost);
+  cudaFree(d);
+  if (e != cudaSuccess) return cuda_fail(e, "bounded-wait self test");
+  if (code == MT_ERR_DEVICE_TIMEOUT) return fail(MT_ERR_DEVICE_TIMEOUT, "bounded wait gave up after %d us", limit_us);
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,309 @@
+// Causal GQA flash attention on the 5th-generation tensor cores.
+//
+// o_h = softmax(q_h k_g^T / sqrt(d) + causal mask) v_g,  g = h / (nh/ng)
+// (core_attention with AttnMaskType.causal in the layer spec of "快速入门" §3.1; GQA through
+// num_query_groups of "ai阅读megatron" TransformerConfig; FlashAttention is the prior art the
+// pages name: exact attention computed block by block with an online softmax, O(S) memory.)
+//
+// One CTA per (128-query block, head, batch row); CTAs are issued longest-first (the last query
+// blocks see the most keys).  Per CTA:
+//   warp 0      TMA: the Q tile once, then K [128 keys x d] and V^T [d x 128 keys] tiles into a
+//               2-stage ring.  V is stored transposed by the QKV GEMM so both MMAs read K-major
+//               operands.
+//   warp 1      one thread issues S_j = Q K_j^T into one of two TMEM score buffers (128 columns
+//               each), and O += P_j V_j into a TMEM output accumulator (d columns).
+//   warps 2..5  softmax, one query row per thread: reads S_j from TMEM, masks the diagonal
+//               block, keeps a running maximum and sum in the log2 domain, writes P_j = 2^(s - m)
+//               as bf16 into shared memory in the 128-byte-swizzled layout the MMA reads, and
+//               rescales O in TMEM only when the running maximum grows by more than 2^8
+//               (between rescales P stays below 256, exact in fp32 sums and in bf16 range).
+//               At the end O / l is written as bf16 to o[t, h*d + i].
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace mt {
+namespace {
+
+constexpr int BQ = 128, BKV = 128;
+
+template <int D>
+struct Geo {
+  static constexpr int ATOM = 128 * 128;          // one [128 rows x 64 bf16] swizzle block, 16 KB
+  static constexpr int Q_BYTES = BQ * D * 2;      // D/64 atoms
+  static constexpr int K_BYTES = BKV * D * 2;     // D/64 atoms
+  static constexpr int V_ATOM = D * 128;          // [D rows x 64 keys]
+  static constexpr int V_BYTES = 2 * V_ATOM;      // two key halves
+  static constexpr int P_BYTES = BQ * BKV * 2;    // two key halves of 16 KB
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int OFF_V = OFF_K + 2 * K_BYTES;
+  static constexpr int OFF_P = OFF_V + 2 * V_BYTES;
+  static constexpr int OFF_BAR = OFF_P + P_BYTES;
+  // Every CTA allocates all 512 TMEM columns, so at most one CTA may live on an SM: ask for more
+  // than half of the SM's shared memory even when the tiles need less.
+  static constexpr size_t SMEM_USED = 1024 + OFF_BAR + 256;
+  static constexpr size_t SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
+  static constexpr uint32_t IDESC_S = idesc_bf16(BQ, BKV);
+  static constexpr uint32_t IDESC_O = idesc_bf16(BQ, D);
+};
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+  using G = Geo<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = base + G::OFF_Q;
+  uint8_t* sP = base + G::OFF_P;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + G::OFF_BAR);
+  // bars: q_full | kv_full[2] | kv_empty[2] | s_full[2] | s_free[2] | p_full | o_done | drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  const uint32_t q_full = bar0;
+  auto kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto kv_empty = [&](int s) { return bar0 + 8u * (3 + s); };
+  auto s_full = [&](int s) { return bar0 + 8u * (5 + s); };
+  auto s_free = [&](int s) { return bar0 + 8u * (7 + s); };
+  const uint32_t p_full = bar0 + 8u * 9, o_done = bar0 + 8u * 10, drain = bar0 + 8u * 11;
+  const uint32_t sQa = smem_u32(sQ), sPa = smem_u32(sP);
+  auto sKa = [&](int st) { return smem_u32(base + G::OFF_K + st * G::K_BYTES); };
+  auto sVa = [&](int st) { return smem_u32(base + G::OFF_V + st * G::V_BYTES); };
+
+  const int bh_count = p.batch * p.nh;
+  const int qb = p.num_qb - 1 - static_cast<int>(blockIdx.x) / bh_count;  // longest first
+  const int bh = static_cast<int>(blockIdx.x) % bh_count;
+  const int b = bh / p.nh, h = bh - b * p.nh;
+  const int g = h / (p.nh / p.ng);
+  const int nkv = qb + 1;  // causal: key blocks 0..qb
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(kv_full(s), 1);
+      mbar_init(kv_empty(s), 1);
+      mbar_init(s_full(s), 1);
+      mbar_init(s_free(s), 4);
+    }
+    mbar_init(p_full, 4);
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(&tmQ);
+    tma_prefetch(&tmK);
+    tma_prefetch(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t tO = tmem_base + 2 * BKV;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, G::Q_BYTES);
+#pragma unroll
+      for (int a = 0; a < D / 64; ++a) tma_load_3d(sQa + a * G::ATOM, &tmQ, q_full, a * 64, qb * BQ, b * p.nh + h);
+      int issued = 0;
+      bool ok = true;
+      for (int j = 0; j < nkv; ++j) {
+        const int st = j & 1;
+        if (!mbar_wait(kv_empty(st), ((j >> 1) & 1) ^ 1u, p.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(kv_full(st), G::K_BYTES + G::V_BYTES);
+#pragma unroll
+        for (int a = 0; a < D / 64; ++a)
+          tma_load_3d(sKa(st) + a * G::ATOM, &tmK, kv_full(st), a * 64, j * BKV, b * p.ng + g);
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+          tma_load_3d(sVa(st) + a * G::V_ATOM, &tmV, kv_full(st), j * BKV + a * 64, 0, b * p.ng + g);
+        ++issued;
+      }
+      if (!ok) {  // let this CTA's own copies in flight land
+        mbar_wait_slow(q_full, 0, nullptr, nullptr, kDrainLimitNs);
+        for (int j = issued - 1; j >= 0 && j >= issued - 2; --j)
+          mbar_wait_slow(kv_full(j & 1), (j >> 1) & 1, nullptr, nullptr, kDrainLimitNs);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      bool ok = mbar_wait(q_full, 0, p.err, abort_flag);
+      auto issue_s = [&](int j) -> bool {
+        const int st = j & 1;
+        if (!mbar_wait(kv_full(st), (j >> 1) & 1, p.err, abort_flag)) return false;
+        if (!mbar_wait(s_free(st), ((j >> 1) & 1) ^ 1u, p.err, abort_flag)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * G::ATOM + (k & 3) * 32;
+          mma_bf16_ss(tmem_base + st * BKV, sw128_desc(sQa + off), sw128_desc(sKa(st) + off), G::IDESC_S,
+                      k > 0 ? 1u : 0u);
+        }
+        mma_commit(s_full(st));
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; ok && j < nkv; ++j) {
+        if (j + 1 < nkv && !issue_s(j + 1)) {
+          ok = false;
+          break;
+        }
+        if (!mbar_wait(p_full, j & 1, p.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int st = j & 1;
+#pragma unroll
+        for (int k = 0; k < BKV / 16; ++k) {
+          const uint32_t pa = sPa + (k >> 2) * G::ATOM + (k & 3) * 32;
+          const uint32_t va = sVa(st) + (k >> 2) * G::V_ATOM + (k & 3) * 32;
+          mma_bf16_ss(tO, sw128_desc(pa), sw128_desc(va), G::IDESC_O, (j > 0 || k > 0) ? 1u : 0u);
+        }
+        mma_commit(kv_empty(st));
+        mma_commit(o_done);
+      }
+      mma_commit(drain);
+      mbar_wait_slow(drain, 0, nullptr, nullptr, ok ? kWaitLimitNs : kDrainLimitNs);
+    }
+  } else {
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;  // query row within the block
+    const int sq = qb * BQ + r;      // its sequence position
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const float c = p.scale_log2;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    uint8_t* prow = sP + r * 128;
+    const int sw = r & 7;
+    for (int j = 0; j < nkv; ++j) {
+      const int sb = j & 1;
+      bool w = mbar_wait(s_full(sb), (j >> 1) & 1, p.err, abort_flag);
+      if (!__all_sync(0xffffffffu, w)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[BKV];
+#pragma unroll
+      for (int cc = 0; cc < BKV / 32; ++cc) tmem_ld32(tmem_base + lane_off + sb * BKV + cc * 32, s + cc * 32);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free(sb));
+      if (j == qb) {  // diagonal block: key j*128+i visible iff i <= r
+#pragma unroll
+        for (int i = 0; i < BKV; ++i)
+          if (i > r) s[i] = -INFINITY;
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < BKV; ++i) mx = fmaxf(mx, s[i]);
+      const float m_new = fmaxf(m_used, mx * c);
+      if (j > 0) {  // P_{j-1} V_{j-1} finished: P may be overwritten and O is stable
+        w = mbar_wait(o_done, (j - 1) & 1, p.err, abort_flag);
+        if (!__all_sync(0xffffffffu, w)) {
+          ok = false;
+          break;
+        }
+      }
+      if (__any_sync(0xffffffffu, m_new > m_used + 8.0f)) {
+        const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m_used - m_new);
+        l *= alpha;
+        if (j > 0) {
+          tc_fence_after();
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
+            float o[32];
+            tmem_ld32(tO + lane_off + cc * 32, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(tO + lane_off + cc * 32, o);
+          }
+        }
+        m_used = m_new;
+      }
+      float rs = 0.f;
+#pragma unroll
+      for (int i = 0; i < BKV; ++i) {
+        s[i] = ex2_approx(fmaf(s[i], c, -m_used));
+        rs += s[i];
+      }
+      l += rs;
+#pragma unroll
+      for (int ch = 0; ch < 16; ++ch) {
+        const int atom = ch >> 3, cw = ch & 7;
+        *reinterpret_cast<uint4*>(prow + atom * G::ATOM + ((cw ^ sw) << 4)) = pack_bf16x8(s + ch * 8);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+    }
+    if (ok) {
+      const bool w = mbar_wait(o_done, (nkv - 1) & 1, p.err, abort_flag);
+      if (__all_sync(0xffffffffu, w)) {
+        tc_fence_after();
+        const float inv_l = 1.f / l;
+        bf16* orow = p.o + (static_cast<size_t>(sq) * p.batch + b) * p.ldo + h * D;
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          float o[32];
+          tmem_ld32(tO + lane_off + cc * 32, o);
+          if (sq < p.seq) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= inv_l;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              *reinterpret_cast<uint4*>(orow + cc * 32 + q4 * 8) = pack_bf16x8(o + q4 * 8);
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnParams& p,
+                     cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(Geo<D>::SMEM));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const unsigned grid = static_cast<unsigned>(p.num_qb) * p.batch * p.nh;
+  attn_kernel<D><<<grid, 192, Geo<D>::SMEM, stream>>>(tmQ, tmK, tmV, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attention(int head_dim, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                             const AttnParams& p, cudaStream_t stream) {
+  if (p.num_qb <= 0) return cudaSuccess;
+  if (head_dim == 64) return launch_d<64>(tmQ, tmK, tmV, p, stream);
+  if (head_dim == 128) return launch_d<128>(tmQ, tmK, tmV, p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace mt

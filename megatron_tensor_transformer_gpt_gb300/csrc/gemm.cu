@@ -1,0 +1,341 @@
+// Dense bf16 GEMM on the 5th-generation tensor cores with fused epilogues:
+//   out[M, N] = epilogue( A[M, K] * B[N, K]^T )
+// A is a row-major activation (tokens x features) and B a weight stored [out, in], so both
+// operands are K-major ("Megatron-LM 深度学习与源码分析文档", Part 2 §2: Y = XW, with the
+// column-parallel QKV / fc1 and the row-parallel output projection / fc2 all of this form).
+//
+// Design (one CTA per SM, persistent over output tiles):
+//   warp 0      TMA producer: A tile [128 x 64] and B tile [256 x 64] per stage, 128-byte swizzle,
+//               a 4-stage shared-memory ring guarded by full/empty mbarriers.
+//   warp 1      one thread issues tcgen05.mma (M=128, N=256, K=16) into one of two TMEM
+//               accumulators (2 x 256 fp32 columns) and commits stages / finished tiles.
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (one TMEM lane = one output row per
+//               thread), fused bias / residual / RoPE / SwiGLU / GeLU, bf16 stores; the second
+//               accumulator lets the next tile's main loop run meanwhile.
+// Tiles are ordered with M fastest so the CTAs in flight share B tiles and the whole A in L2.
+#include "common.cuh"
+#include "internal.h"
+
+namespace mt {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KB (two 128-row boxes)
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr uint32_t IDESC = idesc_bf16(BM, BN);
+constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+
+// ------------------------------------------------------------------ epilogue helpers
+__device__ __forceinline__ void add_vec32(float* v, const bf16* src, int col, int limit) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    if (col + 8 * g < limit) {
+      float f[8];
+      unpack_bf16x8(*reinterpret_cast<const uint4*>(src + col + 8 * g), f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[8 * g + e] += f[e];
+    }
+  }
+}
+
+__device__ __forceinline__ void store_vec32(bf16* dst_row, int col, int limit, const float* v) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+    if (col + 8 * g < limit) *reinterpret_cast<uint4*>(dst_row + col + 8 * g) = pack_bf16x8(v + 8 * g);
+}
+
+__device__ __forceinline__ float gelu_tanh(float u) {
+  // 0.5 u (1 + tanh( sqrt(2/pi) (u + 0.044715 u^3) ))
+  const float k0 = 0.7978845608028654f, k1 = 0.044715f;
+  return 0.5f * u * (1.0f + tanhf(k0 * (u + k1 * u * u * u)));
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
+template <int MODE>
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc, int m0, int tn, int r_in_tile) {
+  const int row = m0 + r_in_tile;
+  const bool valid = row < p.M;
+  if constexpr (MODE == kEpiStore || MODE == kEpiResid || MODE == kEpiGelu) {
+    const int n0 = tn * BN;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      const int col = n0 + c;
+      if (col >= p.N) break;  // uniform across the warp
+      float v[32];
+      tmem_ld32(tacc + c, v);
+      if (valid) {
+        if (p.bias != nullptr) add_vec32(v, p.bias, col, p.N);
+        if constexpr (MODE == kEpiResid) add_vec32(v, p.resid + static_cast<size_t>(row) * p.ldr, col, p.N);
+        if constexpr (MODE == kEpiGelu) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = gelu_tanh(v[e]);
+        }
+        store_vec32(p.out + static_cast<size_t>(row) * p.ldo, col, p.N, v);
+      }
+    }
+  } else if constexpr (MODE == kEpiSwiglu) {
+    const int n0 = tn * 128;
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 32) {
+      const int col = n0 + c;
+      if (col >= p.N) break;
+      float g[32], u[32];
+      tmem_ld32(tacc + c, g);
+      tmem_ld32(tacc + 128 + c, u);
+      if (valid) {
+        if (p.bias != nullptr) {
+          add_vec32(g, p.bias, col, p.N);
+          add_vec32(u, p.bias + p.N, col, p.N);
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) g[e] = silu(g[e]) * u[e];
+        store_vec32(p.out + static_cast<size_t>(row) * p.ldo, col, p.N, g);
+      }
+    }
+  } else {  // kEpiQkv
+    const int d = p.head_dim, half = d >> 1;
+    const int n0 = tn * BN;
+    const int s = valid ? row / p.batch : 0;
+    const int b = valid ? row - s * p.batch : 0;
+#pragma unroll 1
+    for (int hc = 0; hc < BN; hc += d) {
+      const int col = n0 + hc;
+      if (col >= p.N) break;
+      bf16* dst;
+      bool is_v = false;
+      if (col < p.q_w) {
+        const int hh = col / d;
+        dst = p.q + ((static_cast<size_t>(b) * p.nh + hh) * p.seq + s) * d;
+      } else if (col < p.q_w + p.kv_w) {
+        const int gg = (col - p.q_w) / d;
+        dst = p.k + ((static_cast<size_t>(b) * p.ng + gg) * p.seq + s) * d;
+      } else {
+        const int gg = (col - p.q_w - p.kv_w) / d;
+        dst = p.vt + (static_cast<size_t>(b) * p.ng + gg) * d * p.seq_pad + s;
+        is_v = true;
+      }
+      if (!is_v && p.rope != nullptr) {
+        // rotate-half: (x_i, x_{i+d/2}) -> (x_i c - x_{i+d/2} s, x_{i+d/2} c + x_i s)
+#pragma unroll 1
+        for (int i0 = 0; i0 < half; i0 += 32) {
+          float x1[32], x2[32];
+          tmem_ld32(tacc + hc + i0, x1);
+          tmem_ld32(tacc + hc + half + i0, x2);
+          if (valid) {
+            if (p.bias != nullptr) {
+              add_vec32(x1, p.bias, col + i0, p.N);
+              add_vec32(x2, p.bias, col + half + i0, p.N);
+            }
+            const float4* cs = reinterpret_cast<const float4*>(p.rope + static_cast<size_t>(s) * half + i0);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float4 t = cs[e];  // (cos, sin) of elements 2e and 2e+1
+              const float a0 = x1[2 * e], b0 = x2[2 * e], a1 = x1[2 * e + 1], b1 = x2[2 * e + 1];
+              x1[2 * e] = a0 * t.x - b0 * t.y;
+              x2[2 * e] = b0 * t.x + a0 * t.y;
+              x1[2 * e + 1] = a1 * t.z - b1 * t.w;
+              x2[2 * e + 1] = b1 * t.z + a1 * t.w;
+            }
+            store_vec32(dst, i0, d, x1);
+            store_vec32(dst, half + i0, d, x2);
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int i0 = 0; i0 < d; i0 += 32) {
+          float x[32];
+          tmem_ld32(tacc + hc + i0, x);
+          if (valid) {
+            if (p.bias != nullptr) add_vec32(x, p.bias, col + i0, p.N);
+            if (is_v) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) dst[static_cast<size_t>(i0 + e) * p.seq_pad] = __float2bfloat16_rn(x[e]);
+            } else {
+              store_vec32(dst, i0, d, x);
+            }
+          }
+        }
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+template <int MODE>
+__global__ void __launch_bounds__(192, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = base;
+  uint8_t* sB = base + STAGES * A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + STAGES * STAGE_BYTES);
+  // bars: full[STAGES] | empty[STAGES] | tmem_full[2] | tmem_empty[2] | drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+  auto tempty = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+  const uint32_t drain = bar0 + 8u * (2 * STAGES + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull(a), 1);
+      mbar_init(tempty(a), 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(&tmA);
+    tma_prefetch(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int num_kb = (p.K + BK - 1) / BK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        const int tm = tile % p.tiles_m, tn = tile / p.tiles_m;
+        const int m0 = tm * BM;
+        const int r0 = (MODE == kEpiSwiglu) ? tn * 128 : tn * BN;
+        const int r1 = r0 + p.b_row_step;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(empty(stage), phase ^ 1u, p.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full(stage);
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          const uint32_t a_dst = smem_u32(sA + stage * A_BYTES);
+          const uint32_t b_dst = smem_u32(sB + stage * B_BYTES);
+          tma_load_2d(a_dst, &tmA, fb, kb * BK, m0);
+          tma_load_2d(b_dst, &tmB, fb, kb * BK, r0);
+          tma_load_2d(b_dst + B_BYTES / 2, &tmB, fb, kb * BK, r1);
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {  // let this CTA's own copies in flight land before its shared memory goes away
+        for (int s = 0; s < STAGES; ++s)
+          if (s < stage || issued >= STAGES)
+            mbar_wait_slow(full(s), s < stage ? phase : (phase ^ 1u), nullptr, nullptr, kDrainLimitNs);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0, it = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t use = (it >> 1) & 1;
+        if (!mbar_wait(tempty(acc), use ^ 1u, p.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(full(stage), phase, p.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sw128_desc(smem_u32(sA + stage * A_BYTES));
+          const uint64_t bd = sw128_desc(smem_u32(sB + stage * B_BYTES));
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            mma_bf16_ss(d_tmem, ad + 2ull * k, bd + 2ull * k, IDESC, (kb | k) != 0 ? 1u : 0u);
+          mma_commit(empty(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) mma_commit(tfull(acc));
+      }
+      // No MMA may still read shared memory or write TMEM when the CTA releases them.
+      mma_commit(drain);
+      mbar_wait_slow(drain, 0, nullptr, nullptr, ok ? kWaitLimitNs : kDrainLimitNs);
+    }
+  } else {
+    const int quad = warp & 3;  // TMEM lanes this warp may read
+    int it = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
+      const int acc = it & 1;
+      const uint32_t use = (it >> 1) & 1;
+      const bool w = mbar_wait(tfull(acc), use, p.err, abort_flag);
+      if (!__all_sync(0xffffffffu, w)) break;
+      tc_fence_after();
+      const int tm = tile % p.tiles_m, tn = tile / p.tiles_m;
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
+      epilogue_tile<MODE>(p, tacc, tm * BM, tn, quad * 32 + lane);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty(acc));
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+template <int MODE>
+cudaError_t launch_mode(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(SMEM_BYTES));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
+  gemm_kernel<MODE><<<grid, 192, SMEM_BYTES, stream>>>(tmA, tmB, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t gemm_smem_bytes() { return SMEM_BYTES; }
+
+cudaError_t launch_gemm(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,
+                        cudaStream_t stream) {
+  if (p.num_tiles <= 0) return cudaSuccess;
+  switch (mode) {
+    case kEpiStore: return launch_mode<kEpiStore>(tmA, tmB, p, stream);
+    case kEpiResid: return launch_mode<kEpiResid>(tmA, tmB, p, stream);
+    case kEpiQkv: return launch_mode<kEpiQkv>(tmA, tmB, p, stream);
+    case kEpiSwiglu: return launch_mode<kEpiSwiglu>(tmA, tmB, p, stream);
+    case kEpiGelu: return launch_mode<kEpiGelu>(tmA, tmB, p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace mt

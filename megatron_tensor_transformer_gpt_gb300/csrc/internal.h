@@ -1,0 +1,66 @@
+// Host-side declarations shared by the translation units of the layer library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mt {
+
+using bf16 = __nv_bfloat16;
+
+// Epilogue of the tcgen05 GEMM (what happens to each fp32 accumulator row before it is stored).
+enum GemmEpilogue : int {
+  kEpiStore = 0,   // out = acc (+ bias)
+  kEpiResid = 1,   // out = acc (+ bias) + resid            (row-parallel output + bias-dropout-add)
+  kEpiQkv = 2,     // bias, RoPE on q/k heads, scatter q/k to [b, head, s, d] and v to [b, group, d, s]
+  kEpiSwiglu = 3,  // out = silu(gate + b_gate) * (up + b_up); the tile holds 128 gate and 128 up columns
+  kEpiGelu = 4,    // out = gelu_tanh(acc + bias)
+};
+
+struct GemmParams {
+  int M, N, K;        // output rows, output columns (SwiGLU: gate width), reduction length
+  int tiles_m, tiles_n, num_tiles;
+  int b_row_step;     // row offset of the second 128-row B box: 128, or the gate width for SwiGLU
+  bf16* out;
+  int ldo;
+  const bf16* bias;   // [N] (SwiGLU: [2N]) or null
+  const bf16* resid;  // [M, ldr] or null
+  int ldr;
+  // kEpiQkv only
+  bf16 *q, *k, *vt;
+  const float2* rope;  // [seq, d/2] (cos, sin) or null
+  int seq, batch, head_dim, q_w, kv_w, nh, ng, seq_pad;
+  int* err;
+};
+
+struct AttnParams {
+  int seq, batch, nh, ng;  // this rank's query heads and kv groups
+  int num_qb;              // ceil(seq / 128)
+  float scale_log2;        // log2(e) / sqrt(head_dim)
+  bf16* o;                 // [seq*batch, ldo], head h at columns h*head_dim
+  int ldo;
+  int* err;
+};
+
+// Number of SMs of the current device (cached).
+int num_sms();
+
+// Kernel launchers; return a cudaError_t from the launch.
+cudaError_t launch_gemm(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,
+                        cudaStream_t stream);
+size_t gemm_smem_bytes();
+
+cudaError_t launch_attention(int head_dim, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                             const AttnParams& p, cudaStream_t stream);
+
+cudaError_t launch_norm(bool layer_norm, const bf16* x, const bf16* g, const bf16* b, bf16* y, int rows, int hidden,
+                        float eps, cudaStream_t stream);
+
+cudaError_t launch_rope_table(float2* table, const double* theta, int seq, int half, cudaStream_t stream);
+
+cudaError_t launch_wait_selftest(int* err, unsigned long long limit_ns, cudaStream_t stream);
+
+}  // namespace mt
