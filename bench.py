@@ -183,8 +183,9 @@ def run_native(args):
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     smi_index = int(vis.split(",")[local]) if vis and vis.split(",")[local].strip().isdigit() else local
     clocks = ClockSampler(smi_index)
-    clocks.start()
-    t_end = time.perf_counter() + 0.5
+    if not args.quick:
+        clocks.start()
+    t_end = time.perf_counter() + (0.0 if args.quick else 0.5)
     while time.perf_counter() < t_end:
         layer.forward(x, cfg.seq, cfg.batch, w, y)
         torch.cuda.synchronize()
@@ -208,12 +209,13 @@ def run_native(args):
     # end to end through the host-buffer entry point
     xh = x.cpu().pin_memory()
     yh = torch.empty(cfg.tokens, cfg.hidden, dtype=torch.bfloat16).pin_memory()
-    for _ in range(2):
+    n_e2e = 0 if args.quick else args.steps
+    for _ in range(min(2, n_e2e)):
         layer.forward_host(xh, cfg.seq, cfg.batch, w, yh)
     torch.cuda.synchronize()
-    ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_e2e)]
     barrier()
-    for i in range(args.steps):
+    for i in range(n_e2e):
         flush.fill_(i & 0xFF)
         ev2[i][0].record(stream)
         layer.forward_host(xh, cfg.seq, cfg.batch, w, yh)
@@ -225,7 +227,7 @@ def run_native(args):
     e2e_ms = [a.elapsed_time(b) for a, b in ev2]
 
     total_ms = sum(step_ms)
-    total_e2e = sum(e2e_ms)
+    total_e2e = sum(e2e_ms) if e2e_ms else float("nan")
     if world > 1:
         t = torch.tensor([total_ms, total_e2e], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -248,7 +250,7 @@ def run_native(args):
         return
 
     cpu = None
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and not args.quick:
         n_rows = 256
         sf, dt = oracle_sample(cfg, inp, n_rows)
         cpu = {"value": sf / dt / 1e12, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
@@ -270,7 +272,7 @@ def run_native(args):
                      "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": None,
                      "peak_note": f"{peak_src} cuBLAS bf16 burst"},
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": cfg.tokens * cfg.hidden * 2,
+        "e2e": None if args.quick else {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": cfg.tokens * cfg.hidden * 2,
                 "d2h_bytes_per_step": cfg.tokens * cfg.hidden * 2, "ms_per_step": total_e2e / args.steps},
         "gpu_launches": kernel_launches,
         "clocks": clk,
@@ -317,6 +319,8 @@ def main():
     ap.add_argument("--impl", choices=("native", "reference"), default="native")
     ap.add_argument("--workload", default="llama8b", choices=sorted(synth.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true",
+                    help="profiling runs: no clock sampling, no host-buffer pass, no CPU baseline")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.impl == "reference":
