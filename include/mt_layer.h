@@ -159,6 +159,35 @@ int mt_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, voi
  * bounded wait fired and reported itself (the expected outcome), MT_OK if it did not fire. */
 int mt_selftest_bounded_wait(int limit_us);
 
+/* ---- allocation-free variant ------------------------------------------------------------ */
+
+/* The whole-layer forward of mt_layer_create + mt_layer_forward in one call that allocates no
+ * device memory.  The Megatron pages have no counterpart to this call: it is here for callers
+ * that cannot call cudaMalloc -- code that runs inside a host framework whose allocator owns all
+ * device memory, and real-time or embedded callers that forbid device allocation (and the device
+ * synchronisation cudaMalloc/cudaFree can imply) once they have started.
+ *
+ * Same arguments, layouts and results as mt_layer_create(...) followed by mt_layer_set_eps(eps)
+ * and mt_layer_forward(x, seq, batch, w, y_partial, cuda_stream).  The caller passes x, the
+ * weights and y_partial as usual.  The scratch (the layer workspace, the RoPE frequency table and
+ * the device error word) lives in one fixed area of MT_STATIC_AREA_BYTES (32 MiB) compiled into
+ * the library: every GPU on which the library is used holds it until the process exits.  A call
+ * whose workspace would not fit in it (mt_layer_workspace_bytes > MT_STATIC_AREA_BYTES - 1024,
+ * e.g. more than about 370 tokens of the Llama-3-8B-shaped layer) returns MT_ERR_UNSUPPORTED and does
+ * nothing.  No cudaMalloc, cudaFree or allocating library routine is called.
+ *
+ * The first call on a device looks up the area's device address (cudaGetSymbolAddress, with that
+ * device current); make that first call before any stream capture.  Every call clears the error
+ * word and uploads the RoPE frequencies (a small host-to-device copy on cuda_stream) before the
+ * kernels.  All calls share the one area, which keeps the last call's contents: calls whose work
+ * overlaps on the GPU (other streams, other host threads) race and corrupt each other's results.
+ * Device-side timeouts are recorded in the area's error word but cannot be read back through this
+ * entry point. */
+#define MT_STATIC_AREA_BYTES (32u << 20)
+int mt_layer_forward_static(int hidden, int heads, int query_groups, int head_dim, int ffn, int norm, int act,
+                            float rope_base, int tp_size, int tp_rank, float eps, const void* x, int seq, int batch,
+                            const mt_weights* w, void* y_partial, void* cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

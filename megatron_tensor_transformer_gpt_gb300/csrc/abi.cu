@@ -6,6 +6,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -621,3 +622,108 @@ int mt_selftest_bounded_wait(int limit_us) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------- allocation-free variant
+// Scratch for mt_layer_forward_static: a fixed area in the library's own device image.  Its name
+// is only a host-side stand-in in host code; the device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_static_area[MT_STATIC_AREA_BYTES];
+
+namespace {
+constexpr size_t kStaticHeader = 1024;  // error word at offset 0, RoPE frequencies at 256
+constexpr int kMaxDevices = 128;
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDevices];
+
+// Device address of the static area on `dev` (the current device), looked up once per device.
+int static_area(int dev, void** out) {
+  if (dev < 0 || dev >= kMaxDevices) return fail(MT_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (g_static_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_static_area);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the static scratch area");
+    g_static_ptr[dev] = p;
+  }
+  *out = g_static_ptr[dev];
+  return MT_OK;
+}
+}  // namespace
+
+extern "C" int mt_layer_forward_static(int hidden, int heads, int query_groups, int head_dim, int ffn, int norm,
+                                       int act, float rope_base, int tp_size, int tp_rank, float eps, const void* x,
+                                       int seq, int batch, const mt_weights* w, void* y_partial, void* cuda_stream) {
+  if (hidden <= 0 || heads <= 0 || query_groups <= 0 || head_dim <= 0 || ffn <= 0 || tp_size <= 0)
+    return fail(MT_ERR_INVALID_ARG, "sizes must be positive");
+  if (tp_rank < 0 || tp_rank >= tp_size) return fail(MT_ERR_INVALID_ARG, "tp_rank %d outside [0, %d)", tp_rank, tp_size);
+  if (norm != MT_NORM_RMS && norm != MT_NORM_LAYER) return fail(MT_ERR_INVALID_ARG, "unknown norm %d", norm);
+  if (act != MT_ACT_SWIGLU && act != MT_ACT_GELU_TANH) return fail(MT_ERR_INVALID_ARG, "unknown activation %d", act);
+  if (!(rope_base >= 0.f) || std::isinf(rope_base)) return fail(MT_ERR_INVALID_ARG, "rope_base must be finite and >= 0");
+  if (!(eps > 0.f) || std::isinf(eps)) return fail(MT_ERR_INVALID_ARG, "eps must be positive and finite");
+  if (head_dim != 64 && head_dim != 128) return fail(MT_ERR_UNSUPPORTED, "head_dim must be 64 or 128 (got %d)", head_dim);
+  if (heads % query_groups) return fail(MT_ERR_UNSUPPORTED, "heads %% query_groups != 0");
+  if (heads % tp_size || query_groups % tp_size || ffn % tp_size)
+    return fail(MT_ERR_UNSUPPORTED, "heads, query_groups and ffn must be divisible by tp_size");
+  if (hidden % 8 || hidden > 8192) return fail(MT_ERR_UNSUPPORTED, "hidden must be a multiple of 8 and <= 8192");
+  if ((ffn / tp_size) % 8) return fail(MT_ERR_UNSUPPORTED, "ffn/tp_size must be a multiple of 8");
+
+  // A handle on the stack: same fields as mt_layer_create fills, but every device buffer points
+  // into the static area.
+  mt_layer L{};
+  L.hidden = hidden;
+  L.heads = heads;
+  L.groups = query_groups;
+  L.head_dim = head_dim;
+  L.ffn = ffn;
+  L.norm = norm;
+  L.act = act;
+  L.tp = tp_size;
+  L.rank = tp_rank;
+  L.rope_base = rope_base;
+  L.eps = eps;
+  L.nh_r = heads / tp_size;
+  L.ng_r = query_groups / tp_size;
+  L.f_r = ffn / tp_size;
+  L.f1_r = act == MT_ACT_SWIGLU ? 2 * L.f_r : L.f_r;
+  L.q_w = L.nh_r * head_dim;
+  L.kv_w = L.ng_r * head_dim;
+  L.profiling = false;
+  if (seq <= 0 || batch <= 0) return fail(MT_ERR_INVALID_ARG, "seq and batch must be positive (got %d, %d)", seq, batch);
+  const size_t need = layout_for(&L, seq, batch).total;
+  const size_t have = static_cast<size_t>(MT_STATIC_AREA_BYTES) - kStaticHeader;
+  if (need > have)
+    return fail(MT_ERR_UNSUPPORTED, "this call needs %zu bytes of scratch; the static area holds %zu (seq*batch too large)",
+                need, have);
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3)
+    return fail(MT_ERR_UNSUPPORTED, "this library is built for sm_103 (GB300); device %d is sm_%d%d", dev, major, minor);
+  void* base = nullptr;
+  int rc = static_area(dev, &base);
+  if (rc) return rc;
+  L.device = dev;
+  L.d_err = static_cast<int*>(base);
+  L.d_theta = rope_base > 0.f ? reinterpret_cast<double*>(static_cast<char*>(base) + 256) : nullptr;
+  L.ws = static_cast<char*>(base) + kStaticHeader;
+  L.ws_bytes = have;
+
+  Layout lay;
+  if ((rc = check_call(&L, x, y_partial, seq, batch, &lay))) return rc;
+  if ((rc = check_weights(&L, w, true, true))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  e = cudaMemsetAsync(L.d_err, 0, sizeof(int), st);  // the error word must start at zero
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the static error word");
+  if (L.d_theta != nullptr) {
+    double theta[64];
+    for (int i = 0; i < head_dim / 2; ++i) theta[i] = std::pow(static_cast<double>(rope_base), -2.0 * i / head_dim);
+    e = cudaMemcpyAsync(L.d_theta, theta, (head_dim / 2) * sizeof(double), cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(e, "copying the RoPE frequencies");
+  }
+  rc = forward_device(&L, lay, x, seq, batch, w, y_partial, st);
+  return rc ? rc : ok();
+}
+

@@ -64,6 +64,10 @@ _SIGS = {
     "mt_layer_profile_enable": ([ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
     "mt_layer_profile_read": ([ctypes.c_void_p, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_double)],
                               ctypes.c_int),
+    "mt_layer_forward_static": ([ctypes.c_int] * 7 + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                                                      ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                                      ctypes.POINTER(MtWeights), ctypes.c_void_p, ctypes.c_void_p],
+                                ctypes.c_int),
 }
 
 PROFILE_SLOTS = ("rope_table", "norm1", "gemm_qkv", "attention", "gemm_o", "norm2", "gemm_fc1", "gemm_fc2")
@@ -155,6 +159,14 @@ def mt_layer_profile_read(handle):
     launches, ms = (ctypes.c_int * n)(), (ctypes.c_double * n)()
     _check(lib().mt_layer_profile_read(handle, launches, ms))
     return {PROFILE_SLOTS[i]: (launches[i], ms[i]) for i in range(n)}
+
+
+def mt_layer_forward_static(hidden, heads, query_groups, head_dim, ffn, norm, act, rope_base, tp_size, tp_rank, eps,
+                            x, seq, batch, weights: MtWeights, y_partial, stream):
+    """Whole layer without any device allocation (scratch in the library's fixed static area)."""
+    _check(lib().mt_layer_forward_static(hidden, heads, query_groups, head_dim, ffn, norm, act, float(rope_base),
+                                         tp_size, tp_rank, float(eps), x, seq, batch, ctypes.byref(weights),
+                                         y_partial, stream))
 
 
 def mt_gemm_bf16(A, B, C, M, N, K, stream):
