@@ -52,6 +52,42 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def profiled_traffic(summary: str):
+    """DRAM bytes per launch recorded in an ncu summary under profiles/, or None when the kernel
+    sources it names have changed since the counters were taken."""
+    import hashlib
+    import re
+    path = os.path.join(ROOT, "profiles", summary)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+    shas = re.search(r"source_sha256_16:(.*)", text)
+    if not m or not shas:
+        return None
+    csrc = os.path.join(ROOT, "megatron_tensor_transformer_gpt_gb300", "csrc")
+    for name, digest in re.findall(r"([\w.]+)\s+([0-9a-f]{16})", shas.group(1)):
+        f = os.path.join(csrc, name)
+        if not os.path.exists(f) or hashlib.sha256(open(f, "rb").read()).hexdigest()[:16] != digest:
+            return None
+    return int(m.group(1))
+
+
+def max_over_ranks(values, dist=None, device=None):
+    """Element-wise maximum of `values` over all ranks (the slowest rank's times), any backend."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return list(values)
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(world: int, flops_per_step: float, steps: int, total_ms: float) -> float:
+    """Whole-job TFLOP/s: the work of every rank divided by the slowest rank's time."""
+    return world * flops_per_step * steps / (total_ms * 1e-3) / 1e12
+
+
 def sample_flops(cfg, rows) -> float:
     """Algorithmic FLOPs of the oracle's row-sampled pass: K and V of every token, then the whole
     layer for `rows` (causal attention over positions 0..s of each sampled row)."""
@@ -228,12 +264,9 @@ def run_native(args):
 
     total_ms = sum(step_ms)
     total_e2e = sum(e2e_ms) if e2e_ms else float("nan")
-    if world > 1:
-        t = torch.tensor([total_ms, total_e2e], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, total_e2e = t.tolist()
-    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
-    e2e_value = world * flops * args.steps / (total_e2e * 1e-3) / 1e12
+    total_ms, total_e2e = max_over_ranks([total_ms, total_e2e], dist if world > 1 else None, dev)
+    value = job_throughput(world, flops, args.steps, total_ms)
+    e2e_value = job_throughput(world, flops, args.steps, total_e2e)
 
     peaks, peak_src = load_peaks()
     peak_tf = peaks["bf16_tflops"]
@@ -269,7 +302,10 @@ def run_native(args):
         "tokens_per_s": world * cfg.tokens * args.steps / (total_ms * 1e-3),
         "per_kernel_ms": {k: (ms / n if n else 0.0) for k, (n, ms) in prof.items()},
         "roofline": {"kernel": "gemm_fc1 (fc1 GEMM + SwiGLU epilogue)", "bound": "tensor", "achieved": achieved,
-                     "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": None,
+                     "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved / peak_tf,
+                     "traffic": profiled_traffic("gemm_fc1_swiglu_llama8b.md") if cfg.name == "llama8b" else None,
+                     "algorithmic_bytes": 2.0 * cfg.tokens * cfg.hidden + 2.0 * f1 * cfg.hidden
+                                          + 2.0 * cfg.tokens * (f1 // 2 if cfg.act == "swiglu" else f1),
                      "peak_note": f"{peak_src} cuBLAS bf16 burst"},
         "cpu_baseline": cpu,
         "e2e": None if args.quick else {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": cfg.tokens * cfg.hidden * 2,
