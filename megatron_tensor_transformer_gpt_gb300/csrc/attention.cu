@@ -281,6 +281,311 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
+// ------------------------------------------------------------------ two heads of one group per CTA
+// The variant used when each kv group serves an even number of query heads (GQA/MQA): the CTA
+// holds the Q tiles of two heads of the same group for one 128-row query block, so every K/V tile
+// it loads feeds both (half the K/V traffic of one head per CTA).  Two softmax warpgroups (one per
+// head) alternate with the tensor core: while one computes P, the MMAs of the other run.
+//   TMEM (512 columns): head t uses columns [256t, 256t+128) for S_j, overwritten in place by
+//   P_j (bf16 pairs, 64 columns) which the P V MMA reads from TMEM, and [256t+128, +d) for O.
+//   K and V have separate 2-stage rings: K_j is released once both S MMAs of block j are done,
+//   V_j once both P V MMAs are.
+//   10 warps put three warps on some SM sub-partitions, whose 16K-register files then allow 168
+//   registers per thread: P is converted and stored in two halves to stay within that.
+template <int D>
+struct Geo2 {
+  static constexpr int ATOM = 128 * 128;
+  static constexpr int Q_BYTES = BQ * D * 2;  // per head
+  static constexpr int K_BYTES = BKV * D * 2;
+  static constexpr int V_ATOM = D * 128;
+  static constexpr int V_BYTES = 2 * V_ATOM;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = 2 * Q_BYTES;
+  static constexpr int OFF_V = OFF_K + 2 * K_BYTES;
+  static constexpr int OFF_BAR = OFF_V + 2 * V_BYTES;
+  static constexpr size_t SMEM_USED = 1024 + OFF_BAR + 256;
+  static constexpr size_t SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;  // one CTA per SM (TMEM)
+  static constexpr uint32_t IDESC_S = idesc_bf16(BQ, BKV);
+  static constexpr uint32_t IDESC_O = idesc_bf16(BQ, D);
+};
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    attn2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                 const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+  using G = Geo2<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + G::OFF_BAR);
+  // bars: q_full | k_full[2] | k_empty[2] | v_full[2] | v_empty[2] | s_full[2] | p_full[2] | o_done[2] | drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  const uint32_t q_full = bar0;
+  auto k_full = [&](int i) { return bar0 + 8u * (1 + i); };
+  auto k_empty = [&](int i) { return bar0 + 8u * (3 + i); };
+  auto v_full = [&](int i) { return bar0 + 8u * (5 + i); };
+  auto v_empty = [&](int i) { return bar0 + 8u * (7 + i); };
+  auto s_full = [&](int t) { return bar0 + 8u * (9 + t); };
+  auto p_full = [&](int t) { return bar0 + 8u * (11 + t); };
+  auto o_done = [&](int t) { return bar0 + 8u * (13 + t); };
+  const uint32_t drain = bar0 + 8u * 15;
+  auto sQa = [&](int t) { return smem_u32(base + G::OFF_Q + t * G::Q_BYTES); };
+  auto sKa = [&](int st) { return smem_u32(base + G::OFF_K + st * G::K_BYTES); };
+  auto sVa = [&](int st) { return smem_u32(base + G::OFF_V + st * G::V_BYTES); };
+
+  const int pairs = p.nh >> 1;
+  const int bp_count = p.batch * pairs;
+  const int qb = p.num_qb - 1 - static_cast<int>(blockIdx.x) / bp_count;  // longest first
+  const int bp = static_cast<int>(blockIdx.x) % bp_count;
+  const int b = bp / pairs, h0 = 2 * (bp - b * pairs);
+  const int g = h0 / (p.nh / p.ng);
+  const int nkv = qb + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(k_full(i), 1);
+      mbar_init(k_empty(i), 1);
+      mbar_init(v_full(i), 1);
+      mbar_init(v_empty(i), 1);
+      mbar_init(s_full(i), 1);
+      mbar_init(p_full(i), 4);
+      mbar_init(o_done(i), 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(&tmQ);
+    tma_prefetch(&tmK);
+    tma_prefetch(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  auto tS = [&](int t) { return tmem_base + 256u * t; };
+  auto tO = [&](int t) { return tmem_base + 256u * t + 128u; };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, 2 * G::Q_BYTES);
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int a = 0; a < D / 64; ++a)
+          tma_load_3d(sQa(t) + a * G::ATOM, &tmQ, q_full, a * 64, qb * BQ, b * p.nh + h0 + t);
+      int issued_k = 0, issued_v = 0;
+      bool ok = true;
+      for (int j = 0; ok && j < nkv; ++j) {
+        const int st = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        if (!mbar_wait(k_empty(st), ph ^ 1u, p.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(k_full(st), G::K_BYTES);
+#pragma unroll
+        for (int a = 0; a < D / 64; ++a)
+          tma_load_3d(sKa(st) + a * G::ATOM, &tmK, k_full(st), a * 64, j * BKV, b * p.ng + g);
+        ++issued_k;
+        if (!mbar_wait(v_empty(st), ph ^ 1u, p.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(v_full(st), G::V_BYTES);
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+          tma_load_3d(sVa(st) + a * G::V_ATOM, &tmV, v_full(st), j * BKV + a * 64, 0, b * p.ng + g);
+        ++issued_v;
+      }
+      if (!ok) {  // let this CTA's own copies in flight land
+        mbar_wait_slow(q_full, 0, nullptr, nullptr, kDrainLimitNs);
+        for (int j = issued_k - 1; j >= 0 && j >= issued_k - 2; --j)
+          mbar_wait_slow(k_full(j & 1), (j >> 1) & 1, nullptr, nullptr, kDrainLimitNs);
+        for (int j = issued_v - 1; j >= 0 && j >= issued_v - 2; --j)
+          mbar_wait_slow(v_full(j & 1), (j >> 1) & 1, nullptr, nullptr, kDrainLimitNs);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      auto issue_s = [&](int t, int st) {
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * G::ATOM + (k & 3) * 32;
+          mma_bf16_ss(tS(t), sw128_desc(sQa(t) + off), sw128_desc(sKa(st) + off), G::IDESC_S, k > 0 ? 1u : 0u);
+        }
+        mma_commit(s_full(t));
+      };
+      bool ok = mbar_wait(q_full, 0, p.err, abort_flag) && mbar_wait(k_full(0), 0, p.err, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        issue_s(1, 0);
+        mma_commit(k_empty(0));
+      }
+      for (int j = 0; ok && j < nkv; ++j) {
+        const int st = j & 1;
+        if (!mbar_wait(v_full(st), (j >> 1) & 1, p.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (!mbar_wait(p_full(t), j & 1, p.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < BKV / 16; ++k) {
+            const uint32_t va = sVa(st) + (k >> 2) * G::V_ATOM + (k & 3) * 32;
+            mma_bf16_ts(tO(t), tS(t) + 8u * k, sw128_desc(va), G::IDESC_O, (j > 0 || k > 0) ? 1u : 0u);
+          }
+          mma_commit(o_done(t));
+        }
+        if (!ok) break;
+        mma_commit(v_empty(st));
+        if (j + 1 < nkv) {
+          const int st1 = (j + 1) & 1;
+          if (!mbar_wait(k_full(st1), ((j + 1) >> 1) & 1, p.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          for (int t = 0; t < 2; ++t) {
+            // S_t(j+1) overwrites the columns P_t(j) V_j reads: wait until that MMA is done.
+            if (!mbar_wait(o_done(t), j & 1, p.err, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(t, st1);
+          }
+          if (!ok) break;
+          mma_commit(k_empty(st1));
+        }
+      }
+      mma_commit(drain);
+      mbar_wait_slow(drain, 0, nullptr, nullptr, ok ? kWaitLimitNs : kDrainLimitNs);
+    }
+  } else {
+    const int t = (warp - 2) >> 2;  // which head of the pair
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const int sq = qb * BQ + r;
+    const int h = h0 + t;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const float c = p.scale_log2;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nkv; ++j) {
+      bool w = mbar_wait(s_full(t), j & 1, p.err, abort_flag);
+      if (!__all_sync(0xffffffffu, w)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[BKV];
+#pragma unroll
+      for (int cc = 0; cc < BKV / 32; ++cc) tmem_ld32(tS(t) + lane_off + cc * 32, s + cc * 32);
+      if (j == qb) {
+#pragma unroll
+        for (int i = 0; i < BKV; ++i)
+          if (i > r) s[i] = -INFINITY;
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < BKV; ++i) mx = fmaxf(mx, s[i]);
+      const float m_new = fmaxf(m_used, mx * c);
+      if (__any_sync(0xffffffffu, m_new > m_used + 8.0f)) {
+        const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m_used - m_new);
+        l *= alpha;
+        if (j > 0) {
+          w = mbar_wait(o_done(t), (j - 1) & 1, p.err, abort_flag);
+          if (!__all_sync(0xffffffffu, w)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
+            float o[32];
+            tmem_ld32(tO(t) + lane_off + cc * 32, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(tO(t) + lane_off + cc * 32, o);
+          }
+        }
+        m_used = m_new;
+      }
+      float rs = 0.f;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ex2_approx(fmaf(s[64 * hf + 2 * i], c, -m_used));
+          const float p1 = ex2_approx(fmaf(s[64 * hf + 2 * i + 1], c, -m_used));
+          rs += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32_raw(tS(t) + lane_off + 32 * hf, pk);
+      }
+      l += rs;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full(t));
+    }
+    if (ok) {
+      const bool w = mbar_wait(o_done(t), (nkv - 1) & 1, p.err, abort_flag);
+      if (__all_sync(0xffffffffu, w)) {
+        tc_fence_after();
+        const float inv_l = 1.f / l;
+        bf16* orow = p.o + (static_cast<size_t>(sq) * p.batch + b) * p.ldo + h * D;
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          float o[32];
+          tmem_ld32(tO(t) + lane_off + cc * 32, o);
+          if (sq < p.seq) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= inv_l;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              *reinterpret_cast<uint4*>(orow + cc * 32 + q4 * 8) = pack_bf16x8(o + q4 * 8);
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_d2(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnParams& p,
+                      cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn2_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(Geo2<D>::SMEM));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const unsigned grid = static_cast<unsigned>(p.num_qb) * p.batch * (p.nh / 2);
+  attn2_kernel<D><<<grid, 320, Geo2<D>::SMEM, stream>>>(tmQ, tmK, tmV, p);
+  return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch_d(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnParams& p,
                      cudaStream_t stream) {
@@ -301,6 +606,9 @@ cudaError_t launch_d(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUten
 cudaError_t launch_attention(int head_dim, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                              const AttnParams& p, cudaStream_t stream) {
   if (p.num_qb <= 0) return cudaSuccess;
+  const bool paired = ((p.nh / p.ng) & 1) == 0;  // an even number of query heads per kv group
+  if (paired && head_dim == 64) return launch_d2<64>(tmQ, tmK, tmV, p, stream);
+  if (paired && head_dim == 128) return launch_d2<128>(tmQ, tmK, tmV, p, stream);
   if (head_dim == 64) return launch_d<64>(tmQ, tmK, tmV, p, stream);
   if (head_dim == 128) return launch_d<128>(tmQ, tmK, tmV, p, stream);
   return cudaErrorInvalidValue;

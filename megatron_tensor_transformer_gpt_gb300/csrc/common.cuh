@@ -145,6 +145,18 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uin
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T: A (M=128 rows, one per TMEM lane, K packed two bf16 per 32-bit
+// column) is read from tensor memory, B from shared memory.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -178,6 +190,20 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
   uint32_t r[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(v[i]);
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      MT_W32(0), MT_W32(1), MT_W32(2), MT_W32(3), MT_W32(4), MT_W32(5), MT_W32(6), MT_W32(7), MT_W32(8),
+      MT_W32(9), MT_W32(10), MT_W32(11), MT_W32(12), MT_W32(13), MT_W32(14), MT_W32(15), MT_W32(16), MT_W32(17),
+      MT_W32(18), MT_W32(19), MT_W32(20), MT_W32(21), MT_W32(22), MT_W32(23), MT_W32(24), MT_W32(25), MT_W32(26),
+      MT_W32(27), MT_W32(28), MT_W32(29), MT_W32(30), MT_W32(31)
+      : "memory");
+}
+
+// Raw 32-bit variant of tmem_st32 (e.g. packed bf16 pairs).
+__device__ __forceinline__ void tmem_st32_raw(uint32_t taddr, const uint32_t* r) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
       "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
