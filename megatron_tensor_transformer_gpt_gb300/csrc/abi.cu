@@ -2,6 +2,7 @@
 // the kernel sequence of one layer forward on the caller's stream.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -193,23 +194,67 @@ mt::GemmParams gemm_params(int M, int N, int K, bool swiglu, int* err) {
   p.tiles_m = (M + 127) / 128;
   p.tiles_n = swiglu ? (N + 127) / 128 : (N + 255) / 256;
   p.num_tiles = p.tiles_m * p.tiles_n;
-  p.b_row_step = swiglu ? N : 128;
+  p.b_row_step = swiglu ? N : 0;
   p.err = err;
   return p;
+}
+
+// Tile order and tail split of one GEMM (see GemmParams).
+//   Order: if one operand fits in about 56 MB of the 129 MB L2 it is kept resident (the other is
+//   streamed once); otherwise bands of m-tiles (or n-tiles) of about 56 MB, whichever streams
+//   fewer bytes from DRAM.
+//   Split: the tiles of the last partial wave on the SMs are cut into 2 or 4 pieces along N when
+//   the pieces still fit in one wave (QKV pieces keep whole heads; SwiGLU pieces at least 64
+//   outputs, the smallest TMA box used).
+void plan_gemm(mt::GemmParams& p, int mode, int head_dim) {
+  const double budget = 56.0 * 1024 * 1024;
+  const double a_tile = 128.0 * p.K * 2, b_tile = 256.0 * p.K * 2;
+  const double a_all = a_tile * p.tiles_m, b_all = b_tile * p.tiles_n;
+  if (a_all <= budget) {
+    p.band_m = 1;
+    p.band = p.tiles_m;
+  } else if (b_all <= budget) {
+    p.band_m = 0;
+    p.band = p.tiles_n;
+  } else {
+    const int gm = std::max(1, static_cast<int>(budget / a_tile));
+    const int gn = std::max(1, static_cast<int>(budget / b_tile));
+    const double tm = a_all + b_all * ((p.tiles_m + gm - 1) / gm);
+    const double tn = b_all + a_all * ((p.tiles_n + gn - 1) / gn);
+    p.band_m = tm <= tn ? 1 : 0;
+    p.band = tm <= tn ? std::min(gm, p.tiles_m) : std::min(gn, p.tiles_n);
+  }
+  const int sms = mt::num_sms();
+  const int waves = p.num_tiles / sms;
+  const int rest = p.num_tiles - waves * sms;
+  int max_split = 4;
+  if (mode == mt::kEpiSwiglu) max_split = 2;
+  if (mode == mt::kEpiQkv) max_split = std::max(1, 256 / head_dim);
+  p.split = 1;
+  for (int s = max_split; s >= 2; s /= 2)
+    if (rest > 0 && rest * s <= sms) {
+      p.split = s;
+      break;
+    }
+  p.full_units = p.split > 1 ? waves * sms : p.num_tiles;
+  p.num_units = p.full_units + (p.split > 1 ? rest * p.split : 0);
 }
 
 // One GEMM: A [M, K] (pitch lda) x W [rows_w, K]^T with the given epilogue.
 int run_gemm(mt_layer* L, int slot, int mode, const void* A, int lda, const void* W, int rows_w, int M, int N, int K,
              mt::GemmParams p, cudaStream_t st) {
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tb64;
   int rc = map_2d(&ta, A, K, M, lda, 128);
   if (rc) return rc;
   rc = map_2d(&tb, W, K, rows_w, K, 128);
   if (rc) return rc;
+  rc = map_2d(&tb64, W, K, rows_w, K, 64);
+  if (rc) return rc;
+  plan_gemm(p, mode, mode == mt::kEpiQkv ? p.head_dim : 0);
   cudaError_t e;
   {
     Timed t(L, slot, st);
-    e = mt::launch_gemm(mode, ta, tb, p, st);
+    e = mt::launch_gemm(mode, ta, tb, tb64, p, st);
   }
   if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
   return MT_OK;

@@ -12,7 +12,9 @@
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (one TMEM lane = one output row per
 //               thread), fused bias / residual / RoPE / SwiGLU / GeLU, bf16 stores; the second
 //               accumulator lets the next tile's main loop run meanwhile.
-// Tiles are ordered with M fastest so the CTAs in flight share B tiles and the whole A in L2.
+// Tile order is chosen on the host per GEMM (bands of m- or n-tiles sized so the band's operand stays
+// in L2, see GemmParams), and the tiles of the last, partial wave are cut into 2 or 4 narrower
+// pieces along N so that the tail wave is shorter (wave quantisation on 152 SMs).
 #include "common.cuh"
 #include "internal.h"
 
@@ -24,7 +26,6 @@ constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB (two 128-row boxes)
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t TMEM_COLS = 2 * BN;
-constexpr uint32_t IDESC = idesc_bf16(BM, BN);
 constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
 
 // ------------------------------------------------------------------ epilogue helpers
@@ -54,15 +55,60 @@ __device__ __forceinline__ float gelu_tanh(float u) {
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
+// One work unit: tile (tm, tn) of the raster, piece `sub` of `split` along N.
+struct Unit {
+  int tm, tn, sub, split;
+};
+
+__device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u) {
+  Unit w;
+  int tile;
+  if (u < p.full_units) {
+    tile = u;
+    w.sub = 0;
+    w.split = 1;
+  } else {
+    const int v = u - p.full_units;
+    tile = p.full_units + v / p.split;
+    w.sub = v % p.split;
+    w.split = p.split;
+  }
+  if (p.band_m) {
+    const int per_band = p.band * p.tiles_n;
+    const int bi = tile / per_band, r = tile - bi * per_band;
+    const int gm = min(p.band, p.tiles_m - bi * p.band);
+    w.tm = bi * p.band + r % gm;
+    w.tn = r / gm;
+  } else {
+    const int per_band = p.band * p.tiles_m;
+    const int bi = tile / per_band, r = tile - bi * per_band;
+    const int gn = min(p.band, p.tiles_n - bi * p.band);
+    w.tn = bi * p.band + r % gn;
+    w.tm = r / gn;
+  }
+  return w;
+}
+
+// Output columns of a unit: [c0, c0 + width).  SwiGLU tiles cover 128 outputs (256 accumulator
+// columns: gate then up); the others 256.
 template <int MODE>
-__device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc, int m0, int tn, int r_in_tile) {
+__device__ __forceinline__ int unit_width(const Unit& w) {
+  return (MODE == kEpiSwiglu ? 128 : BN) / w.split;
+}
+template <int MODE>
+__device__ __forceinline__ int unit_col0(const Unit& w) {
+  return w.tn * (MODE == kEpiSwiglu ? 128 : BN) + w.sub * unit_width<MODE>(w);
+}
+
+template <int MODE>
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc, int m0, int c0, int width,
+                                              int r_in_tile) {
   const int row = m0 + r_in_tile;
   const bool valid = row < p.M;
   if constexpr (MODE == kEpiStore || MODE == kEpiResid || MODE == kEpiGelu) {
-    const int n0 = tn * BN;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
-      const int col = n0 + c;
+    for (int c = 0; c < width; c += 32) {
+      const int col = c0 + c;
       if (col >= p.N) break;  // uniform across the warp
       float v[32];
       tmem_ld32(tacc + c, v);
@@ -77,14 +123,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
       }
     }
   } else if constexpr (MODE == kEpiSwiglu) {
-    const int n0 = tn * 128;
 #pragma unroll 1
-    for (int c = 0; c < 128; c += 32) {
-      const int col = n0 + c;
+    for (int c = 0; c < width; c += 32) {
+      const int col = c0 + c;
       if (col >= p.N) break;
       float g[32], u[32];
       tmem_ld32(tacc + c, g);
-      tmem_ld32(tacc + 128 + c, u);
+      tmem_ld32(tacc + width + c, u);  // the up half follows the `width` gate columns
       if (valid) {
         if (p.bias != nullptr) {
           add_vec32(g, p.bias, col, p.N);
@@ -95,14 +140,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
         store_vec32(p.out + static_cast<size_t>(row) * p.ldo, col, p.N, g);
       }
     }
-  } else {  // kEpiQkv
+  } else {  // kEpiQkv: `width` is a multiple of head_dim, so every head lies inside one unit
     const int d = p.head_dim, half = d >> 1;
-    const int n0 = tn * BN;
     const int s = valid ? row / p.batch : 0;
     const int b = valid ? row - s * p.batch : 0;
 #pragma unroll 1
-    for (int hc = 0; hc < BN; hc += d) {
-      const int col = n0 + hc;
+    for (int hc = 0; hc < width; hc += d) {
+      const int col = c0 + hc;
       if (col >= p.N) break;
       bf16* dst;
       bool is_v = false;
@@ -166,7 +210,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
 // ------------------------------------------------------------------ kernel
 template <int MODE>
 __global__ void __launch_bounds__(192, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmB64, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = base;
@@ -199,6 +244,7 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch(&tmA);
     tma_prefetch(&tmB);
+    tma_prefetch(&tmB64);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -215,23 +261,35 @@ __global__ void __launch_bounds__(192, 1)
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-        const int tm = tile % p.tiles_m, tn = tile / p.tiles_m;
-        const int m0 = tm * BM;
-        const int r0 = (MODE == kEpiSwiglu) ? tn * 128 : tn * BN;
-        const int r1 = r0 + p.b_row_step;
+      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+        const Unit w = decode_unit(p, u);
+        const int m0 = w.tm * BM;
+        const int width = unit_width<MODE>(w);
+        const int c0 = unit_col0<MODE>(w);
+        // B rows of this unit: SwiGLU gate rows [c0, c0+width) then the matching up rows;
+        // otherwise rows [c0, c0+width).  Boxes of 128 rows, or 64 for the narrowest pieces.
+        const int b_rows = MODE == kEpiSwiglu ? 2 * width : width;
+        const uint32_t stage_bytes = A_BYTES + b_rows * BK * 2;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(empty(stage), phase ^ 1u, p.err, abort_flag)) {
             ok = false;
             break;
           }
           const uint32_t fb = full(stage);
-          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          mbar_arrive_expect_tx(fb, stage_bytes);
           const uint32_t a_dst = smem_u32(sA + stage * A_BYTES);
           const uint32_t b_dst = smem_u32(sB + stage * B_BYTES);
           tma_load_2d(a_dst, &tmA, fb, kb * BK, m0);
-          tma_load_2d(b_dst, &tmB, fb, kb * BK, r0);
-          tma_load_2d(b_dst + B_BYTES / 2, &tmB, fb, kb * BK, r1);
+          if (MODE == kEpiSwiglu) {
+            const CUtensorMap* mb = width == 128 ? &tmB : &tmB64;
+            tma_load_2d(b_dst, mb, fb, kb * BK, c0);
+            tma_load_2d(b_dst + width * BK * 2, mb, fb, kb * BK, c0 + p.b_row_step);
+          } else if (width == 256) {
+            tma_load_2d(b_dst, &tmB, fb, kb * BK, c0);
+            tma_load_2d(b_dst + B_BYTES / 2, &tmB, fb, kb * BK, c0 + 128);
+          } else {
+            tma_load_2d(b_dst, width == 128 ? &tmB : &tmB64, fb, kb * BK, c0);
+          }
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -250,7 +308,10 @@ __global__ void __launch_bounds__(192, 1)
       int stage = 0, it = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
+      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
+        const Unit w = decode_unit(p, u);
+        const int width = unit_width<MODE>(w);
+        const uint32_t idesc = idesc_bf16(BM, MODE == kEpiSwiglu ? 2 * width : width);
         const int acc = it & 1;
         const uint32_t use = (it >> 1) & 1;
         if (!mbar_wait(tempty(acc), use ^ 1u, p.err, abort_flag)) {
@@ -269,7 +330,7 @@ __global__ void __launch_bounds__(192, 1)
           const uint64_t bd = sw128_desc(smem_u32(sB + stage * B_BYTES));
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            mma_bf16_ss(d_tmem, ad + 2ull * k, bd + 2ull * k, IDESC, (kb | k) != 0 ? 1u : 0u);
+            mma_bf16_ss(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb | k) != 0 ? 1u : 0u);
           mma_commit(empty(stage));
           if (++stage == STAGES) {
             stage = 0;
@@ -285,15 +346,15 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     const int quad = warp & 3;  // TMEM lanes this warp may read
     int it = 0;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
+    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++it) {
       const int acc = it & 1;
       const uint32_t use = (it >> 1) & 1;
-      const bool w = mbar_wait(tfull(acc), use, p.err, abort_flag);
-      if (!__all_sync(0xffffffffu, w)) break;
+      const bool ok = mbar_wait(tfull(acc), use, p.err, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      const int tm = tile % p.tiles_m, tn = tile / p.tiles_m;
+      const Unit w = decode_unit(p, u);
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
-      epilogue_tile<MODE>(p, tacc, tm * BM, tn, quad * 32 + lane);
+      epilogue_tile<MODE>(p, tacc, w.tm * BM, unit_col0<MODE>(w), unit_width<MODE>(w), quad * 32 + lane);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty(acc));
@@ -308,7 +369,8 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 template <int MODE>
-cudaError_t launch_mode(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, cudaStream_t stream) {
+cudaError_t launch_mode(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB64, const GemmParams& p,
+                        cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -316,8 +378,8 @@ cudaError_t launch_mode(const CUtensorMap& tmA, const CUtensorMap& tmB, const Ge
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
-  gemm_kernel<MODE><<<grid, 192, SMEM_BYTES, stream>>>(tmA, tmB, p);
+  const int grid = p.num_units < num_sms() ? p.num_units : num_sms();
+  gemm_kernel<MODE><<<grid, 192, SMEM_BYTES, stream>>>(tmA, tmB, tmB64, p);
   return cudaGetLastError();
 }
 
@@ -325,15 +387,15 @@ cudaError_t launch_mode(const CUtensorMap& tmA, const CUtensorMap& tmB, const Ge
 
 size_t gemm_smem_bytes() { return SMEM_BYTES; }
 
-cudaError_t launch_gemm(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,
-                        cudaStream_t stream) {
-  if (p.num_tiles <= 0) return cudaSuccess;
+cudaError_t launch_gemm(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB64,
+                        const GemmParams& p, cudaStream_t stream) {
+  if (p.num_units <= 0) return cudaSuccess;
   switch (mode) {
-    case kEpiStore: return launch_mode<kEpiStore>(tmA, tmB, p, stream);
-    case kEpiResid: return launch_mode<kEpiResid>(tmA, tmB, p, stream);
-    case kEpiQkv: return launch_mode<kEpiQkv>(tmA, tmB, p, stream);
-    case kEpiSwiglu: return launch_mode<kEpiSwiglu>(tmA, tmB, p, stream);
-    case kEpiGelu: return launch_mode<kEpiGelu>(tmA, tmB, p, stream);
+    case kEpiStore: return launch_mode<kEpiStore>(tmA, tmB, tmB64, p, stream);
+    case kEpiResid: return launch_mode<kEpiResid>(tmA, tmB, tmB64, p, stream);
+    case kEpiQkv: return launch_mode<kEpiQkv>(tmA, tmB, tmB64, p, stream);
+    case kEpiSwiglu: return launch_mode<kEpiSwiglu>(tmA, tmB, tmB64, p, stream);
+    case kEpiGelu: return launch_mode<kEpiGelu>(tmA, tmB, tmB64, p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

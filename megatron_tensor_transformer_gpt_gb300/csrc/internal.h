@@ -23,7 +23,13 @@ enum GemmEpilogue : int {
 struct GemmParams {
   int M, N, K;        // output rows, output columns (SwiGLU: gate width), reduction length
   int tiles_m, tiles_n, num_tiles;
-  int b_row_step;     // row offset of the second 128-row B box: 128, or the gate width for SwiGLU
+  int b_row_step;     // SwiGLU: row offset of the up half of W (the gate width); unused otherwise
+  // Tile order (rasterisation): tiles come in bands of `band` m-tiles (band_m = 1, m fastest
+  // inside a band) or `band` n-tiles (band_m = 0, n fastest), so a band's operand stays in L2.
+  int band, band_m;
+  // Work units: [0, full_units) are whole tiles; the tiles after them (the last, partial wave)
+  // are cut into `split` pieces along N so that the tail wave is shorter.  num_units in total.
+  int full_units, split, num_units;
   bf16* out;
   int ldo;
   const bf16* bias;   // [N] (SwiGLU: [2N]) or null
@@ -49,8 +55,8 @@ struct AttnParams {
 int num_sms();
 
 // Kernel launchers; return a cudaError_t from the launch.
-cudaError_t launch_gemm(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,
-                        cudaStream_t stream);
+cudaError_t launch_gemm(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB64,
+                        const GemmParams& p, cudaStream_t stream);
 size_t gemm_smem_bytes();
 
 cudaError_t launch_attention(int head_dim, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
