@@ -115,6 +115,21 @@ int mt_layer_forward_attn(mt_layer* L, const void* x, int seq, int batch, const 
 int mt_layer_forward_mlp(mt_layer* L, const void* h, int seq, int batch, const mt_weights* w, void* y_partial,
                          void* cuda_stream);
 
+/* Packed variable-length samples ("快速入门 / Pai-Megatron-Patch 项目深度学习总结文档" §4.1 and §8,
+ * sequence packing: several samples concatenated into one sequence, with cu_seqlens the cumulative
+ * sample lengths [0, len1, len1+len2, ...] and attention kept inside each sample as FlashAttention's
+ * variable-length form does).  x, y_partial: [total_tokens, H] (batch 1, samples back to back).
+ * cu_seqlens: DEVICE array of num_seqs + 1 ints, cu[0] = 0, non-decreasing, cu[num_seqs] =
+ * total_tokens; max_seqlen (host) bounds every sample's length (empty samples are allowed).
+ * Sample i is tokens [cu[i], cu[i+1]): its queries see only its own earlier keys, and RoPE positions
+ * restart at 0 in every sample, so each sample computes what it would alone.  Otherwise as
+ * mt_layer_forward (TP semantics included).  Workspace: mt_layer_workspace_bytes_packed.
+ * cu_seqlens that turn out inconsistent on the device are reported by mt_layer_status as
+ * MT_ERR_INVALID_ARG (every access stays in bounds; the outputs are then invalid). */
+int mt_layer_workspace_bytes_packed(const mt_layer* L, int total_tokens, int num_seqs, int max_seqlen, size_t* bytes);
+int mt_layer_forward_packed(mt_layer* L, const void* x, int total_tokens, const int* cu_seqlens, int num_seqs,
+                            int max_seqlen, const mt_weights* w, void* y_partial, void* cuda_stream);
+
 /* mt_layer_forward with x and y in HOST memory (pinned for asynchronous copies): copies x
  * into the workspace, runs the layer, copies y back, all on `cuda_stream`; the host buffers
  * must stay valid until the stream reaches this point. */
@@ -129,7 +144,8 @@ int mt_layer_forward_host(mt_layer* L, const void* x_host, int seq, int batch, c
 int mt_layer_workspace_region(const mt_layer* L, int seq, int batch, int which, size_t* offset, size_t* bytes);
 
 /* Synchronise with the work queued by this handle (all streams) and report a device-side
- * failure recorded since the last call (MT_ERR_DEVICE_TIMEOUT), clearing it. */
+ * failure recorded since the last call (MT_ERR_DEVICE_TIMEOUT, or MT_ERR_INVALID_ARG for
+ * inconsistent packed cu_seqlens), clearing it. */
 int mt_layer_status(mt_layer* L);
 
 /* Thread-local description of the last failure on this thread ("" after success). */
@@ -153,6 +169,23 @@ int mt_layer_profile_read(mt_layer* L, int* launches, double* total_ms);
  * ("Megatron-LM 深度学习与源码分析文档" Part 2 §2, Y = XW with W stored [out, in]).
  * Device pointers, 16-byte aligned; K % 8 == 0 and N % 8 == 0. */
 int mt_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, void* cuda_stream);
+
+/* Sequence-parallel epilogue of a row-parallel linear, for one rank's sequence slice
+ * ("Megatron-LM 深度学习与源码分析文档" Part 2 §4 Sequence Parallel: after a RowParallel linear the
+ * output is reduce-scattered back to sequence-sharded activations, and LayerNorm/dropout/residual
+ * run on S/TP rows per rank; its kernel list names "RowParallel reduce-scatter fused add/norm").
+ * On one GPU the ranks' partials are all local, so the reduce-scatter becomes a sum over them:
+ * for the rows [row0, row0 + rows) of the [tokens, hidden] activations (rank r of p holds
+ * row0 = r * tokens / p, rows = tokens / p: the [s, b, h] layout makes a sequence slice contiguous)
+ *     h  = resid + sum_i partials[i] + bias      (fp32 sum; stored as bf16)
+ *     hn = Norm(h)                                (statistics over the stored bf16 h)
+ * partials: host array of num_partials (1..16) device pointers, each a full [tokens, hidden] bf16
+ * pre-reduce partial (e.g. mt_layer_forward_attn outputs).  resid, h_out and hn_out are the slice
+ * ([rows, hidden] bf16, device); bias [hidden] may be NULL; norm_w/norm_b as in mt_weights.
+ * One kernel launch on cuda_stream; hidden % 8 == 0, hidden <= 8192. */
+int mt_sp_reduce_add_norm(const void* const* partials, int num_partials, const void* resid, const void* bias,
+                          const void* norm_w, const void* norm_b, int norm, float eps, int tokens, int hidden, int row0,
+                          int rows, void* h_out, void* hn_out, void* cuda_stream);
 
 /* Fault-detection self test: launches one CTA that waits on a barrier nothing will complete,
  * giving up after `limit_us` microseconds (1..1000000).  Returns MT_ERR_DEVICE_TIMEOUT when the

@@ -98,7 +98,7 @@ struct Timed {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // ------------------------------------------------------------------ workspace layout
-enum Region { kXn = 0, kQ, kK, kVt, kO, kH, kHn, kA, kRope, kXStage, kYStage, kNumRegions };
+enum Region { kXn = 0, kQ, kK, kVt, kO, kH, kHn, kA, kRope, kXStage, kYStage, kPos, kVcol, kNumRegions };
 
 struct Layout {
   size_t off[kNumRegions];
@@ -109,11 +109,13 @@ struct Layout {
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-Layout layout_for(const mt_layer* L, int S, int B) {
+// Workspace of one call: S x B tokens; v^T rows of `vt_pitch` columns; a RoPE table of `rope_rows`
+// positions; `index_tokens` per-token position / v^T-column entries (packed samples only).
+Layout make_layout(const mt_layer* L, int S, int B, int vt_pitch, int rope_rows, int index_tokens) {
   Layout lay{};
   const size_t T = static_cast<size_t>(S) * B;
   const size_t d = L->head_dim;
-  lay.seq_pad = static_cast<int>(round_up(S, 8));
+  lay.seq_pad = vt_pitch;
   lay.size[kXn] = T * L->hidden * 2;
   lay.size[kQ] = static_cast<size_t>(B) * L->nh_r * S * d * 2;
   lay.size[kK] = static_cast<size_t>(B) * L->ng_r * S * d * 2;
@@ -122,9 +124,11 @@ Layout layout_for(const mt_layer* L, int S, int B) {
   lay.size[kH] = T * L->hidden * 2;
   lay.size[kHn] = T * L->hidden * 2;
   lay.size[kA] = T * L->f_r * 2;
-  lay.size[kRope] = L->rope_base > 0.f ? static_cast<size_t>(S) * (d / 2) * sizeof(float2) : 0;
+  lay.size[kRope] = L->rope_base > 0.f ? static_cast<size_t>(rope_rows) * (d / 2) * sizeof(float2) : 0;
   lay.size[kXStage] = T * L->hidden * 2;
   lay.size[kYStage] = T * L->hidden * 2;
+  lay.size[kPos] = static_cast<size_t>(index_tokens) * sizeof(int);
+  lay.size[kVcol] = static_cast<size_t>(index_tokens) * sizeof(int);
   size_t o = 0;
   for (int r = 0; r < kNumRegions; ++r) {
     lay.off[r] = o;
@@ -133,6 +137,23 @@ Layout layout_for(const mt_layer* L, int S, int B) {
   lay.total = o;
   return lay;
 }
+
+Layout layout_for(const mt_layer* L, int S, int B) {
+  return make_layout(L, S, B, static_cast<int>(round_up(S, 8)), S, 0);
+}
+
+// Packed samples: batch 1, T tokens; every sample's v^T columns start on a multiple of 8, at most
+// 8 columns after the previous sample's end.
+int packed_vcols(int T, int num_seqs) { return static_cast<int>(round_up(static_cast<size_t>(T) + 8 * num_seqs, 8)); }
+Layout layout_packed(const mt_layer* L, int T, int num_seqs, int max_seqlen) {
+  return make_layout(L, T, 1, packed_vcols(T, num_seqs), max_seqlen, T);
+}
+
+// Packed-sample description of a call (null for dense batches).
+struct Packed {
+  const int* cu;  // device, num_seqs + 1 entries
+  int num_seqs, max_seqlen;
+};
 
 template <typename T>
 T* region(const mt_layer* L, const Layout& lay, Region r) {
@@ -304,15 +325,26 @@ int check_call(const mt_layer* L, const void* in, const void* out, int S, int B,
 // Attention block: norm1 -> QKV GEMM (+bias, RoPE, scatter) -> flash attention -> output projection.
 // out_mode kEpiStore writes the rank's partial; kEpiResid writes h = x + Y + b_o.
 int run_attention_block(mt_layer* L, const Layout& lay, const void* x, int S, int B, const mt_weights* w, void* out,
-                        int out_mode, cudaStream_t st) {
+                        int out_mode, cudaStream_t st, const Packed* pk = nullptr) {
   const int T = S * B, H = L->hidden, d = L->head_dim;
   cudaError_t e;
   float2* rope = nullptr;
   if (L->rope_base > 0.f) {
     rope = region<float2>(L, lay, kRope);
     Timed t(L, kSlotRope, st);
-    e = mt::launch_rope_table(rope, L->d_theta, S, d / 2, st);
+    e = mt::launch_rope_table(rope, L->d_theta, pk ? pk->max_seqlen : S, d / 2, st);
     if (e != cudaSuccess) return cuda_fail(e, "RoPE table launch");
+  }
+  int *pos = nullptr, *vcol = nullptr;
+  if (pk != nullptr) {
+    // v^T columns between samples are never written: zero them so masked P.V stays finite
+    e = cudaMemsetAsync(region<void>(L, lay, kVt), 0, lay.size[kVt], st);
+    if (e == cudaSuccess) {
+      pos = region<int>(L, lay, kPos);
+      vcol = region<int>(L, lay, kVcol);
+      e = mt::launch_packed_index(pk->cu, pk->num_seqs, T, pk->max_seqlen, lay.seq_pad, pos, vcol, L->d_err, st);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "packed-sample index");
   }
   bf16* xn = region<bf16>(L, lay, kXn);
   {
@@ -338,13 +370,15 @@ int run_attention_block(mt_layer* L, const Layout& lay, const void* x, int S, in
   p.nh = L->nh_r;
   p.ng = L->ng_r;
   p.seq_pad = lay.seq_pad;
+  p.pos = pos;
+  p.vcol = vcol;
   int rc = run_gemm(L, kSlotQkv, mt::kEpiQkv, xn, H, w->w_qkv, nqkv, T, nqkv, H, p, st);
   if (rc) return rc;
 
   CUtensorMap tq, tk, tv;
   if ((rc = map_3d(&tq, q, d, S, static_cast<uint64_t>(B) * L->nh_r, d, static_cast<uint64_t>(S) * d, 128))) return rc;
   if ((rc = map_3d(&tk, k, d, S, static_cast<uint64_t>(B) * L->ng_r, d, static_cast<uint64_t>(S) * d, 128))) return rc;
-  if ((rc = map_3d(&tv, vt, S, d, static_cast<uint64_t>(B) * L->ng_r, lay.seq_pad,
+  if ((rc = map_3d(&tv, vt, pk ? lay.seq_pad : S, d, static_cast<uint64_t>(B) * L->ng_r, lay.seq_pad,
                    static_cast<uint64_t>(d) * lay.seq_pad, static_cast<uint32_t>(d))))
     return rc;
   bf16* o = region<bf16>(L, lay, kO);
@@ -353,7 +387,9 @@ int run_attention_block(mt_layer* L, const Layout& lay, const void* x, int S, in
   ap.batch = B;
   ap.nh = L->nh_r;
   ap.ng = L->ng_r;
-  ap.num_qb = (S + 127) / 128;
+  ap.num_qb = ((pk ? pk->max_seqlen : S) + 127) / 128;
+  ap.cu = pk ? pk->cu : nullptr;
+  ap.num_seqs = pk ? pk->num_seqs : 0;
   ap.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
   ap.o = o;
   ap.ldo = L->q_w;
@@ -409,9 +445,9 @@ int run_mlp_block(mt_layer* L, const Layout& lay, const void* h, int S, int B, c
 }
 
 int forward_device(mt_layer* L, const Layout& lay, const void* x, int S, int B, const mt_weights* w, void* y,
-                   cudaStream_t st) {
+                   cudaStream_t st, const Packed* pk = nullptr) {
   bf16* h = region<bf16>(L, lay, kH);
-  int rc = run_attention_block(L, lay, x, S, B, w, h, mt::kEpiResid, st);
+  int rc = run_attention_block(L, lay, x, S, B, w, h, mt::kEpiResid, st, pk);
   if (rc) return rc;
   return run_mlp_block(L, lay, h, S, B, w, y, L->tp == 1 ? mt::kEpiResid : mt::kEpiStore, st);
 }
@@ -559,6 +595,34 @@ int mt_layer_forward_mlp(mt_layer* L, const void* h, int seq, int batch, const m
   return rc ? rc : ok();
 }
 
+int mt_layer_workspace_bytes_packed(const mt_layer* L, int total_tokens, int num_seqs, int max_seqlen, size_t* bytes) {
+  if (L == nullptr || bytes == nullptr) return fail(MT_ERR_INVALID_ARG, "handle or bytes is NULL");
+  if (total_tokens <= 0 || num_seqs <= 0 || max_seqlen <= 0 || max_seqlen > total_tokens)
+    return fail(MT_ERR_INVALID_ARG, "need total_tokens > 0, num_seqs > 0, 0 < max_seqlen <= total_tokens");
+  *bytes = layout_packed(L, total_tokens, num_seqs, max_seqlen).total;
+  return ok();
+}
+
+int mt_layer_forward_packed(mt_layer* L, const void* x, int total_tokens, const int* cu_seqlens, int num_seqs,
+                            int max_seqlen, const mt_weights* w, void* y_partial, void* cuda_stream) {
+  if (L == nullptr) return fail(MT_ERR_INVALID_ARG, "handle is NULL");
+  if (x == nullptr || y_partial == nullptr || cu_seqlens == nullptr)
+    return fail(MT_ERR_INVALID_ARG, "x, y_partial and cu_seqlens must not be NULL");
+  if (!aligned16(x) || !aligned16(y_partial) || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u))
+    return fail(MT_ERR_INVALID_ARG, "x/y must be 16-byte and cu_seqlens 4-byte aligned");
+  if (total_tokens <= 0 || num_seqs <= 0 || max_seqlen <= 0 || max_seqlen > total_tokens)
+    return fail(MT_ERR_INVALID_ARG, "need total_tokens > 0, num_seqs > 0, 0 < max_seqlen <= total_tokens");
+  if (static_cast<long long>(total_tokens) + 8LL * num_seqs > (1LL << 30)) return fail(MT_ERR_UNSUPPORTED, "too many tokens");
+  const Layout lay = layout_packed(L, total_tokens, num_seqs, max_seqlen);
+  if (L->ws == nullptr || L->ws_bytes < lay.total)
+    return fail(MT_ERR_NO_WORKSPACE, "workspace missing or smaller than the %zu bytes this call needs", lay.total);
+  int rc = check_weights(L, w, true, true);
+  if (rc) return rc;
+  const Packed pk{cu_seqlens, num_seqs, max_seqlen};
+  rc = forward_device(L, lay, x, total_tokens, 1, w, y_partial, static_cast<cudaStream_t>(cuda_stream), &pk);
+  return rc ? rc : ok();
+}
+
 int mt_layer_forward_host(mt_layer* L, const void* x_host, int seq, int batch, const mt_weights* w, void* y_host,
                           void* cuda_stream) {
   if (L == nullptr) return fail(MT_ERR_INVALID_ARG, "handle is NULL");
@@ -589,6 +653,11 @@ int mt_layer_status(mt_layer* L) {
   int code = 0;
   e = cudaMemcpy(&code, L->d_err, sizeof(int), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  if (code == MT_ERR_INVALID_ARG) {
+    cudaMemset(L->d_err, 0, sizeof(int));
+    return fail(MT_ERR_INVALID_ARG, "cu_seqlens were found inconsistent on the device (not 0 .. total_tokens, "
+                                    "decreasing, or a sample longer than max_seqlen); outputs are invalid");
+  }
   if (code != 0) {
     cudaMemset(L->d_err, 0, sizeof(int));
     return fail(MT_ERR_DEVICE_TIMEOUT, "a kernel stopped waiting on a barrier (device code %d); outputs are invalid",
@@ -648,6 +717,43 @@ int mt_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, voi
   p.ldo = N;
   int rc = run_gemm(nullptr, 0, mt::kEpiStore, A, K, B, N, M, N, K, p, static_cast<cudaStream_t>(cuda_stream));
   return rc ? rc : ok();
+}
+
+int mt_sp_reduce_add_norm(const void* const* partials, int num_partials, const void* resid, const void* bias,
+                          const void* norm_w, const void* norm_b, int norm, float eps, int tokens, int hidden, int row0,
+                          int rows, void* h_out, void* hn_out, void* cuda_stream) {
+  if (partials == nullptr || resid == nullptr || norm_w == nullptr || h_out == nullptr || hn_out == nullptr)
+    return fail(MT_ERR_INVALID_ARG, "NULL argument");
+  if (num_partials < 1 || num_partials > mt::kMaxSpParts)
+    return fail(MT_ERR_UNSUPPORTED, "num_partials must be in [1, %d]", mt::kMaxSpParts);
+  if (norm != MT_NORM_RMS && norm != MT_NORM_LAYER) return fail(MT_ERR_INVALID_ARG, "unknown norm %d", norm);
+  if (norm == MT_NORM_LAYER && norm_b == nullptr) return fail(MT_ERR_INVALID_ARG, "LayerNorm needs norm_b");
+  if (!(eps > 0.f) || std::isinf(eps)) return fail(MT_ERR_INVALID_ARG, "eps must be positive and finite");
+  if (tokens <= 0 || hidden <= 0 || rows < 0 || row0 < 0 || row0 + rows > tokens)
+    return fail(MT_ERR_INVALID_ARG, "rows [%d, %d) outside [0, %d)", row0, row0 + rows, tokens);
+  if (hidden % 8 || hidden > 8192) return fail(MT_ERR_UNSUPPORTED, "hidden must be a multiple of 8 and <= 8192");
+  mt::SpParams p{};
+  for (int i = 0; i < num_partials; ++i) {
+    if (partials[i] == nullptr || !aligned16(partials[i])) return fail(MT_ERR_INVALID_ARG, "partial %d is NULL or misaligned", i);
+    p.parts[i] = static_cast<const bf16*>(partials[i]);
+  }
+  const void* ptrs[] = {resid, bias, norm_w, norm_b, h_out, hn_out};
+  for (const void* q : ptrs)
+    if (q != nullptr && !aligned16(q)) return fail(MT_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  p.nparts = num_partials;
+  p.row0 = static_cast<size_t>(row0);
+  p.rows = rows;
+  p.H = hidden;
+  p.resid = static_cast<const bf16*>(resid);
+  p.bias = static_cast<const bf16*>(bias);
+  p.gamma = static_cast<const bf16*>(norm_w);
+  p.beta = static_cast<const bf16*>(norm_b);
+  p.eps = eps;
+  p.h = static_cast<bf16*>(h_out);
+  p.hn = static_cast<bf16*>(hn_out);
+  cudaError_t e = mt::launch_sp_add_norm(norm == MT_NORM_LAYER, p, static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess) return cuda_fail(e, "sequence-parallel epilogue launch");
+  return ok();
 }
 
 int mt_selftest_bounded_wait(int limit_us) {

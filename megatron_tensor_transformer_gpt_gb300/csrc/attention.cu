@@ -28,6 +28,45 @@ namespace {
 
 constexpr int BQ = 128, BKV = 128;
 
+// What one CTA works on: query block qb of a sequence whose rows start at q_row0 - qb*128 and
+// whose keys start at kv_row0 (rows of the [b, head, s, d] q/k buffers), v^T columns at v_col0,
+// `len` tokens long; batch row b, head (or first head of the pair) h.
+struct Work {
+  int qb, b, h, q_row0, kv_row0, v_col0, len;
+};
+
+// Dense batches: blockIdx -> (query block, longest first; batch row; head slot).  Packed samples:
+// (query block, longest first; sample; head slot); returns false when the block lies past the end
+// of its sample (or the sample's bounds are invalid) so the CTA has nothing to do.
+__device__ __forceinline__ bool decode_work(const AttnParams& p, int heads_slots, int head_step, Work& w) {
+  const int bid = static_cast<int>(blockIdx.x);
+  if (p.cu == nullptr) {
+    const int per = p.batch * heads_slots;
+    w.qb = p.num_qb - 1 - bid / per;
+    const int rem = bid % per;
+    w.b = rem / heads_slots;
+    w.h = head_step * (rem - w.b * heads_slots);
+    w.q_row0 = w.qb * BQ;
+    w.kv_row0 = 0;
+    w.v_col0 = 0;
+    w.len = p.seq;
+    return true;
+  }
+  const int per = p.num_seqs * heads_slots;
+  w.qb = p.num_qb - 1 - bid / per;
+  const int rem = bid % per;
+  const int sid = rem / heads_slots;
+  w.b = 0;
+  w.h = head_step * (rem - sid * heads_slots);
+  const int start = p.cu[sid];
+  w.len = p.cu[sid + 1] - start;
+  if (start < 0 || w.len <= w.qb * BQ || start + w.len > p.seq) return false;
+  w.q_row0 = start + w.qb * BQ;
+  w.kv_row0 = start;
+  w.v_col0 = 8 * ((start + 7) / 8) + 8 * sid;
+  return true;
+}
+
 template <int D>
 struct Geo {
   static constexpr int ATOM = 128 * 128;          // one [128 rows x 64 bf16] swizzle block, 16 KB
@@ -73,10 +112,9 @@ __global__ void __launch_bounds__(192, 1)
   auto sKa = [&](int st) { return smem_u32(base + G::OFF_K + st * G::K_BYTES); };
   auto sVa = [&](int st) { return smem_u32(base + G::OFF_V + st * G::V_BYTES); };
 
-  const int bh_count = p.batch * p.nh;
-  const int qb = p.num_qb - 1 - static_cast<int>(blockIdx.x) / bh_count;  // longest first
-  const int bh = static_cast<int>(blockIdx.x) % bh_count;
-  const int b = bh / p.nh, h = bh - b * p.nh;
+  Work wk;
+  if (!decode_work(p, p.nh, 1, wk)) return;  // uniform over the CTA, before any barrier or TMEM use
+  const int qb = wk.qb, b = wk.b, h = wk.h;
   const int g = h / (p.nh / p.ng);
   const int nkv = qb + 1;  // causal: key blocks 0..qb
 
@@ -114,7 +152,7 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) {
       mbar_arrive_expect_tx(q_full, G::Q_BYTES);
 #pragma unroll
-      for (int a = 0; a < D / 64; ++a) tma_load_3d(sQa + a * G::ATOM, &tmQ, q_full, a * 64, qb * BQ, b * p.nh + h);
+      for (int a = 0; a < D / 64; ++a) tma_load_3d(sQa + a * G::ATOM, &tmQ, q_full, a * 64, wk.q_row0, b * p.nh + h);
       int issued = 0;
       bool ok = true;
       for (int j = 0; j < nkv; ++j) {
@@ -126,10 +164,10 @@ __global__ void __launch_bounds__(192, 1)
         mbar_arrive_expect_tx(kv_full(st), G::K_BYTES + G::V_BYTES);
 #pragma unroll
         for (int a = 0; a < D / 64; ++a)
-          tma_load_3d(sKa(st) + a * G::ATOM, &tmK, kv_full(st), a * 64, j * BKV, b * p.ng + g);
+          tma_load_3d(sKa(st) + a * G::ATOM, &tmK, kv_full(st), a * 64, wk.kv_row0 + j * BKV, b * p.ng + g);
 #pragma unroll
         for (int a = 0; a < 2; ++a)
-          tma_load_3d(sVa(st) + a * G::V_ATOM, &tmV, kv_full(st), j * BKV + a * 64, 0, b * p.ng + g);
+          tma_load_3d(sVa(st) + a * G::V_ATOM, &tmV, kv_full(st), wk.v_col0 + j * BKV + a * 64, 0, b * p.ng + g);
         ++issued;
       }
       if (!ok) {  // let this CTA's own copies in flight land
@@ -182,7 +220,7 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     const int quad = warp & 3;
     const int r = quad * 32 + lane;  // query row within the block
-    const int sq = qb * BQ + r;      // its sequence position
+    const bool row_ok = qb * BQ + r < wk.len;  // inside its sequence
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float c = p.scale_log2;
     float m_used = -INFINITY, l = 0.f;
@@ -257,12 +295,12 @@ __global__ void __launch_bounds__(192, 1)
       if (__all_sync(0xffffffffu, w)) {
         tc_fence_after();
         const float inv_l = 1.f / l;
-        bf16* orow = p.o + (static_cast<size_t>(sq) * p.batch + b) * p.ldo + h * D;
+        bf16* orow = p.o + (static_cast<size_t>(wk.q_row0 + r) * p.batch + b) * p.ldo + h * D;
 #pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {
           float o[32];
           tmem_ld32(tO + lane_off + cc * 32, o);
-          if (sq < p.seq) {
+          if (row_ok) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] *= inv_l;
 #pragma unroll
@@ -334,11 +372,9 @@ __global__ void __launch_bounds__(320, 1)
   auto sKa = [&](int st) { return smem_u32(base + G::OFF_K + st * G::K_BYTES); };
   auto sVa = [&](int st) { return smem_u32(base + G::OFF_V + st * G::V_BYTES); };
 
-  const int pairs = p.nh >> 1;
-  const int bp_count = p.batch * pairs;
-  const int qb = p.num_qb - 1 - static_cast<int>(blockIdx.x) / bp_count;  // longest first
-  const int bp = static_cast<int>(blockIdx.x) % bp_count;
-  const int b = bp / pairs, h0 = 2 * (bp - b * pairs);
+  Work wk;
+  if (!decode_work(p, p.nh >> 1, 2, wk)) return;  // uniform over the CTA, before any barrier or TMEM use
+  const int qb = wk.qb, b = wk.b, h0 = wk.h;
   const int g = h0 / (p.nh / p.ng);
   const int nkv = qb + 1;
 
@@ -381,7 +417,7 @@ __global__ void __launch_bounds__(320, 1)
       for (int t = 0; t < 2; ++t)
 #pragma unroll
         for (int a = 0; a < D / 64; ++a)
-          tma_load_3d(sQa(t) + a * G::ATOM, &tmQ, q_full, a * 64, qb * BQ, b * p.nh + h0 + t);
+          tma_load_3d(sQa(t) + a * G::ATOM, &tmQ, q_full, a * 64, wk.q_row0, b * p.nh + h0 + t);
       int issued_k = 0, issued_v = 0;
       bool ok = true;
       for (int j = 0; ok && j < nkv; ++j) {
@@ -394,7 +430,7 @@ __global__ void __launch_bounds__(320, 1)
         mbar_arrive_expect_tx(k_full(st), G::K_BYTES);
 #pragma unroll
         for (int a = 0; a < D / 64; ++a)
-          tma_load_3d(sKa(st) + a * G::ATOM, &tmK, k_full(st), a * 64, j * BKV, b * p.ng + g);
+          tma_load_3d(sKa(st) + a * G::ATOM, &tmK, k_full(st), a * 64, wk.kv_row0 + j * BKV, b * p.ng + g);
         ++issued_k;
         if (!mbar_wait(v_empty(st), ph ^ 1u, p.err, abort_flag)) {
           ok = false;
@@ -403,7 +439,7 @@ __global__ void __launch_bounds__(320, 1)
         mbar_arrive_expect_tx(v_full(st), G::V_BYTES);
 #pragma unroll
         for (int a = 0; a < 2; ++a)
-          tma_load_3d(sVa(st) + a * G::V_ATOM, &tmV, v_full(st), j * BKV + a * 64, 0, b * p.ng + g);
+          tma_load_3d(sVa(st) + a * G::V_ATOM, &tmV, v_full(st), wk.v_col0 + j * BKV + a * 64, 0, b * p.ng + g);
         ++issued_v;
       }
       if (!ok) {  // let this CTA's own copies in flight land
@@ -478,7 +514,7 @@ __global__ void __launch_bounds__(320, 1)
     const int t = (warp - 2) >> 2;  // which head of the pair
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
-    const int sq = qb * BQ + r;
+    const bool row_ok = qb * BQ + r < wk.len;  // inside its sequence
     const int h = h0 + t;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float c = p.scale_log2;
@@ -547,12 +583,12 @@ __global__ void __launch_bounds__(320, 1)
       if (__all_sync(0xffffffffu, w)) {
         tc_fence_after();
         const float inv_l = 1.f / l;
-        bf16* orow = p.o + (static_cast<size_t>(sq) * p.batch + b) * p.ldo + h * D;
+        bf16* orow = p.o + (static_cast<size_t>(wk.q_row0 + r) * p.batch + b) * p.ldo + h * D;
 #pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {
           float o[32];
           tmem_ld32(tO(t) + lane_off + cc * 32, o);
-          if (sq < p.seq) {
+          if (row_ok) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] *= inv_l;
 #pragma unroll
@@ -581,7 +617,7 @@ cudaError_t launch_d2(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUte
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const unsigned grid = static_cast<unsigned>(p.num_qb) * p.batch * (p.nh / 2);
+  const unsigned grid = static_cast<unsigned>(p.num_qb) * (p.cu ? p.num_seqs : p.batch) * (p.nh / 2);
   attn2_kernel<D><<<grid, 320, Geo2<D>::SMEM, stream>>>(tmQ, tmK, tmV, p);
   return cudaGetLastError();
 }
@@ -596,7 +632,7 @@ cudaError_t launch_d(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUten
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const unsigned grid = static_cast<unsigned>(p.num_qb) * p.batch * p.nh;
+  const unsigned grid = static_cast<unsigned>(p.num_qb) * (p.cu ? p.num_seqs : p.batch) * p.nh;
   attn_kernel<D><<<grid, 192, Geo<D>::SMEM, stream>>>(tmQ, tmK, tmV, p);
   return cudaGetLastError();
 }

@@ -142,8 +142,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
     }
   } else {  // kEpiQkv: `width` is a multiple of head_dim, so every head lies inside one unit
     const int d = p.head_dim, half = d >> 1;
-    const int s = valid ? row / p.batch : 0;
+    const int s = valid ? row / p.batch : 0;  // row of the [b, head, s, d] buffers
     const int b = valid ? row - s * p.batch : 0;
+    const int rpos = (valid && p.pos != nullptr) ? p.pos[row] : s;    // RoPE position
+    const int vc = (valid && p.vcol != nullptr) ? p.vcol[row] : s;    // column of v^T
 #pragma unroll 1
     for (int hc = 0; hc < width; hc += d) {
       const int col = c0 + hc;
@@ -158,7 +160,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
         dst = p.k + ((static_cast<size_t>(b) * p.ng + gg) * p.seq + s) * d;
       } else {
         const int gg = (col - p.q_w - p.kv_w) / d;
-        dst = p.vt + (static_cast<size_t>(b) * p.ng + gg) * d * p.seq_pad + s;
+        dst = p.vt + (static_cast<size_t>(b) * p.ng + gg) * d * p.seq_pad + vc;
         is_v = true;
       }
       if (!is_v && p.rope != nullptr) {
@@ -173,7 +175,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
               add_vec32(x1, p.bias, col + i0, p.N);
               add_vec32(x2, p.bias, col + half + i0, p.N);
             }
-            const float4* cs = reinterpret_cast<const float4*>(p.rope + static_cast<size_t>(s) * half + i0);
+            const float4* cs = reinterpret_cast<const float4*>(p.rope + static_cast<size_t>(rpos) * half + i0);
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
               const float4 t = cs[e];  // (cos, sin) of elements 2e and 2e+1

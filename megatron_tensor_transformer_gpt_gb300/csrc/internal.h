@@ -37,18 +37,39 @@ struct GemmParams {
   int ldr;
   // kEpiQkv only
   bf16 *q, *k, *vt;
-  const float2* rope;  // [seq, d/2] (cos, sin) or null
+  const float2* rope;  // [positions, d/2] (cos, sin) or null
   int seq, batch, head_dim, q_w, kv_w, nh, ng, seq_pad;
+  // packed samples (batch 1): per-token RoPE position and column of v^T; null for dense batches
+  const int* pos;
+  const int* vcol;
   int* err;
 };
 
 struct AttnParams {
   int seq, batch, nh, ng;  // this rank's query heads and kv groups
-  int num_qb;              // ceil(seq / 128)
+  int num_qb;              // ceil(seq / 128); packed samples: ceil(max_seqlen / 128)
+  // Packed samples (batch 1, seq = all tokens): sample i is tokens [cu[i], cu[i+1]); its v^T
+  // columns start at 8*ceil(cu[i]/8) + 8*i.  null for dense batches.
+  const int* cu;
+  int num_seqs;
   float scale_log2;        // log2(e) / sqrt(head_dim)
   bf16* o;                 // [seq*batch, ldo], head h at columns h*head_dim
   int ldo;
   int* err;
+};
+
+// Sequence-parallel epilogue (see mt_sp_reduce_add_norm).
+constexpr int kMaxSpParts = 16;
+struct SpParams {
+  const bf16* parts[kMaxSpParts];  // full [T, H] row-parallel partials
+  int nparts;
+  size_t row0;                     // first row of the slice inside the partials
+  int rows, H;
+  const bf16* resid;               // [rows, H]
+  const bf16* bias;                // [H] or null
+  const bf16 *gamma, *beta;        // [H]; beta only for LayerNorm
+  float eps;
+  bf16 *h, *hn;                    // [rows, H]
 };
 
 // Number of SMs of the current device (cached).
@@ -66,6 +87,13 @@ cudaError_t launch_norm(bool layer_norm, const bf16* x, const bf16* g, const bf1
                         float eps, cudaStream_t stream);
 
 cudaError_t launch_rope_table(float2* table, const double* theta, int seq, int half, cudaStream_t stream);
+
+cudaError_t launch_sp_add_norm(bool layer_norm, const SpParams& p, cudaStream_t stream);
+
+// Per-token RoPE position and v^T column of packed samples; invalid cu_seqlens record
+// MT_ERR_INVALID_ARG in *err and give in-range indices.
+cudaError_t launch_packed_index(const int* cu, int num_seqs, int tokens, int max_seqlen, int vcols, int* pos, int* vcol,
+                                int* err, cudaStream_t stream);
 
 cudaError_t launch_wait_selftest(int* err, unsigned long long limit_ns, cudaStream_t stream);
 

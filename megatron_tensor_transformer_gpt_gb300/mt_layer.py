@@ -64,6 +64,15 @@ _SIGS = {
     "mt_layer_profile_enable": ([ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
     "mt_layer_profile_read": ([ctypes.c_void_p, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_double)],
                               ctypes.c_int),
+    "mt_layer_workspace_bytes_packed": ([ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
+    "mt_layer_forward_packed": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                                 ctypes.c_int, ctypes.POINTER(MtWeights), ctypes.c_void_p, ctypes.c_void_p],
+                                ctypes.c_int),
+    "mt_sp_reduce_add_norm": ([ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_int,
+                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                               ctypes.c_void_p], ctypes.c_int),
     "mt_layer_forward_static": ([ctypes.c_int] * 7 + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_float,
                                                       ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                                       ctypes.POINTER(MtWeights), ctypes.c_void_p, ctypes.c_void_p],
@@ -135,6 +144,18 @@ def mt_layer_forward_host(handle, x_host, seq, batch, weights: MtWeights, y_host
     _check(lib().mt_layer_forward_host(handle, x_host, seq, batch, ctypes.byref(weights), y_host, stream))
 
 
+def mt_layer_workspace_bytes_packed(handle, total_tokens, num_seqs, max_seqlen) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().mt_layer_workspace_bytes_packed(handle, total_tokens, num_seqs, max_seqlen, ctypes.byref(n)))
+    return n.value
+
+
+def mt_layer_forward_packed(handle, x, total_tokens, cu_seqlens_dev, num_seqs, max_seqlen, weights: MtWeights,
+                            y_partial, stream):
+    _check(lib().mt_layer_forward_packed(handle, x, total_tokens, cu_seqlens_dev, num_seqs, max_seqlen,
+                                         ctypes.byref(weights), y_partial, stream))
+
+
 def mt_layer_workspace_region(handle, seq, batch, which):
     off, n = ctypes.c_size_t(), ctypes.c_size_t()
     _check(lib().mt_layer_workspace_region(handle, seq, batch, which, ctypes.byref(off), ctypes.byref(n)))
@@ -167,6 +188,14 @@ def mt_layer_forward_static(hidden, heads, query_groups, head_dim, ffn, norm, ac
     _check(lib().mt_layer_forward_static(hidden, heads, query_groups, head_dim, ffn, norm, act, float(rope_base),
                                          tp_size, tp_rank, float(eps), x, seq, batch, ctypes.byref(weights),
                                          y_partial, stream))
+
+
+def mt_sp_reduce_add_norm(partials, resid, bias, norm_w, norm_b, norm, eps, tokens, hidden, row0, rows, h_out,
+                          hn_out, stream):
+    """Sequence-parallel epilogue for one rank's slice; `partials` is a list of device pointers."""
+    arr = (ctypes.c_void_p * len(partials))(*partials)
+    _check(lib().mt_sp_reduce_add_norm(arr, len(partials), resid, bias, norm_w, norm_b, norm, float(eps), tokens,
+                                       hidden, row0, rows, h_out, hn_out, stream))
 
 
 def mt_gemm_bf16(A, B, C, M, N, K, stream):
@@ -238,6 +267,18 @@ class Layer:
     def forward_mlp(self, h, seq, batch, weights: MtWeights, out, stream=None):
         self.workspace(seq, batch, h.device)
         mt_layer_forward_mlp(self.handle, h.data_ptr(), seq, batch, weights, out.data_ptr(), self._stream(stream))
+        return out
+
+    def forward_packed(self, x, cu_seqlens, max_seqlen, weights: MtWeights, out, stream=None):
+        """x, out: [total_tokens, H]; cu_seqlens: int32 device tensor of num_seqs + 1 boundaries."""
+        import torch
+        total, n = x.shape[0], cu_seqlens.numel() - 1
+        need = mt_layer_workspace_bytes_packed(self.handle, total, n, max_seqlen)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(need, dtype=torch.uint8, device=x.device)
+            mt_layer_set_workspace(self.handle, self._ws.data_ptr(), self._ws.numel())
+        mt_layer_forward_packed(self.handle, x.data_ptr(), total, cu_seqlens.data_ptr(), n, max_seqlen, weights,
+                                out.data_ptr(), self._stream(stream))
         return out
 
     def forward_host(self, x_host, seq, batch, weights: MtWeights, y_host, stream=None):

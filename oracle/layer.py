@@ -43,7 +43,7 @@ __all__ = [
     "bf16_to_f64", "rms_norm", "layer_norm", "apply_norm", "linear", "rope_cos_sin", "rope",
     "causal_softmax", "causal_attention", "silu", "gelu_tanh", "activation",
     "attn_partial", "mlp_partial", "layer_forward", "layer_forward_rank_identity",
-    "layer_forward_tp_sum", "split_heads",
+    "layer_forward_tp_sum", "split_heads", "packed_segments",
 ]
 
 
@@ -176,16 +176,34 @@ def _w(wd: Dict, name: str):
     return bf16_to_f64(a) if a.dtype == np.uint16 else np.asarray(a, dtype=np.float64)
 
 
-def attn_partial(cfg, tp: int, x: np.ndarray, wd: Dict, rows: Optional[np.ndarray] = None) -> np.ndarray:
+def packed_segments(cu_seqlens, T: int):
+    """Segment id and in-segment position of each of T packed tokens; sample i holds tokens
+    [cu[i], cu[i+1]) ("快速入门" §4.1 / §8: cu_seqlens are the cumulative sample lengths)."""
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    assert cu[0] == 0 and cu[-1] == T and np.all(np.diff(cu) >= 0)
+    seg = np.searchsorted(cu, np.arange(T), side="right") - 1
+    return seg, np.arange(T) - cu[seg]
+
+
+def attn_partial(cfg, tp: int, x: np.ndarray, wd: Dict, rows: Optional[np.ndarray] = None,
+                 cu_seqlens=None) -> np.ndarray:
     """One rank's pre-reduce attention output Y_attn,i = o_i W_o,i^T for token rows `rows` (all if None).
 
     x: layer input, [T, H] float64 (token t = s*batch + b).  wd: that rank's weights.
     K and V are computed for every token (causality needs all earlier keys);
     queries, attention and the output projection only for the requested rows.
+    cu_seqlens (batch 1 only): packed samples; a query sees only the earlier keys of its own
+    sample, and RoPE positions restart at 0 in every sample (the reading that makes a packed
+    sample compute what it would alone).
     """
     T, B, d = cfg.tokens, cfg.batch, cfg.head_dim
     hr, gr, _ = split_heads(cfg, tp)
     rows = np.arange(T) if rows is None else np.asarray(rows)
+    if cu_seqlens is not None:
+        assert B == 1
+        seg, pos = packed_segments(cu_seqlens, T)
+    else:
+        seg, pos = np.zeros(T, dtype=np.int64), np.arange(T) // B
     xn = apply_norm(cfg, x, _w(wd, "norm1_w"), _w(wd, "norm1_b"))
     w_qkv, b_qkv = _w(wd, "w_qkv"), _w(wd, "b_qkv")
     qw, kw = hr * d, gr * d
@@ -196,16 +214,25 @@ def attn_partial(cfg, tp: int, x: np.ndarray, wd: Dict, rows: Optional[np.ndarra
     k = linear(xn, w_qkv[qw:qw + kw], bk).reshape(T, gr, d)
     v = linear(xn, w_qkv[qw + kw:qw + 2 * kw], bv).reshape(T, gr, d)
     if cfg.rope_base > 0:
-        cq, sq = rope_cos_sin(rows // B, d, cfg.rope_base)
-        ck, sk = rope_cos_sin(np.arange(T) // B, d, cfg.rope_base)
+        cq, sq = rope_cos_sin(pos[rows], d, cfg.rope_base)
+        ck, sk = rope_cos_sin(pos, d, cfg.rope_base)
         q, k = rope(q, cq, sq), rope(k, ck, sk)
     o = np.empty((len(rows), hr, d))
-    for b in range(B):
-        sel = np.nonzero(rows % B == b)[0]
-        if len(sel) == 0:
-            continue
-        kb, vb = k[b::B], v[b::B]                  # [S, gr, d] of batch row b
-        o[sel] = causal_attention(q[sel], kb, vb, rows[sel] // B)
+    if cu_seqlens is not None:
+        cu = np.asarray(cu_seqlens)
+        for i in range(len(cu) - 1):
+            sel = np.nonzero(seg[rows] == i)[0]
+            if len(sel) == 0:
+                continue
+            lo, hi = cu[i], cu[i + 1]                # keys of sample i, at positions 0..len-1
+            o[sel] = causal_attention(q[sel], k[lo:hi], v[lo:hi], pos[rows[sel]])
+    else:
+        for b in range(B):
+            sel = np.nonzero(rows % B == b)[0]
+            if len(sel) == 0:
+                continue
+            kb, vb = k[b::B], v[b::B]                  # [S, gr, d] of batch row b
+            o[sel] = causal_attention(q[sel], kb, vb, rows[sel] // B)
     return linear(o.reshape(len(rows), hr * d), _w(wd, "w_o"))
 
 
@@ -220,13 +247,14 @@ def _add_bias(y, b):
     return y if b is None else y + b
 
 
-def layer_forward(cfg, inp: Dict, rows: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+def layer_forward(cfg, inp: Dict, rows: Optional[np.ndarray] = None, cu_seqlens=None) -> Dict[str, np.ndarray]:
     """Whole layer at TP=1: h = x + Y_attn + b_o; y = h + Y_mlp + b_fc2 (pre-norm order, bias-dropout-add).
 
-    Returns {"h", "y"} for the token rows `rows` (all tokens if None)."""
+    Returns {"h", "y"} for the token rows `rows` (all tokens if None); cu_seqlens: packed samples
+    (see attn_partial)."""
     x = _tokens(inp["x"], cfg)
     rows = np.arange(cfg.tokens) if rows is None else np.asarray(rows)
-    h = x[rows] + attn_partial(cfg, 1, x, inp, rows)
+    h = x[rows] + attn_partial(cfg, 1, x, inp, rows, cu_seqlens)
     h = _add_bias(h, _w(inp, "b_o"))
     y = _add_bias(h + mlp_partial(cfg, 1, h, inp), _w(inp, "b_fc2"))
     return {"h": h, "y": y}

@@ -312,3 +312,26 @@ def test_planted_oracle_mistakes_are_caught(monkeypatch, mutation):
     elif mutation == "rms_no_eps_sqrt":
         monkeypatch.setattr(ol, "rms_norm", lambda x, g, eps: x / (np.sqrt(np.mean(x * x, -1, keepdims=True)) + eps) * g * 1.01)
     assert _restatement_mismatch(cfg, inp) > 1e-4
+
+
+# --------------------------------------------------------------------------- packed samples
+@pytest.mark.parametrize("lens", [[24], [5, 19], [1, 7, 3, 13], [9, 0, 15]])
+def test_packed_layer_equals_each_sample_alone(lens):
+    """A packed sample must compute exactly what the dense layer computes on it alone."""
+    T = sum(lens)
+    cfg = small_cfg(batch=1, seq=T, groups=2)
+    inp = synth.make_inputs(cfg, seed=13, affine="random")
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    packed = ol.layer_forward(cfg, inp, cu_seqlens=cu)["y"]
+    x = inp["x"].reshape(T, cfg.hidden)
+    for i, n in enumerate(lens):
+        if n == 0:
+            continue
+        ci = cfg.replace(seq=n)
+        alone = dict(inp, x=x[cu[i]:cu[i + 1]].reshape(n, 1, cfg.hidden))
+        np.testing.assert_allclose(packed[cu[i]:cu[i + 1]], ol.layer_forward(ci, alone)["y"], rtol=1e-12, atol=1e-12)
+
+
+def test_packed_segments_of_boundaries():
+    seg, pos = ol.packed_segments([0, 3, 3, 5], 5)
+    assert seg.tolist() == [0, 0, 0, 2, 2] and pos.tolist() == [0, 1, 2, 0, 1]
