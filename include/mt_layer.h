@@ -130,6 +130,50 @@ int mt_layer_workspace_bytes_packed(const mt_layer* L, int total_tokens, int num
 int mt_layer_forward_packed(mt_layer* L, const void* x, int total_tokens, const int* cu_seqlens, int num_seqs,
                             int max_seqlen, const mt_weights* w, void* y_partial, void* cuda_stream);
 
+/* ---- FP8 (E4M3) forward path -----------------------------------------------------------
+ * The FP8 recipe of "ai阅读megatron" (--fp8-hybrid: E4M3 in the forward pass) and "快速入门"
+ * §8.2 (dynamic scaling that tracks each tensor's amax over a history, amax_compute_algo max):
+ * the four GEMMs take E4M3 operands.  A tensor with scale s is stored as codes of x * s (round to
+ * nearest even, saturating to +-448) and the fp32 accumulator is multiplied by the two operands'
+ * 1/s.  Weights use current scaling (s = 448 / amax, mt_quantize_e4m3).  The four activations that
+ * feed the GEMMs -- normed x, the attention output, normed h, the MLP hidden -- use delayed
+ * scaling: a forward quantises with the scales in the handle, records each activation's amax in
+ * an amax history, and sets the next scales to 448 / max(history).  q/k/v, the attention, h and
+ * y stay bf16. */
+typedef struct {
+  const void *w_qkv, *w_o, *w_fc1, *w_fc2;           /* E4M3 codes, shapes as in mt_weights       */
+  const float *deq_qkv, *deq_o, *deq_fc1, *deq_fc2;  /* device: each weight's 1/scale             */
+} mt_fp8_weights;
+
+/* Allocate the handle's delayed-scaling state (host call): activation scales 1, an amax history
+ * of amax_history_len entries per activation (1..65536; the pages' recipe uses 1024), zeroed. */
+int mt_layer_fp8_enable(mt_layer* L, int amax_history_len);
+
+/* Set the four activation scales (host array: normed x, attention output, normed h, MLP hidden;
+ * positive, finite) and clear the history.  Synchronises the device. */
+int mt_layer_fp8_set_scales(mt_layer* L, const float* scales);
+
+/* Read the current activation scales and the amax each activation recorded in the last FP8
+ * forward (host arrays of 4).  Synchronises the device. */
+int mt_layer_fp8_state(mt_layer* L, float* scales, float* last_amax);
+
+/* Whole layer with the four GEMMs on E4M3 (needs mt_layer_fp8_enable; hidden and ffn/tp_size
+ * multiples of 16).  w supplies the bf16 norm weights and biases (its projection pointers are not
+ * used); w8 the E4M3 projections.  Semantics, layouts and workspace as mt_layer_forward; 9 kernel
+ * launches (the last updates the amax history). */
+int mt_layer_forward_fp8(mt_layer* L, const void* x, int seq, int batch, const mt_weights* w,
+                         const mt_fp8_weights* w8, void* y_partial, void* cuda_stream);
+
+/* Current per-tensor scaling of n bf16 values (n a multiple of 8): amax_deq[0] <- max |x| (as
+ * float), amax_deq[1] <- 1/s with s = 448 / amax (s = 1 for an all-zero tensor), dst <- E4M3
+ * codes of x * s.  src, dst, amax_deq: device (16/16/8-byte aligned).  Two launches. */
+int mt_quantize_e4m3(const void* src, size_t n, void* dst, float* amax_deq, void* cuda_stream);
+
+/* C[M, N] = (A[M, K] * B[N, K]^T) * (*deq_a) * (*deq_b) with E4M3 A and B, fp32 accumulation,
+ * bf16 C (the FP8 layer's GEMM).  Device pointers; K % 16 == 0, N % 8 == 0. */
+int mt_gemm_e4m3(const void* A, const void* B, void* C, int M, int N, int K, const float* deq_a, const float* deq_b,
+                 void* cuda_stream);
+
 /* mt_layer_forward with x and y in HOST memory (pinned for asynchronous copies): copies x
  * into the workspace, runs the layer, copies y back, all on `cuda_stream`; the host buffers
  * must stay valid until the stream reaches this point. */

@@ -25,6 +25,10 @@ struct mt_layer {
   double* d_theta;  // [head_dim/2] RoPE frequencies base^(-2i/d), or null
   void* ws;
   size_t ws_bytes;
+  // FP8 delayed scaling (mt_layer_fp8_*): device state scale[4] | deq[4] | amax bits[4] | pad[4] |
+  // history[4][f8_len] for the activations (normed x, attention output, normed h, MLP hidden)
+  float* d_f8;
+  int f8_len, f8_pos;
   // per-kernel timing (mt_layer_profile_*)
   bool profiling;
   struct Rec {
@@ -190,6 +194,22 @@ int map_2d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint64
   return MT_OK;
 }
 
+// Row-major E4M3 (byte) matrix [rows, cols], pitch in bytes; box = 128 columns x box_rows.
+int map_2d_u8(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint64_t pitch, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return fail(MT_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {pitch};
+  const cuuint32_t box[2] = {128, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MT_ERR_CUDA, "cuTensorMapEncodeTiled (e4m3 %llu x %llu) failed: %d",
+                                     (unsigned long long)rows, (unsigned long long)cols, (int)r);
+  return MT_OK;
+}
+
 // bf16 tensor [d2][d1][d0] with element pitches p1 (between d1 rows) and p2 (between d2 slabs);
 // box = 64 x box1 x 1.
 int map_3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t p1, uint64_t p2,
@@ -262,20 +282,22 @@ void plan_gemm(mt::GemmParams& p, int mode, int head_dim) {
 }
 
 // One GEMM: A [M, K] (pitch lda) x W [rows_w, K]^T with the given epilogue.
+// fp8: A and W hold E4M3 codes (lda and the W pitch K in bytes).
 int run_gemm(mt_layer* L, int slot, int mode, const void* A, int lda, const void* W, int rows_w, int M, int N, int K,
-             mt::GemmParams p, cudaStream_t st) {
+             mt::GemmParams p, cudaStream_t st, bool fp8 = false) {
   CUtensorMap ta, tb, tb64;
-  int rc = map_2d(&ta, A, K, M, lda, 128);
+  auto mk = fp8 ? map_2d_u8 : map_2d;
+  int rc = mk(&ta, A, K, M, lda, 128);
   if (rc) return rc;
-  rc = map_2d(&tb, W, K, rows_w, K, 128);
+  rc = mk(&tb, W, K, rows_w, K, 128);
   if (rc) return rc;
-  rc = map_2d(&tb64, W, K, rows_w, K, 64);
+  rc = mk(&tb64, W, K, rows_w, K, 64);
   if (rc) return rc;
   plan_gemm(p, mode, mode == mt::kEpiQkv ? p.head_dim : 0);
   cudaError_t e;
   {
     Timed t(L, slot, st);
-    e = mt::launch_gemm(mode, ta, tb, tb64, p, st);
+    e = mt::launch_gemm(mode, fp8, ta, tb, tb64, p, st);
   }
   if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
   return MT_OK;
@@ -450,6 +472,125 @@ int forward_device(mt_layer* L, const Layout& lay, const void* x, int S, int B, 
   int rc = run_attention_block(L, lay, x, S, B, w, h, mt::kEpiResid, st, pk);
   if (rc) return rc;
   return run_mlp_block(L, lay, h, S, B, w, y, L->tp == 1 ? mt::kEpiResid : mt::kEpiStore, st);
+}
+
+// The layer with its four GEMMs on E4M3 operands (delayed scaling of the activations, weights
+// pre-quantised by the caller).  Same semantics as forward_device otherwise.
+int forward_device_fp8(mt_layer* L, const Layout& lay, const void* x, int S, int B, const mt_weights* w,
+                       const mt_fp8_weights* w8, void* y, cudaStream_t st) {
+  const int T = S * B, H = L->hidden, d = L->head_dim;
+  float* scale = L->d_f8;
+  float* deq = L->d_f8 + 4;
+  unsigned* amax = reinterpret_cast<unsigned*>(L->d_f8 + 8);
+  cudaError_t e;
+  float2* rope = nullptr;
+  if (L->rope_base > 0.f) {
+    rope = region<float2>(L, lay, kRope);
+    Timed t(L, kSlotRope, st);
+    e = mt::launch_rope_table(rope, L->d_theta, S, d / 2, st);
+    if (e != cudaSuccess) return cuda_fail(e, "RoPE table launch");
+  }
+  uint8_t* xn8 = region<uint8_t>(L, lay, kXn);
+  {
+    Timed t(L, kSlotNorm1, st);
+    e = mt::launch_norm(L->norm == MT_NORM_LAYER, static_cast<const bf16*>(x), static_cast<const bf16*>(w->norm1_w),
+                        static_cast<const bf16*>(w->norm1_b), nullptr, T, H, L->eps, st, xn8, scale + 0, amax + 0);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "norm1 launch");
+  bf16 *q = region<bf16>(L, lay, kQ), *k = region<bf16>(L, lay, kK), *vt = region<bf16>(L, lay, kVt);
+  const int nqkv = L->q_w + 2 * L->kv_w;
+  mt::GemmParams p = gemm_params(T, nqkv, H, false, L->d_err);
+  p.bias = static_cast<const bf16*>(w->b_qkv);
+  p.q = q;
+  p.k = k;
+  p.vt = vt;
+  p.rope = rope;
+  p.seq = S;
+  p.batch = B;
+  p.head_dim = d;
+  p.q_w = L->q_w;
+  p.kv_w = L->kv_w;
+  p.nh = L->nh_r;
+  p.ng = L->ng_r;
+  p.seq_pad = lay.seq_pad;
+  p.deq_a = deq + 0;
+  p.deq_b = w8->deq_qkv;
+  int rc = run_gemm(L, kSlotQkv, mt::kEpiQkv, xn8, H, w8->w_qkv, nqkv, T, nqkv, H, p, st, true);
+  if (rc) return rc;
+
+  CUtensorMap tq, tk, tv;
+  if ((rc = map_3d(&tq, q, d, S, static_cast<uint64_t>(B) * L->nh_r, d, static_cast<uint64_t>(S) * d, 128))) return rc;
+  if ((rc = map_3d(&tk, k, d, S, static_cast<uint64_t>(B) * L->ng_r, d, static_cast<uint64_t>(S) * d, 128))) return rc;
+  if ((rc = map_3d(&tv, vt, S, d, static_cast<uint64_t>(B) * L->ng_r, lay.seq_pad,
+                   static_cast<uint64_t>(d) * lay.seq_pad, static_cast<uint32_t>(d))))
+    return rc;
+  uint8_t* o8 = region<uint8_t>(L, lay, kO);
+  mt::AttnParams ap{};
+  ap.seq = S;
+  ap.batch = B;
+  ap.nh = L->nh_r;
+  ap.ng = L->ng_r;
+  ap.num_qb = (S + 127) / 128;
+  ap.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+  ap.ldo = L->q_w;
+  ap.err = L->d_err;
+  ap.o8 = o8;
+  ap.q_scale = scale + 1;
+  ap.amax = amax + 1;
+  {
+    Timed t(L, kSlotAttn, st);
+    e = mt::launch_attention(d, tq, tk, tv, ap, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+
+  bf16* h = region<bf16>(L, lay, kH);
+  p = gemm_params(T, H, L->q_w, false, L->d_err);
+  p.out = h;
+  p.ldo = H;
+  p.bias = static_cast<const bf16*>(w->b_o);
+  p.resid = static_cast<const bf16*>(x);
+  p.ldr = H;
+  p.deq_a = deq + 1;
+  p.deq_b = w8->deq_o;
+  if ((rc = run_gemm(L, kSlotO, mt::kEpiResid, o8, L->q_w, w8->w_o, H, T, H, L->q_w, p, st, true))) return rc;
+
+  uint8_t* hn8 = region<uint8_t>(L, lay, kHn);
+  {
+    Timed t(L, kSlotNorm2, st);
+    e = mt::launch_norm(L->norm == MT_NORM_LAYER, h, static_cast<const bf16*>(w->norm2_w),
+                        static_cast<const bf16*>(w->norm2_b), nullptr, T, H, L->eps, st, hn8, scale + 2, amax + 2);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "norm2 launch");
+  uint8_t* a8 = region<uint8_t>(L, lay, kA);
+  const bool swiglu = L->act == MT_ACT_SWIGLU;
+  p = gemm_params(T, L->f_r, H, swiglu, L->d_err);
+  p.ldo = L->f_r;
+  p.bias = static_cast<const bf16*>(w->b_fc1);
+  p.out8 = a8;
+  p.q_scale = scale + 3;
+  p.amax = amax + 3;
+  p.deq_a = deq + 2;
+  p.deq_b = w8->deq_fc1;
+  if ((rc = run_gemm(L, kSlotFc1, swiglu ? mt::kEpiSwiglu : mt::kEpiGelu, hn8, H, w8->w_fc1, L->f1_r, T, L->f_r, H, p,
+                     st, true)))
+    return rc;
+  p = gemm_params(T, H, L->f_r, false, L->d_err);
+  p.out = static_cast<bf16*>(y);
+  p.ldo = H;
+  if (L->tp == 1) {
+    p.bias = static_cast<const bf16*>(w->b_fc2);
+    p.resid = h;
+    p.ldr = H;
+  }
+  p.deq_a = deq + 3;
+  p.deq_b = w8->deq_fc2;
+  if ((rc = run_gemm(L, kSlotFc2, L->tp == 1 ? mt::kEpiResid : mt::kEpiStore, a8, L->f_r, w8->w_fc2, H, T, H, L->f_r,
+                     p, st, true)))
+    return rc;
+  e = mt::launch_fp8_history(L->d_f8, L->f8_len, L->f8_pos, st);
+  if (e != cudaSuccess) return cuda_fail(e, "amax history update");
+  L->f8_pos = (L->f8_pos + 1) % L->f8_len;
+  return MT_OK;
 }
 
 }  // namespace
@@ -672,6 +813,7 @@ void mt_layer_destroy(mt_layer* L) {
   if (L == nullptr) return;
   if (L->d_err) cudaFree(L->d_err);
   if (L->d_theta) cudaFree(L->d_theta);
+  if (L->d_f8) cudaFree(L->d_f8);
   for (auto& r : L->recs) {
     cudaEventDestroy(r.a);
     cudaEventDestroy(r.b);
@@ -716,6 +858,104 @@ int mt_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, voi
   p.out = static_cast<bf16*>(C);
   p.ldo = N;
   int rc = run_gemm(nullptr, 0, mt::kEpiStore, A, K, B, N, M, N, K, p, static_cast<cudaStream_t>(cuda_stream));
+  return rc ? rc : ok();
+}
+
+int mt_layer_fp8_enable(mt_layer* L, int amax_history_len) {
+  if (L == nullptr) return fail(MT_ERR_INVALID_ARG, "handle is NULL");
+  if (amax_history_len < 1 || amax_history_len > (1 << 16))
+    return fail(MT_ERR_INVALID_ARG, "amax_history_len must be in [1, 65536]");
+  if (L->d_f8) cudaFree(L->d_f8);
+  L->d_f8 = nullptr;
+  const size_t n = 16 + 4 * static_cast<size_t>(amax_history_len);
+  cudaError_t e = cudaMalloc(&L->d_f8, n * sizeof(float));
+  if (e == cudaSuccess) e = cudaMemset(L->d_f8, 0, n * sizeof(float));
+  const float ones[8] = {1, 1, 1, 1, 1, 1, 1, 1};
+  if (e == cudaSuccess) e = cudaMemcpy(L->d_f8, ones, sizeof(ones), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "FP8 scaling state");
+  L->f8_len = amax_history_len;
+  L->f8_pos = 0;
+  return ok();
+}
+
+int mt_layer_fp8_set_scales(mt_layer* L, const float* scales) {
+  if (L == nullptr || scales == nullptr) return fail(MT_ERR_INVALID_ARG, "NULL argument");
+  if (L->d_f8 == nullptr) return fail(MT_ERR_INVALID_ARG, "call mt_layer_fp8_enable first");
+  float head[16] = {0};
+  for (int i = 0; i < 4; ++i) {
+    if (!(scales[i] > 0.f) || std::isinf(scales[i])) return fail(MT_ERR_INVALID_ARG, "scales must be positive and finite");
+    head[i] = scales[i];
+    head[4 + i] = 1.0f / scales[i];
+  }
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemset(L->d_f8, 0, (16 + 4 * static_cast<size_t>(L->f8_len)) * sizeof(float));
+  if (e == cudaSuccess) e = cudaMemcpy(L->d_f8, head, sizeof(head), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "setting FP8 scales");
+  L->f8_pos = 0;
+  return ok();
+}
+
+int mt_layer_fp8_state(mt_layer* L, float* scales, float* last_amax) {
+  if (L == nullptr || scales == nullptr || last_amax == nullptr) return fail(MT_ERR_INVALID_ARG, "NULL argument");
+  if (L->d_f8 == nullptr) return fail(MT_ERR_INVALID_ARG, "call mt_layer_fp8_enable first");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(scales, L->d_f8, 4 * sizeof(float), cudaMemcpyDeviceToHost);
+  const int last = (L->f8_pos + L->f8_len - 1) % L->f8_len;
+  for (int t = 0; t < 4 && e == cudaSuccess; ++t)
+    e = cudaMemcpy(last_amax + t, L->d_f8 + 16 + static_cast<size_t>(t) * L->f8_len + last, sizeof(float),
+                   cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading FP8 state");
+  return ok();
+}
+
+int mt_layer_forward_fp8(mt_layer* L, const void* x, int seq, int batch, const mt_weights* w,
+                         const mt_fp8_weights* w8, void* y_partial, void* cuda_stream) {
+  Layout lay;
+  int rc = check_call(L, x, y_partial, seq, batch, &lay);
+  if (rc) return rc;
+  if (L->d_f8 == nullptr) return fail(MT_ERR_INVALID_ARG, "call mt_layer_fp8_enable first");
+  if (L->hidden % 16 || L->f_r % 16)
+    return fail(MT_ERR_UNSUPPORTED, "the FP8 path needs hidden and ffn/tp_size multiples of 16");
+  if (w8 == nullptr) return fail(MT_ERR_INVALID_ARG, "fp8 weights struct is NULL");
+  const void* wp[] = {w8->w_qkv, w8->w_o, w8->w_fc1, w8->w_fc2};
+  const float* dp[] = {w8->deq_qkv, w8->deq_o, w8->deq_fc1, w8->deq_fc2};
+  for (int i = 0; i < 4; ++i)
+    if (wp[i] == nullptr || !aligned16(wp[i]) || dp[i] == nullptr)
+      return fail(MT_ERR_INVALID_ARG, "fp8 weight %d or its dequantisation factor is NULL/misaligned", i);
+  mt_weights wn = *w;  // norms and biases are bf16; the projections come from w8
+  wn.w_qkv = w8->w_qkv;
+  wn.w_o = w8->w_o;
+  wn.w_fc1 = w8->w_fc1;
+  wn.w_fc2 = w8->w_fc2;
+  if ((rc = check_weights(L, &wn, true, true))) return rc;
+  rc = forward_device_fp8(L, lay, x, seq, batch, w, w8, y_partial, static_cast<cudaStream_t>(cuda_stream));
+  return rc ? rc : ok();
+}
+
+int mt_quantize_e4m3(const void* src, size_t n, void* dst, float* amax_deq, void* cuda_stream) {
+  if (src == nullptr || dst == nullptr || amax_deq == nullptr) return fail(MT_ERR_INVALID_ARG, "NULL argument");
+  if (!aligned16(src) || !aligned16(dst) || (reinterpret_cast<uintptr_t>(amax_deq) & 7u))
+    return fail(MT_ERR_INVALID_ARG, "src/dst must be 16-byte and amax_deq 8-byte aligned");
+  if (n == 0 || n % 8) return fail(MT_ERR_UNSUPPORTED, "n must be a positive multiple of 8");
+  cudaError_t e = mt::launch_quantize_e4m3(static_cast<const bf16*>(src), n, static_cast<uint8_t*>(dst), amax_deq,
+                                           static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess) return cuda_fail(e, "E4M3 quantisation launch");
+  return ok();
+}
+
+int mt_gemm_e4m3(const void* A, const void* B, void* C, int M, int N, int K, const float* deq_a, const float* deq_b,
+                 void* cuda_stream) {
+  if (A == nullptr || B == nullptr || C == nullptr || deq_a == nullptr || deq_b == nullptr)
+    return fail(MT_ERR_INVALID_ARG, "NULL operand");
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return fail(MT_ERR_INVALID_ARG, "operands must be 16-byte aligned");
+  if (M <= 0 || N <= 0 || K <= 0) return fail(MT_ERR_INVALID_ARG, "M, N, K must be positive");
+  if (K % 16 || N % 8) return fail(MT_ERR_UNSUPPORTED, "K must be a multiple of 16 and N of 8");
+  mt::GemmParams p = gemm_params(M, N, K, false, nullptr);
+  p.out = static_cast<bf16*>(C);
+  p.ldo = N;
+  p.deq_a = deq_a;
+  p.deq_b = deq_b;
+  int rc = run_gemm(nullptr, 0, mt::kEpiStore, A, K, B, N, M, N, K, p, static_cast<cudaStream_t>(cuda_stream), true);
   return rc ? rc : ok();
 }
 

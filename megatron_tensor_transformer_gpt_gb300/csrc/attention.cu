@@ -295,7 +295,9 @@ __global__ void __launch_bounds__(192, 1)
       if (__all_sync(0xffffffffu, w)) {
         tc_fence_after();
         const float inv_l = 1.f / l;
-        bf16* orow = p.o + (static_cast<size_t>(wk.q_row0 + r) * p.batch + b) * p.ldo + h * D;
+        const size_t orow = (static_cast<size_t>(wk.q_row0 + r) * p.batch + b) * p.ldo + h * D;
+        const float qs = p.o8 != nullptr ? __ldg(p.q_scale) : 1.f;
+        float mx = 0.f;
 #pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {
           float o[32];
@@ -303,10 +305,22 @@ __global__ void __launch_bounds__(192, 1)
           if (row_ok) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] *= inv_l;
+            if (p.o8 != nullptr) {  // E4M3 output for the FP8 output projection
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-              *reinterpret_cast<uint4*>(orow + cc * 32 + q4 * 8) = pack_bf16x8(o + q4 * 8);
+              for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(o[i]));
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4)
+                *reinterpret_cast<uint2*>(p.o8 + orow + cc * 32 + q4 * 8) = pack_e4m3x8(o + q4 * 8, qs);
+            } else {
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4)
+                *reinterpret_cast<uint4*>(p.o + orow + cc * 32 + q4 * 8) = pack_bf16x8(o + q4 * 8);
+            }
           }
+        }
+        if (p.o8 != nullptr) {
+          mx = warp_max(mx);
+          if (lane == 0) atomic_max_abs(p.amax, mx);
         }
       }
     }
@@ -583,7 +597,9 @@ __global__ void __launch_bounds__(320, 1)
       if (__all_sync(0xffffffffu, w)) {
         tc_fence_after();
         const float inv_l = 1.f / l;
-        bf16* orow = p.o + (static_cast<size_t>(wk.q_row0 + r) * p.batch + b) * p.ldo + h * D;
+        const size_t orow = (static_cast<size_t>(wk.q_row0 + r) * p.batch + b) * p.ldo + h * D;
+        const float qs = p.o8 != nullptr ? __ldg(p.q_scale) : 1.f;
+        float mx = 0.f;
 #pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {
           float o[32];
@@ -591,10 +607,22 @@ __global__ void __launch_bounds__(320, 1)
           if (row_ok) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] *= inv_l;
+            if (p.o8 != nullptr) {  // E4M3 output for the FP8 output projection
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-              *reinterpret_cast<uint4*>(orow + cc * 32 + q4 * 8) = pack_bf16x8(o + q4 * 8);
+              for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(o[i]));
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4)
+                *reinterpret_cast<uint2*>(p.o8 + orow + cc * 32 + q4 * 8) = pack_e4m3x8(o + q4 * 8, qs);
+            } else {
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4)
+                *reinterpret_cast<uint4*>(p.o + orow + cc * 32 + q4 * 8) = pack_bf16x8(o + q4 * 8);
+            }
           }
+        }
+        if (p.o8 != nullptr) {
+          mx = warp_max(mx);
+          if (lane == 0) atomic_max_abs(p.amax, mx);
         }
       }
     }

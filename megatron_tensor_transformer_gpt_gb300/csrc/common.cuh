@@ -134,6 +134,26 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
+// Instruction descriptor, kind::f8f6f4: E4M3 A and B (both K-major), fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4)                                   // D format: f32
+         | (0u << 7)                                 // A format: E4M3
+         | (0u << 10)                                // B format: E4M3
+         | (static_cast<uint32_t>(N >> 3) << 17)
+         | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T on E4M3 operands (K = 32 per instruction), one thread.
+__device__ __forceinline__ void mma_e4m3_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
 __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                             uint32_t accumulate) {
@@ -247,6 +267,36 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float* f) {
   u.z = pack_bf16x2(f[4], f[5]);
   u.w = pack_bf16x2(f[6], f[7]);
   return u;
+}
+
+// ---------------------------------------------------------------------------------- E4M3
+// Two fp32 values -> two E4M3 codes (round to nearest even, saturating to +-448); `lo` lands in
+// the low byte.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Eight fp32 values times `scale` -> eight E4M3 codes in memory order.
+__device__ __forceinline__ uint2 pack_e4m3x8(const float* f, float scale) {
+  uint2 u;
+  u.x = cvt_e4m3x2(__fmul_rn(f[0], scale), __fmul_rn(f[1], scale)) |
+        (cvt_e4m3x2(__fmul_rn(f[2], scale), __fmul_rn(f[3], scale)) << 16);
+  u.y = cvt_e4m3x2(__fmul_rn(f[4], scale), __fmul_rn(f[5], scale)) |
+        (cvt_e4m3x2(__fmul_rn(f[6], scale), __fmul_rn(f[7], scale)) << 16);
+  return u;
+}
+
+// Running |x| maximum: non-negative floats order like their bit patterns.
+__device__ __forceinline__ void atomic_max_abs(unsigned* slot, float v) {
+  atomicMax(slot, __float_as_uint(fabsf(v)));
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
 }
 
 }  // namespace mt

@@ -38,10 +38,13 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 // statistics in fp32.
 //   RMSNorm:   y = x / sqrt(mean(x^2) + eps) * g           (input_layernorm for LLaMA)
 //   LayerNorm: y = (x - mean) / sqrt(var + eps) * g + b     (biased variance, two passes)
-template <int VPT, bool LN>
+// OUT8: write E4M3 codes of y * (*q_scale) to y8 instead of bf16 y, and fold max |y| of the row
+// into *amax (one atomic per CTA).
+template <int VPT, bool LN, bool OUT8>
 __global__ void __launch_bounds__(1024) norm_kernel(const bf16* __restrict__ x, const bf16* __restrict__ gamma,
                                                     const bf16* __restrict__ beta, bf16* __restrict__ y, int H,
-                                                    float eps) {
+                                                    float eps, uint8_t* __restrict__ y8, const float* q_scale,
+                                                    unsigned* amax) {
   __shared__ float red[32];
   const size_t row = blockIdx.x;
   const int nvec = H >> 3;
@@ -83,9 +86,10 @@ __global__ void __launch_bounds__(1024) norm_kernel(const bf16* __restrict__ x, 
   } else {
     rstd = rsqrtf(acc * inv_h + eps);
   }
-  uint4* yr = reinterpret_cast<uint4*>(y + row * H);
   const uint4* gr = reinterpret_cast<const uint4*>(gamma);
   const uint4* br = reinterpret_cast<const uint4*>(beta);
+  const float qs = OUT8 ? __ldg(q_scale) : 1.f;
+  float mx = 0.f;
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int idx = i * blockDim.x + threadIdx.x;
@@ -96,24 +100,91 @@ __global__ void __launch_bounds__(1024) norm_kernel(const bf16* __restrict__ x, 
       if (LN) unpack_bf16x8(__ldg(br + idx), bfv);
 #pragma unroll
       for (int e = 0; e < 8; ++e) o[e] = (f[e] - mean) * rstd * gf[e] + (LN ? bfv[e] : 0.f);
-      yr[idx] = pack_bf16x8(o);
+      if (OUT8) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx = fmaxf(mx, fabsf(o[e]));
+        reinterpret_cast<uint2*>(y8 + row * H)[idx] = pack_e4m3x8(o, qs);
+      } else {
+        reinterpret_cast<uint4*>(y + row * H)[idx] = pack_bf16x8(o);
+      }
+    }
+  }
+  if (OUT8) {
+    mx = warp_max(mx);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int i = 1; i < static_cast<int>(blockDim.x >> 5); ++i) mx = fmaxf(mx, red[i]);
+      atomic_max_abs(amax, mx);
     }
   }
 }
 
-template <bool LN>
+template <bool LN, bool OUT8>
 cudaError_t launch_norm_ln(const bf16* x, const bf16* g, const bf16* b, bf16* y, int rows, int H, float eps,
-                           cudaStream_t stream) {
+                           uint8_t* y8, const float* q_scale, unsigned* amax, cudaStream_t stream) {
   const int nvec = H / 8;
   if (nvec >= 256) {  // two vectors per thread
     const int threads = ((nvec + 1) / 2 + 31) / 32 * 32;
     if (threads > 1024) return cudaErrorInvalidValue;
-    norm_kernel<2, LN><<<rows, threads, 0, stream>>>(x, g, b, y, H, eps);
+    norm_kernel<2, LN, OUT8><<<rows, threads, 0, stream>>>(x, g, b, y, H, eps, y8, q_scale, amax);
   } else {
     const int threads = (nvec + 31) / 32 * 32;
-    norm_kernel<1, LN><<<rows, threads, 0, stream>>>(x, g, b, y, H, eps);
+    norm_kernel<1, LN, OUT8><<<rows, threads, 0, stream>>>(x, g, b, y, H, eps, y8, q_scale, amax);
   }
   return cudaGetLastError();
+}
+
+// Largest |x| of n bf16 values into *amax (float bits; the caller zeroes it first).
+__global__ void amax_bf16_kernel(const bf16* __restrict__ x, size_t n8, unsigned* amax) {
+  float mx = 0.f;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n8;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    float f[8];
+    unpack_bf16x8(ld_stream(reinterpret_cast<const uint4*>(x) + i), f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) mx = fmaxf(mx, fabsf(f[e]));
+  }
+  mx = warp_max(mx);
+  if ((threadIdx.x & 31) == 0) atomic_max_abs(amax, mx);
+}
+
+// Per-tensor current scaling: scale = 448 / amax (1 if amax is 0), codes of x * scale; slot[1]
+// receives the dequantisation factor 1 / scale.
+__global__ void quantize_e4m3_kernel(const bf16* __restrict__ x, size_t n8, uint8_t* __restrict__ q, float* slot) {
+  const float amax = __uint_as_float(*reinterpret_cast<const unsigned*>(slot));
+  const float scale = amax > 0.f ? __fdiv_rn(448.0f, amax) : 1.0f;
+  if (blockIdx.x == 0 && threadIdx.x == 0) slot[1] = __frcp_rn(scale);
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n8;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    float f[8];
+    unpack_bf16x8(ld_stream(reinterpret_cast<const uint4*>(x) + i), f);
+    reinterpret_cast<uint2*>(q)[i] = pack_e4m3x8(f, scale);
+  }
+}
+
+// Delayed scaling after a forward: append each activation's amax of this call to its history,
+// clear it, and set scale = 448 / max(history) (1 while the history is all zero), deq = 1/scale.
+// state: scale[4] | deq[4] | amax bits[4] | pad[4] | history[4][len].  One warp per tensor.
+__global__ void fp8_history_kernel(float* state, int len, int pos) {
+  const int t = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (t >= 4) return;
+  unsigned* amax_bits = reinterpret_cast<unsigned*>(state + 8);
+  float* hist = state + 16 + static_cast<size_t>(t) * len;
+  if (lane == 0) {
+    hist[pos] = __uint_as_float(amax_bits[t]);
+    amax_bits[t] = 0u;
+  }
+  __syncwarp();
+  float mx = 0.f;
+  for (int i = lane; i < len; i += 32) mx = fmaxf(mx, hist[i]);
+  mx = warp_max(mx);
+  if (lane == 0) {
+    const float scale = mx > 0.f ? __fdiv_rn(448.0f, mx) : 1.0f;
+    state[t] = scale;
+    state[4 + t] = __frcp_rn(scale);
+  }
 }
 
 // (cos, sin) of s * theta_i for s < seq, i < half.  The angle is formed and reduced modulo 2*pi
@@ -264,10 +335,28 @@ __global__ void packed_index_kernel(const int* __restrict__ cu, int n, int T, in
 }  // namespace
 
 cudaError_t launch_norm(bool layer_norm, const bf16* x, const bf16* g, const bf16* b, bf16* y, int rows, int hidden,
-                        float eps, cudaStream_t stream) {
+                        float eps, cudaStream_t stream, uint8_t* y8, const float* q_scale, unsigned* amax) {
   if (rows <= 0) return cudaSuccess;
-  return layer_norm ? launch_norm_ln<true>(x, g, b, y, rows, hidden, eps, stream)
-                    : launch_norm_ln<false>(x, g, b, y, rows, hidden, eps, stream);
+  if (y8 != nullptr)
+    return layer_norm ? launch_norm_ln<true, true>(x, g, b, y, rows, hidden, eps, y8, q_scale, amax, stream)
+                      : launch_norm_ln<false, true>(x, g, b, y, rows, hidden, eps, y8, q_scale, amax, stream);
+  return layer_norm ? launch_norm_ln<true, false>(x, g, b, y, rows, hidden, eps, y8, q_scale, amax, stream)
+                    : launch_norm_ln<false, false>(x, g, b, y, rows, hidden, eps, y8, q_scale, amax, stream);
+}
+
+cudaError_t launch_quantize_e4m3(const bf16* x, size_t n, uint8_t* q, float* slot, cudaStream_t stream) {
+  const size_t n8 = n / 8;
+  cudaError_t e = cudaMemsetAsync(slot, 0, 2 * sizeof(float), stream);
+  if (e != cudaSuccess || n8 == 0) return e;
+  const int blocks = static_cast<int>(n8 / 256 + 1 < 4 * 152 ? n8 / 256 + 1 : 4 * 152);
+  amax_bf16_kernel<<<blocks, 256, 0, stream>>>(x, n8, reinterpret_cast<unsigned*>(slot));
+  quantize_e4m3_kernel<<<blocks, 256, 0, stream>>>(x, n8, q, slot);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_history(float* state, int len, int pos, cudaStream_t stream) {
+  fp8_history_kernel<<<1, 128, 0, stream>>>(state, len, pos);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_rope_table(float2* table, const double* theta, int seq, int half, cudaStream_t stream) {

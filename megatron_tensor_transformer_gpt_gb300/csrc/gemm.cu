@@ -100,11 +100,27 @@ __device__ __forceinline__ int unit_col0(const Unit& w) {
   return w.tn * (MODE == kEpiSwiglu ? 128 : BN) + w.sub * unit_width<MODE>(w);
 }
 
-template <int MODE>
+__device__ __forceinline__ void scale32(float* v, float f) {
+#pragma unroll
+  for (int e = 0; e < 32; ++e) v[e] *= f;
+}
+
+// 32 outputs as E4M3 codes (pitch in bytes), masked per 8 columns.
+__device__ __forceinline__ void store_e4m3x32(uint8_t* dst_row, int col, int limit, const float* v, float qs) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+    if (col + 8 * g < limit) *reinterpret_cast<uint2*>(dst_row + col + 8 * g) = pack_e4m3x8(v + 8 * g, qs);
+}
+
+template <int MODE, bool F8>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc, int m0, int c0, int width,
                                               int r_in_tile) {
   const int row = m0 + r_in_tile;
   const bool valid = row < p.M;
+  const float deq = F8 ? __ldg(p.deq_a) * __ldg(p.deq_b) : 1.f;
+  const bool out8 = (MODE == kEpiSwiglu || MODE == kEpiGelu) && p.out8 != nullptr;
+  const float qs = out8 ? __ldg(p.q_scale) : 1.f;
+  float amax = 0.f;
   if constexpr (MODE == kEpiStore || MODE == kEpiResid || MODE == kEpiGelu) {
 #pragma unroll 1
     for (int c = 0; c < width; c += 32) {
@@ -113,13 +129,21 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
       float v[32];
       tmem_ld32(tacc + c, v);
       if (valid) {
+        if (F8) scale32(v, deq);
         if (p.bias != nullptr) add_vec32(v, p.bias, col, p.N);
         if constexpr (MODE == kEpiResid) add_vec32(v, p.resid + static_cast<size_t>(row) * p.ldr, col, p.N);
         if constexpr (MODE == kEpiGelu) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = gelu_tanh(v[e]);
         }
-        store_vec32(p.out + static_cast<size_t>(row) * p.ldo, col, p.N, v);
+        if (out8) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (col + e < p.N) amax = fmaxf(amax, fabsf(v[e]));
+          store_e4m3x32(p.out8 + static_cast<size_t>(row) * p.ldo, col, p.N, v, qs);
+        } else {
+          store_vec32(p.out + static_cast<size_t>(row) * p.ldo, col, p.N, v);
+        }
       }
     }
   } else if constexpr (MODE == kEpiSwiglu) {
@@ -131,13 +155,24 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
       tmem_ld32(tacc + c, g);
       tmem_ld32(tacc + width + c, u);  // the up half follows the `width` gate columns
       if (valid) {
+        if (F8) {
+          scale32(g, deq);
+          scale32(u, deq);
+        }
         if (p.bias != nullptr) {
           add_vec32(g, p.bias, col, p.N);
           add_vec32(u, p.bias + p.N, col, p.N);
         }
 #pragma unroll
         for (int e = 0; e < 32; ++e) g[e] = silu(g[e]) * u[e];
-        store_vec32(p.out + static_cast<size_t>(row) * p.ldo, col, p.N, g);
+        if (out8) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (col + e < p.N) amax = fmaxf(amax, fabsf(g[e]));
+          store_e4m3x32(p.out8 + static_cast<size_t>(row) * p.ldo, col, p.N, g, qs);
+        } else {
+          store_vec32(p.out + static_cast<size_t>(row) * p.ldo, col, p.N, g);
+        }
       }
     }
   } else {  // kEpiQkv: `width` is a multiple of head_dim, so every head lies inside one unit
@@ -171,6 +206,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
           tmem_ld32(tacc + hc + i0, x1);
           tmem_ld32(tacc + hc + half + i0, x2);
           if (valid) {
+            if (F8) {
+              scale32(x1, deq);
+              scale32(x2, deq);
+            }
             if (p.bias != nullptr) {
               add_vec32(x1, p.bias, col + i0, p.N);
               add_vec32(x2, p.bias, col + half + i0, p.N);
@@ -195,6 +234,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
           float x[32];
           tmem_ld32(tacc + hc + i0, x);
           if (valid) {
+            if (F8) scale32(x, deq);
             if (p.bias != nullptr) add_vec32(x, p.bias, col + i0, p.N);
             if (is_v) {
 #pragma unroll
@@ -207,10 +247,14 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
       }
     }
   }
+  if (out8) {  // every lane arrives here (the loops above break uniformly)
+    amax = warp_max(amax);
+    if ((threadIdx.x & 31) == 0) atomic_max_abs(p.amax, amax);
+  }
 }
 
 // ------------------------------------------------------------------ kernel
-template <int MODE>
+template <int MODE, bool F8>
 __global__ void __launch_bounds__(192, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmB64, const GemmParams p) {
@@ -256,7 +300,8 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int num_kb = (p.K + BK - 1) / BK;
+  constexpr int KB = F8 ? 128 : BK;  // K elements per stage: one 128-byte swizzle row either way
+  const int num_kb = (p.K + KB - 1) / KB;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -271,7 +316,7 @@ __global__ void __launch_bounds__(192, 1)
         // B rows of this unit: SwiGLU gate rows [c0, c0+width) then the matching up rows;
         // otherwise rows [c0, c0+width).  Boxes of 128 rows, or 64 for the narrowest pieces.
         const int b_rows = MODE == kEpiSwiglu ? 2 * width : width;
-        const uint32_t stage_bytes = A_BYTES + b_rows * BK * 2;
+        const uint32_t stage_bytes = A_BYTES + b_rows * 128;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(empty(stage), phase ^ 1u, p.err, abort_flag)) {
             ok = false;
@@ -281,16 +326,16 @@ __global__ void __launch_bounds__(192, 1)
           mbar_arrive_expect_tx(fb, stage_bytes);
           const uint32_t a_dst = smem_u32(sA + stage * A_BYTES);
           const uint32_t b_dst = smem_u32(sB + stage * B_BYTES);
-          tma_load_2d(a_dst, &tmA, fb, kb * BK, m0);
+          tma_load_2d(a_dst, &tmA, fb, kb * KB, m0);
           if (MODE == kEpiSwiglu) {
             const CUtensorMap* mb = width == 128 ? &tmB : &tmB64;
-            tma_load_2d(b_dst, mb, fb, kb * BK, c0);
-            tma_load_2d(b_dst + width * BK * 2, mb, fb, kb * BK, c0 + p.b_row_step);
+            tma_load_2d(b_dst, mb, fb, kb * KB, c0);
+            tma_load_2d(b_dst + width * 128, mb, fb, kb * KB, c0 + p.b_row_step);
           } else if (width == 256) {
-            tma_load_2d(b_dst, &tmB, fb, kb * BK, c0);
-            tma_load_2d(b_dst + B_BYTES / 2, &tmB, fb, kb * BK, c0 + 128);
+            tma_load_2d(b_dst, &tmB, fb, kb * KB, c0);
+            tma_load_2d(b_dst + B_BYTES / 2, &tmB, fb, kb * KB, c0 + 128);
           } else {
-            tma_load_2d(b_dst, width == 128 ? &tmB : &tmB64, fb, kb * BK, c0);
+            tma_load_2d(b_dst, width == 128 ? &tmB : &tmB64, fb, kb * KB, c0);
           }
           ++issued;
           if (++stage == STAGES) {
@@ -313,7 +358,8 @@ __global__ void __launch_bounds__(192, 1)
       for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
         const Unit w = decode_unit(p, u);
         const int width = unit_width<MODE>(w);
-        const uint32_t idesc = idesc_bf16(BM, MODE == kEpiSwiglu ? 2 * width : width);
+        const int n_mma = MODE == kEpiSwiglu ? 2 * width : width;
+        const uint32_t idesc = F8 ? idesc_e4m3(BM, n_mma) : idesc_bf16(BM, n_mma);
         const int acc = it & 1;
         const uint32_t use = (it >> 1) & 1;
         if (!mbar_wait(tempty(acc), use ^ 1u, p.err, abort_flag)) {
@@ -332,7 +378,10 @@ __global__ void __launch_bounds__(192, 1)
           const uint64_t bd = sw128_desc(smem_u32(sB + stage * B_BYTES));
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            mma_bf16_ss(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            if (F8)
+              mma_e4m3_ss(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            else
+              mma_bf16_ss(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb | k) != 0 ? 1u : 0u);
           mma_commit(empty(stage));
           if (++stage == STAGES) {
             stage = 0;
@@ -356,7 +405,7 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       const Unit w = decode_unit(p, u);
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
-      epilogue_tile<MODE>(p, tacc, w.tm * BM, unit_col0<MODE>(w), unit_width<MODE>(w), quad * 32 + lane);
+      epilogue_tile<MODE, F8>(p, tacc, w.tm * BM, unit_col0<MODE>(w), unit_width<MODE>(w), quad * 32 + lane);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty(acc));
@@ -370,36 +419,43 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
-template <int MODE>
+template <int MODE, bool F8>
 cudaError_t launch_mode(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB64, const GemmParams& p,
                         cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<MODE, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(SMEM_BYTES));
     if (e != cudaSuccess) return e;
     configured = true;
   }
   const int grid = p.num_units < num_sms() ? p.num_units : num_sms();
-  gemm_kernel<MODE><<<grid, 192, SMEM_BYTES, stream>>>(tmA, tmB, tmB64, p);
+  gemm_kernel<MODE, F8><<<grid, 192, SMEM_BYTES, stream>>>(tmA, tmB, tmB64, p);
   return cudaGetLastError();
+}
+
+template <bool F8>
+cudaError_t launch_kind(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB64,
+                        const GemmParams& p, cudaStream_t stream) {
+  switch (mode) {
+    case kEpiStore: return launch_mode<kEpiStore, F8>(tmA, tmB, tmB64, p, stream);
+    case kEpiResid: return launch_mode<kEpiResid, F8>(tmA, tmB, tmB64, p, stream);
+    case kEpiQkv: return launch_mode<kEpiQkv, F8>(tmA, tmB, tmB64, p, stream);
+    case kEpiSwiglu: return launch_mode<kEpiSwiglu, F8>(tmA, tmB, tmB64, p, stream);
+    case kEpiGelu: return launch_mode<kEpiGelu, F8>(tmA, tmB, tmB64, p, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
 
 size_t gemm_smem_bytes() { return SMEM_BYTES; }
 
-cudaError_t launch_gemm(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB64,
+cudaError_t launch_gemm(int mode, bool fp8, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB64,
                         const GemmParams& p, cudaStream_t stream) {
   if (p.num_units <= 0) return cudaSuccess;
-  switch (mode) {
-    case kEpiStore: return launch_mode<kEpiStore>(tmA, tmB, tmB64, p, stream);
-    case kEpiResid: return launch_mode<kEpiResid>(tmA, tmB, tmB64, p, stream);
-    case kEpiQkv: return launch_mode<kEpiQkv>(tmA, tmB, tmB64, p, stream);
-    case kEpiSwiglu: return launch_mode<kEpiSwiglu>(tmA, tmB, tmB64, p, stream);
-    case kEpiGelu: return launch_mode<kEpiGelu>(tmA, tmB, tmB64, p, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  return fp8 ? launch_kind<true>(mode, tmA, tmB, tmB64, p, stream)
+             : launch_kind<false>(mode, tmA, tmB, tmB64, p, stream);
 }
 
 }  // namespace mt

@@ -42,6 +42,14 @@ struct GemmParams {
   // packed samples (batch 1): per-token RoPE position and column of v^T; null for dense batches
   const int* pos;
   const int* vcol;
+  // E4M3 operands: the fp32 accumulator is multiplied by (*deq_a) * (*deq_b); null for bf16
+  const float* deq_a;
+  const float* deq_b;
+  // E4M3 output of the SwiGLU / GeLU epilogue: codes of out * (*q_scale) go to out8 (pitch ldo
+  // bytes) instead of `out`, and max |out| is folded into *amax (float bits)
+  uint8_t* out8;
+  const float* q_scale;
+  unsigned* amax;
   int* err;
 };
 
@@ -55,6 +63,10 @@ struct AttnParams {
   float scale_log2;        // log2(e) / sqrt(head_dim)
   bf16* o;                 // [seq*batch, ldo], head h at columns h*head_dim
   int ldo;
+  // E4M3 output instead of o: codes of o * (*q_scale), pitch ldo bytes; max |o| into *amax
+  uint8_t* o8;
+  const float* q_scale;
+  unsigned* amax;
   int* err;
 };
 
@@ -76,15 +88,25 @@ struct SpParams {
 int num_sms();
 
 // Kernel launchers; return a cudaError_t from the launch.
-cudaError_t launch_gemm(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB64,
+// fp8 = true: A and B are E4M3 (tensor maps of bytes, boxes 128 wide).
+cudaError_t launch_gemm(int mode, bool fp8, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB64,
                         const GemmParams& p, cudaStream_t stream);
 size_t gemm_smem_bytes();
 
 cudaError_t launch_attention(int head_dim, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                              const AttnParams& p, cudaStream_t stream);
 
+// y8 != null: E4M3 output y * (*q_scale) into y8, max |y| folded into *amax.
 cudaError_t launch_norm(bool layer_norm, const bf16* x, const bf16* g, const bf16* b, bf16* y, int rows, int hidden,
-                        float eps, cudaStream_t stream);
+                        float eps, cudaStream_t stream, uint8_t* y8 = nullptr, const float* q_scale = nullptr,
+                        unsigned* amax = nullptr);
+
+// Current per-tensor scaling of n (multiple of 8) bf16 values: slot[0] <- amax (float bits),
+// slot[1] <- 1/scale, q <- E4M3 codes of x * 448 / amax.
+cudaError_t launch_quantize_e4m3(const bf16* x, size_t n, uint8_t* q, float* slot, cudaStream_t stream);
+
+// Delayed-scaling update after an FP8 forward (state layout: see fp8_history_kernel).
+cudaError_t launch_fp8_history(float* state, int len, int pos, cudaStream_t stream);
 
 cudaError_t launch_rope_table(float2* table, const double* theta, int seq, int half, cudaStream_t stream);
 

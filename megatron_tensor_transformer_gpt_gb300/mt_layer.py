@@ -30,6 +30,11 @@ class MtWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_FIELDS]
 
 
+class MtFp8Weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("w_qkv", "w_o", "w_fc1", "w_fc2",
+                                                "deq_qkv", "deq_o", "deq_fc1", "deq_fc2")]
+
+
 class MtError(RuntimeError):
     def __init__(self, code: int, msg: str):
         super().__init__(f"[mt status {code}] {msg}")
@@ -69,6 +74,16 @@ _SIGS = {
     "mt_layer_forward_packed": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
                                  ctypes.c_int, ctypes.POINTER(MtWeights), ctypes.c_void_p, ctypes.c_void_p],
                                 ctypes.c_int),
+    "mt_layer_fp8_enable": ([ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
+    "mt_layer_fp8_set_scales": ([ctypes.c_void_p, ctypes.POINTER(ctypes.c_float)], ctypes.c_int),
+    "mt_layer_fp8_state": ([ctypes.c_void_p, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)],
+                           ctypes.c_int),
+    "mt_layer_forward_fp8": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.POINTER(MtWeights),
+                              ctypes.POINTER(MtFp8Weights), ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "mt_quantize_e4m3": ([ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p],
+                         ctypes.c_int),
+    "mt_gemm_e4m3": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "mt_sp_reduce_add_norm": ([ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_int,
                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
@@ -196,6 +211,35 @@ def mt_sp_reduce_add_norm(partials, resid, bias, norm_w, norm_b, norm, eps, toke
     arr = (ctypes.c_void_p * len(partials))(*partials)
     _check(lib().mt_sp_reduce_add_norm(arr, len(partials), resid, bias, norm_w, norm_b, norm, float(eps), tokens,
                                        hidden, row0, rows, h_out, hn_out, stream))
+
+
+def mt_layer_fp8_enable(handle, amax_history_len=1024):
+    _check(lib().mt_layer_fp8_enable(handle, int(amax_history_len)))
+
+
+def mt_layer_fp8_set_scales(handle, scales):
+    arr = (ctypes.c_float * 4)(*[float(s) for s in scales])
+    _check(lib().mt_layer_fp8_set_scales(handle, arr))
+
+
+def mt_layer_fp8_state(handle):
+    """(scales[4], last_amax[4]) of the activations (normed x, attention out, normed h, MLP hidden)."""
+    sc, am = (ctypes.c_float * 4)(), (ctypes.c_float * 4)()
+    _check(lib().mt_layer_fp8_state(handle, sc, am))
+    return list(sc), list(am)
+
+
+def mt_layer_forward_fp8(handle, x, seq, batch, weights: MtWeights, w8: MtFp8Weights, y_partial, stream):
+    _check(lib().mt_layer_forward_fp8(handle, x, seq, batch, ctypes.byref(weights), ctypes.byref(w8), y_partial,
+                                      stream))
+
+
+def mt_quantize_e4m3(src, n, dst, amax_deq, stream):
+    _check(lib().mt_quantize_e4m3(src, n, dst, amax_deq, stream))
+
+
+def mt_gemm_e4m3(A, B, C, M, N, K, deq_a, deq_b, stream):
+    _check(lib().mt_gemm_e4m3(A, B, C, M, N, K, deq_a, deq_b, stream))
 
 
 def mt_gemm_bf16(A, B, C, M, N, K, stream):

@@ -89,17 +89,26 @@ def _qdq(x, scale):
 ACT_NAMES = ("xn", "o", "hn", "a")
 
 
-def layer_forward_fp8(cfg, inp: Dict, act_scales, rows: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+WEIGHT_NAMES = ("w_qkv", "w_o", "w_fc1", "w_fc2")
+
+
+def quantize_weights(inp: Dict) -> Dict[str, Dict[str, np.ndarray]]:
+    return {k: quantize_weight(inp[k]) for k in WEIGHT_NAMES}
+
+
+def layer_forward_fp8(cfg, inp: Dict, act_scales, rows: Optional[np.ndarray] = None,
+                      wq: Optional[Dict] = None) -> Dict[str, np.ndarray]:
     """Whole layer at TP=1 with the four GEMMs on E4M3 operands.
 
-    act_scales: fp32 scales of (xn, o, hn, a).  Weights use quantize_weight.  Returns y and h for
-    `rows` (all tokens if None) and the amax of each activation over those rows.
+    act_scales: fp32 scales of (xn, o, hn, a).  Weights use quantize_weight (or the precomputed
+    `wq` of quantize_weights(inp)).  Returns y and h for `rows` (all tokens if None) and the amax
+    of each activation over those rows.
     """
     T, B, d = cfg.tokens, cfg.batch, cfg.head_dim
     nh, ng = cfg.heads, cfg.groups
     rows = np.arange(T) if rows is None else np.asarray(rows)
     s_xn, s_o, s_hn, s_a = (np.float32(s) for s in act_scales)
-    wq = {k: quantize_weight(inp[k]) for k in ("w_qkv", "w_o", "w_fc1", "w_fc2")}
+    wq = quantize_weights(inp) if wq is None else wq
     W = {k: dequantize(v["codes"], v["scale"]) for k, v in wq.items()}
     x = ol._tokens(inp["x"], cfg)
     b = {k: ol._w(inp, k) for k in ("b_qkv", "b_o", "b_fc1", "b_fc2")}

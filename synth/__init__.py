@@ -25,7 +25,7 @@ import numpy as np
 
 __all__ = [
     "LayerConfig", "CONFIGS", "WEIGHT_NAMES", "f32_to_bf16_bits", "bf16_bits_to_f32",
-    "make_inputs", "shard_weights", "shard_row_ranges",
+    "make_inputs", "shard_weights", "shard_row_ranges", "random_e4m3_codes",
 ]
 
 NORM_RMS, NORM_LAYER = "rms", "layer"
@@ -223,3 +223,13 @@ def shard_weights(cfg: LayerConfig, w: Dict[str, np.ndarray], tp: int, rank: int
     out["w_fc1"], out["b_fc1"] = rows(w["w_fc1"], r["fc1_rows"]), rows(w.get("b_fc1"), r["fc1_rows"])
     out["w_fc2"] = cols(w["w_fc2"], r["fc2_cols"])
     return out
+
+
+def random_e4m3_codes(shape, seed: int, max_exponent_field: int = 9) -> np.ndarray:
+    """Seeded random E4M3 bit patterns: uniform sign, exponent field 0..max_exponent_field (so no
+    NaN code and magnitudes below 2^(max_exponent_field-6)), uniform 3-bit mantissa."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    sign = rng.integers(0, 2, size=shape, dtype=np.uint8) << np.uint8(7)
+    expo = rng.integers(0, max_exponent_field + 1, size=shape, dtype=np.uint8) << np.uint8(3)
+    mant = rng.integers(0, 8, size=shape, dtype=np.uint8)
+    return (sign | expo | mant).astype(np.uint8)
