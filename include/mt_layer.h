@@ -182,7 +182,8 @@ int mt_layer_forward_host(mt_layer* L, const void* x_host, int seq, int batch, c
 
 /* Where an intermediate lives inside the workspace (for inspection in tests).  `which`:
  * 0 norm1 out [T,H]; 1 q [batch, nh_r, seq, d] after RoPE; 2 k [batch, ng_r, seq, d] after RoPE;
- * 3 v transposed [batch, ng_r, d, seq_pad] (seq_pad = seq rounded up to 8);
+ * 3 v transposed [batch, ng_r, d, seq_pad] in fp16 (seq_pad = seq rounded up to 8; the attention's
+ *   P V product runs on fp16 P and V, so |v| must stay below 65504);
  * 4 attention out [T, q_w]; 5 h [T,H]; 6 norm2 out [T,H]; 7 MLP hidden [T, f_r];
  * 8 RoPE table [seq, d/2] float2 (cos, sin). */
 int mt_layer_workspace_region(const mt_layer* L, int seq, int batch, int which, size_t* offset, size_t* bytes);

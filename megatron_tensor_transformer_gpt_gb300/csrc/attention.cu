@@ -85,7 +85,7 @@ struct Geo {
   static constexpr size_t SMEM_USED = 1024 + OFF_BAR + 256;
   static constexpr size_t SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
   static constexpr uint32_t IDESC_S = idesc_bf16(BQ, BKV);
-  static constexpr uint32_t IDESC_O = idesc_bf16(BQ, D);
+  static constexpr uint32_t IDESC_O = idesc_f16(BQ, D);  // fp16 P and v^T
 };
 
 template <int D>
@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       float mx = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < BKV; ++i) mx = fmaxf(mx, s[i]);
+      for (int i = 0; i < BKV; i += 2) mx = fmax3(mx, s[i], s[i + 1]);
       const float m_new = fmaxf(m_used, mx * c);
       if (j > 0) {  // P_{j-1} V_{j-1} finished: P may be overwritten and O is stable
         w = mbar_wait(o_done, (j - 1) & 1, p.err, abort_flag);
@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
       for (int ch = 0; ch < 16; ++ch) {
         const int atom = ch >> 3, cw = ch & 7;
-        *reinterpret_cast<uint4*>(prow + atom * G::ATOM + ((cw ^ sw) << 4)) = pack_bf16x8(s + ch * 8);
+        *reinterpret_cast<uint4*>(prow + atom * G::ATOM + ((cw ^ sw) << 4)) = pack_f16x8(s + ch * 8);
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -358,7 +358,7 @@ struct Geo2 {
   static constexpr size_t SMEM_USED = 1024 + OFF_BAR + 256;
   static constexpr size_t SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;  // one CTA per SM (TMEM)
   static constexpr uint32_t IDESC_S = idesc_bf16(BQ, BKV);
-  static constexpr uint32_t IDESC_O = idesc_bf16(BQ, D);
+  static constexpr uint32_t IDESC_O = idesc_f16(BQ, D);  // fp16 P and v^T
 };
 
 template <int D>
@@ -551,7 +551,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       float mx = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < BKV; ++i) mx = fmaxf(mx, s[i]);
+      for (int i = 0; i < BKV; i += 2) mx = fmax3(mx, s[i], s[i + 1]);
       const float m_new = fmaxf(m_used, mx * c);
       if (__any_sync(0xffffffffu, m_new > m_used + 8.0f)) {
         const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m_used - m_new);
@@ -574,18 +574,30 @@ __global__ void __launch_bounds__(320, 1)
         }
         m_used = m_new;
       }
+      // P = 2^(s c - m) in packed halves: one fp32x2 FMA, one fp16x2 conversion and one fp16x2
+      // exponential per pair of scores (the argument is at most 8 after the lazy rescaling, so its
+      // fp16 rounding moves P by under 0.6%, the order of P's own 16-bit rounding); row sums in four
+      // fp16x2 partial sums per 64 keys, widened to fp32 once per block.
       float rs = 0.f;
+      const float2 cc = make_float2(c, c), mm = make_float2(-m_used, -m_used);
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         uint32_t pk[32];
+        __half2 acc[4] = {__float2half2_rn(0.f), __float2half2_rn(0.f), __float2half2_rn(0.f),
+                          __float2half2_rn(0.f)};
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2_approx(fmaf(s[64 * hf + 2 * i], c, -m_used));
-          const float p1 = ex2_approx(fmaf(s[64 * hf + 2 * i + 1], c, -m_used));
-          rs += p0 + p1;
-          pk[i] = pack_bf16x2(p0, p1);
+          const float2 xy = ffma2(make_float2(s[64 * hf + 2 * i], s[64 * hf + 2 * i + 1]), cc, mm);
+          const uint32_t e = ex2_f16x2(pack_f16x2(xy.x, xy.y));
+          acc[i & 3] = __hadd2(acc[i & 3], *reinterpret_cast<const __half2*>(&e));
+          pk[i] = e;
         }
         tmem_st32_raw(tS(t) + lane_off + 32 * hf, pk);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = __half22float2(acc[k]);
+          rs += f.x + f.y;
+        }
       }
       l += rs;
       tc_fence_before();

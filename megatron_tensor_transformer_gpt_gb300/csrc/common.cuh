@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -134,6 +135,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
+// Instruction descriptor, kind::f16 with fp16 A and B (both K-major), fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+  return (1u << 4)                                   // D format: f32
+         | (static_cast<uint32_t>(N >> 3) << 17)     // A, B format 0: f16
+         | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // Instruction descriptor, kind::f8f6f4: E4M3 A and B (both K-major), fp32 accumulator.
 __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
   return (1u << 4)                                   // D format: f32
@@ -249,6 +257,44 @@ __device__ __forceinline__ float ex2_approx(float x) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint4 pack_f16x8(const float* f) {
+  uint4 u;
+  u.x = pack_f16x2(f[0], f[1]);
+  u.y = pack_f16x2(f[2], f[3]);
+  u.z = pack_f16x2(f[4], f[5]);
+  u.w = pack_f16x2(f[6], f[7]);
+  return u;
+}
+
+// Two exponentials 2^x of a packed fp16 pair in one special-function instruction.
+__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
+  uint32_t r;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
+}
+
+// d = a * b + c on two fp32 lanes in one instruction.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float m;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
+  return m;
 }
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4& u, float* f) {

@@ -238,7 +238,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
             if (p.bias != nullptr) add_vec32(x, p.bias, col + i0, p.N);
             if (is_v) {
 #pragma unroll
-              for (int e = 0; e < 32; ++e) dst[static_cast<size_t>(i0 + e) * p.seq_pad] = __float2bfloat16_rn(x[e]);
+              for (int e = 0; e < 32; ++e)  // v^T is fp16: the P V product takes fp16 P
+                reinterpret_cast<__half*>(dst)[static_cast<size_t>(i0 + e) * p.seq_pad] = __float2half_rn(x[e]);
             } else {
               store_vec32(dst, i0, d, x);
             }

@@ -79,8 +79,8 @@ def test_intermediates_match_oracle(cfg):
     T, B, S, d, nh, ng = cfg.tokens, cfg.batch, cfg.seq, cfg.head_dim, cfg.heads, cfg.groups
     ref = _oracle_pieces(cfg, inp)
 
-    def reg(name, shape):
-        return to_f64(dl.layer.region(S, B, name).view(torch.bfloat16)[: int(np.prod(shape))].reshape(shape))
+    def reg(name, shape, dtype=torch.bfloat16):
+        return to_f64(dl.layer.region(S, B, name).view(dtype)[: int(np.prod(shape))].reshape(shape))
 
     assert_layer_close(reg("xn", (T, cfg.hidden)), ref["xn"], "norm1")
     q = reg("q", (B, nh, S, d))
@@ -88,7 +88,7 @@ def test_intermediates_match_oracle(cfg):
     k = reg("k", (B, ng, S, d))
     assert_layer_close(k, ref["k"].reshape(S, B, ng, d).transpose(1, 2, 0, 3), "k after RoPE")
     sp = (S + 7) // 8 * 8
-    vt = reg("vt", (B, ng, d, sp))[..., :S]
+    vt = reg("vt", (B, ng, d, sp), torch.float16)[..., :S]
     assert_layer_close(vt, ref["v"].reshape(S, B, ng, d).transpose(1, 2, 3, 0), "v transposed")
     assert_layer_close(reg("o", (T, nh * d)), ref["o"], "attention output")
     full = ol.layer_forward(cfg, inp)
