@@ -39,12 +39,19 @@ def _rope_complex(x, positions, base):
     return torch.cat([z.real, z.imag], dim=-1)
 
 
-def layer_forward(cfg, inp):
-    """TP=1 layer output y [S*B, H] (float64 torch tensor)."""
+def as_tensors(inp):
+    """float64 torch tensors of the bf16 inputs (None stays None)."""
+    return {k: _t(v) for k, v in inp.items()}
+
+
+def layer_forward(cfg, inp, tensors=None):
+    """TP=1 layer output y [S*B, H] (float64 torch tensor).  `tensors`: as_tensors(inp), possibly
+    requiring gradients, used instead of decoding `inp`."""
     S, B, H, d = cfg.seq, cfg.batch, cfg.hidden, cfg.head_dim
     nh, ng = cfg.heads, cfg.groups
-    x = _t(inp["x"]).reshape(S, B, H)
-    w = {k: _t(v) for k, v in inp.items() if k != "x"}
+    t = as_tensors(inp) if tensors is None else tensors
+    x = t["x"].reshape(S, B, H)
+    w = {k: v for k, v in t.items() if k != "x"}
 
     xn = _norm(cfg, x, w["norm1_w"], w.get("norm1_b"))
     qkv = F.linear(xn, w["w_qkv"], w.get("b_qkv"))
