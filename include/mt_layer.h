@@ -180,6 +180,25 @@ int mt_gemm_e4m3(const void* A, const void* B, void* C, int M, int N, int K, con
 int mt_layer_forward_host(mt_layer* L, const void* x_host, int seq, int batch, const mt_weights* w,
                           void* y_host, void* cuda_stream);
 
+/* ---- backward pass (tp_size == 1) ---------------------------------------------------------
+ * Gradients of a scalar loss through the layer, given dL/dy (the pages' purpose is training:
+ * the forward-backward step of "ai阅读megatron"'s training loop).  The forward intermediates are
+ * recomputed first (full activation recompute, "快速入门" §8), then the chain rule runs through
+ * the same readings as the forward.  All gradients are bf16 with fp32 accumulation inside. */
+typedef struct { /* device pointers, shapes as in mt_weights; NULL = gradient not wanted */
+  void *norm1_w, *norm1_b, *w_qkv, *b_qkv, *w_o, *b_o, *norm2_w, *norm2_b, *w_fc1, *b_fc1, *w_fc2, *b_fc2;
+} mt_grads;
+
+/* Workspace the backward pass needs (a superset of the forward's: the forward intermediates,
+ * gradient scratch, per-head fp32 score and dP matrices [seq, seq], and transposes). */
+int mt_layer_backward_workspace_bytes(const mt_layer* L, int seq, int batch, size_t* bytes);
+
+/* dx [T, H] = dL/dx and the requested weight gradients, given x and dy = dL/dy [T, H].  Needs
+ * tp_size == 1, seq % 8 == 0 and a workspace of mt_layer_backward_workspace_bytes.  Asynchronous
+ * on cuda_stream (many launches: the attention part runs head by head). */
+int mt_layer_backward(mt_layer* L, const void* x, const void* dy, int seq, int batch, const mt_weights* w, void* dx,
+                      const mt_grads* g, void* cuda_stream);
+
 /* Where an intermediate lives inside the workspace (for inspection in tests).  `which`:
  * 0 norm1 out [T,H]; 1 q [batch, nh_r, seq, d] after RoPE; 2 k [batch, ng_r, seq, d] after RoPE;
  * 3 v transposed [batch, ng_r, d, seq_pad] in fp16 (seq_pad = seq rounded up to 8; the attention's

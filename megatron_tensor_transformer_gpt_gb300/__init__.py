@@ -4,4 +4,4 @@ The compute path is libmt_layer.so (hand-written sm_103a kernels behind a C ABI,
 include/mt_layer.h); ``mt_layer`` is its Python binding.
 """
 from . import mt_layer  # noqa: F401
-from .mt_layer import Layer, MtError, MtFp8Weights, MtWeights  # noqa: F401
+from .mt_layer import Layer, MtError, MtFp8Weights, MtGrads, MtWeights  # noqa: F401

@@ -84,7 +84,7 @@ struct Timed {
   cudaEvent_t a = nullptr;
   int slot;
   Timed(mt_layer* l, int s, cudaStream_t stream)
-      : L(l), st(stream), on(l != nullptr && l->profiling && l->recs.size() < kMaxRecords), slot(s) {
+      : L(l), st(stream), on(l != nullptr && s >= 0 && l->profiling && l->recs.size() < kMaxRecords), slot(s) {
     if (on) {
       a = pool_event(L);
       cudaEventRecord(a, st);
@@ -593,6 +593,215 @@ int forward_device_fp8(mt_layer* L, const Layout& lay, const void* x, int S, int
   return MT_OK;
 }
 
+// ------------------------------------------------------------------ backward pass (TP=1)
+// Plain GEMM with strided bf16 operands: out = A[M, K] (pitch lda) * B[N, K]^T (pitch ldb), to bf16
+// `out` or fp32 `out32` (acc32: add to it), pitch ldo.
+int gemm_ab(mt_layer* L, const void* A, size_t lda, const void* Bm, size_t ldb, int M, int N, int K, void* out,
+            float* out32, size_t ldo, bool acc32, cudaStream_t st) {
+  CUtensorMap ta, tb, tb64;
+  int rc = map_2d(&ta, A, K, M, lda, 128);
+  if (!rc) rc = map_2d(&tb, Bm, K, N, ldb, 128);
+  if (!rc) rc = map_2d(&tb64, Bm, K, N, ldb, 64);
+  if (rc) return rc;
+  mt::GemmParams p = gemm_params(M, N, K, false, L->d_err);
+  p.out = static_cast<bf16*>(out);
+  p.out32 = out32;
+  p.acc32 = acc32 ? 1 : 0;
+  p.ldo = static_cast<int>(ldo);
+  plan_gemm(p, mt::kEpiStore, 0);
+  cudaError_t e = mt::launch_gemm(mt::kEpiStore, false, ta, tb, tb64, p, st);
+  return e == cudaSuccess ? MT_OK : cuda_fail(e, "backward GEMM launch");
+}
+
+enum BwRegion {
+  kBQkv = 0, kBU, kBA, kBDa, kBDu, kBDhn, kBDh, kBDo, kBDq, kBDk, kBDv, kBDqkv, kBDxn, kBGrow, kBAcc,
+  kBS, kBDp, kBP, kBDs, kBPt, kBDoT, kBKT, kBQT, kBWt, kBAt, kBBt, kBNum
+};
+
+struct BwLayout {
+  Layout fwd;
+  size_t off[kBNum], size[kBNum], total;
+};
+
+BwLayout bw_layout(const mt_layer* L, int S, int B) {
+  BwLayout b{};
+  b.fwd = layout_for(L, S, B);
+  const size_t T = static_cast<size_t>(S) * B, H = L->hidden, d = L->head_dim;
+  const size_t QKV = L->q_w + 2 * L->kv_w, f = L->f_r, f1 = L->f1_r, qw = L->q_w;
+  const size_t maxc = std::max(std::max(QKV, f1), std::max(H, qw));
+  b.size[kBQkv] = T * QKV * 2;
+  b.size[kBU] = T * f1 * 2;
+  b.size[kBA] = T * f * 2;
+  b.size[kBDa] = T * f * 2;
+  b.size[kBDu] = T * f1 * 2;
+  b.size[kBDhn] = T * H * 2;
+  b.size[kBDh] = T * H * 2;
+  b.size[kBDo] = T * qw * 2;
+  b.size[kBDq] = static_cast<size_t>(B) * L->nh_r * S * d * 4;
+  b.size[kBDk] = static_cast<size_t>(B) * L->ng_r * S * d * 4;
+  b.size[kBDv] = static_cast<size_t>(B) * L->ng_r * S * d * 4;
+  b.size[kBDqkv] = T * QKV * 2;
+  b.size[kBDxn] = T * H * 2;
+  b.size[kBGrow] = T * H * 4;
+  b.size[kBAcc] = maxc * 4;
+  b.size[kBS] = static_cast<size_t>(S) * S * 4;
+  b.size[kBDp] = static_cast<size_t>(S) * S * 4;
+  b.size[kBP] = static_cast<size_t>(S) * S * 2;
+  b.size[kBDs] = static_cast<size_t>(S) * S * 2;
+  b.size[kBPt] = static_cast<size_t>(S) * S * 2;
+  b.size[kBDoT] = d * S * 2;
+  b.size[kBKT] = d * S * 2;
+  b.size[kBQT] = d * S * 2;
+  b.size[kBWt] = std::max(std::max(QKV * H, H * qw), std::max(f1 * H, H * f)) * 2;
+  b.size[kBAt] = maxc * T * 2;
+  b.size[kBBt] = maxc * T * 2;
+  size_t o = b.fwd.total;
+  for (int r = 0; r < kBNum; ++r) {
+    b.off[r] = o;
+    o = round_up(o + b.size[r], 1024);
+  }
+  b.total = o;
+  return b;
+}
+
+template <typename T>
+T* bwr(const mt_layer* L, const BwLayout& b, BwRegion r) {
+  return reinterpret_cast<T*>(static_cast<char*>(L->ws) + b.off[r]);
+}
+
+// dst = src^T for a bf16 [R, C] matrix with pitch sp into a dense [C, R] buffer.
+int transpose(const void* src, size_t sp, void* dst, int R, int C, cudaStream_t st) {
+  cudaError_t e = mt::launch_transpose(static_cast<const bf16*>(src), sp, static_cast<bf16*>(dst), R, R, C, st);
+  return e == cudaSuccess ? MT_OK : cuda_fail(e, "transpose launch");
+}
+
+// Gradients of one linear Y = X W^T (+ b) given dY (all bf16, dense):
+//   dW [N, K] = dY^T X, db = column sums of dY, dX [M, K] = dY W (written to dx if not null).
+int linear_bwd(mt_layer* L, const BwLayout& b, const void* dY, const void* X, const void* W, int M, int N, int K,
+               void* dW, void* db, void* dX, cudaStream_t st) {
+  int rc;
+  if (dW != nullptr) {
+    bf16* dYt = bwr<bf16>(L, b, kBAt);
+    bf16* Xt = bwr<bf16>(L, b, kBBt);
+    if ((rc = transpose(dY, N, dYt, M, N, st))) return rc;
+    if ((rc = transpose(X, K, Xt, M, K, st))) return rc;
+    if ((rc = gemm_ab(L, dYt, M, Xt, M, N, K, M, dW, nullptr, K, false, st))) return rc;
+  }
+  if (db != nullptr) {
+    cudaError_t e = mt::launch_colsum(dY, false, N, M, N, bwr<float>(L, b, kBAcc), static_cast<bf16*>(db), st);
+    if (e != cudaSuccess) return cuda_fail(e, "bias gradient");
+  }
+  if (dX != nullptr) {
+    bf16* Wt = bwr<bf16>(L, b, kBWt);
+    if ((rc = transpose(W, K, Wt, N, K, st))) return rc;
+    if ((rc = gemm_ab(L, dY, N, Wt, N, M, K, N, dX, nullptr, K, false, st))) return rc;
+  }
+  return MT_OK;
+}
+
+int norm_bwd(mt_layer* L, const BwLayout& b, const void* dy, const void* x, const void* gamma, const void* add,
+             void* out, void* dgamma, void* dbeta, int T, cudaStream_t st) {
+  const int H = L->hidden;
+  float* grow = bwr<float>(L, b, kBGrow);
+  cudaError_t e = mt::launch_norm_bwd(static_cast<const bf16*>(dy), static_cast<const bf16*>(x),
+                                      static_cast<const bf16*>(gamma), static_cast<const bf16*>(add),
+                                      static_cast<bf16*>(out), grow, T, H, L->eps, L->norm == MT_NORM_LAYER, st);
+  if (e == cudaSuccess && dgamma != nullptr)
+    e = mt::launch_colsum(grow, true, H, T, H, bwr<float>(L, b, kBAcc), static_cast<bf16*>(dgamma), st);
+  if (e == cudaSuccess && dbeta != nullptr && L->norm == MT_NORM_LAYER)
+    e = mt::launch_colsum(dy, false, H, T, H, bwr<float>(L, b, kBAcc), static_cast<bf16*>(dbeta), st);
+  return e == cudaSuccess ? MT_OK : cuda_fail(e, "norm backward");
+}
+
+int backward_device(mt_layer* L, const BwLayout& b, const void* x, const void* dy, int S, int B, const mt_weights* w,
+                    void* dx, const mt_grads* g, cudaStream_t st) {
+  const Layout& lay = b.fwd;
+  const int T = S * B, H = L->hidden, d = L->head_dim, nh = L->nh_r, ng = L->ng_r, rep = nh / ng;
+  const int qw = L->q_w, kvw = L->kv_w, QKV = qw + 2 * kvw, f = L->f_r, f1 = L->f1_r;
+  const bool swiglu = L->act == MT_ACT_SWIGLU;
+  int rc;
+  cudaError_t e;
+  // ---- forward recompute: xn, q, k (after RoPE), o, h (attention block), hn, plain qkv, u, a
+  bf16* h = region<bf16>(L, lay, kH);
+  if ((rc = run_attention_block(L, lay, x, S, B, w, h, mt::kEpiResid, st))) return rc;
+  bf16 *xn = region<bf16>(L, lay, kXn), *hn = region<bf16>(L, lay, kHn), *o = region<bf16>(L, lay, kO);
+  bf16 *q = region<bf16>(L, lay, kQ), *k = region<bf16>(L, lay, kK);
+  e = mt::launch_norm(L->norm == MT_NORM_LAYER, h, static_cast<const bf16*>(w->norm2_w),
+                      static_cast<const bf16*>(w->norm2_b), hn, T, H, L->eps, st);
+  if (e != cudaSuccess) return cuda_fail(e, "norm2 launch");
+  bf16 *qkv = bwr<bf16>(L, b, kBQkv), *u = bwr<bf16>(L, b, kBU), *a = bwr<bf16>(L, b, kBA);
+  {
+    mt::GemmParams p = gemm_params(T, QKV, H, false, L->d_err);
+    p.out = qkv;
+    p.ldo = QKV;
+    p.bias = static_cast<const bf16*>(w->b_qkv);
+    if ((rc = run_gemm(L, -1, mt::kEpiStore, xn, H, w->w_qkv, QKV, T, QKV, H, p, st))) return rc;
+    p = gemm_params(T, f1, H, false, L->d_err);
+    p.out = u;
+    p.ldo = f1;
+    p.bias = static_cast<const bf16*>(w->b_fc1);
+    if ((rc = run_gemm(L, -1, mt::kEpiStore, hn, H, w->w_fc1, f1, T, f1, H, p, st))) return rc;
+  }
+  if ((e = mt::launch_act_fwd(u, a, T, f, swiglu, st)) != cudaSuccess) return cuda_fail(e, "activation");
+
+  // ---- MLP
+  bf16 *da = bwr<bf16>(L, b, kBDa), *du = bwr<bf16>(L, b, kBDu), *dhn = bwr<bf16>(L, b, kBDhn);
+  bf16* dh = bwr<bf16>(L, b, kBDh);
+  if ((rc = linear_bwd(L, b, dy, a, w->w_fc2, T, H, f, g->w_fc2, w->b_fc2 ? g->b_fc2 : nullptr, da, st))) return rc;
+  if ((e = mt::launch_act_bwd(u, da, du, T, f, swiglu, st)) != cudaSuccess) return cuda_fail(e, "activation backward");
+  if ((rc = linear_bwd(L, b, du, hn, w->w_fc1, T, f1, H, g->w_fc1, w->b_fc1 ? g->b_fc1 : nullptr, dhn, st))) return rc;
+  if ((rc = norm_bwd(L, b, dhn, h, w->norm2_w, dy, dh, g->norm2_w, g->norm2_b, T, st))) return rc;
+
+  // ---- output projection
+  bf16* dO = bwr<bf16>(L, b, kBDo);
+  if ((rc = linear_bwd(L, b, dh, o, w->w_o, T, H, qw, g->w_o, w->b_o ? g->b_o : nullptr, dO, st))) return rc;
+
+  // ---- attention, one head at a time: S = Q K^T, dP = dO V^T, (P, dS), dV += P^T dO,
+  //      dQ = dS K, dK += dS^T Q  (scores and dP in fp32; P and dS in bf16)
+  float *dq = bwr<float>(L, b, kBDq), *dk = bwr<float>(L, b, kBDk), *dv = bwr<float>(L, b, kBDv);
+  if ((e = cudaMemsetAsync(dk, 0, b.size[kBDk], st)) != cudaSuccess) return cuda_fail(e, "memset");
+  if ((e = cudaMemsetAsync(dv, 0, b.size[kBDv], st)) != cudaSuccess) return cuda_fail(e, "memset");
+  float *Sm = bwr<float>(L, b, kBS), *dP = bwr<float>(L, b, kBDp);
+  bf16 *P = bwr<bf16>(L, b, kBP), *dS = bwr<bf16>(L, b, kBDs), *Pt = bwr<bf16>(L, b, kBPt);
+  bf16 *dOt = bwr<bf16>(L, b, kBDoT), *Kt = bwr<bf16>(L, b, kBKT), *Qt = bwr<bf16>(L, b, kBQT);
+  const float scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+  for (int bb = 0; bb < B; ++bb) {
+    for (int hh = 0; hh < nh; ++hh) {
+      const int gg = hh / rep;
+      const bf16* Qh = q + (static_cast<size_t>(bb) * nh + hh) * S * d;
+      const bf16* Kg = k + (static_cast<size_t>(bb) * ng + gg) * S * d;
+      const bf16* Vg = qkv + static_cast<size_t>(bb) * QKV + qw + kvw + gg * d;  // pitch B*QKV
+      const bf16* dOh = dO + static_cast<size_t>(bb) * qw + hh * d;             // pitch B*qw
+      float* dQh = dq + (static_cast<size_t>(bb) * nh + hh) * S * d;
+      float* dKg = dk + (static_cast<size_t>(bb) * ng + gg) * S * d;
+      float* dVg = dv + (static_cast<size_t>(bb) * ng + gg) * S * d;
+      if ((rc = gemm_ab(L, Qh, d, Kg, d, S, S, d, nullptr, Sm, S, false, st))) return rc;
+      if ((rc = gemm_ab(L, dOh, static_cast<size_t>(B) * qw, Vg, static_cast<size_t>(B) * QKV, S, S, d, nullptr, dP, S,
+                        false, st)))
+        return rc;
+      if ((e = mt::launch_attn_bwd_rows(Sm, dP, P, dS, S, scale, st)) != cudaSuccess) return cuda_fail(e, "softmax bwd");
+      if ((rc = transpose(P, S, Pt, S, S, st))) return rc;
+      if ((rc = transpose(dOh, static_cast<size_t>(B) * qw, dOt, S, d, st))) return rc;
+      if ((rc = gemm_ab(L, Pt, S, dOt, S, S, d, S, nullptr, dVg, d, true, st))) return rc;
+      if ((rc = transpose(Kg, d, Kt, S, d, st))) return rc;
+      if ((rc = gemm_ab(L, dS, S, Kt, S, S, d, S, nullptr, dQh, d, false, st))) return rc;
+      if ((rc = transpose(dS, S, Pt, S, S, st))) return rc;
+      if ((rc = transpose(Qh, d, Qt, S, d, st))) return rc;
+      if ((rc = gemm_ab(L, Pt, S, Qt, S, S, d, S, nullptr, dKg, d, true, st))) return rc;
+    }
+  }
+  bf16* dqkv = bwr<bf16>(L, b, kBDqkv);
+  const float2* rope = L->rope_base > 0.f ? region<float2>(L, lay, kRope) : nullptr;
+  if ((e = mt::launch_rope_bwd_pack(dq, dk, dv, rope, dqkv, S, B, nh, ng, d, st)) != cudaSuccess)
+    return cuda_fail(e, "RoPE backward");
+
+  // ---- QKV projection and the input norm
+  bf16* dxn = bwr<bf16>(L, b, kBDxn);
+  if ((rc = linear_bwd(L, b, dqkv, xn, w->w_qkv, T, QKV, H, g->w_qkv, w->b_qkv ? g->b_qkv : nullptr, dxn, st)))
+    return rc;
+  return norm_bwd(L, b, dxn, x, w->norm1_w, dh, dx, g->norm1_w, g->norm1_b, T, st);
+}
+
 }  // namespace
 
 namespace mt {
@@ -956,6 +1165,35 @@ int mt_gemm_e4m3(const void* A, const void* B, void* C, int M, int N, int K, con
   p.deq_a = deq_a;
   p.deq_b = deq_b;
   int rc = run_gemm(nullptr, 0, mt::kEpiStore, A, K, B, N, M, N, K, p, static_cast<cudaStream_t>(cuda_stream), true);
+  return rc ? rc : ok();
+}
+
+int mt_layer_backward_workspace_bytes(const mt_layer* L, int seq, int batch, size_t* bytes) {
+  if (L == nullptr || bytes == nullptr) return fail(MT_ERR_INVALID_ARG, "handle or bytes is NULL");
+  if (seq <= 0 || batch <= 0) return fail(MT_ERR_INVALID_ARG, "seq and batch must be positive");
+  *bytes = bw_layout(L, seq, batch).total;
+  return ok();
+}
+
+int mt_layer_backward(mt_layer* L, const void* x, const void* dy, int seq, int batch, const mt_weights* w, void* dx,
+                      const mt_grads* g, void* cuda_stream) {
+  if (L == nullptr) return fail(MT_ERR_INVALID_ARG, "handle is NULL");
+  if (L->tp != 1) return fail(MT_ERR_UNSUPPORTED, "the backward pass is implemented for tp_size == 1");
+  if (x == nullptr || dy == nullptr || dx == nullptr || g == nullptr)
+    return fail(MT_ERR_INVALID_ARG, "x, dy, dx and grads must not be NULL");
+  if (!aligned16(x) || !aligned16(dy) || !aligned16(dx)) return fail(MT_ERR_INVALID_ARG, "x/dy/dx must be 16-byte aligned");
+  if (seq <= 0 || batch <= 0) return fail(MT_ERR_INVALID_ARG, "seq and batch must be positive");
+  if (seq % 8) return fail(MT_ERR_UNSUPPORTED, "the backward pass needs seq % 8 == 0");
+  const void* gp[] = {g->norm1_w, g->norm1_b, g->w_qkv, g->b_qkv, g->w_o, g->b_o,
+                      g->norm2_w, g->norm2_b, g->w_fc1, g->b_fc1, g->w_fc2, g->b_fc2};
+  for (const void* p : gp)
+    if (p != nullptr && !aligned16(p)) return fail(MT_ERR_INVALID_ARG, "gradient buffers must be 16-byte aligned");
+  const BwLayout b = bw_layout(L, seq, batch);
+  if (L->ws == nullptr || L->ws_bytes < b.total)
+    return fail(MT_ERR_NO_WORKSPACE, "the backward pass needs a workspace of %zu bytes", b.total);
+  int rc = check_weights(L, w, true, true);
+  if (rc) return rc;
+  rc = backward_device(L, b, x, dy, seq, batch, w, dx, g, static_cast<cudaStream_t>(cuda_stream));
   return rc ? rc : ok();
 }
 

@@ -141,6 +141,22 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
           for (int e = 0; e < 32; ++e)
             if (col + e < p.N) amax = fmaxf(amax, fabsf(v[e]));
           store_e4m3x32(p.out8 + static_cast<size_t>(row) * p.ldo, col, p.N, v, qs);
+        } else if (MODE == kEpiStore && p.out32 != nullptr) {
+          float* dst = p.out32 + static_cast<size_t>(row) * p.ldo + col;
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            if (col + 4 * g < p.N) {
+              float4 o = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+              if (p.acc32) {
+                const float4 prev = reinterpret_cast<const float4*>(dst)[g];
+                o.x += prev.x;
+                o.y += prev.y;
+                o.z += prev.z;
+                o.w += prev.w;
+              }
+              reinterpret_cast<float4*>(dst)[g] = o;
+            }
+          }
         } else {
           store_vec32(p.out + static_cast<size_t>(row) * p.ldo, col, p.N, v);
         }

@@ -50,6 +50,9 @@ struct GemmParams {
   uint8_t* out8;
   const float* q_scale;
   unsigned* amax;
+  // kEpiStore only: fp32 output to out32 (pitch ldo) instead of bf16; acc32 = 1 adds to it
+  float* out32;
+  int acc32;
   int* err;
 };
 
@@ -104,6 +107,18 @@ cudaError_t launch_norm(bool layer_norm, const bf16* x, const bf16* g, const bf1
 // Current per-tensor scaling of n (multiple of 8) bf16 values: slot[0] <- amax (float bits),
 // slot[1] <- 1/scale, q <- E4M3 codes of x * 448 / amax.
 cudaError_t launch_quantize_e4m3(const bf16* x, size_t n, uint8_t* q, float* slot, cudaStream_t stream);
+
+// ---- backward pass (backward_kernels.cu)
+cudaError_t launch_transpose(const bf16* src, size_t sp, bf16* dst, size_t dp, int R, int C, cudaStream_t st);
+cudaError_t launch_attn_bwd_rows(const float* S, const float* dP, bf16* P, bf16* dS, int n, float scale,
+                                 cudaStream_t st);
+cudaError_t launch_act_fwd(const bf16* u, bf16* a, size_t T, int f, bool swiglu, cudaStream_t st);
+cudaError_t launch_act_bwd(const bf16* u, const bf16* da, bf16* du, size_t T, int f, bool swiglu, cudaStream_t st);
+cudaError_t launch_norm_bwd(const bf16* dy, const bf16* x, const bf16* gamma, const bf16* add, bf16* out, float* grow,
+                            int T, int H, float eps, bool layer_norm, cudaStream_t st);
+cudaError_t launch_colsum(const void* src, bool f32, size_t ld, int T, int N, float* acc, bf16* out, cudaStream_t st);
+cudaError_t launch_rope_bwd_pack(const float* dq, const float* dk, const float* dv, const float2* rope, bf16* dqkv,
+                                 int S, int B, int nh, int ng, int d, cudaStream_t st);
 
 // Delayed-scaling update after an FP8 forward (state layout: see fp8_history_kernel).
 cudaError_t launch_fp8_history(float* state, int len, int pos, cudaStream_t stream);

@@ -30,6 +30,10 @@ class MtWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_FIELDS]
 
 
+class MtGrads(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_FIELDS]
+
+
 class MtFp8Weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("w_qkv", "w_o", "w_fc1", "w_fc2",
                                                 "deq_qkv", "deq_o", "deq_fc1", "deq_fc2")]
@@ -74,6 +78,11 @@ _SIGS = {
     "mt_layer_forward_packed": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
                                  ctypes.c_int, ctypes.POINTER(MtWeights), ctypes.c_void_p, ctypes.c_void_p],
                                 ctypes.c_int),
+    "mt_layer_backward_workspace_bytes": ([ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                           ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
+    "mt_layer_backward": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                           ctypes.POINTER(MtWeights), ctypes.c_void_p, ctypes.POINTER(MtGrads), ctypes.c_void_p],
+                          ctypes.c_int),
     "mt_layer_fp8_enable": ([ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
     "mt_layer_fp8_set_scales": ([ctypes.c_void_p, ctypes.POINTER(ctypes.c_float)], ctypes.c_int),
     "mt_layer_fp8_state": ([ctypes.c_void_p, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)],
@@ -213,6 +222,16 @@ def mt_sp_reduce_add_norm(partials, resid, bias, norm_w, norm_b, norm, eps, toke
                                        hidden, row0, rows, h_out, hn_out, stream))
 
 
+def mt_layer_backward_workspace_bytes(handle, seq, batch) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().mt_layer_backward_workspace_bytes(handle, seq, batch, ctypes.byref(n)))
+    return n.value
+
+
+def mt_layer_backward(handle, x, dy, seq, batch, weights: MtWeights, dx, grads: "MtGrads", stream):
+    _check(lib().mt_layer_backward(handle, x, dy, seq, batch, ctypes.byref(weights), dx, ctypes.byref(grads), stream))
+
+
 def mt_layer_fp8_enable(handle, amax_history_len=1024):
     _check(lib().mt_layer_fp8_enable(handle, int(amax_history_len)))
 
@@ -324,6 +343,21 @@ class Layer:
         mt_layer_forward_packed(self.handle, x.data_ptr(), total, cu_seqlens.data_ptr(), n, max_seqlen, weights,
                                 out.data_ptr(), self._stream(stream))
         return out
+
+    def backward(self, x, dy, seq, batch, weights: MtWeights, dx, grads: Dict[str, "object"], stream=None):
+        """dx and the weight gradients into the given torch tensors (grads: name -> tensor or None)."""
+        import torch
+        need = mt_layer_backward_workspace_bytes(self.handle, seq, batch)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(need, dtype=torch.uint8, device=x.device)
+            mt_layer_set_workspace(self.handle, self._ws.data_ptr(), self._ws.numel())
+        g = MtGrads()
+        for f in WEIGHT_FIELDS:
+            t = grads.get(f)
+            setattr(g, f, None if t is None else t.data_ptr())
+        mt_layer_backward(self.handle, x.data_ptr(), dy.data_ptr(), seq, batch, weights, dx.data_ptr(), g,
+                          self._stream(stream))
+        return dx
 
     def forward_host(self, x_host, seq, batch, weights: MtWeights, y_host, stream=None):
         self.workspace(seq, batch)
