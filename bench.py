@@ -225,6 +225,22 @@ def run_native(args):
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     flops = cfg.flops()
+    if args.backward:
+        # the backward's own algorithmic work: dX and dW of every projection (2x the forward GEMMs)
+        # and dQ, dK, dV, dP plus the recomputed scores (2.5x the causal attention); the forward
+        # recompute it also runs is not counted
+        flops = 2.0 * cfg.gemm_flops() + 2.5 * cfg.attn_flops()
+        rng = np.random.default_rng(rank + 100)
+        dyb = torch.from_numpy(synth.f32_to_bf16_bits(rng.standard_normal((cfg.tokens, cfg.hidden), dtype=np.float32))
+                               .view(np.int16)).view(torch.bfloat16).to(dev)
+        dxb = torch.empty_like(dyb)
+        grads = {k: (None if v is None else torch.empty_like(v)) for k, v in tens.items()}
+
+    def step():
+        if args.backward:
+            layer.backward(x, dyb, cfg.seq, cfg.batch, w, dxb, grads)
+        else:
+            layer.forward(x, cfg.seq, cfg.batch, w, y)
 
     def barrier():
         if world > 1:
@@ -232,7 +248,7 @@ def run_native(args):
 
     # warm-up, extended to about half a second of load so the clock samples see a busy GPU
     for _ in range(args.warmup):
-        layer.forward(x, cfg.seq, cfg.batch, w, y)
+        step()
     torch.cuda.synchronize()
     layer.status()
 
@@ -243,7 +259,7 @@ def run_native(args):
         clocks.start()
     t_end = time.perf_counter() + (0.0 if args.quick else 0.5)
     while time.perf_counter() < t_end:
-        layer.forward(x, cfg.seq, cfg.batch, w, y)
+        step()
         torch.cuda.synchronize()
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -254,7 +270,7 @@ def run_native(args):
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
         ev[i][0].record(stream)
-        layer.forward(x, cfg.seq, cfg.batch, w, y)
+        step()
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -265,7 +281,7 @@ def run_native(args):
     # end to end through the host-buffer entry point
     xh = x.cpu().pin_memory()
     yh = torch.empty(cfg.tokens, cfg.hidden, dtype=torch.bfloat16).pin_memory()
-    n_e2e = 0 if (args.quick or args.fp8) else args.steps
+    n_e2e = 0 if (args.quick or args.fp8 or args.backward) else args.steps
     for _ in range(min(2, n_e2e)):
         layer.forward_host(xh, cfg.seq, cfg.batch, w, yh)
     torch.cuda.synchronize()
@@ -296,7 +312,7 @@ def run_native(args):
     fc1_avg = fc1_ms / max(1, launches)
     f1 = cfg.fc1_out // cfg.tp
     fc1_flops = 2.0 * cfg.tokens * cfg.hidden * f1
-    achieved = fc1_flops / (fc1_avg * 1e-3) / 1e12
+    achieved = fc1_flops / (fc1_avg * 1e-3) / 1e12 if fc1_avg > 0 else None
     kernel_launches = sum(n for n, _ in prof.values())
 
     if rank != 0:
@@ -305,7 +321,7 @@ def run_native(args):
         return
 
     cpu = None
-    if world == 1 and not args.no_cpu_baseline and not args.quick and not args.fp8:
+    if world == 1 and not args.no_cpu_baseline and not args.quick and not args.fp8 and not args.backward:
         n_rows = 256
         sf, dt = oracle_sample(cfg, inp, n_rows)
         cpu = {"value": sf / dt / 1e12, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
@@ -325,7 +341,8 @@ def run_native(args):
         "tokens_per_s": world * cfg.tokens * args.steps / (total_ms * 1e-3),
         "per_kernel_ms": {k: (ms / n if n else 0.0) for k, (n, ms) in prof.items()},
         "roofline": {"kernel": "gemm_fc1 (fc1 GEMM + SwiGLU epilogue)", "bound": "tensor", "achieved": achieved,
-                     "peak": kernel_peak, "unit": "TFLOP/s", "frac": achieved / kernel_peak,
+                     "peak": kernel_peak, "unit": "TFLOP/s",
+                     "frac": achieved / kernel_peak if achieved is not None else None,
                      "traffic": (profiled_traffic("gemm_fc1_swiglu_llama8b.md")
                                  if cfg.name == "llama8b" and not args.fp8 else None),
                      "algorithmic_bytes": 2.0 * cfg.tokens * cfg.hidden + 2.0 * f1 * cfg.hidden
@@ -380,6 +397,8 @@ def main():
     ap.add_argument("--impl", choices=("native", "reference"), default="native")
     ap.add_argument("--workload", default="llama8b", choices=sorted(synth.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="time mt_layer_backward (forward recompute + gradients) instead of the forward")
     ap.add_argument("--fp8", action="store_true",
                     help="time the FP8 (E4M3) forward instead of the bf16 one (no host-buffer pass, no CPU baseline)")
     ap.add_argument("--quick", action="store_true",
