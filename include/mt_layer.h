@@ -234,6 +234,13 @@ int mt_layer_profile_read(mt_layer* L, int* launches, double* total_ms);
  * Device pointers, 16-byte aligned; K % 8 == 0 and N % 8 == 0. */
 int mt_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, void* cuda_stream);
 
+/* GEMM kernel choice for every later launch in the process (all handles): 0 automatic (the
+ * default: pairs of CTAs sharing one M = 256 tcgen05.mma per 256 x 256 tile when M > 128 and the
+ * GEMM fills at least one wave of SM pairs, else one CTA per 128 x 256 tile), 1 one CTA per tile
+ * always, 2 CTA pairs wherever M > 128.  Both kernels compute the same fp32 sums in the same K
+ * order.  A tuning and testing control; returns MT_ERR_INVALID_ARG for other values. */
+int mt_gemm_set_pairing(int mode);
+
 /* Sequence-parallel epilogue of a row-parallel linear, for one rank's sequence slice
  * ("Megatron-LM 深度学习与源码分析文档" Part 2 §4 Sequence Parallel: after a RowParallel linear the
  * output is reduce-scattered back to sequence-sharded activations, and LayerNorm/dropout/residual

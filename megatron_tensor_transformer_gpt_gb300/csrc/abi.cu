@@ -4,6 +4,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -240,16 +241,30 @@ mt::GemmParams gemm_params(int M, int N, int K, bool swiglu, int* err) {
   return p;
 }
 
-// Tile order and tail split of one GEMM (see GemmParams).
+// Which GEMM kernel runs (mt_gemm_set_pairing): 0 automatic, 1 one CTA per tile always,
+// 2 CTA pairs wherever M > 128.
+std::atomic<int> g_pairing{0};
+
+// Kernel, tile order and tail split of one GEMM (see GemmParams).
+//   Kernel: CTA pairs (256 x 256 tiles) when M > 128 and there is at least one full wave of them
+//   on the SM pairs; one CTA per 128 x 256 tile otherwise.
 //   Order: if one operand fits in about 56 MB of the 129 MB L2 it is kept resident (the other is
 //   streamed once); otherwise bands of m-tiles (or n-tiles) of about 56 MB, whichever streams
 //   fewer bytes from DRAM.
-//   Split: the tiles of the last partial wave on the SMs are cut into 2 or 4 pieces along N when
-//   the pieces still fit in one wave (QKV pieces keep whole heads; SwiGLU pieces at least 64
-//   outputs, the smallest TMA box used).
+//   Split: the tiles of the last partial wave are cut into 2 or 4 pieces along N when the pieces
+//   still fit in one wave (QKV pieces keep whole heads; a CTA stages at least 64 B rows, the
+//   smallest TMA box used).
 void plan_gemm(mt::GemmParams& p, int mode, int head_dim) {
+  const int sms = mt::num_sms();
+  const int tiles_m2 = (p.M + 255) / 256;
+  const int mode_pairs = g_pairing.load();
+  p.pair = mode_pairs != 1 && p.M > 128 && (mode_pairs == 2 || tiles_m2 * p.tiles_n >= mt::gemm_pair_slots()) ? 1 : 0;
+  if (p.pair) {
+    p.tiles_m = tiles_m2;
+    p.num_tiles = p.tiles_m * p.tiles_n;
+  }
   const double budget = 56.0 * 1024 * 1024;
-  const double a_tile = 128.0 * p.K * 2, b_tile = 256.0 * p.K * 2;
+  const double a_tile = (p.pair ? 256.0 : 128.0) * p.K * 2, b_tile = 256.0 * p.K * 2;
   const double a_all = a_tile * p.tiles_m, b_all = b_tile * p.tiles_n;
   if (a_all <= budget) {
     p.band_m = 1;
@@ -265,19 +280,20 @@ void plan_gemm(mt::GemmParams& p, int mode, int head_dim) {
     p.band_m = tm <= tn ? 1 : 0;
     p.band = tm <= tn ? std::min(gm, p.tiles_m) : std::min(gn, p.tiles_n);
   }
-  const int sms = mt::num_sms();
-  const int waves = p.num_tiles / sms;
-  const int rest = p.num_tiles - waves * sms;
-  int max_split = 4;
+  const int workers = p.pair ? mt::gemm_pair_slots() : sms;
+  const int waves = p.num_tiles / workers;
+  const int rest = p.num_tiles - waves * workers;
+  // pairs: each CTA stages half of a piece's B rows (SwiGLU: all of its gate or up rows)
+  int max_split = p.pair ? 2 : 4;
   if (mode == mt::kEpiSwiglu) max_split = 2;
-  if (mode == mt::kEpiQkv) max_split = std::max(1, 256 / head_dim);
+  if (mode == mt::kEpiQkv) max_split = std::min(max_split, std::max(1, 256 / head_dim));
   p.split = 1;
   for (int s = max_split; s >= 2; s /= 2)
-    if (rest > 0 && rest * s <= sms) {
+    if (rest > 0 && rest * s <= workers) {
       p.split = s;
       break;
     }
-  p.full_units = p.split > 1 ? waves * sms : p.num_tiles;
+  p.full_units = p.split > 1 ? waves * workers : p.num_tiles;
   p.num_units = p.full_units + (p.split > 1 ? rest * p.split : 0);
 }
 
@@ -1056,6 +1072,12 @@ int mt_layer_profile_read(mt_layer* L, int* launches, double* total_ms) {
   }
   L->recs.clear();
   return rc ? rc : ok();
+}
+
+int mt_gemm_set_pairing(int mode) {
+  if (mode < 0 || mode > 2) return fail(MT_ERR_INVALID_ARG, "pairing mode must be 0, 1 or 2 (got %d)", mode);
+  g_pairing.store(mode);
+  return ok();
 }
 
 int mt_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, void* cuda_stream) {

@@ -436,6 +436,181 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
+// ------------------------------------------------------------------ CTA-pair kernel
+// The same GEMM with 256 x 256 tiles on a cluster of two CTAs (cta_group::2).  Each CTA stages
+// its own 128 rows of A and half of the tile's B rows (N / 2; for SwiGLU the even CTA holds the
+// gate rows and the odd one the up rows), so a CTA moves 32 KB per K block instead of 48 KB and
+// fits P_STAGES stages.  The even CTA's thread issues the M = 256 MMAs, which write each CTA's
+// 128 accumulator rows into that CTA's tensor memory; its commits arrive on the barriers of both
+// CTAs.  Both CTAs' TMA copies complete on the even CTA's `full` barriers, and both CTAs'
+// epilogue warps release an accumulator on the even CTA's `tempty` barrier (count 8).
+constexpr int P_STAGES = 6;
+constexpr int P_B_BYTES = 128 * BK * 2;  // up to 128 B rows per CTA
+constexpr int P_STAGE_BYTES = A_BYTES + P_B_BYTES;
+constexpr size_t P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + 256;
+
+template <int MODE, bool F8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmB64, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = base;
+  uint8_t* sB = base + P_STAGES * A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + P_STAGES * P_STAGE_BYTES);
+  // bars: full[P_STAGES] | empty[P_STAGES] | tmem_full[2] | tmem_empty[2] | drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * P_STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (P_STAGES + s); };
+  auto tfull = [&](int a) { return bar0 + 8u * (2 * P_STAGES + a); };
+  auto tempty = [&](int a) { return bar0 + 8u * (2 * P_STAGES + 2 + a); };
+  const uint32_t drain = bar0 + 8u * (2 * P_STAGES + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P_STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull(a), 1);
+      mbar_init(tempty(a), 8);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(&tmA);
+    tma_prefetch(&tmB);
+    tma_prefetch(&tmB64);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  // both CTAs' barriers are initialised and the tensor memory is allocated before either uses them
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  constexpr int KB = F8 ? 128 : BK;
+  const int num_kb = (p.K + KB - 1) / KB;
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int u = pair; ok && u < p.num_units; u += npairs) {
+        const Unit w = decode_unit(p, u);
+        const int m0 = w.tm * (2 * BM) + static_cast<int>(rank) * BM;
+        const int width = unit_width<MODE>(w);
+        const int c0 = unit_col0<MODE>(w);
+        // this CTA's B rows: SwiGLU gate (even CTA) or up (odd CTA) rows [c0, c0 + width);
+        // otherwise half of [c0, c0 + width)
+        const int b_rows = MODE == kEpiSwiglu ? width : width / 2;
+        const int b_row0 = MODE == kEpiSwiglu ? c0 + (rank ? p.b_row_step : 0) : c0 + static_cast<int>(rank) * b_rows;
+        const CUtensorMap* mb = b_rows == 128 ? &tmB : &tmB64;
+        const uint32_t pair_bytes = 2u * (A_BYTES + b_rows * 128);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(empty(stage), phase ^ 1u, p.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = map_to_rank(full(stage), 0);
+          if (leader) mbar_arrive_expect_tx(full(stage), pair_bytes);
+          tma_load_2d_pair(smem_u32(sA + stage * A_BYTES), &tmA, fb, kb * KB, m0);
+          tma_load_2d_pair(smem_u32(sB + stage * P_B_BYTES), mb, fb, kb * KB, b_row0);
+          ++issued;
+          if (++stage == P_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok && leader) {  // the pair's copies in flight complete on these barriers
+        for (int s = 0; s < P_STAGES; ++s)
+          if (s < stage || issued >= P_STAGES)
+            mbar_wait_slow(full(s), s < stage ? phase : (phase ^ 1u), nullptr, nullptr, kDrainLimitNs);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      int stage = 0, it = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int u = pair; ok && u < p.num_units; u += npairs, ++it) {
+        const Unit w = decode_unit(p, u);
+        const int width = unit_width<MODE>(w);
+        const int n_mma = MODE == kEpiSwiglu ? 2 * width : width;
+        const uint32_t idesc = F8 ? idesc_e4m3(2 * BM, n_mma) : idesc_bf16(2 * BM, n_mma);
+        const int acc = it & 1;
+        const uint32_t use = (it >> 1) & 1;
+        if (!mbar_wait(tempty(acc), use ^ 1u, p.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(full(stage), phase, p.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sw128_desc(smem_u32(sA + stage * A_BYTES));
+          const uint64_t bd = sw128_desc(smem_u32(sB + stage * P_B_BYTES));
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            if (F8)
+              mma_e4m3_pair(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb | k) ? 1u : 0u);
+            else
+              mma_bf16_pair(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb | k) ? 1u : 0u);
+          mma_commit_pair(empty(stage));
+          if (++stage == P_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) mma_commit_pair(tfull(acc));
+      }
+      // No MMA may still read either CTA's shared memory or write tensor memory at the exit.
+      mma_commit_pair(drain);
+      mbar_wait_slow(drain, 0, nullptr, nullptr, ok ? kWaitLimitNs : kDrainLimitNs);
+    }
+  } else {
+    const int quad = warp & 3;
+    int it = 0;
+    for (int u = pair; u < p.num_units; u += npairs, ++it) {
+      const int acc = it & 1;
+      const uint32_t use = (it >> 1) & 1;
+      const bool ok = mbar_wait(tfull(acc), use, p.err, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const Unit w = decode_unit(p, u);
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
+      epilogue_tile<MODE, F8>(p, tacc, w.tm * (2 * BM) + static_cast<int>(rank) * BM, unit_col0<MODE>(w),
+                              unit_width<MODE>(w), quad * 32 + lane);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty(acc), 0));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the pair's MMAs, copies and epilogue reads are over in both CTAs
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
 template <int MODE, bool F8>
 cudaError_t launch_mode(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB64, const GemmParams& p,
                         cudaStream_t stream) {
@@ -443,8 +618,17 @@ cudaError_t launch_mode(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<MODE, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(SMEM_BYTES));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_pair_kernel<MODE, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(P_SMEM_BYTES));
     if (e != cudaSuccess) return e;
     configured = true;
+  }
+  if (p.pair) {
+    const int pairs = gemm_pair_slots();
+    const int grid = 2 * (p.num_units < pairs ? p.num_units : pairs);
+    gemm_pair_kernel<MODE, F8><<<grid, 192, P_SMEM_BYTES, stream>>>(tmA, tmB, tmB64, p);
+    return cudaGetLastError();
   }
   const int grid = p.num_units < num_sms() ? p.num_units : num_sms();
   gemm_kernel<MODE, F8><<<grid, 192, SMEM_BYTES, stream>>>(tmA, tmB, tmB64, p);
@@ -465,6 +649,36 @@ cudaError_t launch_kind(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB
 }
 
 }  // namespace
+
+int gemm_pair_slots() {
+  static int n = 0;
+  if (n == 0) {
+    int slots = 0;
+    cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<kEpiStore, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(P_SMEM_BYTES));
+    if (e == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
+      cfg.blockDim = dim3(192, 1, 1);
+      cfg.dynamicSmemBytes = P_SMEM_BYTES;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      e = cudaOccupancyMaxActiveClusters(&slots, gemm_pair_kernel<kEpiStore, false>, &cfg);
+    }
+    if (e != cudaSuccess || slots <= 0) {
+      cudaGetLastError();  // clear a failed query; fall back to one cluster per two SMs
+      slots = num_sms() / 2;
+    }
+    n = slots < num_sms() / 2 ? slots : num_sms() / 2;
+    if (n < 1) n = 1;
+  }
+  return n;
+}
 
 size_t gemm_smem_bytes() { return SMEM_BYTES; }
 

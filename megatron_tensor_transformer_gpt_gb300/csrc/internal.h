@@ -30,6 +30,9 @@ struct GemmParams {
   // Work units: [0, full_units) are whole tiles; the tiles after them (the last, partial wave)
   // are cut into `split` pieces along N so that the tail wave is shorter.  num_units in total.
   int full_units, split, num_units;
+  // CTA pairs (pair = 1): tiles are 256 x 256 and computed by a cluster of two CTAs sharing one
+  // M = 256 MMA (tiles_m counts 256-row tiles); otherwise one CTA per 128 x 256 tile.
+  int pair;
   bf16* out;
   int ldo;
   const bf16* bias;   // [N] (SwiGLU: [2N]) or null
@@ -89,6 +92,9 @@ struct SpParams {
 
 // Number of SMs of the current device (cached).
 int num_sms();
+// Clusters of two GEMM CTAs that can be resident at once on the current device (cached; at most
+// num_sms() / 2): the persistent grid of the CTA-pair GEMM.
+int gemm_pair_slots();
 
 // Kernel launchers; return a cudaError_t from the launch.
 // fp8 = true: A and B are E4M3 (tensor maps of bytes, boxes 128 wide).

@@ -67,6 +67,7 @@ _SIGS = {
     "mt_layer_status": ([ctypes.c_void_p], ctypes.c_int),
     "mt_last_error": ([], ctypes.c_char_p),
     "mt_layer_destroy": ([ctypes.c_void_p], None),
+    "mt_gemm_set_pairing": ([ctypes.c_int], ctypes.c_int),
     "mt_gemm_bf16": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                       ctypes.c_void_p], ctypes.c_int),
     "mt_selftest_bounded_wait": ([ctypes.c_int], ctypes.c_int),
@@ -259,6 +260,10 @@ def mt_quantize_e4m3(src, n, dst, amax_deq, stream):
 
 def mt_gemm_e4m3(A, B, C, M, N, K, deq_a, deq_b, stream):
     _check(lib().mt_gemm_e4m3(A, B, C, M, N, K, deq_a, deq_b, stream))
+
+
+def mt_gemm_set_pairing(mode):
+    _check(lib().mt_gemm_set_pairing(mode))
 
 
 def mt_gemm_bf16(A, B, C, M, N, K, stream):

@@ -91,3 +91,11 @@ def test_last_error_is_cleared_by_success_and_thread_local(lib):
     th.start()
     th.join()
     assert seen == [""]
+
+
+def test_gemm_pairing_mode_is_checked(lib):
+    assert lib.mt_gemm_set_pairing(3) == ml.MT_ERR_INVALID_ARG
+    assert lib.mt_gemm_set_pairing(-1) == ml.MT_ERR_INVALID_ARG
+    assert "pairing" in ml.mt_last_error()
+    for mode in (1, 2, 0):                 # 0 (automatic) is left in place
+        assert lib.mt_gemm_set_pairing(mode) == ml.MT_OK
