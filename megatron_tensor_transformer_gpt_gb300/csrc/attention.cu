@@ -27,6 +27,20 @@ namespace mt {
 namespace {
 
 constexpr int BQ = 128, BKV = 128;
+static_assert(BKV == 128, "a row of S is read with one 128-column TMEM load");
+
+// Maximum of a row of S (BKV scores in registers) over eight independent chains of three-input
+// maxima (chain k takes elements 2k and 2k+1 of every 16), so the reduction is not one long chain.
+__device__ __forceinline__ float row_max(const float* s) {
+  float m8[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) m8[k] = fmaxf(s[2 * k], s[2 * k + 1]);
+#pragma unroll
+  for (int i = 16; i < BKV; i += 16)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m8[k] = fmax3(m8[k], s[i + 2 * k], s[i + 2 * k + 1]);
+  return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+}
 
 // What one CTA works on: query block qb of a sequence whose rows start at q_row0 - qb*128 and
 // whose keys start at kv_row0 (rows of the [b, head, s, d] q/k buffers), v^T columns at v_col0,
@@ -236,8 +250,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       tc_fence_after();
       float s[BKV];
-#pragma unroll
-      for (int cc = 0; cc < BKV / 32; ++cc) tmem_ld32(tmem_base + lane_off + sb * BKV + cc * 32, s + cc * 32);
+      tmem_ld128(tmem_base + lane_off + sb * BKV, s);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free(sb));
@@ -246,9 +259,7 @@ __global__ void __launch_bounds__(192, 1)
         for (int i = 0; i < BKV; ++i)
           if (i > r) s[i] = -INFINITY;
       }
-      float mx = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < BKV; i += 2) mx = fmax3(mx, s[i], s[i + 1]);
+      const float mx = row_max(s);
       const float m_new = fmaxf(m_used, mx * c);
       if (j > 0) {  // P_{j-1} V_{j-1} finished: P may be overwritten and O is stable
         w = mbar_wait(o_done, (j - 1) & 1, p.err, abort_flag);
@@ -336,30 +347,35 @@ __global__ void __launch_bounds__(192, 1)
 // ------------------------------------------------------------------ two heads of one group per CTA
 // The variant used when each kv group serves an even number of query heads (GQA/MQA): the CTA
 // holds the Q tiles of two heads of the same group for one 128-row query block, so every K/V tile
-// it loads feeds both (half the K/V traffic of one head per CTA).  Two softmax warpgroups (one per
-// head) alternate with the tensor core: while one computes P, the MMAs of the other run.
-//   TMEM (512 columns): head t uses columns [256t, 256t+128) for S_j, overwritten in place by
-//   P_j (bf16 pairs, 64 columns) which the P V MMA reads from TMEM, and [256t+128, +d) for O.
-//   K and V have separate 2-stage rings: K_j is released once both S MMAs of block j are done,
-//   V_j once both P V MMAs are.
+// it loads feeds both (half the K/V traffic of one head per CTA).
+//   TMEM: head t's scores S_t in columns [256t, 256t+128) and its output O_t in [256t+128, +d).
+//   The softmax warps of a head read S_t into registers and release it at once (s_free), so the
+//   tensor core computes S_t(j+1) while they turn S_t(j) into P_t(j); P goes to shared memory (fp16,
+//   128-byte swizzle, per head) and O_t += P_t V_j reads it from there.
+//   Shared memory: Q of both heads, a two-slot K ring, one V slot and the two P tiles.  The
+//   producer keeps K two blocks ahead of V: K_{j+2} may load once both S(j) are done, V_{j+1} once
+//   both P V(j) are.
 //   10 warps put three warps on some SM sub-partitions, whose 16K-register files then allow 168
-//   registers per thread: P is converted and stored in two halves to stay within that.
+//   registers per thread.
 template <int D>
 struct Geo2 {
-  static constexpr int ATOM = 128 * 128;
-  static constexpr int Q_BYTES = BQ * D * 2;  // per head
+  static constexpr int ATOM = 128 * 128;        // [128 rows x 64 fp16/bf16] swizzle block, 16 KB
+  static constexpr int Q_BYTES = BQ * D * 2;    // per head
   static constexpr int K_BYTES = BKV * D * 2;
-  static constexpr int V_ATOM = D * 128;
+  static constexpr int V_ATOM = D * 128;        // [d rows x 64 keys]
   static constexpr int V_BYTES = 2 * V_ATOM;
+  static constexpr int P_BYTES = BQ * BKV * 2;  // per head: two key halves of 16 KB
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = 2 * Q_BYTES;
   static constexpr int OFF_V = OFF_K + 2 * K_BYTES;
-  static constexpr int OFF_BAR = OFF_V + 2 * V_BYTES;
+  static constexpr int OFF_P = OFF_V + V_BYTES;
+  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
   static constexpr size_t SMEM_USED = 1024 + OFF_BAR + 256;
   static constexpr size_t SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;  // one CTA per SM (TMEM)
   static constexpr uint32_t IDESC_S = idesc_bf16(BQ, BKV);
   static constexpr uint32_t IDESC_O = idesc_f16(BQ, D);  // fp16 P and v^T
 };
+static_assert(Geo2<128>::SMEM_USED <= 232448, "attention tiles exceed the shared memory of a CTA");
 
 template <int D>
 __global__ void __launch_bounds__(320, 1)
@@ -369,22 +385,24 @@ __global__ void __launch_bounds__(320, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + G::OFF_BAR);
-  // bars: q_full | k_full[2] | k_empty[2] | v_full[2] | v_empty[2] | s_full[2] | p_full[2] | o_done[2] | drain
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  // bars: q_full | k_full[2] | k_empty[2] | v_full | v_empty | s_full[2] | s_free[2] | p_full[2] |
+  //       o_done[2] | drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
   const uint32_t q_full = bar0;
   auto k_full = [&](int i) { return bar0 + 8u * (1 + i); };
   auto k_empty = [&](int i) { return bar0 + 8u * (3 + i); };
-  auto v_full = [&](int i) { return bar0 + 8u * (5 + i); };
-  auto v_empty = [&](int i) { return bar0 + 8u * (7 + i); };
-  auto s_full = [&](int t) { return bar0 + 8u * (9 + t); };
+  const uint32_t v_full = bar0 + 8u * 5, v_empty = bar0 + 8u * 6;
+  auto s_full = [&](int t) { return bar0 + 8u * (7 + t); };
+  auto s_free = [&](int t) { return bar0 + 8u * (9 + t); };
   auto p_full = [&](int t) { return bar0 + 8u * (11 + t); };
   auto o_done = [&](int t) { return bar0 + 8u * (13 + t); };
   const uint32_t drain = bar0 + 8u * 15;
   auto sQa = [&](int t) { return smem_u32(base + G::OFF_Q + t * G::Q_BYTES); };
   auto sKa = [&](int st) { return smem_u32(base + G::OFF_K + st * G::K_BYTES); };
-  auto sVa = [&](int st) { return smem_u32(base + G::OFF_V + st * G::V_BYTES); };
+  const uint32_t sVa = smem_u32(base + G::OFF_V);
+  auto sPa = [&](int t) { return smem_u32(base + G::OFF_P + t * G::P_BYTES); };
 
   Work wk;
   if (!decode_work(p, p.nh >> 1, 2, wk)) return;  // uniform over the CTA, before any barrier or TMEM use
@@ -398,12 +416,13 @@ __global__ void __launch_bounds__(320, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(k_full(i), 1);
       mbar_init(k_empty(i), 1);
-      mbar_init(v_full(i), 1);
-      mbar_init(v_empty(i), 1);
       mbar_init(s_full(i), 1);
+      mbar_init(s_free(i), 4);
       mbar_init(p_full(i), 4);
       mbar_init(o_done(i), 1);
     }
+    mbar_init(v_full, 1);
+    mbar_init(v_empty, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -432,36 +451,38 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int a = 0; a < D / 64; ++a)
           tma_load_3d(sQa(t) + a * G::ATOM, &tmQ, q_full, a * 64, wk.q_row0, b * p.nh + h0 + t);
+      // load order K0, K1, V0, K2, V1, K3, V2, ...: K_{j+2} before V_{j+1}
       int issued_k = 0, issued_v = 0;
       bool ok = true;
-      for (int j = 0; ok && j < nkv; ++j) {
+      auto load_k = [&](int j) -> bool {
         const int st = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!mbar_wait(k_empty(st), ph ^ 1u, p.err, abort_flag)) {
-          ok = false;
-          break;
-        }
+        if (!mbar_wait(k_empty(st), ((j >> 1) & 1) ^ 1u, p.err, abort_flag)) return false;
         mbar_arrive_expect_tx(k_full(st), G::K_BYTES);
 #pragma unroll
         for (int a = 0; a < D / 64; ++a)
           tma_load_3d(sKa(st) + a * G::ATOM, &tmK, k_full(st), a * 64, wk.kv_row0 + j * BKV, b * p.ng + g);
         ++issued_k;
-        if (!mbar_wait(v_empty(st), ph ^ 1u, p.err, abort_flag)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(v_full(st), G::V_BYTES);
+        return true;
+      };
+      auto load_v = [&](int j) -> bool {
+        if (!mbar_wait(v_empty, (j & 1) ^ 1u, p.err, abort_flag)) return false;
+        mbar_arrive_expect_tx(v_full, G::V_BYTES);
 #pragma unroll
         for (int a = 0; a < 2; ++a)
-          tma_load_3d(sVa(st) + a * G::V_ATOM, &tmV, v_full(st), wk.v_col0 + j * BKV + a * 64, 0, b * p.ng + g);
+          tma_load_3d(sVa + a * G::V_ATOM, &tmV, v_full, wk.v_col0 + j * BKV + a * 64, 0, b * p.ng + g);
         ++issued_v;
+        return true;
+      };
+      ok = load_k(0) && (nkv < 2 || load_k(1));
+      for (int j = 0; ok && j < nkv; ++j) {
+        ok = load_v(j);
+        if (ok && j + 2 < nkv) ok = load_k(j + 2);
       }
       if (!ok) {  // let this CTA's own copies in flight land
         mbar_wait_slow(q_full, 0, nullptr, nullptr, kDrainLimitNs);
         for (int j = issued_k - 1; j >= 0 && j >= issued_k - 2; --j)
           mbar_wait_slow(k_full(j & 1), (j >> 1) & 1, nullptr, nullptr, kDrainLimitNs);
-        for (int j = issued_v - 1; j >= 0 && j >= issued_v - 2; --j)
-          mbar_wait_slow(v_full(j & 1), (j >> 1) & 1, nullptr, nullptr, kDrainLimitNs);
+        if (issued_v > 0) mbar_wait_slow(v_full, (issued_v - 1) & 1, nullptr, nullptr, kDrainLimitNs);
       }
     }
   } else if (warp == 1) {
@@ -482,8 +503,26 @@ __global__ void __launch_bounds__(320, 1)
         mma_commit(k_empty(0));
       }
       for (int j = 0; ok && j < nkv; ++j) {
-        const int st = j & 1;
-        if (!mbar_wait(v_full(st), (j >> 1) & 1, p.err, abort_flag)) {
+        // S(j+1) of both heads as soon as their softmax has taken S(j) into registers
+        if (j + 1 < nkv) {
+          const int st1 = (j + 1) & 1;
+          if (!mbar_wait(k_full(st1), ((j + 1) >> 1) & 1, p.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (!mbar_wait(s_free(t), j & 1, p.err, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(t, st1);
+          }
+          if (!ok) break;
+          mma_commit(k_empty(st1));
+        }
+        // O_t += P_t(j) V_j once the softmax has written P_t(j)
+        if (!mbar_wait(v_full, j & 1, p.err, abort_flag)) {
           ok = false;
           break;
         }
@@ -495,31 +534,14 @@ __global__ void __launch_bounds__(320, 1)
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < BKV / 16; ++k) {
-            const uint32_t va = sVa(st) + (k >> 2) * G::V_ATOM + (k & 3) * 32;
-            mma_bf16_ts(tO(t), tS(t) + 8u * k, sw128_desc(va), G::IDESC_O, (j > 0 || k > 0) ? 1u : 0u);
+            const uint32_t pa = sPa(t) + (k >> 2) * G::ATOM + (k & 3) * 32;
+            const uint32_t va = sVa + (k >> 2) * G::V_ATOM + (k & 3) * 32;
+            mma_bf16_ss(tO(t), sw128_desc(pa), sw128_desc(va), G::IDESC_O, (j > 0 || k > 0) ? 1u : 0u);
           }
           mma_commit(o_done(t));
         }
         if (!ok) break;
-        mma_commit(v_empty(st));
-        if (j + 1 < nkv) {
-          const int st1 = (j + 1) & 1;
-          if (!mbar_wait(k_full(st1), ((j + 1) >> 1) & 1, p.err, abort_flag)) {
-            ok = false;
-            break;
-          }
-          for (int t = 0; t < 2; ++t) {
-            // S_t(j+1) overwrites the columns P_t(j) V_j reads: wait until that MMA is done.
-            if (!mbar_wait(o_done(t), j & 1, p.err, abort_flag)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            issue_s(t, st1);
-          }
-          if (!ok) break;
-          mma_commit(k_empty(st1));
-        }
+        mma_commit(v_empty);
       }
       mma_commit(drain);
       mbar_wait_slow(drain, 0, nullptr, nullptr, ok ? kWaitLimitNs : kDrainLimitNs);
@@ -532,6 +554,8 @@ __global__ void __launch_bounds__(320, 1)
     const int h = h0 + t;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float c = p.scale_log2;
+    uint8_t* prow = base + G::OFF_P + t * G::P_BYTES + r * 128;
+    const int sw = r & 7;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
@@ -542,26 +566,28 @@ __global__ void __launch_bounds__(320, 1)
       }
       tc_fence_after();
       float s[BKV];
-#pragma unroll
-      for (int cc = 0; cc < BKV / 32; ++cc) tmem_ld32(tS(t) + lane_off + cc * 32, s + cc * 32);
+      tmem_ld128(tS(t) + lane_off, s);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free(t));  // the tensor core may overwrite S_t now
       if (j == qb) {
 #pragma unroll
         for (int i = 0; i < BKV; ++i)
           if (i > r) s[i] = -INFINITY;
       }
-      float mx = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < BKV; i += 2) mx = fmax3(mx, s[i], s[i + 1]);
+      const float mx = row_max(s);
       const float m_new = fmaxf(m_used, mx * c);
+      if (j > 0) {  // P_t(j-1) V_{j-1} finished: P_t may be overwritten and O_t is stable
+        w = mbar_wait(o_done(t), (j - 1) & 1, p.err, abort_flag);
+        if (!__all_sync(0xffffffffu, w)) {
+          ok = false;
+          break;
+        }
+      }
       if (__any_sync(0xffffffffu, m_new > m_used + 8.0f)) {
         const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m_used - m_new);
         l *= alpha;
         if (j > 0) {
-          w = mbar_wait(o_done(t), (j - 1) & 1, p.err, abort_flag);
-          if (!__all_sync(0xffffffffu, w)) {
-            ok = false;
-            break;
-          }
           tc_fence_after();
 #pragma unroll 1
           for (int cc = 0; cc < D / 32; ++cc) {
@@ -577,22 +603,26 @@ __global__ void __launch_bounds__(320, 1)
       // P = 2^(s c - m) in packed halves: one fp32x2 FMA, one fp16x2 conversion and one fp16x2
       // exponential per pair of scores (the argument is at most 8 after the lazy rescaling, so its
       // fp16 rounding moves P by under 0.6%, the order of P's own 16-bit rounding); row sums in four
-      // fp16x2 partial sums per 64 keys, widened to fp32 once per block.
+      // fp16x2 partial sums per 64 keys, widened to fp32 once per block.  Each 8-key chunk is stored
+      // at its swizzled position of the 128-byte rows the P V MMA reads.
       float rs = 0.f;
       const float2 cc = make_float2(c, c), mm = make_float2(-m_used, -m_used);
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        uint32_t pk[32];
         __half2 acc[4] = {__float2half2_rn(0.f), __float2half2_rn(0.f), __float2half2_rn(0.f),
                           __float2half2_rn(0.f)};
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float2 xy = ffma2(make_float2(s[64 * hf + 2 * i], s[64 * hf + 2 * i + 1]), cc, mm);
-          const uint32_t e = ex2_f16x2(pack_f16x2(xy.x, xy.y));
-          acc[i & 3] = __hadd2(acc[i & 3], *reinterpret_cast<const __half2*>(&e));
-          pk[i] = e;
+        for (int ch = 0; ch < 8; ++ch) {
+          uint32_t e4[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int i = 64 * hf + 8 * ch + 2 * q;
+            const float2 xy = ffma2(make_float2(s[i], s[i + 1]), cc, mm);
+            e4[q] = ex2_f16x2(pack_f16x2(xy.x, xy.y));
+            acc[q] = __hadd2(acc[q], *reinterpret_cast<const __half2*>(&e4[q]));
+          }
+          *reinterpret_cast<uint4*>(prow + hf * G::ATOM + ((ch ^ sw) << 4)) = make_uint4(e4[0], e4[1], e4[2], e4[3]);
         }
-        tmem_st32_raw(tS(t) + lane_off + 32 * hf, pk);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const float2 f = __half22float2(acc[k]);
@@ -600,6 +630,7 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
       l += rs;
+      fence_proxy_async_smem();  // the P stores become visible to the tensor core
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full(t));
