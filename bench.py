@@ -344,13 +344,13 @@ def run_native(args):
                      "peak": kernel_peak, "unit": "TFLOP/s",
                      "frac": achieved / kernel_peak if achieved is not None else None,
                      "traffic": (profiled_traffic("gemm_fc1_swiglu_llama8b.md")
-                                 if cfg.name == "llama8b" and not args.fp8 else None),
+                                 if cfg.name == "llama8b" and not args.fp8 and not args.backward else None),
                      "algorithmic_bytes": 2.0 * cfg.tokens * cfg.hidden + 2.0 * f1 * cfg.hidden
                                           + 2.0 * cfg.tokens * (f1 // 2 if cfg.act == "swiglu" else f1),
                      "peak_note": (f"{peak_src} cuBLAS bf16 burst x 2 (nominal E4M3 ratio)" if args.fp8
                                    else f"{peak_src} cuBLAS bf16 burst")},
         "cpu_baseline": cpu,
-        "e2e": None if args.quick else {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": cfg.tokens * cfg.hidden * 2,
+        "e2e": None if n_e2e == 0 else {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": cfg.tokens * cfg.hidden * 2,
                 "d2h_bytes_per_step": cfg.tokens * cfg.hidden * 2, "ms_per_step": total_e2e / args.steps},
         "gpu_launches": kernel_launches,
         "clocks": clk,
