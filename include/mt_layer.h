@@ -217,15 +217,22 @@ const char* mt_last_error(void);
 
 void mt_layer_destroy(mt_layer* L);
 
-/* Per-kernel timing.  While enabled, every kernel this handle launches is bracketed by a pair of
- * CUDA events on its stream.  Kernel slots: 0 RoPE table, 1 norm1, 2 QKV GEMM, 3 attention,
- * 4 output-projection GEMM, 5 norm2, 6 fc1 GEMM, 7 fc2 GEMM (MT_PROFILE_SLOTS).  Up to 8192
- * launches are kept.  mt_layer_profile_read waits for the recorded events, writes per slot the
- * number of launches and their summed milliseconds into the caller's arrays (MT_PROFILE_SLOTS
- * entries each) and clears the record. */
+/* Per-kernel timing.  Kernel slots: 0 RoPE table, 1 norm1, 2 QKV GEMM, 3 attention,
+ * 4 output-projection GEMM, 5 norm2, 6 fc1 GEMM, 7 fc2 GEMM (MT_PROFILE_SLOTS).  slot_mask selects
+ * the slots whose launches this handle brackets with a pair of CUDA events on their stream (bit s
+ * for slot s; MT_PROFILE_ALL for every slot, 0 to stop); values outside 0..MT_PROFILE_ALL return
+ * MT_ERR_INVALID_ARG.  Each event pair costs a little time, so a caller timing whole steps
+ * selects only the slots it needs.  Up to 8192 launches are kept.  mt_layer_profile_read waits for
+ * the recorded events, writes per slot the number of launches and their summed milliseconds into
+ * the caller's arrays (MT_PROFILE_SLOTS entries each) and clears the record. */
 #define MT_PROFILE_SLOTS 8
-int mt_layer_profile_enable(mt_layer* L, int enable);
+#define MT_PROFILE_ALL ((1 << MT_PROFILE_SLOTS) - 1)
+int mt_layer_profile_enable(mt_layer* L, int slot_mask);
 int mt_layer_profile_read(mt_layer* L, int* launches, double* total_ms);
+
+/* Number of kernels this handle has launched since it was created (every forward, backward and
+ * staged call, profiled or not), written to *count.  MT_ERR_INVALID_ARG on NULL arguments. */
+int mt_layer_launch_count(const mt_layer* L, unsigned long long* count);
 
 /* ---- utility entry points (kernel-level; used by the parity tests) -------------------- */
 

@@ -31,7 +31,8 @@ struct mt_layer {
   float* d_f8;
   int f8_len, f8_pos;
   // per-kernel timing (mt_layer_profile_*)
-  bool profiling;
+  int profile_mask;  // bit s: bracket the launches of kernel slot s with events
+  unsigned long long launch_count;  // kernels launched by this handle (mt_layer_launch_count)
   struct Rec {
     int slot;
     cudaEvent_t a, b;
@@ -77,7 +78,7 @@ cudaEvent_t pool_event(mt_layer* L) {
   return e;
 }
 
-// Brackets one kernel launch with events when the handle is profiling.
+// Counts one kernel launch of the handle and brackets it with events when its slot is profiled.
 struct Timed {
   mt_layer* L;
   cudaStream_t st;
@@ -85,7 +86,8 @@ struct Timed {
   cudaEvent_t a = nullptr;
   int slot;
   Timed(mt_layer* l, int s, cudaStream_t stream)
-      : L(l), st(stream), on(l != nullptr && s >= 0 && l->profiling && l->recs.size() < kMaxRecords), slot(s) {
+      : L(l), st(stream), on(l != nullptr && s >= 0 && s < MT_PROFILE_SLOTS && ((l->profile_mask >> s) & 1) && l->recs.size() < kMaxRecords), slot(s) {
+    if (l != nullptr) ++l->launch_count;
     if (on) {
       a = pool_event(L);
       cudaEventRecord(a, st);
@@ -99,6 +101,11 @@ struct Timed {
     }
   }
 };
+
+// Counts a kernel launch that no profiling slot covers.
+void count_launch(mt_layer* L) {
+  if (L != nullptr) ++L->launch_count;
+}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -380,6 +387,7 @@ int run_attention_block(mt_layer* L, const Layout& lay, const void* x, int S, in
     if (e == cudaSuccess) {
       pos = region<int>(L, lay, kPos);
       vcol = region<int>(L, lay, kVcol);
+      count_launch(L);
       e = mt::launch_packed_index(pk->cu, pk->num_seqs, T, pk->max_seqlen, lay.seq_pad, pos, vcol, L->d_err, st);
     }
     if (e != cudaSuccess) return cuda_fail(e, "packed-sample index");
@@ -603,6 +611,7 @@ int forward_device_fp8(mt_layer* L, const Layout& lay, const void* x, int S, int
   if ((rc = run_gemm(L, kSlotFc2, L->tp == 1 ? mt::kEpiResid : mt::kEpiStore, a8, L->f_r, w8->w_fc2, H, T, H, L->f_r,
                      p, st, true)))
     return rc;
+  count_launch(L);
   e = mt::launch_fp8_history(L->d_f8, L->f8_len, L->f8_pos, st);
   if (e != cudaSuccess) return cuda_fail(e, "amax history update");
   L->f8_pos = (L->f8_pos + 1) % L->f8_len;
@@ -625,6 +634,7 @@ int gemm_ab(mt_layer* L, const void* A, size_t lda, const void* Bm, size_t ldb, 
   p.acc32 = acc32 ? 1 : 0;
   p.ldo = static_cast<int>(ldo);
   plan_gemm(p, mt::kEpiStore, 0);
+  count_launch(L);
   cudaError_t e = mt::launch_gemm(mt::kEpiStore, false, ta, tb, tb64, p, st);
   return e == cudaSuccess ? MT_OK : cuda_fail(e, "backward GEMM launch");
 }
@@ -686,7 +696,8 @@ T* bwr(const mt_layer* L, const BwLayout& b, BwRegion r) {
 }
 
 // dst = src^T for a bf16 [R, C] matrix with pitch sp into a dense [C, R] buffer.
-int transpose(const void* src, size_t sp, void* dst, int R, int C, cudaStream_t st) {
+int transpose(mt_layer* L, const void* src, size_t sp, void* dst, int R, int C, cudaStream_t st) {
+  count_launch(L);
   cudaError_t e = mt::launch_transpose(static_cast<const bf16*>(src), sp, static_cast<bf16*>(dst), R, R, C, st);
   return e == cudaSuccess ? MT_OK : cuda_fail(e, "transpose launch");
 }
@@ -699,17 +710,18 @@ int linear_bwd(mt_layer* L, const BwLayout& b, const void* dY, const void* X, co
   if (dW != nullptr) {
     bf16* dYt = bwr<bf16>(L, b, kBAt);
     bf16* Xt = bwr<bf16>(L, b, kBBt);
-    if ((rc = transpose(dY, N, dYt, M, N, st))) return rc;
-    if ((rc = transpose(X, K, Xt, M, K, st))) return rc;
+    if ((rc = transpose(L, dY, N, dYt, M, N, st))) return rc;
+    if ((rc = transpose(L, X, K, Xt, M, K, st))) return rc;
     if ((rc = gemm_ab(L, dYt, M, Xt, M, N, K, M, dW, nullptr, K, false, st))) return rc;
   }
   if (db != nullptr) {
+    count_launch(L);
     cudaError_t e = mt::launch_colsum(dY, false, N, M, N, bwr<float>(L, b, kBAcc), static_cast<bf16*>(db), st);
     if (e != cudaSuccess) return cuda_fail(e, "bias gradient");
   }
   if (dX != nullptr) {
     bf16* Wt = bwr<bf16>(L, b, kBWt);
-    if ((rc = transpose(W, K, Wt, N, K, st))) return rc;
+    if ((rc = transpose(L, W, K, Wt, N, K, st))) return rc;
     if ((rc = gemm_ab(L, dY, N, Wt, N, M, K, N, dX, nullptr, K, false, st))) return rc;
   }
   return MT_OK;
@@ -719,13 +731,18 @@ int norm_bwd(mt_layer* L, const BwLayout& b, const void* dy, const void* x, cons
              void* out, void* dgamma, void* dbeta, int T, cudaStream_t st) {
   const int H = L->hidden;
   float* grow = bwr<float>(L, b, kBGrow);
+  count_launch(L);
   cudaError_t e = mt::launch_norm_bwd(static_cast<const bf16*>(dy), static_cast<const bf16*>(x),
                                       static_cast<const bf16*>(gamma), static_cast<const bf16*>(add),
                                       static_cast<bf16*>(out), grow, T, H, L->eps, L->norm == MT_NORM_LAYER, st);
-  if (e == cudaSuccess && dgamma != nullptr)
+  if (e == cudaSuccess && dgamma != nullptr) {
+    count_launch(L);
     e = mt::launch_colsum(grow, true, H, T, H, bwr<float>(L, b, kBAcc), static_cast<bf16*>(dgamma), st);
-  if (e == cudaSuccess && dbeta != nullptr && L->norm == MT_NORM_LAYER)
+  }
+  if (e == cudaSuccess && dbeta != nullptr && L->norm == MT_NORM_LAYER) {
+    count_launch(L);
     e = mt::launch_colsum(dy, false, H, T, H, bwr<float>(L, b, kBAcc), static_cast<bf16*>(dbeta), st);
+  }
   return e == cudaSuccess ? MT_OK : cuda_fail(e, "norm backward");
 }
 
@@ -742,6 +759,7 @@ int backward_device(mt_layer* L, const BwLayout& b, const void* x, const void* d
   if ((rc = run_attention_block(L, lay, x, S, B, w, h, mt::kEpiResid, st))) return rc;
   bf16 *xn = region<bf16>(L, lay, kXn), *hn = region<bf16>(L, lay, kHn), *o = region<bf16>(L, lay, kO);
   bf16 *q = region<bf16>(L, lay, kQ), *k = region<bf16>(L, lay, kK);
+  count_launch(L);
   e = mt::launch_norm(L->norm == MT_NORM_LAYER, h, static_cast<const bf16*>(w->norm2_w),
                       static_cast<const bf16*>(w->norm2_b), hn, T, H, L->eps, st);
   if (e != cudaSuccess) return cuda_fail(e, "norm2 launch");
@@ -758,12 +776,14 @@ int backward_device(mt_layer* L, const BwLayout& b, const void* x, const void* d
     p.bias = static_cast<const bf16*>(w->b_fc1);
     if ((rc = run_gemm(L, -1, mt::kEpiStore, hn, H, w->w_fc1, f1, T, f1, H, p, st))) return rc;
   }
+  count_launch(L);
   if ((e = mt::launch_act_fwd(u, a, T, f, swiglu, st)) != cudaSuccess) return cuda_fail(e, "activation");
 
   // ---- MLP
   bf16 *da = bwr<bf16>(L, b, kBDa), *du = bwr<bf16>(L, b, kBDu), *dhn = bwr<bf16>(L, b, kBDhn);
   bf16* dh = bwr<bf16>(L, b, kBDh);
   if ((rc = linear_bwd(L, b, dy, a, w->w_fc2, T, H, f, g->w_fc2, w->b_fc2 ? g->b_fc2 : nullptr, da, st))) return rc;
+  count_launch(L);
   if ((e = mt::launch_act_bwd(u, da, du, T, f, swiglu, st)) != cudaSuccess) return cuda_fail(e, "activation backward");
   if ((rc = linear_bwd(L, b, du, hn, w->w_fc1, T, f1, H, g->w_fc1, w->b_fc1 ? g->b_fc1 : nullptr, dhn, st))) return rc;
   if ((rc = norm_bwd(L, b, dhn, h, w->norm2_w, dy, dh, g->norm2_w, g->norm2_b, T, st))) return rc;
@@ -795,19 +815,21 @@ int backward_device(mt_layer* L, const BwLayout& b, const void* x, const void* d
       if ((rc = gemm_ab(L, dOh, static_cast<size_t>(B) * qw, Vg, static_cast<size_t>(B) * QKV, S, S, d, nullptr, dP, S,
                         false, st)))
         return rc;
+      count_launch(L);
       if ((e = mt::launch_attn_bwd_rows(Sm, dP, P, dS, S, scale, st)) != cudaSuccess) return cuda_fail(e, "softmax bwd");
-      if ((rc = transpose(P, S, Pt, S, S, st))) return rc;
-      if ((rc = transpose(dOh, static_cast<size_t>(B) * qw, dOt, S, d, st))) return rc;
+      if ((rc = transpose(L, P, S, Pt, S, S, st))) return rc;
+      if ((rc = transpose(L, dOh, static_cast<size_t>(B) * qw, dOt, S, d, st))) return rc;
       if ((rc = gemm_ab(L, Pt, S, dOt, S, S, d, S, nullptr, dVg, d, true, st))) return rc;
-      if ((rc = transpose(Kg, d, Kt, S, d, st))) return rc;
+      if ((rc = transpose(L, Kg, d, Kt, S, d, st))) return rc;
       if ((rc = gemm_ab(L, dS, S, Kt, S, S, d, S, nullptr, dQh, d, false, st))) return rc;
-      if ((rc = transpose(dS, S, Pt, S, S, st))) return rc;
-      if ((rc = transpose(Qh, d, Qt, S, d, st))) return rc;
+      if ((rc = transpose(L, dS, S, Pt, S, S, st))) return rc;
+      if ((rc = transpose(L, Qh, d, Qt, S, d, st))) return rc;
       if ((rc = gemm_ab(L, Pt, S, Qt, S, S, d, S, nullptr, dKg, d, true, st))) return rc;
     }
   }
   bf16* dqkv = bwr<bf16>(L, b, kBDqkv);
   const float2* rope = L->rope_base > 0.f ? region<float2>(L, lay, kRope) : nullptr;
+  count_launch(L);
   if ((e = mt::launch_rope_bwd_pack(dq, dk, dv, rope, dqkv, S, B, nh, ng, d, st)) != cudaSuccess)
     return cuda_fail(e, "RoPE backward");
 
@@ -1047,9 +1069,16 @@ void mt_layer_destroy(mt_layer* L) {
   delete L;
 }
 
-int mt_layer_profile_enable(mt_layer* L, int enable) {
+int mt_layer_profile_enable(mt_layer* L, int slot_mask) {
   if (L == nullptr) return fail(MT_ERR_INVALID_ARG, "handle is NULL");
-  L->profiling = enable != 0;
+  if (slot_mask < 0 || slot_mask > MT_PROFILE_ALL) return fail(MT_ERR_INVALID_ARG, "slot mask 0x%x out of range", slot_mask);
+  L->profile_mask = slot_mask;
+  return ok();
+}
+
+int mt_layer_launch_count(const mt_layer* L, unsigned long long* count) {
+  if (L == nullptr || count == nullptr) return fail(MT_ERR_INVALID_ARG, "NULL argument");
+  *count = L->launch_count;
   return ok();
 }
 
@@ -1337,7 +1366,7 @@ extern "C" int mt_layer_forward_static(int hidden, int heads, int query_groups, 
   L.f1_r = act == MT_ACT_SWIGLU ? 2 * L.f_r : L.f_r;
   L.q_w = L.nh_r * head_dim;
   L.kv_w = L.ng_r * head_dim;
-  L.profiling = false;
+  L.profile_mask = 0;
   if (seq <= 0 || batch <= 0) return fail(MT_ERR_INVALID_ARG, "seq and batch must be positive (got %d, %d)", seq, batch);
   const size_t need = layout_for(&L, seq, batch).total;
   const size_t have = static_cast<size_t>(MT_STATIC_AREA_BYTES) - kStaticHeader;

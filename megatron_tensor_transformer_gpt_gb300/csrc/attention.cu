@@ -126,6 +126,8 @@ __global__ void __launch_bounds__(192, 1)
   auto sKa = [&](int st) { return smem_u32(base + G::OFF_K + st * G::K_BYTES); };
   auto sVa = [&](int st) { return smem_u32(base + G::OFF_V + st * G::V_BYTES); };
 
+  pdl_wait();  // q, k, v^T (and cu_seqlens) are written by the kernels before
+  pdl_trigger();
   Work wk;
   if (!decode_work(p, p.nh, 1, wk)) return;  // uniform over the CTA, before any barrier or TMEM use
   const int qb = wk.qb, b = wk.b, h = wk.h;
@@ -404,6 +406,8 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t sVa = smem_u32(base + G::OFF_V);
   auto sPa = [&](int t) { return smem_u32(base + G::OFF_P + t * G::P_BYTES); };
 
+  pdl_wait();  // q, k, v^T (and cu_seqlens) are written by the kernels before
+  pdl_trigger();
   Work wk;
   if (!decode_work(p, p.nh >> 1, 2, wk)) return;  // uniform over the CTA, before any barrier or TMEM use
   const int qb = wk.qb, b = wk.b, h0 = wk.h;
@@ -689,8 +693,7 @@ cudaError_t launch_d2(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUte
     configured = true;
   }
   const unsigned grid = static_cast<unsigned>(p.num_qb) * (p.cu ? p.num_seqs : p.batch) * (p.nh / 2);
-  attn2_kernel<D><<<grid, 320, Geo2<D>::SMEM, stream>>>(tmQ, tmK, tmV, p);
-  return cudaGetLastError();
+  return launch_pdl(attn2_kernel<D>, dim3(grid), dim3(320), Geo2<D>::SMEM, stream, tmQ, tmK, tmV, p);
 }
 
 template <int D>
@@ -704,8 +707,7 @@ cudaError_t launch_d(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUten
     configured = true;
   }
   const unsigned grid = static_cast<unsigned>(p.num_qb) * (p.cu ? p.num_seqs : p.batch) * p.nh;
-  attn_kernel<D><<<grid, 192, Geo<D>::SMEM, stream>>>(tmQ, tmK, tmV, p);
-  return cudaGetLastError();
+  return launch_pdl(attn_kernel<D>, dim3(grid), dim3(192), Geo<D>::SMEM, stream, tmQ, tmK, tmV, p);
 }
 
 }  // namespace

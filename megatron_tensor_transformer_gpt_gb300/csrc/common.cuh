@@ -29,6 +29,16 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// ---------------------------------------------------------------------------------- stream order
+// Programmatic dependent launch: a kernel launched with programmatic stream serialization may
+// start while the previous kernel of the stream is finishing.  pdl_wait() returns once the grids
+// it depends on have completed and their writes are visible (at once for a kernel launched
+// without the attribute); every kernel calls it before its first global load or store.
+// pdl_trigger() lets the next kernel be scheduled; each kernel calls it after its own wait, so a
+// grid's dependents launch only once all its CTAs are resident and past their wait.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

@@ -46,6 +46,8 @@ __global__ void __launch_bounds__(1024) norm_kernel(const bf16* __restrict__ x, 
                                                     float eps, uint8_t* __restrict__ y8, const float* q_scale,
                                                     unsigned* amax) {
   __shared__ float red[32];
+  pdl_wait();
+  pdl_trigger();
   const size_t row = blockIdx.x;
   const int nvec = H >> 3;
   const uint4* xr = reinterpret_cast<const uint4*>(x + row * H);
@@ -128,12 +130,11 @@ cudaError_t launch_norm_ln(const bf16* x, const bf16* g, const bf16* b, bf16* y,
   if (nvec >= 256) {  // two vectors per thread
     const int threads = ((nvec + 1) / 2 + 31) / 32 * 32;
     if (threads > 1024) return cudaErrorInvalidValue;
-    norm_kernel<2, LN, OUT8><<<rows, threads, 0, stream>>>(x, g, b, y, H, eps, y8, q_scale, amax);
+    return launch_pdl(norm_kernel<2, LN, OUT8>, dim3(rows), dim3(threads), 0, stream, x, g, b, y, H, eps, y8, q_scale, amax);
   } else {
     const int threads = (nvec + 31) / 32 * 32;
-    norm_kernel<1, LN, OUT8><<<rows, threads, 0, stream>>>(x, g, b, y, H, eps, y8, q_scale, amax);
+    return launch_pdl(norm_kernel<1, LN, OUT8>, dim3(rows), dim3(threads), 0, stream, x, g, b, y, H, eps, y8, q_scale, amax);
   }
-  return cudaGetLastError();
 }
 
 // Largest |x| of n bf16 values into *amax (float bits; the caller zeroes it first).
@@ -190,6 +191,8 @@ __global__ void fp8_history_kernel(float* state, int len, int pos) {
 // (cos, sin) of s * theta_i for s < seq, i < half.  The angle is formed and reduced modulo 2*pi
 // in double precision, so the single-precision sine/cosine act on an argument in [-pi, pi].
 __global__ void rope_table_kernel(float2* __restrict__ tab, const double* __restrict__ theta, int seq, int half) {
+  pdl_wait();
+  pdl_trigger();
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= seq * half) return;
   const int s = idx / half, i = idx - s * half;
@@ -362,8 +365,7 @@ cudaError_t launch_fp8_history(float* state, int len, int pos, cudaStream_t stre
 cudaError_t launch_rope_table(float2* table, const double* theta, int seq, int half, cudaStream_t stream) {
   const int n = seq * half;
   if (n <= 0) return cudaSuccess;
-  rope_table_kernel<<<(n + 255) / 256, 256, 0, stream>>>(table, theta, seq, half);
-  return cudaGetLastError();
+  return launch_pdl(rope_table_kernel, dim3((n + 255) / 256), dim3(256), 0, stream, table, theta, seq, half);
 }
 
 cudaError_t launch_wait_selftest(int* err, unsigned long long limit_ns, cudaStream_t stream) {

@@ -316,6 +316,8 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();  // the setup above overlaps the end of the previous kernel
+  pdl_trigger();
   const uint32_t tmem_base = *tmem_slot;
   constexpr int KB = F8 ? 128 : BK;  // K elements per stage: one 128-byte swizzle row either way
   const int num_kb = (p.K + KB - 1) / KB;
@@ -497,6 +499,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   tc_fence_before();
   cluster_sync();
   tc_fence_after();
+  pdl_wait();  // the setup above overlaps the end of the previous kernel
+  pdl_trigger();
   const uint32_t tmem_base = *tmem_slot;
   constexpr int KB = F8 ? 128 : BK;
   const int num_kb = (p.K + KB - 1) / KB;
@@ -627,12 +631,10 @@ cudaError_t launch_mode(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
   if (p.pair) {
     const int pairs = gemm_pair_slots();
     const int grid = 2 * (p.num_units < pairs ? p.num_units : pairs);
-    gemm_pair_kernel<MODE, F8><<<grid, 192, P_SMEM_BYTES, stream>>>(tmA, tmB, tmB64, p);
-    return cudaGetLastError();
+    return launch_pdl(gemm_pair_kernel<MODE, F8>, dim3(grid), dim3(192), P_SMEM_BYTES, stream, tmA, tmB, tmB64, p);
   }
   const int grid = p.num_units < num_sms() ? p.num_units : num_sms();
-  gemm_kernel<MODE, F8><<<grid, 192, SMEM_BYTES, stream>>>(tmA, tmB, tmB64, p);
-  return cudaGetLastError();
+  return launch_pdl(gemm_kernel<MODE, F8>, dim3(grid), dim3(192), SMEM_BYTES, stream, tmA, tmB, tmB64, p);
 }
 
 template <bool F8>

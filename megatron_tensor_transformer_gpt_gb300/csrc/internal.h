@@ -90,6 +90,25 @@ struct SpParams {
   bf16 *h, *hn;                    // [rows, H]
 };
 
+// Launch with programmatic stream serialization (the kernel may start while the previous kernel of
+// the stream finishes; the kernels of this library wait for it with griddepcontrol.wait before
+// touching global memory).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Number of SMs of the current device (cached).
 int num_sms();
 // Clusters of two GEMM CTAs that can be resident at once on the current device (cached; at most

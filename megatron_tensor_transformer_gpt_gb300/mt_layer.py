@@ -72,6 +72,7 @@ _SIGS = {
                       ctypes.c_void_p], ctypes.c_int),
     "mt_selftest_bounded_wait": ([ctypes.c_int], ctypes.c_int),
     "mt_layer_profile_enable": ([ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
+    "mt_layer_launch_count": ([ctypes.c_void_p, ctypes.POINTER(ctypes.c_ulonglong)], ctypes.c_int),
     "mt_layer_profile_read": ([ctypes.c_void_p, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_double)],
                               ctypes.c_int),
     "mt_layer_workspace_bytes_packed": ([ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -195,8 +196,19 @@ def mt_layer_destroy(handle):
     lib().mt_layer_destroy(handle)
 
 
-def mt_layer_profile_enable(handle, enable: bool):
-    _check(lib().mt_layer_profile_enable(handle, 1 if enable else 0))
+def mt_layer_launch_count(handle) -> int:
+    n = ctypes.c_ulonglong(0)
+    _check(lib().mt_layer_launch_count(handle, ctypes.byref(n)))
+    return n.value
+
+
+PROFILE_ALL = (1 << 8) - 1
+
+
+def mt_layer_profile_enable(handle, slots=True):
+    """slots: True (every kernel slot), False (none) or an int bit mask over the slots."""
+    mask = PROFILE_ALL if slots is True else (0 if slots is False else int(slots))
+    _check(lib().mt_layer_profile_enable(handle, mask))
 
 
 def mt_layer_profile_read(handle):

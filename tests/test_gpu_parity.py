@@ -236,6 +236,30 @@ def test_deterministic_and_host_path_matches():
     assert torch.equal(y1.cpu(), yh)
 
 
+def test_launch_count_and_profile_mask():
+    """A dense forward launches eight kernels; a slot mask brackets only the selected slot."""
+    cfg = small()
+    inp = synth.make_inputs(cfg, seed=5)
+    dl = DeviceLayer(cfg, inp)
+    x = to_dev(inp["x"]).reshape(cfg.tokens, cfg.hidden)
+    dl.forward(x)
+    torch.cuda.synchronize()
+    n0 = ml.mt_layer_launch_count(dl.layer.handle)
+    fc1 = ml.PROFILE_SLOTS.index("gemm_fc1")
+    ml.mt_layer_profile_enable(dl.layer.handle, 1 << fc1)
+    dl.forward(x)
+    dl.forward(x)
+    torch.cuda.synchronize()
+    prof = ml.mt_layer_profile_read(dl.layer.handle)
+    ml.mt_layer_profile_enable(dl.layer.handle, False)
+    assert ml.mt_layer_launch_count(dl.layer.handle) - n0 == 16
+    assert prof["gemm_fc1"][0] == 2 and prof["gemm_fc1"][1] > 0
+    assert all(n == 0 for k, (n, _) in prof.items() if k != "gemm_fc1")
+    with pytest.raises(ml.MtError):
+        ml.mt_layer_profile_enable(dl.layer.handle, 1 << 8)
+    dl.close()
+
+
 def test_output_guard_regions_untouched():
     cfg = small(batch=1, seq=200)
     inp = synth.make_inputs(cfg, seed=5)
