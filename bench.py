@@ -333,8 +333,13 @@ def run_native(args):
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline and not args.quick and not args.fp8 and not args.backward:
+        # about 10 s of CPU work: rows from the end of the sequence (the costliest under the causal
+        # mask), doubled until the oracle runs that long or covers the whole layer
         n_rows = 256
         sf, dt = oracle_sample(cfg, inp, n_rows)
+        while dt < 10.0 and n_rows < cfg.tokens:
+            n_rows = min(cfg.tokens, 2 * n_rows)
+            sf, dt = oracle_sample(cfg, inp, n_rows)
         cpu = {"value": sf / dt / 1e12, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
                "sample": f"float64 NumPy oracle: K/V of all {cfg.tokens} tokens + the whole layer for the last "
                          f"{n_rows} rows ({sf / 1e9:.1f} GFLOP algorithmic, {dt:.1f} s)"}
