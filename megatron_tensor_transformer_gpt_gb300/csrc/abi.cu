@@ -370,7 +370,7 @@ int check_call(const mt_layer* L, const void* in, const void* out, int S, int B,
 // Attention block: norm1 -> QKV GEMM (+bias, RoPE, scatter) -> flash attention -> output projection.
 // out_mode kEpiStore writes the rank's partial; kEpiResid writes h = x + Y + b_o.
 int run_attention_block(mt_layer* L, const Layout& lay, const void* x, int S, int B, const mt_weights* w, void* out,
-                        int out_mode, cudaStream_t st, const Packed* pk = nullptr) {
+                        int out_mode, cudaStream_t st, const Packed* pk = nullptr, float* lse = nullptr) {
   const int T = S * B, H = L->hidden, d = L->head_dim;
   cudaError_t e;
   float2* rope = nullptr;
@@ -439,6 +439,7 @@ int run_attention_block(mt_layer* L, const Layout& lay, const void* x, int S, in
   ap.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
   ap.o = o;
   ap.ldo = L->q_w;
+  ap.lse = lse;
   ap.err = L->d_err;
   {
     Timed t(L, kSlotAttn, st);
@@ -641,7 +642,7 @@ int gemm_ab(mt_layer* L, const void* A, size_t lda, const void* Bm, size_t ldb, 
 
 enum BwRegion {
   kBQkv = 0, kBU, kBA, kBDa, kBDu, kBDhn, kBDh, kBDo, kBDq, kBDk, kBDv, kBDqkv, kBDxn, kBGrow, kBAcc,
-  kBS, kBDp, kBP, kBDs, kBPt, kBDoT, kBKT, kBQT, kBWt, kBAt, kBBt, kBNum
+  kBLse, kBDsum, kBDoH, kBVh, kBDoT, kBKT, kBQT, kBWt, kBAt, kBBt, kBNum
 };
 
 struct BwLayout {
@@ -670,14 +671,16 @@ BwLayout bw_layout(const mt_layer* L, int S, int B) {
   b.size[kBDxn] = T * H * 2;
   b.size[kBGrow] = T * H * 4;
   b.size[kBAcc] = maxc * 4;
-  b.size[kBS] = static_cast<size_t>(S) * S * 4;
-  b.size[kBDp] = static_cast<size_t>(S) * S * 4;
-  b.size[kBP] = static_cast<size_t>(S) * S * 2;
-  b.size[kBDs] = static_cast<size_t>(S) * S * 2;
-  b.size[kBPt] = static_cast<size_t>(S) * S * 2;
-  b.size[kBDoT] = d * S * 2;
-  b.size[kBKT] = d * S * 2;
-  b.size[kBQT] = d * S * 2;
+  // attention backward: row statistics, head-major dO and V, transposed Q, dO and K ([z][d][S_pad])
+  const size_t sp = (static_cast<size_t>(S) + 7) / 8 * 8, zq = static_cast<size_t>(B) * L->nh_r,
+               zk = static_cast<size_t>(B) * L->ng_r;
+  b.size[kBLse] = zq * S * 4;
+  b.size[kBDsum] = zq * S * 4;
+  b.size[kBDoH] = zq * S * d * 2;
+  b.size[kBVh] = zk * S * d * 2;
+  b.size[kBDoT] = zq * d * sp * 2;
+  b.size[kBKT] = zk * d * sp * 2;
+  b.size[kBQT] = zq * d * sp * 2;
   b.size[kBWt] = std::max(std::max(QKV * H, H * qw), std::max(f1 * H, H * f)) * 2;
   b.size[kBAt] = maxc * T * 2;
   b.size[kBBt] = maxc * T * 2;
@@ -756,7 +759,8 @@ int backward_device(mt_layer* L, const BwLayout& b, const void* x, const void* d
   cudaError_t e;
   // ---- forward recompute: xn, q, k (after RoPE), o, h (attention block), hn, plain qkv, u, a
   bf16* h = region<bf16>(L, lay, kH);
-  if ((rc = run_attention_block(L, lay, x, S, B, w, h, mt::kEpiResid, st))) return rc;
+  if ((rc = run_attention_block(L, lay, x, S, B, w, h, mt::kEpiResid, st, nullptr, bwr<float>(L, b, kBLse))))
+    return rc;
   bf16 *xn = region<bf16>(L, lay, kXn), *hn = region<bf16>(L, lay, kHn), *o = region<bf16>(L, lay, kO);
   bf16 *q = region<bf16>(L, lay, kQ), *k = region<bf16>(L, lay, kK);
   count_launch(L);
@@ -792,40 +796,65 @@ int backward_device(mt_layer* L, const BwLayout& b, const void* x, const void* d
   bf16* dO = bwr<bf16>(L, b, kBDo);
   if ((rc = linear_bwd(L, b, dh, o, w->w_o, T, H, qw, g->w_o, w->b_o ? g->b_o : nullptr, dO, st))) return rc;
 
-  // ---- attention, one head at a time: S = Q K^T, dP = dO V^T, (P, dS), dV += P^T dO,
-  //      dQ = dS K, dK += dS^T Q  (scores and dP in fp32; P and dS in bf16)
+  // ---- attention, flash-style: P and dS are rebuilt tile by tile from the row log-sum-exp the
+  //      forward recompute wrote; fp32 dQ, dK, dV
   float *dq = bwr<float>(L, b, kBDq), *dk = bwr<float>(L, b, kBDk), *dv = bwr<float>(L, b, kBDv);
-  if ((e = cudaMemsetAsync(dk, 0, b.size[kBDk], st)) != cudaSuccess) return cuda_fail(e, "memset");
-  if ((e = cudaMemsetAsync(dv, 0, b.size[kBDv], st)) != cudaSuccess) return cuda_fail(e, "memset");
-  float *Sm = bwr<float>(L, b, kBS), *dP = bwr<float>(L, b, kBDp);
-  bf16 *P = bwr<bf16>(L, b, kBP), *dS = bwr<bf16>(L, b, kBDs), *Pt = bwr<bf16>(L, b, kBPt);
+  float *lse = bwr<float>(L, b, kBLse), *dsum = bwr<float>(L, b, kBDsum);
+  bf16 *dOh = bwr<bf16>(L, b, kBDoH), *Vh = bwr<bf16>(L, b, kBVh);
   bf16 *dOt = bwr<bf16>(L, b, kBDoT), *Kt = bwr<bf16>(L, b, kBKT), *Qt = bwr<bf16>(L, b, kBQT);
-  const float scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
-  for (int bb = 0; bb < B; ++bb) {
-    for (int hh = 0; hh < nh; ++hh) {
-      const int gg = hh / rep;
-      const bf16* Qh = q + (static_cast<size_t>(bb) * nh + hh) * S * d;
-      const bf16* Kg = k + (static_cast<size_t>(bb) * ng + gg) * S * d;
-      const bf16* Vg = qkv + static_cast<size_t>(bb) * QKV + qw + kvw + gg * d;  // pitch B*QKV
-      const bf16* dOh = dO + static_cast<size_t>(bb) * qw + hh * d;             // pitch B*qw
-      float* dQh = dq + (static_cast<size_t>(bb) * nh + hh) * S * d;
-      float* dKg = dk + (static_cast<size_t>(bb) * ng + gg) * S * d;
-      float* dVg = dv + (static_cast<size_t>(bb) * ng + gg) * S * d;
-      if ((rc = gemm_ab(L, Qh, d, Kg, d, S, S, d, nullptr, Sm, S, false, st))) return rc;
-      if ((rc = gemm_ab(L, dOh, static_cast<size_t>(B) * qw, Vg, static_cast<size_t>(B) * QKV, S, S, d, nullptr, dP, S,
-                        false, st)))
-        return rc;
-      count_launch(L);
-      if ((e = mt::launch_attn_bwd_rows(Sm, dP, P, dS, S, scale, st)) != cudaSuccess) return cuda_fail(e, "softmax bwd");
-      if ((rc = transpose(L, P, S, Pt, S, S, st))) return rc;
-      if ((rc = transpose(L, dOh, static_cast<size_t>(B) * qw, dOt, S, d, st))) return rc;
-      if ((rc = gemm_ab(L, Pt, S, dOt, S, S, d, S, nullptr, dVg, d, true, st))) return rc;
-      if ((rc = transpose(L, Kg, d, Kt, S, d, st))) return rc;
-      if ((rc = gemm_ab(L, dS, S, Kt, S, S, d, S, nullptr, dQh, d, false, st))) return rc;
-      if ((rc = transpose(L, dS, S, Pt, S, S, st))) return rc;
-      if ((rc = transpose(L, Qh, d, Qt, S, d, st))) return rc;
-      if ((rc = gemm_ab(L, Pt, S, Qt, S, S, d, S, nullptr, dKg, d, true, st))) return rc;
-    }
+  const size_t sp = (static_cast<size_t>(S) + 7) / 8 * 8;
+  const int zq = B * nh, zk = B * ng;
+  const size_t sd = static_cast<size_t>(S) * d;
+  struct Slice {
+    bool tr;
+    const bf16* src;
+    size_t pitch, sb, sh;
+    int zdiv, Z;
+    bf16* dst;
+    size_t dp;
+  } slices[] = {
+      {false, dO, static_cast<size_t>(B) * qw, static_cast<size_t>(qw), static_cast<size_t>(d), nh, zq, dOh, static_cast<size_t>(d)},
+      {true, dO, static_cast<size_t>(B) * qw, static_cast<size_t>(qw), static_cast<size_t>(d), nh, zq, dOt, sp},
+      {false, qkv + qw + kvw, static_cast<size_t>(B) * QKV, static_cast<size_t>(QKV), static_cast<size_t>(d), ng, zk, Vh,
+       static_cast<size_t>(d)},
+      {true, q, static_cast<size_t>(d), sd, 0, 1, zq, Qt, sp},
+      {true, k, static_cast<size_t>(d), sd, 0, 1, zk, Kt, sp},
+  };
+  for (const Slice& sl : slices) {
+    count_launch(L);
+    if ((e = mt::launch_head_slices(sl.tr, sl.src, sl.pitch, sl.sb, sl.sh, sl.zdiv, sl.Z, sl.dst, sl.dp, S, d, st)) !=
+        cudaSuccess)
+      return cuda_fail(e, "attention backward operands");
+  }
+  count_launch(L);
+  if ((e = mt::launch_row_dot(dO, o, dsum, S, B, nh, d, st)) != cudaSuccess) return cuda_fail(e, "rowsum(dO o O)");
+  {
+    CUtensorMap m[11];
+    const uint64_t Zq = zq, Zk = zk;
+    if ((rc = map_3d(&m[0], q, d, S, Zq, d, sd, 128)) || (rc = map_3d(&m[1], dOh, d, S, Zq, d, sd, 128)) ||
+        (rc = map_3d(&m[2], k, d, S, Zk, d, sd, 64)) || (rc = map_3d(&m[3], Vh, d, S, Zk, d, sd, 64)) ||
+        (rc = map_3d(&m[4], Kt, S, d, Zk, sp, d * sp, d)) || (rc = map_3d(&m[5], k, d, S, Zk, d, sd, 128)) ||
+        (rc = map_3d(&m[6], Vh, d, S, Zk, d, sd, 128)) || (rc = map_3d(&m[7], q, d, S, Zq, d, sd, 64)) ||
+        (rc = map_3d(&m[8], dOh, d, S, Zq, d, sd, 64)) || (rc = map_3d(&m[9], Qt, S, d, Zq, sp, d * sp, d)) ||
+        (rc = map_3d(&m[10], dOt, S, d, Zq, sp, d * sp, d)))
+      return rc;
+    mt::AttnBwdParams ap{};
+    ap.seq = S;
+    ap.batch = B;
+    ap.nh = nh;
+    ap.ng = ng;
+    ap.num_qb = (S + 127) / 128;
+    ap.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+    ap.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+    ap.lse = lse;
+    ap.dsum = dsum;
+    ap.dq = dq;
+    ap.dk = dk;
+    ap.dv = dv;
+    ap.err = L->d_err;
+    count_launch(L);
+    count_launch(L);
+    if ((e = mt::launch_attention_bwd(d, m, ap, st)) != cudaSuccess) return cuda_fail(e, "attention backward");
   }
   bf16* dqkv = bwr<bf16>(L, b, kBDqkv);
   const float2* rope = L->rope_base > 0.f ? region<float2>(L, lay, kRope) : nullptr;

@@ -309,6 +309,8 @@ __global__ void __launch_bounds__(192, 1)
         tc_fence_after();
         const float inv_l = 1.f / l;
         const size_t orow = (static_cast<size_t>(wk.q_row0 + r) * p.batch + b) * p.ldo + h * D;
+        if (p.lse != nullptr && row_ok)
+          p.lse[(static_cast<size_t>(b) * p.nh + h) * p.seq + wk.q_row0 + r] = m_used + log2f(l);
         const float qs = p.o8 != nullptr ? __ldg(p.q_scale) : 1.f;
         float mx = 0.f;
 #pragma unroll 1
@@ -645,6 +647,8 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after();
         const float inv_l = 1.f / l;
         const size_t orow = (static_cast<size_t>(wk.q_row0 + r) * p.batch + b) * p.ldo + h * D;
+        if (p.lse != nullptr && row_ok)
+          p.lse[(static_cast<size_t>(b) * p.nh + h) * p.seq + wk.q_row0 + r] = m_used + log2f(l);
         const float qs = p.o8 != nullptr ? __ldg(p.q_scale) : 1.f;
         float mx = 0.f;
 #pragma unroll 1

@@ -1,0 +1,611 @@
+// Backward pass of the causal GQA attention, flash-style: P and dS are formed tile by tile on
+// chip from the forward's per-row log-sum-exp and never reach memory
+// (training step of "ai阅读megatron"; activation recompute, "快速入门" §8).  For one head, with
+// scores S = Q K^T, P = softmax(S / sqrt(d)) and D_i = dO_i . O_i:
+//     dS = P o (dP - D) / sqrt(d),  dP = dO V^T,
+//     dV = P^T dO,  dK = dS^T Q,  dQ = dS K   (dK, dV summed over the query heads of a group).
+// Two kernels, each a producer warp (TMA), one MMA-issuing thread (tcgen05) and four elementwise
+// warps with one TMEM lane (row) per thread:
+//   attn_bwd_dq_kernel:   one CTA per (128 queries, head); steps over 64-key blocks j <= i:
+//                         S and dP into TMEM, dS (bf16) into shared memory, dQ += dS K in TMEM.
+//   attn_bwd_dkdv_kernel: one CTA per (128 keys, kv group); steps over the group's heads and the
+//                         64-query blocks i >= j: S^T and dP^T into TMEM, P^T and dS^T into shared
+//                         memory, dV += P^T dO and dK += dS^T Q in TMEM.
+// Every operand is K-major: the caller provides head-major copies of dO and V and the transposes
+// Q^T, dO^T and K^T (prep kernels below).
+#include "common.cuh"
+#include "internal.h"
+
+namespace mt {
+namespace {
+
+constexpr int ATOM128 = 128 * 128;  // [128 rows x 64] bf16 block with the 128-byte swizzle, 16 KB
+constexpr int ATOM64 = 64 * 128;    // [64 rows x 64] block, 8 KB
+
+// ------------------------------------------------------------------ prep
+// Batched copy (TRANS = false: dst[z][r][c]) or transpose (TRANS = true: dst[z][c][r], row pitch
+// dp) of the R x C slices src_z = src + (z / zdiv) * sb + (z % zdiv) * sh (row pitch sp).
+template <bool TRANS>
+__global__ void head_slices_kernel(const bf16* __restrict__ src, size_t sp, size_t sb, size_t sh, int zdiv,
+                                   bf16* __restrict__ dst, size_t dp, int R, int C) {
+  __shared__ uint16_t tile[32][33];
+  const int z = blockIdx.z;
+  const uint16_t* s = reinterpret_cast<const uint16_t*>(src + (z / zdiv) * sb + (z % zdiv) * sh);
+  uint16_t* d = reinterpret_cast<uint16_t*>(dst) + static_cast<size_t>(z) * (TRANS ? C * dp : R * dp);
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int r = r0 + i, c = c0 + threadIdx.x;
+    if (r < R && c < C) {
+      const uint16_t v = s[static_cast<size_t>(r) * sp + c];
+      if (TRANS)
+        tile[i][threadIdx.x] = v;
+      else
+        d[static_cast<size_t>(r) * dp + c] = v;
+    }
+  }
+  if (TRANS) {
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+      const int c = c0 + i, r = r0 + threadIdx.x;
+      if (r < R && c < C) d[static_cast<size_t>(c) * dp + r] = tile[threadIdx.x][i];
+    }
+  }
+}
+
+// D[(b * nh + h) * S + s] = sum_c dO[s b, h c] * O[s b, h c]  (both [S * B, nh * d] bf16), one warp
+// per (token, head).
+__global__ void row_dot_kernel(const bf16* __restrict__ dO, const bf16* __restrict__ O, float* __restrict__ Dsum,
+                               int S, int B, int nh, int d) {
+  const size_t wid = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const size_t rows = static_cast<size_t>(S) * B * nh;
+  if (wid >= rows) return;
+  const int h = static_cast<int>(wid % nh);
+  const size_t t = wid / nh;  // token s * B + b
+  const int b = static_cast<int>(t % B), s = static_cast<int>(t / B);
+  const size_t off = t * static_cast<size_t>(nh) * d + static_cast<size_t>(h) * d;
+  float acc = 0.f;
+  for (int c = lane * 8; c < d; c += 256) {
+    float a[8], o[8];
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(dO + off + c), a);
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(O + off + c), o);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc += a[e] * o[e];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) Dsum[(static_cast<size_t>(b) * nh + h) * S + s] = acc;
+}
+
+// Bounded wait shared by the roles below (records the error and raises the CTA's abort flag).
+__device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, int* err, volatile int* abort_flag) {
+  const bool ok = mbar_wait(bar, parity, err, abort_flag);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Eight values of row r, as bf16 (one 16-byte chunk), into chunk ch of the row's 128 bytes in a
+// K-major tile with the 128-byte swizzle: chunk ch of row r sits at ((ch ^ (r & 7)) << 4).
+__device__ __forceinline__ void store_row_chunk(uint8_t* row, int r, int ch, const float* v8) {
+  *reinterpret_cast<uint4*>(row + ((ch ^ (r & 7)) << 4)) = pack_bf16x8(v8);
+}
+
+// ------------------------------------------------------------------ dQ
+template <int D>
+struct GeoQ {
+  static constexpr int QD_BYTES = 128 * D * 2;          // Q_i or dO_i: D/64 blocks of [128 x 64]
+  static constexpr int K_BYTES = 64 * D * 2;            // K_j or V_j: D/64 blocks of [64 x 64]
+  static constexpr int KT_BYTES = D * 64 * 2;           // K_j^T: one [D x 64] block
+  static constexpr int STAGE = 2 * K_BYTES + KT_BYTES;  // K, V, K^T of one key block
+  static constexpr int DS_BYTES = 128 * 64 * 2;         // dS [128 queries x 64 keys]
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_DO = QD_BYTES;
+  static constexpr int OFF_ST = 2 * QD_BYTES;
+  static constexpr int OFF_DS = OFF_ST + 2 * STAGE;
+  static constexpr int OFF_BAR = OFF_DS + 2 * DS_BYTES;
+  static constexpr size_t SMEM_USED = 1024 + OFF_BAR + 256;
+  static constexpr size_t SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;  // one CTA per SM (TMEM)
+  static constexpr uint32_t IDESC_S = idesc_bf16(128, 64);
+  static constexpr uint32_t IDESC_Q = idesc_bf16(128, D);
+};
+static_assert(GeoQ<128>::SMEM_USED <= 232448, "dQ tiles exceed the shared memory of a CTA");
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+                       const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ CUtensorMap tmKT, const AttnBwdParams p) {
+  using G = GeoQ<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + G::OFF_BAR);
+  // bars: q_full | kv_full[2] | kv_empty[2] | s_full[2] | s_free[2] | ds_full[2] | ds_free[2] | done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  const uint32_t q_full = bar0, done = bar0 + 8u * 13;
+  auto kv_full = [&](int i) { return bar0 + 8u * (1 + i); };
+  auto kv_empty = [&](int i) { return bar0 + 8u * (3 + i); };
+  auto s_full = [&](int i) { return bar0 + 8u * (5 + i); };
+  auto s_free = [&](int i) { return bar0 + 8u * (7 + i); };
+  auto ds_full = [&](int i) { return bar0 + 8u * (9 + i); };
+  auto ds_free = [&](int i) { return bar0 + 8u * (11 + i); };
+  const uint32_t sQ = smem_u32(base + G::OFF_Q), sDO = smem_u32(base + G::OFF_DO);
+  auto sK = [&](int st) { return smem_u32(base + G::OFF_ST + st * G::STAGE); };
+  auto sV = [&](int st) { return smem_u32(base + G::OFF_ST + st * G::STAGE + G::K_BYTES); };
+  auto sKT = [&](int st) { return smem_u32(base + G::OFF_ST + st * G::STAGE + 2 * G::K_BYTES); };
+  auto sDS = [&](int i) { return smem_u32(base + G::OFF_DS + i * G::DS_BYTES); };
+
+  pdl_wait();
+  pdl_trigger();
+  const int per = p.batch * p.nh;
+  const int qb = p.num_qb - 1 - static_cast<int>(blockIdx.x) / per;  // longest rows first
+  const int zq = static_cast<int>(blockIdx.x) % per;                  // b * nh + h
+  const int b = zq / p.nh, h = zq % p.nh;
+  const int zk = b * p.ng + h / (p.nh / p.ng);
+  const int nst = min(2 * qb + 2, (p.seq + 63) / 64);  // 64-key blocks j with 64 j <= last query
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(kv_full(i), 1);
+      mbar_init(kv_empty(i), 1);
+      mbar_init(s_full(i), 1);
+      mbar_init(s_free(i), 4);
+      mbar_init(ds_full(i), 4);
+      mbar_init(ds_free(i), 1);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(&tmQ);
+    tma_prefetch(&tmDO);
+    tma_prefetch(&tmK);
+    tma_prefetch(&tmV);
+    tma_prefetch(&tmKT);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  auto tS = [&](int i) { return tmem_base + 64u * i; };
+  auto tP = [&](int i) { return tmem_base + 128u + 64u * i; };
+  const uint32_t tQ = tmem_base + 256u;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, 2 * G::QD_BYTES);
+#pragma unroll
+      for (int a = 0; a < D / 64; ++a) {
+        tma_load_3d(sQ + a * ATOM128, &tmQ, q_full, a * 64, qb * 128, zq);
+        tma_load_3d(sDO + a * ATOM128, &tmDO, q_full, a * 64, qb * 128, zq);
+      }
+      int issued = 0;
+      bool ok = true;
+      for (int n = 0; n < nst; ++n) {
+        const int st = n & 1;
+        if (!mbar_wait(kv_empty(st), ((n >> 1) & 1) ^ 1u, p.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(kv_full(st), G::STAGE);
+#pragma unroll
+        for (int a = 0; a < D / 64; ++a) {
+          tma_load_3d(sK(st) + a * ATOM64, &tmK, kv_full(st), a * 64, n * 64, zk);
+          tma_load_3d(sV(st) + a * ATOM64, &tmV, kv_full(st), a * 64, n * 64, zk);
+        }
+        tma_load_3d(sKT(st), &tmKT, kv_full(st), n * 64, 0, zk);
+        ++issued;
+      }
+      if (!ok) {  // let this CTA's own copies in flight land
+        mbar_wait_slow(q_full, 0, nullptr, nullptr, kDrainLimitNs);
+        for (int n = issued - 1; n >= 0 && n >= issued - 2; --n)
+          mbar_wait_slow(kv_full(n & 1), (n >> 1) & 1, nullptr, nullptr, kDrainLimitNs);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      bool ok = mbar_wait(q_full, 0, p.err, abort_flag);
+      auto issue_dq = [&](int m) -> bool {  // dQ += dS(m) K_m
+        const int i = m & 1;
+        if (!mbar_wait(ds_full(i), (m >> 1) & 1, p.err, abort_flag)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_bf16_ss(tQ, sw128_desc(sDS(i) + k * 32), sw128_desc(sKT(i) + k * 32), G::IDESC_Q,
+                      (m > 0 || k > 0) ? 1u : 0u);
+        mma_commit(ds_free(i));
+        mma_commit(kv_empty(i));
+        return true;
+      };
+      for (int n = 0; ok && n < nst; ++n) {
+        const int i = n & 1;
+        const uint32_t ph = (n >> 1) & 1;
+        if (!mbar_wait(kv_full(i), ph, p.err, abort_flag) ||
+            (n >= 2 && !mbar_wait(s_free(i), ph ^ 1u, p.err, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {  // S = Q K^T and dP = dO V^T for keys 64 n ..
+          const uint32_t oq = (k >> 2) * ATOM128 + (k & 3) * 32, ok_ = (k >> 2) * ATOM64 + (k & 3) * 32;
+          mma_bf16_ss(tS(i), sw128_desc(sQ + oq), sw128_desc(sK(i) + ok_), G::IDESC_S, k > 0 ? 1u : 0u);
+          mma_bf16_ss(tP(i), sw128_desc(sDO + oq), sw128_desc(sV(i) + ok_), G::IDESC_S, k > 0 ? 1u : 0u);
+        }
+        mma_commit(s_full(i));
+        if (n >= 1 && !issue_dq(n - 1)) ok = false;
+      }
+      if (ok && nst > 0) ok = issue_dq(nst - 1);
+      mma_commit(done);
+      mbar_wait_slow(done, 0, nullptr, nullptr, ok ? kWaitLimitNs : kDrainLimitNs);
+    }
+  } else {
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const int qi = qb * 128 + r;  // query row
+    const bool row_ok = qi < p.seq;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const size_t rix = static_cast<size_t>(zq) * p.seq + qi;
+    const float lse = row_ok ? p.lse[rix] : 0.f;
+    const float dsum = row_ok ? p.dsum[rix] : 0.f;
+    bool ok = true;
+    for (int n = 0; n < nst; ++n) {
+      const int i = n & 1;
+      const uint32_t ph = (n >> 1) & 1;
+      if (!wait_all(s_full(i), ph, p.err, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[64], dp[64];
+      tmem_ld32(tS(i) + lane_off, s);
+      tmem_ld32(tS(i) + lane_off + 32, s + 32);
+      tmem_ld32(tP(i) + lane_off, dp);
+      tmem_ld32(tP(i) + lane_off + 32, dp + 32);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free(i));
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const bool valid = row_ok && n * 64 + c <= qi;
+        const float pv = valid ? ex2_approx(s[c] * p.scale_log2 - lse) : 0.f;
+        s[c] = pv * (dp[c] - dsum) * p.scale;  // dS
+      }
+      if (n >= 2 && !wait_all(ds_free(i), ph ^ 1u, p.err, abort_flag)) {
+        ok = false;
+        break;
+      }
+      uint8_t* row = base + G::OFF_DS + i * G::DS_BYTES + r * 128;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) store_row_chunk(row, r, ch, s + 8 * ch);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ds_full(i));
+    }
+    if (ok && wait_all(done, 0, p.err, abort_flag)) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        float v[32];
+        tmem_ld32(tQ + lane_off + cc * 32, v);
+        if (row_ok) {
+          float4* dst = reinterpret_cast<float4*>(p.dq + rix * D + cc * 32);
+#pragma unroll
+          for (int g = 0; g < 8; ++g) dst[g] = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+// ------------------------------------------------------------------ dK, dV
+template <int D>
+struct GeoKV {
+  static constexpr int KV_BYTES = 128 * D * 2;            // K_j or V_j: D/64 blocks of [128 x 64]
+  static constexpr int QD_BYTES = 64 * D * 2;             // Q_i or dO_i: D/64 blocks of [64 x 64]
+  static constexpr int T_BYTES = D * 64 * 2;              // Q_i^T or dO_i^T: one [D x 64] block
+  static constexpr int STAGE = 2 * QD_BYTES + 2 * T_BYTES;
+  static constexpr int PT_BYTES = 128 * 64 * 2;           // P^T or dS^T [128 keys x 64 queries]
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = KV_BYTES;
+  static constexpr int OFF_ST = 2 * KV_BYTES;
+  static constexpr int OFF_PT = OFF_ST + 2 * STAGE;
+  static constexpr int OFF_DST = OFF_PT + PT_BYTES;
+  static constexpr int OFF_BAR = OFF_DST + PT_BYTES;
+  static constexpr size_t SMEM_USED = 1024 + OFF_BAR + 256;
+  static constexpr size_t SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
+  static constexpr uint32_t IDESC_S = idesc_bf16(128, 64);
+  static constexpr uint32_t IDESC_G = idesc_bf16(128, D);
+};
+static_assert(GeoKV<128>::SMEM_USED <= 232448, "dK/dV tiles exceed the shared memory of a CTA");
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                         const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+                         const __grid_constant__ CUtensorMap tmQT, const __grid_constant__ CUtensorMap tmDOT,
+                         const AttnBwdParams p) {
+  using G = GeoKV<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + G::OFF_BAR);
+  // bars: kv_full | st_full[2] | st_empty[2] | s_full[2] | s_free[2] | pt_full | pt_free | done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  const uint32_t kv_full = bar0, pt_full = bar0 + 8u * 9, pt_free = bar0 + 8u * 10, done = bar0 + 8u * 11;
+  auto st_full = [&](int i) { return bar0 + 8u * (1 + i); };
+  auto st_empty = [&](int i) { return bar0 + 8u * (3 + i); };
+  auto s_full = [&](int i) { return bar0 + 8u * (5 + i); };
+  auto s_free = [&](int i) { return bar0 + 8u * (7 + i); };
+  const uint32_t sK = smem_u32(base + G::OFF_K), sV = smem_u32(base + G::OFF_V);
+  auto sQ = [&](int st) { return smem_u32(base + G::OFF_ST + st * G::STAGE); };
+  auto sDO = [&](int st) { return smem_u32(base + G::OFF_ST + st * G::STAGE + G::QD_BYTES); };
+  auto sQT = [&](int st) { return smem_u32(base + G::OFF_ST + st * G::STAGE + 2 * G::QD_BYTES); };
+  auto sDOT = [&](int st) { return smem_u32(base + G::OFF_ST + st * G::STAGE + 2 * G::QD_BYTES + G::T_BYTES); };
+  const uint32_t sPT = smem_u32(base + G::OFF_PT), sDST = smem_u32(base + G::OFF_DST);
+
+  pdl_wait();
+  pdl_trigger();
+  const int per = p.batch * p.ng;
+  const int kb = static_cast<int>(blockIdx.x) / per;  // key block 0 has the most query blocks
+  const int zk = static_cast<int>(blockIdx.x) % per;  // b * ng + g
+  const int b = zk / p.ng, g = zk % p.ng;
+  const int rep = p.nh / p.ng;
+  const int nq64 = (p.seq + 63) / 64;
+  const int i0 = 2 * kb;            // first 64-query block that sees a key of this block
+  const int per_head = nq64 - i0;   // >= 1 for every launched key block
+  const int nst = rep * per_head;   // steps: (head of the group, query block)
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(st_full(i), 1);
+      mbar_init(st_empty(i), 1);
+      mbar_init(s_full(i), 1);
+      mbar_init(s_free(i), 4);
+    }
+    mbar_init(pt_full, 4);
+    mbar_init(pt_free, 1);
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(&tmK);
+    tma_prefetch(&tmV);
+    tma_prefetch(&tmQ);
+    tma_prefetch(&tmDO);
+    tma_prefetch(&tmQT);
+    tma_prefetch(&tmDOT);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  auto tS = [&](int i) { return tmem_base + 64u * i; };
+  auto tP = [&](int i) { return tmem_base + 128u + 64u * i; };
+  const uint32_t tV = tmem_base + 256u, tK = tmem_base + 256u + D;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(kv_full, 2 * G::KV_BYTES);
+#pragma unroll
+      for (int a = 0; a < D / 64; ++a) {
+        tma_load_3d(sK + a * ATOM128, &tmK, kv_full, a * 64, kb * 128, zk);
+        tma_load_3d(sV + a * ATOM128, &tmV, kv_full, a * 64, kb * 128, zk);
+      }
+      int issued = 0;
+      bool ok = true;
+      for (int n = 0; n < nst; ++n) {
+        const int st = n & 1;
+        const int zq = b * p.nh + g * rep + n / per_head;
+        const int qi0 = (i0 + n % per_head) * 64;
+        if (!mbar_wait(st_empty(st), ((n >> 1) & 1) ^ 1u, p.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(st_full(st), G::STAGE);
+#pragma unroll
+        for (int a = 0; a < D / 64; ++a) {
+          tma_load_3d(sQ(st) + a * ATOM64, &tmQ, st_full(st), a * 64, qi0, zq);
+          tma_load_3d(sDO(st) + a * ATOM64, &tmDO, st_full(st), a * 64, qi0, zq);
+        }
+        tma_load_3d(sQT(st), &tmQT, st_full(st), qi0, 0, zq);
+        tma_load_3d(sDOT(st), &tmDOT, st_full(st), qi0, 0, zq);
+        ++issued;
+      }
+      if (!ok) {
+        mbar_wait_slow(kv_full, 0, nullptr, nullptr, kDrainLimitNs);
+        for (int n = issued - 1; n >= 0 && n >= issued - 2; --n)
+          mbar_wait_slow(st_full(n & 1), (n >> 1) & 1, nullptr, nullptr, kDrainLimitNs);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      bool ok = mbar_wait(kv_full, 0, p.err, abort_flag);
+      auto issue_grad = [&](int m) -> bool {  // dV += P^T dO, dK += dS^T Q for step m
+        const int st = m & 1;
+        if (!mbar_wait(pt_full, m & 1, p.err, abort_flag)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          mma_bf16_ss(tV, sw128_desc(sPT + k * 32), sw128_desc(sDOT(st) + k * 32), G::IDESC_G,
+                      (m > 0 || k > 0) ? 1u : 0u);
+          mma_bf16_ss(tK, sw128_desc(sDST + k * 32), sw128_desc(sQT(st) + k * 32), G::IDESC_G,
+                      (m > 0 || k > 0) ? 1u : 0u);
+        }
+        mma_commit(pt_free);
+        mma_commit(st_empty(st));
+        return true;
+      };
+      for (int n = 0; ok && n < nst; ++n) {
+        const int i = n & 1;
+        const uint32_t ph = (n >> 1) & 1;
+        if (!mbar_wait(st_full(i), ph, p.err, abort_flag) ||
+            (n >= 2 && !mbar_wait(s_free(i), ph ^ 1u, p.err, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {  // S^T = K Q^T and dP^T = V dO^T for one 64-query block
+          const uint32_t okv = (k >> 2) * ATOM128 + (k & 3) * 32, oq = (k >> 2) * ATOM64 + (k & 3) * 32;
+          mma_bf16_ss(tS(i), sw128_desc(sK + okv), sw128_desc(sQ(i) + oq), G::IDESC_S, k > 0 ? 1u : 0u);
+          mma_bf16_ss(tP(i), sw128_desc(sV + okv), sw128_desc(sDO(i) + oq), G::IDESC_S, k > 0 ? 1u : 0u);
+        }
+        mma_commit(s_full(i));
+        if (n >= 1 && !issue_grad(n - 1)) ok = false;
+      }
+      if (ok && nst > 0) ok = issue_grad(nst - 1);
+      mma_commit(done);
+      mbar_wait_slow(done, 0, nullptr, nullptr, ok ? kWaitLimitNs : kDrainLimitNs);
+    }
+  } else {
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const int kj = kb * 128 + r;  // key row
+    const bool row_ok = kj < p.seq;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    bool ok = true;
+    for (int n = 0; n < nst; ++n) {
+      const int i = n & 1;
+      const uint32_t ph = (n >> 1) & 1;
+      const int zq = b * p.nh + g * rep + n / per_head;
+      const int qi0 = (i0 + n % per_head) * 64;
+      if (!wait_all(s_full(i), ph, p.err, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[64], dp[64];
+      tmem_ld32(tS(i) + lane_off, s);
+      tmem_ld32(tS(i) + lane_off + 32, s + 32);
+      tmem_ld32(tP(i) + lane_off, dp);
+      tmem_ld32(tP(i) + lane_off + 32, dp + 32);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free(i));
+      const float* lse = p.lse + static_cast<size_t>(zq) * p.seq;
+      const float* dsum = p.dsum + static_cast<size_t>(zq) * p.seq;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const int qi = qi0 + c;
+        const bool valid = row_ok && qi < p.seq && qi >= kj;
+        const int qc = qi < p.seq ? qi : p.seq - 1;
+        const float pv = valid ? ex2_approx(s[c] * p.scale_log2 - __ldg(lse + qc)) : 0.f;
+        s[c] = pv;                                           // P^T
+        dp[c] = pv * (dp[c] - __ldg(dsum + qc)) * p.scale;  // dS^T
+      }
+      if (n >= 1 && !wait_all(pt_free, (n - 1) & 1, p.err, abort_flag)) {
+        ok = false;
+        break;
+      }
+      uint8_t* prow = base + G::OFF_PT + r * 128;
+      uint8_t* drow = base + G::OFF_DST + r * 128;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        store_row_chunk(prow, r, ch, s + 8 * ch);
+        store_row_chunk(drow, r, ch, dp + 8 * ch);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pt_full);
+    }
+    if (ok && wait_all(done, 0, p.err, abort_flag)) {
+      tc_fence_after();
+      const size_t row = static_cast<size_t>(zk) * p.seq + kj;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        float v[32], k32[32];
+        tmem_ld32(tV + lane_off + cc * 32, v);
+        tmem_ld32(tK + lane_off + cc * 32, k32);
+        if (row_ok) {
+          float4* dv = reinterpret_cast<float4*>(p.dv + row * D + cc * 32);
+          float4* dk = reinterpret_cast<float4*>(p.dk + row * D + cc * 32);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            dv[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            dk[q] = make_float4(k32[4 * q], k32[4 * q + 1], k32[4 * q + 2], k32[4 * q + 3]);
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const CUtensorMap* maps, const AttnBwdParams& p, cudaStream_t st) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(GeoQ<D>::SMEM));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(GeoKV<D>::SMEM));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const unsigned nb = static_cast<unsigned>((p.seq + 127) / 128);
+  // maps: Q128, dO128, K64, V64, K^T | K128, V128, Q64, dO64, Q^T, dO^T
+  cudaError_t e = launch_pdl(attn_bwd_dq_kernel<D>, dim3(nb * p.batch * p.nh), dim3(192), GeoQ<D>::SMEM, st,
+                             maps[0], maps[1], maps[2], maps[3], maps[4], p);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(attn_bwd_dkdv_kernel<D>, dim3(nb * p.batch * p.ng), dim3(192), GeoKV<D>::SMEM, st, maps[5],
+                    maps[6], maps[7], maps[8], maps[9], maps[10], p);
+}
+
+}  // namespace
+
+cudaError_t launch_head_slices(bool transpose, const bf16* src, size_t sp, size_t sb, size_t sh, int zdiv, int Z,
+                               bf16* dst, size_t dp, int R, int C, cudaStream_t st) {
+  if (Z <= 0 || R <= 0 || C <= 0) return cudaSuccess;
+  const dim3 grid((C + 31) / 32, (R + 31) / 32, Z), block(32, 8);
+  if (transpose)
+    head_slices_kernel<true><<<grid, block, 0, st>>>(src, sp, sb, sh, zdiv, dst, dp, R, C);
+  else
+    head_slices_kernel<false><<<grid, block, 0, st>>>(src, sp, sb, sh, zdiv, dst, dp, R, C);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_row_dot(const bf16* dO, const bf16* O, float* Dsum, int S, int B, int nh, int d, cudaStream_t st) {
+  const size_t warps = static_cast<size_t>(S) * B * nh;
+  if (warps == 0) return cudaSuccess;
+  row_dot_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, st>>>(dO, O, Dsum, S, B, nh, d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attention_bwd(int head_dim, const CUtensorMap* maps, const AttnBwdParams& p, cudaStream_t st) {
+  if (p.seq <= 0) return cudaSuccess;
+  if (head_dim == 64) return launch_bwd_d<64>(maps, p, st);
+  if (head_dim == 128) return launch_bwd_d<128>(maps, p, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace mt

@@ -1,5 +1,6 @@
 // Bandwidth-bound kernels of the layer's backward pass (the matrix products run on the tcgen05
-// GEMM).  The chain rule through the forward: norms, RoPE, causal softmax, SwiGLU / GeLU(tanh).
+// GEMM; the attention's own backward is in attention_bwd.cu).  The chain rule through the forward:
+// norms, RoPE, SwiGLU / GeLU(tanh).
 #include <math.h>
 
 #include "common.cuh"
@@ -26,17 +27,6 @@ __device__ __forceinline__ float cta_sum(float v, float* red) {
   return t;
 }
 
-__device__ __forceinline__ float cta_max(float v, float* red) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  v = warp_max(v);
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  float t = -INFINITY;
-  for (int i = 0; i < nw; ++i) t = fmaxf(t, red[i]);
-  return t;
-}
-
 // dst[c][r] = src[r][c] for an R x C bf16 matrix (pitches in elements); 32 x 32 tiles.
 __global__ void transpose_kernel(const bf16* __restrict__ src, size_t sp, bf16* __restrict__ dst, size_t dp, int R,
                                  int C) {
@@ -52,39 +42,6 @@ __global__ void transpose_kernel(const bf16* __restrict__ src, size_t sp, bf16* 
   for (int i = threadIdx.y; i < 32; i += blockDim.y) {
     const int c = c0 + i, r = r0 + threadIdx.x;
     if (r < R && c < C) d[static_cast<size_t>(c) * dp + r] = tile[threadIdx.x][i];
-  }
-}
-
-// One row i of the attention backward of one head: from the fp32 scores S[i, :] (unscaled) and
-// dP[i, :] = dO_i . V_j, recompute P = softmax(S scale) over the keys j <= i and write
-// P (bf16) and dS = P (dP - sum_j P dP) scale (bf16, the gradient of the unscaled scores);
-// entries j > i are 0.
-__global__ void attn_bwd_rows_kernel(const float* __restrict__ S, const float* __restrict__ dP, bf16* __restrict__ P,
-                                     bf16* __restrict__ dS, int n, float scale) {
-  __shared__ float red[32];
-  const int i = blockIdx.x;
-  const float* s = S + static_cast<size_t>(i) * n;
-  const float* dp = dP + static_cast<size_t>(i) * n;
-  float mx = -INFINITY;
-  for (int j = threadIdx.x; j <= i; j += blockDim.x) mx = fmaxf(mx, s[j] * scale);
-  mx = cta_max(mx, red);
-  float sum = 0.f;
-  for (int j = threadIdx.x; j <= i; j += blockDim.x) sum += expf(s[j] * scale - mx);
-  sum = cta_sum(sum, red);
-  const float inv = 1.0f / sum;
-  float dot = 0.f;
-  for (int j = threadIdx.x; j <= i; j += blockDim.x) dot += expf(s[j] * scale - mx) * inv * dp[j];
-  dot = cta_sum(dot, red);
-  bf16* pr = P + static_cast<size_t>(i) * n;
-  bf16* dr = dS + static_cast<size_t>(i) * n;
-  for (int j = threadIdx.x; j < n; j += blockDim.x) {
-    float p = 0.f, g = 0.f;
-    if (j <= i) {
-      p = expf(s[j] * scale - mx) * inv;
-      g = p * (dp[j] - dot) * scale;
-    }
-    pr[j] = __float2bfloat16_rn(p);
-    dr[j] = __float2bfloat16_rn(g);
   }
 }
 
@@ -242,12 +199,6 @@ __global__ void rope_bwd_pack_kernel(const float* __restrict__ dq, const float* 
 cudaError_t launch_transpose(const bf16* src, size_t sp, bf16* dst, size_t dp, int R, int C, cudaStream_t st) {
   if (R <= 0 || C <= 0) return cudaSuccess;
   transpose_kernel<<<dim3((C + 31) / 32, (R + 31) / 32), dim3(32, 8), 0, st>>>(src, sp, dst, dp, R, C);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_attn_bwd_rows(const float* S, const float* dP, bf16* P, bf16* dS, int n, float scale,
-                                 cudaStream_t st) {
-  attn_bwd_rows_kernel<<<n, 256, 0, st>>>(S, dP, P, dS, n, scale);
   return cudaGetLastError();
 }
 

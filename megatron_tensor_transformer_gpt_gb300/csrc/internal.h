@@ -73,6 +73,21 @@ struct AttnParams {
   uint8_t* o8;
   const float* q_scale;
   unsigned* amax;
+  // when set (dense batches): log2 of each query row's softmax denominator in the base-2 units of
+  // the kernel, lse[(b * nh + h) * seq + s] = m + log2(l), so P = 2^(S * scale_log2 - lse)
+  float* lse;
+  int* err;
+};
+
+// Attention backward (dense batches): from the forward's lse and D = rowsum(dO o O) (both
+// [b * nh + h][seq] fp32), fp32 dq [b * nh + h][seq][d] and dk, dv [b * ng + g][seq][d].
+struct AttnBwdParams {
+  int seq, batch, nh, ng;
+  int num_qb;                // ceil(seq / 128)
+  float scale, scale_log2;   // 1 / sqrt(d) and log2(e) / sqrt(d)
+  const float* lse;
+  const float* dsum;
+  float *dq, *dk, *dv;
   int* err;
 };
 
@@ -117,6 +132,17 @@ int gemm_pair_slots();
 
 // Kernel launchers; return a cudaError_t from the launch.
 // fp8 = true: A and B are E4M3 (tensor maps of bytes, boxes 128 wide).
+// Attention backward: maps = {Q [.,128 rows], dO [.,128], K [.,64], V [.,64], K^T [., d rows] for
+// the dQ kernel; K [.,128], V [.,128], Q [.,64], dO [.,64], Q^T [., d], dO^T [., d] for dK/dV}
+// (bf16, 64-element inner boxes, head-major [z][rows][cols] tensors).
+cudaError_t launch_attention_bwd(int head_dim, const CUtensorMap* maps, const AttnBwdParams& p, cudaStream_t st);
+// Batched copy / transpose of R x C bf16 slices z = 0..Z-1 at src + (z / zdiv) sb + (z % zdiv) sh
+// (row pitch sp) into dst + z R dp (copy, pitch dp) or dst + z C dp (transpose, pitch dp).
+cudaError_t launch_head_slices(bool transpose, const bf16* src, size_t sp, size_t sb, size_t sh, int zdiv, int Z,
+                               bf16* dst, size_t dp, int R, int C, cudaStream_t st);
+// Dsum[(b nh + h) S + s] = dO[s b, h] . O[s b, h] over the head's d columns.
+cudaError_t launch_row_dot(const bf16* dO, const bf16* O, float* Dsum, int S, int B, int nh, int d, cudaStream_t st);
+
 cudaError_t launch_gemm(int mode, bool fp8, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB64,
                         const GemmParams& p, cudaStream_t stream);
 size_t gemm_smem_bytes();
@@ -135,8 +161,6 @@ cudaError_t launch_quantize_e4m3(const bf16* x, size_t n, uint8_t* q, float* slo
 
 // ---- backward pass (backward_kernels.cu)
 cudaError_t launch_transpose(const bf16* src, size_t sp, bf16* dst, size_t dp, int R, int C, cudaStream_t st);
-cudaError_t launch_attn_bwd_rows(const float* S, const float* dP, bf16* P, bf16* dS, int n, float scale,
-                                 cudaStream_t st);
 cudaError_t launch_act_fwd(const bf16* u, bf16* a, size_t T, int f, bool swiglu, cudaStream_t st);
 cudaError_t launch_act_bwd(const bf16* u, const bf16* da, bf16* du, size_t T, int f, bool swiglu, cudaStream_t st);
 cudaError_t launch_norm_bwd(const bf16* dy, const bf16* x, const bf16* gamma, const bf16* add, bf16* out, float* grow,
