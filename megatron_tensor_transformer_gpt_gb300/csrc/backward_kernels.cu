@@ -47,22 +47,69 @@ __global__ void transpose_kernel(const bf16* __restrict__ src, size_t sp, bf16* 
 
 __device__ __forceinline__ float sigmoidf(float g) { return 1.0f / (1.0f + expf(-g)); }
 
+// dst[c][r] = src[r][c] in 64 x 64 tiles with 16-byte loads and stores (pitches multiples of 8
+// elements); the tile passes through shared memory with a 2-element pad per row.
+__global__ void __launch_bounds__(256) transpose64_kernel(const bf16* __restrict__ src, size_t sp,
+                                                          bf16* __restrict__ dst, size_t dp, int R, int C) {
+  __shared__ uint16_t tile[64][66];
+  const int c0 = blockIdx.x * 64, r0 = blockIdx.y * 64;
+  const uint16_t* s = reinterpret_cast<const uint16_t*>(src);
+  uint16_t* d = reinterpret_cast<uint16_t*>(dst);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int idx = threadIdx.x + 256 * i, r = idx >> 3, c = (idx & 7) * 8;
+    const size_t at = static_cast<size_t>(r0 + r) * sp + c0 + c;
+    if (r0 + r < R && c0 + c + 8 <= C) {
+      const uint4 v = *reinterpret_cast<const uint4*>(s + at);
+      const uint16_t* e = reinterpret_cast<const uint16_t*>(&v);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) tile[r][c + k] = e[k];
+    } else if (r0 + r < R) {
+      for (int k = 0; k < 8 && c0 + c + k < C; ++k) tile[r][c + k] = s[at + k];
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int idx = threadIdx.x + 256 * i, oc = idx >> 3, r = (idx & 7) * 8;  // output row = input column
+    const size_t at = static_cast<size_t>(c0 + oc) * dp + r0 + r;
+    if (c0 + oc >= C) continue;
+    if (r0 + r + 8 <= R) {
+      uint4 v;
+      uint16_t* e = reinterpret_cast<uint16_t*>(&v);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) e[k] = tile[r + k][oc];
+      *reinterpret_cast<uint4*>(d + at) = v;
+    } else {
+      for (int k = 0; k < 8 && r0 + r + k < R; ++k) d[at + k] = tile[r + k][oc];
+    }
+  }
+}
+
 // SwiGLU / GeLU(tanh) forward from the stored fc1 output u: a = silu(u[:, :f]) u[:, f:] or gelu(u).
 __global__ void act_fwd_kernel(const bf16* __restrict__ u, bf16* __restrict__ a, size_t T, int f, int swiglu) {
-  const size_t n = T * f;
-  for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < n;
-       idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const size_t t = idx / f;
-    const int c = static_cast<int>(idx - t * f);
-    float r;
+  // eight outputs (16 bytes) per thread and iteration; f is a multiple of 8
+  const int f8 = f >> 3;
+  const size_t n8 = T * f8;
+  for (size_t v = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; v < n8;
+       v += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t t = v / f8;
+    const int c = static_cast<int>(v - t * f8) * 8;
+    float r[8];
     if (swiglu) {
-      const float g = __bfloat162float(u[t * 2 * f + c]), up = __bfloat162float(u[t * 2 * f + f + c]);
-      r = g * sigmoidf(g) * up;
+      float g[8], up[8];
+      unpack_bf16x8(*reinterpret_cast<const uint4*>(u + t * 2 * f + c), g);
+      unpack_bf16x8(*reinterpret_cast<const uint4*>(u + t * 2 * f + f + c), up);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) r[e] = g[e] * sigmoidf(g[e]) * up[e];
     } else {
-      const float x = __bfloat162float(u[t * f + c]);
-      r = 0.5f * x * (1.0f + tanhf(0.7978845608028654f * (x + 0.044715f * x * x * x)));
+      float x[8];
+      unpack_bf16x8(*reinterpret_cast<const uint4*>(u + t * f + c), x);
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        r[e] = 0.5f * x[e] * (1.0f + tanhf(0.7978845608028654f * (x[e] + 0.044715f * x[e] * x[e] * x[e])));
     }
-    a[idx] = __float2bfloat16_rn(r);
+    *reinterpret_cast<uint4*>(a + t * f + c) = pack_bf16x8(r);
   }
 }
 
@@ -71,23 +118,37 @@ __global__ void act_fwd_kernel(const bf16* __restrict__ u, bf16* __restrict__ a,
 //   GeLU(tanh): du = da gelu'(u)
 __global__ void act_bwd_kernel(const bf16* __restrict__ u, const bf16* __restrict__ da, bf16* __restrict__ du, size_t T,
                                int f, int swiglu) {
-  const size_t n = T * f;
-  for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < n;
-       idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const size_t t = idx / f;
-    const int c = static_cast<int>(idx - t * f);
-    const float g_a = __bfloat162float(da[idx]);
+  const int f8 = f >> 3;
+  const size_t n8 = T * f8;
+  for (size_t v = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; v < n8;
+       v += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t t = v / f8;
+    const int c = static_cast<int>(v - t * f8) * 8;
+    float ga[8];
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(da + t * f + c), ga);
     if (swiglu) {
-      const float g = __bfloat162float(u[t * 2 * f + c]), up = __bfloat162float(u[t * 2 * f + f + c]);
-      const float s = sigmoidf(g);
-      du[t * 2 * f + c] = __float2bfloat16_rn(g_a * up * s * (1.0f + g * (1.0f - s)));
-      du[t * 2 * f + f + c] = __float2bfloat16_rn(g_a * g * s);
+      float g[8], up[8], dg[8], dup[8];
+      unpack_bf16x8(*reinterpret_cast<const uint4*>(u + t * 2 * f + c), g);
+      unpack_bf16x8(*reinterpret_cast<const uint4*>(u + t * 2 * f + f + c), up);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float sg = sigmoidf(g[e]);
+        dg[e] = ga[e] * up[e] * sg * (1.0f + g[e] * (1.0f - sg));
+        dup[e] = ga[e] * g[e] * sg;
+      }
+      *reinterpret_cast<uint4*>(du + t * 2 * f + c) = pack_bf16x8(dg);
+      *reinterpret_cast<uint4*>(du + t * 2 * f + f + c) = pack_bf16x8(dup);
     } else {
-      const float x = __bfloat162float(u[idx]);
+      float x[8], r[8];
+      unpack_bf16x8(*reinterpret_cast<const uint4*>(u + t * f + c), x);
       const float k0 = 0.7978845608028654f, k1 = 0.044715f;
-      const float th = tanhf(k0 * (x + k1 * x * x * x));
-      const float d = 0.5f * (1.0f + th) + 0.5f * x * (1.0f - th * th) * k0 * (1.0f + 3.0f * k1 * x * x);
-      du[idx] = __float2bfloat16_rn(g_a * d);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float th = tanhf(k0 * (x[e] + k1 * x[e] * x[e] * x[e]));
+        const float d = 0.5f * (1.0f + th) + 0.5f * x[e] * (1.0f - th * th) * k0 * (1.0f + 3.0f * k1 * x[e] * x[e]);
+        r[e] = ga[e] * d;
+      }
+      *reinterpret_cast<uint4*>(du + t * f + c) = pack_bf16x8(r);
     }
   }
 }
@@ -198,17 +259,32 @@ __global__ void rope_bwd_pack_kernel(const float* __restrict__ dq, const float* 
 
 cudaError_t launch_transpose(const bf16* src, size_t sp, bf16* dst, size_t dp, int R, int C, cudaStream_t st) {
   if (R <= 0 || C <= 0) return cudaSuccess;
-  transpose_kernel<<<dim3((C + 31) / 32, (R + 31) / 32), dim3(32, 8), 0, st>>>(src, sp, dst, dp, R, C);
+  const bool vec = sp % 8 == 0 && dp % 8 == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0 &&
+                   (reinterpret_cast<uintptr_t>(dst) & 15) == 0;
+  if (vec)
+    transpose64_kernel<<<dim3((C + 63) / 64, (R + 63) / 64), 256, 0, st>>>(src, sp, dst, dp, R, C);
+  else
+    transpose_kernel<<<dim3((C + 31) / 32, (R + 31) / 32), dim3(32, 8), 0, st>>>(src, sp, dst, dp, R, C);
   return cudaGetLastError();
 }
 
+// Blocks of 256 threads for T x f / 8 vectors: one pass, at most 32 blocks per SM.
+static unsigned act_grid(size_t T, int f) {
+  const size_t n8 = T * static_cast<size_t>(f / 8);
+  const size_t blocks = (n8 + 255) / 256;
+  const size_t cap = static_cast<size_t>(num_sms()) * 32;
+  return static_cast<unsigned>(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
+}
+
 cudaError_t launch_act_fwd(const bf16* u, bf16* a, size_t T, int f, bool swiglu, cudaStream_t st) {
-  act_fwd_kernel<<<4 * 152, 256, 0, st>>>(u, a, T, f, swiglu ? 1 : 0);
+  if (f % 8) return cudaErrorInvalidValue;
+  act_fwd_kernel<<<act_grid(T, f), 256, 0, st>>>(u, a, T, f, swiglu ? 1 : 0);
   return cudaGetLastError();
 }
 
 cudaError_t launch_act_bwd(const bf16* u, const bf16* da, bf16* du, size_t T, int f, bool swiglu, cudaStream_t st) {
-  act_bwd_kernel<<<4 * 152, 256, 0, st>>>(u, da, du, T, f, swiglu ? 1 : 0);
+  if (f % 8) return cudaErrorInvalidValue;
+  act_bwd_kernel<<<act_grid(T, f), 256, 0, st>>>(u, da, du, T, f, swiglu ? 1 : 0);
   return cudaGetLastError();
 }
 
