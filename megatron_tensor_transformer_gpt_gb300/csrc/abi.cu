@@ -642,7 +642,7 @@ int gemm_ab(mt_layer* L, const void* A, size_t lda, const void* Bm, size_t ldb, 
 
 enum BwRegion {
   kBQkv = 0, kBU, kBA, kBDa, kBDu, kBDhn, kBDh, kBDo, kBDq, kBDk, kBDv, kBDqkv, kBDxn, kBGrow, kBAcc,
-  kBLse, kBDsum, kBDoH, kBVh, kBDoT, kBKT, kBQT, kBWt, kBAt, kBBt, kBNum
+  kBLse, kBDsum, kBDoH, kBVh, kBWt, kBAt, kBBt, kBNum
 };
 
 struct BwLayout {
@@ -671,16 +671,12 @@ BwLayout bw_layout(const mt_layer* L, int S, int B) {
   b.size[kBDxn] = T * H * 2;
   b.size[kBGrow] = T * H * 4;
   b.size[kBAcc] = maxc * 4;
-  // attention backward: row statistics, head-major dO and V, transposed Q, dO and K ([z][d][S_pad])
-  const size_t sp = (static_cast<size_t>(S) + 7) / 8 * 8, zq = static_cast<size_t>(B) * L->nh_r,
-               zk = static_cast<size_t>(B) * L->ng_r;
+  // attention backward: row statistics, head-major dO and V
+  const size_t zq = static_cast<size_t>(B) * L->nh_r, zk = static_cast<size_t>(B) * L->ng_r;
   b.size[kBLse] = zq * S * 4;
   b.size[kBDsum] = zq * S * 4;
   b.size[kBDoH] = zq * S * d * 2;
   b.size[kBVh] = zk * S * d * 2;
-  b.size[kBDoT] = zq * d * sp * 2;
-  b.size[kBKT] = zk * d * sp * 2;
-  b.size[kBQT] = zq * d * sp * 2;
   b.size[kBWt] = std::max(std::max(QKV * H, H * qw), std::max(f1 * H, H * f)) * 2;
   b.size[kBAt] = maxc * T * 2;
   b.size[kBBt] = maxc * T * 2;
@@ -801,8 +797,6 @@ int backward_device(mt_layer* L, const BwLayout& b, const void* x, const void* d
   float *dq = bwr<float>(L, b, kBDq), *dk = bwr<float>(L, b, kBDk), *dv = bwr<float>(L, b, kBDv);
   float *lse = bwr<float>(L, b, kBLse), *dsum = bwr<float>(L, b, kBDsum);
   bf16 *dOh = bwr<bf16>(L, b, kBDoH), *Vh = bwr<bf16>(L, b, kBVh);
-  bf16 *dOt = bwr<bf16>(L, b, kBDoT), *Kt = bwr<bf16>(L, b, kBKT), *Qt = bwr<bf16>(L, b, kBQT);
-  const size_t sp = (static_cast<size_t>(S) + 7) / 8 * 8;
   const int zq = B * nh, zk = B * ng;
   const size_t sd = static_cast<size_t>(S) * d;
   struct Slice {
@@ -814,11 +808,8 @@ int backward_device(mt_layer* L, const BwLayout& b, const void* x, const void* d
     size_t dp;
   } slices[] = {
       {false, dO, static_cast<size_t>(B) * qw, static_cast<size_t>(qw), static_cast<size_t>(d), nh, zq, dOh, static_cast<size_t>(d)},
-      {true, dO, static_cast<size_t>(B) * qw, static_cast<size_t>(qw), static_cast<size_t>(d), nh, zq, dOt, sp},
       {false, qkv + qw + kvw, static_cast<size_t>(B) * QKV, static_cast<size_t>(QKV), static_cast<size_t>(d), ng, zk, Vh,
        static_cast<size_t>(d)},
-      {true, q, static_cast<size_t>(d), sd, 0, 1, zq, Qt, sp},
-      {true, k, static_cast<size_t>(d), sd, 0, 1, zk, Kt, sp},
   };
   for (const Slice& sl : slices) {
     count_launch(L);
@@ -829,14 +820,12 @@ int backward_device(mt_layer* L, const BwLayout& b, const void* x, const void* d
   count_launch(L);
   if ((e = mt::launch_row_dot(dO, o, dsum, S, B, nh, d, st)) != cudaSuccess) return cuda_fail(e, "rowsum(dO o O)");
   {
-    CUtensorMap m[11];
+    CUtensorMap m[8];
     const uint64_t Zq = zq, Zk = zk;
     if ((rc = map_3d(&m[0], q, d, S, Zq, d, sd, 128)) || (rc = map_3d(&m[1], dOh, d, S, Zq, d, sd, 128)) ||
         (rc = map_3d(&m[2], k, d, S, Zk, d, sd, 64)) || (rc = map_3d(&m[3], Vh, d, S, Zk, d, sd, 64)) ||
-        (rc = map_3d(&m[4], Kt, S, d, Zk, sp, d * sp, d)) || (rc = map_3d(&m[5], k, d, S, Zk, d, sd, 128)) ||
-        (rc = map_3d(&m[6], Vh, d, S, Zk, d, sd, 128)) || (rc = map_3d(&m[7], q, d, S, Zq, d, sd, 64)) ||
-        (rc = map_3d(&m[8], dOh, d, S, Zq, d, sd, 64)) || (rc = map_3d(&m[9], Qt, S, d, Zq, sp, d * sp, d)) ||
-        (rc = map_3d(&m[10], dOt, S, d, Zq, sp, d * sp, d)))
+        (rc = map_3d(&m[4], k, d, S, Zk, d, sd, 128)) || (rc = map_3d(&m[5], Vh, d, S, Zk, d, sd, 128)) ||
+        (rc = map_3d(&m[6], q, d, S, Zq, d, sd, 64)) || (rc = map_3d(&m[7], dOh, d, S, Zq, d, sd, 64)))
       return rc;
     mt::AttnBwdParams ap{};
     ap.seq = S;

@@ -4,15 +4,17 @@
 // scores S = Q K^T, P = softmax(S / sqrt(d)) and D_i = dO_i . O_i:
 //     dS = P o (dP - D) / sqrt(d),  dP = dO V^T,
 //     dV = P^T dO,  dK = dS^T Q,  dQ = dS K   (dK, dV summed over the query heads of a group).
-// Two kernels, each a producer warp (TMA), one MMA-issuing thread (tcgen05) and four elementwise
-// warps with one TMEM lane (row) per thread:
+// Two kernels, each a producer warp (TMA), one MMA-issuing thread (tcgen05) and eight elementwise
+// warps: two per TMEM lane quadrant, one row per thread, each warp taking half of a step's 64
+// columns:
 //   attn_bwd_dq_kernel:   one CTA per (128 queries, head); steps over 64-key blocks j <= i:
 //                         S and dP into TMEM, dS (bf16) into shared memory, dQ += dS K in TMEM.
 //   attn_bwd_dkdv_kernel: one CTA per (128 keys, kv group); steps over the group's heads and the
 //                         64-query blocks i >= j: S^T and dP^T into TMEM, P^T and dS^T into shared
 //                         memory, dV += P^T dO and dK += dS^T Q in TMEM.
-// Every operand is K-major: the caller provides head-major copies of dO and V and the transposes
-// Q^T, dO^T and K^T (prep kernels below).
+// The caller provides head-major copies of dO and V (prep kernel below); the second operands of the
+// gradient products (K for dQ, dO for dV, Q for dK) are the tiles already staged for the score
+// products, read as MN-major operands.
 #include "common.cuh"
 #include "internal.h"
 
@@ -94,45 +96,44 @@ template <int D>
 struct GeoQ {
   static constexpr int QD_BYTES = 128 * D * 2;          // Q_i or dO_i: D/64 blocks of [128 x 64]
   static constexpr int K_BYTES = 64 * D * 2;            // K_j or V_j: D/64 blocks of [64 x 64]
-  static constexpr int KT_BYTES = D * 64 * 2;           // K_j^T: one [D x 64] block
-  static constexpr int STAGE = 2 * K_BYTES + KT_BYTES;  // K, V, K^T of one key block
+  static constexpr int STAGE = 2 * K_BYTES;             // K, V of one key block
+  static constexpr int NSTG = 3;                        // key blocks in flight
   static constexpr int DS_BYTES = 128 * 64 * 2;         // dS [128 queries x 64 keys]
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_DO = QD_BYTES;
   static constexpr int OFF_ST = 2 * QD_BYTES;
-  static constexpr int OFF_DS = OFF_ST + 2 * STAGE;
+  static constexpr int OFF_DS = OFF_ST + NSTG * STAGE;
   static constexpr int OFF_BAR = OFF_DS + 2 * DS_BYTES;
   static constexpr size_t SMEM_USED = 1024 + OFF_BAR + 256;
   static constexpr size_t SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;  // one CTA per SM (TMEM)
   static constexpr uint32_t IDESC_S = idesc_bf16(128, 64);
-  static constexpr uint32_t IDESC_Q = idesc_bf16(128, D);
+  static constexpr uint32_t IDESC_Q = idesc_bf16_bmn(128, D);  // B = K_j read MN-major
 };
 static_assert(GeoQ<128>::SMEM_USED <= 232448, "dQ tiles exceed the shared memory of a CTA");
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                        const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                       const __grid_constant__ CUtensorMap tmKT, const AttnBwdParams p) {
+                       const AttnBwdParams p) {
   using G = GeoQ<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + G::OFF_BAR);
-  // bars: q_full | kv_full[2] | kv_empty[2] | s_full[2] | s_free[2] | ds_full[2] | ds_free[2] | done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+  // bars: q_full | kv_full[3] | kv_empty[3] | s_full[2] | s_free[2] | ds_full[2] | ds_free[2] | done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
-  const uint32_t q_full = bar0, done = bar0 + 8u * 13;
+  const uint32_t q_full = bar0, done = bar0 + 8u * 15;
   auto kv_full = [&](int i) { return bar0 + 8u * (1 + i); };
-  auto kv_empty = [&](int i) { return bar0 + 8u * (3 + i); };
-  auto s_full = [&](int i) { return bar0 + 8u * (5 + i); };
-  auto s_free = [&](int i) { return bar0 + 8u * (7 + i); };
-  auto ds_full = [&](int i) { return bar0 + 8u * (9 + i); };
-  auto ds_free = [&](int i) { return bar0 + 8u * (11 + i); };
+  auto kv_empty = [&](int i) { return bar0 + 8u * (4 + i); };
+  auto s_full = [&](int i) { return bar0 + 8u * (7 + i); };
+  auto s_free = [&](int i) { return bar0 + 8u * (9 + i); };
+  auto ds_full = [&](int i) { return bar0 + 8u * (11 + i); };
+  auto ds_free = [&](int i) { return bar0 + 8u * (13 + i); };
   const uint32_t sQ = smem_u32(base + G::OFF_Q), sDO = smem_u32(base + G::OFF_DO);
   auto sK = [&](int st) { return smem_u32(base + G::OFF_ST + st * G::STAGE); };
   auto sV = [&](int st) { return smem_u32(base + G::OFF_ST + st * G::STAGE + G::K_BYTES); };
-  auto sKT = [&](int st) { return smem_u32(base + G::OFF_ST + st * G::STAGE + 2 * G::K_BYTES); };
   auto sDS = [&](int i) { return smem_u32(base + G::OFF_DS + i * G::DS_BYTES); };
 
   pdl_wait();
@@ -147,12 +148,14 @@ __global__ void __launch_bounds__(192, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < G::NSTG; ++i) {
       mbar_init(kv_full(i), 1);
       mbar_init(kv_empty(i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(s_full(i), 1);
-      mbar_init(s_free(i), 4);
-      mbar_init(ds_full(i), 4);
+      mbar_init(s_free(i), 8);
+      mbar_init(ds_full(i), 8);
       mbar_init(ds_free(i), 1);
     }
     mbar_init(done, 1);
@@ -164,7 +167,6 @@ __global__ void __launch_bounds__(192, 1)
     tma_prefetch(&tmDO);
     tma_prefetch(&tmK);
     tma_prefetch(&tmV);
-    tma_prefetch(&tmKT);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -189,8 +191,8 @@ __global__ void __launch_bounds__(192, 1)
       int issued = 0;
       bool ok = true;
       for (int n = 0; n < nst; ++n) {
-        const int st = n & 1;
-        if (!mbar_wait(kv_empty(st), ((n >> 1) & 1) ^ 1u, p.err, abort_flag)) {
+        const int st = n % G::NSTG;
+        if (!mbar_wait(kv_empty(st), ((n / G::NSTG) & 1) ^ 1u, p.err, abort_flag)) {
           ok = false;
           break;
         }
@@ -200,34 +202,33 @@ __global__ void __launch_bounds__(192, 1)
           tma_load_3d(sK(st) + a * ATOM64, &tmK, kv_full(st), a * 64, n * 64, zk);
           tma_load_3d(sV(st) + a * ATOM64, &tmV, kv_full(st), a * 64, n * 64, zk);
         }
-        tma_load_3d(sKT(st), &tmKT, kv_full(st), n * 64, 0, zk);
         ++issued;
       }
       if (!ok) {  // let this CTA's own copies in flight land
         mbar_wait_slow(q_full, 0, nullptr, nullptr, kDrainLimitNs);
-        for (int n = issued - 1; n >= 0 && n >= issued - 2; --n)
-          mbar_wait_slow(kv_full(n & 1), (n >> 1) & 1, nullptr, nullptr, kDrainLimitNs);
+        for (int n = issued - 1; n >= 0 && n >= issued - G::NSTG; --n)
+          mbar_wait_slow(kv_full(n % G::NSTG), (n / G::NSTG) & 1, nullptr, nullptr, kDrainLimitNs);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       bool ok = mbar_wait(q_full, 0, p.err, abort_flag);
-      auto issue_dq = [&](int m) -> bool {  // dQ += dS(m) K_m
-        const int i = m & 1;
+      auto issue_dq = [&](int m) -> bool {  // dQ += dS(m) K_m, K_m read MN-major (d contiguous)
+        const int i = m & 1, st = m % G::NSTG;
         if (!mbar_wait(ds_full(i), (m >> 1) & 1, p.err, abort_flag)) return false;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_bf16_ss(tQ, sw128_desc(sDS(i) + k * 32), sw128_desc(sKT(i) + k * 32), G::IDESC_Q,
+          mma_bf16_ss(tQ, sw128_desc(sDS(i) + k * 32), sw128_desc_mn(sK(st) + k * 2048, ATOM64), G::IDESC_Q,
                       (m > 0 || k > 0) ? 1u : 0u);
         mma_commit(ds_free(i));
-        mma_commit(kv_empty(i));
+        mma_commit(kv_empty(st));
         return true;
       };
       for (int n = 0; ok && n < nst; ++n) {
-        const int i = n & 1;
+        const int i = n & 1, st = n % G::NSTG;
         const uint32_t ph = (n >> 1) & 1;
-        if (!mbar_wait(kv_full(i), ph, p.err, abort_flag) ||
+        if (!mbar_wait(kv_full(st), (n / G::NSTG) & 1, p.err, abort_flag) ||
             (n >= 2 && !mbar_wait(s_free(i), ph ^ 1u, p.err, abort_flag))) {
           ok = false;
           break;
@@ -236,8 +237,8 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {  // S = Q K^T and dP = dO V^T for keys 64 n ..
           const uint32_t oq = (k >> 2) * ATOM128 + (k & 3) * 32, ok_ = (k >> 2) * ATOM64 + (k & 3) * 32;
-          mma_bf16_ss(tS(i), sw128_desc(sQ + oq), sw128_desc(sK(i) + ok_), G::IDESC_S, k > 0 ? 1u : 0u);
-          mma_bf16_ss(tP(i), sw128_desc(sDO + oq), sw128_desc(sV(i) + ok_), G::IDESC_S, k > 0 ? 1u : 0u);
+          mma_bf16_ss(tS(i), sw128_desc(sQ + oq), sw128_desc(sK(st) + ok_), G::IDESC_S, k > 0 ? 1u : 0u);
+          mma_bf16_ss(tP(i), sw128_desc(sDO + oq), sw128_desc(sV(st) + ok_), G::IDESC_S, k > 0 ? 1u : 0u);
         }
         mma_commit(s_full(i));
         if (n >= 1 && !issue_dq(n - 1)) ok = false;
@@ -247,7 +248,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_wait_slow(done, 0, nullptr, nullptr, ok ? kWaitLimitNs : kDrainLimitNs);
     }
   } else {
-    const int quad = warp & 3;
+    const int quad = warp & 3, half = (warp - 2) >> 2;  // columns [32 half, 32 half + 32) of a step
     const int r = quad * 32 + lane;
     const int qi = qb * 128 + r;  // query row
     const bool row_ok = qi < p.seq;
@@ -264,17 +265,15 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       tc_fence_after();
-      float s[64], dp[64];
-      tmem_ld32(tS(i) + lane_off, s);
-      tmem_ld32(tS(i) + lane_off + 32, s + 32);
-      tmem_ld32(tP(i) + lane_off, dp);
-      tmem_ld32(tP(i) + lane_off + 32, dp + 32);
+      float s[32], dp[32];
+      tmem_ld32(tS(i) + lane_off + 32 * half, s);
+      tmem_ld32(tP(i) + lane_off + 32 * half, dp);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free(i));
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const bool valid = row_ok && n * 64 + c <= qi;
+      for (int c = 0; c < 32; ++c) {
+        const bool valid = row_ok && n * 64 + 32 * half + c <= qi;
         const float pv = valid ? ex2_approx(s[c] * p.scale_log2 - lse) : 0.f;
         s[c] = pv * (dp[c] - dsum) * p.scale;  // dS
       }
@@ -284,7 +283,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       uint8_t* row = base + G::OFF_DS + i * G::DS_BYTES + r * 128;
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) store_row_chunk(row, r, ch, s + 8 * ch);
+      for (int ch = 0; ch < 4; ++ch) store_row_chunk(row, r, 4 * half + ch, s + 8 * ch);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -293,7 +292,7 @@ __global__ void __launch_bounds__(192, 1)
     if (ok && wait_all(done, 0, p.err, abort_flag)) {
       tc_fence_after();
 #pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
+      for (int cc = half * (D / 64); cc < (half + 1) * (D / 64); ++cc) {
         float v[32];
         tmem_ld32(tQ + lane_off + cc * 32, v);
         if (row_ok) {
@@ -317,46 +316,43 @@ template <int D>
 struct GeoKV {
   static constexpr int KV_BYTES = 128 * D * 2;            // K_j or V_j: D/64 blocks of [128 x 64]
   static constexpr int QD_BYTES = 64 * D * 2;             // Q_i or dO_i: D/64 blocks of [64 x 64]
-  static constexpr int T_BYTES = D * 64 * 2;              // Q_i^T or dO_i^T: one [D x 64] block
-  static constexpr int STAGE = 2 * QD_BYTES + 2 * T_BYTES;
+  static constexpr int STAGE = 2 * QD_BYTES;
+  static constexpr int NSTG = 4;                          // query blocks in flight
   static constexpr int PT_BYTES = 128 * 64 * 2;           // P^T or dS^T [128 keys x 64 queries]
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = KV_BYTES;
   static constexpr int OFF_ST = 2 * KV_BYTES;
-  static constexpr int OFF_PT = OFF_ST + 2 * STAGE;
+  static constexpr int OFF_PT = OFF_ST + NSTG * STAGE;
   static constexpr int OFF_DST = OFF_PT + PT_BYTES;
   static constexpr int OFF_BAR = OFF_DST + PT_BYTES;
   static constexpr size_t SMEM_USED = 1024 + OFF_BAR + 256;
   static constexpr size_t SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
   static constexpr uint32_t IDESC_S = idesc_bf16(128, 64);
-  static constexpr uint32_t IDESC_G = idesc_bf16(128, D);
+  static constexpr uint32_t IDESC_G = idesc_bf16_bmn(128, D);  // B = dO_i or Q_i read MN-major
 };
 static_assert(GeoKV<128>::SMEM_USED <= 232448, "dK/dV tiles exceed the shared memory of a CTA");
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                          const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
-                         const __grid_constant__ CUtensorMap tmQT, const __grid_constant__ CUtensorMap tmDOT,
                          const AttnBwdParams p) {
   using G = GeoKV<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + G::OFF_BAR);
-  // bars: kv_full | st_full[2] | st_empty[2] | s_full[2] | s_free[2] | pt_full | pt_free | done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  // bars: kv_full | st_full[4] | st_empty[4] | s_full[2] | s_free[2] | pt_full | pt_free | done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
-  const uint32_t kv_full = bar0, pt_full = bar0 + 8u * 9, pt_free = bar0 + 8u * 10, done = bar0 + 8u * 11;
+  const uint32_t kv_full = bar0, pt_full = bar0 + 8u * 13, pt_free = bar0 + 8u * 14, done = bar0 + 8u * 15;
   auto st_full = [&](int i) { return bar0 + 8u * (1 + i); };
-  auto st_empty = [&](int i) { return bar0 + 8u * (3 + i); };
-  auto s_full = [&](int i) { return bar0 + 8u * (5 + i); };
-  auto s_free = [&](int i) { return bar0 + 8u * (7 + i); };
+  auto st_empty = [&](int i) { return bar0 + 8u * (5 + i); };
+  auto s_full = [&](int i) { return bar0 + 8u * (9 + i); };
+  auto s_free = [&](int i) { return bar0 + 8u * (11 + i); };
   const uint32_t sK = smem_u32(base + G::OFF_K), sV = smem_u32(base + G::OFF_V);
   auto sQ = [&](int st) { return smem_u32(base + G::OFF_ST + st * G::STAGE); };
   auto sDO = [&](int st) { return smem_u32(base + G::OFF_ST + st * G::STAGE + G::QD_BYTES); };
-  auto sQT = [&](int st) { return smem_u32(base + G::OFF_ST + st * G::STAGE + 2 * G::QD_BYTES); };
-  auto sDOT = [&](int st) { return smem_u32(base + G::OFF_ST + st * G::STAGE + 2 * G::QD_BYTES + G::T_BYTES); };
   const uint32_t sPT = smem_u32(base + G::OFF_PT), sDST = smem_u32(base + G::OFF_DST);
 
   pdl_wait();
@@ -374,13 +370,15 @@ __global__ void __launch_bounds__(192, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < G::NSTG; ++i) {
       mbar_init(st_full(i), 1);
       mbar_init(st_empty(i), 1);
-      mbar_init(s_full(i), 1);
-      mbar_init(s_free(i), 4);
     }
-    mbar_init(pt_full, 4);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(s_full(i), 1);
+      mbar_init(s_free(i), 8);
+    }
+    mbar_init(pt_full, 8);
     mbar_init(pt_free, 1);
     mbar_init(done, 1);
     *abort_flag = 0;
@@ -391,8 +389,6 @@ __global__ void __launch_bounds__(192, 1)
     tma_prefetch(&tmV);
     tma_prefetch(&tmQ);
     tma_prefetch(&tmDO);
-    tma_prefetch(&tmQT);
-    tma_prefetch(&tmDOT);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -417,10 +413,10 @@ __global__ void __launch_bounds__(192, 1)
       int issued = 0;
       bool ok = true;
       for (int n = 0; n < nst; ++n) {
-        const int st = n & 1;
+        const int st = n % G::NSTG;
         const int zq = b * p.nh + g * rep + n / per_head;
         const int qi0 = (i0 + n % per_head) * 64;
-        if (!mbar_wait(st_empty(st), ((n >> 1) & 1) ^ 1u, p.err, abort_flag)) {
+        if (!mbar_wait(st_empty(st), ((n / G::NSTG) & 1) ^ 1u, p.err, abort_flag)) {
           ok = false;
           break;
         }
@@ -430,28 +426,26 @@ __global__ void __launch_bounds__(192, 1)
           tma_load_3d(sQ(st) + a * ATOM64, &tmQ, st_full(st), a * 64, qi0, zq);
           tma_load_3d(sDO(st) + a * ATOM64, &tmDO, st_full(st), a * 64, qi0, zq);
         }
-        tma_load_3d(sQT(st), &tmQT, st_full(st), qi0, 0, zq);
-        tma_load_3d(sDOT(st), &tmDOT, st_full(st), qi0, 0, zq);
         ++issued;
       }
       if (!ok) {
         mbar_wait_slow(kv_full, 0, nullptr, nullptr, kDrainLimitNs);
-        for (int n = issued - 1; n >= 0 && n >= issued - 2; --n)
-          mbar_wait_slow(st_full(n & 1), (n >> 1) & 1, nullptr, nullptr, kDrainLimitNs);
+        for (int n = issued - 1; n >= 0 && n >= issued - G::NSTG; --n)
+          mbar_wait_slow(st_full(n % G::NSTG), (n / G::NSTG) & 1, nullptr, nullptr, kDrainLimitNs);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       bool ok = mbar_wait(kv_full, 0, p.err, abort_flag);
-      auto issue_grad = [&](int m) -> bool {  // dV += P^T dO, dK += dS^T Q for step m
-        const int st = m & 1;
+      auto issue_grad = [&](int m) -> bool {  // dV += P^T dO, dK += dS^T Q for step m (dO, Q MN-major)
+        const int st = m % G::NSTG;
         if (!mbar_wait(pt_full, m & 1, p.err, abort_flag)) return false;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          mma_bf16_ss(tV, sw128_desc(sPT + k * 32), sw128_desc(sDOT(st) + k * 32), G::IDESC_G,
+          mma_bf16_ss(tV, sw128_desc(sPT + k * 32), sw128_desc_mn(sDO(st) + k * 2048, ATOM64), G::IDESC_G,
                       (m > 0 || k > 0) ? 1u : 0u);
-          mma_bf16_ss(tK, sw128_desc(sDST + k * 32), sw128_desc(sQT(st) + k * 32), G::IDESC_G,
+          mma_bf16_ss(tK, sw128_desc(sDST + k * 32), sw128_desc_mn(sQ(st) + k * 2048, ATOM64), G::IDESC_G,
                       (m > 0 || k > 0) ? 1u : 0u);
         }
         mma_commit(pt_free);
@@ -459,9 +453,9 @@ __global__ void __launch_bounds__(192, 1)
         return true;
       };
       for (int n = 0; ok && n < nst; ++n) {
-        const int i = n & 1;
+        const int i = n & 1, st = n % G::NSTG;
         const uint32_t ph = (n >> 1) & 1;
-        if (!mbar_wait(st_full(i), ph, p.err, abort_flag) ||
+        if (!mbar_wait(st_full(st), (n / G::NSTG) & 1, p.err, abort_flag) ||
             (n >= 2 && !mbar_wait(s_free(i), ph ^ 1u, p.err, abort_flag))) {
           ok = false;
           break;
@@ -470,8 +464,8 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {  // S^T = K Q^T and dP^T = V dO^T for one 64-query block
           const uint32_t okv = (k >> 2) * ATOM128 + (k & 3) * 32, oq = (k >> 2) * ATOM64 + (k & 3) * 32;
-          mma_bf16_ss(tS(i), sw128_desc(sK + okv), sw128_desc(sQ(i) + oq), G::IDESC_S, k > 0 ? 1u : 0u);
-          mma_bf16_ss(tP(i), sw128_desc(sV + okv), sw128_desc(sDO(i) + oq), G::IDESC_S, k > 0 ? 1u : 0u);
+          mma_bf16_ss(tS(i), sw128_desc(sK + okv), sw128_desc(sQ(st) + oq), G::IDESC_S, k > 0 ? 1u : 0u);
+          mma_bf16_ss(tP(i), sw128_desc(sV + okv), sw128_desc(sDO(st) + oq), G::IDESC_S, k > 0 ? 1u : 0u);
         }
         mma_commit(s_full(i));
         if (n >= 1 && !issue_grad(n - 1)) ok = false;
@@ -481,7 +475,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_wait_slow(done, 0, nullptr, nullptr, ok ? kWaitLimitNs : kDrainLimitNs);
     }
   } else {
-    const int quad = warp & 3;
+    const int quad = warp & 3, half = (warp - 2) >> 2;  // query columns [32 half, 32 half + 32) of a step
     const int r = quad * 32 + lane;
     const int kj = kb * 128 + r;  // key row
     const bool row_ok = kj < p.seq;
@@ -491,30 +485,31 @@ __global__ void __launch_bounds__(192, 1)
       const int i = n & 1;
       const uint32_t ph = (n >> 1) & 1;
       const int zq = b * p.nh + g * rep + n / per_head;
-      const int qi0 = (i0 + n % per_head) * 64;
+      const int qc0 = (i0 + n % per_head) * 64 + 32 * half;  // this warp's first query column
+      // lane l holds the row statistics of query qc0 + l; column c reads them from lane c
+      const int ql = min(qc0 + lane, p.seq - 1);
+      const float lse_l = __ldg(p.lse + static_cast<size_t>(zq) * p.seq + ql);
+      const float dsum_l = __ldg(p.dsum + static_cast<size_t>(zq) * p.seq + ql);
       if (!wait_all(s_full(i), ph, p.err, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float s[64], dp[64];
-      tmem_ld32(tS(i) + lane_off, s);
-      tmem_ld32(tS(i) + lane_off + 32, s + 32);
-      tmem_ld32(tP(i) + lane_off, dp);
-      tmem_ld32(tP(i) + lane_off + 32, dp + 32);
+      float s[32], dp[32];
+      tmem_ld32(tS(i) + lane_off + 32 * half, s);
+      tmem_ld32(tP(i) + lane_off + 32 * half, dp);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free(i));
-      const float* lse = p.lse + static_cast<size_t>(zq) * p.seq;
-      const float* dsum = p.dsum + static_cast<size_t>(zq) * p.seq;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const int qi = qi0 + c;
+      for (int c = 0; c < 32; ++c) {
+        const int qi = qc0 + c;
+        const float lse_c = __shfl_sync(0xffffffffu, lse_l, c);
+        const float dsum_c = __shfl_sync(0xffffffffu, dsum_l, c);
         const bool valid = row_ok && qi < p.seq && qi >= kj;
-        const int qc = qi < p.seq ? qi : p.seq - 1;
-        const float pv = valid ? ex2_approx(s[c] * p.scale_log2 - __ldg(lse + qc)) : 0.f;
-        s[c] = pv;                                           // P^T
-        dp[c] = pv * (dp[c] - __ldg(dsum + qc)) * p.scale;  // dS^T
+        const float pv = valid ? ex2_approx(s[c] * p.scale_log2 - lse_c) : 0.f;
+        s[c] = pv;                                    // P^T
+        dp[c] = pv * (dp[c] - dsum_c) * p.scale;      // dS^T
       }
       if (n >= 1 && !wait_all(pt_free, (n - 1) & 1, p.err, abort_flag)) {
         ok = false;
@@ -523,9 +518,9 @@ __global__ void __launch_bounds__(192, 1)
       uint8_t* prow = base + G::OFF_PT + r * 128;
       uint8_t* drow = base + G::OFF_DST + r * 128;
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        store_row_chunk(prow, r, ch, s + 8 * ch);
-        store_row_chunk(drow, r, ch, dp + 8 * ch);
+      for (int ch = 0; ch < 4; ++ch) {
+        store_row_chunk(prow, r, 4 * half + ch, s + 8 * ch);
+        store_row_chunk(drow, r, 4 * half + ch, dp + 8 * ch);
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -536,7 +531,7 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       const size_t row = static_cast<size_t>(zk) * p.seq + kj;
 #pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
+      for (int cc = half * (D / 64); cc < (half + 1) * (D / 64); ++cc) {
         float v[32], k32[32];
         tmem_ld32(tV + lane_off + cc * 32, v);
         tmem_ld32(tK + lane_off + cc * 32, k32);
@@ -573,12 +568,12 @@ cudaError_t launch_bwd_d(const CUtensorMap* maps, const AttnBwdParams& p, cudaSt
     configured = true;
   }
   const unsigned nb = static_cast<unsigned>((p.seq + 127) / 128);
-  // maps: Q128, dO128, K64, V64, K^T | K128, V128, Q64, dO64, Q^T, dO^T
-  cudaError_t e = launch_pdl(attn_bwd_dq_kernel<D>, dim3(nb * p.batch * p.nh), dim3(192), GeoQ<D>::SMEM, st,
-                             maps[0], maps[1], maps[2], maps[3], maps[4], p);
+  // maps: Q128, dO128, K64, V64 | K128, V128, Q64, dO64
+  cudaError_t e = launch_pdl(attn_bwd_dq_kernel<D>, dim3(nb * p.batch * p.nh), dim3(320), GeoQ<D>::SMEM, st,
+                             maps[0], maps[1], maps[2], maps[3], p);
   if (e != cudaSuccess) return e;
-  return launch_pdl(attn_bwd_dkdv_kernel<D>, dim3(nb * p.batch * p.ng), dim3(192), GeoKV<D>::SMEM, st, maps[5],
-                    maps[6], maps[7], maps[8], maps[9], maps[10], p);
+  return launch_pdl(attn_bwd_dkdv_kernel<D>, dim3(nb * p.batch * p.ng), dim3(320), GeoKV<D>::SMEM, st, maps[4],
+                    maps[5], maps[6], maps[7], p);
 }
 
 }  // namespace

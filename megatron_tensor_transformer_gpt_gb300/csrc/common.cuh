@@ -136,6 +136,21 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
+// Shared-memory descriptor of an MN-major operand stored with the 128-byte swizzle: each 128-byte
+// row holds 64 consecutive M (or N) elements at one K index, 8-row K groups are 1024 B apart and
+// further 64-element M (N) blocks `mn_block_bytes` apart (the leading byte offset); advancing K by
+// 16 adds 2048 B to the start address.  (A tile loaded K-major as [K rows][64 elements] blocks is
+// read this way as the transposed operand.)
+__device__ __forceinline__ uint64_t sw128_desc_mn(uint32_t saddr, uint32_t mn_block_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((mn_block_bytes >> 4) & 0x3FFFu) << 16;  // leading byte offset
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;                       // stride byte offset: 8 K rows
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B (both K-major), fp32 accumulator, M x N tile.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4)                                   // D format: f32
@@ -144,6 +159,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
+
+// As idesc_bf16 with B MN-major (its N index contiguous in shared memory).
+__host__ __device__ constexpr uint32_t idesc_bf16_bmn(int M, int N) { return idesc_bf16(M, N) | (1u << 16); }
 
 // Instruction descriptor, kind::f16 with fp16 A and B (both K-major), fp32 accumulator.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {

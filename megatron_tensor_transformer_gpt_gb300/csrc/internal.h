@@ -132,9 +132,9 @@ int gemm_pair_slots();
 
 // Kernel launchers; return a cudaError_t from the launch.
 // fp8 = true: A and B are E4M3 (tensor maps of bytes, boxes 128 wide).
-// Attention backward: maps = {Q [.,128 rows], dO [.,128], K [.,64], V [.,64], K^T [., d rows] for
-// the dQ kernel; K [.,128], V [.,128], Q [.,64], dO [.,64], Q^T [., d], dO^T [., d] for dK/dV}
-// (bf16, 64-element inner boxes, head-major [z][rows][cols] tensors).
+// Attention backward: maps = {Q [.,128 rows], dO [.,128], K [.,64], V [.,64] for the dQ kernel;
+// K [.,128], V [.,128], Q [.,64], dO [.,64] for dK/dV} (bf16, 64-element inner boxes, head-major
+// [z][seq][d] tensors).
 cudaError_t launch_attention_bwd(int head_dim, const CUtensorMap* maps, const AttnBwdParams& p, cudaStream_t st);
 // Batched copy / transpose of R x C bf16 slices z = 0..Z-1 at src + (z / zdiv) sb + (z % zdiv) sh
 // (row pitch sp) into dst + z R dp (copy, pitch dp) or dst + z C dp (transpose, pitch dp).
