@@ -241,6 +241,15 @@ int mt_layer_launch_count(const mt_layer* L, unsigned long long* count);
  * Device pointers, 16-byte aligned; K % 8 == 0 and N % 8 == 0. */
 int mt_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, void* cuda_stream);
 
+/* C[M, N] = A B^T as mt_gemm_bf16 with either operand stored transposed: a_layout 0 = A is [M, K]
+ * row-major, 1 = A is [K, M] row-major (M contiguous); b_layout 0 = B is [N, K], 1 = B is [K, N].
+ * The tcgen05 MMA reads a transposed operand directly (MN-major shared-memory tiles), the form the
+ * backward pass uses for dW = dY^T X and dX = dY W.  Device pointers, 16-byte aligned; the contiguous
+ * dimension of each operand and N must be multiples of 8 (MT_ERR_UNSUPPORTED otherwise);
+ * MT_ERR_INVALID_ARG for NULL pointers, non-positive sizes or layouts other than 0 and 1. */
+int mt_gemm_bf16_t(const void* A, int a_layout, const void* B, int b_layout, void* C, int M, int N, int K,
+                   void* cuda_stream);
+
 /* GEMM kernel choice for every later launch in the process (all handles): 0 automatic (the
  * default: pairs of CTAs sharing one M = 256 tcgen05.mma per 256 x 256 tile when M > 128 and the
  * GEMM fills at least one wave of SM pairs, else one CTA per 128 x 256 tile), 1 one CTA per tile

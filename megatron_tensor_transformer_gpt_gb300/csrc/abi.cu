@@ -620,29 +620,33 @@ int forward_device_fp8(mt_layer* L, const Layout& lay, const void* x, int S, int
 }
 
 // ------------------------------------------------------------------ backward pass (TP=1)
-// Plain GEMM with strided bf16 operands: out = A[M, K] (pitch lda) * B[N, K]^T (pitch ldb), to bf16
-// `out` or fp32 `out32` (acc32: add to it), pitch ldo.
-int gemm_ab(mt_layer* L, const void* A, size_t lda, const void* Bm, size_t ldb, int M, int N, int K, void* out,
-            float* out32, size_t ldo, bool acc32, cudaStream_t st) {
+// Plain bf16 GEMM out[M, N] = A B^T with fp32 accumulation, to bf16 `out` or fp32 `out32` (acc32: add
+// to it), pitch ldo.  A is stored [M, K] (a_mn = false) or [K, M] (a_mn = true), pitch lda; B is
+// stored [N, K] (b_mn = false) or [K, N] (b_mn = true), pitch ldb.  L may be null (no error word,
+// no launch count).
+int gemm_ab(mt_layer* L, const void* A, size_t lda, bool a_mn, const void* Bm, size_t ldb, bool b_mn, int M, int N,
+            int K, void* out, float* out32, size_t ldo, bool acc32, cudaStream_t st) {
   CUtensorMap ta, tb, tb64;
-  int rc = map_2d(&ta, A, K, M, lda, 128);
-  if (!rc) rc = map_2d(&tb, Bm, K, N, ldb, 128);
-  if (!rc) rc = map_2d(&tb64, Bm, K, N, ldb, 64);
+  int rc = a_mn ? map_2d(&ta, A, M, K, lda, 64) : map_2d(&ta, A, K, M, lda, 128);
+  if (!rc) rc = b_mn ? map_2d(&tb, Bm, N, K, ldb, 64) : map_2d(&tb, Bm, K, N, ldb, 128);
+  if (!rc) rc = b_mn ? map_2d(&tb64, Bm, N, K, ldb, 64) : map_2d(&tb64, Bm, K, N, ldb, 64);
   if (rc) return rc;
-  mt::GemmParams p = gemm_params(M, N, K, false, L->d_err);
+  mt::GemmParams p = gemm_params(M, N, K, false, L != nullptr ? L->d_err : nullptr);
   p.out = static_cast<bf16*>(out);
   p.out32 = out32;
   p.acc32 = acc32 ? 1 : 0;
   p.ldo = static_cast<int>(ldo);
+  p.a_mn = a_mn ? 1 : 0;
+  p.b_mn = b_mn ? 1 : 0;
   plan_gemm(p, mt::kEpiStore, 0);
   count_launch(L);
   cudaError_t e = mt::launch_gemm(mt::kEpiStore, false, ta, tb, tb64, p, st);
-  return e == cudaSuccess ? MT_OK : cuda_fail(e, "backward GEMM launch");
+  return e == cudaSuccess ? MT_OK : cuda_fail(e, "GEMM launch");
 }
 
 enum BwRegion {
   kBQkv = 0, kBU, kBA, kBDa, kBDu, kBDhn, kBDh, kBDo, kBDq, kBDk, kBDv, kBDqkv, kBDxn, kBGrow, kBAcc,
-  kBLse, kBDsum, kBDoH, kBVh, kBWt, kBAt, kBBt, kBNum
+  kBLse, kBDsum, kBDoH, kBVh, kBNum
 };
 
 struct BwLayout {
@@ -677,9 +681,6 @@ BwLayout bw_layout(const mt_layer* L, int S, int B) {
   b.size[kBDsum] = zq * S * 4;
   b.size[kBDoH] = zq * S * d * 2;
   b.size[kBVh] = zk * S * d * 2;
-  b.size[kBWt] = std::max(std::max(QKV * H, H * qw), std::max(f1 * H, H * f)) * 2;
-  b.size[kBAt] = maxc * T * 2;
-  b.size[kBBt] = maxc * T * 2;
   size_t o = b.fwd.total;
   for (int r = 0; r < kBNum; ++r) {
     b.off[r] = o;
@@ -694,35 +695,20 @@ T* bwr(const mt_layer* L, const BwLayout& b, BwRegion r) {
   return reinterpret_cast<T*>(static_cast<char*>(L->ws) + b.off[r]);
 }
 
-// dst = src^T for a bf16 [R, C] matrix with pitch sp into a dense [C, R] buffer.
-int transpose(mt_layer* L, const void* src, size_t sp, void* dst, int R, int C, cudaStream_t st) {
-  count_launch(L);
-  cudaError_t e = mt::launch_transpose(static_cast<const bf16*>(src), sp, static_cast<bf16*>(dst), R, R, C, st);
-  return e == cudaSuccess ? MT_OK : cuda_fail(e, "transpose launch");
-}
-
 // Gradients of one linear Y = X W^T (+ b) given dY (all bf16, dense):
 //   dW [N, K] = dY^T X, db = column sums of dY, dX [M, K] = dY W (written to dx if not null).
 int linear_bwd(mt_layer* L, const BwLayout& b, const void* dY, const void* X, const void* W, int M, int N, int K,
                void* dW, void* db, void* dX, cudaStream_t st) {
   int rc;
-  if (dW != nullptr) {
-    bf16* dYt = bwr<bf16>(L, b, kBAt);
-    bf16* Xt = bwr<bf16>(L, b, kBBt);
-    if ((rc = transpose(L, dY, N, dYt, M, N, st))) return rc;
-    if ((rc = transpose(L, X, K, Xt, M, K, st))) return rc;
-    if ((rc = gemm_ab(L, dYt, M, Xt, M, N, K, M, dW, nullptr, K, false, st))) return rc;
-  }
+  // Y [M, N] = X [M, K] W[N, K]^T:  dW = dY^T X  (both operands read MN-major, no transposes),
+  //                                  dX = dY W    (W read MN-major)
+  if (dW != nullptr && (rc = gemm_ab(L, dY, N, true, X, K, true, N, K, M, dW, nullptr, K, false, st))) return rc;
   if (db != nullptr) {
     count_launch(L);
     cudaError_t e = mt::launch_colsum(dY, false, N, M, N, bwr<float>(L, b, kBAcc), static_cast<bf16*>(db), st);
     if (e != cudaSuccess) return cuda_fail(e, "bias gradient");
   }
-  if (dX != nullptr) {
-    bf16* Wt = bwr<bf16>(L, b, kBWt);
-    if ((rc = transpose(L, W, K, Wt, N, K, st))) return rc;
-    if ((rc = gemm_ab(L, dY, N, Wt, N, M, K, N, dX, nullptr, K, false, st))) return rc;
-  }
+  if (dX != nullptr && (rc = gemm_ab(L, dY, N, false, W, K, true, M, K, N, dX, nullptr, K, false, st))) return rc;
   return MT_OK;
 }
 
@@ -800,21 +786,18 @@ int backward_device(mt_layer* L, const BwLayout& b, const void* x, const void* d
   const int zq = B * nh, zk = B * ng;
   const size_t sd = static_cast<size_t>(S) * d;
   struct Slice {
-    bool tr;
     const bf16* src;
     size_t pitch, sb, sh;
     int zdiv, Z;
     bf16* dst;
-    size_t dp;
   } slices[] = {
-      {false, dO, static_cast<size_t>(B) * qw, static_cast<size_t>(qw), static_cast<size_t>(d), nh, zq, dOh, static_cast<size_t>(d)},
-      {false, qkv + qw + kvw, static_cast<size_t>(B) * QKV, static_cast<size_t>(QKV), static_cast<size_t>(d), ng, zk, Vh,
-       static_cast<size_t>(d)},
+      {dO, static_cast<size_t>(B) * qw, static_cast<size_t>(qw), static_cast<size_t>(d), nh, zq, dOh},
+      {qkv + qw + kvw, static_cast<size_t>(B) * QKV, static_cast<size_t>(QKV), static_cast<size_t>(d), ng, zk, Vh},
   };
   for (const Slice& sl : slices) {
     count_launch(L);
-    if ((e = mt::launch_head_slices(sl.tr, sl.src, sl.pitch, sl.sb, sl.sh, sl.zdiv, sl.Z, sl.dst, sl.dp, S, d, st)) !=
-        cudaSuccess)
+    if ((e = mt::launch_head_slices(sl.src, sl.pitch, sl.sb, sl.sh, sl.zdiv, sl.Z, sl.dst, static_cast<size_t>(d), S,
+                                    d, st)) != cudaSuccess)
       return cuda_fail(e, "attention backward operands");
   }
   count_launch(L);
@@ -1125,6 +1108,20 @@ int mt_gemm_set_pairing(int mode) {
   if (mode < 0 || mode > 2) return fail(MT_ERR_INVALID_ARG, "pairing mode must be 0, 1 or 2 (got %d)", mode);
   g_pairing.store(mode);
   return ok();
+}
+
+int mt_gemm_bf16_t(const void* A, int a_layout, const void* B, int b_layout, void* C, int M, int N, int K,
+                   void* cuda_stream) {
+  if (A == nullptr || B == nullptr || C == nullptr) return fail(MT_ERR_INVALID_ARG, "NULL operand");
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return fail(MT_ERR_INVALID_ARG, "operands must be 16-byte aligned");
+  if (M <= 0 || N <= 0 || K <= 0) return fail(MT_ERR_INVALID_ARG, "M, N, K must be positive");
+  if ((a_layout != 0 && a_layout != 1) || (b_layout != 0 && b_layout != 1))
+    return fail(MT_ERR_INVALID_ARG, "layouts must be 0 or 1 (got %d, %d)", a_layout, b_layout);
+  if ((a_layout ? M : K) % 8 || (b_layout ? N : K) % 8 || N % 8)
+    return fail(MT_ERR_UNSUPPORTED, "the contiguous dimension of each operand and N must be multiples of 8");
+  const int rc = gemm_ab(nullptr, A, a_layout ? M : K, a_layout != 0, B, b_layout ? N : K, b_layout != 0, M, N, K, C,
+                         nullptr, N, false, static_cast<cudaStream_t>(cuda_stream));
+  return rc ? rc : ok();
 }
 
 int mt_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, void* cuda_stream) {

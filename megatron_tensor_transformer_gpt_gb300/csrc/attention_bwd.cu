@@ -12,7 +12,7 @@
 //   attn_bwd_dkdv_kernel: one CTA per (128 keys, kv group); steps over the group's heads and the
 //                         64-query blocks i >= j: S^T and dP^T into TMEM, P^T and dS^T into shared
 //                         memory, dV += P^T dO and dK += dS^T Q in TMEM.
-// The caller provides head-major copies of dO and V (prep kernel below); the second operands of the
+// The caller provides head-major copies of dO and V (head_slices_kernel below); the second operands of the
 // gradient products (K for dQ, dO for dV, Q for dK) are the tiles already staged for the score
 // products, read as MN-major operands.
 #include "common.cuh"
@@ -25,32 +25,17 @@ constexpr int ATOM128 = 128 * 128;  // [128 rows x 64] bf16 block with the 128-b
 constexpr int ATOM64 = 64 * 128;    // [64 rows x 64] block, 8 KB
 
 // ------------------------------------------------------------------ prep
-// Batched copy (TRANS = false: dst[z][r][c]) or transpose (TRANS = true: dst[z][c][r], row pitch
-// dp) of the R x C slices src_z = src + (z / zdiv) * sb + (z % zdiv) * sh (row pitch sp).
-template <bool TRANS>
+// Batched copy of the R x C slices src_z = src + (z / zdiv) * sb + (z % zdiv) * sh (row pitch sp) into
+// dst + z R dp (row pitch dp): the head-major copies of dO and V.
 __global__ void head_slices_kernel(const bf16* __restrict__ src, size_t sp, size_t sb, size_t sh, int zdiv,
                                    bf16* __restrict__ dst, size_t dp, int R, int C) {
-  __shared__ uint16_t tile[32][33];
   const int z = blockIdx.z;
   const uint16_t* s = reinterpret_cast<const uint16_t*>(src + (z / zdiv) * sb + (z % zdiv) * sh);
-  uint16_t* d = reinterpret_cast<uint16_t*>(dst) + static_cast<size_t>(z) * (TRANS ? C * dp : R * dp);
+  uint16_t* d = reinterpret_cast<uint16_t*>(dst) + static_cast<size_t>(z) * R * dp;
   const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
   for (int i = threadIdx.y; i < 32; i += blockDim.y) {
     const int r = r0 + i, c = c0 + threadIdx.x;
-    if (r < R && c < C) {
-      const uint16_t v = s[static_cast<size_t>(r) * sp + c];
-      if (TRANS)
-        tile[i][threadIdx.x] = v;
-      else
-        d[static_cast<size_t>(r) * dp + c] = v;
-    }
-  }
-  if (TRANS) {
-    __syncthreads();
-    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-      const int c = c0 + i, r = r0 + threadIdx.x;
-      if (r < R && c < C) d[static_cast<size_t>(c) * dp + r] = tile[threadIdx.x][i];
-    }
+    if (r < R && c < C) d[static_cast<size_t>(r) * dp + c] = s[static_cast<size_t>(r) * sp + c];
   }
 }
 
@@ -578,14 +563,10 @@ cudaError_t launch_bwd_d(const CUtensorMap* maps, const AttnBwdParams& p, cudaSt
 
 }  // namespace
 
-cudaError_t launch_head_slices(bool transpose, const bf16* src, size_t sp, size_t sb, size_t sh, int zdiv, int Z,
-                               bf16* dst, size_t dp, int R, int C, cudaStream_t st) {
+cudaError_t launch_head_slices(const bf16* src, size_t sp, size_t sb, size_t sh, int zdiv, int Z, bf16* dst, size_t dp,
+                               int R, int C, cudaStream_t st) {
   if (Z <= 0 || R <= 0 || C <= 0) return cudaSuccess;
-  const dim3 grid((C + 31) / 32, (R + 31) / 32, Z), block(32, 8);
-  if (transpose)
-    head_slices_kernel<true><<<grid, block, 0, st>>>(src, sp, sb, sh, zdiv, dst, dp, R, C);
-  else
-    head_slices_kernel<false><<<grid, block, 0, st>>>(src, sp, sb, sh, zdiv, dst, dp, R, C);
+  head_slices_kernel<<<dim3((C + 31) / 32, (R + 31) / 32, Z), dim3(32, 8), 0, st>>>(src, sp, sb, sh, zdiv, dst, dp, R, C);
   return cudaGetLastError();
 }
 

@@ -27,64 +27,7 @@ __device__ __forceinline__ float cta_sum(float v, float* red) {
   return t;
 }
 
-// dst[c][r] = src[r][c] for an R x C bf16 matrix (pitches in elements); 32 x 32 tiles.
-__global__ void transpose_kernel(const bf16* __restrict__ src, size_t sp, bf16* __restrict__ dst, size_t dp, int R,
-                                 int C) {
-  __shared__ uint16_t tile[32][33];
-  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
-  const uint16_t* s = reinterpret_cast<const uint16_t*>(src);
-  uint16_t* d = reinterpret_cast<uint16_t*>(dst);
-  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-    const int r = r0 + i, c = c0 + threadIdx.x;
-    if (r < R && c < C) tile[i][threadIdx.x] = s[static_cast<size_t>(r) * sp + c];
-  }
-  __syncthreads();
-  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-    const int c = c0 + i, r = r0 + threadIdx.x;
-    if (r < R && c < C) d[static_cast<size_t>(c) * dp + r] = tile[threadIdx.x][i];
-  }
-}
-
 __device__ __forceinline__ float sigmoidf(float g) { return 1.0f / (1.0f + expf(-g)); }
-
-// dst[c][r] = src[r][c] in 64 x 64 tiles with 16-byte loads and stores (pitches multiples of 8
-// elements); the tile passes through shared memory with a 2-element pad per row.
-__global__ void __launch_bounds__(256) transpose64_kernel(const bf16* __restrict__ src, size_t sp,
-                                                          bf16* __restrict__ dst, size_t dp, int R, int C) {
-  __shared__ uint16_t tile[64][66];
-  const int c0 = blockIdx.x * 64, r0 = blockIdx.y * 64;
-  const uint16_t* s = reinterpret_cast<const uint16_t*>(src);
-  uint16_t* d = reinterpret_cast<uint16_t*>(dst);
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int idx = threadIdx.x + 256 * i, r = idx >> 3, c = (idx & 7) * 8;
-    const size_t at = static_cast<size_t>(r0 + r) * sp + c0 + c;
-    if (r0 + r < R && c0 + c + 8 <= C) {
-      const uint4 v = *reinterpret_cast<const uint4*>(s + at);
-      const uint16_t* e = reinterpret_cast<const uint16_t*>(&v);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) tile[r][c + k] = e[k];
-    } else if (r0 + r < R) {
-      for (int k = 0; k < 8 && c0 + c + k < C; ++k) tile[r][c + k] = s[at + k];
-    }
-  }
-  __syncthreads();
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int idx = threadIdx.x + 256 * i, oc = idx >> 3, r = (idx & 7) * 8;  // output row = input column
-    const size_t at = static_cast<size_t>(c0 + oc) * dp + r0 + r;
-    if (c0 + oc >= C) continue;
-    if (r0 + r + 8 <= R) {
-      uint4 v;
-      uint16_t* e = reinterpret_cast<uint16_t*>(&v);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) e[k] = tile[r + k][oc];
-      *reinterpret_cast<uint4*>(d + at) = v;
-    } else {
-      for (int k = 0; k < 8 && r0 + r + k < R; ++k) d[at + k] = tile[r + k][oc];
-    }
-  }
-}
 
 // SwiGLU / GeLU(tanh) forward from the stored fc1 output u: a = silu(u[:, :f]) u[:, f:] or gelu(u).
 __global__ void act_fwd_kernel(const bf16* __restrict__ u, bf16* __restrict__ a, size_t T, int f, int swiglu) {
@@ -256,17 +199,6 @@ __global__ void rope_bwd_pack_kernel(const float* __restrict__ dq, const float* 
 }
 
 }  // namespace
-
-cudaError_t launch_transpose(const bf16* src, size_t sp, bf16* dst, size_t dp, int R, int C, cudaStream_t st) {
-  if (R <= 0 || C <= 0) return cudaSuccess;
-  const bool vec = sp % 8 == 0 && dp % 8 == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0 &&
-                   (reinterpret_cast<uintptr_t>(dst) & 15) == 0;
-  if (vec)
-    transpose64_kernel<<<dim3((C + 63) / 64, (R + 63) / 64), 256, 0, st>>>(src, sp, dst, dp, R, C);
-  else
-    transpose_kernel<<<dim3((C + 31) / 32, (R + 31) / 32), dim3(32, 8), 0, st>>>(src, sp, dst, dp, R, C);
-  return cudaGetLastError();
-}
 
 // Blocks of 256 threads for T x f / 8 vectors: one pass, at most 32 blocks per SM.
 static unsigned act_grid(size_t T, int f) {

@@ -345,8 +345,15 @@ __global__ void __launch_bounds__(192, 1)
           mbar_arrive_expect_tx(fb, stage_bytes);
           const uint32_t a_dst = smem_u32(sA + stage * A_BYTES);
           const uint32_t b_dst = smem_u32(sB + stage * B_BYTES);
-          tma_load_2d(a_dst, &tmA, fb, kb * KB, m0);
-          if (MODE == kEpiSwiglu) {
+          if (!F8 && p.a_mn) {  // A stored [K, M]: two [64 K x 64 M] blocks
+            tma_load_2d(a_dst, &tmA, fb, m0, kb * KB);
+            tma_load_2d(a_dst + 8192, &tmA, fb, m0 + 64, kb * KB);
+          } else {
+            tma_load_2d(a_dst, &tmA, fb, kb * KB, m0);
+          }
+          if (!F8 && MODE == kEpiStore && p.b_mn) {  // B stored [K, N]: width / 64 blocks of [64 K x 64 N]
+            for (int a = 0; a < width / 64; ++a) tma_load_2d(b_dst + a * 8192, &tmB, fb, c0 + 64 * a, kb * KB);
+          } else if (MODE == kEpiSwiglu) {
             const CUtensorMap* mb = width == 128 ? &tmB : &tmB64;
             tma_load_2d(b_dst, mb, fb, kb * KB, c0);
             tma_load_2d(b_dst + width * 128, mb, fb, kb * KB, c0 + p.b_row_step);
@@ -378,7 +385,8 @@ __global__ void __launch_bounds__(192, 1)
         const Unit w = decode_unit(p, u);
         const int width = unit_width<MODE>(w);
         const int n_mma = MODE == kEpiSwiglu ? 2 * width : width;
-        const uint32_t idesc = F8 ? idesc_e4m3(BM, n_mma) : idesc_bf16(BM, n_mma);
+        const uint32_t idesc = F8 ? idesc_e4m3(BM, n_mma)
+                                  : (idesc_bf16(BM, n_mma) | (p.a_mn ? 1u << 15 : 0u) | (p.b_mn ? 1u << 16 : 0u));
         const int acc = it & 1;
         const uint32_t use = (it >> 1) & 1;
         if (!mbar_wait(tempty(acc), use ^ 1u, p.err, abort_flag)) {
@@ -393,14 +401,17 @@ __global__ void __launch_bounds__(192, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t ad = sw128_desc(smem_u32(sA + stage * A_BYTES));
-          const uint64_t bd = sw128_desc(smem_u32(sB + stage * B_BYTES));
+          // K-major tiles advance 32 B per 16-deep K step, MN-major tiles 2048 B (16 K rows)
+          const uint32_t a_s = smem_u32(sA + stage * A_BYTES), b_s = smem_u32(sB + stage * B_BYTES);
+          const uint64_t ad = (!F8 && p.a_mn) ? sw128_desc_mn(a_s, 8192) : sw128_desc(a_s);
+          const uint64_t bd = (!F8 && p.b_mn) ? sw128_desc_mn(b_s, 8192) : sw128_desc(b_s);
+          const uint64_t astep = (!F8 && p.a_mn) ? 128ull : 2ull, bstep = (!F8 && p.b_mn) ? 128ull : 2ull;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
             if (F8)
               mma_e4m3_ss(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb | k) != 0 ? 1u : 0u);
             else
-              mma_bf16_ss(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb | k) != 0 ? 1u : 0u);
+              mma_bf16_ss(d_tmem, ad + astep * k, bd + bstep * k, idesc, (kb | k) != 0 ? 1u : 0u);
           mma_commit(empty(stage));
           if (++stage == STAGES) {
             stage = 0;
@@ -529,8 +540,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           }
           const uint32_t fb = map_to_rank(full(stage), 0);
           if (leader) mbar_arrive_expect_tx(full(stage), pair_bytes);
-          tma_load_2d_pair(smem_u32(sA + stage * A_BYTES), &tmA, fb, kb * KB, m0);
-          tma_load_2d_pair(smem_u32(sB + stage * P_B_BYTES), mb, fb, kb * KB, b_row0);
+          const uint32_t a_dst = smem_u32(sA + stage * A_BYTES), b_dst = smem_u32(sB + stage * P_B_BYTES);
+          if (!F8 && p.a_mn) {  // A stored [K, M]: two [64 K x 64 M] blocks
+            tma_load_2d_pair(a_dst, &tmA, fb, m0, kb * KB);
+            tma_load_2d_pair(a_dst + 8192, &tmA, fb, m0 + 64, kb * KB);
+          } else {
+            tma_load_2d_pair(a_dst, &tmA, fb, kb * KB, m0);
+          }
+          if (!F8 && MODE == kEpiStore && p.b_mn) {  // B stored [K, N]: b_rows / 64 blocks of [64 K x 64 N]
+            for (int a = 0; a < b_rows / 64; ++a) tma_load_2d_pair(b_dst + a * 8192, &tmB, fb, b_row0 + 64 * a, kb * KB);
+          } else {
+            tma_load_2d_pair(b_dst, mb, fb, kb * KB, b_row0);
+          }
           ++issued;
           if (++stage == P_STAGES) {
             stage = 0;
@@ -553,7 +574,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         const Unit w = decode_unit(p, u);
         const int width = unit_width<MODE>(w);
         const int n_mma = MODE == kEpiSwiglu ? 2 * width : width;
-        const uint32_t idesc = F8 ? idesc_e4m3(2 * BM, n_mma) : idesc_bf16(2 * BM, n_mma);
+        const uint32_t idesc = F8 ? idesc_e4m3(2 * BM, n_mma)
+                                  : (idesc_bf16(2 * BM, n_mma) | (p.a_mn ? 1u << 15 : 0u) | (p.b_mn ? 1u << 16 : 0u));
         const int acc = it & 1;
         const uint32_t use = (it >> 1) & 1;
         if (!mbar_wait(tempty(acc), use ^ 1u, p.err, abort_flag)) {
@@ -568,14 +590,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t ad = sw128_desc(smem_u32(sA + stage * A_BYTES));
-          const uint64_t bd = sw128_desc(smem_u32(sB + stage * P_B_BYTES));
+          const uint32_t a_s = smem_u32(sA + stage * A_BYTES), b_s = smem_u32(sB + stage * P_B_BYTES);
+          const uint64_t ad = (!F8 && p.a_mn) ? sw128_desc_mn(a_s, 8192) : sw128_desc(a_s);
+          const uint64_t bd = (!F8 && p.b_mn) ? sw128_desc_mn(b_s, 8192) : sw128_desc(b_s);
+          const uint64_t astep = (!F8 && p.a_mn) ? 128ull : 2ull, bstep = (!F8 && p.b_mn) ? 128ull : 2ull;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
             if (F8)
               mma_e4m3_pair(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb | k) ? 1u : 0u);
             else
-              mma_bf16_pair(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb | k) ? 1u : 0u);
+              mma_bf16_pair(d_tmem, ad + astep * k, bd + bstep * k, idesc, (kb | k) ? 1u : 0u);
           mma_commit_pair(empty(stage));
           if (++stage == P_STAGES) {
             stage = 0;

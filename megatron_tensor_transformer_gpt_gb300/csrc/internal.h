@@ -33,6 +33,10 @@ struct GemmParams {
   // CTA pairs (pair = 1): tiles are 256 x 256 and computed by a cluster of two CTAs sharing one
   // M = 256 MMA (tiles_m counts 256-row tiles); otherwise one CTA per 128 x 256 tile.
   int pair;
+  // Operand layouts (bf16 only): a_mn = 1 when A is stored [K, M] (M contiguous) instead of [M, K];
+  // b_mn = 1 when B is stored [K, N] instead of [N, K].  The tensor maps then hold 64 x 64 boxes
+  // (64 M or N elements by 64 K rows) and the MMA reads the tiles MN-major.  Plain stores only.
+  int a_mn, b_mn;
   bf16* out;
   int ldo;
   const bf16* bias;   // [N] (SwiGLU: [2N]) or null
@@ -136,10 +140,10 @@ int gemm_pair_slots();
 // K [.,128], V [.,128], Q [.,64], dO [.,64] for dK/dV} (bf16, 64-element inner boxes, head-major
 // [z][seq][d] tensors).
 cudaError_t launch_attention_bwd(int head_dim, const CUtensorMap* maps, const AttnBwdParams& p, cudaStream_t st);
-// Batched copy / transpose of R x C bf16 slices z = 0..Z-1 at src + (z / zdiv) sb + (z % zdiv) sh
-// (row pitch sp) into dst + z R dp (copy, pitch dp) or dst + z C dp (transpose, pitch dp).
-cudaError_t launch_head_slices(bool transpose, const bf16* src, size_t sp, size_t sb, size_t sh, int zdiv, int Z,
-                               bf16* dst, size_t dp, int R, int C, cudaStream_t st);
+// Batched copy of R x C bf16 slices z = 0..Z-1 at src + (z / zdiv) sb + (z % zdiv) sh (row pitch sp)
+// into dst + z R dp (row pitch dp).
+cudaError_t launch_head_slices(const bf16* src, size_t sp, size_t sb, size_t sh, int zdiv, int Z, bf16* dst, size_t dp,
+                               int R, int C, cudaStream_t st);
 // Dsum[(b nh + h) S + s] = dO[s b, h] . O[s b, h] over the head's d columns.
 cudaError_t launch_row_dot(const bf16* dO, const bf16* O, float* Dsum, int S, int B, int nh, int d, cudaStream_t st);
 
@@ -160,7 +164,6 @@ cudaError_t launch_norm(bool layer_norm, const bf16* x, const bf16* g, const bf1
 cudaError_t launch_quantize_e4m3(const bf16* x, size_t n, uint8_t* q, float* slot, cudaStream_t stream);
 
 // ---- backward pass (backward_kernels.cu)
-cudaError_t launch_transpose(const bf16* src, size_t sp, bf16* dst, size_t dp, int R, int C, cudaStream_t st);
 cudaError_t launch_act_fwd(const bf16* u, bf16* a, size_t T, int f, bool swiglu, cudaStream_t st);
 cudaError_t launch_act_bwd(const bf16* u, const bf16* da, bf16* du, size_t T, int f, bool swiglu, cudaStream_t st);
 cudaError_t launch_norm_bwd(const bf16* dy, const bf16* x, const bf16* gamma, const bf16* add, bf16* out, float* grow,

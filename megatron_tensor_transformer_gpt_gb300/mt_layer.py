@@ -68,6 +68,8 @@ _SIGS = {
     "mt_last_error": ([], ctypes.c_char_p),
     "mt_layer_destroy": ([ctypes.c_void_p], None),
     "mt_gemm_set_pairing": ([ctypes.c_int], ctypes.c_int),
+    "mt_gemm_bf16_t": ([ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                        ctypes.c_int, ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
     "mt_gemm_bf16": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                       ctypes.c_void_p], ctypes.c_int),
     "mt_selftest_bounded_wait": ([ctypes.c_int], ctypes.c_int),
@@ -272,6 +274,10 @@ def mt_quantize_e4m3(src, n, dst, amax_deq, stream):
 
 def mt_gemm_e4m3(A, B, C, M, N, K, deq_a, deq_b, stream):
     _check(lib().mt_gemm_e4m3(A, B, C, M, N, K, deq_a, deq_b, stream))
+
+
+def mt_gemm_bf16_t(A, a_layout, B, b_layout, C, M, N, K, stream):
+    _check(lib().mt_gemm_bf16_t(A, a_layout, B, b_layout, C, M, N, K, stream))
 
 
 def mt_gemm_set_pairing(mode):

@@ -104,3 +104,11 @@ def test_gemm_pairing_mode_is_checked(lib):
 def test_profile_mask_and_launch_count_check_arguments(lib):
     assert lib.mt_layer_profile_enable(None, 1) == ml.MT_ERR_INVALID_ARG
     assert lib.mt_layer_launch_count(None, None) == ml.MT_ERR_INVALID_ARG
+
+
+def test_transposed_gemm_checks_arguments(lib):
+    a = ctypes.c_void_p(0x1000)
+    assert lib.mt_gemm_bf16_t(None, 0, a, 0, a, 8, 8, 8, None) == ml.MT_ERR_INVALID_ARG
+    assert lib.mt_gemm_bf16_t(a, 2, a, 0, a, 8, 8, 8, None) == ml.MT_ERR_INVALID_ARG
+    assert lib.mt_gemm_bf16_t(a, 1, a, 0, a, 12, 8, 16, None) == ml.MT_ERR_UNSUPPORTED  # A [K, M] needs M % 8
+    assert lib.mt_gemm_bf16_t(a, 0, a, 1, a, 8, 12, 16, None) == ml.MT_ERR_UNSUPPORTED  # B [K, N] needs N % 8

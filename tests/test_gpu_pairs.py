@@ -67,6 +67,25 @@ def test_pairs_and_single_agree_bitwise():
     assert torch.equal(out[0], out[1])
 
 
+@pytest.mark.parametrize("mode", [2, 1], ids=["pairs", "single"])
+@pytest.mark.parametrize("a_layout,b_layout", [(0, 1), (1, 1), (1, 0)], ids=["B_KN", "A_KM_B_KN", "A_KM"])
+@pytest.mark.parametrize("M,N,K", [(256, 512, 128), (520, 264, 1000), (1000, 1376, 688), (4096, 1024, 4104)])
+def test_gemm_transposed_operands(M, N, K, a_layout, b_layout, mode):
+    """Operands stored [K, M] / [K, N] are read MN-major by the MMA (the backward's dW and dX form)."""
+    ml.mt_gemm_set_pairing(mode)
+    rng = np.random.default_rng(M + 3 * N + 7 * K + 11 * a_layout + 13 * b_layout)
+    a = synth.f32_to_bf16_bits(rng.standard_normal((M, K), dtype=np.float32))
+    b = synth.f32_to_bf16_bits(rng.standard_normal((N, K), dtype=np.float32))
+    A = to_dev(np.ascontiguousarray(a.T) if a_layout else a)
+    B = to_dev(np.ascontiguousarray(b.T) if b_layout else b)
+    C = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ml.mt_gemm_bf16_t(A.data_ptr(), a_layout, B.data_ptr(), b_layout, C.data_ptr(), M, N, K, _stream())
+    torch.cuda.synchronize()
+    want = ol.linear(ol.bf16_to_f64(a), ol.bf16_to_f64(b))
+    err = np.abs(to_f64(C) - want)
+    assert np.all(err <= 4e-3 * np.abs(want) + 1e-3 * np.max(np.abs(want))), err.max()
+
+
 @pytest.mark.parametrize("M,N,K", [(300, 520, 208), (1000, 1376, 688), (2048, 3072, 4096)])
 def test_gemm_e4m3(M, N, K):
     a = synth.random_e4m3_codes((M, K), seed=M + 3 * K)
