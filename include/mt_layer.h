@@ -195,14 +195,15 @@ int mt_layer_backward_workspace_bytes(const mt_layer* L, int seq, int batch, siz
 
 /* dx [T, H] = dL/dx and the requested weight gradients, given x and dy = dL/dy [T, H].  Needs
  * tp_size == 1, seq % 8 == 0 and a workspace of mt_layer_backward_workspace_bytes.  Asynchronous
- * on cuda_stream (many launches: the attention part runs head by head). */
+ * on cuda_stream: the forward recomputed, then the GEMMs, elementwise kernels and the two
+ * flash-attention backward kernels (dQ; dK and dV), all on the stream. */
 int mt_layer_backward(mt_layer* L, const void* x, const void* dy, int seq, int batch, const mt_weights* w, void* dx,
                       const mt_grads* g, void* cuda_stream);
 
 /* Where an intermediate lives inside the workspace (for inspection in tests).  `which`:
  * 0 norm1 out [T,H]; 1 q [batch, nh_r, seq, d] after RoPE; 2 k [batch, ng_r, seq, d] after RoPE;
- * 3 v transposed [batch, ng_r, d, seq_pad] in fp16 (seq_pad = seq rounded up to 8; the attention's
- *   P V product runs on fp16 P and V, so |v| must stay below 65504);
+ * 3 v [batch, ng_r, seq, d] in fp16 (the attention's P V product runs on fp16 P and V, so |v|
+ *   must stay below 65504);
  * 4 attention out [T, q_w]; 5 h [T,H]; 6 norm2 out [T,H]; 7 MLP hidden [T, f_r];
  * 8 RoPE table [seq, d/2] float2 (cos, sin). */
 int mt_layer_workspace_region(const mt_layer* L, int seq, int batch, int which, size_t* offset, size_t* bytes);

@@ -110,28 +110,26 @@ void count_launch(mt_layer* L) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // ------------------------------------------------------------------ workspace layout
-enum Region { kXn = 0, kQ, kK, kVt, kO, kH, kHn, kA, kRope, kXStage, kYStage, kPos, kVcol, kNumRegions };
+enum Region { kXn = 0, kQ, kK, kV, kO, kH, kHn, kA, kRope, kXStage, kYStage, kPos, kNumRegions };
 
 struct Layout {
   size_t off[kNumRegions];
   size_t size[kNumRegions];
   size_t total;
-  int seq_pad;
 };
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Workspace of one call: S x B tokens; v^T rows of `vt_pitch` columns; a RoPE table of `rope_rows`
-// positions; `index_tokens` per-token position / v^T-column entries (packed samples only).
-Layout make_layout(const mt_layer* L, int S, int B, int vt_pitch, int rope_rows, int index_tokens) {
+// Workspace of one call: S x B tokens; a RoPE table of `rope_rows` positions; `index_tokens`
+// per-token positions (packed samples only).
+Layout make_layout(const mt_layer* L, int S, int B, int rope_rows, int index_tokens) {
   Layout lay{};
   const size_t T = static_cast<size_t>(S) * B;
   const size_t d = L->head_dim;
-  lay.seq_pad = vt_pitch;
   lay.size[kXn] = T * L->hidden * 2;
   lay.size[kQ] = static_cast<size_t>(B) * L->nh_r * S * d * 2;
   lay.size[kK] = static_cast<size_t>(B) * L->ng_r * S * d * 2;
-  lay.size[kVt] = static_cast<size_t>(B) * L->ng_r * d * lay.seq_pad * 2;
+  lay.size[kV] = static_cast<size_t>(B) * L->ng_r * S * d * 2;
   lay.size[kO] = T * L->q_w * 2;
   lay.size[kH] = T * L->hidden * 2;
   lay.size[kHn] = T * L->hidden * 2;
@@ -140,7 +138,6 @@ Layout make_layout(const mt_layer* L, int S, int B, int vt_pitch, int rope_rows,
   lay.size[kXStage] = T * L->hidden * 2;
   lay.size[kYStage] = T * L->hidden * 2;
   lay.size[kPos] = static_cast<size_t>(index_tokens) * sizeof(int);
-  lay.size[kVcol] = static_cast<size_t>(index_tokens) * sizeof(int);
   size_t o = 0;
   for (int r = 0; r < kNumRegions; ++r) {
     lay.off[r] = o;
@@ -151,15 +148,11 @@ Layout make_layout(const mt_layer* L, int S, int B, int vt_pitch, int rope_rows,
 }
 
 Layout layout_for(const mt_layer* L, int S, int B) {
-  return make_layout(L, S, B, static_cast<int>(round_up(S, 8)), S, 0);
+  return make_layout(L, S, B, S, 0);
 }
 
-// Packed samples: batch 1, T tokens; every sample's v^T columns start on a multiple of 8, at most
-// 8 columns after the previous sample's end.
-int packed_vcols(int T, int num_seqs) { return static_cast<int>(round_up(static_cast<size_t>(T) + 8 * num_seqs, 8)); }
-Layout layout_packed(const mt_layer* L, int T, int num_seqs, int max_seqlen) {
-  return make_layout(L, T, 1, packed_vcols(T, num_seqs), max_seqlen, T);
-}
+// Packed samples: batch 1, T tokens.
+Layout layout_packed(const mt_layer* L, int T, int max_seqlen) { return make_layout(L, T, 1, max_seqlen, T); }
 
 // Packed-sample description of a call (null for dense batches).
 struct Packed {
@@ -380,16 +373,11 @@ int run_attention_block(mt_layer* L, const Layout& lay, const void* x, int S, in
     e = mt::launch_rope_table(rope, L->d_theta, pk ? pk->max_seqlen : S, d / 2, st);
     if (e != cudaSuccess) return cuda_fail(e, "RoPE table launch");
   }
-  int *pos = nullptr, *vcol = nullptr;
+  int* pos = nullptr;
   if (pk != nullptr) {
-    // v^T columns between samples are never written: zero them so masked P.V stays finite
-    e = cudaMemsetAsync(region<void>(L, lay, kVt), 0, lay.size[kVt], st);
-    if (e == cudaSuccess) {
-      pos = region<int>(L, lay, kPos);
-      vcol = region<int>(L, lay, kVcol);
-      count_launch(L);
-      e = mt::launch_packed_index(pk->cu, pk->num_seqs, T, pk->max_seqlen, lay.seq_pad, pos, vcol, L->d_err, st);
-    }
+    pos = region<int>(L, lay, kPos);
+    count_launch(L);
+    e = mt::launch_packed_index(pk->cu, pk->num_seqs, T, pk->max_seqlen, pos, L->d_err, st);
     if (e != cudaSuccess) return cuda_fail(e, "packed-sample index");
   }
   bf16* xn = region<bf16>(L, lay, kXn);
@@ -400,13 +388,14 @@ int run_attention_block(mt_layer* L, const Layout& lay, const void* x, int S, in
   }
   if (e != cudaSuccess) return cuda_fail(e, "norm1 launch");
 
-  bf16 *q = region<bf16>(L, lay, kQ), *k = region<bf16>(L, lay, kK), *vt = region<bf16>(L, lay, kVt);
+  bf16 *q = region<bf16>(L, lay, kQ), *k = region<bf16>(L, lay, kK);
+  __half* v = region<__half>(L, lay, kV);
   const int nqkv = L->q_w + 2 * L->kv_w;
   mt::GemmParams p = gemm_params(T, nqkv, H, false, L->d_err);
   p.bias = static_cast<const bf16*>(w->b_qkv);
   p.q = q;
   p.k = k;
-  p.vt = vt;
+  p.v = v;
   p.rope = rope;
   p.seq = S;
   p.batch = B;
@@ -415,18 +404,14 @@ int run_attention_block(mt_layer* L, const Layout& lay, const void* x, int S, in
   p.kv_w = L->kv_w;
   p.nh = L->nh_r;
   p.ng = L->ng_r;
-  p.seq_pad = lay.seq_pad;
   p.pos = pos;
-  p.vcol = vcol;
   int rc = run_gemm(L, kSlotQkv, mt::kEpiQkv, xn, H, w->w_qkv, nqkv, T, nqkv, H, p, st);
   if (rc) return rc;
 
   CUtensorMap tq, tk, tv;
   if ((rc = map_3d(&tq, q, d, S, static_cast<uint64_t>(B) * L->nh_r, d, static_cast<uint64_t>(S) * d, 128))) return rc;
   if ((rc = map_3d(&tk, k, d, S, static_cast<uint64_t>(B) * L->ng_r, d, static_cast<uint64_t>(S) * d, 128))) return rc;
-  if ((rc = map_3d(&tv, vt, pk ? lay.seq_pad : S, d, static_cast<uint64_t>(B) * L->ng_r, lay.seq_pad,
-                   static_cast<uint64_t>(d) * lay.seq_pad, static_cast<uint32_t>(d))))
-    return rc;
+  if ((rc = map_3d(&tv, v, d, S, static_cast<uint64_t>(B) * L->ng_r, d, static_cast<uint64_t>(S) * d, 128))) return rc;
   bf16* o = region<bf16>(L, lay, kO);
   mt::AttnParams ap{};
   ap.seq = S;
@@ -522,13 +507,14 @@ int forward_device_fp8(mt_layer* L, const Layout& lay, const void* x, int S, int
                         static_cast<const bf16*>(w->norm1_b), nullptr, T, H, L->eps, st, xn8, scale + 0, amax + 0);
   }
   if (e != cudaSuccess) return cuda_fail(e, "norm1 launch");
-  bf16 *q = region<bf16>(L, lay, kQ), *k = region<bf16>(L, lay, kK), *vt = region<bf16>(L, lay, kVt);
+  bf16 *q = region<bf16>(L, lay, kQ), *k = region<bf16>(L, lay, kK);
+  __half* v = region<__half>(L, lay, kV);
   const int nqkv = L->q_w + 2 * L->kv_w;
   mt::GemmParams p = gemm_params(T, nqkv, H, false, L->d_err);
   p.bias = static_cast<const bf16*>(w->b_qkv);
   p.q = q;
   p.k = k;
-  p.vt = vt;
+  p.v = v;
   p.rope = rope;
   p.seq = S;
   p.batch = B;
@@ -537,7 +523,6 @@ int forward_device_fp8(mt_layer* L, const Layout& lay, const void* x, int S, int
   p.kv_w = L->kv_w;
   p.nh = L->nh_r;
   p.ng = L->ng_r;
-  p.seq_pad = lay.seq_pad;
   p.deq_a = deq + 0;
   p.deq_b = w8->deq_qkv;
   int rc = run_gemm(L, kSlotQkv, mt::kEpiQkv, xn8, H, w8->w_qkv, nqkv, T, nqkv, H, p, st, true);
@@ -546,9 +531,7 @@ int forward_device_fp8(mt_layer* L, const Layout& lay, const void* x, int S, int
   CUtensorMap tq, tk, tv;
   if ((rc = map_3d(&tq, q, d, S, static_cast<uint64_t>(B) * L->nh_r, d, static_cast<uint64_t>(S) * d, 128))) return rc;
   if ((rc = map_3d(&tk, k, d, S, static_cast<uint64_t>(B) * L->ng_r, d, static_cast<uint64_t>(S) * d, 128))) return rc;
-  if ((rc = map_3d(&tv, vt, S, d, static_cast<uint64_t>(B) * L->ng_r, lay.seq_pad,
-                   static_cast<uint64_t>(d) * lay.seq_pad, static_cast<uint32_t>(d))))
-    return rc;
+  if ((rc = map_3d(&tv, v, d, S, static_cast<uint64_t>(B) * L->ng_r, d, static_cast<uint64_t>(S) * d, 128))) return rc;
   uint8_t* o8 = region<uint8_t>(L, lay, kO);
   mt::AttnParams ap{};
   ap.seq = S;
@@ -988,7 +971,7 @@ int mt_layer_workspace_bytes_packed(const mt_layer* L, int total_tokens, int num
   if (L == nullptr || bytes == nullptr) return fail(MT_ERR_INVALID_ARG, "handle or bytes is NULL");
   if (total_tokens <= 0 || num_seqs <= 0 || max_seqlen <= 0 || max_seqlen > total_tokens)
     return fail(MT_ERR_INVALID_ARG, "need total_tokens > 0, num_seqs > 0, 0 < max_seqlen <= total_tokens");
-  *bytes = layout_packed(L, total_tokens, num_seqs, max_seqlen).total;
+  *bytes = layout_packed(L, total_tokens, max_seqlen).total;
   return ok();
 }
 
@@ -1001,8 +984,8 @@ int mt_layer_forward_packed(mt_layer* L, const void* x, int total_tokens, const 
     return fail(MT_ERR_INVALID_ARG, "x/y must be 16-byte and cu_seqlens 4-byte aligned");
   if (total_tokens <= 0 || num_seqs <= 0 || max_seqlen <= 0 || max_seqlen > total_tokens)
     return fail(MT_ERR_INVALID_ARG, "need total_tokens > 0, num_seqs > 0, 0 < max_seqlen <= total_tokens");
-  if (static_cast<long long>(total_tokens) + 8LL * num_seqs > (1LL << 30)) return fail(MT_ERR_UNSUPPORTED, "too many tokens");
-  const Layout lay = layout_packed(L, total_tokens, num_seqs, max_seqlen);
+  if (total_tokens > (1 << 30)) return fail(MT_ERR_UNSUPPORTED, "too many tokens");
+  const Layout lay = layout_packed(L, total_tokens, max_seqlen);
   if (L->ws == nullptr || L->ws_bytes < lay.total)
     return fail(MT_ERR_NO_WORKSPACE, "workspace missing or smaller than the %zu bytes this call needs", lay.total);
   int rc = check_weights(L, w, true, true);

@@ -7,9 +7,8 @@
 //
 // One CTA per (128-query block, head, batch row); CTAs are issued longest-first (the last query
 // blocks see the most keys).  Per CTA:
-//   warp 0      TMA: the Q tile once, then K [128 keys x d] and V^T [d x 128 keys] tiles into a
-//               2-stage ring.  V is stored transposed by the QKV GEMM so both MMAs read K-major
-//               operands.
+//   warp 0      TMA: the Q tile once, then K and V tiles [128 keys x d] into a 2-stage ring.  The
+//               P V product reads the V tile as an MN-major operand (its d index contiguous).
 //   warp 1      one thread issues S_j = Q K_j^T into one of two TMEM score buffers (128 columns
 //               each), and O += P_j V_j into a TMEM output accumulator (d columns).
 //   warps 2..5  softmax, one query row per thread: reads S_j from TMEM, masks the diagonal
@@ -43,10 +42,10 @@ __device__ __forceinline__ float row_max(const float* s) {
 }
 
 // What one CTA works on: query block qb of a sequence whose rows start at q_row0 - qb*128 and
-// whose keys start at kv_row0 (rows of the [b, head, s, d] q/k buffers), v^T columns at v_col0,
-// `len` tokens long; batch row b, head (or first head of the pair) h.
+// whose keys start at kv_row0 (rows of the [b, head, s, d] q, k, v buffers), `len` tokens long;
+// batch row b, head (or first head of the pair) h.
 struct Work {
-  int qb, b, h, q_row0, kv_row0, v_col0, len;
+  int qb, b, h, q_row0, kv_row0, len;
 };
 
 // Dense batches: blockIdx -> (query block, longest first; batch row; head slot).  Packed samples:
@@ -62,7 +61,6 @@ __device__ __forceinline__ bool decode_work(const AttnParams& p, int heads_slots
     w.h = head_step * (rem - w.b * heads_slots);
     w.q_row0 = w.qb * BQ;
     w.kv_row0 = 0;
-    w.v_col0 = 0;
     w.len = p.seq;
     return true;
   }
@@ -77,7 +75,6 @@ __device__ __forceinline__ bool decode_work(const AttnParams& p, int heads_slots
   if (start < 0 || w.len <= w.qb * BQ || start + w.len > p.seq) return false;
   w.q_row0 = start + w.qb * BQ;
   w.kv_row0 = start;
-  w.v_col0 = 8 * ((start + 7) / 8) + 8 * sid;
   return true;
 }
 
@@ -86,8 +83,7 @@ struct Geo {
   static constexpr int ATOM = 128 * 128;          // one [128 rows x 64 bf16] swizzle block, 16 KB
   static constexpr int Q_BYTES = BQ * D * 2;      // D/64 atoms
   static constexpr int K_BYTES = BKV * D * 2;     // D/64 atoms
-  static constexpr int V_ATOM = D * 128;          // [D rows x 64 keys]
-  static constexpr int V_BYTES = 2 * V_ATOM;      // two key halves
+  static constexpr int V_BYTES = BKV * D * 2;     // [128 keys x D]: D/64 atoms
   static constexpr int P_BYTES = BQ * BKV * 2;    // two key halves of 16 KB
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
@@ -99,7 +95,7 @@ struct Geo {
   static constexpr size_t SMEM_USED = 1024 + OFF_BAR + 256;
   static constexpr size_t SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
   static constexpr uint32_t IDESC_S = idesc_bf16(BQ, BKV);
-  static constexpr uint32_t IDESC_O = idesc_f16(BQ, D);  // fp16 P and v^T
+  static constexpr uint32_t IDESC_O = idesc_f16(BQ, D) | (1u << 16);  // fp16 P (K-major), fp16 V (MN-major)
 };
 
 template <int D>
@@ -126,7 +122,7 @@ __global__ void __launch_bounds__(192, 1)
   auto sKa = [&](int st) { return smem_u32(base + G::OFF_K + st * G::K_BYTES); };
   auto sVa = [&](int st) { return smem_u32(base + G::OFF_V + st * G::V_BYTES); };
 
-  pdl_wait();  // q, k, v^T (and cu_seqlens) are written by the kernels before
+  pdl_wait();  // q, k, v (and cu_seqlens) are written by the kernels before
   pdl_trigger();
   Work wk;
   if (!decode_work(p, p.nh, 1, wk)) return;  // uniform over the CTA, before any barrier or TMEM use
@@ -182,8 +178,8 @@ __global__ void __launch_bounds__(192, 1)
         for (int a = 0; a < D / 64; ++a)
           tma_load_3d(sKa(st) + a * G::ATOM, &tmK, kv_full(st), a * 64, wk.kv_row0 + j * BKV, b * p.ng + g);
 #pragma unroll
-        for (int a = 0; a < 2; ++a)
-          tma_load_3d(sVa(st) + a * G::V_ATOM, &tmV, kv_full(st), wk.v_col0 + j * BKV + a * 64, 0, b * p.ng + g);
+        for (int a = 0; a < D / 64; ++a)
+          tma_load_3d(sVa(st) + a * G::ATOM, &tmV, kv_full(st), a * 64, wk.kv_row0 + j * BKV, b * p.ng + g);
         ++issued;
       }
       if (!ok) {  // let this CTA's own copies in flight land
@@ -224,8 +220,8 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
         for (int k = 0; k < BKV / 16; ++k) {
           const uint32_t pa = sPa + (k >> 2) * G::ATOM + (k & 3) * 32;
-          const uint32_t va = sVa(st) + (k >> 2) * G::V_ATOM + (k & 3) * 32;
-          mma_bf16_ss(tO, sw128_desc(pa), sw128_desc(va), G::IDESC_O, (j > 0 || k > 0) ? 1u : 0u);
+          mma_bf16_ss(tO, sw128_desc(pa), sw128_desc_mn(sVa(st) + k * 2048, G::ATOM), G::IDESC_O,
+                      (j > 0 || k > 0) ? 1u : 0u);
         }
         mma_commit(kv_empty(st));
         mma_commit(o_done);
@@ -366,8 +362,7 @@ struct Geo2 {
   static constexpr int ATOM = 128 * 128;        // [128 rows x 64 fp16/bf16] swizzle block, 16 KB
   static constexpr int Q_BYTES = BQ * D * 2;    // per head
   static constexpr int K_BYTES = BKV * D * 2;
-  static constexpr int V_ATOM = D * 128;        // [d rows x 64 keys]
-  static constexpr int V_BYTES = 2 * V_ATOM;
+  static constexpr int V_BYTES = BKV * D * 2;  // [128 keys x d]: d/64 atoms
   static constexpr int P_BYTES = BQ * BKV * 2;  // per head: two key halves of 16 KB
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = 2 * Q_BYTES;
@@ -377,7 +372,7 @@ struct Geo2 {
   static constexpr size_t SMEM_USED = 1024 + OFF_BAR + 256;
   static constexpr size_t SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;  // one CTA per SM (TMEM)
   static constexpr uint32_t IDESC_S = idesc_bf16(BQ, BKV);
-  static constexpr uint32_t IDESC_O = idesc_f16(BQ, D);  // fp16 P and v^T
+  static constexpr uint32_t IDESC_O = idesc_f16(BQ, D) | (1u << 16);  // fp16 P (K-major), fp16 V (MN-major)
 };
 static_assert(Geo2<128>::SMEM_USED <= 232448, "attention tiles exceed the shared memory of a CTA");
 
@@ -408,7 +403,7 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t sVa = smem_u32(base + G::OFF_V);
   auto sPa = [&](int t) { return smem_u32(base + G::OFF_P + t * G::P_BYTES); };
 
-  pdl_wait();  // q, k, v^T (and cu_seqlens) are written by the kernels before
+  pdl_wait();  // q, k, v (and cu_seqlens) are written by the kernels before
   pdl_trigger();
   Work wk;
   if (!decode_work(p, p.nh >> 1, 2, wk)) return;  // uniform over the CTA, before any barrier or TMEM use
@@ -474,8 +469,8 @@ __global__ void __launch_bounds__(320, 1)
         if (!mbar_wait(v_empty, (j & 1) ^ 1u, p.err, abort_flag)) return false;
         mbar_arrive_expect_tx(v_full, G::V_BYTES);
 #pragma unroll
-        for (int a = 0; a < 2; ++a)
-          tma_load_3d(sVa + a * G::V_ATOM, &tmV, v_full, wk.v_col0 + j * BKV + a * 64, 0, b * p.ng + g);
+        for (int a = 0; a < D / 64; ++a)
+          tma_load_3d(sVa + a * G::ATOM, &tmV, v_full, a * 64, wk.kv_row0 + j * BKV, b * p.ng + g);
         ++issued_v;
         return true;
       };
@@ -541,8 +536,8 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int k = 0; k < BKV / 16; ++k) {
             const uint32_t pa = sPa(t) + (k >> 2) * G::ATOM + (k & 3) * 32;
-            const uint32_t va = sVa + (k >> 2) * G::V_ATOM + (k & 3) * 32;
-            mma_bf16_ss(tO(t), sw128_desc(pa), sw128_desc(va), G::IDESC_O, (j > 0 || k > 0) ? 1u : 0u);
+            mma_bf16_ss(tO(t), sw128_desc(pa), sw128_desc_mn(sVa + k * 2048, G::ATOM), G::IDESC_O,
+                        (j > 0 || k > 0) ? 1u : 0u);
           }
           mma_commit(o_done(t));
         }

@@ -311,12 +311,11 @@ cudaError_t launch_sp_ln(const SpParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-// Per-token index of packed samples: token t of sample i (cu[i] <= t < cu[i+1]) has RoPE
-// position t - cu[i] and v^T column 8*ceil(cu[i]/8) + 8*i + (t - cu[i]) (every sample starts on
-// a 16-byte boundary of v^T, as the TMA loads need).  Inconsistent cu_seqlens are reported in
-// *err and mapped to index 0, which keeps every later access in bounds.
-__global__ void packed_index_kernel(const int* __restrict__ cu, int n, int T, int max_len, int vcols,
-                                    int* __restrict__ pos, int* __restrict__ vcol, int* err) {
+// Per-token RoPE position of packed samples: token t of sample i (cu[i] <= t < cu[i+1]) has
+// position t - cu[i].  Inconsistent cu_seqlens are reported in *err and mapped to position 0, which
+// keeps every later access in bounds.
+__global__ void packed_index_kernel(const int* __restrict__ cu, int n, int T, int max_len, int* __restrict__ pos,
+                                    int* err) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= T) return;
   bool ok = (t != 0 || (cu[0] == 0 && cu[n] == T));
@@ -328,11 +327,9 @@ __global__ void packed_index_kernel(const int* __restrict__ cu, int n, int T, in
   }
   const int start = cu[lo], end = cu[lo + 1];
   const int p = t - start;
-  const int v = 8 * ((start + 7) / 8) + 8 * lo + p;
-  ok = ok && start <= t && t < end && p < max_len && start >= 0 && v < vcols;
+  ok = ok && start <= t && t < end && p < max_len && start >= 0;
   if (!ok) atomicCAS(err, 0, 1);  // MT_ERR_INVALID_ARG
   pos[t] = ok ? p : 0;
-  vcol[t] = ok ? v : 0;
 }
 
 }  // namespace
@@ -378,10 +375,10 @@ cudaError_t launch_sp_add_norm(bool layer_norm, const SpParams& p, cudaStream_t 
   return layer_norm ? launch_sp_ln<true>(p, stream) : launch_sp_ln<false>(p, stream);
 }
 
-cudaError_t launch_packed_index(const int* cu, int num_seqs, int tokens, int max_seqlen, int vcols, int* pos, int* vcol,
-                                int* err, cudaStream_t stream) {
+cudaError_t launch_packed_index(const int* cu, int num_seqs, int tokens, int max_seqlen, int* pos, int* err,
+                                cudaStream_t stream) {
   if (tokens <= 0) return cudaSuccess;
-  packed_index_kernel<<<(tokens + 255) / 256, 256, 0, stream>>>(cu, num_seqs, tokens, max_seqlen, vcols, pos, vcol, err);
+  packed_index_kernel<<<(tokens + 255) / 256, 256, 0, stream>>>(cu, num_seqs, tokens, max_seqlen, pos, err);
   return cudaGetLastError();
 }
 

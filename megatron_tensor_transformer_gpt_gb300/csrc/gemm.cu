@@ -196,13 +196,12 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
     const int s = valid ? row / p.batch : 0;  // row of the [b, head, s, d] buffers
     const int b = valid ? row - s * p.batch : 0;
     const int rpos = (valid && p.pos != nullptr) ? p.pos[row] : s;    // RoPE position
-    const int vc = (valid && p.vcol != nullptr) ? p.vcol[row] : s;    // column of v^T
 #pragma unroll 1
     for (int hc = 0; hc < width; hc += d) {
       const int col = c0 + hc;
       if (col >= p.N) break;
-      bf16* dst;
-      bool is_v = false;
+      bf16* dst = nullptr;
+      __half* vdst = nullptr;
       if (col < p.q_w) {
         const int hh = col / d;
         dst = p.q + ((static_cast<size_t>(b) * p.nh + hh) * p.seq + s) * d;
@@ -211,10 +210,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
         dst = p.k + ((static_cast<size_t>(b) * p.ng + gg) * p.seq + s) * d;
       } else {
         const int gg = (col - p.q_w - p.kv_w) / d;
-        dst = p.vt + (static_cast<size_t>(b) * p.ng + gg) * d * p.seq_pad + vc;
-        is_v = true;
+        vdst = p.v + ((static_cast<size_t>(b) * p.ng + gg) * p.seq + s) * d;
       }
-      if (!is_v && p.rope != nullptr) {
+      if (vdst == nullptr && p.rope != nullptr) {
         // rotate-half: (x_i, x_{i+d/2}) -> (x_i c - x_{i+d/2} s, x_{i+d/2} c + x_i s)
 #pragma unroll 1
         for (int i0 = 0; i0 < half; i0 += 32) {
@@ -252,10 +250,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
           if (valid) {
             if (F8) scale32(x, deq);
             if (p.bias != nullptr) add_vec32(x, p.bias, col + i0, p.N);
-            if (is_v) {
+            if (vdst != nullptr) {
 #pragma unroll
-              for (int e = 0; e < 32; ++e)  // v^T is fp16: the P V product takes fp16 P
-                reinterpret_cast<__half*>(dst)[static_cast<size_t>(i0 + e) * p.seq_pad] = __float2half_rn(x[e]);
+              for (int g8 = 0; g8 < 4; ++g8) *reinterpret_cast<uint4*>(vdst + i0 + 8 * g8) = pack_f16x8(x + 8 * g8);
             } else {
               store_vec32(dst, i0, d, x);
             }

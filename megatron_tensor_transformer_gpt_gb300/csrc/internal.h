@@ -3,6 +3,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -15,7 +16,7 @@ using bf16 = __nv_bfloat16;
 enum GemmEpilogue : int {
   kEpiStore = 0,   // out = acc (+ bias)
   kEpiResid = 1,   // out = acc (+ bias) + resid            (row-parallel output + bias-dropout-add)
-  kEpiQkv = 2,     // bias, RoPE on q/k heads, scatter q/k to [b, head, s, d] and v to [b, group, d, s]
+  kEpiQkv = 2,     // bias, RoPE on q/k heads, scatter q/k to [b, head, s, d] and v (fp16) to [b, group, s, d]
   kEpiSwiglu = 3,  // out = silu(gate + b_gate) * (up + b_up); the tile holds 128 gate and 128 up columns
   kEpiGelu = 4,    // out = gelu_tanh(acc + bias)
 };
@@ -43,12 +44,12 @@ struct GemmParams {
   const bf16* resid;  // [M, ldr] or null
   int ldr;
   // kEpiQkv only
-  bf16 *q, *k, *vt;
+  bf16 *q, *k;
+  __half* v;           // fp16: the P V product of the attention takes fp16 P
   const float2* rope;  // [positions, d/2] (cos, sin) or null
-  int seq, batch, head_dim, q_w, kv_w, nh, ng, seq_pad;
-  // packed samples (batch 1): per-token RoPE position and column of v^T; null for dense batches
+  int seq, batch, head_dim, q_w, kv_w, nh, ng;
+  // packed samples (batch 1): per-token RoPE position; null for dense batches
   const int* pos;
-  const int* vcol;
   // E4M3 operands: the fp32 accumulator is multiplied by (*deq_a) * (*deq_b); null for bf16
   const float* deq_a;
   const float* deq_b;
@@ -66,8 +67,8 @@ struct GemmParams {
 struct AttnParams {
   int seq, batch, nh, ng;  // this rank's query heads and kv groups
   int num_qb;              // ceil(seq / 128); packed samples: ceil(max_seqlen / 128)
-  // Packed samples (batch 1, seq = all tokens): sample i is tokens [cu[i], cu[i+1]); its v^T
-  // columns start at 8*ceil(cu[i]/8) + 8*i.  null for dense batches.
+  // Packed samples (batch 1, seq = all tokens): sample i is tokens [cu[i], cu[i+1]), rows
+  // [cu[i], cu[i+1]) of q, k and v.  null for dense batches.
   const int* cu;
   int num_seqs;
   float scale_log2;        // log2(e) / sqrt(head_dim)
@@ -179,10 +180,10 @@ cudaError_t launch_rope_table(float2* table, const double* theta, int seq, int h
 
 cudaError_t launch_sp_add_norm(bool layer_norm, const SpParams& p, cudaStream_t stream);
 
-// Per-token RoPE position and v^T column of packed samples; invalid cu_seqlens record
-// MT_ERR_INVALID_ARG in *err and give in-range indices.
-cudaError_t launch_packed_index(const int* cu, int num_seqs, int tokens, int max_seqlen, int vcols, int* pos, int* vcol,
-                                int* err, cudaStream_t stream);
+// Per-token RoPE position of packed samples; invalid cu_seqlens record MT_ERR_INVALID_ARG in *err
+// and give in-range positions.
+cudaError_t launch_packed_index(const int* cu, int num_seqs, int tokens, int max_seqlen, int* pos, int* err,
+                                cudaStream_t stream);
 
 cudaError_t launch_wait_selftest(int* err, unsigned long long limit_ns, cudaStream_t stream);
 

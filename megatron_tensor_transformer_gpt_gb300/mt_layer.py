@@ -23,7 +23,7 @@ WEIGHT_FIELDS = ("norm1_w", "norm1_b", "w_qkv", "b_qkv", "w_o", "b_o",
                  "norm2_w", "norm2_b", "w_fc1", "b_fc1", "w_fc2", "b_fc2")
 
 # workspace regions (mt_layer_workspace_region)
-REGION = {"xn": 0, "q": 1, "k": 2, "vt": 3, "o": 4, "h": 5, "hn": 6, "a": 7, "rope": 8}
+REGION = {"xn": 0, "q": 1, "k": 2, "v": 3, "o": 4, "h": 5, "hn": 6, "a": 7, "rope": 8}
 
 
 class MtWeights(ctypes.Structure):

@@ -87,9 +87,8 @@ def test_intermediates_match_oracle(cfg):
     assert_layer_close(q, ref["q"].reshape(S, B, nh, d).transpose(1, 2, 0, 3), "q after RoPE")
     k = reg("k", (B, ng, S, d))
     assert_layer_close(k, ref["k"].reshape(S, B, ng, d).transpose(1, 2, 0, 3), "k after RoPE")
-    sp = (S + 7) // 8 * 8
-    vt = reg("vt", (B, ng, d, sp), torch.float16)[..., :S]
-    assert_layer_close(vt, ref["v"].reshape(S, B, ng, d).transpose(1, 2, 3, 0), "v transposed")
+    v = reg("v", (B, ng, S, d), torch.float16)
+    assert_layer_close(v, ref["v"].reshape(S, B, ng, d).transpose(1, 2, 0, 3), "v (fp16)")
     assert_layer_close(reg("o", (T, nh * d)), ref["o"], "attention output")
     full = ol.layer_forward(cfg, inp)
     assert_layer_close(reg("h", (T, cfg.hidden)), full["h"], "h")
