@@ -352,22 +352,22 @@ __global__ void __launch_bounds__(192, 1)
 //   The softmax warps of a head read S_t into registers and release it at once (s_free), so the
 //   tensor core computes S_t(j+1) while they turn S_t(j) into P_t(j); P goes to shared memory (fp16,
 //   128-byte swizzle, per head) and O_t += P_t V_j reads it from there.
-//   Shared memory: Q of both heads, a two-slot K ring, one V slot and the two P tiles.  The
-//   producer keeps K two blocks ahead of V: K_{j+2} may load once both S(j) are done, V_{j+1} once
-//   both P V(j) are.
+//   Shared memory: Q of both heads, a three-slot ring of K and V tiles and the two P tiles.  Tiles
+//   enter the ring in the order K0, K1, V0, K2, V1, K3, ..., each taking the slot of the tile three
+//   places earlier: V_j loads as soon as both S(j) are done and K_{j+2} as soon as both P V(j-1)
+//   are, so each tile has about one block of lead time.  The softmax forms P_t(j) in registers
+//   before it waits for P_t(j-1) V_{j-1}, and only the shared-memory stores wait.
 //   10 warps put three warps on some SM sub-partitions, whose 16K-register files then allow 168
 //   registers per thread.
 template <int D>
 struct Geo2 {
   static constexpr int ATOM = 128 * 128;        // [128 rows x 64 fp16/bf16] swizzle block, 16 KB
   static constexpr int Q_BYTES = BQ * D * 2;    // per head
-  static constexpr int K_BYTES = BKV * D * 2;
-  static constexpr int V_BYTES = BKV * D * 2;  // [128 keys x d]: d/64 atoms
+  static constexpr int KV_BYTES = BKV * D * 2;  // a K or V tile [128 keys x d]: d/64 atoms
   static constexpr int P_BYTES = BQ * BKV * 2;  // per head: two key halves of 16 KB
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = 2 * Q_BYTES;
-  static constexpr int OFF_V = OFF_K + 2 * K_BYTES;
-  static constexpr int OFF_P = OFF_V + V_BYTES;
+  static constexpr int OFF_KV = 2 * Q_BYTES;  // three-slot ring shared by K and V tiles
+  static constexpr int OFF_P = OFF_KV + 3 * KV_BYTES;
   static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
   static constexpr size_t SMEM_USED = 1024 + OFF_BAR + 256;
   static constexpr size_t SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;  // one CTA per SM (TMEM)
@@ -384,23 +384,23 @@ __global__ void __launch_bounds__(320, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + G::OFF_BAR);
-  // bars: q_full | k_full[2] | k_empty[2] | v_full | v_empty | s_full[2] | s_free[2] | p_full[2] |
+  // bars: q_full | kv_full[3] | kv_empty[3] | s_full[2] | s_free[2] | p_full[2] |
   //       o_done[2] | drain
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
   const uint32_t q_full = bar0;
-  auto k_full = [&](int i) { return bar0 + 8u * (1 + i); };
-  auto k_empty = [&](int i) { return bar0 + 8u * (3 + i); };
-  const uint32_t v_full = bar0 + 8u * 5, v_empty = bar0 + 8u * 6;
+  // tile number n of the load sequence sits in ring slot n % 3, in that slot's (n / 3)-th use
+  auto kv_full = [&](int n) { return bar0 + 8u * (1 + n % 3); };
+  auto kv_empty = [&](int n) { return bar0 + 8u * (4 + n % 3); };
+  auto use_parity = [](int n) { return static_cast<uint32_t>((n / 3) & 1); };
   auto s_full = [&](int t) { return bar0 + 8u * (7 + t); };
   auto s_free = [&](int t) { return bar0 + 8u * (9 + t); };
   auto p_full = [&](int t) { return bar0 + 8u * (11 + t); };
   auto o_done = [&](int t) { return bar0 + 8u * (13 + t); };
   const uint32_t drain = bar0 + 8u * 15;
   auto sQa = [&](int t) { return smem_u32(base + G::OFF_Q + t * G::Q_BYTES); };
-  auto sKa = [&](int st) { return smem_u32(base + G::OFF_K + st * G::K_BYTES); };
-  const uint32_t sVa = smem_u32(base + G::OFF_V);
+  auto sKV = [&](int n) { return smem_u32(base + G::OFF_KV + (n % 3) * G::KV_BYTES); };
   auto sPa = [&](int t) { return smem_u32(base + G::OFF_P + t * G::P_BYTES); };
 
   pdl_wait();  // q, k, v (and cu_seqlens) are written by the kernels before
@@ -414,16 +414,16 @@ __global__ void __launch_bounds__(320, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    for (int i = 0; i < 3; ++i) {
+      mbar_init(kv_full(i), 1);
+      mbar_init(kv_empty(i), 1);
+    }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(k_full(i), 1);
-      mbar_init(k_empty(i), 1);
       mbar_init(s_full(i), 1);
       mbar_init(s_free(i), 4);
       mbar_init(p_full(i), 4);
       mbar_init(o_done(i), 1);
     }
-    mbar_init(v_full, 1);
-    mbar_init(v_empty, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -452,62 +452,56 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int a = 0; a < D / 64; ++a)
           tma_load_3d(sQa(t) + a * G::ATOM, &tmQ, q_full, a * 64, wk.q_row0, b * p.nh + h0 + t);
-      // load order K0, K1, V0, K2, V1, K3, V2, ...: K_{j+2} before V_{j+1}
-      int issued_k = 0, issued_v = 0;
-      bool ok = true;
-      auto load_k = [&](int j) -> bool {
-        const int st = j & 1;
-        if (!mbar_wait(k_empty(st), ((j >> 1) & 1) ^ 1u, p.err, abort_flag)) return false;
-        mbar_arrive_expect_tx(k_full(st), G::K_BYTES);
+      // Load sequence K0, K1, V0, K2, V1, K3, V2, ..., K(n-1), V(n-2), V(n-1) through the ring:
+      // tile n reuses the slot of tile n - 3, so V_j waits only for S(j) (K_j's slot) and K_{j+2}
+      // for P V(j-1) (V_{j-1}'s slot), each a block ahead of its own use.
+      int issued = 0;
+      auto load = [&](const CUtensorMap* map, int j) -> bool {
+        const int n = issued;
+        if (!mbar_wait(kv_empty(n), use_parity(n) ^ 1u, p.err, abort_flag)) return false;
+        mbar_arrive_expect_tx(kv_full(n), G::KV_BYTES);
 #pragma unroll
         for (int a = 0; a < D / 64; ++a)
-          tma_load_3d(sKa(st) + a * G::ATOM, &tmK, k_full(st), a * 64, wk.kv_row0 + j * BKV, b * p.ng + g);
-        ++issued_k;
+          tma_load_3d(sKV(n) + a * G::ATOM, map, kv_full(n), a * 64, wk.kv_row0 + j * BKV, b * p.ng + g);
+        ++issued;
         return true;
       };
-      auto load_v = [&](int j) -> bool {
-        if (!mbar_wait(v_empty, (j & 1) ^ 1u, p.err, abort_flag)) return false;
-        mbar_arrive_expect_tx(v_full, G::V_BYTES);
-#pragma unroll
-        for (int a = 0; a < D / 64; ++a)
-          tma_load_3d(sVa + a * G::ATOM, &tmV, v_full, a * 64, wk.kv_row0 + j * BKV, b * p.ng + g);
-        ++issued_v;
-        return true;
-      };
-      ok = load_k(0) && (nkv < 2 || load_k(1));
+      bool ok = load(&tmK, 0) && (nkv < 2 || load(&tmK, 1));
       for (int j = 0; ok && j < nkv; ++j) {
-        ok = load_v(j);
-        if (ok && j + 2 < nkv) ok = load_k(j + 2);
+        ok = load(&tmV, j);
+        if (ok && j + 2 < nkv) ok = load(&tmK, j + 2);
       }
       if (!ok) {  // let this CTA's own copies in flight land
         mbar_wait_slow(q_full, 0, nullptr, nullptr, kDrainLimitNs);
-        for (int j = issued_k - 1; j >= 0 && j >= issued_k - 2; --j)
-          mbar_wait_slow(k_full(j & 1), (j >> 1) & 1, nullptr, nullptr, kDrainLimitNs);
-        if (issued_v > 0) mbar_wait_slow(v_full, (issued_v - 1) & 1, nullptr, nullptr, kDrainLimitNs);
+        for (int n = issued - 1; n >= 0 && n >= issued - 3; --n)
+          mbar_wait_slow(kv_full(n), use_parity(n), nullptr, nullptr, kDrainLimitNs);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      auto issue_s = [&](int t, int st) {
+      // tile numbers of K_j and V_j in the loader's sequence
+      auto tile_k = [](int j) { return j < 2 ? j : 2 * j - 1; };
+      auto tile_v = [nkv](int j) { return (nkv > 1 ? 2 : 1) + 2 * j - ((j == nkv - 1 && nkv >= 2) ? 1 : 0); };
+      auto issue_s = [&](int t, int n) {
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * G::ATOM + (k & 3) * 32;
-          mma_bf16_ss(tS(t), sw128_desc(sQa(t) + off), sw128_desc(sKa(st) + off), G::IDESC_S, k > 0 ? 1u : 0u);
+          mma_bf16_ss(tS(t), sw128_desc(sQa(t) + off), sw128_desc(sKV(n) + off), G::IDESC_S, k > 0 ? 1u : 0u);
         }
         mma_commit(s_full(t));
       };
-      bool ok = mbar_wait(q_full, 0, p.err, abort_flag) && mbar_wait(k_full(0), 0, p.err, abort_flag);
+      bool ok = mbar_wait(q_full, 0, p.err, abort_flag) && mbar_wait(kv_full(0), use_parity(0), p.err, abort_flag);
       if (ok) {
         tc_fence_after();
         issue_s(0, 0);
         issue_s(1, 0);
-        mma_commit(k_empty(0));
+        mma_commit(kv_empty(0));
       }
       for (int j = 0; ok && j < nkv; ++j) {
         // S(j+1) of both heads as soon as their softmax has taken S(j) into registers
         if (j + 1 < nkv) {
-          const int st1 = (j + 1) & 1;
-          if (!mbar_wait(k_full(st1), ((j + 1) >> 1) & 1, p.err, abort_flag)) {
+          const int nk = tile_k(j + 1);
+          if (!mbar_wait(kv_full(nk), use_parity(nk), p.err, abort_flag)) {
             ok = false;
             break;
           }
@@ -517,13 +511,15 @@ __global__ void __launch_bounds__(320, 1)
               break;
             }
             tc_fence_after();
-            issue_s(t, st1);
+            issue_s(t, nk);
           }
           if (!ok) break;
-          mma_commit(k_empty(st1));
+          mma_commit(kv_empty(nk));
         }
         // O_t += P_t(j) V_j once the softmax has written P_t(j)
-        if (!mbar_wait(v_full, j & 1, p.err, abort_flag)) {
+        const int nv = tile_v(j);
+        const uint32_t sV = sKV(nv);
+        if (!mbar_wait(kv_full(nv), use_parity(nv), p.err, abort_flag)) {
           ok = false;
           break;
         }
@@ -536,13 +532,13 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int k = 0; k < BKV / 16; ++k) {
             const uint32_t pa = sPa(t) + (k >> 2) * G::ATOM + (k & 3) * 32;
-            mma_bf16_ss(tO(t), sw128_desc(pa), sw128_desc_mn(sVa + k * 2048, G::ATOM), G::IDESC_O,
+            mma_bf16_ss(tO(t), sw128_desc(pa), sw128_desc_mn(sV + k * 2048, G::ATOM), G::IDESC_O,
                         (j > 0 || k > 0) ? 1u : 0u);
           }
           mma_commit(o_done(t));
         }
         if (!ok) break;
-        mma_commit(v_empty);
+        mma_commit(kv_empty(nv));
       }
       mma_commit(drain);
       mbar_wait_slow(drain, 0, nullptr, nullptr, ok ? kWaitLimitNs : kDrainLimitNs);
@@ -578,17 +574,47 @@ __global__ void __launch_bounds__(320, 1)
       }
       const float mx = row_max(s);
       const float m_new = fmaxf(m_used, mx * c);
+      const bool grow = __any_sync(0xffffffffu, m_new > m_used + 8.0f);
+      float alpha = 1.f;
+      if (grow) {
+        alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m_used - m_new);
+        m_used = m_new;
+      }
+      // P = 2^(s c - m) in packed halves, formed in registers while the tensor core still runs
+      // P_t(j-1) V_{j-1}: one fp32x2 FMA, one fp16x2 conversion and one fp16x2 exponential per pair
+      // of scores (the argument is at most 8 after the lazy rescaling, so its fp16 rounding moves P
+      // by under 0.6%, the order of P's own 16-bit rounding); row sums in four fp16x2 partial sums
+      // per 64 keys, widened to fp32 once per block.
+      uint32_t pk[BKV / 2];
+      float rs = 0.f;
+      {
+        const float2 cc = make_float2(c, c), mm = make_float2(-m_used, -m_used);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          __half2 acc[4] = {__float2half2_rn(0.f), __float2half2_rn(0.f), __float2half2_rn(0.f),
+                            __float2half2_rn(0.f)};
+#pragma unroll
+          for (int q = 0; q < 32; ++q) {
+            const int i = 64 * hf + 2 * q;
+            const float2 xy = ffma2(make_float2(s[i], s[i + 1]), cc, mm);
+            pk[32 * hf + q] = ex2_f16x2(pack_f16x2(xy.x, xy.y));
+            acc[q & 3] = __hadd2(acc[q & 3], *reinterpret_cast<const __half2*>(&pk[32 * hf + q]));
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 f = __half22float2(acc[k]);
+            rs += f.x + f.y;
+          }
+        }
+      }
+      l = l * alpha + rs;
       if (j > 0) {  // P_t(j-1) V_{j-1} finished: P_t may be overwritten and O_t is stable
         w = mbar_wait(o_done(t), (j - 1) & 1, p.err, abort_flag);
         if (!__all_sync(0xffffffffu, w)) {
           ok = false;
           break;
         }
-      }
-      if (__any_sync(0xffffffffu, m_new > m_used + 8.0f)) {
-        const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m_used - m_new);
-        l *= alpha;
-        if (j > 0) {
+        if (grow) {
           tc_fence_after();
 #pragma unroll 1
           for (int cc = 0; cc < D / 32; ++cc) {
@@ -599,38 +625,15 @@ __global__ void __launch_bounds__(320, 1)
             tmem_st32(tO(t) + lane_off + cc * 32, o);
           }
         }
-        m_used = m_new;
       }
-      // P = 2^(s c - m) in packed halves: one fp32x2 FMA, one fp16x2 conversion and one fp16x2
-      // exponential per pair of scores (the argument is at most 8 after the lazy rescaling, so its
-      // fp16 rounding moves P by under 0.6%, the order of P's own 16-bit rounding); row sums in four
-      // fp16x2 partial sums per 64 keys, widened to fp32 once per block.  Each 8-key chunk is stored
-      // at its swizzled position of the 128-byte rows the P V MMA reads.
-      float rs = 0.f;
-      const float2 cc = make_float2(c, c), mm = make_float2(-m_used, -m_used);
+      // each 8-key chunk at its swizzled position of the 128-byte rows the P V MMA reads
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        __half2 acc[4] = {__float2half2_rn(0.f), __float2half2_rn(0.f), __float2half2_rn(0.f),
-                          __float2half2_rn(0.f)};
+      for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
-          uint32_t e4[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int i = 64 * hf + 8 * ch + 2 * q;
-            const float2 xy = ffma2(make_float2(s[i], s[i + 1]), cc, mm);
-            e4[q] = ex2_f16x2(pack_f16x2(xy.x, xy.y));
-            acc[q] = __hadd2(acc[q], *reinterpret_cast<const __half2*>(&e4[q]));
-          }
+          const uint32_t* e4 = pk + 32 * hf + 4 * ch;
           *reinterpret_cast<uint4*>(prow + hf * G::ATOM + ((ch ^ sw) << 4)) = make_uint4(e4[0], e4[1], e4[2], e4[3]);
         }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 f = __half22float2(acc[k]);
-          rs += f.x + f.y;
-        }
-      }
-      l += rs;
       fence_proxy_async_smem();  // the P stores become visible to the tensor core
       tc_fence_before();
       __syncwarp();
