@@ -227,12 +227,16 @@ def test_deterministic_and_host_path_matches():
     x = to_dev(inp["x"]).reshape(cfg.tokens, cfg.hidden)
     y1 = dl.forward(x).clone()
     y2 = dl.forward(x).clone()
-    xh = x.cpu().pin_memory()
-    yh = torch.empty(cfg.tokens, cfg.hidden, dtype=torch.bfloat16).pin_memory()
-    dl.layer.forward_host(xh, cfg.seq, cfg.batch, dl.w, yh)
-    torch.cuda.synchronize()
     assert torch.equal(y1, y2)
-    assert torch.equal(y1.cpu(), yh)
+    # pinned (asynchronous copies) and pageable (staged copies) host buffers give the same y
+    for x_pinned in (True, False):
+        for y_pinned in (True, False):
+            xh = x.cpu().pin_memory() if x_pinned else x.cpu()
+            yh = torch.full((cfg.tokens, cfg.hidden), float("nan"), dtype=torch.bfloat16)
+            yh = yh.pin_memory() if y_pinned else yh
+            dl.layer.forward_host(xh, cfg.seq, cfg.batch, dl.w, yh)
+            torch.cuda.synchronize()
+            assert torch.equal(y1.cpu(), yh), (x_pinned, y_pinned)
 
 
 def test_launch_count_and_profile_mask():
