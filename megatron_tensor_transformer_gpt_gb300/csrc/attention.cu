@@ -27,6 +27,7 @@ namespace {
 
 constexpr int BQ = 128, BKV = 128;
 static_assert(BKV == 128, "a row of S is read with one 128-column TMEM load");
+constexpr int P_ATOM = BQ * 128;  // one 64-key half of a P tile: [128 rows x 64 fp16], 16 KB
 
 // Maximum of a row of S (BKV scores in registers) over eight independent chains of three-input
 // maxima (chain k takes elements 2k and 2k+1 of every 16), so the reduction is not one long chain.
@@ -359,6 +360,148 @@ __global__ void __launch_bounds__(192, 1)
 //   before it waits for P_t(j-1) V_{j-1}, and only the shared-memory stores wait.
 //   10 warps put three warps on some SM sub-partitions, whose 16K-register files then allow 168
 //   registers per thread.
+// The softmax role for one head (four warps, one query row per thread, warp w on TMEM lane quadrant
+// `quad`): per key block it waits for S in tensor memory, releases it at once, masks the diagonal
+// block, forms P = 2^(s c - m) in registers, waits for the previous P V product (then rescales O
+// if the running maximum grew by more than 2^8) and stores P into its shared-memory tile in the
+// 128-byte-swizzled layout the P V MMA reads.  At the end O / l goes to o (bf16, or E4M3 with its
+// amax) and m + log2(l) to lse.  `arrive` signals a barrier the MMA thread waits on.
+template <int D, typename Arrive>
+__device__ __forceinline__ void softmax_head(const AttnParams& p, const Work& wk, int h, int quad, int lane,
+                                             uint32_t tS, uint32_t tO, uint8_t* ptile, uint32_t s_full,
+                                             uint32_t s_free, uint32_t p_full, uint32_t o_done,
+                                             volatile int* abort_flag, Arrive arrive) {
+  const int qb = wk.qb, b = wk.b, nkv = qb + 1;
+  const int r = quad * 32 + lane;
+  const bool row_ok = qb * BQ + r < wk.len;  // inside its sequence
+  const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+  const float c = p.scale_log2;
+  uint8_t* prow = ptile + r * 128;
+  const int sw = r & 7;
+  float m_used = -INFINITY, l = 0.f;
+  bool ok = true;
+  for (int j = 0; j < nkv; ++j) {
+    bool w = mbar_wait(s_full, j & 1, p.err, abort_flag);
+    if (!__all_sync(0xffffffffu, w)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    float s[BKV];
+    tmem_ld128(tS + lane_off, s);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) arrive(s_free);  // the tensor core may overwrite S now
+    if (j == qb) {
+#pragma unroll
+      for (int i = 0; i < BKV; ++i)
+        if (i > r) s[i] = -INFINITY;
+    }
+    const float mx = row_max(s);
+    const float m_new = fmaxf(m_used, mx * c);
+    const bool grow = __any_sync(0xffffffffu, m_new > m_used + 8.0f);
+    float alpha = 1.f;
+    if (grow) {
+      alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m_used - m_new);
+      m_used = m_new;
+    }
+    // P = 2^(s c - m) in packed halves, formed in registers while the tensor core still runs
+    // P(j-1) V_{j-1}: one fp32x2 FMA, one fp16x2 conversion and one fp16x2 exponential per pair
+    // of scores (the argument is at most 8 after the lazy rescaling, so its fp16 rounding moves P
+    // by under 0.6%, the order of P's own 16-bit rounding); row sums in four fp16x2 partial sums
+    // per 64 keys, widened to fp32 once per block.
+    uint32_t pk[BKV / 2];
+    float rs = 0.f;
+    {
+      const float2 cc = make_float2(c, c), mm = make_float2(-m_used, -m_used);
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        __half2 acc[4] = {__float2half2_rn(0.f), __float2half2_rn(0.f), __float2half2_rn(0.f),
+                          __float2half2_rn(0.f)};
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          const int i = 64 * hf + 2 * q;
+          const float2 xy = ffma2(make_float2(s[i], s[i + 1]), cc, mm);
+          pk[32 * hf + q] = ex2_f16x2(pack_f16x2(xy.x, xy.y));
+          acc[q & 3] = __hadd2(acc[q & 3], *reinterpret_cast<const __half2*>(&pk[32 * hf + q]));
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = __half22float2(acc[k]);
+          rs += f.x + f.y;
+        }
+      }
+    }
+    l = l * alpha + rs;
+    if (j > 0) {  // P(j-1) V_{j-1} finished: P may be overwritten and O is stable
+      w = mbar_wait(o_done, (j - 1) & 1, p.err, abort_flag);
+      if (!__all_sync(0xffffffffu, w)) {
+        ok = false;
+        break;
+      }
+      if (grow) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          float o[32];
+          tmem_ld32(tO + lane_off + cc * 32, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32(tO + lane_off + cc * 32, o);
+        }
+      }
+    }
+    // each 8-key chunk at its swizzled position of the 128-byte rows the P V MMA reads
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        const uint32_t* e4 = pk + 32 * hf + 4 * ch;
+        *reinterpret_cast<uint4*>(prow + hf * P_ATOM + ((ch ^ sw) << 4)) = make_uint4(e4[0], e4[1], e4[2], e4[3]);
+      }
+    fence_proxy_async_smem();  // the P stores become visible to the tensor core
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) arrive(p_full);
+  }
+  if (ok) {
+    const bool w = mbar_wait(o_done, (nkv - 1) & 1, p.err, abort_flag);
+    if (__all_sync(0xffffffffu, w)) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      const size_t orow = (static_cast<size_t>(wk.q_row0 + r) * p.batch + b) * p.ldo + h * D;
+      if (p.lse != nullptr && row_ok)
+        p.lse[(static_cast<size_t>(b) * p.nh + h) * p.seq + wk.q_row0 + r] = m_used + log2f(l);
+      const float qs = p.o8 != nullptr ? __ldg(p.q_scale) : 1.f;
+      float mx = 0.f;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        float o[32];
+        tmem_ld32(tO + lane_off + cc * 32, o);
+        if (row_ok) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= inv_l;
+          if (p.o8 != nullptr) {  // E4M3 output for the FP8 output projection
+#pragma unroll
+            for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(o[i]));
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              *reinterpret_cast<uint2*>(p.o8 + orow + cc * 32 + q4 * 8) = pack_e4m3x8(o + q4 * 8, qs);
+          } else {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              *reinterpret_cast<uint4*>(p.o + orow + cc * 32 + q4 * 8) = pack_bf16x8(o + q4 * 8);
+          }
+        }
+      }
+      if (p.o8 != nullptr) {
+        mx = warp_max(mx);
+        if (lane == 0) atomic_max_abs(p.amax, mx);
+      }
+    }
+  }
+}
+
 template <int D>
 struct Geo2 {
   static constexpr int ATOM = 128 * 128;        // [128 rows x 64 fp16/bf16] swizzle block, 16 KB
@@ -545,136 +688,8 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else {
     const int t = (warp - 2) >> 2;  // which head of the pair
-    const int quad = warp & 3;
-    const int r = quad * 32 + lane;
-    const bool row_ok = qb * BQ + r < wk.len;  // inside its sequence
-    const int h = h0 + t;
-    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const float c = p.scale_log2;
-    uint8_t* prow = base + G::OFF_P + t * G::P_BYTES + r * 128;
-    const int sw = r & 7;
-    float m_used = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      bool w = mbar_wait(s_full(t), j & 1, p.err, abort_flag);
-      if (!__all_sync(0xffffffffu, w)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float s[BKV];
-      tmem_ld128(tS(t) + lane_off, s);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_free(t));  // the tensor core may overwrite S_t now
-      if (j == qb) {
-#pragma unroll
-        for (int i = 0; i < BKV; ++i)
-          if (i > r) s[i] = -INFINITY;
-      }
-      const float mx = row_max(s);
-      const float m_new = fmaxf(m_used, mx * c);
-      const bool grow = __any_sync(0xffffffffu, m_new > m_used + 8.0f);
-      float alpha = 1.f;
-      if (grow) {
-        alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m_used - m_new);
-        m_used = m_new;
-      }
-      // P = 2^(s c - m) in packed halves, formed in registers while the tensor core still runs
-      // P_t(j-1) V_{j-1}: one fp32x2 FMA, one fp16x2 conversion and one fp16x2 exponential per pair
-      // of scores (the argument is at most 8 after the lazy rescaling, so its fp16 rounding moves P
-      // by under 0.6%, the order of P's own 16-bit rounding); row sums in four fp16x2 partial sums
-      // per 64 keys, widened to fp32 once per block.
-      uint32_t pk[BKV / 2];
-      float rs = 0.f;
-      {
-        const float2 cc = make_float2(c, c), mm = make_float2(-m_used, -m_used);
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          __half2 acc[4] = {__float2half2_rn(0.f), __float2half2_rn(0.f), __float2half2_rn(0.f),
-                            __float2half2_rn(0.f)};
-#pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            const int i = 64 * hf + 2 * q;
-            const float2 xy = ffma2(make_float2(s[i], s[i + 1]), cc, mm);
-            pk[32 * hf + q] = ex2_f16x2(pack_f16x2(xy.x, xy.y));
-            acc[q & 3] = __hadd2(acc[q & 3], *reinterpret_cast<const __half2*>(&pk[32 * hf + q]));
-          }
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float2 f = __half22float2(acc[k]);
-            rs += f.x + f.y;
-          }
-        }
-      }
-      l = l * alpha + rs;
-      if (j > 0) {  // P_t(j-1) V_{j-1} finished: P_t may be overwritten and O_t is stable
-        w = mbar_wait(o_done(t), (j - 1) & 1, p.err, abort_flag);
-        if (!__all_sync(0xffffffffu, w)) {
-          ok = false;
-          break;
-        }
-        if (grow) {
-          tc_fence_after();
-#pragma unroll 1
-          for (int cc = 0; cc < D / 32; ++cc) {
-            float o[32];
-            tmem_ld32(tO(t) + lane_off + cc * 32, o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tmem_st32(tO(t) + lane_off + cc * 32, o);
-          }
-        }
-      }
-      // each 8-key chunk at its swizzled position of the 128-byte rows the P V MMA reads
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const uint32_t* e4 = pk + 32 * hf + 4 * ch;
-          *reinterpret_cast<uint4*>(prow + hf * G::ATOM + ((ch ^ sw) << 4)) = make_uint4(e4[0], e4[1], e4[2], e4[3]);
-        }
-      fence_proxy_async_smem();  // the P stores become visible to the tensor core
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full(t));
-    }
-    if (ok) {
-      const bool w = mbar_wait(o_done(t), (nkv - 1) & 1, p.err, abort_flag);
-      if (__all_sync(0xffffffffu, w)) {
-        tc_fence_after();
-        const float inv_l = 1.f / l;
-        const size_t orow = (static_cast<size_t>(wk.q_row0 + r) * p.batch + b) * p.ldo + h * D;
-        if (p.lse != nullptr && row_ok)
-          p.lse[(static_cast<size_t>(b) * p.nh + h) * p.seq + wk.q_row0 + r] = m_used + log2f(l);
-        const float qs = p.o8 != nullptr ? __ldg(p.q_scale) : 1.f;
-        float mx = 0.f;
-#pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
-          float o[32];
-          tmem_ld32(tO(t) + lane_off + cc * 32, o);
-          if (row_ok) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= inv_l;
-            if (p.o8 != nullptr) {  // E4M3 output for the FP8 output projection
-#pragma unroll
-              for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(o[i]));
-#pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4)
-                *reinterpret_cast<uint2*>(p.o8 + orow + cc * 32 + q4 * 8) = pack_e4m3x8(o + q4 * 8, qs);
-            } else {
-#pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4)
-                *reinterpret_cast<uint4*>(p.o + orow + cc * 32 + q4 * 8) = pack_bf16x8(o + q4 * 8);
-            }
-          }
-        }
-        if (p.o8 != nullptr) {
-          mx = warp_max(mx);
-          if (lane == 0) atomic_max_abs(p.amax, mx);
-        }
-      }
-    }
+    softmax_head<D>(p, wk, h0 + t, warp & 3, lane, tS(t), tO(t), base + G::OFF_P + t * G::P_BYTES, s_full(t),
+                    s_free(t), p_full(t), o_done(t), abort_flag, [](uint32_t bar) { mbar_arrive(bar); });
   }
   __syncthreads();
   if (warp == 1) {

@@ -122,6 +122,8 @@ def check_first_codes(f8, cfg, inp, scales):
                       rope_base=1e4),
     synth.LayerConfig("f8ln", batch=1, seq=200, hidden=512, heads=4, groups=4, head_dim=128, ffn=1024,
                       norm="layer", act="gelu_tanh", rope_base=0.0, bias=True),
+    synth.LayerConfig("f8gqa128", batch=2, seq=300, hidden=512, heads=8, groups=2, head_dim=128, ffn=1024,
+                      rope_base=5e5),                     # four heads per group: the CTA-pair attention
 ], ids=lambda c: c.name)
 def test_fp8_layer_matches_oracle(cfg):
     inp = synth.make_inputs(cfg, seed=61, affine="random", biases="random")
