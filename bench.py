@@ -7,7 +7,7 @@ causal GQA flash attention, output projection + residual, norm, fc1 + SwiGLU, fc
 on inputs already resident in HBM.  L2 is flushed (a 256 MiB write) between steps, outside the
 timed spans; each step is timed with CUDA events on the launching stream.  `e2e` repeats the
 measurement through mt_layer_forward_host with pinned host buffers (x copied in and y copied out
-inside every step).  With N > 1 (torchrun) every rank runs an independent replica -- the layer
+inside every step, in two row chunks overlapped with the layer's first and last GEMMs).  With N > 1 (torchrun) every rank runs an independent replica -- the layer
 forward of one data-parallel replica needs no collective -- and the slowest rank's time counts.
 
 --impl reference times the float64 CPU oracle (the "reference" arm of this build) on the host

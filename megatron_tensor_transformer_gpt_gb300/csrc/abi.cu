@@ -39,6 +39,9 @@ struct mt_layer {
   };
   std::vector<Rec> recs;
   std::vector<cudaEvent_t> pool;
+  // host-buffer forward: a copy stream and its events (created on first use)
+  cudaStream_t copy_stream;
+  cudaEvent_t copy_ev[5];
 };
 
 namespace {
@@ -108,6 +111,32 @@ void count_launch(mt_layer* L) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Page-locked host memory (copies from and to it run asynchronously, overlapped with kernels).
+bool pinned(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the error of an unknown pointer
+    return false;
+  }
+  return a.type == cudaMemoryTypeHost;
+}
+
+// The handle's copy stream and its five events, created on first use.
+int ensure_copy_stream(mt_layer* L) {
+  if (L->copy_stream != nullptr) return MT_OK;
+  cudaStream_t s = nullptr;
+  cudaError_t e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
+  if (e != cudaSuccess) return cuda_fail(e, "creating the copy stream");
+  for (auto& ev : L->copy_ev) {
+    if (ev == nullptr && (e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess) {
+      cudaStreamDestroy(s);
+      return cuda_fail(e, "creating the copy events");
+    }
+  }
+  L->copy_stream = s;
+  return MT_OK;
+}
 
 // ------------------------------------------------------------------ workspace layout
 enum Region { kXn = 0, kQ, kK, kV, kO, kH, kHn, kA, kRope, kXStage, kYStage, kPos, kNumRegions };
@@ -360,10 +389,20 @@ int check_call(const mt_layer* L, const void* in, const void* out, int S, int B,
 }
 
 // ------------------------------------------------------------------ the two blocks
+// Token rows in two chunks [0, split) and [split, T) (split a multiple of 256): on input, the rows of
+// chunk c are ready once event ready[c] has been reached (a copy on another stream); on output, the
+// rows of chunk c are final at event done[c], recorded on the compute stream.
+struct Chunks {
+  int split;
+  cudaEvent_t ev[2];
+};
+
 // Attention block: norm1 -> QKV GEMM (+bias, RoPE, scatter) -> flash attention -> output projection.
-// out_mode kEpiStore writes the rank's partial; kEpiResid writes h = x + Y + b_o.
+// out_mode kEpiStore writes the rank's partial; kEpiResid writes h = x + Y + b_o.  in != null: norm1
+// and the QKV GEMM run per input chunk, each after its rows have arrived.
 int run_attention_block(mt_layer* L, const Layout& lay, const void* x, int S, int B, const mt_weights* w, void* out,
-                        int out_mode, cudaStream_t st, const Packed* pk = nullptr, float* lse = nullptr) {
+                        int out_mode, cudaStream_t st, const Packed* pk = nullptr, float* lse = nullptr,
+                        const Chunks* in = nullptr) {
   const int T = S * B, H = L->hidden, d = L->head_dim;
   cudaError_t e;
   float2* rope = nullptr;
@@ -381,32 +420,41 @@ int run_attention_block(mt_layer* L, const Layout& lay, const void* x, int S, in
     if (e != cudaSuccess) return cuda_fail(e, "packed-sample index");
   }
   bf16* xn = region<bf16>(L, lay, kXn);
-  {
-    Timed t(L, kSlotNorm1, st);
-    e = mt::launch_norm(L->norm == MT_NORM_LAYER, static_cast<const bf16*>(x), static_cast<const bf16*>(w->norm1_w),
-                      static_cast<const bf16*>(w->norm1_b), xn, T, H, L->eps, st);
-  }
-  if (e != cudaSuccess) return cuda_fail(e, "norm1 launch");
-
   bf16 *q = region<bf16>(L, lay, kQ), *k = region<bf16>(L, lay, kK);
   __half* v = region<__half>(L, lay, kV);
   const int nqkv = L->q_w + 2 * L->kv_w;
-  mt::GemmParams p = gemm_params(T, nqkv, H, false, L->d_err);
-  p.bias = static_cast<const bf16*>(w->b_qkv);
-  p.q = q;
-  p.k = k;
-  p.v = v;
-  p.rope = rope;
-  p.seq = S;
-  p.batch = B;
-  p.head_dim = d;
-  p.q_w = L->q_w;
-  p.kv_w = L->kv_w;
-  p.nh = L->nh_r;
-  p.ng = L->ng_r;
-  p.pos = pos;
-  int rc = run_gemm(L, kSlotQkv, mt::kEpiQkv, xn, H, w->w_qkv, nqkv, T, nqkv, H, p, st);
-  if (rc) return rc;
+  mt::GemmParams p;
+  int rc;
+  const int nchunks = in != nullptr ? 2 : 1;
+  for (int c = 0; c < nchunks; ++c) {
+    const int r0 = c == 0 ? 0 : in->split, rows = nchunks == 1 ? T : (c == 0 ? in->split : T - in->split);
+    if (in != nullptr && (e = cudaStreamWaitEvent(st, in->ev[c], 0)) != cudaSuccess)
+      return cuda_fail(e, "waiting for the input rows");
+    const size_t off = static_cast<size_t>(r0) * H;
+    {
+      Timed t(L, kSlotNorm1, st);
+      e = mt::launch_norm(L->norm == MT_NORM_LAYER, static_cast<const bf16*>(x) + off,
+                          static_cast<const bf16*>(w->norm1_w), static_cast<const bf16*>(w->norm1_b), xn + off, rows,
+                          H, L->eps, st);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "norm1 launch");
+    p = gemm_params(rows, nqkv, H, false, L->d_err);
+    p.bias = static_cast<const bf16*>(w->b_qkv);
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.rope = rope;
+    p.seq = S;
+    p.batch = B;
+    p.head_dim = d;
+    p.q_w = L->q_w;
+    p.kv_w = L->kv_w;
+    p.nh = L->nh_r;
+    p.ng = L->ng_r;
+    p.pos = pos;
+    p.row0 = r0;
+    if ((rc = run_gemm(L, kSlotQkv, mt::kEpiQkv, xn + off, H, w->w_qkv, nqkv, rows, nqkv, H, p, st))) return rc;
+  }
 
   CUtensorMap tq, tk, tv;
   if ((rc = map_3d(&tq, q, d, S, static_cast<uint64_t>(B) * L->nh_r, d, static_cast<uint64_t>(S) * d, 128))) return rc;
@@ -444,9 +492,10 @@ int run_attention_block(mt_layer* L, const Layout& lay, const void* x, int S, in
 }
 
 // MLP block: norm2 -> fc1 GEMM (+bias, SwiGLU / GeLU) -> fc2 GEMM.
-// out_mode kEpiStore writes the rank's partial; kEpiResid writes y = h + Y + b_fc2.
+// out_mode kEpiStore writes the rank's partial; kEpiResid writes y = h + Y + b_fc2.  out_chunks !=
+// null: fc2 runs per output chunk and records the chunk's event after it.
 int run_mlp_block(mt_layer* L, const Layout& lay, const void* h, int S, int B, const mt_weights* w, void* out,
-                  int out_mode, cudaStream_t st) {
+                  int out_mode, cudaStream_t st, const Chunks* out_chunks = nullptr) {
   const int T = S * B, H = L->hidden;
   bf16* hn = region<bf16>(L, lay, kHn);
   cudaError_t e;
@@ -465,23 +514,34 @@ int run_mlp_block(mt_layer* L, const Layout& lay, const void* h, int S, int B, c
   p.bias = static_cast<const bf16*>(w->b_fc1);
   int rc = run_gemm(L, kSlotFc1, swiglu ? mt::kEpiSwiglu : mt::kEpiGelu, hn, H, w->w_fc1, L->f1_r, T, L->f_r, H, p, st);
   if (rc) return rc;
-  p = gemm_params(T, H, L->f_r, false, L->d_err);
-  p.out = static_cast<bf16*>(out);
-  p.ldo = H;
-  if (out_mode == mt::kEpiResid) {
-    p.bias = static_cast<const bf16*>(w->b_fc2);
-    p.resid = static_cast<const bf16*>(h);
-    p.ldr = H;
+  const int nchunks = out_chunks != nullptr ? 2 : 1;
+  for (int c = 0; c < nchunks; ++c) {
+    const int r0 = c == 0 ? 0 : out_chunks->split;
+    const int rows = nchunks == 1 ? T : (c == 0 ? out_chunks->split : T - out_chunks->split);
+    p = gemm_params(rows, H, L->f_r, false, L->d_err);
+    p.out = static_cast<bf16*>(out) + static_cast<size_t>(r0) * H;
+    p.ldo = H;
+    if (out_mode == mt::kEpiResid) {
+      p.bias = static_cast<const bf16*>(w->b_fc2);
+      p.resid = static_cast<const bf16*>(h) + static_cast<size_t>(r0) * H;
+      p.ldr = H;
+    }
+    if ((rc = run_gemm(L, kSlotFc2, out_mode, a + static_cast<size_t>(r0) * L->f_r, L->f_r, w->w_fc2, H, rows, H,
+                       L->f_r, p, st)))
+      return rc;
+    if (out_chunks != nullptr && (e = cudaEventRecord(out_chunks->ev[c], st)) != cudaSuccess)
+      return cuda_fail(e, "recording an output chunk");
   }
-  return run_gemm(L, kSlotFc2, out_mode, a, L->f_r, w->w_fc2, H, T, H, L->f_r, p, st);
+  return MT_OK;
 }
 
 int forward_device(mt_layer* L, const Layout& lay, const void* x, int S, int B, const mt_weights* w, void* y,
-                   cudaStream_t st, const Packed* pk = nullptr) {
+                   cudaStream_t st, const Packed* pk = nullptr, const Chunks* in = nullptr,
+                   const Chunks* out_chunks = nullptr) {
   bf16* h = region<bf16>(L, lay, kH);
-  int rc = run_attention_block(L, lay, x, S, B, w, h, mt::kEpiResid, st, pk);
+  int rc = run_attention_block(L, lay, x, S, B, w, h, mt::kEpiResid, st, pk, nullptr, in);
   if (rc) return rc;
-  return run_mlp_block(L, lay, h, S, B, w, y, L->tp == 1 ? mt::kEpiResid : mt::kEpiStore, st);
+  return run_mlp_block(L, lay, h, S, B, w, y, L->tp == 1 ? mt::kEpiResid : mt::kEpiStore, st, out_chunks);
 }
 
 // The layer with its four GEMMs on E4M3 operands (delayed scaling of the activations, weights
@@ -1009,6 +1069,36 @@ int mt_layer_forward_host(mt_layer* L, const void* x_host, int seq, int batch, c
   void* xd = region<void>(L, lay, kXStage);
   void* yd = region<void>(L, lay, kYStage);
   const size_t bytes = lay.size[kXStage];
+  const int T = seq * batch;
+  const int split = (T / 2) / 256 * 256;  // a multiple of the 256-row GEMM tile
+  if (pinned(x_host) && pinned(y_host) && split >= 256 && T - split >= 256) {
+    // Overlap the copies with the layer: x arrives in two chunks on the copy stream and norm1 + QKV
+    // of the first chunk run while the second is copied; fc2 runs per chunk and the first chunk of
+    // y is copied back while the second is computed.  The stream `st` waits for the last copy.
+    if ((rc = ensure_copy_stream(L))) return rc;
+    cudaStream_t cs = L->copy_stream;
+    cudaEvent_t* ev = L->copy_ev;  // start | x chunk 0 | x chunk 1 | y chunk 0 | y chunk 1 (then: copies done)
+    const size_t b0 = static_cast<size_t>(split) * L->hidden * 2;
+    const uint8_t* xs = static_cast<const uint8_t*>(x_host);
+    uint8_t* ys = static_cast<uint8_t*>(y_host);
+    cudaError_t e = cudaEventRecord(ev[0], st);  // the host buffers' earlier users on `st` come first
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev[0], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(xd, xs, b0, cudaMemcpyHostToDevice, cs);
+    if (e == cudaSuccess) e = cudaEventRecord(ev[1], cs);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(static_cast<uint8_t*>(xd) + b0, xs + b0, bytes - b0, cudaMemcpyHostToDevice, cs);
+    if (e == cudaSuccess) e = cudaEventRecord(ev[2], cs);
+    if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy of x");
+    const Chunks in{split, {ev[1], ev[2]}}, out{split, {ev[3], ev[4]}};
+    if ((rc = forward_device(L, lay, xd, seq, batch, w, yd, st, nullptr, &in, &out))) return rc;
+    e = cudaStreamWaitEvent(cs, ev[3], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(ys, yd, b0, cudaMemcpyDeviceToHost, cs);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev[4], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(ys + b0, static_cast<uint8_t*>(yd) + b0, bytes - b0, cudaMemcpyDeviceToHost, cs);
+    if (e == cudaSuccess) e = cudaEventRecord(ev[0], cs);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev[0], 0);
+    if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy of y");
+    return ok();
+  }
   cudaError_t e = cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy of x");
   rc = forward_device(L, lay, xd, seq, batch, w, yd, st);
@@ -1050,6 +1140,9 @@ void mt_layer_destroy(mt_layer* L) {
     cudaEventDestroy(r.b);
   }
   for (auto e : L->pool) cudaEventDestroy(e);
+  for (auto e : L->copy_ev)
+    if (e) cudaEventDestroy(e);
+  if (L->copy_stream) cudaStreamDestroy(L->copy_stream);
   delete L;
 }
 

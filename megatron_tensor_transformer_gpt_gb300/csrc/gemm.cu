@@ -193,9 +193,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
     }
   } else {  // kEpiQkv: `width` is a multiple of head_dim, so every head lies inside one unit
     const int d = p.head_dim, half = d >> 1;
-    const int s = valid ? row / p.batch : 0;  // row of the [b, head, s, d] buffers
-    const int b = valid ? row - s * p.batch : 0;
-    const int rpos = (valid && p.pos != nullptr) ? p.pos[row] : s;    // RoPE position
+    const int trow = row + p.row0;               // token row
+    const int s = valid ? trow / p.batch : 0;  // row of the [b, head, s, d] buffers
+    const int b = valid ? trow - s * p.batch : 0;
+    const int rpos = (valid && p.pos != nullptr) ? p.pos[trow] : s;    // RoPE position
 #pragma unroll 1
     for (int hc = 0; hc < width; hc += d) {
       const int col = c0 + hc;

@@ -50,6 +50,7 @@ struct GemmParams {
   int seq, batch, head_dim, q_w, kv_w, nh, ng;
   // packed samples (batch 1): per-token RoPE position; null for dense batches
   const int* pos;
+  int row0;            // token row of the launch's first A row (a launch over a chunk of the rows)
   // E4M3 operands: the fp32 accumulator is multiplied by (*deq_a) * (*deq_b); null for bf16
   const float* deq_a;
   const float* deq_b;

@@ -239,6 +239,26 @@ def test_deterministic_and_host_path_matches():
             assert torch.equal(y1.cpu(), yh), (x_pinned, y_pinned)
 
 
+@pytest.mark.parametrize("cfg", [small(batch=2, seq=320), small(seq=700, heads=4, groups=1, head_dim=128)],
+                         ids=["640-tokens-gqa", "700-tokens-mqa-d128"])
+def test_host_path_chunked_copies_match(cfg):
+    """With pinned buffers and 512 tokens or more the host-buffer path copies x and y in two chunks on
+    a copy stream, overlapped with norm1 + QKV of the first input chunk and fc2 of the second output
+    chunk; every row still equals the device path bit for bit, also over repeated calls."""
+    inp = synth.make_inputs(cfg, seed=9, affine="random")
+    dl = DeviceLayer(cfg, inp)
+    x = to_dev(inp["x"]).reshape(cfg.tokens, cfg.hidden)
+    want = dl.forward(x).cpu()
+    xh = x.cpu().pin_memory()
+    for _ in range(3):
+        yh = torch.full((cfg.tokens, cfg.hidden), float("nan"), dtype=torch.bfloat16).pin_memory()
+        dl.layer.forward_host(xh, cfg.seq, cfg.batch, dl.w, yh)
+        torch.cuda.synchronize()
+        assert torch.equal(want, yh)
+    dl.layer.status()
+    dl.close()
+
+
 def test_launch_count_and_profile_mask():
     """A dense forward launches eight kernels; a slot mask brackets only the selected slot."""
     cfg = small()
