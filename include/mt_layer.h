@@ -177,10 +177,10 @@ int mt_gemm_e4m3(const void* A, const void* B, void* C, int M, int N, int K, con
 /* mt_layer_forward with x and y in HOST memory: copies x into the workspace, runs the layer and
  * copies y back; `cuda_stream` reaches the end of the call once y is in host memory, and the host
  * buffers must stay valid until then.  With both buffers pinned and at least 512 tokens the copies
- * are overlapped with the layer on a copy stream owned by the handle: x arrives in two row chunks
- * (norm1 and the QKV GEMM of the first chunk run while the second is copied) and the fc2 GEMM runs
- * per chunk (the first chunk of y is copied back while the second is computed).  Pageable buffers
- * are copied before and after the layer. */
+ * are overlapped with the layer on a copy stream owned by the handle: x arrives in row chunks (two,
+ * up to four from 8192 tokens; norm1 and the QKV GEMM of a chunk run as soon as it is in) and the
+ * fc2 GEMM runs per chunk (each chunk of y is copied back while the next is computed).  Pageable
+ * buffers are copied before and after the layer. */
 int mt_layer_forward_host(mt_layer* L, const void* x_host, int seq, int batch, const mt_weights* w,
                           void* y_host, void* cuda_stream);
 

@@ -41,7 +41,7 @@ struct mt_layer {
   std::vector<cudaEvent_t> pool;
   // host-buffer forward: a copy stream and its events (created on first use)
   cudaStream_t copy_stream;
-  cudaEvent_t copy_ev[5];
+  cudaEvent_t copy_ev[9];
 };
 
 namespace {
@@ -122,7 +122,7 @@ bool pinned(const void* p) {
   return a.type == cudaMemoryTypeHost;
 }
 
-// The handle's copy stream and its five events, created on first use.
+// The handle's copy stream and its events, created on first use.
 int ensure_copy_stream(mt_layer* L) {
   if (L->copy_stream != nullptr) return MT_OK;
   cudaStream_t s = nullptr;
@@ -389,12 +389,14 @@ int check_call(const mt_layer* L, const void* in, const void* out, int S, int B,
 }
 
 // ------------------------------------------------------------------ the two blocks
-// Token rows in two chunks [0, split) and [split, T) (split a multiple of 256): on input, the rows of
-// chunk c are ready once event ready[c] has been reached (a copy on another stream); on output, the
-// rows of chunk c are final at event done[c], recorded on the compute stream.
+// Token rows in n chunks [row[c], row[c + 1]) (boundaries at multiples of 256): on input, the rows of
+// chunk c are ready once event ev[c] has been reached (a copy on another stream); on output, the rows
+// of chunk c are final at event ev[c], recorded on the compute stream.
+constexpr int kMaxChunks = 4;
 struct Chunks {
-  int split;
-  cudaEvent_t ev[2];
+  int n;
+  int row[kMaxChunks + 1];
+  cudaEvent_t ev[kMaxChunks];
 };
 
 // Attention block: norm1 -> QKV GEMM (+bias, RoPE, scatter) -> flash attention -> output projection.
@@ -425,9 +427,9 @@ int run_attention_block(mt_layer* L, const Layout& lay, const void* x, int S, in
   const int nqkv = L->q_w + 2 * L->kv_w;
   mt::GemmParams p;
   int rc;
-  const int nchunks = in != nullptr ? 2 : 1;
+  const int nchunks = in != nullptr ? in->n : 1;
   for (int c = 0; c < nchunks; ++c) {
-    const int r0 = c == 0 ? 0 : in->split, rows = nchunks == 1 ? T : (c == 0 ? in->split : T - in->split);
+    const int r0 = in != nullptr ? in->row[c] : 0, rows = in != nullptr ? in->row[c + 1] - r0 : T;
     if (in != nullptr && (e = cudaStreamWaitEvent(st, in->ev[c], 0)) != cudaSuccess)
       return cuda_fail(e, "waiting for the input rows");
     const size_t off = static_cast<size_t>(r0) * H;
@@ -514,10 +516,10 @@ int run_mlp_block(mt_layer* L, const Layout& lay, const void* h, int S, int B, c
   p.bias = static_cast<const bf16*>(w->b_fc1);
   int rc = run_gemm(L, kSlotFc1, swiglu ? mt::kEpiSwiglu : mt::kEpiGelu, hn, H, w->w_fc1, L->f1_r, T, L->f_r, H, p, st);
   if (rc) return rc;
-  const int nchunks = out_chunks != nullptr ? 2 : 1;
+  const int nchunks = out_chunks != nullptr ? out_chunks->n : 1;
   for (int c = 0; c < nchunks; ++c) {
-    const int r0 = c == 0 ? 0 : out_chunks->split;
-    const int rows = nchunks == 1 ? T : (c == 0 ? out_chunks->split : T - out_chunks->split);
+    const int r0 = out_chunks != nullptr ? out_chunks->row[c] : 0;
+    const int rows = out_chunks != nullptr ? out_chunks->row[c + 1] - r0 : T;
     p = gemm_params(rows, H, L->f_r, false, L->d_err);
     p.out = static_cast<bf16*>(out) + static_cast<size_t>(r0) * H;
     p.ldo = H;
@@ -1070,30 +1072,42 @@ int mt_layer_forward_host(mt_layer* L, const void* x_host, int seq, int batch, c
   void* yd = region<void>(L, lay, kYStage);
   const size_t bytes = lay.size[kXStage];
   const int T = seq * batch;
-  const int split = (T / 2) / 256 * 256;  // a multiple of the 256-row GEMM tile
-  if (pinned(x_host) && pinned(y_host) && split >= 256 && T - split >= 256) {
-    // Overlap the copies with the layer: x arrives in two chunks on the copy stream and norm1 + QKV
-    // of the first chunk run while the second is copied; fc2 runs per chunk and the first chunk of
-    // y is copied back while the second is computed.  The stream `st` waits for the last copy.
+  // Row chunks at multiples of the 256-row GEMM tile, about 2048 rows or more each (two to four):
+  // smaller chunks cost the split GEMMs more than they hide (four chunks of a 4096-token layer
+  // measured slower than two).
+  const int n = T < 512 ? 1 : std::min(kMaxChunks, std::max(2, T / 2048));
+  if (n > 1 && pinned(x_host) && pinned(y_host)) {
+    // Overlap the copies with the layer: x arrives in n row chunks on the copy stream and norm1 + QKV
+    // of chunk c run as soon as it is in; fc2 runs per chunk and each chunk of y is copied back while
+    // the next is computed.  The stream `st` waits for the last copy.
     if ((rc = ensure_copy_stream(L))) return rc;
     cudaStream_t cs = L->copy_stream;
-    cudaEvent_t* ev = L->copy_ev;  // start | x chunk 0 | x chunk 1 | y chunk 0 | y chunk 1 (then: copies done)
-    const size_t b0 = static_cast<size_t>(split) * L->hidden * 2;
+    cudaEvent_t* ev = L->copy_ev;  // start (then: copies done) | x chunks [n] | y chunks [n]
+    Chunks in{n, {}, {}}, out{n, {}, {}};
+    for (int c = 0; c <= n; ++c) in.row[c] = out.row[c] = c == n ? T : (c * (T / n)) / 256 * 256;
+    for (int c = 0; c < n; ++c) {
+      in.ev[c] = ev[1 + c];
+      out.ev[c] = ev[1 + kMaxChunks + c];
+    }
+    const size_t row_bytes = static_cast<size_t>(L->hidden) * 2;
     const uint8_t* xs = static_cast<const uint8_t*>(x_host);
     uint8_t* ys = static_cast<uint8_t*>(y_host);
+    uint8_t* xdb = static_cast<uint8_t*>(xd);
+    uint8_t* ydb = static_cast<uint8_t*>(yd);
     cudaError_t e = cudaEventRecord(ev[0], st);  // the host buffers' earlier users on `st` come first
     if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev[0], 0);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(xd, xs, b0, cudaMemcpyHostToDevice, cs);
-    if (e == cudaSuccess) e = cudaEventRecord(ev[1], cs);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(static_cast<uint8_t*>(xd) + b0, xs + b0, bytes - b0, cudaMemcpyHostToDevice, cs);
-    if (e == cudaSuccess) e = cudaEventRecord(ev[2], cs);
+    for (int c = 0; c < n && e == cudaSuccess; ++c) {
+      const size_t o = in.row[c] * row_bytes, nb = (in.row[c + 1] - in.row[c]) * row_bytes;
+      e = cudaMemcpyAsync(xdb + o, xs + o, nb, cudaMemcpyHostToDevice, cs);
+      if (e == cudaSuccess) e = cudaEventRecord(in.ev[c], cs);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy of x");
-    const Chunks in{split, {ev[1], ev[2]}}, out{split, {ev[3], ev[4]}};
     if ((rc = forward_device(L, lay, xd, seq, batch, w, yd, st, nullptr, &in, &out))) return rc;
-    e = cudaStreamWaitEvent(cs, ev[3], 0);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(ys, yd, b0, cudaMemcpyDeviceToHost, cs);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev[4], 0);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(ys + b0, static_cast<uint8_t*>(yd) + b0, bytes - b0, cudaMemcpyDeviceToHost, cs);
+    for (int c = 0; c < n && e == cudaSuccess; ++c) {
+      const size_t o = out.row[c] * row_bytes, nb = (out.row[c + 1] - out.row[c]) * row_bytes;
+      e = cudaStreamWaitEvent(cs, out.ev[c], 0);
+      if (e == cudaSuccess) e = cudaMemcpyAsync(ys + o, ydb + o, nb, cudaMemcpyDeviceToHost, cs);
+    }
     if (e == cudaSuccess) e = cudaEventRecord(ev[0], cs);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev[0], 0);
     if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy of y");

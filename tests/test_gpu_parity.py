@@ -239,12 +239,13 @@ def test_deterministic_and_host_path_matches():
             assert torch.equal(y1.cpu(), yh), (x_pinned, y_pinned)
 
 
-@pytest.mark.parametrize("cfg", [small(batch=2, seq=320), small(seq=700, heads=4, groups=1, head_dim=128)],
-                         ids=["640-tokens-gqa", "700-tokens-mqa-d128"])
+@pytest.mark.parametrize("cfg", [small(batch=2, seq=320), small(seq=700, heads=4, groups=1, head_dim=128),
+                                 small(batch=2, seq=4096)],
+                         ids=["640-tokens-gqa", "700-tokens-mqa-d128", "8192-tokens-four-chunks"])
 def test_host_path_chunked_copies_match(cfg):
-    """With pinned buffers and 512 tokens or more the host-buffer path copies x and y in two chunks on
-    a copy stream, overlapped with norm1 + QKV of the first input chunk and fc2 of the second output
-    chunk; every row still equals the device path bit for bit, also over repeated calls."""
+    """With pinned buffers and 512 tokens or more (8192: four chunks) the host-buffer path copies x and
+    y in row chunks on a copy stream, overlapped with norm1 + QKV of the chunks already in and fc2 of
+    the chunks still to come; every row still equals the device path bit for bit, over repeated calls."""
     inp = synth.make_inputs(cfg, seed=9, affine="random")
     dl = DeviceLayer(cfg, inp)
     x = to_dev(inp["x"]).reshape(cfg.tokens, cfg.hidden)
