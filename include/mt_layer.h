@@ -198,7 +198,7 @@ typedef struct { /* device pointers, shapes as in mt_weights; NULL = gradient no
 int mt_layer_backward_workspace_bytes(const mt_layer* L, int seq, int batch, size_t* bytes);
 
 /* dx [T, H] = dL/dx and the requested weight gradients, given x and dy = dL/dy [T, H].  Needs
- * tp_size == 1, seq % 8 == 0 and a workspace of mt_layer_backward_workspace_bytes.  Asynchronous
+ * tp_size == 1, seq % 8 == 0, hidden <= 8192 and a workspace of mt_layer_backward_workspace_bytes.  Asynchronous
  * on cuda_stream: the forward recomputed, then the GEMMs, elementwise kernels and the two
  * flash-attention backward kernels (dQ; dK and dV), all on the stream. */
 int mt_layer_backward(mt_layer* L, const void* x, const void* dy, int seq, int batch, const mt_weights* w, void* dx,

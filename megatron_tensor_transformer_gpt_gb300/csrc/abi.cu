@@ -718,7 +718,7 @@ BwLayout bw_layout(const mt_layer* L, int S, int B) {
   b.size[kBDv] = static_cast<size_t>(B) * L->ng_r * S * d * 4;
   b.size[kBDqkv] = T * QKV * 2;
   b.size[kBDxn] = T * H * 2;
-  b.size[kBGrow] = T * H * 4;
+  b.size[kBGrow] = 2 * static_cast<size_t>(mt::norm_bwd_blocks(static_cast<int>(T))) * H * 4;  // norm partials
   b.size[kBAcc] = maxc * 4;
   // attention backward: row statistics, head-major dO and V
   const size_t zq = static_cast<size_t>(B) * L->nh_r, zk = static_cast<size_t>(B) * L->ng_r;
@@ -760,18 +760,20 @@ int linear_bwd(mt_layer* L, const BwLayout& b, const void* dY, const void* X, co
 int norm_bwd(mt_layer* L, const BwLayout& b, const void* dy, const void* x, const void* gamma, const void* add,
              void* out, void* dgamma, void* dbeta, int T, cudaStream_t st) {
   const int H = L->hidden;
-  float* grow = bwr<float>(L, b, kBGrow);
+  float* part = bwr<float>(L, b, kBGrow);  // per-CTA partial rows of d gamma, then of d beta
+  const int nb = mt::norm_bwd_blocks(T);
   count_launch(L);
   cudaError_t e = mt::launch_norm_bwd(static_cast<const bf16*>(dy), static_cast<const bf16*>(x),
                                       static_cast<const bf16*>(gamma), static_cast<const bf16*>(add),
-                                      static_cast<bf16*>(out), grow, T, H, L->eps, L->norm == MT_NORM_LAYER, st);
+                                      static_cast<bf16*>(out), part, T, H, L->eps, L->norm == MT_NORM_LAYER, st);
   if (e == cudaSuccess && dgamma != nullptr) {
     count_launch(L);
-    e = mt::launch_colsum(grow, true, H, T, H, bwr<float>(L, b, kBAcc), static_cast<bf16*>(dgamma), st);
+    e = mt::launch_colsum(part, true, H, nb, H, bwr<float>(L, b, kBAcc), static_cast<bf16*>(dgamma), st);
   }
   if (e == cudaSuccess && dbeta != nullptr && L->norm == MT_NORM_LAYER) {
     count_launch(L);
-    e = mt::launch_colsum(dy, false, H, T, H, bwr<float>(L, b, kBAcc), static_cast<bf16*>(dbeta), st);
+    e = mt::launch_colsum(part + static_cast<size_t>(nb) * H, true, H, nb, H, bwr<float>(L, b, kBAcc),
+                          static_cast<bf16*>(dbeta), st);
   }
   return e == cudaSuccess ? MT_OK : cuda_fail(e, "norm backward");
 }
@@ -1340,6 +1342,7 @@ int mt_layer_backward(mt_layer* L, const void* x, const void* dy, int seq, int b
   if (!aligned16(x) || !aligned16(dy) || !aligned16(dx)) return fail(MT_ERR_INVALID_ARG, "x/dy/dx must be 16-byte aligned");
   if (seq <= 0 || batch <= 0) return fail(MT_ERR_INVALID_ARG, "seq and batch must be positive");
   if (seq % 8) return fail(MT_ERR_UNSUPPORTED, "the backward pass needs seq % 8 == 0");
+  if (L->hidden > 8192) return fail(MT_ERR_UNSUPPORTED, "the backward pass needs hidden <= 8192");
   const void* gp[] = {g->norm1_w, g->norm1_b, g->w_qkv, g->b_qkv, g->w_o, g->b_o,
                       g->norm2_w, g->norm2_b, g->w_fc1, g->b_fc1, g->w_fc2, g->b_fc2};
   for (const void* p : gp)

@@ -3,6 +3,8 @@
 // norms, RoPE, SwiGLU / GeLU(tanh).
 #include <math.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -100,52 +102,129 @@ __global__ void act_bwd_kernel(const bf16* __restrict__ u, const bf16* __restric
 // x and gx = dy * gamma,
 //   RMSNorm:   dx = r (gx - xhat mean(gx xhat))
 //   LayerNorm: dx = r (gx - mean(gx) - xhat mean(gx xhat))
-// out = add + dx (the residual branch's gradient, may be null); growth[t, :] = dy * xhat (summed
-// over rows into d gamma afterwards).
-__global__ void norm_bwd_kernel(const bf16* __restrict__ dy, const bf16* __restrict__ x, const bf16* __restrict__ gamma,
-                                const bf16* __restrict__ add, bf16* __restrict__ out, float* __restrict__ grow, int H,
-                                float eps, int layer_norm) {
-  __shared__ float red[32];
-  const size_t row = blockIdx.x;
-  const bf16* xr = x + row * H;
-  const bf16* dr = dy + row * H;
-  float s1 = 0.f, s2 = 0.f;
-  for (int c = threadIdx.x; c < H; c += blockDim.x) {
-    const float v = __bfloat162float(xr[c]);
-    s1 += v;
-    s2 += v * v;
+// out = add + dx (the residual branch's gradient, may be null); d gamma = sum over rows of dy * xhat
+// and d beta = sum of dy (LayerNorm), gathered as per-CTA partial rows.
+constexpr int kNormBwdRows = 16;  // rows per CTA: one partial row of d gamma (and d beta) per CTA
+
+// Sum of (a, b) over the CTA; every thread gets both totals.
+__device__ __forceinline__ float2 cta_sum2(float a, float b, float2* red) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  a = warp_sum_f(a);
+  b = warp_sum_f(b);
+  __syncthreads();
+  if (lane == 0) red[warp] = make_float2(a, b);
+  __syncthreads();
+  float2 t = make_float2(0.f, 0.f);
+  for (int i = 0; i < nw; ++i) {
+    t.x += red[i].x;
+    t.y += red[i].y;
   }
-  s1 = cta_sum(s1, red);
-  s2 = cta_sum(s2, red);
-  const float mean = layer_norm ? s1 / H : 0.f;
-  const float var = layer_norm ? fmaxf(s2 / H - mean * mean, 0.f) : s2 / H;
-  float var2 = var;
-  if (layer_norm) {  // two-pass variance for accuracy
-    float sq = 0.f;
-    for (int c = threadIdx.x; c < H; c += blockDim.x) {
-      const float dd = __bfloat162float(xr[c]) - mean;
-      sq += dd * dd;
+  return t;
+}
+
+// One CTA per kNormBwdRows rows; each thread holds VPT 8-column vectors of a row in registers (x
+// and dy read once, 16 bytes at a time).  partial[blockIdx.x, :] = sum over the CTA's rows of
+// dy * xhat (and, LayerNorm, partial[gridDim.x + blockIdx.x, :] = sum of dy), folded over the CTAs
+// by the column-sum kernel into d gamma (d beta).
+template <int VPT, bool LN>
+__global__ void __launch_bounds__(1024) norm_bwd_kernel(const bf16* __restrict__ dy, const bf16* __restrict__ x,
+                                                        const bf16* __restrict__ gamma, const bf16* __restrict__ add,
+                                                        bf16* __restrict__ out, float* __restrict__ partial, int T,
+                                                        int H, float eps) {
+  __shared__ float2 red[32];
+  const int nvec = H >> 3;
+  const float inv_h = 1.0f / static_cast<float>(H);
+  float gm[VPT][8], pg[VPT][8], pb[VPT][8];
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int idx = i * blockDim.x + threadIdx.x;
+    if (idx < nvec) {
+      unpack_bf16x8(reinterpret_cast<const uint4*>(gamma)[idx], gm[i]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) gm[i][e] = 0.f;
     }
-    var2 = cta_sum(sq, red) / H;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) pg[i][e] = pb[i][e] = 0.f;
   }
-  const float r = rsqrtf(var2 + eps);
-  float a1 = 0.f, a2 = 0.f;
-  for (int c = threadIdx.x; c < H; c += blockDim.x) {
-    const float xh = (__bfloat162float(xr[c]) - mean) * r;
-    const float gx = __bfloat162float(dr[c]) * __bfloat162float(gamma[c]);
-    a1 += gx;
-    a2 += gx * xh;
+  const int r_end = min(T, static_cast<int>(blockIdx.x + 1) * kNormBwdRows);
+  for (int row = blockIdx.x * kNormBwdRows; row < r_end; ++row) {
+    const size_t base = static_cast<size_t>(row) * nvec;
+    float xv[VPT][8], gv[VPT][8];
+    float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int idx = i * blockDim.x + threadIdx.x;
+      const bool in = idx < nvec;
+      unpack_bf16x8(in ? reinterpret_cast<const uint4*>(x)[base + idx] : make_uint4(0u, 0u, 0u, 0u), xv[i]);
+      unpack_bf16x8(in ? reinterpret_cast<const uint4*>(dy)[base + idx] : make_uint4(0u, 0u, 0u, 0u), gv[i]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        s1 += xv[i][e];
+        s2 += xv[i][e] * xv[i][e];
+      }
+    }
+    float mean = 0.f, var;
+    if (LN) {  // two-pass variance from the registers
+      mean = cta_sum2(s1, 0.f, red).x * inv_h;
+      float sq = 0.f;
+#pragma unroll
+      for (int i = 0; i < VPT; ++i)
+        if (i * static_cast<int>(blockDim.x) + static_cast<int>(threadIdx.x) < nvec)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float dd = xv[i][e] - mean;
+            sq += dd * dd;
+          }
+      var = cta_sum2(sq, 0.f, red).x * inv_h;
+    } else {
+      var = cta_sum2(s2, 0.f, red).x * inv_h;
+    }
+    const float r = rsqrtf(var + eps);
+    float a1 = 0.f, a2 = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float xh = (xv[i][e] - mean) * r, gx = gv[i][e] * gm[i][e];
+        a1 += gx;
+        a2 += gx * xh;
+      }
+    const float2 a = cta_sum2(a1, a2, red);
+    const float m1 = LN ? a.x * inv_h : 0.f, m2 = a.y * inv_h;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int idx = i * blockDim.x + threadIdx.x;
+      if (idx >= nvec) continue;
+      float ad[8], o[8];
+      if (add != nullptr) {
+        unpack_bf16x8(reinterpret_cast<const uint4*>(add)[base + idx], ad);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ad[e] = 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float xh = (xv[i][e] - mean) * r;
+        o[e] = r * (gv[i][e] * gm[i][e] - xh * m2 - m1) + ad[e];
+        pg[i][e] += gv[i][e] * xh;
+        pb[i][e] += gv[i][e];
+      }
+      reinterpret_cast<uint4*>(out)[base + idx] = pack_bf16x8(o);
+    }
   }
-  a1 = cta_sum(a1, red) / H;
-  a2 = cta_sum(a2, red) / H;
-  for (int c = threadIdx.x; c < H; c += blockDim.x) {
-    const float xh = (__bfloat162float(xr[c]) - mean) * r;
-    const float g = __bfloat162float(dr[c]);
-    const float gx = g * __bfloat162float(gamma[c]);
-    float dx = r * (gx - xh * a2 - (layer_norm ? a1 : 0.f));
-    if (add != nullptr) dx += __bfloat162float(add[row * H + c]);
-    out[row * H + c] = __float2bfloat16_rn(dx);
-    grow[row * H + c] = g * xh;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int idx = i * blockDim.x + threadIdx.x;
+    if (idx >= nvec) continue;
+    float4* pr = reinterpret_cast<float4*>(partial + static_cast<size_t>(blockIdx.x) * H + idx * 8);
+    pr[0] = make_float4(pg[i][0], pg[i][1], pg[i][2], pg[i][3]);
+    pr[1] = make_float4(pg[i][4], pg[i][5], pg[i][6], pg[i][7]);
+    if (LN) {
+      float4* pq = reinterpret_cast<float4*>(partial + static_cast<size_t>(gridDim.x + blockIdx.x) * H + idx * 8);
+      pq[0] = make_float4(pb[i][0], pb[i][1], pb[i][2], pb[i][3]);
+      pq[1] = make_float4(pb[i][4], pb[i][5], pb[i][6], pb[i][7]);
+    }
   }
 }
 
@@ -181,20 +260,34 @@ __global__ void rope_bwd_pack_kernel(const float* __restrict__ dq, const float* 
   const int s = t / B, b = t - s * B;
   const int half = d / 2;
   const int ncols = (nh + 2 * ng) * d;
-  for (int c = threadIdx.x; c < ncols; c += blockDim.x) {
+  // eight consecutive columns of one head per thread and step (d / 2 is a multiple of 8)
+  for (int c = threadIdx.x * 8; c < ncols; c += blockDim.x * 8) {
     const int head = c / d, i = c - head * d;
     const float* src;
     if (head < nh) src = dq + ((static_cast<size_t>(b) * nh + head) * S + s) * d;
     else if (head < nh + ng) src = dk + ((static_cast<size_t>(b) * ng + head - nh) * S + s) * d;
     else src = dv + ((static_cast<size_t>(b) * ng + head - nh - ng) * S + s) * d;
-    float g = src[i];
+    float g[8];
+    *reinterpret_cast<float4*>(g) = *reinterpret_cast<const float4*>(src + i);
+    *reinterpret_cast<float4*>(g + 4) = *reinterpret_cast<const float4*>(src + i + 4);
     if (rope != nullptr && head < nh + ng) {
-      const int p = i < half ? i : i - half;
-      const float2 cs = rope[static_cast<size_t>(s) * half + p];
       // forward: y1 = x1 c - x2 s, y2 = x2 c + x1 s  ->  dx1 = dy1 c + dy2 s, dx2 = dy2 c - dy1 s
-      g = i < half ? src[i] * cs.x + src[i + half] * cs.y : src[i] * cs.x - src[i - half] * cs.y;
+      const bool first = i < half;
+      const int p = first ? i : i - half;
+      const float* o_src = src + (first ? i + half : i - half);
+      float o[8];
+      *reinterpret_cast<float4*>(o) = *reinterpret_cast<const float4*>(o_src);
+      *reinterpret_cast<float4*>(o + 4) = *reinterpret_cast<const float4*>(o_src + 4);
+      const float4* cs4 = reinterpret_cast<const float4*>(rope + static_cast<size_t>(s) * half + p);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float4 cs = cs4[k];  // (cos, sin) of columns p + 2k and p + 2k + 1
+        const float sg = first ? 1.f : -1.f;
+        g[2 * k] = g[2 * k] * cs.x + sg * o[2 * k] * cs.y;
+        g[2 * k + 1] = g[2 * k + 1] * cs.z + sg * o[2 * k + 1] * cs.w;
+      }
     }
-    dqkv[static_cast<size_t>(t) * ncols + c] = __float2bfloat16_rn(g);
+    *reinterpret_cast<uint4*>(dqkv + static_cast<size_t>(t) * ncols + c) = pack_bf16x8(g);
   }
 }
 
@@ -220,10 +313,16 @@ cudaError_t launch_act_bwd(const bf16* u, const bf16* da, bf16* du, size_t T, in
   return cudaGetLastError();
 }
 
-cudaError_t launch_norm_bwd(const bf16* dy, const bf16* x, const bf16* gamma, const bf16* add, bf16* out, float* grow,
-                            int T, int H, float eps, bool layer_norm, cudaStream_t st) {
+int norm_bwd_blocks(int T) { return (T + kNormBwdRows - 1) / kNormBwdRows; }
+
+cudaError_t launch_norm_bwd(const bf16* dy, const bf16* x, const bf16* gamma, const bf16* add, bf16* out,
+                            float* partial, int T, int H, float eps, bool layer_norm, cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
-  norm_bwd_kernel<<<T, 256, 0, st>>>(dy, x, gamma, add, out, grow, H, eps, layer_norm ? 1 : 0);
+  if (H % 8 != 0 || H > 8192) return cudaErrorInvalidValue;  // one 8-column vector per thread
+  const int threads = (H / 8 + 31) / 32 * 32;
+  const int blocks = norm_bwd_blocks(T);
+  if (layer_norm) norm_bwd_kernel<1, true><<<blocks, threads, 0, st>>>(dy, x, gamma, add, out, partial, T, H, eps);
+  else norm_bwd_kernel<1, false><<<blocks, threads, 0, st>>>(dy, x, gamma, add, out, partial, T, H, eps);
   return cudaGetLastError();
 }
 
@@ -239,7 +338,9 @@ cudaError_t launch_colsum(const void* src, bool f32, size_t ld, int T, int N, fl
 
 cudaError_t launch_rope_bwd_pack(const float* dq, const float* dk, const float* dv, const float2* rope, bf16* dqkv,
                                  int S, int B, int nh, int ng, int d, cudaStream_t st) {
-  rope_bwd_pack_kernel<<<S * B, 256, 0, st>>>(dq, dk, dv, rope, dqkv, S, B, nh, ng, d);
+  if (d % 16 != 0) return cudaErrorInvalidValue;  // eight-column vectors inside each half of a head
+  const int threads = std::min(256, ((nh + 2 * ng) * d / 8 + 31) / 32 * 32);
+  rope_bwd_pack_kernel<<<S * B, threads, 0, st>>>(dq, dk, dv, rope, dqkv, S, B, nh, ng, d);
   return cudaGetLastError();
 }
 

@@ -168,8 +168,11 @@ cudaError_t launch_quantize_e4m3(const bf16* x, size_t n, uint8_t* q, float* slo
 // ---- backward pass (backward_kernels.cu)
 cudaError_t launch_act_fwd(const bf16* u, bf16* a, size_t T, int f, bool swiglu, cudaStream_t st);
 cudaError_t launch_act_bwd(const bf16* u, const bf16* da, bf16* du, size_t T, int f, bool swiglu, cudaStream_t st);
-cudaError_t launch_norm_bwd(const bf16* dy, const bf16* x, const bf16* gamma, const bf16* add, bf16* out, float* grow,
-                            int T, int H, float eps, bool layer_norm, cudaStream_t st);
+// dx of a norm (plus `add`), and per-CTA partial rows of d gamma (rows [0, norm_bwd_blocks(T)) of
+// `partial`, pitch H) and, for LayerNorm, of d beta (the next norm_bwd_blocks(T) rows).
+int norm_bwd_blocks(int T);
+cudaError_t launch_norm_bwd(const bf16* dy, const bf16* x, const bf16* gamma, const bf16* add, bf16* out,
+                            float* partial, int T, int H, float eps, bool layer_norm, cudaStream_t st);
 cudaError_t launch_colsum(const void* src, bool f32, size_t ld, int T, int N, float* acc, bf16* out, cudaStream_t st);
 cudaError_t launch_rope_bwd_pack(const float* dq, const float* dk, const float* dv, const float2* rope, bf16* dqkv,
                                  int S, int B, int nh, int ng, int d, cudaStream_t st);
