@@ -502,11 +502,14 @@ __device__ __forceinline__ void softmax_head(const AttnParams& p, const Work& wk
   }
 }
 
-template <int D>
+// TG (two groups): the CTA's two heads belong to different kv groups (MHA, or an odd number of
+// heads per group) and every ring slot holds both groups' tiles, head t's at offset t * 16 KB; d = 64.
+template <int D, bool TG = false>
 struct Geo2 {
+  static_assert(!TG || D == 64, "a ring slot holds two groups' tiles only at d = 64");
   static constexpr int ATOM = 128 * 128;        // [128 rows x 64 fp16/bf16] swizzle block, 16 KB
   static constexpr int Q_BYTES = BQ * D * 2;    // per head
-  static constexpr int KV_BYTES = BKV * D * 2;  // a K or V tile [128 keys x d]: d/64 atoms
+  static constexpr int KV_BYTES = (TG ? 2 : 1) * BKV * D * 2;  // K or V tiles [128 keys x d]: d/64 atoms each
   static constexpr int P_BYTES = BQ * BKV * 2;  // per head: two key halves of 16 KB
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = 2 * Q_BYTES;  // three-slot ring shared by K and V tiles
@@ -517,13 +520,14 @@ struct Geo2 {
   static constexpr uint32_t IDESC_S = idesc_bf16(BQ, BKV);
   static constexpr uint32_t IDESC_O = idesc_f16(BQ, D) | (1u << 16);  // fp16 P (K-major), fp16 V (MN-major)
 };
-static_assert(Geo2<128>::SMEM_USED <= 232448, "attention tiles exceed the shared memory of a CTA");
+static_assert(Geo2<128>::SMEM_USED <= 232448 && Geo2<64, true>::SMEM_USED <= 232448,
+              "attention tiles exceed the shared memory of a CTA");
 
-template <int D>
+template <int D, bool TG>
 __global__ void __launch_bounds__(320, 1)
     attn2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
-  using G = Geo2<D>;
+  using G = Geo2<D, TG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + G::OFF_BAR);
@@ -551,7 +555,8 @@ __global__ void __launch_bounds__(320, 1)
   Work wk;
   if (!decode_work(p, p.nh >> 1, 2, wk)) return;  // uniform over the CTA, before any barrier or TMEM use
   const int qb = wk.qb, b = wk.b, h0 = wk.h;
-  const int g = h0 / (p.nh / p.ng);
+  const int g = h0 / (p.nh / p.ng), g1 = (h0 + 1) / (p.nh / p.ng);  // the heads' kv groups (equal unless TG)
+  constexpr uint32_t HEAD_OFF = TG ? G::ATOM : 0u;  // head 1's tile inside a ring slot
   const int nkv = qb + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -603,9 +608,14 @@ __global__ void __launch_bounds__(320, 1)
         const int n = issued;
         if (!mbar_wait(kv_empty(n), use_parity(n) ^ 1u, p.err, abort_flag)) return false;
         mbar_arrive_expect_tx(kv_full(n), G::KV_BYTES);
+        if (TG) {  // both heads' groups, one [128 x 64] box each
+          tma_load_3d(sKV(n), map, kv_full(n), 0, wk.kv_row0 + j * BKV, b * p.ng + g);
+          tma_load_3d(sKV(n) + HEAD_OFF, map, kv_full(n), 0, wk.kv_row0 + j * BKV, b * p.ng + g1);
+        } else {
 #pragma unroll
-        for (int a = 0; a < D / 64; ++a)
-          tma_load_3d(sKV(n) + a * G::ATOM, map, kv_full(n), a * 64, wk.kv_row0 + j * BKV, b * p.ng + g);
+          for (int a = 0; a < D / 64; ++a)
+            tma_load_3d(sKV(n) + a * G::ATOM, map, kv_full(n), a * 64, wk.kv_row0 + j * BKV, b * p.ng + g);
+        }
         ++issued;
         return true;
       };
@@ -629,7 +639,8 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * G::ATOM + (k & 3) * 32;
-          mma_bf16_ss(tS(t), sw128_desc(sQa(t) + off), sw128_desc(sKV(n) + off), G::IDESC_S, k > 0 ? 1u : 0u);
+          mma_bf16_ss(tS(t), sw128_desc(sQa(t) + off), sw128_desc(sKV(n) + t * HEAD_OFF + off), G::IDESC_S,
+                      k > 0 ? 1u : 0u);
         }
         mma_commit(s_full(t));
       };
@@ -675,7 +686,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int k = 0; k < BKV / 16; ++k) {
             const uint32_t pa = sPa(t) + (k >> 2) * G::ATOM + (k & 3) * 32;
-            mma_bf16_ss(tO(t), sw128_desc(pa), sw128_desc_mn(sV + k * 2048, G::ATOM), G::IDESC_O,
+            mma_bf16_ss(tO(t), sw128_desc(pa), sw128_desc_mn(sV + t * HEAD_OFF + k * 2048, G::ATOM), G::IDESC_O,
                         (j > 0 || k > 0) ? 1u : 0u);
           }
           mma_commit(o_done(t));
@@ -699,18 +710,18 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-template <int D>
+template <int D, bool TG>
 cudaError_t launch_d2(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnParams& p,
                       cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn2_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(Geo2<D>::SMEM));
+    cudaError_t e = cudaFuncSetAttribute(attn2_kernel<D, TG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(Geo2<D, TG>::SMEM));
     if (e != cudaSuccess) return e;
     configured = true;
   }
   const unsigned grid = static_cast<unsigned>(p.num_qb) * (p.cu ? p.num_seqs : p.batch) * (p.nh / 2);
-  return launch_pdl(attn2_kernel<D>, dim3(grid), dim3(320), Geo2<D>::SMEM, stream, tmQ, tmK, tmV, p);
+  return launch_pdl(attn2_kernel<D, TG>, dim3(grid), dim3(320), Geo2<D, TG>::SMEM, stream, tmQ, tmK, tmV, p);
 }
 
 template <int D>
@@ -733,8 +744,10 @@ cudaError_t launch_attention(int head_dim, const CUtensorMap& tmQ, const CUtenso
                              const AttnParams& p, cudaStream_t stream) {
   if (p.num_qb <= 0) return cudaSuccess;
   const bool paired = ((p.nh / p.ng) & 1) == 0;  // an even number of query heads per kv group
-  if (paired && head_dim == 64) return launch_d2<64>(tmQ, tmK, tmV, p, stream);
-  if (paired && head_dim == 128) return launch_d2<128>(tmQ, tmK, tmV, p, stream);
+  if (paired && head_dim == 64) return launch_d2<64, false>(tmQ, tmK, tmV, p, stream);
+  if (paired && head_dim == 128) return launch_d2<128, false>(tmQ, tmK, tmV, p, stream);
+  // d = 64 with an odd number of heads per group (MHA): two heads of two groups per CTA
+  if (head_dim == 64 && (p.nh & 1) == 0) return launch_d2<64, true>(tmQ, tmK, tmV, p, stream);
   if (head_dim == 64) return launch_d<64>(tmQ, tmK, tmV, p, stream);
   if (head_dim == 128) return launch_d<128>(tmQ, tmK, tmV, p, stream);
   return cudaErrorInvalidValue;

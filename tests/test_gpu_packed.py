@@ -44,9 +44,9 @@ LENS = [
 
 
 @pytest.mark.parametrize("lens", LENS, ids=lambda l: "-".join(map(str, l)))
-@pytest.mark.parametrize("shape", ["gqa_d64", "mha_d128_ln_gelu", "gqa4_d128"])
+@pytest.mark.parametrize("shape", ["gqa_d64", "mha_d128_ln_gelu", "gqa4_d128", "mha_d64"])
 def test_packed_layer_matches_oracle(lens, shape):
-    kw = {"gqa_d64": {}, "gqa4_d128": dict(heads=8, groups=2, head_dim=128),  # the CTA-pair attention
+    kw = {"gqa_d64": {}, "gqa4_d128": dict(heads=8, groups=2, head_dim=128), "mha_d64": dict(groups=8),
           "mha_d128_ln_gelu": dict(heads=4, groups=4, head_dim=128, norm="layer", act="gelu_tanh", bias=True)}[shape]
     cfg = _cfg(lens, **kw)
     inp = synth.make_inputs(cfg, seed=51, affine="random", biases="random")

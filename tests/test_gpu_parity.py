@@ -106,6 +106,7 @@ EDGE = [
     small(seq=130, head_dim=128, heads=4, groups=1, norm="layer", act="gelu_tanh", rope_base=0.0, bias=True),
     small(batch=2, seq=384, heads=16, groups=2, ffn=1376),     # 8 heads per group
     small(hidden=264, heads=2, groups=2, ffn=520, seq=64),     # hidden and ffn not multiples of 64/128
+    small(heads=6, groups=2, seq=300),                         # 3 heads per group: a CTA's two heads straddle groups
 ]
 
 
