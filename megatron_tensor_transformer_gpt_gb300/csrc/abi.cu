@@ -324,6 +324,9 @@ void plan_gemm(mt::GemmParams& p, int mode, int head_dim) {
     }
   p.full_units = p.split > 1 ? waves * workers : p.num_tiles;
   p.num_units = p.full_units + (p.split > 1 ? rest * p.split : 0);
+  // two epilogue warps per quadrant where the epilogue would pace the GEMM: a short main loop per
+  // tile (K <= 2048) or at most one tile per CTA; one elsewhere (measured faster for long K)
+  p.epi_split = (p.K <= 2048 || p.num_units <= workers) ? 2 : 1;
 }
 
 // One GEMM: A [M, K] (pitch lda) x W [rows_w, K]^T with the given epilogue.

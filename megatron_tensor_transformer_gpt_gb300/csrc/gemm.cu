@@ -114,7 +114,7 @@ __device__ __forceinline__ void store_e4m3x32(uint8_t* dst_row, int col, int lim
 
 template <int MODE, bool F8>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc, int m0, int c0, int width,
-                                              int r_in_tile) {
+                                              int r_in_tile, int lo, int hi) {
   const int row = m0 + r_in_tile;
   const bool valid = row < p.M;
   const float deq = F8 ? __ldg(p.deq_a) * __ldg(p.deq_b) : 1.f;
@@ -123,7 +123,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
   float amax = 0.f;
   if constexpr (MODE == kEpiStore || MODE == kEpiResid || MODE == kEpiGelu) {
 #pragma unroll 1
-    for (int c = 0; c < width; c += 32) {
+    for (int c = lo; c < hi; c += 32) {
       const int col = c0 + c;
       if (col >= p.N) break;  // uniform across the warp
       float v[32];
@@ -164,7 +164,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
     }
   } else if constexpr (MODE == kEpiSwiglu) {
 #pragma unroll 1
-    for (int c = 0; c < width; c += 32) {
+    for (int c = lo; c < hi; c += 32) {
       const int col = c0 + c;
       if (col >= p.N) break;
       float g[32], u[32];
@@ -198,7 +198,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
     const int b = valid ? trow - s * p.batch : 0;
     const int rpos = (valid && p.pos != nullptr) ? p.pos[trow] : s;    // RoPE position
 #pragma unroll 1
-    for (int hc = 0; hc < width; hc += d) {
+    for (int hc = lo; hc < hi; hc += d) {
       const int col = c0 + hc;
       if (col >= p.N) break;
       bf16* dst = nullptr;
@@ -268,9 +268,23 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
   }
 }
 
+// Epilogue warps: two per TMEM lane quadrant.  With p.epi_split == 2 both store part of a unit's
+// `width` columns (part 0 the first half, rounded down to 32 columns, QKV: to whole heads; part 1
+// the rest; a unit too narrow to split goes to part 0 alone); with 1 the first warp of each quadrant
+// stores all of them and the second stays idle.
+constexpr int EPI_WARPS = 8;
+constexpr int GEMM_THREADS = 64 + 32 * EPI_WARPS;  // TMA warp, MMA warp, epilogue warps
+template <int MODE>
+__device__ __forceinline__ void epilogue_part(const GemmParams& p, int width, int part, int& lo, int& hi) {
+  const int gran = MODE == kEpiQkv ? p.head_dim : 32;
+  const int mid = p.epi_split == 2 ? (width / 2) / gran * gran : 0;
+  lo = part == 0 ? 0 : (mid == 0 ? width : mid);
+  hi = part == 0 ? (mid == 0 ? width : mid) : width;
+}
+
 // ------------------------------------------------------------------ kernel
 template <int MODE, bool F8>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmB64, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -296,7 +310,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull(a), 1);
-      mbar_init(tempty(a), 4);
+      mbar_init(tempty(a), 4 * p.epi_split);  // the active epilogue warps
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -424,8 +438,9 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     const int quad = warp & 3;  // TMEM lanes this warp may read
+    const int part = (warp - 2) >> 2;
     int it = 0;
-    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++it) {
+    for (int u = blockIdx.x; part < p.epi_split && u < p.num_units; u += gridDim.x, ++it) {
       const int acc = it & 1;
       const uint32_t use = (it >> 1) & 1;
       const bool ok = mbar_wait(tfull(acc), use, p.err, abort_flag);
@@ -433,7 +448,10 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       const Unit w = decode_unit(p, u);
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
-      epilogue_tile<MODE, F8>(p, tacc, w.tm * BM, unit_col0<MODE>(w), unit_width<MODE>(w), quad * 32 + lane);
+      int lo, hi;
+      epilogue_part<MODE>(p, unit_width<MODE>(w), part, lo, hi);
+      if (lo < hi)
+        epilogue_tile<MODE, F8>(p, tacc, w.tm * BM, unit_col0<MODE>(w), unit_width<MODE>(w), quad * 32 + lane, lo, hi);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty(acc));
@@ -454,14 +472,14 @@ __global__ void __launch_bounds__(192, 1)
 // fits P_STAGES stages.  The even CTA's thread issues the M = 256 MMAs, which write each CTA's
 // 128 accumulator rows into that CTA's tensor memory; its commits arrive on the barriers of both
 // CTAs.  Both CTAs' TMA copies complete on the even CTA's `full` barriers, and both CTAs'
-// epilogue warps release an accumulator on the even CTA's `tempty` barrier (count 8).
+// active epilogue warps release an accumulator on the even CTA's `tempty` barrier (count 8 * epi_split).
 constexpr int P_STAGES = 6;
 constexpr int P_B_BYTES = 128 * BK * 2;  // up to 128 B rows per CTA
 constexpr int P_STAGE_BYTES = A_BYTES + P_B_BYTES;
 constexpr size_t P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + 256;
 
 template <int MODE, bool F8>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmB64, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -489,7 +507,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull(a), 1);
-      mbar_init(tempty(a), 8);
+      mbar_init(tempty(a), 8 * p.epi_split);  // both CTAs' active epilogue warps
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -612,8 +630,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     }
   } else {
     const int quad = warp & 3;
+    const int part = (warp - 2) >> 2;
     int it = 0;
-    for (int u = pair; u < p.num_units; u += npairs, ++it) {
+    for (int u = pair; part < p.epi_split && u < p.num_units; u += npairs, ++it) {
       const int acc = it & 1;
       const uint32_t use = (it >> 1) & 1;
       const bool ok = mbar_wait(tfull(acc), use, p.err, abort_flag);
@@ -621,8 +640,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       tc_fence_after();
       const Unit w = decode_unit(p, u);
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
-      epilogue_tile<MODE, F8>(p, tacc, w.tm * (2 * BM) + static_cast<int>(rank) * BM, unit_col0<MODE>(w),
-                              unit_width<MODE>(w), quad * 32 + lane);
+      int lo, hi;
+      epilogue_part<MODE>(p, unit_width<MODE>(w), part, lo, hi);
+      if (lo < hi)
+        epilogue_tile<MODE, F8>(p, tacc, w.tm * (2 * BM) + static_cast<int>(rank) * BM, unit_col0<MODE>(w),
+                                unit_width<MODE>(w), quad * 32 + lane, lo, hi);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty(acc), 0));
@@ -653,10 +675,10 @@ cudaError_t launch_mode(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
   if (p.pair) {
     const int pairs = gemm_pair_slots();
     const int grid = 2 * (p.num_units < pairs ? p.num_units : pairs);
-    return launch_pdl(gemm_pair_kernel<MODE, F8>, dim3(grid), dim3(192), P_SMEM_BYTES, stream, tmA, tmB, tmB64, p);
+    return launch_pdl(gemm_pair_kernel<MODE, F8>, dim3(grid), dim3(GEMM_THREADS), P_SMEM_BYTES, stream, tmA, tmB, tmB64, p);
   }
   const int grid = p.num_units < num_sms() ? p.num_units : num_sms();
-  return launch_pdl(gemm_kernel<MODE, F8>, dim3(grid), dim3(192), SMEM_BYTES, stream, tmA, tmB, tmB64, p);
+  return launch_pdl(gemm_kernel<MODE, F8>, dim3(grid), dim3(GEMM_THREADS), SMEM_BYTES, stream, tmA, tmB, tmB64, p);
 }
 
 template <bool F8>

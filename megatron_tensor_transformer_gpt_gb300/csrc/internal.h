@@ -34,6 +34,9 @@ struct GemmParams {
   // CTA pairs (pair = 1): tiles are 256 x 256 and computed by a cluster of two CTAs sharing one
   // M = 256 MMA (tiles_m counts 256-row tiles); otherwise one CTA per 128 x 256 tile.
   int pair;
+  // epilogue warps per TMEM lane quadrant that store a tile (1 or 2): 2 where the epilogue would
+  // otherwise pace the GEMM (a short main loop per tile, or a single wave of tiles)
+  int epi_split;
   // Operand layouts (bf16 only): a_mn = 1 when A is stored [K, M] (M contiguous) instead of [M, K];
   // b_mn = 1 when B is stored [K, N] instead of [N, K].  The tensor maps then hold 64 x 64 boxes
   // (64 M or N elements by 64 K rows) and the MMA reads the tiles MN-major.  Plain stores only.
