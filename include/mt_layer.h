@@ -256,9 +256,9 @@ int mt_gemm_bf16_t(const void* A, int a_layout, const void* B, int b_layout, voi
                    void* cuda_stream);
 
 /* GEMM kernel choice for every later launch in the process (all handles): 0 automatic (the
- * default: pairs of CTAs sharing one M = 256 tcgen05.mma per 256 x 256 tile when M > 128 and the
- * GEMM fills at least one wave of SM pairs, else one CTA per 128 x 256 tile), 1 one CTA per tile
- * always, 2 CTA pairs wherever M > 128.  Both kernels compute the same fp32 sums in the same K
+ * default: pairs of CTAs sharing one M = 256 tcgen05.mma per 256 x 256 tile when M > 128, else one
+ * CTA per 128 x 256 tile), 1 one CTA per tile always, 2 CTA pairs wherever M > 128 (the same as
+ * 0 now; kept for the tests that force each kernel).  Both kernels compute the same fp32 sums in the same K
  * order.  A tuning and testing control; returns MT_ERR_INVALID_ARG for other values. */
 int mt_gemm_set_pairing(int mode);
 
