@@ -787,7 +787,7 @@ int norm_bwd(mt_layer* L, const BwLayout& b, const void* dy, const void* x, cons
 int backward_device(mt_layer* L, const BwLayout& b, const void* x, const void* dy, int S, int B, const mt_weights* w,
                     void* dx, const mt_grads* g, cudaStream_t st) {
   const Layout& lay = b.fwd;
-  const int T = S * B, H = L->hidden, d = L->head_dim, nh = L->nh_r, ng = L->ng_r, rep = nh / ng;
+  const int T = S * B, H = L->hidden, d = L->head_dim, nh = L->nh_r, ng = L->ng_r;
   const int qw = L->q_w, kvw = L->kv_w, QKV = qw + 2 * kvw, f = L->f_r, f1 = L->f1_r;
   const bool swiglu = L->act == MT_ACT_SWIGLU;
   int rc;
