@@ -5,18 +5,22 @@
 // num_query_groups of "ai阅读megatron" TransformerConfig; FlashAttention is the prior art the
 // pages name: exact attention computed block by block with an online softmax, O(S) memory.)
 //
-// One CTA per (128-query block, head, batch row); CTAs are issued longest-first (the last query
-// blocks see the most keys).  Per CTA:
-//   warp 0      TMA: the Q tile once, then K and V tiles [128 keys x d] into a 2-stage ring.  The
-//               P V product reads the V tile as an MN-major operand (its d index contiguous).
-//   warp 1      one thread issues S_j = Q K_j^T into one of two TMEM score buffers (128 columns
-//               each), and O += P_j V_j into a TMEM output accumulator (d columns).
-//   warps 2..5  softmax, one query row per thread: reads S_j from TMEM, masks the diagonal
-//               block, keeps a running maximum and sum in the log2 domain, writes P_j = 2^(s - m)
-//               as bf16 into shared memory in the 128-byte-swizzled layout the MMA reads, and
-//               rescales O in TMEM only when the running maximum grows by more than 2^8
-//               (between rescales P stays below 256, exact in fp32 sums and in bf16 range).
-//               At the end O / l is written as bf16 to o[t, h*d + i].
+// Three forms share one scheme, chosen by launch_attention from d and the heads per kv group:
+//   attn2_kernel<D, false>  an even number of heads per group: one CTA takes two heads of one group
+//                           for a 128-query block, so every K/V tile feeds both (all GQA/MQA
+//                           workloads);
+//   attn2_kernel<64, true>  d = 64 with an odd number of heads per group (MHA): two heads of two
+//                           groups, each ring slot holding both groups' tiles;
+//   attn_kernel<D>          otherwise (MHA at d = 128, or an odd number of heads): one head per CTA.
+// CTAs are issued longest-first (the last query blocks see the most keys).  In every form warp 0
+// loads the Q tile(s) and then K and V tiles [128 keys x d] by TMA; one thread of warp 1 issues
+// S_j = Q K_j^T into a TMEM score buffer and O += P_j V_j into a TMEM accumulator, reading V as an
+// MN-major operand (its d index contiguous); the softmax warps (one query row per thread) read S_j
+// from TMEM and release it at once, mask the diagonal block, keep a running maximum and sum in the
+// log2 domain, write P_j = 2^(s c - m) as fp16 into shared memory in the 128-byte-swizzled layout the
+// MMA reads, and rescale O in TMEM only when the running maximum grows by more than 2^8 (between
+// rescales P stays below 256).  At the end O / l is written as bf16 (or E4M3) to o[t, h*d + i] and,
+// when asked, m + log2(l) to lse for the backward pass.
 #include <math.h>
 
 #include "common.cuh"
