@@ -413,13 +413,10 @@ int run_attention_block(mt_layer* L, const Layout& lay, const void* x, int S, in
                         const Chunks* in = nullptr) {
   const int T = S * B, H = L->hidden, d = L->head_dim;
   cudaError_t e;
-  float2* rope = nullptr;
-  if (L->rope_base > 0.f) {
-    rope = region<float2>(L, lay, kRope);
-    Timed t(L, kSlotRope, st);
-    e = mt::launch_rope_table(rope, L->d_theta, pk ? pk->max_seqlen : S, d / 2, st);
-    if (e != cudaSuccess) return cuda_fail(e, "RoPE table launch");
-  }
+  // The RoPE table (positions 0 .. seq or max_seqlen, never more than the T token rows) is written
+  // by the norm1 launches, row by row, before the QKV GEMMs read it.
+  float2* rope = L->rope_base > 0.f ? region<float2>(L, lay, kRope) : nullptr;
+  mt::RopeRows rope_rows{rope, L->d_theta, pk ? pk->max_seqlen : S, d / 2, 0};
   int* pos = nullptr;
   if (pk != nullptr) {
     pos = region<int>(L, lay, kPos);
@@ -441,9 +438,10 @@ int run_attention_block(mt_layer* L, const Layout& lay, const void* x, int S, in
     const size_t off = static_cast<size_t>(r0) * H;
     {
       Timed t(L, kSlotNorm1, st);
+      rope_rows.row0 = r0;
       e = mt::launch_norm(L->norm == MT_NORM_LAYER, static_cast<const bf16*>(x) + off,
                           static_cast<const bf16*>(w->norm1_w), static_cast<const bf16*>(w->norm1_b), xn + off, rows,
-                          H, L->eps, st);
+                          H, L->eps, st, nullptr, nullptr, nullptr, rope != nullptr ? &rope_rows : nullptr);
     }
     if (e != cudaSuccess) return cuda_fail(e, "norm1 launch");
     p = gemm_params(rows, nqkv, H, false, L->d_err);
@@ -561,18 +559,14 @@ int forward_device_fp8(mt_layer* L, const Layout& lay, const void* x, int S, int
   float* deq = L->d_f8 + 4;
   unsigned* amax = reinterpret_cast<unsigned*>(L->d_f8 + 8);
   cudaError_t e;
-  float2* rope = nullptr;
-  if (L->rope_base > 0.f) {
-    rope = region<float2>(L, lay, kRope);
-    Timed t(L, kSlotRope, st);
-    e = mt::launch_rope_table(rope, L->d_theta, S, d / 2, st);
-    if (e != cudaSuccess) return cuda_fail(e, "RoPE table launch");
-  }
+  float2* rope = L->rope_base > 0.f ? region<float2>(L, lay, kRope) : nullptr;  // rows written by norm1
+  const mt::RopeRows rope_rows{rope, L->d_theta, S, d / 2, 0};
   uint8_t* xn8 = region<uint8_t>(L, lay, kXn);
   {
     Timed t(L, kSlotNorm1, st);
     e = mt::launch_norm(L->norm == MT_NORM_LAYER, static_cast<const bf16*>(x), static_cast<const bf16*>(w->norm1_w),
-                        static_cast<const bf16*>(w->norm1_b), nullptr, T, H, L->eps, st, xn8, scale + 0, amax + 0);
+                        static_cast<const bf16*>(w->norm1_b), nullptr, T, H, L->eps, st, xn8, scale + 0, amax + 0,
+                        rope != nullptr ? &rope_rows : nullptr);
   }
   if (e != cudaSuccess) return cuda_fail(e, "norm1 launch");
   bf16 *q = region<bf16>(L, lay, kQ), *k = region<bf16>(L, lay, kK);

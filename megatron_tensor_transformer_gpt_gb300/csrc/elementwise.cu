@@ -40,14 +40,33 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 //   LayerNorm: y = (x - mean) / sqrt(var + eps) * g + b     (biased variance, two passes)
 // OUT8: write E4M3 codes of y * (*q_scale) to y8 instead of bf16 y, and fold max |y| of the row
 // into *amax (one atomic per CTA).
+// (cos, sin) of s * theta_i.  The angle is formed and reduced modulo 2*pi in double precision, so
+// the single-precision sine/cosine act on an argument in [-pi, pi].
+__device__ __forceinline__ float2 rope_entry(int s, double theta_i) {
+  const double a = static_cast<double>(s) * theta_i;
+  const double turns = rint(a * 0.15915494309189535);  // a / (2 pi)
+  const float r = static_cast<float>(fma(-turns, 6.283185307179586, a));
+  float sn, cs;
+  sincosf(r, &sn, &cs);
+  return make_float2(cs, sn);
+}
+
+// rope.tab != null: the CTA of row r also writes row rope.row0 + r of the RoPE table (when below
+// rope.rows), so the table needs no launch of its own.
 template <int VPT, bool LN, bool OUT8>
 __global__ void __launch_bounds__(1024) norm_kernel(const bf16* __restrict__ x, const bf16* __restrict__ gamma,
                                                     const bf16* __restrict__ beta, bf16* __restrict__ y, int H,
                                                     float eps, uint8_t* __restrict__ y8, const float* q_scale,
-                                                    unsigned* amax) {
+                                                    unsigned* amax, const RopeRows rope) {
   __shared__ float red[32];
   pdl_wait();
   pdl_trigger();
+  if (rope.tab != nullptr) {
+    const int s = rope.row0 + static_cast<int>(blockIdx.x);
+    if (s < rope.rows)
+      for (int i = threadIdx.x; i < rope.half; i += blockDim.x)
+        rope.tab[static_cast<size_t>(s) * rope.half + i] = rope_entry(s, rope.theta[i]);
+  }
   const size_t row = blockIdx.x;
   const int nvec = H >> 3;
   const uint4* xr = reinterpret_cast<const uint4*>(x + row * H);
@@ -125,15 +144,16 @@ __global__ void __launch_bounds__(1024) norm_kernel(const bf16* __restrict__ x, 
 
 template <bool LN, bool OUT8>
 cudaError_t launch_norm_ln(const bf16* x, const bf16* g, const bf16* b, bf16* y, int rows, int H, float eps,
-                           uint8_t* y8, const float* q_scale, unsigned* amax, cudaStream_t stream) {
+                           uint8_t* y8, const float* q_scale, unsigned* amax, const RopeRows& rope,
+                           cudaStream_t stream) {
   const int nvec = H / 8;
   if (nvec >= 256) {  // two vectors per thread
     const int threads = ((nvec + 1) / 2 + 31) / 32 * 32;
     if (threads > 1024) return cudaErrorInvalidValue;
-    return launch_pdl(norm_kernel<2, LN, OUT8>, dim3(rows), dim3(threads), 0, stream, x, g, b, y, H, eps, y8, q_scale, amax);
+    return launch_pdl(norm_kernel<2, LN, OUT8>, dim3(rows), dim3(threads), 0, stream, x, g, b, y, H, eps, y8, q_scale, amax, rope);
   } else {
     const int threads = (nvec + 31) / 32 * 32;
-    return launch_pdl(norm_kernel<1, LN, OUT8>, dim3(rows), dim3(threads), 0, stream, x, g, b, y, H, eps, y8, q_scale, amax);
+    return launch_pdl(norm_kernel<1, LN, OUT8>, dim3(rows), dim3(threads), 0, stream, x, g, b, y, H, eps, y8, q_scale, amax, rope);
   }
 }
 
@@ -186,22 +206,6 @@ __global__ void fp8_history_kernel(float* state, int len, int pos) {
     state[t] = scale;
     state[4 + t] = __frcp_rn(scale);
   }
-}
-
-// (cos, sin) of s * theta_i for s < seq, i < half.  The angle is formed and reduced modulo 2*pi
-// in double precision, so the single-precision sine/cosine act on an argument in [-pi, pi].
-__global__ void rope_table_kernel(float2* __restrict__ tab, const double* __restrict__ theta, int seq, int half) {
-  pdl_wait();
-  pdl_trigger();
-  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= seq * half) return;
-  const int s = idx / half, i = idx - s * half;
-  const double a = static_cast<double>(s) * theta[i];
-  const double turns = rint(a * 0.15915494309189535);  // a / (2 pi)
-  const float r = static_cast<float>(fma(-turns, 6.283185307179586, a));
-  float sn, cs;
-  sincosf(r, &sn, &cs);
-  tab[idx] = make_float2(cs, sn);
 }
 
 // A barrier nothing will ever complete: the bounded wait has to give up and report.
@@ -335,13 +339,15 @@ __global__ void packed_index_kernel(const int* __restrict__ cu, int n, int T, in
 }  // namespace
 
 cudaError_t launch_norm(bool layer_norm, const bf16* x, const bf16* g, const bf16* b, bf16* y, int rows, int hidden,
-                        float eps, cudaStream_t stream, uint8_t* y8, const float* q_scale, unsigned* amax) {
+                        float eps, cudaStream_t stream, uint8_t* y8, const float* q_scale, unsigned* amax,
+                        const RopeRows* rope) {
   if (rows <= 0) return cudaSuccess;
+  const RopeRows rr = rope != nullptr ? *rope : RopeRows{};
   if (y8 != nullptr)
-    return layer_norm ? launch_norm_ln<true, true>(x, g, b, y, rows, hidden, eps, y8, q_scale, amax, stream)
-                      : launch_norm_ln<false, true>(x, g, b, y, rows, hidden, eps, y8, q_scale, amax, stream);
-  return layer_norm ? launch_norm_ln<true, false>(x, g, b, y, rows, hidden, eps, y8, q_scale, amax, stream)
-                    : launch_norm_ln<false, false>(x, g, b, y, rows, hidden, eps, y8, q_scale, amax, stream);
+    return layer_norm ? launch_norm_ln<true, true>(x, g, b, y, rows, hidden, eps, y8, q_scale, amax, rr, stream)
+                      : launch_norm_ln<false, true>(x, g, b, y, rows, hidden, eps, y8, q_scale, amax, rr, stream);
+  return layer_norm ? launch_norm_ln<true, false>(x, g, b, y, rows, hidden, eps, y8, q_scale, amax, rr, stream)
+                    : launch_norm_ln<false, false>(x, g, b, y, rows, hidden, eps, y8, q_scale, amax, rr, stream);
 }
 
 cudaError_t launch_quantize_e4m3(const bf16* x, size_t n, uint8_t* q, float* slot, cudaStream_t stream) {
@@ -357,12 +363,6 @@ cudaError_t launch_quantize_e4m3(const bf16* x, size_t n, uint8_t* q, float* slo
 cudaError_t launch_fp8_history(float* state, int len, int pos, cudaStream_t stream) {
   fp8_history_kernel<<<1, 128, 0, stream>>>(state, len, pos);
   return cudaGetLastError();
-}
-
-cudaError_t launch_rope_table(float2* table, const double* theta, int seq, int half, cudaStream_t stream) {
-  const int n = seq * half;
-  if (n <= 0) return cudaSuccess;
-  return launch_pdl(rope_table_kernel, dim3((n + 255) / 256), dim3(256), 0, stream, table, theta, seq, half);
 }
 
 cudaError_t launch_wait_selftest(int* err, unsigned long long limit_ns, cudaStream_t stream) {

@@ -159,10 +159,20 @@ size_t gemm_smem_bytes();
 cudaError_t launch_attention(int head_dim, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                              const AttnParams& p, cudaStream_t stream);
 
-// y8 != null: E4M3 output y * (*q_scale) into y8, max |y| folded into *amax.
+// RoPE table rows written by a norm launch: the CTA of row r writes table row row0 + r when it is
+// below `rows` ((cos, sin) of s * theta_i, i < half).  The caller's norm launches must cover rows
+// [0, rows) before the table is read.
+struct RopeRows {
+  float2* tab;
+  const double* theta;
+  int rows, half, row0;
+};
+
+// y8 != null: E4M3 output y * (*q_scale) into y8, max |y| folded into *amax.  rope != null: the
+// launch also writes RoPE table rows (see RopeRows).
 cudaError_t launch_norm(bool layer_norm, const bf16* x, const bf16* g, const bf16* b, bf16* y, int rows, int hidden,
                         float eps, cudaStream_t stream, uint8_t* y8 = nullptr, const float* q_scale = nullptr,
-                        unsigned* amax = nullptr);
+                        unsigned* amax = nullptr, const RopeRows* rope = nullptr);
 
 // Current per-tensor scaling of n (multiple of 8) bf16 values: slot[0] <- amax (float bits),
 // slot[1] <- 1/scale, q <- E4M3 codes of x * 448 / amax.
@@ -183,7 +193,6 @@ cudaError_t launch_rope_bwd_pack(const float* dq, const float* dk, const float* 
 // Delayed-scaling update after an FP8 forward (state layout: see fp8_history_kernel).
 cudaError_t launch_fp8_history(float* state, int len, int pos, cudaStream_t stream);
 
-cudaError_t launch_rope_table(float2* table, const double* theta, int seq, int half, cudaStream_t stream);
 
 cudaError_t launch_sp_add_norm(bool layer_norm, const SpParams& p, cudaStream_t stream);
 
