@@ -201,18 +201,6 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uin
       : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]^T: A (M=128 rows, one per TMEM lane, K packed two bf16 per 32-bit
-// column) is read from tensor memory, B from shared memory.
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                            uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -331,20 +319,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
       : "memory");
 }
 
-// Raw 32-bit variant of tmem_st32 (e.g. packed bf16 pairs).
-__device__ __forceinline__ void tmem_st32_raw(uint32_t taddr, const uint32_t* r) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
-      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
-      MT_W32(0), MT_W32(1), MT_W32(2), MT_W32(3), MT_W32(4), MT_W32(5), MT_W32(6), MT_W32(7), MT_W32(8),
-      MT_W32(9), MT_W32(10), MT_W32(11), MT_W32(12), MT_W32(13), MT_W32(14), MT_W32(15), MT_W32(16), MT_W32(17),
-      MT_W32(18), MT_W32(19), MT_W32(20), MT_W32(21), MT_W32(22), MT_W32(23), MT_W32(24), MT_W32(25), MT_W32(26),
-      MT_W32(27), MT_W32(28), MT_W32(29), MT_W32(30), MT_W32(31)
-      : "memory");
-}
-
 // Each thread reads 128 consecutive fp32 columns of its own TMEM lane in one instruction and
 // waits for them.
 __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float* v) {
@@ -358,12 +332,6 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float* v) {
 #pragma unroll
   for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
 }
-
-// tmem_st32_raw without the wait: a later tcgen05.wait::st (tmem_st_wait) completes it.
-__device__ __forceinline__ void tmem_st32_raw_nowait(uint32_t taddr, const uint32_t* r) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]) : "memory");
-}
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 #undef MT_R32
 #undef MT_W32
