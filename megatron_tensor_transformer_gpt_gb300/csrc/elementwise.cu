@@ -2,8 +2,6 @@
 // bounded-wait self test.
 #include <math.h>
 
-#include <algorithm>
-
 #include "common.cuh"
 #include "internal.h"
 
@@ -36,6 +34,12 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return t;
 }
 
+// One CTA per row; thread i holds VPT 16-byte vectors (8 bf16 each) of the row in registers,
+// statistics in fp32.
+//   RMSNorm:   y = x / sqrt(mean(x^2) + eps) * g           (input_layernorm for LLaMA)
+//   LayerNorm: y = (x - mean) / sqrt(var + eps) * g + b     (biased variance, two passes)
+// OUT8: write E4M3 codes of y * (*q_scale) to y8 instead of bf16 y, and fold max |y| of the row
+// into *amax (one atomic per CTA).
 // (cos, sin) of s * theta_i.  The angle is formed and reduced modulo 2*pi in double precision, so
 // the single-precision sine/cosine act on an argument in [-pi, pi].
 __device__ __forceinline__ float2 rope_entry(int s, double theta_i) {
@@ -47,98 +51,84 @@ __device__ __forceinline__ float2 rope_entry(int s, double theta_i) {
   return make_float2(cs, sn);
 }
 
-// Rows r = blockIdx.x, blockIdx.x + gridDim.x, ...; thread i holds VPT 16-byte vectors (8 bf16
-// each) of a row in registers and loads those of the CTA's next row before it reduces the current
-// one, so each CTA keeps a row's loads in flight while it computes; statistics in fp32.
-//   RMSNorm:   y = x / sqrt(mean(x^2) + eps) * g           (input_layernorm for LLaMA)
-//   LayerNorm: y = (x - mean) / sqrt(var + eps) * g + b     (biased variance, two passes)
-// OUT8: write E4M3 codes of y * (*q_scale) to y8 instead of bf16 y, and fold max |y| of the CTA's
-// rows into *amax (one atomic per CTA).
-// rope.tab != null: with row r the CTA also writes row rope.row0 + r of the RoPE table (when below
+// rope.tab != null: the CTA of row r also writes row rope.row0 + r of the RoPE table (when below
 // rope.rows), so the table needs no launch of its own.
 template <int VPT, bool LN, bool OUT8>
 __global__ void __launch_bounds__(1024) norm_kernel(const bf16* __restrict__ x, const bf16* __restrict__ gamma,
-                                                    const bf16* __restrict__ beta, bf16* __restrict__ y, int rows,
-                                                    int H, float eps, uint8_t* __restrict__ y8,
-                                                    const float* q_scale, unsigned* amax, const RopeRows rope) {
+                                                    const bf16* __restrict__ beta, bf16* __restrict__ y, int H,
+                                                    float eps, uint8_t* __restrict__ y8, const float* q_scale,
+                                                    unsigned* amax, const RopeRows rope) {
   __shared__ float red[32];
   pdl_wait();
   pdl_trigger();
+  if (rope.tab != nullptr) {
+    const int s = rope.row0 + static_cast<int>(blockIdx.x);
+    if (s < rope.rows)
+      for (int i = threadIdx.x; i < rope.half; i += blockDim.x)
+        rope.tab[static_cast<size_t>(s) * rope.half + i] = rope_entry(s, rope.theta[i]);
+  }
+  const size_t row = blockIdx.x;
   const int nvec = H >> 3;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + row * H);
+  uint4 raw[VPT];
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int idx = i * blockDim.x + threadIdx.x;
+    raw[i] = idx < nvec ? ld_stream(xr + idx) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    float f[8];
+    unpack_bf16x8(raw[i], f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc += LN ? f[e] : f[e] * f[e];
+  }
+  acc = block_sum(acc, red);
   const float inv_h = 1.0f / static_cast<float>(H);
+  float mean = 0.f, rstd;
+  if (LN) {
+    mean = acc * inv_h;
+    float sq = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      if (i * static_cast<int>(blockDim.x) + static_cast<int>(threadIdx.x) < nvec) {
+        float f[8];
+        unpack_bf16x8(raw[i], f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float dd = f[e] - mean;
+          sq += dd * dd;
+        }
+      }
+    }
+    sq = block_sum(sq, red);
+    rstd = rsqrtf(sq * inv_h + eps);
+  } else {
+    rstd = rsqrtf(acc * inv_h + eps);
+  }
   const uint4* gr = reinterpret_cast<const uint4*>(gamma);
   const uint4* br = reinterpret_cast<const uint4*>(beta);
   const float qs = OUT8 ? __ldg(q_scale) : 1.f;
   float mx = 0.f;
-  auto load_row = [&](int row, uint4* raw) {
-    const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(row) * H);
 #pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      const int idx = i * blockDim.x + threadIdx.x;
-      raw[i] = idx < nvec ? ld_stream(xr + idx) : make_uint4(0u, 0u, 0u, 0u);
-    }
-  };
-  uint4 raw[VPT], nxt[VPT];
-  if (static_cast<int>(blockIdx.x) < rows) load_row(blockIdx.x, raw);
-  for (int row = blockIdx.x; row < rows; row += gridDim.x) {
-    if (row + static_cast<int>(gridDim.x) < rows) load_row(row + gridDim.x, nxt);
-    if (rope.tab != nullptr) {
-      const int s = rope.row0 + row;
-      if (s < rope.rows)
-        for (int i = threadIdx.x; i < rope.half; i += blockDim.x)
-          rope.tab[static_cast<size_t>(s) * rope.half + i] = rope_entry(s, rope.theta[i]);
-    }
-    float acc = 0.f;
-#pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      float f[8];
+  for (int i = 0; i < VPT; ++i) {
+    const int idx = i * blockDim.x + threadIdx.x;
+    if (idx < nvec) {
+      float f[8], gf[8], bfv[8], o[8];
       unpack_bf16x8(raw[i], f);
+      unpack_bf16x8(__ldg(gr + idx), gf);
+      if (LN) unpack_bf16x8(__ldg(br + idx), bfv);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc += LN ? f[e] : f[e] * f[e];
-    }
-    acc = block_sum(acc, red);
-    float mean = 0.f, rstd;
-    if (LN) {
-      mean = acc * inv_h;
-      float sq = 0.f;
+      for (int e = 0; e < 8; ++e) o[e] = (f[e] - mean) * rstd * gf[e] + (LN ? bfv[e] : 0.f);
+      if (OUT8) {
 #pragma unroll
-      for (int i = 0; i < VPT; ++i) {
-        if (i * static_cast<int>(blockDim.x) + static_cast<int>(threadIdx.x) < nvec) {
-          float f[8];
-          unpack_bf16x8(raw[i], f);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float dd = f[e] - mean;
-            sq += dd * dd;
-          }
-        }
-      }
-      sq = block_sum(sq, red);
-      rstd = rsqrtf(sq * inv_h + eps);
-    } else {
-      rstd = rsqrtf(acc * inv_h + eps);
-    }
-#pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      const int idx = i * blockDim.x + threadIdx.x;
-      if (idx < nvec) {
-        float f[8], gf[8], bfv[8], o[8];
-        unpack_bf16x8(raw[i], f);
-        unpack_bf16x8(__ldg(gr + idx), gf);
-        if (LN) unpack_bf16x8(__ldg(br + idx), bfv);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = (f[e] - mean) * rstd * gf[e] + (LN ? bfv[e] : 0.f);
-        if (OUT8) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) mx = fmaxf(mx, fabsf(o[e]));
-          reinterpret_cast<uint2*>(y8 + static_cast<size_t>(row) * H)[idx] = pack_e4m3x8(o, qs);
-        } else {
-          reinterpret_cast<uint4*>(y + static_cast<size_t>(row) * H)[idx] = pack_bf16x8(o);
-        }
+        for (int e = 0; e < 8; ++e) mx = fmaxf(mx, fabsf(o[e]));
+        reinterpret_cast<uint2*>(y8 + row * H)[idx] = pack_e4m3x8(o, qs);
+      } else {
+        reinterpret_cast<uint4*>(y + row * H)[idx] = pack_bf16x8(o);
       }
     }
-#pragma unroll
-    for (int i = 0; i < VPT; ++i) raw[i] = nxt[i];
   }
   if (OUT8) {
     mx = warp_max(mx);
@@ -152,9 +142,6 @@ __global__ void __launch_bounds__(1024) norm_kernel(const bf16* __restrict__ x, 
   }
 }
 
-// CTAs of the norm: as many as fit on the GPU at once (2048 threads per SM), at most one per row.
-int norm_grid(int rows, int threads) { return std::max(1, std::min(rows, num_sms() * (2048 / threads))); }
-
 template <bool LN, bool OUT8>
 cudaError_t launch_norm_ln(const bf16* x, const bf16* g, const bf16* b, bf16* y, int rows, int H, float eps,
                            uint8_t* y8, const float* q_scale, unsigned* amax, const RopeRows& rope,
@@ -163,12 +150,10 @@ cudaError_t launch_norm_ln(const bf16* x, const bf16* g, const bf16* b, bf16* y,
   if (nvec >= 256) {  // two vectors per thread
     const int threads = ((nvec + 1) / 2 + 31) / 32 * 32;
     if (threads > 1024) return cudaErrorInvalidValue;
-    return launch_pdl(norm_kernel<2, LN, OUT8>, dim3(norm_grid(rows, threads)), dim3(threads), 0, stream, x, g, b, y,
-                      rows, H, eps, y8, q_scale, amax, rope);
+    return launch_pdl(norm_kernel<2, LN, OUT8>, dim3(rows), dim3(threads), 0, stream, x, g, b, y, H, eps, y8, q_scale, amax, rope);
   } else {
     const int threads = (nvec + 31) / 32 * 32;
-    return launch_pdl(norm_kernel<1, LN, OUT8>, dim3(norm_grid(rows, threads)), dim3(threads), 0, stream, x, g, b, y,
-                      rows, H, eps, y8, q_scale, amax, rope);
+    return launch_pdl(norm_kernel<1, LN, OUT8>, dim3(rows), dim3(threads), 0, stream, x, g, b, y, H, eps, y8, q_scale, amax, rope);
   }
 }
 
