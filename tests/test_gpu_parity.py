@@ -240,6 +240,32 @@ def test_deterministic_and_host_path_matches():
             assert torch.equal(y1.cpu(), yh), (x_pinned, y_pinned)
 
 
+@pytest.mark.parametrize("cfg", [small(), synth.CONFIGS["llama8b"]], ids=["small", "llama8b"])
+def test_forward_replays_from_a_cuda_graph(cfg):
+    """The forward is stream-ordered (programmatic-dependent launches, no host synchronisation), so a
+    CUDA graph captured from it replays it: the output equals the eager forward bit for bit."""
+    inp = synth.make_inputs(cfg, seed=8, affine="random")
+    dl = DeviceLayer(cfg, inp)
+    x = to_dev(inp["x"]).reshape(cfg.tokens, cfg.hidden)
+    want = dl.forward(x).clone()  # eager first: kernel attributes and workspace are set up here
+    y = torch.full_like(want, float("nan"))
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        dl.layer.forward(x, cfg.seq, cfg.batch, dl.w, y)  # one run on the capture stream before capturing
+        with torch.cuda.graph(graph, stream=side):
+            dl.layer.forward(x, cfg.seq, cfg.batch, dl.w, y)
+    torch.cuda.current_stream().wait_stream(side)
+    y.fill_(float("nan"))
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    dl.layer.status()
+    assert torch.equal(want, y)
+    dl.close()
+
+
 @pytest.mark.parametrize("cfg", [small(batch=2, seq=320), small(seq=700, heads=4, groups=1, head_dim=128),
                                  small(batch=2, seq=4096)],
                          ids=["640-tokens-gqa", "700-tokens-mqa-d128", "8192-tokens-four-chunks"])
