@@ -263,6 +263,16 @@ int mt_gemm_bf16_t(const void* A, int a_layout, const void* B, int b_layout, voi
  * order.  A tuning and testing control; returns MT_ERR_INVALID_ARG for other values. */
 int mt_gemm_set_pairing(int mode);
 
+/* How the CTA-pair GEMM cuts the tiles of its last, partial wave, for every later launch in the
+ * process: 0 automatic (the default): the GEMMs of a layer handle cut each tail tile into 2 to 4
+ * ranges of K when the tail still fits in one wave of SM pairs and each range drops at least 16 K
+ * blocks; the range holding the first K blocks waits (bounded) for the others' fp32 partial sums,
+ * adds them in K order and runs the epilogue; elsewhere (and for the handle-less mt_gemm_* calls)
+ * the tail tiles are cut into 2 or 4 pieces along N.  1: along N only.  The K ranges change the
+ * fp32 summation order of the tail tiles (the results stay deterministic).  A tuning and testing
+ * control; returns MT_ERR_INVALID_ARG for other values. */
+int mt_gemm_set_tail_split(int mode);
+
 /* Sequence-parallel epilogue of a row-parallel linear, for one rank's sequence slice
  * ("Megatron-LM 深度学习与源码分析文档" Part 2 §4 Sequence Parallel: after a RowParallel linear the
  * output is reduce-scattered back to sequence-sharded activations, and LayerNorm/dropout/residual

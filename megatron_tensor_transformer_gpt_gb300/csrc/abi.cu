@@ -17,6 +17,10 @@
 
 using mt::bf16;
 
+// K-split tails of the CTA-pair GEMM: at most kKsTiles tail tiles and kKsSlots partial sums of
+// 256 x 256 fp32 per launch (a tail of r tiles cut into s K ranges stores r (s - 1) of them).
+constexpr int kKsSlots = 64, kKsTiles = 64;
+
 struct mt_layer {
   int hidden, heads, groups, head_dim, ffn, norm, act, tp, rank;
   float rope_base, eps;
@@ -42,6 +46,10 @@ struct mt_layer {
   // host-buffer forward: a copy stream and its events (created on first use)
   cudaStream_t copy_stream;
   cudaEvent_t copy_ev[9];
+  // K-split tails of the CTA-pair GEMM: partial sums (kKsSlots slots of 256 x 256 fp32) and
+  // arrival counters (kept at zero between launches)
+  float4* d_kws;
+  int* d_kflags;
 };
 
 namespace {
@@ -273,6 +281,10 @@ mt::GemmParams gemm_params(int M, int N, int K, bool swiglu, int* err) {
 // Which GEMM kernel runs (mt_gemm_set_pairing): 0 automatic, 1 one CTA per tile always,
 // 2 CTA pairs wherever M > 128.
 std::atomic<int> g_pairing{0};
+// How the last partial wave of a CTA-pair GEMM is cut (mt_gemm_set_tail_split): 0 automatic
+// (along K where a handle provides the partial-sum space and K is long enough, else along N),
+// 1 along N only.
+std::atomic<int> g_tail{0};
 
 // Kernel, tile order and tail split of one GEMM (see GemmParams).
 //   Kernel: CTA pairs (256 x 256 tiles) when M > 128 and there is at least one full wave of them
@@ -280,10 +292,13 @@ std::atomic<int> g_pairing{0};
 //   Order: if one operand fits in about 56 MB of the 129 MB L2 it is kept resident (the other is
 //   streamed once); otherwise bands of m-tiles (or n-tiles) of about 56 MB, whichever streams
 //   fewer bytes from DRAM.
-//   Split: the tiles of the last partial wave are cut into 2 or 4 pieces along N when the pieces
-//   still fit in one wave (QKV pieces keep whole heads; a CTA stages at least 64 B rows, the
-//   smallest TMA box used).
-void plan_gemm(mt::GemmParams& p, int mode, int head_dim) {
+//   Split: the tiles of the last partial wave are cut into pieces that still fit in one wave.  CTA
+//   pairs with a handle: into 2 to 4 ranges of K, when each range drops at least 16 K blocks (a
+//   unit's main loop runs at about the same rate per K block whatever its width, so only shorter
+//   K shortens the tail; the partial sums cost one fp32 write and read of the tile per extra
+//   range).  Otherwise into 2 or 4 pieces along N (QKV pieces keep whole heads; a CTA stages at
+//   least 64 B rows, the smallest TMA box used).
+void plan_gemm(mt::GemmParams& p, int mode, int head_dim, const mt_layer* L, bool fp8) {
   const int sms = mt::num_sms();
   const int tiles_m2 = (p.M + 255) / 256;
   const int mode_pairs = g_pairing.load();
@@ -320,13 +335,27 @@ void plan_gemm(mt::GemmParams& p, int mode, int head_dim) {
   if (mode == mt::kEpiSwiglu) max_split = 2;
   if (mode == mt::kEpiQkv) max_split = std::min(max_split, std::max(1, 256 / head_dim));
   p.split = 1;
-  for (int s = max_split; s >= 2; s /= 2)
-    if (rest > 0 && rest * s <= workers) {
-      p.split = s;
-      break;
-    }
-  p.full_units = p.split > 1 ? waves * workers : p.num_tiles;
-  p.num_units = p.full_units + (p.split > 1 ? rest * p.split : 0);
+  p.ksplit = 1;
+  p.kws = nullptr;
+  p.kflags = nullptr;
+  const int num_kb = (p.K + (fp8 ? 127 : 63)) / (fp8 ? 128 : 64);
+  if (p.pair && L != nullptr && L->d_kws != nullptr && g_tail.load() == 0 && rest > 0)
+    for (int s = 4; s >= 2; --s)
+      if (rest * s <= workers && rest * (s - 1) <= kKsSlots && rest <= kKsTiles && num_kb - num_kb / s >= 16) {
+        p.ksplit = s;
+        p.kws = L->d_kws;
+        p.kflags = L->d_kflags;
+        break;
+      }
+  if (p.ksplit == 1)
+    for (int s = max_split; s >= 2; s /= 2)
+      if (rest > 0 && rest * s <= workers) {
+        p.split = s;
+        break;
+      }
+  const int pieces = p.ksplit > 1 ? p.ksplit : p.split;
+  p.full_units = pieces > 1 ? waves * workers : p.num_tiles;
+  p.num_units = p.full_units + (pieces > 1 ? rest * pieces : 0);
   // two epilogue warps per quadrant where the epilogue would pace the GEMM: a short main loop per
   // tile (K <= 2048) or at most one tile per CTA; one elsewhere (measured faster for long K)
   p.epi_split = (p.K <= 2048 || p.num_units <= workers) ? 2 : 1;
@@ -344,7 +373,7 @@ int run_gemm(mt_layer* L, int slot, int mode, const void* A, int lda, const void
   if (rc) return rc;
   rc = mk(&tb64, W, K, rows_w, K, 64);
   if (rc) return rc;
-  plan_gemm(p, mode, mode == mt::kEpiQkv ? p.head_dim : 0);
+  plan_gemm(p, mode, mode == mt::kEpiQkv ? p.head_dim : 0, L, fp8);
   cudaError_t e;
   {
     Timed t(L, slot, st);
@@ -683,7 +712,7 @@ int gemm_ab(mt_layer* L, const void* A, size_t lda, bool a_mn, const void* Bm, s
   p.ldo = static_cast<int>(ldo);
   p.a_mn = a_mn ? 1 : 0;
   p.b_mn = b_mn ? 1 : 0;
-  plan_gemm(p, mt::kEpiStore, 0);
+  plan_gemm(p, mt::kEpiStore, 0, L, false);
   count_launch(L);
   cudaError_t e = mt::launch_gemm(mt::kEpiStore, false, ta, tb, tb64, p, st);
   return e == cudaSuccess ? MT_OK : cuda_fail(e, "GEMM launch");
@@ -953,6 +982,9 @@ int mt_layer_create(int hidden, int heads, int query_groups, int head_dim, int f
   L->device = dev;
   e = cudaMalloc(&L->d_err, sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(L->d_err, 0, sizeof(int));
+  if (e == cudaSuccess) e = cudaMalloc(&L->d_kws, static_cast<size_t>(kKsSlots) * 256 * 256 * sizeof(float));
+  if (e == cudaSuccess) e = cudaMalloc(&L->d_kflags, kKsTiles * 16 * sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(L->d_kflags, 0, kKsTiles * 16 * sizeof(int));
   if (e == cudaSuccess && rope_base > 0.f) {
     const int half = head_dim / 2;
     double theta[64];
@@ -1131,6 +1163,8 @@ int mt_layer_status(mt_layer* L) {
   int code = 0;
   e = cudaMemcpy(&code, L->d_err, sizeof(int), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  // a launch that gave up may have left K-split arrivals counted: start the next one from zero
+  if (code != 0) cudaMemset(L->d_kflags, 0, kKsTiles * 16 * sizeof(int));
   if (code == MT_ERR_INVALID_ARG) {
     cudaMemset(L->d_err, 0, sizeof(int));
     return fail(MT_ERR_INVALID_ARG, "cu_seqlens were found inconsistent on the device (not 0 .. total_tokens, "
@@ -1151,6 +1185,8 @@ void mt_layer_destroy(mt_layer* L) {
   if (L->d_err) cudaFree(L->d_err);
   if (L->d_theta) cudaFree(L->d_theta);
   if (L->d_f8) cudaFree(L->d_f8);
+  if (L->d_kws) cudaFree(L->d_kws);
+  if (L->d_kflags) cudaFree(L->d_kflags);
   for (auto& r : L->recs) {
     cudaEventDestroy(r.a);
     cudaEventDestroy(r.b);
@@ -1199,6 +1235,12 @@ int mt_layer_profile_read(mt_layer* L, int* launches, double* total_ms) {
 int mt_gemm_set_pairing(int mode) {
   if (mode < 0 || mode > 2) return fail(MT_ERR_INVALID_ARG, "pairing mode must be 0, 1 or 2 (got %d)", mode);
   g_pairing.store(mode);
+  return ok();
+}
+
+int mt_gemm_set_tail_split(int mode) {
+  if (mode < 0 || mode > 1) return fail(MT_ERR_INVALID_ARG, "tail split mode must be 0 or 1 (got %d)", mode);
+  g_tail.store(mode);
   return ok();
 }
 

@@ -58,15 +58,27 @@ __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 // One work unit: tile (tm, tn) of the raster, piece `sub` of `split` along N.
 struct Unit {
   int tm, tn, sub, split;
+  int kpart, ks, tail;  // K range kpart of ks (ks = 1: all of K); tail: the tile's index in the tail wave
 };
 
 __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u) {
   Unit w;
   int tile;
+  w.kpart = 0;
+  w.ks = 1;
+  w.tail = 0;
   if (u < p.full_units) {
     tile = u;
     w.sub = 0;
     w.split = 1;
+  } else if (p.ksplit > 1) {
+    const int v = u - p.full_units;
+    w.tail = v / p.ksplit;
+    tile = p.full_units + w.tail;
+    w.sub = 0;
+    w.split = 1;
+    w.kpart = v - w.tail * p.ksplit;
+    w.ks = p.ksplit;
   } else {
     const int v = u - p.full_units;
     tile = p.full_units + v / p.split;
@@ -100,6 +112,45 @@ __device__ __forceinline__ int unit_col0(const Unit& w) {
   return w.tn * (MODE == kEpiSwiglu ? 128 : BN) + w.sub * unit_width<MODE>(w);
 }
 
+// K blocks [unit_kb0, unit_kb1) of a unit: all of them, or K range kpart of ks (balanced).
+__device__ __forceinline__ int unit_kb0(const Unit& w, int num_kb) { return w.kpart * num_kb / w.ks; }
+__device__ __forceinline__ int unit_kb1(const Unit& w, int num_kb) { return (w.kpart + 1) * num_kb / w.ks; }
+
+// K-split partial sums of one epilogue warp (its 32 rows of one CTA): `parts` slots of 8 chunks
+// of 32 accumulator columns, each chunk stored as [8][lane 32] float4 so that a warp's store or
+// load of 512 B is contiguous.
+constexpr int kKsWarpF4 = 8 * 256;           // float4 per warp and slot
+constexpr int kKsSlotF4 = 2 * 4 * kKsWarpF4;  // float4 per slot (two CTAs, four quadrants)
+struct KFold {
+  const float4* base;  // this lane's float4 of chunk 0 in the first slot
+  int parts;           // 0: nothing to add
+};
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* a) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_gpu_add(int* a, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+
+// 32 accumulator columns starting at `col` of this warp's lanes, plus the K-split partials.
+__device__ __forceinline__ void acc_ld32(uint32_t tacc, int col, float* v, const KFold& kf) {
+  tmem_ld32(tacc + col, v);
+  for (int q = 0; q < kf.parts; ++q) {
+    const float4* src = kf.base + static_cast<size_t>(q) * kKsSlotF4 + (col >> 5) * 256;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      const float4 t = __ldcg(src + 32 * g);
+      v[4 * g] += t.x;
+      v[4 * g + 1] += t.y;
+      v[4 * g + 2] += t.z;
+      v[4 * g + 3] += t.w;
+    }
+  }
+}
+
 __device__ __forceinline__ void scale32(float* v, float f) {
 #pragma unroll
   for (int e = 0; e < 32; ++e) v[e] *= f;
@@ -114,7 +165,7 @@ __device__ __forceinline__ void store_e4m3x32(uint8_t* dst_row, int col, int lim
 
 template <int MODE, bool F8>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc, int m0, int c0, int width,
-                                              int r_in_tile, int lo, int hi) {
+                                              int r_in_tile, int lo, int hi, const KFold& kf) {
   const int row = m0 + r_in_tile;
   const bool valid = row < p.M;
   const float deq = F8 ? __ldg(p.deq_a) * __ldg(p.deq_b) : 1.f;
@@ -127,7 +178,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
       const int col = c0 + c;
       if (col >= p.N) break;  // uniform across the warp
       float v[32];
-      tmem_ld32(tacc + c, v);
+      acc_ld32(tacc, c, v, kf);
       if (valid) {
         if (F8) scale32(v, deq);
         if (p.bias != nullptr) add_vec32(v, p.bias, col, p.N);
@@ -168,8 +219,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
       const int col = c0 + c;
       if (col >= p.N) break;
       float g[32], u[32];
-      tmem_ld32(tacc + c, g);
-      tmem_ld32(tacc + width + c, u);  // the up half follows the `width` gate columns
+      acc_ld32(tacc, c, g, kf);
+      acc_ld32(tacc, width + c, u, kf);  // the up half follows the `width` gate columns
       if (valid) {
         if (F8) {
           scale32(g, deq);
@@ -218,8 +269,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
 #pragma unroll 1
         for (int i0 = 0; i0 < half; i0 += 32) {
           float x1[32], x2[32];
-          tmem_ld32(tacc + hc + i0, x1);
-          tmem_ld32(tacc + hc + half + i0, x2);
+          acc_ld32(tacc, hc + i0, x1, kf);
+          acc_ld32(tacc, hc + half + i0, x2, kf);
           if (valid) {
             if (F8) {
               scale32(x1, deq);
@@ -247,7 +298,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
 #pragma unroll 1
         for (int i0 = 0; i0 < d; i0 += 32) {
           float x[32];
-          tmem_ld32(tacc + hc + i0, x);
+          acc_ld32(tacc, hc + i0, x, kf);
           if (valid) {
             if (F8) scale32(x, deq);
             if (p.bias != nullptr) add_vec32(x, p.bias, col + i0, p.N);
@@ -451,7 +502,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       int lo, hi;
       epilogue_part<MODE>(p, unit_width<MODE>(w), part, lo, hi);
       if (lo < hi)
-        epilogue_tile<MODE, F8>(p, tacc, w.tm * BM, unit_col0<MODE>(w), unit_width<MODE>(w), quad * 32 + lane, lo, hi);
+        epilogue_tile<MODE, F8>(p, tacc, w.tm * BM, unit_col0<MODE>(w), unit_width<MODE>(w), quad * 32 + lane, lo, hi,
+                                KFold{nullptr, 0});
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty(acc));
@@ -463,6 +515,51 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
   }
+}
+
+// K-split tail, a unit with kpart > 0: this warp's columns of the partial sum (the columns its
+// epilogue part would store) go to slot kpart - 1, then one arrival on the tile's counter.
+template <int MODE>
+__device__ __forceinline__ void kpart_store(const GemmParams& p, const Unit& w, uint32_t tacc, int c0, int width,
+                                            int rank, int quad, int part, int lo, int hi) {
+  const int lane = threadIdx.x & 31;
+  float4* dst = p.kws + (static_cast<size_t>(w.tail * (w.ks - 1) + w.kpart - 1) * 8 + rank * 4 + quad) * kKsWarpF4 + lane;
+  const int halves = MODE == kEpiSwiglu ? 2 : 1;  // SwiGLU: gate columns, then the up columns `width` later
+#pragma unroll 1
+  for (int c = lo; c < hi; c += 32) {
+    if (c0 + c >= p.N) break;  // uniform across the warp; the storing unit stops at the same column
+    for (int h = 0; h < halves; ++h) {
+      const int col = c + h * width;
+      float v[32];
+      tmem_ld32(tacc + col, v);
+#pragma unroll
+      for (int g = 0; g < 8; ++g)
+        __stcg(dst + (col >> 5) * 256 + 32 * g, make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]));
+    }
+  }
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) red_release_gpu_add(p.kflags + ((w.tail * 2 + rank) * 4 + quad) * 2 + part, 1);
+}
+
+// K-split tail, the unit with kpart 0: waits (bounded) until the other ks - 1 units have stored
+// this warp's partials; returns the fold to add, or no fold (and the error word set) on timeout.
+__device__ __forceinline__ KFold kpart_wait(const GemmParams& p, const Unit& w, int rank, int quad, int part) {
+  const int lane = threadIdx.x & 31;
+  const int* flag = p.kflags + ((w.tail * 2 + rank) * 4 + quad) * 2 + part;
+  bool ok = ld_acquire_gpu(flag) >= w.ks - 1;
+  if (!ok) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!(ok = ld_acquire_gpu(flag) >= w.ks - 1)) {
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        atomicCAS(p.err, 0, kErrTimeout);
+        break;
+      }
+    }
+  }
+  if (!__all_sync(0xffffffffu, ok)) return KFold{nullptr, 0};
+  const float4* base = p.kws + (static_cast<size_t>(w.tail * (w.ks - 1)) * 8 + rank * 4 + quad) * kKsWarpF4 + lane;
+  return KFold{base, w.ks - 1};
 }
 
 // ------------------------------------------------------------------ CTA-pair kernel
@@ -549,7 +646,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         const int b_row0 = MODE == kEpiSwiglu ? c0 + (rank ? p.b_row_step : 0) : c0 + static_cast<int>(rank) * b_rows;
         const CUtensorMap* mb = b_rows == 128 ? &tmB : &tmB64;
         const uint32_t pair_bytes = 2u * (A_BYTES + b_rows * 128);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        const int kb1 = unit_kb1(w, num_kb);
+        for (int kb = unit_kb0(w, num_kb); kb < kb1; ++kb) {
           if (!mbar_wait(empty(stage), phase ^ 1u, p.err, abort_flag)) {
             ok = false;
             break;
@@ -600,7 +698,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        const int kb0 = unit_kb0(w, num_kb), kb1 = unit_kb1(w, num_kb);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(full(stage), phase, p.err, abort_flag)) {
             ok = false;
             break;
@@ -613,9 +712,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
             if (F8)
-              mma_e4m3_pair(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb | k) ? 1u : 0u);
+              mma_e4m3_pair(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb != kb0 || k) ? 1u : 0u);
             else
-              mma_bf16_pair(d_tmem, ad + astep * k, bd + bstep * k, idesc, (kb | k) ? 1u : 0u);
+              mma_bf16_pair(d_tmem, ad + astep * k, bd + bstep * k, idesc, (kb != kb0 || k) ? 1u : 0u);
           mma_commit_pair(empty(stage));
           if (++stage == P_STAGES) {
             stage = 0;
@@ -642,9 +741,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
       int lo, hi;
       epilogue_part<MODE>(p, unit_width<MODE>(w), part, lo, hi);
-      if (lo < hi)
-        epilogue_tile<MODE, F8>(p, tacc, w.tm * (2 * BM) + static_cast<int>(rank) * BM, unit_col0<MODE>(w),
-                                unit_width<MODE>(w), quad * 32 + lane, lo, hi);
+      if (w.kpart > 0) {
+        kpart_store<MODE>(p, w, tacc, unit_col0<MODE>(w), unit_width<MODE>(w), static_cast<int>(rank), quad, part, lo,
+                          hi);
+      } else {
+        const KFold kf = w.ks > 1 ? kpart_wait(p, w, static_cast<int>(rank), quad, part) : KFold{nullptr, 0};
+        if (lo < hi)
+          epilogue_tile<MODE, F8>(p, tacc, w.tm * (2 * BM) + static_cast<int>(rank) * BM, unit_col0<MODE>(w),
+                                  unit_width<MODE>(w), quad * 32 + lane, lo, hi, kf);
+        __syncwarp();
+        if (w.ks > 1 && lane == 0)  // every partial of this launch has arrived and been read
+          p.kflags[((w.tail * 2 + static_cast<int>(rank)) * 4 + quad) * 2 + part] = 0;
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty(acc), 0));
@@ -672,6 +780,8 @@ cudaError_t launch_mode(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
     if (e != cudaSuccess) return e;
     configured = true;
   }
+  if (!p.pair && p.ksplit > 1) return cudaErrorInvalidValue;  // K ranges only in the pair kernel
+  if (p.ksplit > 1 && (p.kws == nullptr || p.kflags == nullptr || p.err == nullptr)) return cudaErrorInvalidValue;
   if (p.pair) {
     const int pairs = gemm_pair_slots();
     const int grid = 2 * (p.num_units < pairs ? p.num_units : pairs);

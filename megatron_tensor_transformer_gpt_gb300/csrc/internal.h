@@ -29,8 +29,16 @@ struct GemmParams {
   // inside a band) or `band` n-tiles (band_m = 0, n fastest), so a band's operand stays in L2.
   int band, band_m;
   // Work units: [0, full_units) are whole tiles; the tiles after them (the last, partial wave)
-  // are cut into `split` pieces along N so that the tail wave is shorter.  num_units in total.
+  // are cut into `split` pieces along N, or (CTA pairs with a K-split workspace) into `ksplit`
+  // ranges of K, so that the tail wave is shorter.  num_units in total.
   int full_units, split, num_units;
+  // K-split tail (pair kernel): the unit holding K range 0 of a tail tile stores the tile; the
+  // others write fp32 partial sums to kws and count them on kflags, which that unit waits for,
+  // adds in K order and resets to zero.  kws: [tail tile][ksplit - 1][CTA 2][quadrant 4]
+  // [32-column chunk 8][8][lane 32] float4; kflags: [tail tile][CTA 2][quadrant 4][epilogue part 2].
+  int ksplit;
+  float4* kws;
+  int* kflags;
   // CTA pairs (pair = 1): tiles are 256 x 256 and computed by a cluster of two CTAs sharing one
   // M = 256 MMA (tiles_m counts 256-row tiles); otherwise one CTA per 128 x 256 tile.
   int pair;

@@ -68,6 +68,7 @@ _SIGS = {
     "mt_last_error": ([], ctypes.c_char_p),
     "mt_layer_destroy": ([ctypes.c_void_p], None),
     "mt_gemm_set_pairing": ([ctypes.c_int], ctypes.c_int),
+    "mt_gemm_set_tail_split": ([ctypes.c_int], ctypes.c_int),
     "mt_gemm_bf16_t": ([ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
                         ctypes.c_int, ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
     "mt_gemm_bf16": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -282,6 +283,10 @@ def mt_gemm_bf16_t(A, a_layout, B, b_layout, C, M, N, K, stream):
 
 def mt_gemm_set_pairing(mode):
     _check(lib().mt_gemm_set_pairing(mode))
+
+
+def mt_gemm_set_tail_split(mode):
+    _check(lib().mt_gemm_set_tail_split(mode))
 
 
 def mt_gemm_bf16(A, B, C, M, N, K, stream):

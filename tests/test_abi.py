@@ -101,6 +101,14 @@ def test_gemm_pairing_mode_is_checked(lib):
         assert lib.mt_gemm_set_pairing(mode) == ml.MT_OK
 
 
+def test_gemm_tail_split_mode_is_checked(lib):
+    assert lib.mt_gemm_set_tail_split(2) == ml.MT_ERR_INVALID_ARG
+    assert lib.mt_gemm_set_tail_split(-1) == ml.MT_ERR_INVALID_ARG
+    assert "tail split" in ml.mt_last_error()
+    for mode in (1, 0):                    # 0 (automatic) is left in place
+        assert lib.mt_gemm_set_tail_split(mode) == ml.MT_OK
+
+
 def test_profile_mask_and_launch_count_check_arguments(lib):
     assert lib.mt_layer_profile_enable(None, 1) == ml.MT_ERR_INVALID_ARG
     assert lib.mt_layer_launch_count(None, None) == ml.MT_ERR_INVALID_ARG
