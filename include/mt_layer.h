@@ -28,8 +28,9 @@
  *   GQA: q head h (within the rank) reads kv group h / (nh_r/ng_r).
  *
  * Ownership.  The caller owns x, the weights, every output and the workspace (all device
- * memory unless stated).  The library owns the handle and a 4-byte device error word,
- * allocated in mt_layer_create and freed in mt_layer_destroy.  Calls that take a stream are
+ * memory unless stated).  The library owns the handle, a 4-byte device error word and 16 MiB
+ * of device memory for the fp32 partial sums of the GEMMs' K-split tail tiles (with 4 KiB of
+ * arrival counters), allocated in mt_layer_create and freed in mt_layer_destroy.  Calls that take a stream are
  * asynchronous on it; a handle must not be used from two host threads at once.
  *
  * Errors.  Every call returns an mt_status; on failure no kernel is launched and
@@ -78,8 +79,9 @@ typedef struct {
  * num_query_groups, kv_channels, ffn_hidden_size).  rope_base == 0 disables RoPE.
  * Supported: head_dim in {64, 128}; heads % query_groups == 0; heads, query_groups and ffn
  * divisible by tp_size; hidden % 8 == 0, hidden <= 8192; (ffn/tp_size) % 8 == 0.
- * Needs the current CUDA device to be sm_103 (GB300).  Host call; allocates 4 bytes of
- * device memory.  Returns MT_ERR_UNSUPPORTED / MT_ERR_INVALID_ARG otherwise. */
+ * Needs the current CUDA device to be sm_103 (GB300).  Host call; allocates about 16 MiB of
+ * device memory (the error word, the RoPE frequencies and the K-split partial sums).  Returns
+ * MT_ERR_UNSUPPORTED / MT_ERR_INVALID_ARG otherwise. */
 int mt_layer_create(int hidden, int heads, int query_groups, int head_dim, int ffn, int norm, int act,
                     float rope_base, int tp_size, int tp_rank, mt_layer** out);
 
@@ -214,7 +216,8 @@ int mt_layer_workspace_region(const mt_layer* L, int seq, int batch, int which, 
 
 /* Synchronise with the work queued by this handle (all streams) and report a device-side
  * failure recorded since the last call (MT_ERR_DEVICE_TIMEOUT, or MT_ERR_INVALID_ARG for
- * inconsistent packed cu_seqlens), clearing it. */
+ * inconsistent packed cu_seqlens), clearing it (and, after a failure, the K-split arrival
+ * counters, which a launch that gave up may have left counted). */
 int mt_layer_status(mt_layer* L);
 
 /* Thread-local description of the last failure on this thread ("" after success). */

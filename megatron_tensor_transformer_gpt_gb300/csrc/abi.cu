@@ -357,8 +357,9 @@ void plan_gemm(mt::GemmParams& p, int mode, int head_dim, const mt_layer* L, boo
   p.full_units = pieces > 1 ? waves * workers : p.num_tiles;
   p.num_units = p.full_units + (pieces > 1 ? rest * pieces : 0);
   // two epilogue warps per quadrant where the epilogue would pace the GEMM: a short main loop per
-  // tile (K <= 2048) or at most one tile per CTA; one elsewhere (measured faster for long K)
-  p.epi_split = (p.K <= 2048 || p.num_units <= workers) ? 2 : 1;
+  // tile (K <= 2048), at most one tile per CTA, or a K-split tail with K <= 4096 (its first range
+  // adds the partial sums before the epilogue); one elsewhere (measured faster for long K)
+  p.epi_split = (p.K <= 2048 || p.num_units <= workers || (p.ksplit > 1 && p.K <= 4096)) ? 2 : 1;
 }
 
 // One GEMM: A [M, K] (pitch lda) x W [rows_w, K]^T with the given epilogue.

@@ -116,15 +116,11 @@ __device__ __forceinline__ int unit_col0(const Unit& w) {
 __device__ __forceinline__ int unit_kb0(const Unit& w, int num_kb) { return w.kpart * num_kb / w.ks; }
 __device__ __forceinline__ int unit_kb1(const Unit& w, int num_kb) { return (w.kpart + 1) * num_kb / w.ks; }
 
-// K-split partial sums of one epilogue warp (its 32 rows of one CTA): `parts` slots of 8 chunks
-// of 32 accumulator columns, each chunk stored as [8][lane 32] float4 so that a warp's store or
-// load of 512 B is contiguous.
+// K-split partial sums of one epilogue warp (its 32 rows of one CTA): one slot per K range after
+// the first, 8 chunks of 32 accumulator columns each, a chunk stored as [8][lane 32] float4 so
+// that a warp's store or load of 512 B is contiguous.
 constexpr int kKsWarpF4 = 8 * 256;           // float4 per warp and slot
 constexpr int kKsSlotF4 = 2 * 4 * kKsWarpF4;  // float4 per slot (two CTAs, four quadrants)
-struct KFold {
-  const float4* base;  // this lane's float4 of chunk 0 in the first slot
-  int parts;           // 0: nothing to add
-};
 
 __device__ __forceinline__ int ld_acquire_gpu(const int* a) {
   int v;
@@ -133,22 +129,6 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* a) {
 }
 __device__ __forceinline__ void red_release_gpu_add(int* a, int v) {
   asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
-}
-
-// 32 accumulator columns starting at `col` of this warp's lanes, plus the K-split partials.
-__device__ __forceinline__ void acc_ld32(uint32_t tacc, int col, float* v, const KFold& kf) {
-  tmem_ld32(tacc + col, v);
-  for (int q = 0; q < kf.parts; ++q) {
-    const float4* src = kf.base + static_cast<size_t>(q) * kKsSlotF4 + (col >> 5) * 256;
-#pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      const float4 t = __ldcg(src + 32 * g);
-      v[4 * g] += t.x;
-      v[4 * g + 1] += t.y;
-      v[4 * g + 2] += t.z;
-      v[4 * g + 3] += t.w;
-    }
-  }
 }
 
 __device__ __forceinline__ void scale32(float* v, float f) {
@@ -165,7 +145,7 @@ __device__ __forceinline__ void store_e4m3x32(uint8_t* dst_row, int col, int lim
 
 template <int MODE, bool F8>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc, int m0, int c0, int width,
-                                              int r_in_tile, int lo, int hi, const KFold& kf) {
+                                              int r_in_tile, int lo, int hi) {
   const int row = m0 + r_in_tile;
   const bool valid = row < p.M;
   const float deq = F8 ? __ldg(p.deq_a) * __ldg(p.deq_b) : 1.f;
@@ -178,7 +158,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
       const int col = c0 + c;
       if (col >= p.N) break;  // uniform across the warp
       float v[32];
-      acc_ld32(tacc, c, v, kf);
+      tmem_ld32(tacc + c, v);
       if (valid) {
         if (F8) scale32(v, deq);
         if (p.bias != nullptr) add_vec32(v, p.bias, col, p.N);
@@ -219,8 +199,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
       const int col = c0 + c;
       if (col >= p.N) break;
       float g[32], u[32];
-      acc_ld32(tacc, c, g, kf);
-      acc_ld32(tacc, width + c, u, kf);  // the up half follows the `width` gate columns
+      tmem_ld32(tacc + c, g);
+      tmem_ld32(tacc + width + c, u);  // the up half follows the `width` gate columns
       if (valid) {
         if (F8) {
           scale32(g, deq);
@@ -269,8 +249,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
 #pragma unroll 1
         for (int i0 = 0; i0 < half; i0 += 32) {
           float x1[32], x2[32];
-          acc_ld32(tacc, hc + i0, x1, kf);
-          acc_ld32(tacc, hc + half + i0, x2, kf);
+          tmem_ld32(tacc + hc + i0, x1);
+          tmem_ld32(tacc + hc + half + i0, x2);
           if (valid) {
             if (F8) {
               scale32(x1, deq);
@@ -298,7 +278,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
 #pragma unroll 1
         for (int i0 = 0; i0 < d; i0 += 32) {
           float x[32];
-          acc_ld32(tacc, hc + i0, x, kf);
+          tmem_ld32(tacc + hc + i0, x);
           if (valid) {
             if (F8) scale32(x, deq);
             if (p.bias != nullptr) add_vec32(x, p.bias, col + i0, p.N);
@@ -502,8 +482,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       int lo, hi;
       epilogue_part<MODE>(p, unit_width<MODE>(w), part, lo, hi);
       if (lo < hi)
-        epilogue_tile<MODE, F8>(p, tacc, w.tm * BM, unit_col0<MODE>(w), unit_width<MODE>(w), quad * 32 + lane, lo, hi,
-                                KFold{nullptr, 0});
+        epilogue_tile<MODE, F8>(p, tacc, w.tm * BM, unit_col0<MODE>(w), unit_width<MODE>(w), quad * 32 + lane, lo, hi);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty(acc));
@@ -519,32 +498,76 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
 // K-split tail, a unit with kpart > 0: this warp's columns of the partial sum (the columns its
 // epilogue part would store) go to slot kpart - 1, then one arrival on the tile's counter.
+// Accumulator columns an epilogue part reads: 32-column chunks c of [lo, hi) with c0 + c < N
+// (SwiGLU: each also the up chunk `width` columns later).  Returns the count; col(i) the i-th.
+template <int MODE>
+struct PartCols {
+  int lo, width, n_gate;
+  __device__ __forceinline__ PartCols(const GemmParams& p, int c0, int width_, int lo_, int hi) : lo(lo_), width(width_) {
+    const int end = min(hi, p.N - c0);
+    n_gate = end > lo ? (end - lo + 31) / 32 : 0;
+  }
+  __device__ __forceinline__ int count() const { return MODE == kEpiSwiglu ? 2 * n_gate : n_gate; }
+  __device__ __forceinline__ int col(int i) const {
+    return MODE == kEpiSwiglu && i >= n_gate ? width + lo + 32 * (i - n_gate) : lo + 32 * i;
+  }
+};
+
 template <int MODE>
 __device__ __forceinline__ void kpart_store(const GemmParams& p, const Unit& w, uint32_t tacc, int c0, int width,
                                             int rank, int quad, int part, int lo, int hi) {
   const int lane = threadIdx.x & 31;
   float4* dst = p.kws + (static_cast<size_t>(w.tail * (w.ks - 1) + w.kpart - 1) * 8 + rank * 4 + quad) * kKsWarpF4 + lane;
-  const int halves = MODE == kEpiSwiglu ? 2 : 1;  // SwiGLU: gate columns, then the up columns `width` later
+  const PartCols<MODE> pc(p, c0, width, lo, hi);
 #pragma unroll 1
-  for (int c = lo; c < hi; c += 32) {
-    if (c0 + c >= p.N) break;  // uniform across the warp; the storing unit stops at the same column
-    for (int h = 0; h < halves; ++h) {
-      const int col = c + h * width;
-      float v[32];
-      tmem_ld32(tacc + col, v);
+  for (int i = 0; i < pc.count(); ++i) {
+    const int col = pc.col(i);
+    float v[32];
+    tmem_ld32(tacc + col, v);
 #pragma unroll
-      for (int g = 0; g < 8; ++g)
-        __stcg(dst + (col >> 5) * 256 + 32 * g, make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]));
-    }
+    for (int g = 0; g < 8; ++g)
+      __stcg(dst + (col >> 5) * 256 + 32 * g, make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]));
   }
   __threadfence();
   __syncwarp();
   if (lane == 0) red_release_gpu_add(p.kflags + ((w.tail * 2 + rank) * 4 + quad) * 2 + part, 1);
 }
 
+// Adds NP (1 or 2) partial slots to this warp's accumulator columns, one 32-column chunk at a
+// time with the chunk's loads of both slots issued before the first add (the partials come from
+// L2, and their latency, not their bytes, paces the fold).
+template <int MODE, int NP>
+__device__ __forceinline__ void fold_chunks(const float4* base, uint32_t tacc, const PartCols<MODE>& pc) {
+#pragma unroll 1
+  for (int i = 0; i < pc.count(); ++i) {
+    const int col = pc.col(i);
+    const float4* src = base + (col >> 5) * 256;
+    float4 t[NP][8];
+#pragma unroll
+    for (int q = 0; q < NP; ++q)
+#pragma unroll
+      for (int g = 0; g < 8; ++g) t[q][g] = __ldcg(src + static_cast<size_t>(q) * kKsSlotF4 + 32 * g);
+    float v[32];
+    tmem_ld32(tacc + col, v);
+#pragma unroll
+    for (int q = 0; q < NP; ++q)
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        v[4 * g] += t[q][g].x;
+        v[4 * g + 1] += t[q][g].y;
+        v[4 * g + 2] += t[q][g].z;
+        v[4 * g + 3] += t[q][g].w;
+      }
+    tmem_st32(tacc + col, v);
+  }
+}
+
 // K-split tail, the unit with kpart 0: waits (bounded) until the other ks - 1 units have stored
-// this warp's partials; returns the fold to add, or no fold (and the error word set) on timeout.
-__device__ __forceinline__ KFold kpart_wait(const GemmParams& p, const Unit& w, int rank, int quad, int part) {
+// this warp's partials and adds them, in K order, to its accumulator columns in TMEM; on timeout
+// sets the error word and leaves the accumulator as it is.
+template <int MODE>
+__device__ __forceinline__ void kpart_fold(const GemmParams& p, const Unit& w, uint32_t tacc, int c0, int width,
+                                           int rank, int quad, int part, int lo, int hi) {
   const int lane = threadIdx.x & 31;
   const int* flag = p.kflags + ((w.tail * 2 + rank) * 4 + quad) * 2 + part;
   bool ok = ld_acquire_gpu(flag) >= w.ks - 1;
@@ -557,9 +580,16 @@ __device__ __forceinline__ KFold kpart_wait(const GemmParams& p, const Unit& w, 
       }
     }
   }
-  if (!__all_sync(0xffffffffu, ok)) return KFold{nullptr, 0};
+  if (!__all_sync(0xffffffffu, ok)) return;
   const float4* base = p.kws + (static_cast<size_t>(w.tail * (w.ks - 1)) * 8 + rank * 4 + quad) * kKsWarpF4 + lane;
-  return KFold{base, w.ks - 1};
+  const PartCols<MODE> pc(p, c0, width, lo, hi);
+  // the partials are added to the fp32 accumulator in K order: ((acc + part 1) + part 2) + part 3
+  if (w.ks == 2) {
+    fold_chunks<MODE, 1>(base, tacc, pc);
+  } else {
+    fold_chunks<MODE, 2>(base, tacc, pc);
+    if (w.ks == 4) fold_chunks<MODE, 1>(base + 2 * kKsSlotF4, tacc, pc);
+  }
 }
 
 // ------------------------------------------------------------------ CTA-pair kernel
@@ -745,10 +775,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         kpart_store<MODE>(p, w, tacc, unit_col0<MODE>(w), unit_width<MODE>(w), static_cast<int>(rank), quad, part, lo,
                           hi);
       } else {
-        const KFold kf = w.ks > 1 ? kpart_wait(p, w, static_cast<int>(rank), quad, part) : KFold{nullptr, 0};
+        if (w.ks > 1)
+          kpart_fold<MODE>(p, w, tacc, unit_col0<MODE>(w), unit_width<MODE>(w), static_cast<int>(rank), quad, part, lo,
+                           hi);
         if (lo < hi)
           epilogue_tile<MODE, F8>(p, tacc, w.tm * (2 * BM) + static_cast<int>(rank) * BM, unit_col0<MODE>(w),
-                                  unit_width<MODE>(w), quad * 32 + lane, lo, hi, kf);
+                                  unit_width<MODE>(w), quad * 32 + lane, lo, hi);
         __syncwarp();
         if (w.ks > 1 && lane == 0)  // every partial of this launch has arrived and been read
           p.kflags[((w.tail * 2 + static_cast<int>(rank)) * 4 + quad) * 2 + part] = 0;
