@@ -276,6 +276,20 @@ int mt_gemm_set_pairing(int mode);
  * control; returns MT_ERR_INVALID_ARG for other values. */
 int mt_gemm_set_tail_split(int mode);
 
+/* How a GEMM launch of this library is planned, computed on the host without any CUDA call (a
+ * testing and tuning aid): C[M, N] with the given epilogue (0 store, 1 residual add, 2 QKV with
+ * RoPE and scatter (head_dim 64 or 128), 3 SwiGLU (N = the gate width), 4 GeLU), E4M3 operands
+ * when fp8 != 0, as a layer handle's GEMMs (with_handle != 0: K ranges allowed for the tail) or
+ * as the handle-less mt_gemm_* calls, on a device with `sms` SMs of which `pair_slots` CTA pairs
+ * can be resident (152 and 76 on GB300), under the current mt_gemm_set_pairing and
+ * mt_gemm_set_tail_split modes.  Writes plan[0..7] = {pair (1: CTA-pair kernel, 256-row tiles),
+ * tiles_m, tiles_n, split (N pieces per tail tile), ksplit (K ranges per tail tile), full_units
+ * (whole tiles before the tail), num_units, epi_split (epilogue warps per TMEM lane quadrant that
+ * store a tile)}.  MT_ERR_INVALID_ARG for a NULL plan, non-positive sizes, another epilogue or
+ * head_dim, or sms < 2, pair_slots outside 1 .. sms / 2. */
+int mt_gemm_plan(int M, int N, int K, int epilogue, int head_dim, int fp8, int with_handle, int sms, int pair_slots,
+                 int* plan);
+
 /* Sequence-parallel epilogue of a row-parallel linear, for one rank's sequence slice
  * ("Megatron-LM 深度学习与源码分析文档" Part 2 §4 Sequence Parallel: after a RowParallel linear the
  * output is reduce-scattered back to sequence-sharded activations, and LayerNorm/dropout/residual

@@ -298,8 +298,9 @@ std::atomic<int> g_tail{0};
 //   K shortens the tail; the partial sums cost one fp32 write and read of the tile per extra
 //   range).  Otherwise into 2 or 4 pieces along N (QKV pieces keep whole heads; a CTA stages at
 //   least 64 B rows, the smallest TMA box used).
-void plan_gemm(mt::GemmParams& p, int mode, int head_dim, const mt_layer* L, bool fp8) {
-  const int sms = mt::num_sms();
+// The planning itself, for a device with `sms` SMs of which `pair_slots` CTA pairs can be resident;
+// ksplit_ok: the GEMM has a handle's partial-sum space (no CUDA call here).
+void plan_gemm_on(mt::GemmParams& p, int mode, int head_dim, bool ksplit_ok, bool fp8, int sms, int pair_slots) {
   const int tiles_m2 = (p.M + 255) / 256;
   const int mode_pairs = g_pairing.load();
   // CTA pairs for every GEMM with more than 128 rows: measured as fast or faster than the one-CTA
@@ -327,7 +328,7 @@ void plan_gemm(mt::GemmParams& p, int mode, int head_dim, const mt_layer* L, boo
     p.band_m = tm <= tn ? 1 : 0;
     p.band = tm <= tn ? std::min(gm, p.tiles_m) : std::min(gn, p.tiles_n);
   }
-  const int workers = p.pair ? mt::gemm_pair_slots() : sms;
+  const int workers = p.pair ? pair_slots : sms;
   const int waves = p.num_tiles / workers;
   const int rest = p.num_tiles - waves * workers;
   // pairs: each CTA stages half of a piece's B rows (SwiGLU: all of its gate or up rows)
@@ -339,12 +340,10 @@ void plan_gemm(mt::GemmParams& p, int mode, int head_dim, const mt_layer* L, boo
   p.kws = nullptr;
   p.kflags = nullptr;
   const int num_kb = (p.K + (fp8 ? 127 : 63)) / (fp8 ? 128 : 64);
-  if (p.pair && L != nullptr && L->d_kws != nullptr && g_tail.load() == 0 && rest > 0)
+  if (p.pair && ksplit_ok && g_tail.load() == 0 && rest > 0)
     for (int s = 4; s >= 2; --s)
       if (rest * s <= workers && rest * (s - 1) <= kKsSlots && rest <= kKsTiles && num_kb - num_kb / s >= 16) {
         p.ksplit = s;
-        p.kws = L->d_kws;
-        p.kflags = L->d_kflags;
         break;
       }
   if (p.ksplit == 1)
@@ -360,6 +359,18 @@ void plan_gemm(mt::GemmParams& p, int mode, int head_dim, const mt_layer* L, boo
   // tile (K <= 2048), at most one tile per CTA, or a K-split tail with K <= 4096 (its first range
   // adds the partial sums before the epilogue); one elsewhere (measured faster for long K)
   p.epi_split = (p.K <= 2048 || p.num_units <= workers || (p.ksplit > 1 && p.K <= 4096)) ? 2 : 1;
+}
+
+void plan_gemm(mt::GemmParams& p, int mode, int head_dim, const mt_layer* L, bool fp8) {
+  const bool ksplit_ok = L != nullptr && L->d_kws != nullptr;
+  const int sms = mt::num_sms();
+  // the resident-pair query only where the pair kernel can be chosen (as the planner decides it)
+  const int pair_slots = (g_pairing.load() != 1 && p.M > 128) ? mt::gemm_pair_slots() : std::max(1, sms / 2);
+  plan_gemm_on(p, mode, head_dim, ksplit_ok, fp8, sms, pair_slots);
+  if (p.ksplit > 1) {
+    p.kws = L->d_kws;
+    p.kflags = L->d_kflags;
+  }
 }
 
 // One GEMM: A [M, K] (pitch lda) x W [rows_w, K]^T with the given epilogue.
@@ -1242,6 +1253,23 @@ int mt_gemm_set_pairing(int mode) {
 int mt_gemm_set_tail_split(int mode) {
   if (mode < 0 || mode > 1) return fail(MT_ERR_INVALID_ARG, "tail split mode must be 0 or 1 (got %d)", mode);
   g_tail.store(mode);
+  return ok();
+}
+
+int mt_gemm_plan(int M, int N, int K, int epilogue, int head_dim, int fp8, int with_handle, int sms, int pair_slots,
+                 int* plan) {
+  if (plan == nullptr) return fail(MT_ERR_INVALID_ARG, "plan is NULL");
+  if (M <= 0 || N <= 0 || K <= 0) return fail(MT_ERR_INVALID_ARG, "M, N, K must be positive");
+  if (epilogue < mt::kEpiStore || epilogue > mt::kEpiGelu)
+    return fail(MT_ERR_INVALID_ARG, "epilogue must be 0 .. 4 (got %d)", epilogue);
+  if (epilogue == mt::kEpiQkv && head_dim != 64 && head_dim != 128)
+    return fail(MT_ERR_INVALID_ARG, "head_dim must be 64 or 128 for the QKV epilogue (got %d)", head_dim);
+  if (sms < 2 || pair_slots < 1 || pair_slots > sms / 2)
+    return fail(MT_ERR_INVALID_ARG, "need sms >= 2 and 1 <= pair_slots <= sms / 2 (got %d, %d)", sms, pair_slots);
+  mt::GemmParams p = gemm_params(M, N, K, epilogue == mt::kEpiSwiglu, nullptr);
+  plan_gemm_on(p, epilogue, epilogue == mt::kEpiQkv ? head_dim : 0, with_handle != 0, fp8 != 0, sms, pair_slots);
+  const int out[8] = {p.pair, p.tiles_m, p.tiles_n, p.split, p.ksplit, p.full_units, p.num_units, p.epi_split};
+  for (int i = 0; i < 8; ++i) plan[i] = out[i];
   return ok();
 }
 

@@ -69,6 +69,7 @@ _SIGS = {
     "mt_layer_destroy": ([ctypes.c_void_p], None),
     "mt_gemm_set_pairing": ([ctypes.c_int], ctypes.c_int),
     "mt_gemm_set_tail_split": ([ctypes.c_int], ctypes.c_int),
+    "mt_gemm_plan": ([ctypes.c_int] * 9 + [ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
     "mt_gemm_bf16_t": ([ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
                         ctypes.c_int, ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
     "mt_gemm_bf16": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -287,6 +288,15 @@ def mt_gemm_set_pairing(mode):
 
 def mt_gemm_set_tail_split(mode):
     _check(lib().mt_gemm_set_tail_split(mode))
+
+
+PLAN_FIELDS = ("pair", "tiles_m", "tiles_n", "split", "ksplit", "full_units", "num_units", "epi_split")
+
+
+def mt_gemm_plan(M, N, K, epilogue, head_dim=0, fp8=False, with_handle=True, sms=152, pair_slots=76):
+    out = (ctypes.c_int * 8)()
+    _check(lib().mt_gemm_plan(M, N, K, epilogue, head_dim, int(fp8), int(with_handle), sms, pair_slots, out))
+    return dict(zip(PLAN_FIELDS, list(out)))
 
 
 def mt_gemm_bf16(A, B, C, M, N, K, stream):

@@ -101,6 +101,93 @@ def test_gemm_pairing_mode_is_checked(lib):
         assert lib.mt_gemm_set_pairing(mode) == ml.MT_OK
 
 
+# Llama-3-8B-shaped layer, 4096 tokens, on 152 SMs / 76 resident CTA pairs (epilogue codes:
+# 0 store, 1 residual, 2 QKV, 3 SwiGLU, 4 GeLU)
+LLAMA8B_GEMMS = {
+    # name: (N, K, epilogue, expected plan)
+    "qkv": (6144, 4096, 2, dict(pair=1, tiles_m=16, tiles_n=24, split=1, ksplit=4, full_units=380,
+                                num_units=396, epi_split=2)),
+    "o": (4096, 4096, 1, dict(pair=1, tiles_m=16, tiles_n=16, split=1, ksplit=2, full_units=228,
+                              num_units=284, epi_split=2)),
+    "fc1": (14336, 4096, 3, dict(pair=1, tiles_m=16, tiles_n=112, split=1, ksplit=1, full_units=1792,
+                                 num_units=1792, epi_split=1)),
+    "fc2": (4096, 14336, 1, dict(pair=1, tiles_m=16, tiles_n=16, split=1, ksplit=2, full_units=228,
+                                 num_units=284, epi_split=1)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(LLAMA8B_GEMMS))
+def test_gemm_plan_llama8b(lib, name):
+    """The tail of each projection as measured: QKV 4 tail tiles in 4 K ranges, the output
+    projection and fc2 28 tail tiles in 2, fc1's 44 left whole (88 pieces exceed 76 pairs)."""
+    N, K, epi, want = LLAMA8B_GEMMS[name]
+    assert ml.mt_gemm_plan(4096, N, K, epi, head_dim=128) == want
+
+
+def test_gemm_plan_tail_forms(lib):
+    o = dict(M=4096, N=4096, K=4096, epilogue=1)
+    # handle-less calls and tail split mode 1 cut the 28 tail tiles into 2 pieces along N
+    for plan in (ml.mt_gemm_plan(**o, with_handle=False), _with_tail_split(1, lambda: ml.mt_gemm_plan(**o))):
+        assert (plan["split"], plan["ksplit"], plan["num_units"]) == (2, 1, 228 + 56)
+        assert plan["epi_split"] == 1
+    # E4M3 operands: 128-deep K blocks, 32 for K = 4096: QKV's 4 tail tiles still take 4 ranges (each
+    # drops 24 blocks), the output projection's 28 take 2
+    f8 = ml.mt_gemm_plan(4096, 6144, 4096, 2, head_dim=128, fp8=True)
+    assert f8["ksplit"] == 4
+    assert ml.mt_gemm_plan(**o, fp8=True)["ksplit"] == 2
+    # K = 1024 (16 K blocks): no range would drop 16 of them, so the N cut (GPT-345M's QKV)
+    gpt = ml.mt_gemm_plan(4096, 3072, 1024, 2, head_dim=64)
+    assert (gpt["ksplit"], gpt["epi_split"]) == (1, 2)
+    # 128 rows or fewer: the one-CTA kernel, 128 x 256 tiles, never K ranges
+    small = ml.mt_gemm_plan(128, 4096, 4096, 0)
+    assert (small["pair"], small["tiles_m"], small["ksplit"]) == (0, 1, 1)
+    # a whole wave and no tail: nothing to cut
+    full = ml.mt_gemm_plan(256 * 76, 256, 4096, 0)
+    assert (full["split"], full["ksplit"], full["num_units"]) == (1, 1, 76)
+
+
+def _with_tail_split(mode, fn):
+    ml.mt_gemm_set_tail_split(mode)
+    try:
+        return fn()
+    finally:
+        ml.mt_gemm_set_tail_split(0)
+
+
+def test_gemm_plan_invariants(lib):
+    """Over a sweep of shapes: the units cover the tiles, a cut tail still fits in one wave, K
+    ranges only where each drops at least 16 K blocks."""
+    for M in (129, 1000, 4096, 8192):
+        for N, epi in ((1024, 0), (4096, 1), (6144, 2), (14336, 3), (8192, 4), (520, 0)):
+            for K in (512, 1024, 2048, 4096, 14336):
+                for handle in (True, False):
+                    p = ml.mt_gemm_plan(M, N, K, epi, head_dim=128, with_handle=handle)
+                    tiles = p["tiles_m"] * p["tiles_n"]
+                    workers = 76 if p["pair"] else 152
+                    rest = tiles - p["full_units"]
+                    pieces = max(p["split"], p["ksplit"])
+                    assert p["split"] == 1 or p["ksplit"] == 1
+                    if pieces == 1:
+                        assert p["full_units"] == p["num_units"] == tiles
+                    else:
+                        assert p["full_units"] % workers == 0 and 0 < rest
+                        assert p["num_units"] == p["full_units"] + rest * pieces and rest * pieces <= workers
+                    if p["ksplit"] > 1:
+                        nkb = (K + 63) // 64
+                        assert handle and p["pair"] and nkb - nkb // p["ksplit"] >= 16
+                    assert p["epi_split"] in (1, 2)
+
+
+def test_gemm_plan_checks_arguments(lib):
+    out = (ctypes.c_int * 8)()
+    assert lib.mt_gemm_plan(0, 1, 1, 0, 0, 0, 1, 152, 76, out) == ml.MT_ERR_INVALID_ARG
+    assert lib.mt_gemm_plan(1, 1, 1, 5, 0, 0, 1, 152, 76, out) == ml.MT_ERR_INVALID_ARG
+    assert lib.mt_gemm_plan(256, 768, 64, 2, 96, 0, 1, 152, 76, out) == ml.MT_ERR_INVALID_ARG
+    assert lib.mt_gemm_plan(256, 256, 64, 0, 0, 0, 1, 152, 77, out) == ml.MT_ERR_INVALID_ARG
+    assert lib.mt_gemm_plan(256, 256, 64, 0, 0, 0, 1, 152, 76, None) == ml.MT_ERR_INVALID_ARG
+    assert lib.mt_gemm_plan(256, 256, 64, 0, 0, 0, 1, 152, 76, out) == ml.MT_OK
+
+
 def test_gemm_tail_split_mode_is_checked(lib):
     assert lib.mt_gemm_set_tail_split(2) == ml.MT_ERR_INVALID_ARG
     assert lib.mt_gemm_set_tail_split(-1) == ml.MT_ERR_INVALID_ARG
