@@ -496,8 +496,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   }
 }
 
-// K-split tail, a unit with kpart > 0: this warp's columns of the partial sum (the columns its
-// epilogue part would store) go to slot kpart - 1, then one arrival on the tile's counter.
 // Accumulator columns an epilogue part reads: 32-column chunks c of [lo, hi) with c0 + c < N
 // (SwiGLU: each also the up chunk `width` columns later).  Returns the count; col(i) the i-th.
 template <int MODE>
@@ -513,6 +511,8 @@ struct PartCols {
   }
 };
 
+// K-split tail, a unit with kpart > 0: this warp's columns of the partial sum (the columns its
+// epilogue part would store) go to slot kpart - 1, then one arrival on the tile's counter.
 template <int MODE>
 __device__ __forceinline__ void kpart_store(const GemmParams& p, const Unit& w, uint32_t tacc, int c0, int width,
                                             int rank, int quad, int part, int lo, int hi) {
