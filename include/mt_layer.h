@@ -30,8 +30,10 @@
  * Ownership.  The caller owns x, the weights, every output and the workspace (all device
  * memory unless stated).  The library owns the handle, a 4-byte device error word and 16 MiB
  * of device memory for the fp32 partial sums of the GEMMs' K-split tail tiles (with 4 KiB of
- * arrival counters), allocated in mt_layer_create and freed in mt_layer_destroy.  Calls that take a stream are
- * asynchronous on it; a handle must not be used from two host threads at once.
+ * arrival counters), allocated in mt_layer_create and freed in mt_layer_destroy.  Calls that take a
+ * stream are asynchronous on it; a handle must not be used from two host threads at once, and its
+ * calls must not overlap on the GPU (on two streams without an ordering event between them): they
+ * share the workspace, the partial sums and the counters.
  *
  * Errors.  Every call returns an mt_status; on failure no kernel is launched and
  * mt_last_error() describes the problem (thread-local string, valid until the next call on the
