@@ -1,0 +1,61 @@
+"""Host logic of bench.py that needs no GPU: the DRAM traffic a bench line reports for its roofline
+kernel comes from an ncu summary under profiles/ only while the kernel sources that summary names
+are unchanged (otherwise the line reports null)."""
+import hashlib
+import os
+import re
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _tree(tmp, source, recorded_source=None, traffic=412984576):
+    csrc = tmp / "megatron_tensor_transformer_gpt_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "k.cu").write_text(source)
+    (csrc / "c.cuh").write_text("common")
+    sha = hashlib.sha256((recorded_source or source).encode()).hexdigest()[:16]
+    common = hashlib.sha256(b"common").hexdigest()[:16]
+    prof = tmp / "profiles"
+    prof.mkdir()
+    (prof / "k.md").write_text(f"# k\n\nsource_sha256_16: k.cu {sha}, c.cuh {common}\n"
+                               f"traffic_bytes_per_launch: {traffic}\n")
+
+
+def test_traffic_is_read_while_the_sources_match(tmp_path, monkeypatch):
+    _tree(tmp_path, "kernel v1")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profiled_traffic("k.md") == 412984576
+
+
+def test_traffic_is_null_once_a_source_changed(tmp_path, monkeypatch):
+    _tree(tmp_path, "kernel v1", recorded_source="kernel v0")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profiled_traffic("k.md") is None
+
+
+def test_traffic_is_null_without_a_summary(tmp_path, monkeypatch):
+    _tree(tmp_path, "kernel v1")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profiled_traffic("missing.md") is None
+
+
+def test_committed_summaries_name_existing_sources():
+    """Every committed summary that records traffic or source hashes names sources that exist, in
+    the form the bench parses."""
+    csrc = os.path.join(ROOT, "megatron_tensor_transformer_gpt_gb300", "csrc")
+    seen = 0
+    for name in sorted(os.listdir(os.path.join(ROOT, "profiles"))):
+        text = open(os.path.join(ROOT, "profiles", name)).read()
+        shas = re.search(r"source_sha256_16:(.*)", text)
+        if "traffic_bytes_per_launch" in text:
+            assert shas, name
+            assert int(re.search(r"traffic_bytes_per_launch:\s*(\d+)", text).group(1)) > 0
+        if shas:
+            pairs = re.findall(r"([\w.]+)\s+([0-9a-f]{16})", shas.group(1))
+            assert pairs, name
+            for src, _ in pairs:
+                assert os.path.exists(os.path.join(csrc, src)), (name, src)
+            seen += 1
+    assert seen >= 1
