@@ -287,16 +287,16 @@ std::atomic<int> g_pairing{0};
 std::atomic<int> g_tail{0};
 
 // Kernel, tile order and tail split of one GEMM (see GemmParams).
-//   Kernel: CTA pairs (256 x 256 tiles) when M > 128 and there is at least one full wave of them
-//   on the SM pairs; one CTA per 128 x 256 tile otherwise.
+//   Kernel: CTA pairs (256 x 256 tiles) when M > 128, also below one wave of them on the SM
+//   pairs; one CTA per 128 x 256 tile otherwise.
 //   Order: if one operand fits in about 56 MB of the 129 MB L2 it is kept resident (the other is
 //   streamed once); otherwise bands of m-tiles (or n-tiles) of about 56 MB, whichever streams
 //   fewer bytes from DRAM.
 //   Split: the tiles of the last partial wave are cut into pieces that still fit in one wave.  CTA
-//   pairs with a handle: into 2 to 4 ranges of K, when each range drops at least 16 K blocks (a
-//   unit's main loop runs at about the same rate per K block whatever its width, so only shorter
-//   K shortens the tail; the partial sums cost one fp32 write and read of the tile per extra
-//   range).  Otherwise into 2 or 4 pieces along N (QKV pieces keep whole heads; a CTA stages at
+//   pairs with a handle: into 2 to 4 ranges of K, each at least 16 K blocks shorter than the whole
+//   tile (a unit's main loop runs at about the same rate per K block whatever its width, so only
+//   shorter K shortens the tail; the partial sums cost one fp32 write and read of the tile per
+//   extra range).  Otherwise into 2 or 4 pieces along N (QKV pieces keep whole heads; a CTA stages at
 //   least 64 B rows, the smallest TMA box used).
 // The planning itself, for a device with `sms` SMs of which `pair_slots` CTA pairs can be resident;
 // ksplit_ok: the GEMM has a handle's partial-sum space (no CUDA call here).
