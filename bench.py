@@ -5,7 +5,8 @@
 A step is one call of mt_layer_forward (all nine steps of the layer: norm, QKV GEMM + RoPE,
 causal GQA flash attention, output projection + residual, norm, fc1 + SwiGLU, fc2 + residual)
 on inputs already resident in HBM.  L2 is flushed (a 256 MiB write) between steps, outside the
-timed spans; each step is timed with CUDA events on the launching stream.  `e2e` repeats the
+timed spans; each step is timed with CUDA events on the launching stream (`step_ms`: their median,
+10th and 90th percentile; `ms_per_step`: their mean).  `e2e` repeats the
 measurement through mt_layer_forward_host with pinned host buffers (x copied in and y copied out
 inside every step, in two row chunks overlapped with the layer's first and last GEMMs).  With N > 1 (torchrun) every rank runs an independent replica -- the layer
 forward of one data-parallel replica needs no collective -- and the slowest rank's time counts.
@@ -86,6 +87,12 @@ def max_over_ranks(values, dist=None, device=None):
 def job_throughput(world: int, flops_per_step: float, steps: int, total_ms: float) -> float:
     """Whole-job TFLOP/s: the work of every rank divided by the slowest rank's time."""
     return world * flops_per_step * steps / (total_ms * 1e-3) / 1e12
+
+
+def step_stats(ms):
+    """Median, 10th and 90th percentile (linear interpolation) of per-step times."""
+    a = np.asarray(ms, dtype=np.float64)
+    return [float(np.median(a)), float(np.percentile(a, 10)), float(np.percentile(a, 90))]
 
 
 def sample_flops(cfg, rows) -> float:
@@ -313,6 +320,7 @@ def run_native(args):
     total_ms = sum(step_ms)
     total_e2e = sum(e2e_ms) if e2e_ms else float("nan")
     total_ms, total_e2e = max_over_ranks([total_ms, total_e2e], dist if world > 1 else None, dev)
+    step_med, step_p10, step_p90 = max_over_ranks(step_stats(step_ms), dist if world > 1 else None, dev)
     value = job_throughput(world, flops, args.steps, total_ms)
     e2e_value = job_throughput(world, flops, args.steps, total_e2e)
 
@@ -346,7 +354,10 @@ def run_native(args):
 
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": total_ms / args.steps,
+        "step_ms": {"median": step_med, "p10": step_p10, "p90": step_p90,
+                    "note": "CUDA-event time of each timed step; the slowest rank's statistic"},
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 GEMMs, bf16 elsewhere" if args.fp8 else "bf16",
         "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights)",
         "config": {"workload": workload_desc(cfg), "seq": cfg.seq, "batch": cfg.batch, "tokens": cfg.tokens,

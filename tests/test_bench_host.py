@@ -1,6 +1,6 @@
 """Host logic of bench.py that needs no GPU: the DRAM traffic a bench line reports for its roofline
 kernel comes from an ncu summary under profiles/ only while the kernel sources that summary names
-are unchanged (otherwise the line reports null)."""
+are unchanged (otherwise the line reports null); the per-step statistics of the timed steps."""
 import hashlib
 import os
 import re
@@ -59,3 +59,8 @@ def test_committed_summaries_name_existing_sources():
                 assert os.path.exists(os.path.join(csrc, src)), (name, src)
             seen += 1
     assert seen >= 1
+
+
+def test_step_statistics():
+    assert bench.step_stats([5.0, 1.0, 3.0, 2.0, 4.0]) == [3.0, 1.4, 4.6]
+    assert bench.step_stats([2.5]) == [2.5, 2.5, 2.5]
