@@ -89,6 +89,14 @@ def job_throughput(world: int, flops_per_step: float, steps: int, total_ms: floa
     return world * flops_per_step * steps / (total_ms * 1e-3) / 1e12
 
 
+def dense_convention_flops(cfg) -> float:
+    """A forward's FLOPs with the attention counted as if unmasked (4 d S^2 per head and batch row),
+    the convention of MFU figures that ignore the causal mask; the line's own count keeps the
+    unmasked half only."""
+    heads = cfg.heads // cfg.tp
+    return cfg.gemm_flops() + 4.0 * cfg.head_dim * cfg.seq * cfg.seq * heads * cfg.batch
+
+
 def step_stats(ms):
     """Median, 10th and 90th percentile (linear interpolation) of per-step times."""
     a = np.asarray(ms, dtype=np.float64)
@@ -364,6 +372,10 @@ def run_native(args):
                    "gflop_per_step": flops / 1e9, "l2": "flushed by a 256 MiB write between timed steps",
                    "parallelism": f"replicas x{world}"},
         "mfu": value / peak_tf, "mfu_vs_sustained": value / peaks["bf16_tflops_sustained"],
+        "mfu_dense_convention": (None if args.backward else
+                                 value * dense_convention_flops(cfg) / flops / peak_tf),
+        "mfu_dense_convention_note": "attention counted as 4 d S^2 per head (causal mask ignored); "
+                                     "mfu counts the unmasked half only",
         "peak_source": f"{peak_src}: bf16 {peak_tf} TF/s burst, {peaks['bf16_tflops_sustained']} sustained",
         "tokens_per_s": world * cfg.tokens * args.steps / (total_ms * 1e-3),
         "per_kernel_ms": {k: (ms / n if n else 0.0) for k, (n, ms) in prof.items()},

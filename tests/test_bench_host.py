@@ -1,11 +1,13 @@
 """Host logic of bench.py that needs no GPU: the DRAM traffic a bench line reports for its roofline
 kernel comes from an ncu summary under profiles/ only while the kernel sources that summary names
-are unchanged (otherwise the line reports null); the per-step statistics of the timed steps."""
+are unchanged (otherwise the line reports null); the per-step statistics of the timed steps; the
+dense-convention FLOP count."""
 import hashlib
 import os
 import re
 
 import bench
+import synth
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -64,3 +66,13 @@ def test_committed_summaries_name_existing_sources():
 def test_step_statistics():
     assert bench.step_stats([5.0, 1.0, 3.0, 2.0, 4.0]) == [3.0, 1.4, 4.6]
     assert bench.step_stats([2.5]) == [2.5, 2.5, 2.5]
+
+
+def test_dense_convention_counts_the_whole_score_square():
+    cfg = synth.CONFIGS["llama8b"]
+    attn_half = cfg.attn_flops()                       # 4 d S (S + 1) / 2 per head
+    dense = bench.dense_convention_flops(cfg)
+    assert abs(dense - (cfg.flops() - attn_half + 2.0 * attn_half * cfg.seq / (cfg.seq + 1))) < 1e3
+    assert round(dense / 1e9, 1) == 2061.6
+    rank = synth.CONFIGS["llama70b_tp8"]                # one rank of eight: its own heads only
+    assert bench.dense_convention_flops(rank) == rank.gemm_flops() + 4.0 * 128 * 4096 * 4096 * 8
