@@ -146,6 +146,20 @@ def test_gemm_plan_tail_forms(lib):
     assert (full["split"], full["ksplit"], full["num_units"]) == (1, 1, 76)
 
 
+def test_gemm_plan_of_the_ksplit_test_layers(lib):
+    """The GPU K-split tests' layers (hidden 2048, 16 x 128 heads, 4 groups) put 3, 2 and 4 K ranges
+    under the QKV, SwiGLU, residual and GeLU epilogues."""
+    ks = lambda M, N, K, epi: ml.mt_gemm_plan(M, N, K, epi, head_dim=128)["ksplit"]
+    assert ks(2048, 3072, 2048, 2) == 3      # QKV, tail 20 tiles
+    assert ks(2048, 4096, 2048, 3) == 2      # fc1 SwiGLU, tail 28
+    assert ks(2560, 2048, 2048, 1) == 4      # output projection, tail 4
+    assert ks(2560, 2048, 4096, 1) == 4      # fc2
+    assert ks(2560, 4096, 2048, 3) == 4      # fc1 SwiGLU, tail 16
+    assert ks(2560, 6144, 2048, 2) == 4      # MHA QKV, tail 12
+    assert ks(2560, 8192, 2048, 4) == 4      # fc1 GeLU, tail 16
+    assert ks(2560, 2048, 2048, 0) == 4      # TP = 2 rank's fc2 partial (K = 2048 per rank)
+
+
 def _with_tail_split(mode, fn):
     ml.mt_gemm_set_tail_split(mode)
     try:
