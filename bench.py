@@ -334,7 +334,7 @@ def run_native(args):
 
     peaks, peak_src = load_peaks()
     peak_tf = peaks["bf16_tflops"]
-    # the FP8 path is judged against the bf16 measurement times the nominal E4M3 / bf16 ratio (2)
+    # the FP8 path is compared with the bf16 measurement times the nominal E4M3 / bf16 ratio (2)
     kernel_peak = 2.0 * peak_tf if args.fp8 else peak_tf
     launches, fc1_ms = prof_timed["gemm_fc1"]
     fc1_avg = fc1_ms / max(1, launches)
