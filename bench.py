@@ -10,6 +10,9 @@ timed spans; each step is timed with CUDA events on the launching stream (`step_
 measurement through mt_layer_forward_host with pinned host buffers (x copied in and y copied out
 inside every step, in two row chunks overlapped with the layer's first and last GEMMs).  With N > 1 (torchrun) every rank runs an independent replica -- the layer
 forward of one data-parallel replica needs no collective -- and the slowest rank's time counts.
+`workloads` adds the GPU-only time of the other configurations (tiny, GPT-345M-shaped, one TP=8
+rank of the 70B-shaped layer, the 32k-token 8B-shaped layer), timed the same way; `cpu_oracle_extras`
+times the oracle on the tiny layer with one thread and on the 70B-shaped layer's eight shards.
 
 --impl reference times the float64 CPU oracle (the "reference" arm of this build) on the host
 cores: each step is a bounded sample of the same workload (K and V of every token plus the whole
@@ -35,6 +38,7 @@ import synth  # noqa: E402
 
 METRIC = "Layer fwd TFLOP/s & MFU vs GB300 bf16 dense peak; tokens/s per layer (1 GPU)"
 UNIT = "TFLOP/s"
+EXTRA_WORKLOADS = ("tiny", "gpt345m", "llama70b_tp8", "llama8b_32k")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -133,6 +137,108 @@ def oracle_sample(cfg, inp, n_rows):
     oracle.layer_forward(cfg, inp, rows=rows)
     dt = time.perf_counter() - t0
     return sample_flops(cfg, rows), dt
+
+
+def rank_shapes(cfg):
+    """One rank's weight shapes (rank 0 of cfg.tp), rows = output features."""
+    H, d, tp = cfg.hidden, cfg.head_dim, cfg.tp
+    qw, kvw, f = cfg.heads // tp * d, cfg.groups // tp * d, cfg.ffn // tp
+    f1 = 2 * f if cfg.act == "swiglu" else f
+    shapes = {"norm1_w": (H,), "w_qkv": (qw + 2 * kvw, H), "w_o": (H, qw), "norm2_w": (H,), "w_fc1": (f1, H),
+              "w_fc2": (H, f)}
+    if cfg.norm == "layer":
+        shapes.update(norm1_b=(H,), norm2_b=(H,))
+    if cfg.bias:
+        shapes.update(b_qkv=(qw + 2 * kvw,), b_o=(H,), b_fc1=(f1,), b_fc2=(H,))
+    return shapes
+
+
+def device_inputs(cfg, dev, seed):
+    """Seeded synthetic inputs of one rank drawn on the device, with the distributions of the seeded
+    host inputs (x ~ N(0, 1), projection weights ~ N(0, 0.02), norm gains 1, shifts and biases 0),
+    for workloads that are timed but not compared (drawing the 70B-shaped layer on the host would
+    take longer than timing it)."""
+    import torch
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    out = {"x": torch.randn(cfg.tokens, cfg.hidden, generator=g, device=dev).to(torch.bfloat16)}
+    for name, shape in rank_shapes(cfg).items():
+        if name.startswith("w_"):
+            out[name] = (torch.randn(shape, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+        else:
+            fill = 1.0 if name in ("norm1_w", "norm2_w") else 0.0
+            out[name] = torch.full(shape, fill, dtype=torch.bfloat16, device=dev)
+    return out
+
+
+def time_workload(ml, cfg, dev, steps, warmup, flush, peak_tf):
+    """GPU-only time of one forward of `cfg` (one rank of cfg.tp in the identity-reduce timing mode),
+    timed as the headline: CUDA events around every step, the L2 flushed between steps."""
+    import torch
+    tens = device_inputs(cfg, dev, seed=7)
+    x = tens.pop("x")
+    layer = ml.Layer.from_config(cfg, tp_rank=0)
+    w = layer.weights(tens)
+    y = torch.empty(cfg.tokens, cfg.hidden, dtype=torch.bfloat16, device=dev)
+    layer.workspace(cfg.seq, cfg.batch, dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        layer.forward(x, cfg.seq, cfg.batch, w, y)
+    torch.cuda.synchronize()
+    n0 = ml.mt_layer_launch_count(layer.handle)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        layer.forward(x, cfg.seq, cfg.batch, w, y)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    layer.status()
+    launches = ml.mt_layer_launch_count(layer.handle) - n0
+    ms = [a.elapsed_time(b) for a, b in ev]
+    layer.close()
+    mean = sum(ms) / len(ms)
+    tf = cfg.flops() / (mean * 1e-3) / 1e12
+    return {"workload": workload_desc(cfg), "gflop_per_step": cfg.flops() / 1e9, "steps": steps,
+            "ms_per_step": mean, "step_ms_median": float(np.median(ms)), "tflops": tf, "frac_of_burst": tf / peak_tf,
+            "tokens_per_s": cfg.tokens / (mean * 1e-3), "gpu_launches": launches}
+
+
+def cpu_oracle_extras():
+    """Two more timings of the float64 oracle on the host cores: the tiny layer whole on one thread,
+    and the 70B-shaped TP = 8 layer as its eight shards (K and V of every token for each shard, then
+    each shard's partials for the last rows, summed)."""
+    import oracle
+    out = {}
+    cfg = synth.CONFIGS["tiny"]
+    # one thread: a child process whose BLAS is limited before NumPy loads it
+    code = ("import json, time, oracle, synth\n"
+            "cfg = synth.CONFIGS['tiny']\ninp = synth.make_inputs(cfg, seed=0)\n"
+            "oracle.layer_forward(cfg, inp)\nt0 = time.perf_counter()\noracle.layer_forward(cfg, inp)\n"
+            "print(json.dumps(time.perf_counter() - t0))\n")
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, "-c", code], env=env, cwd=ROOT, capture_output=True, text=True, timeout=300)
+    if r.returncode == 0:
+        dt = float(r.stdout.strip().splitlines()[-1])
+        out["tiny_one_thread"] = {"value": cfg.flops() / dt / 1e12, "unit": UNIT, "cores": 1, "seconds": dt,
+                                  "sample": f"the whole {cfg.tokens}-token layer ({cfg.flops() / 1e9:.3f} GFLOP)"}
+    cfg = synth.CONFIGS["llama70b_tp8"]
+    t0 = time.perf_counter()
+    inp = synth.make_inputs(cfg, seed=0)
+    shards = [synth.shard_weights(cfg, inp, cfg.tp, r) for r in range(cfg.tp)]
+    gen = time.perf_counter() - t0
+    n_rows = 256
+    rows = np.arange(cfg.tokens - n_rows, cfg.tokens)
+    t0 = time.perf_counter()
+    oracle.layer_forward_tp_sum(cfg, cfg.tp, inp["x"], shards, rows=rows)
+    dt = time.perf_counter() - t0
+    full = cfg.replace(tp=1)
+    sf = sample_flops(full, rows)
+    out["llama70b_tp8_eight_shards"] = {
+        "value": sf / dt / 1e12, "unit": UNIT, "cores": blas_threads(), "seconds": dt,
+        "sample": f"all {cfg.tp} shards: K/V of all {cfg.tokens} tokens + both blocks for the last {n_rows} rows, "
+                  f"partials summed ({sf / 1e9:.1f} GFLOP algorithmic); drawing the inputs took {gen:.1f} s"}
+    return out
 
 
 # ------------------------------------------------------------------------------------ clocks
@@ -305,6 +411,13 @@ def run_native(args):
     prof = ml.mt_layer_profile_read(layer.handle)
     ml.mt_layer_profile_enable(layer.handle, False)
 
+    # the other workloads, GPU time only (their oracle comparisons are the parity tests)
+    workloads = {}
+    if not (args.quick or args.fp8 or args.backward or args.no_workloads) and args.workload == "llama8b":
+        for name in EXTRA_WORKLOADS:
+            workloads[name] = time_workload(ml, synth.CONFIGS[name], dev, args.steps, args.warmup, flush,
+                                            load_peaks()[0]["bf16_tflops"])
+
     # end to end through the host-buffer entry point
     xh = x.cpu().pin_memory()
     yh = torch.empty(cfg.tokens, cfg.hidden, dtype=torch.bfloat16).pin_memory()
@@ -360,6 +473,10 @@ def run_native(args):
                "sample": f"float64 NumPy oracle: K/V of all {cfg.tokens} tokens + the whole layer for the last "
                          f"{n_rows} rows ({sf / 1e9:.1f} GFLOP algorithmic, {dt:.1f} s)"}
 
+    cpu_extra = None
+    if cpu is not None and args.workload == "llama8b":
+        cpu_extra = cpu_oracle_extras()
+
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total_ms / args.steps,
@@ -395,6 +512,11 @@ def run_native(args):
                 "d2h_bytes_per_step": cfg.tokens * cfg.hidden * 2, "ms_per_step": total_e2e / args.steps},
         "gpu_launches": kernel_launches,
         "clocks": clk,
+        "workloads": workloads or None,
+        "workloads_note": ("the other configurations, GPU time only, timed like the headline (events, L2 flushed "
+                           "between steps); seeded inputs drawn on the device; the 70B-shaped layer is one TP=8 "
+                           "rank with the all-reduce replaced by the identity"),
+        "cpu_oracle_extras": cpu_extra,
     }
     print(json.dumps(out))
     if world > 1:
@@ -438,6 +560,8 @@ def main():
     ap.add_argument("--impl", choices=("native", "reference"), default="native")
     ap.add_argument("--workload", default="llama8b", choices=sorted(synth.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the GPU-only timings of the other configurations")
     ap.add_argument("--backward", action="store_true",
                     help="time mt_layer_backward (forward recompute + gradients) instead of the forward")
     ap.add_argument("--fp8", action="store_true",

@@ -99,12 +99,16 @@ int mt_layer_workspace_bytes(const mt_layer* L, int seq, int batch, size_t* byte
  * The caller keeps ownership and must keep it alive while calls using it are in flight. */
 int mt_layer_set_workspace(mt_layer* L, void* dev_ptr, size_t bytes);
 
-/* Whole layer.  x [T, H] -> y_partial [T, H].
+/* Whole layer.  x [T, H] -> y_partial [T, H], in the order of the layer spec of "快速入门 /
+ * Pai-Megatron-Patch 项目深度学习总结文档" §3.1 (input_layernorm, linear_qkv, core_attention with the
+ * causal mask, linear_proj, bias-dropout-add, pre_mlp_layernorm, linear_fc1, linear_fc2,
+ * bias-dropout-add), with the column/row splits of "Megatron-LM 深度学习与源码分析文档" Part 2 §2:
  *   tp_size == 1: y = h + fc2(act(fc1(norm2(h)))) + b_fc2, with h = x + o_proj(attn(norm1(x))) + b_o.
  *   tp_size  > 1: the all-reduce between the two blocks is replaced by the identity,
  *                 h = x + Y_attn,i + b_o, and y_partial = Y_mlp,i(h) is this rank's
  *                 pre-reduce row-parallel partial (no bias, no residual).
- * 8 kernel launches on `cuda_stream` (a cudaStream_t; NULL = legacy default stream). */
+ * 7 kernel launches on `cuda_stream` (a cudaStream_t; NULL = legacy default stream): norm1 (which
+ * also writes the RoPE table), QKV GEMM, attention, output projection, norm2, fc1, fc2. */
 int mt_layer_forward(mt_layer* L, const void* x, int seq, int batch, const mt_weights* w, void* y_partial,
                      void* cuda_stream);
 
@@ -197,8 +201,10 @@ typedef struct { /* device pointers, shapes as in mt_weights; NULL = gradient no
   void *norm1_w, *norm1_b, *w_qkv, *b_qkv, *w_o, *b_o, *norm2_w, *norm2_b, *w_fc1, *b_fc1, *w_fc2, *b_fc2;
 } mt_grads;
 
-/* Workspace the backward pass needs (a superset of the forward's: the forward intermediates,
- * gradient scratch, per-head fp32 score and dP matrices [seq, seq], and transposes). */
+/* Workspace the backward pass needs (a superset of the forward's: the forward intermediates, the
+ * plain QKV and fc1 outputs, gradient scratch in bf16, fp32 dq/dk/dv in head-major order, the
+ * per-row softmax statistics and head-major copies of dO and V).  No [seq, seq] matrix is stored:
+ * the attention backward rebuilds the probabilities tile by tile. */
 int mt_layer_backward_workspace_bytes(const mt_layer* L, int seq, int batch, size_t* bytes);
 
 /* dx [T, H] = dL/dx and the requested weight gradients, given x and dy = dL/dy [T, H].  Needs
@@ -216,10 +222,12 @@ int mt_layer_backward(mt_layer* L, const void* x, const void* dy, int seq, int b
  * 8 RoPE table [seq, d/2] float2 (cos, sin). */
 int mt_layer_workspace_region(const mt_layer* L, int seq, int batch, int which, size_t* offset, size_t* bytes);
 
-/* Synchronise with the work queued by this handle (all streams) and report a device-side
- * failure recorded since the last call (MT_ERR_DEVICE_TIMEOUT, or MT_ERR_INVALID_ARG for
- * inconsistent packed cu_seqlens), clearing it (and, after a failure, the K-split arrival
- * counters, which a launch that gave up may have left counted). */
+/* Wait for the work this handle queued (the stream of its last call and its own copy stream;
+ * other streams of the process are not waited for) and report a device-side failure recorded
+ * since the last call (MT_ERR_DEVICE_TIMEOUT, or MT_ERR_INVALID_ARG for inconsistent packed
+ * cu_seqlens), clearing it (and, after a failure, the K-split arrival counters, which a launch
+ * that gave up may have left counted).  The error word is read through the handle's copy stream,
+ * so no device-wide synchronisation happens.  Host call. */
 int mt_layer_status(mt_layer* L);
 
 /* Thread-local description of the last failure on this thread ("" after success). */
@@ -332,12 +340,14 @@ int mt_selftest_bounded_wait(int limit_us);
  * nothing.  No cudaMalloc, cudaFree or allocating library routine is called.
  *
  * The first call on a device looks up the area's device address (cudaGetSymbolAddress, with that
- * device current); make that first call before any stream capture.  Every call clears the error
- * word and uploads the RoPE frequencies (a small host-to-device copy on cuda_stream) before the
- * kernels.  All calls share the one area, which keeps the last call's contents: calls whose work
- * overlaps on the GPU (other streams, other host threads) race and corrupt each other's results.
- * Device-side timeouts are recorded in the area's error word but cannot be read back through this
- * entry point. */
+ * device current); make that first call before any stream capture.  The address is kept per
+ * device and CUDA context: after cudaDeviceReset (a new context) the next call looks it up again,
+ * so that call too should come before any stream capture.  Every call first launches a one-CTA
+ * set-up kernel on cuda_stream that clears the error word and writes the RoPE frequencies (passed
+ * as kernel arguments), then the layer's kernels.  All calls share the one area, which keeps the
+ * last call's contents: calls whose work overlaps on the GPU (other streams, other host threads)
+ * race and corrupt each other's results.  Device-side timeouts are recorded in the area's error
+ * word but cannot be read back through this entry point. */
 #define MT_STATIC_AREA_BYTES (32u << 20)
 int mt_layer_forward_static(int hidden, int heads, int query_groups, int head_dim, int ffn, int norm, int act,
                             float rope_base, int tp_size, int tp_rank, float eps, const void* x, int seq, int batch,

@@ -50,6 +50,10 @@ struct mt_layer {
   // arrival counters (kept at zero between launches)
   float4* d_kws;
   int* d_kflags;
+  // recorded on the caller's stream at the end of every call that queues work (mt_layer_status
+  // waits for it instead of the whole device)
+  cudaEvent_t done_ev;
+  bool done_pending;
 };
 
 namespace {
@@ -73,6 +77,14 @@ int ok() {
 
 int cuda_fail(cudaError_t e, const char* what) {
   return fail(MT_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// Successful end of a call that queued work on `st`: marks the point mt_layer_status waits for.
+int done(mt_layer* L, cudaStream_t st) {
+  cudaError_t e = cudaEventRecord(L->done_ev, st);
+  if (e != cudaSuccess) return cuda_fail(e, "recording the end of the call");
+  L->done_pending = true;
+  return ok();
 }
 
 enum Slot { kSlotRope = 0, kSlotNorm1, kSlotQkv, kSlotAttn, kSlotO, kSlotNorm2, kSlotFc1, kSlotFc2 };
@@ -997,6 +1009,7 @@ int mt_layer_create(int hidden, int heads, int query_groups, int head_dim, int f
   if (e == cudaSuccess) e = cudaMalloc(&L->d_kws, static_cast<size_t>(kKsSlots) * 256 * 256 * sizeof(float));
   if (e == cudaSuccess) e = cudaMalloc(&L->d_kflags, kKsTiles * 16 * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(L->d_kflags, 0, kKsTiles * 16 * sizeof(int));
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&L->done_ev, cudaEventDisableTiming);
   if (e == cudaSuccess && rope_base > 0.f) {
     const int half = head_dim / 2;
     double theta[64];
@@ -1052,7 +1065,7 @@ int mt_layer_forward(mt_layer* L, const void* x, int seq, int batch, const mt_we
   if (rc) return rc;
   if ((rc = check_weights(L, w, true, true))) return rc;
   rc = forward_device(L, lay, x, seq, batch, w, y_partial, static_cast<cudaStream_t>(cuda_stream));
-  return rc ? rc : ok();
+  return rc ? rc : done(L, static_cast<cudaStream_t>(cuda_stream));
 }
 
 int mt_layer_forward_attn(mt_layer* L, const void* x, int seq, int batch, const mt_weights* w, void* attn_out,
@@ -1062,7 +1075,7 @@ int mt_layer_forward_attn(mt_layer* L, const void* x, int seq, int batch, const 
   if (rc) return rc;
   if ((rc = check_weights(L, w, true, false))) return rc;
   rc = run_attention_block(L, lay, x, seq, batch, w, attn_out, mt::kEpiStore, static_cast<cudaStream_t>(cuda_stream));
-  return rc ? rc : ok();
+  return rc ? rc : done(L, static_cast<cudaStream_t>(cuda_stream));
 }
 
 int mt_layer_forward_mlp(mt_layer* L, const void* h, int seq, int batch, const mt_weights* w, void* y_partial,
@@ -1072,7 +1085,7 @@ int mt_layer_forward_mlp(mt_layer* L, const void* h, int seq, int batch, const m
   if (rc) return rc;
   if ((rc = check_weights(L, w, false, true))) return rc;
   rc = run_mlp_block(L, lay, h, seq, batch, w, y_partial, mt::kEpiStore, static_cast<cudaStream_t>(cuda_stream));
-  return rc ? rc : ok();
+  return rc ? rc : done(L, static_cast<cudaStream_t>(cuda_stream));
 }
 
 int mt_layer_workspace_bytes_packed(const mt_layer* L, int total_tokens, int num_seqs, int max_seqlen, size_t* bytes) {
@@ -1100,7 +1113,7 @@ int mt_layer_forward_packed(mt_layer* L, const void* x, int total_tokens, const 
   if (rc) return rc;
   const Packed pk{cu_seqlens, num_seqs, max_seqlen};
   rc = forward_device(L, lay, x, total_tokens, 1, w, y_partial, static_cast<cudaStream_t>(cuda_stream), &pk);
-  return rc ? rc : ok();
+  return rc ? rc : done(L, static_cast<cudaStream_t>(cuda_stream));
 }
 
 int mt_layer_forward_host(mt_layer* L, const void* x_host, int seq, int batch, const mt_weights* w, void* y_host,
@@ -1157,7 +1170,7 @@ int mt_layer_forward_host(mt_layer* L, const void* x_host, int seq, int batch, c
     if (e == cudaSuccess) e = cudaEventRecord(ev[0], cs);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev[0], 0);
     if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy of y");
-    return ok();
+    return done(L, st);
   }
   cudaError_t e = cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy of x");
@@ -1165,28 +1178,36 @@ int mt_layer_forward_host(mt_layer* L, const void* x_host, int seq, int batch, c
   if (rc) return rc;
   e = cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, st);
   if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy of y");
-  return ok();
+  return done(L, st);
 }
 
 int mt_layer_status(mt_layer* L) {
   if (L == nullptr) return fail(MT_ERR_INVALID_ARG, "handle is NULL");
-  cudaError_t e = cudaDeviceSynchronize();
-  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  // wait for the handle's own work only: the end of its last call and its copy stream
+  cudaError_t e = L->done_pending ? cudaEventSynchronize(L->done_ev) : cudaSuccess;
+  if (e != cudaSuccess) return cuda_fail(e, "waiting for the handle's last call");
+  L->done_pending = false;
+  int rc = ensure_copy_stream(L);
+  if (rc) return rc;
+  cudaStream_t cs = L->copy_stream;
   int code = 0;
-  e = cudaMemcpy(&code, L->d_err, sizeof(int), cudaMemcpyDeviceToHost);
+  e = cudaStreamSynchronize(cs);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&code, L->d_err, sizeof(int), cudaMemcpyDeviceToHost, cs);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
   if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
-  // a launch that gave up may have left K-split arrivals counted: start the next one from zero
-  if (code != 0) cudaMemset(L->d_kflags, 0, kKsTiles * 16 * sizeof(int));
-  if (code == MT_ERR_INVALID_ARG) {
-    cudaMemset(L->d_err, 0, sizeof(int));
+  if (code != 0) {
+    // a launch that gave up may have left K-split arrivals counted: start the next one from zero
+    e = cudaMemsetAsync(L->d_kflags, 0, kKsTiles * 16 * sizeof(int), cs);
+    if (e == cudaSuccess) e = cudaMemsetAsync(L->d_err, 0, sizeof(int), cs);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+  }
+  if (code == MT_ERR_INVALID_ARG)
     return fail(MT_ERR_INVALID_ARG, "cu_seqlens were found inconsistent on the device (not 0 .. total_tokens, "
                                     "decreasing, or a sample longer than max_seqlen); outputs are invalid");
-  }
-  if (code != 0) {
-    cudaMemset(L->d_err, 0, sizeof(int));
+  if (code != 0)
     return fail(MT_ERR_DEVICE_TIMEOUT, "a kernel stopped waiting on a barrier (device code %d); outputs are invalid",
                 code);
-  }
   return ok();
 }
 
@@ -1207,6 +1228,7 @@ void mt_layer_destroy(mt_layer* L) {
   for (auto e : L->copy_ev)
     if (e) cudaEventDestroy(e);
   if (L->copy_stream) cudaStreamDestroy(L->copy_stream);
+  if (L->done_ev) cudaEventDestroy(L->done_ev);
   delete L;
 }
 
@@ -1367,7 +1389,7 @@ int mt_layer_forward_fp8(mt_layer* L, const void* x, int seq, int batch, const m
   wn.w_fc2 = w8->w_fc2;
   if ((rc = check_weights(L, &wn, true, true))) return rc;
   rc = forward_device_fp8(L, lay, x, seq, batch, w, w8, y_partial, static_cast<cudaStream_t>(cuda_stream));
-  return rc ? rc : ok();
+  return rc ? rc : done(L, static_cast<cudaStream_t>(cuda_stream));
 }
 
 int mt_quantize_e4m3(const void* src, size_t n, void* dst, float* amax_deq, void* cuda_stream) {
@@ -1424,7 +1446,7 @@ int mt_layer_backward(mt_layer* L, const void* x, const void* dy, int seq, int b
   int rc = check_weights(L, w, true, true);
   if (rc) return rc;
   rc = backward_device(L, b, x, dy, seq, batch, w, dx, g, static_cast<cudaStream_t>(cuda_stream));
-  return rc ? rc : ok();
+  return rc ? rc : done(L, static_cast<cudaStream_t>(cuda_stream));
 }
 
 int mt_sp_reduce_add_norm(const void* const* partials, int num_partials, const void* resid, const void* bias,
@@ -1491,20 +1513,63 @@ namespace {
 constexpr size_t kStaticHeader = 1024;  // error word at offset 0, RoPE frequencies at 256
 constexpr int kMaxDevices = 128;
 std::mutex g_static_mu;
-void* g_static_ptr[kMaxDevices];
+struct StaticSlot {
+  unsigned long long ctx_id;  // the CUDA context the address belongs to
+  void* ptr;
+};
+StaticSlot g_static[kMaxDevices];
 
-// Device address of the static area on `dev` (the current device), looked up once per device.
+// Id of the context current on this thread (0 if none is current yet).
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_ctx = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  if (get_ctx == nullptr || get_id == nullptr) {
+    void* a = nullptr;
+    void* b = nullptr;
+    cudaDriverEntryPointQueryResult qa, qb;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 4000, cudaEnableDefault, &qa) != cudaSuccess ||
+        qa != cudaDriverEntryPointSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) != cudaSuccess ||
+        qb != cudaDriverEntryPointSuccess)
+      return 0;
+    get_ctx = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(a);
+    get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(b);
+  }
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the static area on `dev` (the current device).  It is looked up once per
+// device and context: a context created anew (after cudaDeviceReset, say) gets a fresh lookup.
 int static_area(int dev, void** out) {
   if (dev < 0 || dev >= kMaxDevices) return fail(MT_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
   std::lock_guard<std::mutex> lock(g_static_mu);
-  if (g_static_ptr[dev] == nullptr) {
+  const unsigned long long id = current_context_id();
+  StaticSlot& slot = g_static[dev];
+  if (slot.ptr == nullptr || id == 0 || slot.ctx_id != id) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_static_area);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the static scratch area");
-    g_static_ptr[dev] = p;
+    slot.ptr = p;
+    slot.ctx_id = current_context_id();  // the lookup has made the context current if none was
   }
-  *out = g_static_ptr[dev];
+  *out = slot.ptr;
   return MT_OK;
+}
+
+// Per-call set-up of the static area, as kernel arguments (so no host memory is read by a copy):
+// clears the error word and writes the RoPE frequencies.
+struct StaticSetup {
+  double theta[64];
+  int half;
+};
+
+__global__ void static_setup_kernel(int* err, double* theta, StaticSetup s) {
+  const int i = threadIdx.x;
+  if (i == 0) *err = 0;
+  if (theta != nullptr && i < s.half) theta[i] = s.theta[i];
 }
 }  // namespace
 
@@ -1574,14 +1639,16 @@ extern "C" int mt_layer_forward_static(int hidden, int heads, int query_groups, 
   if ((rc = check_call(&L, x, y_partial, seq, batch, &lay))) return rc;
   if ((rc = check_weights(&L, w, true, true))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  e = cudaMemsetAsync(L.d_err, 0, sizeof(int), st);  // the error word must start at zero
-  if (e != cudaSuccess) return cuda_fail(e, "clearing the static error word");
-  if (L.d_theta != nullptr) {
-    double theta[64];
-    for (int i = 0; i < head_dim / 2; ++i) theta[i] = std::pow(static_cast<double>(rope_base), -2.0 * i / head_dim);
-    e = cudaMemcpyAsync(L.d_theta, theta, (head_dim / 2) * sizeof(double), cudaMemcpyHostToDevice, st);
-    if (e != cudaSuccess) return cuda_fail(e, "copying the RoPE frequencies");
-  }
+  StaticSetup setup{};
+  setup.half = head_dim / 2;
+  for (int i = 0; i < setup.half; ++i)
+    setup.theta[i] = std::pow(static_cast<double>(rope_base), -2.0 * i / head_dim);  // as mt_layer_create
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(64);
+  cfg.stream = st;
+  e = cudaLaunchKernelEx(&cfg, static_setup_kernel, L.d_err, L.d_theta, setup);  // the error word starts at zero
+  if (e != cudaSuccess) return cuda_fail(e, "static area set-up launch");
   rc = forward_device(&L, lay, x, seq, batch, w, y_partial, st);
   return rc ? rc : ok();
 }

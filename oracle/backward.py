@@ -73,14 +73,16 @@ def layer_backward(cfg, inp: Dict, dy: np.ndarray) -> Dict[str, np.ndarray]:
         cs, sn = ol.rope_cos_sin(np.arange(T) // B, d, cfg.rope_base)
         q, k = ol.rope(q, cs, sn), ol.rope(k, cs, sn)
     scale = 1.0 / np.sqrt(d)
-    P = {}
+
+    def probs(b, h):
+        """Causal softmax of one head's scores (formed again where the backward needs them, so that
+        no more than one [S, S] matrix is held at a time)."""
+        return ol.causal_softmax((q[b::B, h] @ k[b::B, h // rep].T) * scale, np.arange(S))
+
     o = np.empty((T, nh, d))
     for b in range(B):
         for h in range(nh):
-            g = h // rep
-            p = ol.causal_softmax((q[b::B, h] @ k[b::B, g].T) * scale, np.arange(S))
-            P[b, h] = p
-            o[b::B, h] = p @ v[b::B, g]
+            o[b::B, h] = probs(b, h) @ v[b::B, h // rep]
     o2 = o.reshape(T, nh * d)
     h_ = x + ol.linear(o2, W["w_o"], W.get("b_o"))
     hn, xhat2, r2 = _norm_fwd(cfg, h_, W["norm2_w"], W.get("norm2_b"))
@@ -110,7 +112,7 @@ def layer_backward(cfg, inp: Dict, dy: np.ndarray) -> Dict[str, np.ndarray]:
     for b in range(B):
         for h in range(nh):
             g = h // rep
-            p = P[b, h]
+            p = probs(b, h)
             dob = do[b::B, h]
             dv[b::B, g] += p.T @ dob
             dp = dob @ v[b::B, g].T

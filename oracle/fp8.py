@@ -19,6 +19,11 @@ Readings (where the pages are silent):
   * Which tensors are FP8: the four GEMM inputs of each side -- normed x, the attention output,
     normed h and the MLP hidden (activations, delayed scaling), and the four projection weights
     (current scaling at quantisation time).  q/k/v, the attention itself, h and y stay bf16.
+  * A quantised code is an integer decided by floating point, so where a comparison needs the
+    codes of the attention output or of normed h to be decided from the same values as the
+    kernels decide them, the oracle takes the kernels' storage precision for the intermediates
+    they store between launches: q and k in bf16, v in fp16 (after RoPE), h in bf16
+    (storage_rounding=True).  Everything else stays float64.
 """
 from __future__ import annotations
 
@@ -96,46 +101,93 @@ def quantize_weights(inp: Dict) -> Dict[str, Dict[str, np.ndarray]]:
     return {k: quantize_weight(inp[k]) for k in WEIGHT_NAMES}
 
 
-def layer_forward_fp8(cfg, inp: Dict, act_scales, rows: Optional[np.ndarray] = None,
-                      wq: Optional[Dict] = None) -> Dict[str, np.ndarray]:
-    """Whole layer at TP=1 with the four GEMMs on E4M3 operands.
+def round_bf16(x) -> np.ndarray:
+    """float64 -> the value a kernel stores: fp32 (nearest even), then bfloat16 (nearest even)."""
+    f = np.asarray(x, dtype=np.float64).astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    u = (u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
+    return (u.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
 
-    act_scales: fp32 scales of (xn, o, hn, a).  Weights use quantize_weight (or the precomputed
-    `wq` of quantize_weights(inp)).  Returns y and h for `rows` (all tokens if None) and the amax
-    of each activation over those rows.
-    """
+
+def round_fp16(x) -> np.ndarray:
+    """float64 -> fp32 -> IEEE half (nearest even), as a kernel stores v for the P V product."""
+    return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float16).astype(np.float64)
+
+
+def _cast(name: str, x, scale):
+    """The E4M3 cast of activation `name` (one of ACT_NAMES) as the next GEMM sees it."""
+    return _qdq(x, scale)
+
+
+def attention_block_fp8(cfg, inp: Dict, act_scales, rows: Optional[np.ndarray] = None, wq: Optional[Dict] = None,
+                        storage_rounding: bool = False) -> Dict[str, np.ndarray]:
+    """Attention half of the FP8 layer at TP=1: xn = Norm1(x) cast to E4M3, QKV, RoPE, causal GQA
+    attention, its output o cast to E4M3, the output projection, h = x + Y_attn + b_o (float64).
+
+    storage_rounding: q and k are rounded to bf16 and v to fp16 after RoPE, as the kernels store
+    them between launches; the E4M3 code of o is then decided from the same stored operands as the
+    kernel decides it.  Returns xn, o and h for `rows` (all tokens if None)."""
     T, B, d = cfg.tokens, cfg.batch, cfg.head_dim
     nh, ng = cfg.heads, cfg.groups
     rows = np.arange(T) if rows is None else np.asarray(rows)
-    s_xn, s_o, s_hn, s_a = (np.float32(s) for s in act_scales)
+    s_xn, s_o = np.float32(act_scales[0]), np.float32(act_scales[1])
     wq = quantize_weights(inp) if wq is None else wq
-    W = {k: dequantize(v["codes"], v["scale"]) for k, v in wq.items()}
+    w_qkv = dequantize(wq["w_qkv"]["codes"], wq["w_qkv"]["scale"])
+    w_o = dequantize(wq["w_o"]["codes"], wq["w_o"]["scale"])
     x = ol._tokens(inp["x"], cfg)
-    b = {k: ol._w(inp, k) for k in ("b_qkv", "b_o", "b_fc1", "b_fc2")}
-
+    b_qkv, b_o = ol._w(inp, "b_qkv"), ol._w(inp, "b_o")
     xn = ol.apply_norm(cfg, x, ol._w(inp, "norm1_w"), ol._w(inp, "norm1_b"))
-    xq = _qdq(xn, s_xn)
+    xq = _cast("xn", xn, s_xn)
     qw, kw = nh * d, ng * d
-    bq = None if b["b_qkv"] is None else b["b_qkv"][:qw]
-    bk = None if b["b_qkv"] is None else b["b_qkv"][qw:qw + kw]
-    bv = None if b["b_qkv"] is None else b["b_qkv"][qw + kw:]
-    q = ol.linear(xq[rows], W["w_qkv"][:qw], bq).reshape(len(rows), nh, d)
-    k = ol.linear(xq, W["w_qkv"][qw:qw + kw], bk).reshape(T, ng, d)
-    v = ol.linear(xq, W["w_qkv"][qw + kw:], bv).reshape(T, ng, d)
+    bq = None if b_qkv is None else b_qkv[:qw]
+    bk = None if b_qkv is None else b_qkv[qw:qw + kw]
+    bv = None if b_qkv is None else b_qkv[qw + kw:]
+    q = ol.linear(xq[rows], w_qkv[:qw], bq).reshape(len(rows), nh, d)
+    k = ol.linear(xq, w_qkv[qw:qw + kw], bk).reshape(T, ng, d)
+    v = ol.linear(xq, w_qkv[qw + kw:], bv).reshape(T, ng, d)
     if cfg.rope_base > 0:
         cq, sq = ol.rope_cos_sin(rows // B, d, cfg.rope_base)
         ck, sk = ol.rope_cos_sin(np.arange(T) // B, d, cfg.rope_base)
         q, k = ol.rope(q, cq, sq), ol.rope(k, ck, sk)
+    if storage_rounding:
+        q, k, v = round_bf16(q), round_bf16(k), round_fp16(v)
     o = np.empty((len(rows), nh, d))
     for bb in range(B):
         sel = np.nonzero(rows % B == bb)[0]
         if len(sel):
             o[sel] = ol.causal_attention(q[sel], k[bb::B], v[bb::B], rows[sel] // B)
     o = o.reshape(len(rows), qw)
-    h = x[rows] + ol.linear(_qdq(o, s_o), W["w_o"], b["b_o"])
+    h = x[rows] + ol.linear(_cast("o", o, s_o), w_o, b_o)
+    return {"xn": xn[rows], "o": o, "h": h}
+
+
+def mlp_block_fp8(cfg, inp: Dict, act_scales, h: np.ndarray, wq: Optional[Dict] = None) -> Dict[str, np.ndarray]:
+    """MLP half of the FP8 layer at TP=1 from h [n, H]: hn = Norm2(h) cast to E4M3, fc1, SwiGLU /
+    GeLU, the hidden a cast to E4M3, fc2; y = h + Y_mlp + b_fc2 (float64)."""
+    s_hn, s_a = np.float32(act_scales[2]), np.float32(act_scales[3])
+    wq = quantize_weights(inp) if wq is None else wq
+    w_fc1 = dequantize(wq["w_fc1"]["codes"], wq["w_fc1"]["scale"])
+    w_fc2 = dequantize(wq["w_fc2"]["codes"], wq["w_fc2"]["scale"])
     hn = ol.apply_norm(cfg, h, ol._w(inp, "norm2_w"), ol._w(inp, "norm2_b"))
-    u = ol.linear(_qdq(hn, s_hn), W["w_fc1"], b["b_fc1"])
+    u = ol.linear(_cast("hn", hn, s_hn), w_fc1, ol._w(inp, "b_fc1"))
     a = ol.activation(cfg, u)
-    y = h + ol.linear(_qdq(a, s_a), W["w_fc2"], b["b_fc2"])
-    amax = {"xn": np.max(np.abs(xn[rows])), "o": np.max(np.abs(o)), "hn": np.max(np.abs(hn)), "a": np.max(np.abs(a))}
-    return {"y": y, "h": h, "amax": amax}
+    y = h + ol.linear(_cast("a", a, s_a), w_fc2, ol._w(inp, "b_fc2"))
+    return {"hn": hn, "a": a, "y": y}
+
+
+def layer_forward_fp8(cfg, inp: Dict, act_scales, rows: Optional[np.ndarray] = None,
+                      wq: Optional[Dict] = None, storage_rounding: bool = False) -> Dict[str, np.ndarray]:
+    """Whole layer at TP=1 with the four GEMMs on E4M3 operands.
+
+    act_scales: fp32 scales of (xn, o, hn, a).  Weights use quantize_weight (or the precomputed
+    `wq` of quantize_weights(inp)).  storage_rounding: the stored intermediates q, k (bf16), v (fp16)
+    and h (bf16) are rounded as the kernels store them (see attention_block_fp8).  Returns y and h
+    for `rows` (all tokens if None) and the amax of each activation over those rows.
+    """
+    wq = quantize_weights(inp) if wq is None else wq
+    att = attention_block_fp8(cfg, inp, act_scales, rows=rows, wq=wq, storage_rounding=storage_rounding)
+    h = round_bf16(att["h"]) if storage_rounding else att["h"]
+    mlp = mlp_block_fp8(cfg, inp, act_scales, h, wq=wq)
+    amax = {"xn": np.max(np.abs(att["xn"])), "o": np.max(np.abs(att["o"])), "hn": np.max(np.abs(mlp["hn"])),
+            "a": np.max(np.abs(mlp["a"]))}
+    return {"y": mlp["y"], "h": h, "amax": amax}

@@ -160,6 +160,23 @@ def test_gemm_plan_of_the_ksplit_test_layers(lib):
     assert ks(2560, 2048, 2048, 0) == 4      # TP = 2 rank's fc2 partial (K = 2048 per rank)
 
 
+def test_gemm_plan_of_the_backward_ksplit_layers(lib):
+    """The weight-gradient GEMMs of the GPU backward tests' K-split layers (dW [out, in] = dY^T X,
+    K = the 2048 or 2064 tokens) are single partial waves cut into 4 ranges of K, and so are the
+    Llama-3-8B-shaped layer's dW of QKV (tail 4 tiles); its output projection's dW (tail 28 tiles)
+    takes 2.  Planning does not depend on the operands' layout."""
+    ks = lambda M, N, K: ml.mt_gemm_plan(M, N, K, 0)["ksplit"]
+    for T in (2048, 2064):
+        assert ks(512, 1024, T) == 4     # dW_fc2 (hidden 512, ffn 1024)
+        assert ks(2048, 512, T) == 4     # dW_fc1, SwiGLU rows
+        assert ks(512, 512, T) == 4      # dW_o
+        assert ks(768, 512, T) == 4      # dW_qkv, 8 x 64 heads over 2 groups
+    assert ks(1000, 512, 2064) == 4      # dW_fc1, GeLU ffn 1000 of the ragged layer
+    assert ks(512, 1000, 2064) == 4      # dW_fc2
+    assert ks(6144, 4096, 4096) == 4     # Llama-3-8B dW_qkv
+    assert ks(4096, 4096, 4096) == 2     # Llama-3-8B dW_o
+
+
 def _with_tail_split(mode, fn):
     ml.mt_gemm_set_tail_split(mode)
     try:

@@ -76,3 +76,16 @@ def test_dense_convention_counts_the_whole_score_square():
     assert round(dense / 1e9, 1) == 2061.6
     rank = synth.CONFIGS["llama70b_tp8"]                # one rank of eight: its own heads only
     assert bench.dense_convention_flops(rank) == rank.gemm_flops() + 4.0 * 128 * 4096 * 4096 * 8
+
+
+def test_rank_shapes_match_the_sharded_host_inputs():
+    """The device-drawn inputs of the bench's other workloads have the shapes of one rank's shard
+    of the seeded host inputs (absent tensors absent)."""
+    for name in ("tiny", "gpt345m", "llama70b_tp8"):
+        cfg = synth.CONFIGS[name]
+        small = cfg.replace(hidden=64, heads=cfg.tp * 2, groups=cfg.tp, head_dim=cfg.head_dim, ffn=cfg.tp * 16,
+                            seq=8, batch=1)
+        inp = synth.make_inputs(small, seed=0)
+        shard = synth.shard_weights(small, inp, small.tp, 0) if small.tp > 1 else inp
+        want = {k: v.shape for k, v in shard.items() if v is not None and k != "x"}
+        assert bench.rank_shapes(small) == want, name

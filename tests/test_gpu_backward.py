@@ -29,6 +29,17 @@ def assert_grad_close(got, want, what):
     assert rel < 2e-2, f"{what}: relative Frobenius error {rel:.3e}"
 
 
+# Shapes whose weight-gradient GEMMs (dW = dY^T X: K = T tokens, both operands read MN-major) take
+# the layer handle's K-split tail: with K = 2048 or 2064 tokens every dW GEMM of these small layers
+# is a single partial wave, cut into 4 ranges of K (tests/test_abi.py pins the plan); the second
+# has a ragged last K block (T = 2064) and batch 2.
+KSPLIT_CFGS = [
+    synth.LayerConfig("bw_ksplit", batch=1, seq=2048, hidden=512, heads=8, groups=2, head_dim=64, ffn=1024,
+                      rope_base=1e4, bias=True),
+    synth.LayerConfig("bw_ksplit_ragged", batch=2, seq=1032, hidden=512, heads=4, groups=1, head_dim=128,
+                      ffn=1000, norm="layer", act="gelu_tanh", rope_base=0.0, bias=True),
+]
+
 CFGS = [
     synth.CONFIGS["tiny"],
     synth.LayerConfig("bw_gqa", batch=2, seq=128, hidden=256, heads=8, groups=2, head_dim=64, ffn=512,
@@ -40,8 +51,11 @@ CFGS = [
 ]
 
 
-@pytest.mark.parametrize("cfg", CFGS, ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", CFGS + KSPLIT_CFGS + [synth.CONFIGS["llama8b"]], ids=lambda c: c.name)
 def test_backward_matches_oracle(cfg):
+    """Every element of dx and of the twelve weight gradients; the Llama-3-8B-shaped layer at its
+    full size (4096 tokens) is the benchmarked backward, whose dW GEMMs for the output projection
+    and QKV take K-split tails."""
     inp = synth.make_inputs(cfg, seed=81, affine="random", biases="random")
     T, H = cfg.tokens, cfg.hidden
     dy_bits = synth.f32_to_bf16_bits(np.random.default_rng(82).standard_normal((T, H)).astype(np.float32))
@@ -53,14 +67,20 @@ def test_backward_matches_oracle(cfg):
     dl.layer.backward(x, dy, cfg.seq, cfg.batch, dl.w, dx, grads)
     torch.cuda.synchronize()
     dl.layer.status()
+    got = {"x": to_f64(dx)}
+    got.update({k: (None if t is None else to_f64(t)) for k, t in grads.items()})
+    dl.close()
+    del x, dy, dx, grads
+    torch.cuda.empty_cache()
     want = ob.layer_backward(cfg, inp, ol.bf16_to_f64(dy_bits))
-    assert_grad_close(to_f64(dx), want["x"], "dx")
-    for name, t in grads.items():
+    assert_grad_close(got["x"], want["x"], "dx")
+    for name, t in got.items():
+        if name == "x":
+            continue
         if t is None:
             assert want[name] is None, name
             continue
-        assert_grad_close(to_f64(t), want[name], name)
-    dl.close()
+        assert_grad_close(t, want[name], name)
 
 
 def test_backward_rejects_unsupported():

@@ -2,16 +2,21 @@
 
 * mt_quantize_e4m3 (current scaling of a weight) gives exactly the oracle's codes and factors.
 * mt_gemm_e4m3 on seeded random codes matches the exact product (fp32 accumulation, bf16 out).
-* mt_layer_forward_fp8 with given activation scales: the first quantised activation (normed x) has
-  the oracle's codes; the output matches oracle.fp8.layer_forward_fp8 within the FP8 tolerance
-  below; and the delayed-scaling history yields scale = 448 / max(history) after each call.
+* mt_layer_forward_fp8 with given activation scales, stage by stage (tests/fp8_check.py): the
+  codes of all four quantised activations (normed x, attention output, normed h, MLP hidden),
+  each against the oracle's codes of the same values; the stored h against the oracle's attention
+  block; y against the oracle's MLP block run from the GPU's own h.  A quantised code is an integer
+  decided by floating point, so the oracle takes the kernels' storage precision for the stored
+  intermediates the codes depend on (q, k bf16, v fp16, h bf16), and the MLP stage starts from the
+  h the GPU stored.  The delayed-scaling history yields scale = 448 / max(history) after each call.
 
-FP8 tolerance.  Two FP8 computations of the same layer whose inputs to a cast differ by bf16
-rounding (the GPU keeps q, k, v and h in bf16, the oracle in float64) round some values to
-neighbouring E4M3 codes, 6-12% apart, so their outputs scatter by up to the FP8 method's own
-deviation from the exact layer.  The bar is therefore, element by element,
+Whole-layer tolerance as well.  Two FP8 computations whose inputs to a cast differ by bf16
+rounding round some values to neighbouring E4M3 codes, 6-12% apart, so y is also checked element
+by element against the end-to-end FP8 oracle within
     |gpu - oracle_fp8| <= 2e-2 max|oracle_fp8| + 1e-3 + |oracle_fp8 - oracle_exact|_max,
 and the GPU result may be no further from the exact layer than 1.5x the oracle FP8 result is.
+That bound alone would not notice a skipped cast (y is dominated by the residual); the stage
+checks would (the CPU tests plant each skipped cast in the oracle and see them fail).
 """
 import numpy as np
 import pytest
@@ -21,6 +26,7 @@ import synth
 from oracle import fp8 as of
 from oracle import layer as ol
 from megatron_tensor_transformer_gpt_gb300 import mt_layer as ml
+from tests import fp8_check as fc
 from tests.gpu_util import DeviceLayer, assert_layer_close, sample_rows, to_dev, to_f64
 
 pytestmark = pytest.mark.gpu
@@ -110,10 +116,35 @@ def check_first_codes(f8, cfg, inp, scales):
     T, H = cfg.tokens, cfg.hidden
     xn8 = f8.dl.layer.region(cfg.seq, cfg.batch, "xn")[: T * H].view(T, H).cpu().numpy()
     xn = ol.apply_norm(cfg, ol._tokens(inp["x"], cfg), ol._w(inp, "norm1_w"), ol._w(inp, "norm1_b"))
-    want = of.quantize(xn, np.float32(scales[0]))
-    got, want = (np.where(c == 0x80, 0, c) for c in (xn8, want))      # -0 and +0 are one value
-    step = np.abs(got.astype(np.int16) - want.astype(np.int16))      # same sign: code distance = ulps
-    assert (got != want).mean() < 1e-4 and step.max() <= 1
+    fc.assert_codes_close(xn8, of.quantize(xn, np.float32(scales[0])), 1e-4, "xn codes")
+
+
+def check_stages(f8, cfg, inp, scales, wq, y, rows=None):
+    """The attention output's codes and the stored h against the oracle's attention block; the codes
+    of normed h and of the MLP hidden, and y, against the oracle's MLP block from the GPU's own h."""
+    T, H, S, B = cfg.tokens, cfg.hidden, cfg.seq, cfg.batch
+    rows = np.arange(T) if rows is None else np.asarray(rows)
+    L = f8.dl.layer
+
+    def region(name, cols, dtype=torch.uint8):
+        t = L.region(S, B, name).view(dtype)[: T * cols].view(T, cols)
+        return t[torch.from_numpy(rows).to(t.device)].cpu()
+
+    s = [np.float32(v) for v in scales]
+    att = of.attention_block_fp8(cfg, inp, scales, rows=rows, wq=wq, storage_rounding=True)
+    fc.assert_codes_close(region("o", cfg.heads * cfg.head_dim).numpy(), of.quantize(att["o"], s[1]), 5e-2,
+                          "attention-output codes")
+    h = to_f64(region("h", H, torch.bfloat16))
+    fc.assert_attention_stage(h, att["h"], ol.layer_forward(cfg, inp, rows=rows)["h"], "attention stage")
+    hn = ol.apply_norm(cfg, h, ol._w(inp, "norm2_w"), ol._w(inp, "norm2_b"))
+    hn8 = region("hn", H).numpy()
+    fc.assert_codes_close(hn8, of.quantize(hn, s[2]), 1e-3, "normed-h codes")
+    w_fc1 = of.dequantize(wq["w_fc1"]["codes"], wq["w_fc1"]["scale"])
+    a = ol.activation(cfg, ol.linear(of.dequantize(hn8, s[2]), w_fc1, ol._w(inp, "b_fc1")))
+    fc.assert_codes_close(region("a", cfg.ffn).numpy(), of.quantize(a, s[3]), 1e-3, "MLP-hidden codes")
+    b_fc2 = ol._w(inp, "b_fc2")
+    y_exact = h + ol.mlp_partial(cfg, 1, h, inp) + (0.0 if b_fc2 is None else b_fc2)
+    fc.assert_mlp_stage(y, of.mlp_block_fp8(cfg, inp, scales, h, wq=wq)["y"], y_exact, "MLP stage")
 
 
 @pytest.mark.parametrize("cfg", [
@@ -134,8 +165,10 @@ def test_fp8_layer_matches_oracle(cfg):
     torch.cuda.synchronize()
     f8.dl.layer.status()
     check_first_codes(f8, cfg, inp, scales)
+    got = to_f64(y)
+    check_stages(f8, cfg, inp, scales, of.quantize_weights(inp), got)
     want = of.layer_forward_fp8(cfg, inp, scales)["y"]
-    assert_fp8_close(to_f64(y), want, ol.layer_forward(cfg, inp)["y"], f"fp8 layer {cfg.name}")
+    assert_fp8_close(got, want, ol.layer_forward(cfg, inp)["y"], f"fp8 layer {cfg.name}")
     f8.dl.close()
 
 
@@ -154,6 +187,7 @@ def test_fp8_layer_llama8b_sampled_rows():
     f8.dl.layer.status()
     check_first_codes(f8, cfg, inp, scales)
     got = to_f64(y[torch.from_numpy(rows).cuda()])
+    check_stages(f8, cfg, inp, scales, wq, got, rows=rows)
     f8.dl.close()
     assert_fp8_close(got, of.layer_forward_fp8(cfg, inp, scales, rows=rows, wq=wq)["y"],
                      ol.layer_forward(cfg, inp, rows=rows)["y"], "fp8 llama8b")

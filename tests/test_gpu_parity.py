@@ -1,8 +1,9 @@
 """GPU parity: the CUDA path (through the C ABI) against the float64 CPU oracle on the same seeded inputs.
 
 Tolerance (the layer's): |gpu - oracle| <= 2e-2 * max|oracle| + 1e-3 elementwise, bf16 inputs,
-fp32 accumulation.  Small cases compare every element; the full-size workloads compare sampled
-rows that the oracle computes one by one (K and V for every token, the rest for the sampled rows).
+fp32 accumulation.  Small cases, the Llama-3-8B-shaped layer and the eight summed shards of the
+70B-shaped TP = 8 layer compare every element; the 32k-token layer compares sampled rows that the
+oracle computes one by one (K and V for every token, the rest for the sampled rows).
 """
 import numpy as np
 import pytest
@@ -152,9 +153,12 @@ def test_tp_shards_sum_to_the_unsharded_layer(tp):
     assert_layer_close(to_f64(y), ol.layer_forward_tp_sum(cfg, tp, inp["x"], shards)["y"], "y vs oracle TP sum")
 
 
-def test_rank_identity_mode():
-    cfg = small(heads=8, groups=4, ffn=1024)
-    inp = synth.make_inputs(cfg, seed=10, affine="random")
+@pytest.mark.parametrize("bias", [False, True], ids=["no-bias", "biases"])
+def test_rank_identity_mode(bias):
+    """One rank with the all-reduce replaced by the identity: h = x + Y_attn,i + b_o (b_o once) and
+    y_partial = Y_mlp,i(h) without residual or b_fc2; with random biases on every linear."""
+    cfg = small(heads=8, groups=4, ffn=1024, bias=bias)
+    inp = synth.make_inputs(cfg, seed=10, affine="random", biases="random")
     tp, r = 4, 1
     dl = DeviceLayer(cfg, inp, tp, r)
     y = dl.forward(to_dev(inp["x"]).reshape(cfg.tokens, cfg.hidden))
@@ -168,6 +172,22 @@ def test_rank_identity_mode():
 
 
 # ----------------------------------------------------------------------------------- full-size workloads
+def test_llama8b_full_size_every_row():
+    """The Llama-3-8B-shaped layer at its full size (4096 tokens), every element of y against the
+    oracle's whole layer."""
+    cfg = synth.CONFIGS["llama8b"]
+    inp = synth.make_inputs(cfg, seed=0)
+    dl = DeviceLayer(cfg, inp)
+    y = dl.forward(to_dev(inp["x"]).reshape(cfg.tokens, cfg.hidden))
+    torch.cuda.synchronize()
+    dl.layer.status()
+    got = to_f64(y)
+    dl.close()
+    del y
+    torch.cuda.empty_cache()
+    assert_layer_close(got, ol.layer_forward(cfg, inp)["y"], "llama8b, all rows")
+
+
 def _full_size_sampled(name, n_random):
     cfg = synth.CONFIGS[name]
     inp = synth.make_inputs(cfg, seed=0)
@@ -183,25 +203,24 @@ def _full_size_sampled(name, n_random):
     assert_layer_close(got, ol.layer_forward(cfg, inp, rows=rows)["y"], name)
 
 
-def test_llama8b_full_size_sampled_rows():
-    _full_size_sampled("llama8b", 192)
-
-
 def test_llama8b_32k_full_size_sampled_rows():
     _full_size_sampled("llama8b_32k", 128)
 
 
 def test_llama70b_tp8_all_shards_sum_to_unsharded_oracle():
+    """The eight TP = 8 ranks of the 70B-shaped layer, run one after another; their row-parallel
+    partials summed (fp32) give h and y, compared on every row with the unsharded oracle layer."""
     cfg = synth.CONFIGS["llama70b_tp8"]
     inp = synth.make_inputs(cfg, seed=0)
     x = to_dev(inp["x"]).reshape(cfg.tokens, cfg.hidden)
     h, y = tp_sum_on_device(cfg, inp, x, cfg.tp)
     torch.cuda.synchronize()
-    rows = sample_rows(cfg.tokens, seed=2, n_random=32)
-    got = to_f64(y[torch.from_numpy(rows).cuda()])
-    del h, y
+    got_h, got_y = to_f64(h), to_f64(y)
+    del h, y, x
     torch.cuda.empty_cache()
-    assert_layer_close(got, ol.layer_forward(cfg, inp, rows=rows)["y"], "llama70b tp8 summed")
+    want = ol.layer_forward(cfg, inp)
+    assert_layer_close(got_h, want["h"], "llama70b tp8 summed h")
+    assert_layer_close(got_y, want["y"], "llama70b tp8 summed y")
 
 
 def test_llama70b_tp8_one_rank_identity_mode():

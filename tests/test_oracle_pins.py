@@ -256,14 +256,47 @@ def test_row_split_sum_of_partials_reproduces_tp1(tp):
     np.testing.assert_allclose(ol.layer_forward_tp_sum(cfg, tp, inp["x"], shards)["y"], full, rtol=1e-11, atol=1e-12)
 
 
-def test_rank_identity_mode_definition():
-    cfg = small_cfg(groups=2)
-    inp = synth.make_inputs(cfg, seed=7)
-    sh = synth.shard_weights(cfg, inp, 2, 1)
-    out = ol.layer_forward_rank_identity(cfg, 2, inp["x"], sh)
+def test_rank_identity_at_tp1_is_the_layer_without_its_mlp_residual_and_bias():
+    """At tp = 1 the identity-mode rank is the whole layer: its h is the layer's h (b_o added once)
+    and its y_partial is y - h - b_fc2 (the fc2 partial carries neither the residual nor the bias)."""
+    cfg = small_cfg(groups=2, bias=True, norm="layer", act="gelu_tanh")
+    inp = synth.make_inputs(cfg, seed=7, affine="random", biases="random")
+    out = ol.layer_forward_rank_identity(cfg, 1, inp["x"], inp)
+    full = ol.layer_forward(cfg, inp)
+    np.testing.assert_allclose(out["h"], full["h"], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(out["y_partial"], full["y"] - full["h"] - ol.bf16_to_f64(inp["b_fc2"]),
+                               rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("tp", [2, 4])
+def test_rank_identity_h_carries_b_o_once_per_rank(tp):
+    """Each identity-mode rank forms h_r = x + Y_attn,r + b_o, so over the ranks
+    sum_r (h_r - x - b_o) is the row-parallel sum sum_r Y_attn,r = h - x - b_o of the unsharded
+    layer.  A rank that dropped b_o or added it twice breaks this by b_o per rank."""
+    cfg = small_cfg(groups=4, bias=True)
+    inp = synth.make_inputs(cfg, seed=17, affine="random", biases="random")
     x = ol._tokens(inp["x"], cfg)
-    np.testing.assert_allclose(out["h"], x + ol.attn_partial(cfg, 2, x, sh), rtol=1e-14)
-    np.testing.assert_allclose(out["y_partial"], ol.mlp_partial(cfg, 2, out["h"], sh), rtol=1e-14)
+    b_o = ol.bf16_to_f64(inp["b_o"])
+    acc = sum(ol.layer_forward_rank_identity(cfg, tp, inp["x"], synth.shard_weights(cfg, inp, tp, r))["h"] - x - b_o
+              for r in range(tp))
+    np.testing.assert_allclose(acc, ol.layer_forward(cfg, inp)["h"] - x - b_o, rtol=1e-10, atol=1e-12)
+    assert np.max(np.abs(b_o)) > 1e-3   # the check above is sensitive to b_o
+
+
+@pytest.mark.parametrize("tp", [2, 4])
+def test_rank_identity_y_partials_sum_when_every_rank_sees_the_same_h(tp):
+    """With W_o = 0 every rank's h_r is x + b_o, the unsharded layer's h; the ranks' y_partial then
+    sum to the row-parallel MLP output y - h - b_fc2 of the unsharded layer."""
+    cfg = small_cfg(groups=4, bias=True, norm="layer")
+    inp = dict(synth.make_inputs(cfg, seed=18, affine="random", biases="random"))
+    inp["w_o"] = np.zeros_like(inp["w_o"])
+    full = ol.layer_forward(cfg, inp)
+    parts = [ol.layer_forward_rank_identity(cfg, tp, inp["x"], synth.shard_weights(cfg, inp, tp, r))
+             for r in range(tp)]
+    for p in parts:
+        np.testing.assert_allclose(p["h"], full["h"], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(sum(p["y_partial"] for p in parts), full["y"] - full["h"] - ol.bf16_to_f64(inp["b_fc2"]),
+                               rtol=1e-10, atol=1e-12)
 
 
 def test_row_sampling_matches_full_layer():

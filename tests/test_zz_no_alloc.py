@@ -1,16 +1,19 @@
-"""The allocation-free entry point (mt_layer_forward_static) against the handle-based forward.
+"""The allocation-free entry point (mt_layer_forward_static) against the float64 oracle and the
+handle-based forward.
 
 Some callers cannot call cudaMalloc (code inside a host framework whose allocator owns all device
 memory, real-time or embedded callers that forbid device allocation after start-up); the static
 variant keeps its scratch in a fixed area inside the library instead of a caller-lent workspace.
-This file is collected last so that a failure here comes after every other test has run; it also
-passes on its own in a fresh process.
+After its first call on a device (which looks up the area's address and loads its kernels), a
+call must leave the device's free memory unchanged.  This file is collected last so that a
+failure here comes after every other test has run; it also passes on its own in a fresh process.
 """
 import numpy as np
 import pytest
 import torch
 
 import synth
+from oracle import layer as ol
 from megatron_tensor_transformer_gpt_gb300 import mt_layer as ml
 from tests.gpu_util import DeviceLayer, assert_layer_close, to_dev, to_f64
 
@@ -31,19 +34,29 @@ def _static_forward(cfg, dl, x, y):
     synth.CONFIGS["tiny"],
     synth.LayerConfig("small_ln_gelu", batch=2, seq=100, hidden=512, heads=8, groups=2, head_dim=64, ffn=1000,
                       norm="layer", act="gelu_tanh", rope_base=0.0, bias=True),
+    synth.LayerConfig("gqa_d128_rope", batch=1, seq=200, hidden=512, heads=8, groups=2, head_dim=128, ffn=1024,
+                      rope_base=5e5, bias=True),
 ], ids=lambda c: c.name)
-def test_static_forward_matches_handle_forward_on_two_calls(cfg):
+def test_static_forward_matches_oracle_and_handle_on_two_calls(cfg):
     torch.cuda.set_device(0)
     inp = synth.make_inputs(cfg, seed=31, affine="random", biases="random")
     dl = DeviceLayer(cfg, inp)
     assert dl.layer.workspace(cfg.seq, cfg.batch).numel() <= STATIC_BYTES - 1024
     x = to_dev(inp["x"]).reshape(cfg.tokens, cfg.hidden)
-    want = to_f64(dl.forward(x))
-    for _ in range(2):
-        y = torch.full((cfg.tokens, cfg.hidden), float("nan"), dtype=torch.bfloat16, device="cuda")
+    handle_y = to_f64(dl.forward(x))
+    oracle_y = ol.layer_forward(cfg, inp)["y"]
+    ys = [torch.full((cfg.tokens, cfg.hidden), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    _static_forward(cfg, dl, x, ys[0])  # first call: address lookup and kernel loading
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for y in ys[1:]:
         _static_forward(cfg, dl, x, y)
         torch.cuda.synchronize()
-        assert_layer_close(to_f64(y), want, f"static forward ({cfg.name})")
+        assert torch.cuda.mem_get_info()[0] == free0, "a static call changed the device's free memory"
+    for y in ys:
+        got = to_f64(y)
+        assert_layer_close(got, oracle_y, f"static forward vs oracle ({cfg.name})")
+        assert_layer_close(got, handle_y, f"static forward vs handle forward ({cfg.name})")
     dl.close()
 
 
