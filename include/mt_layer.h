@@ -227,7 +227,8 @@ int mt_layer_workspace_region(const mt_layer* L, int seq, int batch, int which, 
  * since the last call (MT_ERR_DEVICE_TIMEOUT, or MT_ERR_INVALID_ARG for inconsistent packed
  * cu_seqlens), clearing it (and, after a failure, the K-split arrival counters, which a launch
  * that gave up may have left counted).  The error word is read through the handle's copy stream,
- * so no device-wide synchronisation happens.  Host call. */
+ * so no device-wide synchronisation happens.  Calls captured into a CUDA graph are not waited for:
+ * synchronise the stream that launches the graph first.  Host call. */
 int mt_layer_status(mt_layer* L);
 
 /* Thread-local description of the last failure on this thread ("" after success). */

@@ -80,7 +80,14 @@ int cuda_fail(cudaError_t e, const char* what) {
 }
 
 // Successful end of a call that queued work on `st`: marks the point mt_layer_status waits for.
+// A call captured into a CUDA graph marks nothing (its work runs when the graph is launched).
 int done(mt_layer* L, cudaStream_t st) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) {
+    cudaGetLastError();  // the legacy stream cannot be queried while another stream captures
+    return ok();
+  }
+  if (cap != cudaStreamCaptureStatusNone) return ok();
   cudaError_t e = cudaEventRecord(L->done_ev, st);
   if (e != cudaSuccess) return cuda_fail(e, "recording the end of the call");
   L->done_pending = true;

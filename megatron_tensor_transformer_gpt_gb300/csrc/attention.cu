@@ -6,9 +6,9 @@
 // pages name: exact attention computed block by block with an online softmax, O(S) memory.)
 //
 // Three forms share one scheme, chosen by launch_attention from d and the heads per kv group:
-//   attn2_kernel<D, false>  an even number of heads per group: one CTA takes two heads of one group
+//   attn_tp_kernel<D>       an even number of heads per group: one CTA takes two heads of one group
 //                           for a 128-query block, so every K/V tile feeds both (all GQA/MQA
-//                           workloads);
+//                           workloads); P stays in tensor memory;
 //   attn2_kernel<64, true>  d = 64 with an odd number of heads per group (MHA): two heads of two
 //                           groups, each ring slot holding both groups' tiles;
 //   attn_kernel<D>          otherwise (MHA at d = 128, or an odd number of heads): one head per CTA.
@@ -16,10 +16,10 @@
 // loads the Q tile(s) and then K and V tiles [128 keys x d] by TMA; one thread of warp 1 issues
 // S_j = Q K_j^T into a TMEM score buffer and O += P_j V_j into a TMEM accumulator, reading V as an
 // MN-major operand (its d index contiguous); the softmax warps (one query row per thread) read S_j
-// from TMEM and release it at once, mask the diagonal block, keep a running maximum and sum in the
-// log2 domain, write P_j = 2^(s c - m) as fp16 into shared memory in the 128-byte-swizzled layout the
-// MMA reads, and rescale O in TMEM only when the running maximum grows by more than 2^8 (between
-// rescales P stays below 256).  At the end O / l is written as bf16 (or E4M3) to o[t, h*d + i] and,
+// from TMEM, mask the diagonal block, keep a running maximum and sum in the log2 domain, write
+// P_j = 2^(s c - m) as fp16 (into shared memory in the 128-byte-swizzled layout the MMA reads, or,
+// in attn_tp_kernel, over S_j in tensor memory), and rescale O in TMEM only when the running
+// maximum grows by more than 2^8 (between rescales P stays below 256).  At the end O / l is written as bf16 (or E4M3) to o[t, h*d + i] and,
 // when asked, m + log2(l) to lse for the backward pass.
 #include <math.h>
 
@@ -349,10 +349,9 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
-// ------------------------------------------------------------------ two heads of one group per CTA
-// The variant used when each kv group serves an even number of query heads (GQA/MQA): the CTA
-// holds the Q tiles of two heads of the same group for one 128-row query block, so every K/V tile
-// it loads feeds both (half the K/V traffic of one head per CTA).
+// ------------------------------------------------------------------ two heads per CTA, P in shared memory
+// The form used for MHA at d = 64 (two heads of two groups, TG); attn_tp_kernel below replaces it
+// for two heads of one group.  The CTA holds the Q tiles of two heads for one 128-row query block.
 //   TMEM: head t's scores S_t in columns [256t, 256t+128) and its output O_t in [256t+128, +d).
 //   The softmax warps of a head read S_t into registers and release it at once (s_free), so the
 //   tensor core computes S_t(j+1) while they turn S_t(j) into P_t(j); P goes to shared memory (fp16,
@@ -524,8 +523,7 @@ struct Geo2 {
   static constexpr uint32_t IDESC_S = idesc_bf16(BQ, BKV);
   static constexpr uint32_t IDESC_O = idesc_f16(BQ, D) | (1u << 16);  // fp16 P (K-major), fp16 V (MN-major)
 };
-static_assert(Geo2<128>::SMEM_USED <= 232448 && Geo2<64, true>::SMEM_USED <= 232448,
-              "attention tiles exceed the shared memory of a CTA");
+static_assert(Geo2<64, true>::SMEM_USED <= 232448, "attention tiles exceed the shared memory of a CTA");
 
 template <int D, bool TG>
 __global__ void __launch_bounds__(320, 1)
@@ -714,6 +712,321 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
+// ------------------------------------------------------------------ two heads of one group, P in TMEM
+// The variant for an even number of query heads per kv group (GQA/MQA), with the probabilities kept
+// in tensor memory: the softmax warps of head t write P_t(j) (fp16) over the first 64 columns of
+// S_t(j), which they have read into registers, and O_t += P_t(j) V_j takes P as its A operand from
+// tensor memory.  No shared-memory P tile and no generic-to-async proxy fence; the freed shared
+// memory holds a deeper ring of K and V tiles (NS slots, loaded K0, V0, K1, V1, ... in the order
+// the MMAs use them).
+//   TMEM: head t's S_t (and P_t) in columns [256t, 256t+128), O_t in [256t+128, 256t+128+d).
+//   MMA order: S_A(0), S_B(0); then per key block j: P_A V_j, S_A(j+1), P_B V_j, S_B(j+1).  The
+//   MMAs of one thread run in issue order, so S_t(j+1) overwrites S_t's columns only after
+//   P_t(j) V_j has read P_t(j) from them; the softmax of one head runs while the tensor core
+//   works on the other head's pair of products.  One barrier per head (s_full) completes after
+//   S_t(j) -- and so also after P_t(j-1) V_{j-1}, which makes O_t stable for a rescale -- and, one
+//   block after the last, when O_t is final; p_full tells the MMA thread that P_t(j) is written
+//   (and any rescale of O_t done).
+template <int D>
+struct GeoT {
+  static constexpr int ATOM = 128 * 128;          // [128 rows x 64 bf16] swizzle block, 16 KB
+  static constexpr int Q_BYTES = BQ * D * 2;      // per head
+  static constexpr int KV_BYTES = BKV * D * 2;    // one K or V tile [128 keys x d]
+  static constexpr int NS = D == 128 ? 5 : 8;     // ring slots
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = 2 * Q_BYTES;
+  static constexpr int OFF_BAR = OFF_KV + NS * KV_BYTES;
+  static constexpr size_t SMEM_USED = 1024 + OFF_BAR + 256;
+  static constexpr size_t SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;  // one CTA per SM (TMEM)
+  static constexpr uint32_t IDESC_S = idesc_bf16(BQ, BKV);
+  static constexpr uint32_t IDESC_O = idesc_f16(BQ, D) | (1u << 16);  // fp16 P (K-major), fp16 V (MN-major)
+};
+static_assert(GeoT<128>::SMEM_USED <= 232448 && GeoT<64>::SMEM_USED <= 232448,
+              "attention tiles exceed the shared memory of a CTA");
+
+// Softmax of one head (four warps, one query row per thread) for attn_tp_kernel: per key block it
+// waits for S, masks the diagonal block, forms P = 2^(s c - m) as fp16 pairs, rescales O when the
+// running maximum grew by more than 2^8, writes P over S's first 64 columns and signals p_full.
+template <int D>
+__device__ __forceinline__ void softmax_head_tm(const AttnParams& p, const Work& wk, int h, int quad, int lane,
+                                                uint32_t tS, uint32_t tO, uint32_t s_full, uint32_t p_full,
+                                                volatile int* abort_flag) {
+  const int qb = wk.qb, b = wk.b, nkv = qb + 1;
+  const int r = quad * 32 + lane;
+  const bool row_ok = qb * BQ + r < wk.len;  // inside its sequence
+  const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+  const float c = p.scale_log2;
+  float m_used = -INFINITY, l = 0.f;
+  bool ok = true;
+  for (int j = 0; j < nkv; ++j) {
+    const bool w = mbar_wait(s_full, j & 1, p.err, abort_flag);
+    if (!__all_sync(0xffffffffu, w)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    float s[BKV];
+    tmem_ld128(tS + lane_off, s);
+    if (j == qb) {  // diagonal block: key j*128+i visible iff i <= r
+#pragma unroll
+      for (int i = 0; i < BKV; ++i)
+        if (i > r) s[i] = -INFINITY;
+    }
+    const float mx = row_max(s);
+    const float m_new = fmaxf(m_used, mx * c);
+    const bool grow = __any_sync(0xffffffffu, m_new > m_used + 8.0f);
+    float alpha = 1.f;
+    if (grow) {
+      alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m_used - m_new);
+      m_used = m_new;
+    }
+    // P = 2^(s c - m) in packed halves (one fp32x2 FMA, one fp16x2 conversion and one fp16x2
+    // exponential per pair of scores; the argument is at most 8 after the lazy rescaling); row sums
+    // in four fp16x2 partial sums per 64 keys, widened to fp32 once per block.
+    uint32_t pk[BKV / 2];
+    float rs = 0.f;
+    {
+      const float2 cc = make_float2(c, c), mm = make_float2(-m_used, -m_used);
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        __half2 acc[4] = {__float2half2_rn(0.f), __float2half2_rn(0.f), __float2half2_rn(0.f),
+                          __float2half2_rn(0.f)};
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          const int i = 64 * hf + 2 * q;
+          const float2 xy = ffma2(make_float2(s[i], s[i + 1]), cc, mm);
+          pk[32 * hf + q] = ex2_f16x2(pack_f16x2(xy.x, xy.y));
+          acc[q & 3] = __hadd2(acc[q & 3], *reinterpret_cast<const __half2*>(&pk[32 * hf + q]));
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = __half22float2(acc[k]);
+          rs += f.x + f.y;
+        }
+      }
+    }
+    l = l * alpha + rs;
+    if (grow && j > 0) {  // P(j-1) V_{j-1} has completed (it precedes S(j)): O is stable
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        float o[32];
+        tmem_ld32(tO + lane_off + cc * 32, o);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+        tmem_st32(tO + lane_off + cc * 32, o);
+      }
+    }
+    tmem_st64(tS + lane_off, pk);  // key 2i (low half) and 2i+1 of P in column i
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(p_full);
+  }
+  if (ok) {
+    const bool w = mbar_wait(s_full, nkv & 1, p.err, abort_flag);  // the last P V product is done
+    if (__all_sync(0xffffffffu, w)) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      const size_t orow = (static_cast<size_t>(wk.q_row0 + r) * p.batch + b) * p.ldo + h * D;
+      if (p.lse != nullptr && row_ok)
+        p.lse[(static_cast<size_t>(b) * p.nh + h) * p.seq + wk.q_row0 + r] = m_used + log2f(l);
+      const float qs = p.o8 != nullptr ? __ldg(p.q_scale) : 1.f;
+      float mx = 0.f;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        float o[32];
+        tmem_ld32(tO + lane_off + cc * 32, o);
+        if (row_ok) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= inv_l;
+          if (p.o8 != nullptr) {  // E4M3 output for the FP8 output projection
+#pragma unroll
+            for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(o[i]));
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              *reinterpret_cast<uint2*>(p.o8 + orow + cc * 32 + q4 * 8) = pack_e4m3x8(o + q4 * 8, qs);
+          } else {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              *reinterpret_cast<uint4*>(p.o + orow + cc * 32 + q4 * 8) = pack_bf16x8(o + q4 * 8);
+          }
+        }
+      }
+      if (p.o8 != nullptr) {
+        mx = warp_max(mx);
+        if (lane == 0) atomic_max_abs(p.amax, mx);
+      }
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    attn_tp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+  using G = GeoT<D>;
+  constexpr int NS = G::NS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + G::OFF_BAR);
+  // bars: q_full | kv_full[NS] | kv_empty[NS] | s_full[2] | p_full[2] | drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 6 + 2 * NS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  const uint32_t q_full = bar0;
+  // tile n of the load sequence (K_j = 2j, V_j = 2j + 1) sits in ring slot n % NS, in that slot's
+  // (n / NS)-th use
+  auto kv_full = [&](int n) { return bar0 + 8u * (1 + n % NS); };
+  auto kv_empty = [&](int n) { return bar0 + 8u * (1 + NS + n % NS); };
+  auto use_parity = [](int n) { return static_cast<uint32_t>((n / NS) & 1); };
+  auto s_full = [&](int t) { return bar0 + 8u * (1 + 2 * NS + t); };
+  auto p_full = [&](int t) { return bar0 + 8u * (3 + 2 * NS + t); };
+  const uint32_t drain = bar0 + 8u * (5 + 2 * NS);
+  auto sQa = [&](int t) { return smem_u32(base + G::OFF_Q + t * G::Q_BYTES); };
+  auto sKV = [&](int n) { return smem_u32(base + G::OFF_KV + (n % NS) * G::KV_BYTES); };
+
+  pdl_wait();  // q, k, v (and cu_seqlens) are written by the kernels before
+  pdl_trigger();
+  Work wk;
+  if (!decode_work(p, p.nh >> 1, 2, wk)) return;  // uniform over the CTA, before any barrier or TMEM use
+  const int qb = wk.qb, b = wk.b, h0 = wk.h;
+  const int g = h0 / (p.nh / p.ng);  // both heads' kv group (an even number of heads per group)
+  const int nkv = qb + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(kv_full(i), 1);
+      mbar_init(kv_empty(i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(s_full(i), 1);
+      mbar_init(p_full(i), 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(&tmQ);
+    tma_prefetch(&tmK);
+    tma_prefetch(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  auto tS = [&](int t) { return tmem_base + 256u * t; };
+  auto tO = [&](int t) { return tmem_base + 256u * t + 128u; };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, 2 * G::Q_BYTES);
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int a = 0; a < D / 64; ++a)
+          tma_load_3d(sQa(t) + a * G::ATOM, &tmQ, q_full, a * 64, wk.q_row0, b * p.nh + h0 + t);
+      int issued = 0;
+      bool ok = true;
+      for (int n = 0; ok && n < 2 * nkv; ++n) {
+        const CUtensorMap* map = (n & 1) ? &tmV : &tmK;
+        if (!mbar_wait(kv_empty(n), use_parity(n) ^ 1u, p.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(kv_full(n), G::KV_BYTES);
+#pragma unroll
+        for (int a = 0; a < D / 64; ++a)
+          tma_load_3d(sKV(n) + a * G::ATOM, map, kv_full(n), a * 64, wk.kv_row0 + (n >> 1) * BKV, b * p.ng + g);
+        ++issued;
+      }
+      if (!ok) {  // let this CTA's own copies in flight land
+        mbar_wait_slow(q_full, 0, nullptr, nullptr, kDrainLimitNs);
+        for (int n = issued - 1; n >= 0 && n >= issued - NS; --n)
+          mbar_wait_slow(kv_full(n), use_parity(n), nullptr, nullptr, kDrainLimitNs);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      auto issue_s = [&](int t, int n) {
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * G::ATOM + (k & 3) * 32;
+          mma_bf16_ss(tS(t), sw128_desc(sQa(t) + off), sw128_desc(sKV(n) + off), G::IDESC_S, k > 0 ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(q_full, 0, p.err, abort_flag) && mbar_wait(kv_full(0), use_parity(0), p.err, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        mma_commit(s_full(0));
+        issue_s(1, 0);
+        mma_commit(s_full(1));
+        mma_commit(kv_empty(0));
+      }
+      for (int j = 0; ok && j < nkv; ++j) {
+        const int nv = 2 * j + 1, nk = 2 * j + 2;  // tiles V_j and K_{j+1}
+        if (!mbar_wait(kv_full(nv), use_parity(nv), p.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (!mbar_wait(p_full(t), j & 1, p.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < BKV / 16; ++k)
+            mma_f16_ts(tO(t), tS(t) + 8u * k, sw128_desc_mn(sKV(nv) + k * 2048, G::ATOM), G::IDESC_O,
+                       (j > 0 || k > 0) ? 1u : 0u);
+          if (j + 1 < nkv) {
+            if (t == 0 && !mbar_wait(kv_full(nk), use_parity(nk), p.err, abort_flag)) {
+              ok = false;
+              break;
+            }
+            issue_s(t, nk);
+          }
+          mma_commit(s_full(t));
+        }
+        if (!ok) break;
+        mma_commit(kv_empty(nv));
+        if (j + 1 < nkv) mma_commit(kv_empty(nk));
+      }
+      mma_commit(drain);
+      mbar_wait_slow(drain, 0, nullptr, nullptr, ok ? kWaitLimitNs : kDrainLimitNs);
+    }
+  } else {
+    const int t = (warp - 2) >> 2;  // which head of the pair
+    softmax_head_tm<D>(p, wk, h0 + t, warp & 3, lane, tS(t), tO(t), s_full(t), p_full(t), abort_flag);
+  }
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_tp(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnParams& p,
+                      cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_tp_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(GeoT<D>::SMEM));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const unsigned grid = static_cast<unsigned>(p.num_qb) * (p.cu ? p.num_seqs : p.batch) * (p.nh / 2);
+  return launch_pdl(attn_tp_kernel<D>, dim3(grid), dim3(320), GeoT<D>::SMEM, stream, tmQ, tmK, tmV, p);
+}
+
 template <int D, bool TG>
 cudaError_t launch_d2(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnParams& p,
                       cudaStream_t stream) {
@@ -748,8 +1061,8 @@ cudaError_t launch_attention(int head_dim, const CUtensorMap& tmQ, const CUtenso
                              const AttnParams& p, cudaStream_t stream) {
   if (p.num_qb <= 0) return cudaSuccess;
   const bool paired = ((p.nh / p.ng) & 1) == 0;  // an even number of query heads per kv group
-  if (paired && head_dim == 64) return launch_d2<64, false>(tmQ, tmK, tmV, p, stream);
-  if (paired && head_dim == 128) return launch_d2<128, false>(tmQ, tmK, tmV, p, stream);
+  if (paired && head_dim == 64) return launch_tp<64>(tmQ, tmK, tmV, p, stream);
+  if (paired && head_dim == 128) return launch_tp<128>(tmQ, tmK, tmV, p, stream);
   // d = 64 with an odd number of heads per group (MHA): two heads of two groups per CTA
   if (head_dim == 64 && (p.nh & 1) == 0) return launch_d2<64, true>(tmQ, tmK, tmV, p, stream);
   if (head_dim == 64) return launch_d<64>(tmQ, tmK, tmV, p, stream);

@@ -201,6 +201,28 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uin
       : "memory");
 }
 
+// Each thread writes 64 consecutive 32-bit columns of its own TMEM lane (warp w of the CTA may
+// touch lanes 32*(w%4) .. 32*(w%4)+31) and waits for the write.
+__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]), "r"(r[32]), "r"(r[33]), "r"(r[34]), "r"(r[35]), "r"(r[36]), "r"(r[37]), "r"(r[38]), "r"(r[39]), "r"(r[40]), "r"(r[41]), "r"(r[42]), "r"(r[43]), "r"(r[44]), "r"(r[45]), "r"(r[46]), "r"(r[47]), "r"(r[48]), "r"(r[49]), "r"(r[50]), "r"(r[51]), "r"(r[52]), "r"(r[53]), "r"(r[54]), "r"(r[55]), "r"(r[56]), "r"(r[57]), "r"(r[58]), "r"(r[59]), "r"(r[60]), "r"(r[61]), "r"(r[62]), "r"(r[63])
+      : "memory");
+}
+
+// D[M x N] (+)= A[M x K] B[K x N] with A (fp16/bf16, K-major) in tensor memory at column a_tmem
+// (row i of A in lane i, two elements per 32-bit column) and B in shared memory; kind::f16.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -318,6 +340,32 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
       MT_W32(27), MT_W32(28), MT_W32(29), MT_W32(30), MT_W32(31)
       : "memory");
 }
+
+// tmem_ld32 in two halves, so that other work runs while the load is in flight: tmem_ld32_issue
+// starts the load into r (not yet valid), tmem_ld32_wait waits for every TMEM load of the thread
+// and ties r to that point, so no read of r can be scheduled before it.
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : MT_R32(0), MT_R32(1), MT_R32(2), MT_R32(3), MT_R32(4), MT_R32(5), MT_R32(6), MT_R32(7), MT_R32(8),
+        MT_R32(9), MT_R32(10), MT_R32(11), MT_R32(12), MT_R32(13), MT_R32(14), MT_R32(15), MT_R32(16),
+        MT_R32(17), MT_R32(18), MT_R32(19), MT_R32(20), MT_R32(21), MT_R32(22), MT_R32(23), MT_R32(24),
+        MT_R32(25), MT_R32(26), MT_R32(27), MT_R32(28), MT_R32(29), MT_R32(30), MT_R32(31)
+      : "r"(taddr));
+}
+
+#define MT_RW32(i) "+r"(r[i])
+__device__ __forceinline__ void tmem_ld32_wait(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : MT_RW32(0), MT_RW32(1), MT_RW32(2), MT_RW32(3), MT_RW32(4), MT_RW32(5), MT_RW32(6), MT_RW32(7),
+                 MT_RW32(8), MT_RW32(9), MT_RW32(10), MT_RW32(11), MT_RW32(12), MT_RW32(13), MT_RW32(14),
+                 MT_RW32(15), MT_RW32(16), MT_RW32(17), MT_RW32(18), MT_RW32(19), MT_RW32(20), MT_RW32(21),
+                 MT_RW32(22), MT_RW32(23), MT_RW32(24), MT_RW32(25), MT_RW32(26), MT_RW32(27), MT_RW32(28),
+                 MT_RW32(29), MT_RW32(30), MT_RW32(31));
+}
+#undef MT_RW32
 
 // Each thread reads 128 consecutive fp32 columns of its own TMEM lane in one instruction and
 // waits for them.

@@ -143,9 +143,121 @@ __device__ __forceinline__ void store_e4m3x32(uint8_t* dst_row, int col, int lim
     if (col + 8 * g < limit) *reinterpret_cast<uint2*>(dst_row + col + 8 * g) = pack_e4m3x8(v + 8 * g, qs);
 }
 
+// Eight bf16 values at src[col + 8g], g < 4, as 16-byte vectors; zeros past `limit` (or for a row
+// outside the output).
+__device__ __forceinline__ void load_vec32(const bf16* src, int col, int limit, bool valid, uint4 (&o)[4]) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+    o[g] = (valid && col + 8 * g < limit) ? *reinterpret_cast<const uint4*>(src + col + 8 * g) : make_uint4(0, 0, 0, 0);
+}
+
+__device__ __forceinline__ void add_loaded32(float* v, const uint4 (&a)[4]) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    float f[8];
+    unpack_bf16x8(a[g], f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[8 * g + e] += f[e];
+  }
+}
+
+// Epilogue of the bf16-output modes (store, residual, GeLU) as a two-deep software pipeline over
+// the warp's 32-column chunks: the TMEM load of chunk i + 1 and the global load of its residual
+// row segment are in flight while chunk i is formed and stored, so one chunk's latency (TMEM, then
+// L2) is not paid again for every chunk.  SwiGLU, whose chunk holds twice the accumulator columns,
+// starts the next chunk's TMEM loads once the current chunk is packed to bf16, before its stores.
+// Same arithmetic, in the same order, as the one-chunk-at-a-time form.
+template <int MODE, bool F8>
+__device__ __forceinline__ void epilogue_tile_bf16(const GemmParams& p, uint32_t tacc, int m0, int c0, int width,
+                                                   int r_in_tile, int lo, int hi) {
+  const int row = m0 + r_in_tile;
+  const bool valid = row < p.M;
+  const float deq = F8 ? __ldg(p.deq_a) * __ldg(p.deq_b) : 1.f;
+  const int end = min(hi, p.N - c0);
+  const int n = end > lo ? (end - lo + 31) / 32 : 0;
+  if (n == 0) return;
+  bf16* out_row = p.out + static_cast<size_t>(row) * p.ldo;
+  if constexpr (MODE == kEpiSwiglu) {
+    uint32_t g[32], u[32];
+    tmem_ld32_issue(tacc + lo, g);
+    tmem_ld32_issue(tacc + width + lo, u);  // the up half follows the `width` gate columns
+#pragma unroll 1
+    for (int i = 0; i < n; ++i) {
+      const int col = c0 + lo + 32 * i;
+      tmem_ld32_wait(g);
+      tmem_ld32_wait(u);
+      float v[32], w[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        v[e] = __uint_as_float(g[e]);
+        w[e] = __uint_as_float(u[e]);
+      }
+      if (i + 1 < n) {
+        tmem_ld32_issue(tacc + lo + 32 * (i + 1), g);
+        tmem_ld32_issue(tacc + width + lo + 32 * (i + 1), u);
+      }
+      if (F8) {
+        scale32(v, deq);
+        scale32(w, deq);
+      }
+      if (valid) {
+        if (p.bias != nullptr) {
+          add_vec32(v, p.bias, col, p.N);
+          add_vec32(w, p.bias + p.N, col, p.N);
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = silu(v[e]) * w[e];
+        store_vec32(out_row, col, p.N, v);
+      }
+    }
+  } else {
+    const bf16* resid = MODE == kEpiResid ? p.resid + static_cast<size_t>(row) * p.ldr : nullptr;
+    uint32_t ga[32], gb[32];
+    uint4 ra[4], rb[4];
+    auto issue = [&](int i, uint32_t (&r32)[32], uint4 (&res)[4]) {
+      const int c = lo + 32 * i;
+      tmem_ld32_issue(tacc + c, r32);
+      if (MODE == kEpiResid) load_vec32(resid, c0 + c, p.N, valid, res);
+    };
+    auto finish = [&](int i, const uint32_t (&r32)[32], const uint4 (&res)[4]) {
+      const int col = c0 + lo + 32 * i;
+      if (!valid) return;
+      float v[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r32[e]);
+      if (F8) scale32(v, deq);
+      if (p.bias != nullptr) add_vec32(v, p.bias, col, p.N);
+      if (MODE == kEpiResid) add_loaded32(v, res);
+      if (MODE == kEpiGelu) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = gelu_tanh(v[e]);
+      }
+      store_vec32(out_row, col, p.N, v);
+    };
+    issue(0, ga, ra);
+#pragma unroll 1
+    for (int i = 0; i < n; i += 2) {
+      tmem_ld32_wait(ga);
+      if (i + 1 < n) issue(i + 1, gb, rb);
+      finish(i, ga, ra);
+      if (i + 1 < n) {
+        tmem_ld32_wait(gb);
+        if (i + 2 < n) issue(i + 2, ga, ra);
+        finish(i + 1, gb, rb);
+      }
+    }
+  }
+}
+
 template <int MODE, bool F8>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc, int m0, int c0, int width,
                                               int r_in_tile, int lo, int hi) {
+  if constexpr (MODE == kEpiStore || MODE == kEpiResid || MODE == kEpiGelu || MODE == kEpiSwiglu) {
+    if (p.out8 == nullptr && (MODE != kEpiStore || p.out32 == nullptr)) {
+      epilogue_tile_bf16<MODE, F8>(p, tacc, m0, c0, width, r_in_tile, lo, hi);
+      return;
+    }
+  }
   const int row = m0 + r_in_tile;
   const bool valid = row < p.M;
   const float deq = F8 ? __ldg(p.deq_a) * __ldg(p.deq_b) : 1.f;

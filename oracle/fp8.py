@@ -126,7 +126,7 @@ def attention_block_fp8(cfg, inp: Dict, act_scales, rows: Optional[np.ndarray] =
 
     storage_rounding: q and k are rounded to bf16 and v to fp16 after RoPE, as the kernels store
     them between launches; the E4M3 code of o is then decided from the same stored operands as the
-    kernel decides it.  Returns xn, o and h for `rows` (all tokens if None)."""
+    kernel decides it.  Returns xn, o and h for `rows` (all tokens if None), and v (all tokens)."""
     T, B, d = cfg.tokens, cfg.batch, cfg.head_dim
     nh, ng = cfg.heads, cfg.groups
     rows = np.arange(T) if rows is None else np.asarray(rows)
@@ -158,7 +158,7 @@ def attention_block_fp8(cfg, inp: Dict, act_scales, rows: Optional[np.ndarray] =
             o[sel] = ol.causal_attention(q[sel], k[bb::B], v[bb::B], rows[sel] // B)
     o = o.reshape(len(rows), qw)
     h = x[rows] + ol.linear(_cast("o", o, s_o), w_o, b_o)
-    return {"xn": xn[rows], "o": o, "h": h}
+    return {"xn": xn[rows], "o": o, "h": h, "v": v}
 
 
 def mlp_block_fp8(cfg, inp: Dict, act_scales, h: np.ndarray, wq: Optional[Dict] = None) -> Dict[str, np.ndarray]:

@@ -5,7 +5,9 @@ A quantised code is an integer decided by floating point, so each stage is check
 that both sides hold identically wherever the implementation exposes them:
 
 * codes: the E4M3 codes of an activation against the oracle's codes of the same values, as the
-  fraction of codes that differ (and by at most one step);
+  fraction of codes that differ, each by at most one step or, where the two sides' inputs to the
+  cast differ by a bounded amount, by at most that amount (`slack`, in the scaled units the codes
+  encode: near zero, where E4M3 steps are fine, a small difference spans several codes);
 * attention stage: the stored bf16 h = x + Y_attn + b_o against the oracle's attention block with
   the kernels' storage precision (q, k bf16, v fp16), rounded to bf16 the same way; the relative
   Frobenius distance must stay below H_STAGE_FRAC of the FP8 envelope of that block (the distance
@@ -34,13 +36,15 @@ def code_positions(codes):
     return np.where(c & 0x80, -mag, mag)
 
 
-def assert_codes_close(got, want, max_mismatch, what):
+def assert_codes_close(got, want, max_mismatch, what, slack=0.0):
     g, w = code_positions(got), code_positions(want)
     assert g.shape == w.shape, (what, g.shape, w.shape)
     frac = float(np.mean(g != w))
-    step = int(np.max(np.abs(g - w))) if g.size else 0
-    assert frac <= max_mismatch and step <= 1, (f"{what}: {frac:.2e} of the codes differ (bound {max_mismatch:.1e}), "
-                                                f"largest step {step}")
+    dv = np.abs(of.e4m3_decode(got) - of.e4m3_decode(want))
+    bad = (np.abs(g - w) > 1) & ~(dv <= slack)
+    assert frac <= max_mismatch and not bad.any(), (
+        f"{what}: {frac:.2e} of the codes differ (bound {max_mismatch:.1e}); {int(bad.sum())} by more than one step "
+        f"and more than {slack:.3g} (largest value difference {float(dv.max()) if dv.size else 0.0:.3g})")
     return frac
 
 

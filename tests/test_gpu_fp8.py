@@ -132,8 +132,11 @@ def check_stages(f8, cfg, inp, scales, wq, y, rows=None):
 
     s = [np.float32(v) for v in scales]
     att = of.attention_block_fp8(cfg, inp, scales, rows=rows, wq=wq, storage_rounding=True)
+    # the GPU forms o from fp16 probabilities (relative rounding 2^-11, and 2^-10 from the half-precision
+    # exponential): |o_gpu - o| <= 2^-9 max|v| leaves a code at most that far (scaled) from the oracle's
+    slack = 2.0 ** -9 * float(np.max(np.abs(att["v"]))) * float(s[1])
     fc.assert_codes_close(region("o", cfg.heads * cfg.head_dim).numpy(), of.quantize(att["o"], s[1]), 5e-2,
-                          "attention-output codes")
+                          "attention-output codes", slack=slack)
     h = to_f64(region("h", H, torch.bfloat16))
     fc.assert_attention_stage(h, att["h"], ol.layer_forward(cfg, inp, rows=rows)["h"], "attention stage")
     hn = ol.apply_norm(cfg, h, ol._w(inp, "norm2_w"), ol._w(inp, "norm2_b"))
