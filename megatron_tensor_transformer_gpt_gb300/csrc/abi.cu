@@ -251,6 +251,29 @@ int map_2d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint64
   return MT_OK;
 }
 
+// A GEMM's bf16 output [rows, cols] with `pitch` elements per row, written by TMA stores of 32 x 32 boxes
+// staged in shared memory with the 64-byte swizzle.
+int map_out(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint64_t pitch) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return fail(MT_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {pitch * 2};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MT_ERR_CUDA, "cuTensorMapEncodeTiled (output %llu x %llu) failed: %d",
+                                     (unsigned long long)rows, (unsigned long long)cols, (int)r);
+  return MT_OK;
+}
+
+// Sets up the TMA output of a GEMM whose epilogue writes bf16 `out` (store, residual, GeLU, SwiGLU).
+int prepare_out(mt::GemmParams& p, int mode, CUtensorMap* to) {
+  p.tma_out = (mode != mt::kEpiQkv && p.out != nullptr && p.out8 == nullptr && p.out32 == nullptr) ? 1 : 0;
+  return p.tma_out ? map_out(to, p.out, p.N, p.M, p.ldo) : MT_OK;
+}
+
 // Row-major E4M3 (byte) matrix [rows, cols], pitch in bytes; box = 128 columns x box_rows.
 int map_2d_u8(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint64_t pitch, uint32_t box_rows) {
   auto fn = encode_fn();
@@ -405,10 +428,12 @@ int run_gemm(mt_layer* L, int slot, int mode, const void* A, int lda, const void
   rc = mk(&tb64, W, K, rows_w, K, 64);
   if (rc) return rc;
   plan_gemm(p, mode, mode == mt::kEpiQkv ? p.head_dim : 0, L, fp8);
+  CUtensorMap to = ta;
+  if ((rc = prepare_out(p, mode, &to))) return rc;
   cudaError_t e;
   {
     Timed t(L, slot, st);
-    e = mt::launch_gemm(mode, fp8, ta, tb, tb64, p, st);
+    e = mt::launch_gemm(mode, fp8, ta, tb, tb64, to, p, st);
   }
   if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
   return MT_OK;
@@ -744,8 +769,10 @@ int gemm_ab(mt_layer* L, const void* A, size_t lda, bool a_mn, const void* Bm, s
   p.a_mn = a_mn ? 1 : 0;
   p.b_mn = b_mn ? 1 : 0;
   plan_gemm(p, mt::kEpiStore, 0, L, false);
+  CUtensorMap to = ta;
+  if ((rc = prepare_out(p, mt::kEpiStore, &to))) return rc;
   count_launch(L);
-  cudaError_t e = mt::launch_gemm(mt::kEpiStore, false, ta, tb, tb64, p, st);
+  cudaError_t e = mt::launch_gemm(mt::kEpiStore, false, ta, tb, tb64, to, p, st);
   return e == cudaSuccess ? MT_OK : cuda_fail(e, "GEMM launch");
 }
 

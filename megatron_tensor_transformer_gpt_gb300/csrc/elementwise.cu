@@ -73,12 +73,6 @@ __global__ void __launch_bounds__(NW * 32, VPL == 1 ? 2048 / (NW * 32) : 1536 / 
   const bool valid = r < rows;
   pdl_wait();
   pdl_trigger();
-  if (valid && rope.tab != nullptr) {
-    const int s = rope.row0 + r;
-    if (s < rope.rows)
-      for (int i = sub * 32 + lane; i < rope.half; i += 32 * W)
-        rope.tab[static_cast<size_t>(s) * rope.half + i] = rope_entry(s, rope.theta[i]);
-  }
   const size_t row = static_cast<size_t>(valid ? r : 0);
   const int nvec = H >> 3;
   const uint4* xr = reinterpret_cast<const uint4*>(x + row * H);
@@ -155,6 +149,13 @@ __global__ void __launch_bounds__(NW * 32, VPL == 1 ? 2048 / (NW * 32) : 1536 / 
         reinterpret_cast<uint4*>(y + row * H)[idx] = pack_bf16x8(o);
       }
     }
+  }
+  // the RoPE table rows last, so that their arithmetic does not delay the row's loads
+  if (valid && rope.tab != nullptr) {
+    const int s = rope.row0 + r;
+    if (s < rope.rows)
+      for (int i = sub * 32 + lane; i < rope.half; i += 32 * W)
+        rope.tab[static_cast<size_t>(s) * rope.half + i] = rope_entry(s, rope.theta[i]);
   }
   if (OUT8) {
     mx = warp_max(mx);

@@ -26,7 +26,11 @@ constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB (two 128-row boxes)
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t TMEM_COLS = 2 * BN;
-constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+// Epilogue staging for TMA stores: per epilogue warp two [32 rows x 32 columns] bf16 boxes (2 KB each),
+// after the 1 KB that holds the barriers.
+constexpr int EPI_BOX_BYTES = 32 * 32 * 2;
+constexpr int EPI_STAGE_BYTES = 8 * 2 * EPI_BOX_BYTES;
+constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 1024 + EPI_STAGE_BYTES;
 
 // ------------------------------------------------------------------ epilogue helpers
 __device__ __forceinline__ void add_vec32(float* v, const bf16* src, int col, int limit) {
@@ -167,9 +171,46 @@ __device__ __forceinline__ void add_loaded32(float* v, const uint4 (&a)[4]) {
 // L2) is not paid again for every chunk.  SwiGLU, whose chunk holds twice the accumulator columns,
 // starts the next chunk's TMEM loads once the current chunk is packed to bf16, before its stores.
 // Same arithmetic, in the same order, as the one-chunk-at-a-time form.
+// The chunk's 32 bf16 outputs of this thread's row, through the warp's staging box and one TMA
+// store per chunk (p.tma_out), or as four 16-byte stores.  Box row `lane` holds the thread's 64 bytes,
+// its 16-byte piece c at position c ^ ((lane >> 1) & 3) (the 64-byte swizzle of the output tensor
+// map, which also keeps the warp's shared-memory stores free of bank conflicts).  The staging box
+// alternates between two buffers; a buffer is rewritten once the store issued two chunks earlier has
+// read it.
+struct EpiStore {
+  const CUtensorMap* map;
+  uint8_t* stage;  // this warp's two boxes
+  int y0;          // output row of box row 0
+  int n;           // chunks stored so far
+};
+
+__device__ __forceinline__ void store_chunk(const GemmParams& p, EpiStore& es, bf16* out_row, int col, bool valid,
+                                            const float* v) {
+  if (!p.tma_out) {
+    if (valid) store_vec32(out_row, col, p.N, v);
+    return;
+  }
+  const int lane = threadIdx.x & 31;
+  uint8_t* box = es.stage + (es.n & 1) * EPI_BOX_BYTES;
+  if (es.n >= 2) {
+    if (lane == 0) cp_bulk_wait_read<1>();
+    __syncwarp();
+  }
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(box + lane * 64 + ((c ^ sw) << 4)) = pack_bf16x8(v + 8 * c);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(es.map, smem_u32(box), col, es.y0);
+    cp_bulk_commit();
+  }
+  ++es.n;
+}
+
 template <int MODE, bool F8>
 __device__ __forceinline__ void epilogue_tile_bf16(const GemmParams& p, uint32_t tacc, int m0, int c0, int width,
-                                                   int r_in_tile, int lo, int hi) {
+                                                   int r_in_tile, int lo, int hi, EpiStore& es) {
   const int row = m0 + r_in_tile;
   const bool valid = row < p.M;
   const float deq = F8 ? __ldg(p.deq_a) * __ldg(p.deq_b) : 1.f;
@@ -177,6 +218,7 @@ __device__ __forceinline__ void epilogue_tile_bf16(const GemmParams& p, uint32_t
   const int n = end > lo ? (end - lo + 31) / 32 : 0;
   if (n == 0) return;
   bf16* out_row = p.out + static_cast<size_t>(row) * p.ldo;
+  es.y0 = row - (threadIdx.x & 31);
   if constexpr (MODE == kEpiSwiglu) {
     uint32_t g[32], u[32];
     tmem_ld32_issue(tacc + lo, g);
@@ -207,8 +249,8 @@ __device__ __forceinline__ void epilogue_tile_bf16(const GemmParams& p, uint32_t
         }
 #pragma unroll
         for (int e = 0; e < 32; ++e) v[e] = silu(v[e]) * w[e];
-        store_vec32(out_row, col, p.N, v);
       }
+      store_chunk(p, es, out_row, col, valid, v);
     }
   } else {
     const bf16* resid = MODE == kEpiResid ? p.resid + static_cast<size_t>(row) * p.ldr : nullptr;
@@ -221,18 +263,19 @@ __device__ __forceinline__ void epilogue_tile_bf16(const GemmParams& p, uint32_t
     };
     auto finish = [&](int i, const uint32_t (&r32)[32], const uint4 (&res)[4]) {
       const int col = c0 + lo + 32 * i;
-      if (!valid) return;
       float v[32];
 #pragma unroll
       for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r32[e]);
-      if (F8) scale32(v, deq);
-      if (p.bias != nullptr) add_vec32(v, p.bias, col, p.N);
-      if (MODE == kEpiResid) add_loaded32(v, res);
-      if (MODE == kEpiGelu) {
+      if (valid) {
+        if (F8) scale32(v, deq);
+        if (p.bias != nullptr) add_vec32(v, p.bias, col, p.N);
+        if (MODE == kEpiResid) add_loaded32(v, res);
+        if (MODE == kEpiGelu) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = gelu_tanh(v[e]);
+          for (int e = 0; e < 32; ++e) v[e] = gelu_tanh(v[e]);
+        }
       }
-      store_vec32(out_row, col, p.N, v);
+      store_chunk(p, es, out_row, col, valid, v);
     };
     issue(0, ga, ra);
 #pragma unroll 1
@@ -251,10 +294,10 @@ __device__ __forceinline__ void epilogue_tile_bf16(const GemmParams& p, uint32_t
 
 template <int MODE, bool F8>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc, int m0, int c0, int width,
-                                              int r_in_tile, int lo, int hi) {
+                                              int r_in_tile, int lo, int hi, EpiStore& es) {
   if constexpr (MODE == kEpiStore || MODE == kEpiResid || MODE == kEpiGelu || MODE == kEpiSwiglu) {
     if (p.out8 == nullptr && (MODE != kEpiStore || p.out32 == nullptr)) {
-      epilogue_tile_bf16<MODE, F8>(p, tacc, m0, c0, width, r_in_tile, lo, hi);
+      epilogue_tile_bf16<MODE, F8>(p, tacc, m0, c0, width, r_in_tile, lo, hi, es);
       return;
     }
   }
@@ -429,7 +472,8 @@ __device__ __forceinline__ void epilogue_part(const GemmParams& p, int width, in
 template <int MODE, bool F8>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmB64, const GemmParams p) {
+                const __grid_constant__ CUtensorMap tmB64, const __grid_constant__ CUtensorMap tmO,
+                const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = base;
@@ -463,6 +507,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tma_prefetch(&tmA);
     tma_prefetch(&tmB);
     tma_prefetch(&tmB64);
+    if (p.tma_out) tma_prefetch(&tmO);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -582,6 +627,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   } else {
     const int quad = warp & 3;  // TMEM lanes this warp may read
     const int part = (warp - 2) >> 2;
+    EpiStore es{&tmO, base + STAGES * STAGE_BYTES + 1024 + (warp - 2) * 2 * EPI_BOX_BYTES, 0, 0};
     int it = 0;
     for (int u = blockIdx.x; part < p.epi_split && u < p.num_units; u += gridDim.x, ++it) {
       const int acc = it & 1;
@@ -594,11 +640,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       int lo, hi;
       epilogue_part<MODE>(p, unit_width<MODE>(w), part, lo, hi);
       if (lo < hi)
-        epilogue_tile<MODE, F8>(p, tacc, w.tm * BM, unit_col0<MODE>(w), unit_width<MODE>(w), quad * 32 + lane, lo, hi);
+        epilogue_tile<MODE, F8>(p, tacc, w.tm * BM, unit_col0<MODE>(w), unit_width<MODE>(w), quad * 32 + lane, lo, hi,
+                                es);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty(acc));
     }
+    if (es.n > 0 && lane == 0) cp_bulk_wait_all();  // this warp's output stores are complete
   }
   __syncthreads();
   if (warp == 1) {
@@ -715,12 +763,14 @@ __device__ __forceinline__ void kpart_fold(const GemmParams& p, const Unit& w, u
 constexpr int P_STAGES = 6;
 constexpr int P_B_BYTES = 128 * BK * 2;  // up to 128 B rows per CTA
 constexpr int P_STAGE_BYTES = A_BYTES + P_B_BYTES;
-constexpr size_t P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + 256;
+constexpr size_t P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + 1024 + EPI_STAGE_BYTES;
+static_assert(SMEM_BYTES <= 232448 && P_SMEM_BYTES <= 232448, "GEMM tiles exceed the shared memory of a CTA");
 
 template <int MODE, bool F8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmB64, const GemmParams p) {
+                     const __grid_constant__ CUtensorMap tmB64, const __grid_constant__ CUtensorMap tmO,
+                     const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = base;
@@ -756,6 +806,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     tma_prefetch(&tmA);
     tma_prefetch(&tmB);
     tma_prefetch(&tmB64);
+    if (p.tma_out) tma_prefetch(&tmO);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
@@ -872,6 +923,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
   } else {
     const int quad = warp & 3;
     const int part = (warp - 2) >> 2;
+    EpiStore es{&tmO, base + P_STAGES * P_STAGE_BYTES + 1024 + (warp - 2) * 2 * EPI_BOX_BYTES, 0, 0};
     int it = 0;
     for (int u = pair; part < p.epi_split && u < p.num_units; u += npairs, ++it) {
       const int acc = it & 1;
@@ -892,7 +944,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                            hi);
         if (lo < hi)
           epilogue_tile<MODE, F8>(p, tacc, w.tm * (2 * BM) + static_cast<int>(rank) * BM, unit_col0<MODE>(w),
-                                  unit_width<MODE>(w), quad * 32 + lane, lo, hi);
+                                  unit_width<MODE>(w), quad * 32 + lane, lo, hi, es);
         __syncwarp();
         if (w.ks > 1 && lane == 0)  // every partial of this launch has arrived and been read
           p.kflags[((w.tail * 2 + static_cast<int>(rank)) * 4 + quad) * 2 + part] = 0;
@@ -901,6 +953,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty(acc), 0));
     }
+    if (es.n > 0 && lane == 0) cp_bulk_wait_all();  // this warp's output stores are complete
   }
   tc_fence_before();
   __syncthreads();
@@ -912,8 +965,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
 }
 
 template <int MODE, bool F8>
-cudaError_t launch_mode(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB64, const GemmParams& p,
-                        cudaStream_t stream) {
+cudaError_t launch_mode(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB64, const CUtensorMap& tmO,
+                        const GemmParams& p, cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<MODE, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -929,21 +982,22 @@ cudaError_t launch_mode(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
   if (p.pair) {
     const int pairs = gemm_pair_slots();
     const int grid = 2 * (p.num_units < pairs ? p.num_units : pairs);
-    return launch_pdl(gemm_pair_kernel<MODE, F8>, dim3(grid), dim3(GEMM_THREADS), P_SMEM_BYTES, stream, tmA, tmB, tmB64, p);
+    return launch_pdl(gemm_pair_kernel<MODE, F8>, dim3(grid), dim3(GEMM_THREADS), P_SMEM_BYTES, stream, tmA, tmB, tmB64,
+                      tmO, p);
   }
   const int grid = p.num_units < num_sms() ? p.num_units : num_sms();
-  return launch_pdl(gemm_kernel<MODE, F8>, dim3(grid), dim3(GEMM_THREADS), SMEM_BYTES, stream, tmA, tmB, tmB64, p);
+  return launch_pdl(gemm_kernel<MODE, F8>, dim3(grid), dim3(GEMM_THREADS), SMEM_BYTES, stream, tmA, tmB, tmB64, tmO, p);
 }
 
 template <bool F8>
 cudaError_t launch_kind(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB64,
-                        const GemmParams& p, cudaStream_t stream) {
+                        const CUtensorMap& tmO, const GemmParams& p, cudaStream_t stream) {
   switch (mode) {
-    case kEpiStore: return launch_mode<kEpiStore, F8>(tmA, tmB, tmB64, p, stream);
-    case kEpiResid: return launch_mode<kEpiResid, F8>(tmA, tmB, tmB64, p, stream);
-    case kEpiQkv: return launch_mode<kEpiQkv, F8>(tmA, tmB, tmB64, p, stream);
-    case kEpiSwiglu: return launch_mode<kEpiSwiglu, F8>(tmA, tmB, tmB64, p, stream);
-    case kEpiGelu: return launch_mode<kEpiGelu, F8>(tmA, tmB, tmB64, p, stream);
+    case kEpiStore: return launch_mode<kEpiStore, F8>(tmA, tmB, tmB64, tmO, p, stream);
+    case kEpiResid: return launch_mode<kEpiResid, F8>(tmA, tmB, tmB64, tmO, p, stream);
+    case kEpiQkv: return launch_mode<kEpiQkv, F8>(tmA, tmB, tmB64, tmO, p, stream);
+    case kEpiSwiglu: return launch_mode<kEpiSwiglu, F8>(tmA, tmB, tmB64, tmO, p, stream);
+    case kEpiGelu: return launch_mode<kEpiGelu, F8>(tmA, tmB, tmB64, tmO, p, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -983,10 +1037,11 @@ int gemm_pair_slots() {
 size_t gemm_smem_bytes() { return SMEM_BYTES; }
 
 cudaError_t launch_gemm(int mode, bool fp8, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB64,
-                        const GemmParams& p, cudaStream_t stream) {
+                        const CUtensorMap& tmO, const GemmParams& p, cudaStream_t stream) {
   if (p.num_units <= 0) return cudaSuccess;
-  return fp8 ? launch_kind<true>(mode, tmA, tmB, tmB64, p, stream)
-             : launch_kind<false>(mode, tmA, tmB, tmB64, p, stream);
+  if (p.tma_out && (mode == kEpiQkv || p.out8 != nullptr || p.out32 != nullptr)) return cudaErrorInvalidValue;
+  return fp8 ? launch_kind<true>(mode, tmA, tmB, tmB64, tmO, p, stream)
+             : launch_kind<false>(mode, tmA, tmB, tmB64, tmO, p, stream);
 }
 
 }  // namespace mt

@@ -73,6 +73,10 @@ struct GemmParams {
   // kEpiStore only: fp32 output to out32 (pitch ldo) instead of bf16; acc32 = 1 adds to it
   float* out32;
   int acc32;
+  // bf16 output of the store / residual / GeLU / SwiGLU epilogues through the output tensor map
+  // (boxes of 32 rows x 32 columns staged in shared memory and written by TMA) instead of per-thread
+  // stores
+  int tma_out;
   int* err;
 };
 
@@ -160,8 +164,9 @@ cudaError_t launch_head_slices(const bf16* src, size_t sp, size_t sb, size_t sh,
 // Dsum[(b nh + h) S + s] = dO[s b, h] . O[s b, h] over the head's d columns.
 cudaError_t launch_row_dot(const bf16* dO, const bf16* O, float* Dsum, int S, int B, int nh, int d, cudaStream_t st);
 
+// tmO: the bf16 output [M, N] (pitch ldo) in 32 x 32 boxes with the 64-byte swizzle, read only when p.tma_out.
 cudaError_t launch_gemm(int mode, bool fp8, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB64,
-                        const GemmParams& p, cudaStream_t stream);
+                        const CUtensorMap& tmO, const GemmParams& p, cudaStream_t stream);
 size_t gemm_smem_bytes();
 
 cudaError_t launch_attention(int head_dim, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
