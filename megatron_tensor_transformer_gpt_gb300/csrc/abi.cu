@@ -430,6 +430,9 @@ int run_gemm(mt_layer* L, int slot, int mode, const void* A, int lda, const void
   plan_gemm(p, mode, mode == mt::kEpiQkv ? p.head_dim : 0, L, fp8);
   CUtensorMap to = ta;
   if ((rc = prepare_out(p, mode, &to))) return rc;
+  // a layer's GEMMs take the weights as B, which no kernel of the layer writes; the handle-less calls
+  // may multiply by the output of the kernel just before them
+  p.b_static = L != nullptr ? 1 : 0;
   cudaError_t e;
   {
     Timed t(L, slot, st);

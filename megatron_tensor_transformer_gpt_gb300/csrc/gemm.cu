@@ -752,6 +752,22 @@ __device__ __forceinline__ void kpart_fold(const GemmParams& p, const Unit& w, u
   }
 }
 
+// Residual epilogue: the row segment this warp's lane will add, pulled into L2 while the unit's
+// main loop still runs (the residual is typically cold in DRAM; its latency, one chunk at a time,
+// otherwise paces the epilogue of short-K GEMMs).
+template <int MODE>
+__device__ __forceinline__ void prefetch_resid(const GemmParams& p, const Unit& w, int m0, int part, int r_in_tile) {
+  if constexpr (MODE == kEpiResid) {
+    const int width = unit_width<MODE>(w), c0 = unit_col0<MODE>(w);
+    int lo, hi;
+    epilogue_part<MODE>(p, width, part, lo, hi);
+    const int row = m0 + r_in_tile, end = min(hi, p.N - c0);
+    if (row >= p.M || end <= lo) return;
+    const char* src = reinterpret_cast<const char*>(p.resid + static_cast<size_t>(row) * p.ldr + c0 + lo);
+    for (int off = 0; off < (end - lo) * 2; off += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(src + off));
+  }
+}
+
 // ------------------------------------------------------------------ CTA-pair kernel
 // The same GEMM with 256 x 256 tiles on a cluster of two CTAs (cta_group::2).  Each CTA stages
 // its own 128 rows of A and half of the tile's B rows (N / 2; for SwiGLU the even CTA holds the
@@ -816,7 +832,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
   tc_fence_before();
   cluster_sync();
   tc_fence_after();
-  pdl_wait();  // the setup above overlaps the end of the previous kernel
+  // the setup above overlaps the end of the previous kernel; the producer waits for it only after
+  // issuing the weight loads that do not depend on it
+  if (warp != 0) pdl_wait();
   pdl_trigger();
   const uint32_t tmem_base = *tmem_slot;
   constexpr int KB = F8 ? 128 : BK;
@@ -828,6 +846,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       bool ok = true;
+      // B (a weight) of the first unit's first stages, before the wait for the previous kernel
+      int pre = 0;
+      if (p.b_static && pair < p.num_units && !(!F8 && MODE == kEpiStore && p.b_mn)) {
+        const Unit w = decode_unit(p, pair);
+        const int width = unit_width<MODE>(w);
+        const int c0 = unit_col0<MODE>(w);
+        const int b_rows = MODE == kEpiSwiglu ? width : width / 2;
+        const int b_row0 = MODE == kEpiSwiglu ? c0 + (rank ? p.b_row_step : 0) : c0 + static_cast<int>(rank) * b_rows;
+        const CUtensorMap* mb = b_rows == 128 ? &tmB : &tmB64;
+        const uint32_t pair_bytes = 2u * (A_BYTES + b_rows * 128);
+        const int kb0 = unit_kb0(w, num_kb);
+        pre = min(P_STAGES, unit_kb1(w, num_kb) - kb0);
+        for (int s = 0; s < pre; ++s) {  // fresh stages: nothing to wait for
+          const uint32_t fb = map_to_rank(full(s), 0);
+          if (leader) mbar_arrive_expect_tx(full(s), pair_bytes);
+          tma_load_2d_pair(smem_u32(sB + s * P_B_BYTES), mb, fb, (kb0 + s) * KB, b_row0);
+        }
+      }
+      pdl_wait();
       for (int u = pair; ok && u < p.num_units; u += npairs) {
         const Unit w = decode_unit(p, u);
         const int m0 = w.tm * (2 * BM) + static_cast<int>(rank) * BM;
@@ -841,12 +878,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         const uint32_t pair_bytes = 2u * (A_BYTES + b_rows * 128);
         const int kb1 = unit_kb1(w, num_kb);
         for (int kb = unit_kb0(w, num_kb); kb < kb1; ++kb) {
-          if (!mbar_wait(empty(stage), phase ^ 1u, p.err, abort_flag)) {
+          const bool early = issued < pre;  // this stage's B and expected bytes are already issued
+          if (!early && !mbar_wait(empty(stage), phase ^ 1u, p.err, abort_flag)) {
             ok = false;
             break;
           }
           const uint32_t fb = map_to_rank(full(stage), 0);
-          if (leader) mbar_arrive_expect_tx(full(stage), pair_bytes);
+          if (leader && !early) mbar_arrive_expect_tx(full(stage), pair_bytes);
           const uint32_t a_dst = smem_u32(sA + stage * A_BYTES), b_dst = smem_u32(sB + stage * P_B_BYTES);
           if (!F8 && p.a_mn) {  // A stored [K, M]: two [64 K x 64 M] blocks
             tma_load_2d_pair(a_dst, &tmA, fb, m0, kb * KB);
@@ -854,7 +892,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
           } else {
             tma_load_2d_pair(a_dst, &tmA, fb, kb * KB, m0);
           }
-          if (!F8 && MODE == kEpiStore && p.b_mn) {  // B stored [K, N]: b_rows / 64 blocks of [64 K x 64 N]
+          if (early) {
+          } else if (!F8 && MODE == kEpiStore && p.b_mn) {  // B stored [K, N]: b_rows / 64 blocks of [64 K x 64 N]
             for (int a = 0; a < b_rows / 64; ++a) tma_load_2d_pair(b_dst + a * 8192, &tmB, fb, b_row0 + 64 * a, kb * KB);
           } else {
             tma_load_2d_pair(b_dst, mb, fb, kb * KB, b_row0);
@@ -928,10 +967,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     for (int u = pair; part < p.epi_split && u < p.num_units; u += npairs, ++it) {
       const int acc = it & 1;
       const uint32_t use = (it >> 1) & 1;
+      const Unit w = decode_unit(p, u);
+      if (w.kpart == 0) prefetch_resid<MODE>(p, w, w.tm * (2 * BM) + static_cast<int>(rank) * BM, part, quad * 32 + lane);
       const bool ok = mbar_wait(tfull(acc), use, p.err, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      const Unit w = decode_unit(p, u);
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
       int lo, hi;
       epilogue_part<MODE>(p, unit_width<MODE>(w), part, lo, hi);

@@ -77,6 +77,9 @@ struct GemmParams {
   // (boxes of 32 rows x 32 columns staged in shared memory and written by TMA) instead of per-thread
   // stores
   int tma_out;
+  // B is a weight that no kernel of the stream writes: the pair kernel issues the first stages' B
+  // loads before it waits for the previous kernel (programmatic dependent launch)
+  int b_static;
   int* err;
 };
 
