@@ -51,13 +51,23 @@ __device__ __forceinline__ void store_vec32(bf16* dst_row, int col, int limit, c
     if (col + 8 * g < limit) *reinterpret_cast<uint4*>(dst_row + col + 8 * g) = pack_bf16x8(v + 8 * g);
 }
 
-__device__ __forceinline__ float gelu_tanh(float u) {
-  // 0.5 u (1 + tanh( sqrt(2/pi) (u + 0.044715 u^3) ))
-  const float k0 = 0.7978845608028654f, k1 = 0.044715f;
-  return 0.5f * u * (1.0f + tanhf(k0 * (u + k1 * u * u * u)));
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
-__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+// 0.5 u (1 + tanh(z)), z = sqrt(2/pi) (u + 0.044715 u^3), with 1 + tanh(z) = 2 - 2 / (1 + e^(2z)) formed from
+// one base-2 exponential and one reciprocal (both special-function instructions; at |z| -> inf the
+// reciprocal goes to 0 or 1 and the result to u or 0)
+__device__ __forceinline__ float gelu_tanh(float u) {
+  const float k0 = 0.7978845608028654f, k1 = 0.044715f, two_log2e = 2.8853900817779268f;
+  const float z = k0 * (u + k1 * u * u * u);
+  return u * (1.0f - rcp_approx(1.0f + ex2_approx(z * two_log2e)));
+}
+
+// silu(g) = g sigmoid(g), sigmoid(g) = 1 / (1 + e^-g): one base-2 exponential and one reciprocal
+__device__ __forceinline__ float silu(float g) { return g * rcp_approx(1.0f + ex2_approx(-g * 1.4426950408889634f)); }
 
 // One work unit: tile (tm, tn) of the raster, piece `sub` of `split` along N.
 struct Unit {
