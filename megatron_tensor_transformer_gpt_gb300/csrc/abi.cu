@@ -428,15 +428,16 @@ int run_gemm(mt_layer* L, int slot, int mode, const void* A, int lda, const void
   rc = mk(&tb64, W, K, rows_w, K, 64);
   if (rc) return rc;
   plan_gemm(p, mode, mode == mt::kEpiQkv ? p.head_dim : 0, L, fp8);
-  CUtensorMap to = ta;
+  CUtensorMap to = ta, tr = ta;
   if ((rc = prepare_out(p, mode, &to))) return rc;
+  if (p.tma_out && mode == mt::kEpiResid && (rc = map_out(&tr, p.resid, p.N, p.M, p.ldr))) return rc;
   // a layer's GEMMs take the weights as B, which no kernel of the layer writes; the handle-less calls
   // may multiply by the output of the kernel just before them
   p.b_static = L != nullptr ? 1 : 0;
   cudaError_t e;
   {
     Timed t(L, slot, st);
-    e = mt::launch_gemm(mode, fp8, ta, tb, tb64, to, p, st);
+    e = mt::launch_gemm(mode, fp8, ta, tb, tb64, to, tr, p, st);
   }
   if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
   return MT_OK;
@@ -775,7 +776,7 @@ int gemm_ab(mt_layer* L, const void* A, size_t lda, bool a_mn, const void* Bm, s
   CUtensorMap to = ta;
   if ((rc = prepare_out(p, mt::kEpiStore, &to))) return rc;
   count_launch(L);
-  cudaError_t e = mt::launch_gemm(mt::kEpiStore, false, ta, tb, tb64, to, p, st);
+  cudaError_t e = mt::launch_gemm(mt::kEpiStore, false, ta, tb, tb64, to, ta, p, st);
   return e == cudaSuccess ? MT_OK : cuda_fail(e, "GEMM launch");
 }
 

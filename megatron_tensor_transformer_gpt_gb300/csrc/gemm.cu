@@ -192,7 +192,27 @@ struct EpiStore {
   uint8_t* stage;  // this warp's two boxes
   int y0;          // output row of box row 0
   int n;           // chunks stored so far
+  // residual epilogue: the residual box of a chunk is loaded by TMA into the box the chunk's output
+  // will be staged in (rmap: the residual [M, N] in the same 32 x 32 boxes; rbar: this warp's two
+  // mbarriers, one per box)
+  const CUtensorMap* rmap;
+  uint32_t rbar;
+  int* err;
 };
+
+// Residual box of the warp's `g`-th chunk (box g & 1) at output column `col`: once every store of
+// this warp has finished reading its boxes (the box's previous output), one TMA load completing on
+// the box's mbarrier.
+__device__ __forceinline__ void resid_box_load(EpiStore& es, int g, int col) {
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) {
+    if (es.n > 0) cp_bulk_wait_read<0>();
+    const uint32_t bar = es.rbar + 8u * (g & 1);
+    mbar_arrive_expect_tx(bar, EPI_BOX_BYTES);
+    tma_load_2d(smem_u32(es.stage + (g & 1) * EPI_BOX_BYTES), es.rmap, bar, col, es.y0);
+  }
+  __syncwarp();
+}
 
 __device__ __forceinline__ void store_chunk(const GemmParams& p, EpiStore& es, bf16* out_row, int col, bool valid,
                                             const float* v) {
@@ -263,6 +283,51 @@ __device__ __forceinline__ void epilogue_tile_bf16(const GemmParams& p, uint32_t
       store_chunk(p, es, out_row, col, valid, v);
     }
   } else {
+    if constexpr (MODE == kEpiResid) {
+      if (p.tma_out) {  // residual boxes by TMA into the staging boxes, one chunk ahead
+        const int lane = threadIdx.x & 31, sw = (lane >> 1) & 3;
+        uint32_t g32[32];
+        tmem_ld32_issue(tacc + lo, g32);
+        resid_box_load(es, es.n, c0 + lo);
+#pragma unroll 1
+        for (int i = 0; i < n; ++i) {
+          const int col = c0 + lo + 32 * i, g = es.n;
+          tmem_ld32_wait(g32);
+          float v[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(g32[e]);
+          if (i + 1 < n) {
+            tmem_ld32_issue(tacc + lo + 32 * (i + 1), g32);
+            resid_box_load(es, g + 1, col + 32);
+          }
+          const bool got = mbar_wait(es.rbar + 8u * (g & 1), (g >> 1) & 1, es.err, nullptr);
+          if (!__all_sync(0xffffffffu, got)) {  // recorded in the error word; let the next box's load land
+            if (i + 1 < n && lane == 0)
+              mbar_wait_slow(es.rbar + 8u * ((g + 1) & 1), ((g + 1) >> 1) & 1, nullptr, nullptr, kDrainLimitNs);
+            return;
+          }
+          uint8_t* box = es.stage + (g & 1) * EPI_BOX_BYTES + lane * 64;
+          if (valid) {
+            if (F8) scale32(v, deq);
+            if (p.bias != nullptr) add_vec32(v, p.bias, col, p.N);
+            uint4 rr[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) rr[c] = *reinterpret_cast<const uint4*>(box + ((c ^ sw) << 4));
+            add_loaded32(v, rr);
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(box + ((c ^ sw) << 4)) = pack_bf16x8(v + 8 * c);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(es.map, smem_u32(box - lane * 64), col, es.y0);
+            cp_bulk_commit();
+          }
+          ++es.n;
+        }
+        return;
+      }
+    }
     const bf16* resid = MODE == kEpiResid ? p.resid + static_cast<size_t>(row) * p.ldr : nullptr;
     uint32_t ga[32], gb[32];
     uint4 ra[4], rb[4];
@@ -483,7 +548,7 @@ template <int MODE, bool F8>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmB64, const __grid_constant__ CUtensorMap tmO,
-                const GemmParams p) {
+                const __grid_constant__ CUtensorMap tmR, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = base;
@@ -510,6 +575,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       mbar_init(tempty(a), 4 * p.epi_split);  // the active epilogue warps
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < 2 * EPI_WARPS; ++i) mbar_init(bar0 + 256u + 8u * i, 1);  // residual boxes
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -518,6 +584,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tma_prefetch(&tmB);
     tma_prefetch(&tmB64);
     if (p.tma_out) tma_prefetch(&tmO);
+    if (p.tma_out && MODE == kEpiResid) tma_prefetch(&tmR);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -637,7 +704,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   } else {
     const int quad = warp & 3;  // TMEM lanes this warp may read
     const int part = (warp - 2) >> 2;
-    EpiStore es{&tmO, base + STAGES * STAGE_BYTES + 1024 + (warp - 2) * 2 * EPI_BOX_BYTES, 0, 0};
+    EpiStore es{&tmO, base + STAGES * STAGE_BYTES + 1024 + (warp - 2) * 2 * EPI_BOX_BYTES, 0, 0, &tmR,
+                bar0 + 256u + 16u * (warp - 2), p.err};
     int it = 0;
     for (int u = blockIdx.x; part < p.epi_split && u < p.num_units; u += gridDim.x, ++it) {
       const int acc = it & 1;
@@ -796,7 +864,7 @@ template <int MODE, bool F8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmB64, const __grid_constant__ CUtensorMap tmO,
-                     const GemmParams p) {
+                     const __grid_constant__ CUtensorMap tmR, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = base;
@@ -825,6 +893,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       mbar_init(tempty(a), 8 * p.epi_split);  // both CTAs' active epilogue warps
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < 2 * EPI_WARPS; ++i) mbar_init(bar0 + 256u + 8u * i, 1);  // residual boxes
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -833,6 +902,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     tma_prefetch(&tmB);
     tma_prefetch(&tmB64);
     if (p.tma_out) tma_prefetch(&tmO);
+    if (p.tma_out && MODE == kEpiResid) tma_prefetch(&tmR);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
@@ -972,7 +1042,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
   } else {
     const int quad = warp & 3;
     const int part = (warp - 2) >> 2;
-    EpiStore es{&tmO, base + P_STAGES * P_STAGE_BYTES + 1024 + (warp - 2) * 2 * EPI_BOX_BYTES, 0, 0};
+    EpiStore es{&tmO, base + P_STAGES * P_STAGE_BYTES + 1024 + (warp - 2) * 2 * EPI_BOX_BYTES, 0, 0, &tmR,
+                bar0 + 256u + 16u * (warp - 2), p.err};
     int it = 0;
     for (int u = pair; part < p.epi_split && u < p.num_units; u += npairs, ++it) {
       const int acc = it & 1;
@@ -1016,7 +1087,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
 
 template <int MODE, bool F8>
 cudaError_t launch_mode(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB64, const CUtensorMap& tmO,
-                        const GemmParams& p, cudaStream_t stream) {
+                        const CUtensorMap& tmR, const GemmParams& p, cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<MODE, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1033,21 +1104,22 @@ cudaError_t launch_mode(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
     const int pairs = gemm_pair_slots();
     const int grid = 2 * (p.num_units < pairs ? p.num_units : pairs);
     return launch_pdl(gemm_pair_kernel<MODE, F8>, dim3(grid), dim3(GEMM_THREADS), P_SMEM_BYTES, stream, tmA, tmB, tmB64,
-                      tmO, p);
+                      tmO, tmR, p);
   }
   const int grid = p.num_units < num_sms() ? p.num_units : num_sms();
-  return launch_pdl(gemm_kernel<MODE, F8>, dim3(grid), dim3(GEMM_THREADS), SMEM_BYTES, stream, tmA, tmB, tmB64, tmO, p);
+  return launch_pdl(gemm_kernel<MODE, F8>, dim3(grid), dim3(GEMM_THREADS), SMEM_BYTES, stream, tmA, tmB, tmB64, tmO, tmR,
+                    p);
 }
 
 template <bool F8>
 cudaError_t launch_kind(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB64,
-                        const CUtensorMap& tmO, const GemmParams& p, cudaStream_t stream) {
+                        const CUtensorMap& tmO, const CUtensorMap& tmR, const GemmParams& p, cudaStream_t stream) {
   switch (mode) {
-    case kEpiStore: return launch_mode<kEpiStore, F8>(tmA, tmB, tmB64, tmO, p, stream);
-    case kEpiResid: return launch_mode<kEpiResid, F8>(tmA, tmB, tmB64, tmO, p, stream);
-    case kEpiQkv: return launch_mode<kEpiQkv, F8>(tmA, tmB, tmB64, tmO, p, stream);
-    case kEpiSwiglu: return launch_mode<kEpiSwiglu, F8>(tmA, tmB, tmB64, tmO, p, stream);
-    case kEpiGelu: return launch_mode<kEpiGelu, F8>(tmA, tmB, tmB64, tmO, p, stream);
+    case kEpiStore: return launch_mode<kEpiStore, F8>(tmA, tmB, tmB64, tmO, tmR, p, stream);
+    case kEpiResid: return launch_mode<kEpiResid, F8>(tmA, tmB, tmB64, tmO, tmR, p, stream);
+    case kEpiQkv: return launch_mode<kEpiQkv, F8>(tmA, tmB, tmB64, tmO, tmR, p, stream);
+    case kEpiSwiglu: return launch_mode<kEpiSwiglu, F8>(tmA, tmB, tmB64, tmO, tmR, p, stream);
+    case kEpiGelu: return launch_mode<kEpiGelu, F8>(tmA, tmB, tmB64, tmO, tmR, p, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1087,11 +1159,11 @@ int gemm_pair_slots() {
 size_t gemm_smem_bytes() { return SMEM_BYTES; }
 
 cudaError_t launch_gemm(int mode, bool fp8, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB64,
-                        const CUtensorMap& tmO, const GemmParams& p, cudaStream_t stream) {
+                        const CUtensorMap& tmO, const CUtensorMap& tmR, const GemmParams& p, cudaStream_t stream) {
   if (p.num_units <= 0) return cudaSuccess;
   if (p.tma_out && (mode == kEpiQkv || p.out8 != nullptr || p.out32 != nullptr)) return cudaErrorInvalidValue;
-  return fp8 ? launch_kind<true>(mode, tmA, tmB, tmB64, tmO, p, stream)
-             : launch_kind<false>(mode, tmA, tmB, tmB64, tmO, p, stream);
+  return fp8 ? launch_kind<true>(mode, tmA, tmB, tmB64, tmO, tmR, p, stream)
+             : launch_kind<false>(mode, tmA, tmB, tmB64, tmO, tmR, p, stream);
 }
 
 }  // namespace mt

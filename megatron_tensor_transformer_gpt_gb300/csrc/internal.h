@@ -167,9 +167,10 @@ cudaError_t launch_head_slices(const bf16* src, size_t sp, size_t sb, size_t sh,
 // Dsum[(b nh + h) S + s] = dO[s b, h] . O[s b, h] over the head's d columns.
 cudaError_t launch_row_dot(const bf16* dO, const bf16* O, float* Dsum, int S, int B, int nh, int d, cudaStream_t st);
 
-// tmO: the bf16 output [M, N] (pitch ldo) in 32 x 32 boxes with the 64-byte swizzle, read only when p.tma_out.
+// tmO: the bf16 output [M, N] (pitch ldo) in 32 x 32 boxes with the 64-byte swizzle, read only when p.tma_out;
+// tmR: the residual [M, N] (pitch ldr) in the same boxes, read only when p.tma_out in the residual mode.
 cudaError_t launch_gemm(int mode, bool fp8, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB64,
-                        const CUtensorMap& tmO, const GemmParams& p, cudaStream_t stream);
+                        const CUtensorMap& tmO, const CUtensorMap& tmR, const GemmParams& p, cudaStream_t stream);
 size_t gemm_smem_bytes();
 
 cudaError_t launch_attention(int head_dim, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
