@@ -194,10 +194,12 @@ Layout make_layout(const mt_layer* L, int S, int B, int rope_rows, int index_tok
   lay.size[kXStage] = T * L->hidden * 2;
   lay.size[kYStage] = T * L->hidden * 2;
   lay.size[kPos] = static_cast<size_t>(index_tokens) * sizeof(int);
+  // q, k and v back to back (their sizes are multiples of 16 bytes), so that the QKV epilogue can
+  // write all three through one [heads][tokens][d] tensor map at batch 1
   size_t o = 0;
   for (int r = 0; r < kNumRegions; ++r) {
     lay.off[r] = o;
-    o = round_up(o + lay.size[r], 1024);
+    o = (r == kQ || r == kK) ? o + lay.size[r] : round_up(o + lay.size[r], 1024);
   }
   lay.total = o;
   return lay;
@@ -265,6 +267,22 @@ int map_out(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint6
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(MT_ERR_CUDA, "cuTensorMapEncodeTiled (output %llu x %llu) failed: %d",
                                      (unsigned long long)rows, (unsigned long long)cols, (int)r);
+  return MT_OK;
+}
+
+// q, k and v of a batch-1 call as one bf16 tensor [heads][tokens][d] (the heads of q, then of k,
+// then of v: the QKV GEMM's column order), for TMA stores of 32-token x 32-column boxes.
+int map_qkv_out(CUtensorMap* m, const void* q, uint64_t d, uint64_t tokens, uint64_t heads) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return fail(MT_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[3] = {d, tokens, heads};
+  const cuuint64_t strides[2] = {d * 2, tokens * d * 2};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MT_ERR_CUDA, "cuTensorMapEncodeTiled (qkv output) failed: %d", (int)r);
   return MT_OK;
 }
 
@@ -416,9 +434,10 @@ void plan_gemm(mt::GemmParams& p, int mode, int head_dim, const mt_layer* L, boo
 }
 
 // One GEMM: A [M, K] (pitch lda) x W [rows_w, K]^T with the given epilogue.
-// fp8: A and W hold E4M3 codes (lda and the W pitch K in bytes).
+// fp8: A and W hold E4M3 codes (lda and the W pitch K in bytes).  qkv_out (QKV epilogue at batch 1):
+// the tensor map of q, k, v as one [heads][tokens][d] tensor, written by TMA stores.
 int run_gemm(mt_layer* L, int slot, int mode, const void* A, int lda, const void* W, int rows_w, int M, int N, int K,
-             mt::GemmParams p, cudaStream_t st, bool fp8 = false) {
+             mt::GemmParams p, cudaStream_t st, bool fp8 = false, const CUtensorMap* qkv_out = nullptr) {
   CUtensorMap ta, tb, tb64;
   auto mk = fp8 ? map_2d_u8 : map_2d;
   int rc = mk(&ta, A, K, M, lda, 128);
@@ -430,6 +449,10 @@ int run_gemm(mt_layer* L, int slot, int mode, const void* A, int lda, const void
   plan_gemm(p, mode, mode == mt::kEpiQkv ? p.head_dim : 0, L, fp8);
   CUtensorMap to = ta, tr = ta;
   if ((rc = prepare_out(p, mode, &to))) return rc;
+  if (mode == mt::kEpiQkv && qkv_out != nullptr) {
+    to = *qkv_out;
+    p.tma_out = 1;
+  }
   if (p.tma_out && mode == mt::kEpiResid && (rc = map_out(&tr, p.resid, p.N, p.M, p.ldr))) return rc;
   // a layer's GEMMs take the weights as B, which no kernel of the layer writes; the handle-less calls
   // may multiply by the output of the kernel just before them
@@ -519,6 +542,9 @@ int run_attention_block(mt_layer* L, const Layout& lay, const void* x, int S, in
   const int nqkv = L->q_w + 2 * L->kv_w;
   mt::GemmParams p;
   int rc;
+  CUtensorMap tqkv;
+  const bool qkv_tma = B == 1;  // q, k, v rows are then the token rows
+  if (qkv_tma && (rc = map_qkv_out(&tqkv, q, d, S, static_cast<uint64_t>(L->nh_r) + 2 * L->ng_r))) return rc;
   const int nchunks = in != nullptr ? in->n : 1;
   for (int c = 0; c < nchunks; ++c) {
     const int r0 = in != nullptr ? in->row[c] : 0, rows = in != nullptr ? in->row[c + 1] - r0 : T;
@@ -548,7 +574,9 @@ int run_attention_block(mt_layer* L, const Layout& lay, const void* x, int S, in
     p.ng = L->ng_r;
     p.pos = pos;
     p.row0 = r0;
-    if ((rc = run_gemm(L, kSlotQkv, mt::kEpiQkv, xn + off, H, w->w_qkv, nqkv, rows, nqkv, H, p, st))) return rc;
+    if ((rc = run_gemm(L, kSlotQkv, mt::kEpiQkv, xn + off, H, w->w_qkv, nqkv, rows, nqkv, H, p, st, false,
+                       qkv_tma ? &tqkv : nullptr)))
+      return rc;
   }
 
   CUtensorMap tq, tk, tv;
@@ -676,8 +704,12 @@ int forward_device_fp8(mt_layer* L, const Layout& lay, const void* x, int S, int
   p.ng = L->ng_r;
   p.deq_a = deq + 0;
   p.deq_b = w8->deq_qkv;
-  int rc = run_gemm(L, kSlotQkv, mt::kEpiQkv, xn8, H, w8->w_qkv, nqkv, T, nqkv, H, p, st, true);
+  CUtensorMap tqkv;
+  int rc = B == 1 ? map_qkv_out(&tqkv, q, d, S, static_cast<uint64_t>(L->nh_r) + 2 * L->ng_r) : MT_OK;
   if (rc) return rc;
+  if ((rc = run_gemm(L, kSlotQkv, mt::kEpiQkv, xn8, H, w8->w_qkv, nqkv, T, nqkv, H, p, st, true,
+                     B == 1 ? &tqkv : nullptr)))
+    return rc;
 
   CUtensorMap tq, tk, tv;
   if ((rc = map_3d(&tq, q, d, S, static_cast<uint64_t>(B) * L->nh_r, d, static_cast<uint64_t>(S) * d, 128))) return rc;

@@ -238,6 +238,28 @@ __device__ __forceinline__ void store_chunk(const GemmParams& p, EpiStore& es, b
   ++es.n;
 }
 
+// 32 values of this thread's row (8-element groups packed by `pack`) through the warp's next staging
+// box, stored with one TMA store at (x, y, z) of the 3-D output map (the QKV epilogue's q, k, v heads).
+template <typename Pack>
+__device__ __forceinline__ void store_box3(EpiStore& es, const float* v, int x, int y, int z, Pack pack) {
+  const int lane = threadIdx.x & 31;
+  uint8_t* box = es.stage + (es.n & 1) * EPI_BOX_BYTES;
+  if (es.n >= 2) {
+    if (lane == 0) cp_bulk_wait_read<1>();
+    __syncwarp();
+  }
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(box + lane * 64 + ((c ^ sw) << 4)) = pack(v + 8 * c);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_3d(es.map, smem_u32(box), x, y, z);
+    cp_bulk_commit();
+  }
+  ++es.n;
+}
+
 template <int MODE, bool F8>
 __device__ __forceinline__ void epilogue_tile_bf16(const GemmParams& p, uint32_t tacc, int m0, int c0, int width,
                                                    int r_in_tile, int lo, int hi, EpiStore& es) {
@@ -449,6 +471,67 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
           store_e4m3x32(p.out8 + static_cast<size_t>(row) * p.ldo, col, p.N, g, qs);
         } else {
           store_vec32(p.out + static_cast<size_t>(row) * p.ldo, col, p.N, g);
+        }
+      }
+    }
+  } else if (p.tma_out) {
+    // kEpiQkv, batch 1: q, k and v are one [heads q | k | v][token][d] tensor, so the head of column
+    // `col` is col / d; each 32-column piece of a head goes out as one TMA store of 32 tokens
+    const int d = p.head_dim, half = d >> 1;
+    const int lane = threadIdx.x & 31;
+    const int y0 = row - lane + p.row0;  // token row of box row 0
+    const int rpos = (valid && p.pos != nullptr) ? p.pos[row + p.row0] : row + p.row0;  // RoPE position
+    auto bf16x8 = [](const float* f) { return pack_bf16x8(f); };
+    auto f16x8 = [](const float* f) { return pack_f16x8(f); };
+#pragma unroll 1
+    for (int hc = lo; hc < hi; hc += d) {
+      const int col = c0 + hc;
+      if (col >= p.N) break;
+      const int hz = col / d;
+      if (col < p.q_w + p.kv_w && p.rope != nullptr) {
+        // rotate-half: (x_i, x_{i+d/2}) -> (x_i c - x_{i+d/2} s, x_{i+d/2} c + x_i s)
+#pragma unroll 1
+        for (int i0 = 0; i0 < half; i0 += 32) {
+          float x1[32], x2[32];
+          tmem_ld32(tacc + hc + i0, x1);
+          tmem_ld32(tacc + hc + half + i0, x2);
+          if (valid) {
+            if (F8) {
+              scale32(x1, deq);
+              scale32(x2, deq);
+            }
+            if (p.bias != nullptr) {
+              add_vec32(x1, p.bias, col + i0, p.N);
+              add_vec32(x2, p.bias, col + half + i0, p.N);
+            }
+            const float4* cs = reinterpret_cast<const float4*>(p.rope + static_cast<size_t>(rpos) * half + i0);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float4 t = cs[e];  // (cos, sin) of elements 2e and 2e+1
+              const float a0 = x1[2 * e], b0 = x2[2 * e], a1 = x1[2 * e + 1], b1 = x2[2 * e + 1];
+              x1[2 * e] = a0 * t.x - b0 * t.y;
+              x2[2 * e] = b0 * t.x + a0 * t.y;
+              x1[2 * e + 1] = a1 * t.z - b1 * t.w;
+              x2[2 * e + 1] = b1 * t.z + a1 * t.w;
+            }
+          }
+          store_box3(es, x1, i0, y0, hz, bf16x8);
+          store_box3(es, x2, half + i0, y0, hz, bf16x8);
+        }
+      } else {
+        const bool is_v = col >= p.q_w + p.kv_w;
+#pragma unroll 1
+        for (int i0 = 0; i0 < d; i0 += 32) {
+          float x[32];
+          tmem_ld32(tacc + hc + i0, x);
+          if (valid) {
+            if (F8) scale32(x, deq);
+            if (p.bias != nullptr) add_vec32(x, p.bias, col + i0, p.N);
+          }
+          if (is_v)
+            store_box3(es, x, i0, y0, hz, f16x8);
+          else
+            store_box3(es, x, i0, y0, hz, bf16x8);
         }
       }
     }
@@ -1161,7 +1244,8 @@ size_t gemm_smem_bytes() { return SMEM_BYTES; }
 cudaError_t launch_gemm(int mode, bool fp8, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB64,
                         const CUtensorMap& tmO, const CUtensorMap& tmR, const GemmParams& p, cudaStream_t stream) {
   if (p.num_units <= 0) return cudaSuccess;
-  if (p.tma_out && (mode == kEpiQkv || p.out8 != nullptr || p.out32 != nullptr)) return cudaErrorInvalidValue;
+  if (p.tma_out && (p.out8 != nullptr || p.out32 != nullptr || (mode == kEpiQkv && p.batch != 1)))
+    return cudaErrorInvalidValue;
   return fp8 ? launch_kind<true>(mode, tmA, tmB, tmB64, tmO, tmR, p, stream)
              : launch_kind<false>(mode, tmA, tmB, tmB64, tmO, tmR, p, stream);
 }
