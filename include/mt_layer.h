@@ -277,6 +277,15 @@ int mt_gemm_bf16_t(const void* A, int a_layout, const void* B, int b_layout, voi
  * order.  A tuning and testing control; returns MT_ERR_INVALID_ARG for other values. */
 int mt_gemm_set_pairing(int mode);
 
+/* Attention kernel form for every later launch in the process (all handles): 0 automatic (the
+ * default: one CTA takes two query heads of one kv group when the group serves an even number of
+ * heads and those two-head CTAs number at least twice the SMs, or, at head_dim 64 with an odd
+ * number of heads per group, two heads of two groups; otherwise one head per CTA), 1 one head per
+ * CTA always, 2 two heads per CTA wherever a form allows it.  One or two heads of one group per
+ * CTA give bit-identical outputs (each head's products and softmax are the same instructions in
+ * the same order).  A tuning and testing control; returns MT_ERR_INVALID_ARG for other values. */
+int mt_attn_set_heads_per_cta(int mode);
+
 /* How the CTA-pair GEMM cuts the tiles of its last, partial wave, for every later launch in the
  * process: 0 automatic (the default): the GEMMs of a layer handle cut each tail tile into 2 to 4
  * ranges of K when the tail still fits in one wave of SM pairs and each range drops at least 16 K

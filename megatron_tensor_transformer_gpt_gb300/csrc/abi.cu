@@ -1342,6 +1342,12 @@ int mt_gemm_set_pairing(int mode) {
   return ok();
 }
 
+int mt_attn_set_heads_per_cta(int mode) {
+  if (mode < 0 || mode > 2) return fail(MT_ERR_INVALID_ARG, "attention heads-per-CTA mode must be 0, 1 or 2 (got %d)", mode);
+  mt::set_attention_heads_mode(mode);
+  return ok();
+}
+
 int mt_gemm_set_tail_split(int mode) {
   if (mode < 0 || mode > 1) return fail(MT_ERR_INVALID_ARG, "tail split mode must be 0 or 1 (got %d)", mode);
   g_tail.store(mode);

@@ -5,23 +5,29 @@
 // num_query_groups of "ai阅读megatron" TransformerConfig; FlashAttention is the prior art the
 // pages name: exact attention computed block by block with an online softmax, O(S) memory.)
 //
-// Three forms share one scheme, chosen by launch_attention from d and the heads per kv group:
+// Two forms share one scheme, chosen by launch_attention from d, the heads per kv group and the
+// number of CTAs:
 //   attn_tp_kernel<D>       an even number of heads per group: one CTA takes two heads of one group
-//                           for a 128-query block, so every K/V tile feeds both (all GQA/MQA
+//                           for a 128-query block, so every K/V tile feeds both (the GQA/MQA
 //                           workloads); P stays in tensor memory;
+//   attn_db_kernel<D>       one head per CTA with two score buffers in tensor memory: an odd
+//                           number of heads per group (MHA at d = 128), or too few two-head CTAs
+//                           to fill the SMs twice over (then the longest query block's chain of
+//                           key blocks sets the time);
 //   attn2_kernel<64, true>  d = 64 with an odd number of heads per group (MHA): two heads of two
-//                           groups, each ring slot holding both groups' tiles;
-//   attn_kernel<D>          otherwise (MHA at d = 128, or an odd number of heads): one head per CTA.
+//                           groups, each ring slot holding both groups' tiles.
 // CTAs are issued longest-first (the last query blocks see the most keys).  In every form warp 0
 // loads the Q tile(s) and then K and V tiles [128 keys x d] by TMA; one thread of warp 1 issues
 // S_j = Q K_j^T into a TMEM score buffer and O += P_j V_j into a TMEM accumulator, reading V as an
 // MN-major operand (its d index contiguous); the softmax warps (one query row per thread) read S_j
 // from TMEM, mask the diagonal block, keep a running maximum and sum in the log2 domain, write
-// P_j = 2^(s c - m) as fp16 (into shared memory in the 128-byte-swizzled layout the MMA reads, or,
-// in attn_tp_kernel, over S_j in tensor memory), and rescale O in TMEM only when the running
+// P_j = 2^(s c - m) as fp16 (into shared memory in the 128-byte-swizzled layout the MMA reads in
+// attn2_kernel, over S_j in tensor memory in attn_tp_kernel), and rescale O in TMEM only when the running
 // maximum grows by more than 2^8 (between rescales P stays below 256).  At the end O / l is written as bf16 (or E4M3) to o[t, h*d + i] and,
 // when asked, m + log2(l) to lse for the backward pass.
 #include <math.h>
+
+#include <atomic>
 
 #include "common.cuh"
 #include "internal.h"
@@ -81,272 +87,6 @@ __device__ __forceinline__ bool decode_work(const AttnParams& p, int heads_slots
   w.q_row0 = start + w.qb * BQ;
   w.kv_row0 = start;
   return true;
-}
-
-template <int D>
-struct Geo {
-  static constexpr int ATOM = 128 * 128;          // one [128 rows x 64 bf16] swizzle block, 16 KB
-  static constexpr int Q_BYTES = BQ * D * 2;      // D/64 atoms
-  static constexpr int K_BYTES = BKV * D * 2;     // D/64 atoms
-  static constexpr int V_BYTES = BKV * D * 2;     // [128 keys x D]: D/64 atoms
-  static constexpr int P_BYTES = BQ * BKV * 2;    // two key halves of 16 KB
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + Q_BYTES;
-  static constexpr int OFF_V = OFF_K + 2 * K_BYTES;
-  static constexpr int OFF_P = OFF_V + 2 * V_BYTES;
-  static constexpr int OFF_BAR = OFF_P + P_BYTES;
-  // Every CTA allocates all 512 TMEM columns, so at most one CTA may live on an SM: ask for more
-  // than half of the SM's shared memory even when the tiles need less.
-  static constexpr size_t SMEM_USED = 1024 + OFF_BAR + 256;
-  static constexpr size_t SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
-  static constexpr uint32_t IDESC_S = idesc_bf16(BQ, BKV);
-  static constexpr uint32_t IDESC_O = idesc_f16(BQ, D) | (1u << 16);  // fp16 P (K-major), fp16 V (MN-major)
-};
-
-template <int D>
-__global__ void __launch_bounds__(192, 1)
-    attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
-  using G = Geo<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = base + G::OFF_Q;
-  uint8_t* sP = base + G::OFF_P;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + G::OFF_BAR);
-  // bars: q_full | kv_full[2] | kv_empty[2] | s_full[2] | s_free[2] | p_full | o_done | drain
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  const uint32_t bar0 = smem_u32(bars);
-  const uint32_t q_full = bar0;
-  auto kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto kv_empty = [&](int s) { return bar0 + 8u * (3 + s); };
-  auto s_full = [&](int s) { return bar0 + 8u * (5 + s); };
-  auto s_free = [&](int s) { return bar0 + 8u * (7 + s); };
-  const uint32_t p_full = bar0 + 8u * 9, o_done = bar0 + 8u * 10, drain = bar0 + 8u * 11;
-  const uint32_t sQa = smem_u32(sQ), sPa = smem_u32(sP);
-  auto sKa = [&](int st) { return smem_u32(base + G::OFF_K + st * G::K_BYTES); };
-  auto sVa = [&](int st) { return smem_u32(base + G::OFF_V + st * G::V_BYTES); };
-
-  pdl_wait();  // q, k, v (and cu_seqlens) are written by the kernels before
-  pdl_trigger();
-  Work wk;
-  if (!decode_work(p, p.nh, 1, wk)) return;  // uniform over the CTA, before any barrier or TMEM use
-  const int qb = wk.qb, b = wk.b, h = wk.h;
-  const int g = h / (p.nh / p.ng);
-  const int nkv = qb + 1;  // causal: key blocks 0..qb
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(kv_full(s), 1);
-      mbar_init(kv_empty(s), 1);
-      mbar_init(s_full(s), 1);
-      mbar_init(s_free(s), 4);
-    }
-    mbar_init(p_full, 4);
-    mbar_init(o_done, 1);
-    mbar_init(drain, 1);
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch(&tmQ);
-    tma_prefetch(&tmK);
-    tma_prefetch(&tmV);
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-  const uint32_t tO = tmem_base + 2 * BKV;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      mbar_arrive_expect_tx(q_full, G::Q_BYTES);
-#pragma unroll
-      for (int a = 0; a < D / 64; ++a) tma_load_3d(sQa + a * G::ATOM, &tmQ, q_full, a * 64, wk.q_row0, b * p.nh + h);
-      int issued = 0;
-      bool ok = true;
-      for (int j = 0; j < nkv; ++j) {
-        const int st = j & 1;
-        if (!mbar_wait(kv_empty(st), ((j >> 1) & 1) ^ 1u, p.err, abort_flag)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(kv_full(st), G::K_BYTES + G::V_BYTES);
-#pragma unroll
-        for (int a = 0; a < D / 64; ++a)
-          tma_load_3d(sKa(st) + a * G::ATOM, &tmK, kv_full(st), a * 64, wk.kv_row0 + j * BKV, b * p.ng + g);
-#pragma unroll
-        for (int a = 0; a < D / 64; ++a)
-          tma_load_3d(sVa(st) + a * G::ATOM, &tmV, kv_full(st), a * 64, wk.kv_row0 + j * BKV, b * p.ng + g);
-        ++issued;
-      }
-      if (!ok) {  // let this CTA's own copies in flight land
-        mbar_wait_slow(q_full, 0, nullptr, nullptr, kDrainLimitNs);
-        for (int j = issued - 1; j >= 0 && j >= issued - 2; --j)
-          mbar_wait_slow(kv_full(j & 1), (j >> 1) & 1, nullptr, nullptr, kDrainLimitNs);
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      bool ok = mbar_wait(q_full, 0, p.err, abort_flag);
-      auto issue_s = [&](int j) -> bool {
-        const int st = j & 1;
-        if (!mbar_wait(kv_full(st), (j >> 1) & 1, p.err, abort_flag)) return false;
-        if (!mbar_wait(s_free(st), ((j >> 1) & 1) ^ 1u, p.err, abort_flag)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * G::ATOM + (k & 3) * 32;
-          mma_bf16_ss(tmem_base + st * BKV, sw128_desc(sQa + off), sw128_desc(sKa(st) + off), G::IDESC_S,
-                      k > 0 ? 1u : 0u);
-        }
-        mma_commit(s_full(st));
-        return true;
-      };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; ok && j < nkv; ++j) {
-        if (j + 1 < nkv && !issue_s(j + 1)) {
-          ok = false;
-          break;
-        }
-        if (!mbar_wait(p_full, j & 1, p.err, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const int st = j & 1;
-#pragma unroll
-        for (int k = 0; k < BKV / 16; ++k) {
-          const uint32_t pa = sPa + (k >> 2) * G::ATOM + (k & 3) * 32;
-          mma_bf16_ss(tO, sw128_desc(pa), sw128_desc_mn(sVa(st) + k * 2048, G::ATOM), G::IDESC_O,
-                      (j > 0 || k > 0) ? 1u : 0u);
-        }
-        mma_commit(kv_empty(st));
-        mma_commit(o_done);
-      }
-      mma_commit(drain);
-      mbar_wait_slow(drain, 0, nullptr, nullptr, ok ? kWaitLimitNs : kDrainLimitNs);
-    }
-  } else {
-    const int quad = warp & 3;
-    const int r = quad * 32 + lane;  // query row within the block
-    const bool row_ok = qb * BQ + r < wk.len;  // inside its sequence
-    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const float c = p.scale_log2;
-    float m_used = -INFINITY, l = 0.f;
-    bool ok = true;
-    uint8_t* prow = sP + r * 128;
-    const int sw = r & 7;
-    for (int j = 0; j < nkv; ++j) {
-      const int sb = j & 1;
-      bool w = mbar_wait(s_full(sb), (j >> 1) & 1, p.err, abort_flag);
-      if (!__all_sync(0xffffffffu, w)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float s[BKV];
-      tmem_ld128(tmem_base + lane_off + sb * BKV, s);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_free(sb));
-      if (j == qb) {  // diagonal block: key j*128+i visible iff i <= r
-#pragma unroll
-        for (int i = 0; i < BKV; ++i)
-          if (i > r) s[i] = -INFINITY;
-      }
-      const float mx = row_max(s);
-      const float m_new = fmaxf(m_used, mx * c);
-      if (j > 0) {  // P_{j-1} V_{j-1} finished: P may be overwritten and O is stable
-        w = mbar_wait(o_done, (j - 1) & 1, p.err, abort_flag);
-        if (!__all_sync(0xffffffffu, w)) {
-          ok = false;
-          break;
-        }
-      }
-      if (__any_sync(0xffffffffu, m_new > m_used + 8.0f)) {
-        const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m_used - m_new);
-        l *= alpha;
-        if (j > 0) {
-          tc_fence_after();
-#pragma unroll 1
-          for (int cc = 0; cc < D / 32; ++cc) {
-            float o[32];
-            tmem_ld32(tO + lane_off + cc * 32, o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tmem_st32(tO + lane_off + cc * 32, o);
-          }
-        }
-        m_used = m_new;
-      }
-      float rs = 0.f;
-#pragma unroll
-      for (int i = 0; i < BKV; ++i) {
-        s[i] = ex2_approx(fmaf(s[i], c, -m_used));
-        rs += s[i];
-      }
-      l += rs;
-#pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
-        const int atom = ch >> 3, cw = ch & 7;
-        *reinterpret_cast<uint4*>(prow + atom * G::ATOM + ((cw ^ sw) << 4)) = pack_f16x8(s + ch * 8);
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
-    }
-    if (ok) {
-      const bool w = mbar_wait(o_done, (nkv - 1) & 1, p.err, abort_flag);
-      if (__all_sync(0xffffffffu, w)) {
-        tc_fence_after();
-        const float inv_l = 1.f / l;
-        const size_t orow = (static_cast<size_t>(wk.q_row0 + r) * p.batch + b) * p.ldo + h * D;
-        if (p.lse != nullptr && row_ok)
-          p.lse[(static_cast<size_t>(b) * p.nh + h) * p.seq + wk.q_row0 + r] = m_used + log2f(l);
-        const float qs = p.o8 != nullptr ? __ldg(p.q_scale) : 1.f;
-        float mx = 0.f;
-#pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
-          float o[32];
-          tmem_ld32(tO + lane_off + cc * 32, o);
-          if (row_ok) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= inv_l;
-            if (p.o8 != nullptr) {  // E4M3 output for the FP8 output projection
-#pragma unroll
-              for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(o[i]));
-#pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4)
-                *reinterpret_cast<uint2*>(p.o8 + orow + cc * 32 + q4 * 8) = pack_e4m3x8(o + q4 * 8, qs);
-            } else {
-#pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4)
-                *reinterpret_cast<uint4*>(p.o + orow + cc * 32 + q4 * 8) = pack_bf16x8(o + q4 * 8);
-            }
-          }
-        }
-        if (p.o8 != nullptr) {
-          mx = warp_max(mx);
-          if (lane == 0) atomic_max_abs(p.amax, mx);
-        }
-      }
-    }
-  }
-  __syncthreads();
-  if (warp == 1) {
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc(tmem_base, 512);
-  }
 }
 
 // ------------------------------------------------------------------ two heads per CTA, P in shared memory
@@ -727,30 +467,38 @@ __global__ void __launch_bounds__(320, 1)
 //   S_t(j) -- and so also after P_t(j-1) V_{j-1}, which makes O_t stable for a rescale -- and, one
 //   block after the last, when O_t is final; p_full tells the MMA thread that P_t(j) is written
 //   (and any rescale of O_t done).
-template <int D>
+template <int D, int NH>
 struct GeoT {
   static constexpr int ATOM = 128 * 128;          // [128 rows x 64 bf16] swizzle block, 16 KB
   static constexpr int Q_BYTES = BQ * D * 2;      // per head
   static constexpr int KV_BYTES = BKV * D * 2;    // one K or V tile [128 keys x d]
-  static constexpr int NS = D == 128 ? 5 : 8;     // ring slots
+  static constexpr int NS = D == 128 ? (NH == 2 ? 5 : 6) : 8;  // ring slots (NH: heads per CTA)
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_KV = 2 * Q_BYTES;
+  static constexpr int OFF_KV = NH * Q_BYTES;
   static constexpr int OFF_BAR = OFF_KV + NS * KV_BYTES;
   static constexpr size_t SMEM_USED = 1024 + OFF_BAR + 256;
-  static constexpr size_t SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;  // one CTA per SM (TMEM)
+  static constexpr size_t SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;  // one CTA per SM
+  // two heads: S and O of each (4 x 128 columns); one head: two S buffers and O (3 x 128)
+  static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t IDESC_S = idesc_bf16(BQ, BKV);
   static constexpr uint32_t IDESC_O = idesc_f16(BQ, D) | (1u << 16);  // fp16 P (K-major), fp16 V (MN-major)
 };
-static_assert(GeoT<128>::SMEM_USED <= 232448 && GeoT<64>::SMEM_USED <= 232448,
+static_assert(GeoT<128, 2>::SMEM_USED <= 232448 && GeoT<64, 2>::SMEM_USED <= 232448 &&
+                  GeoT<128, 1>::SMEM_USED <= 232448 && GeoT<64, 1>::SMEM_USED <= 232448,
               "attention tiles exceed the shared memory of a CTA");
 
-// Softmax of one head (four warps, one query row per thread) for attn_tp_kernel: per key block it
-// waits for S, masks the diagonal block, forms P = 2^(s c - m) as fp16 pairs, rescales O when the
-// running maximum grew by more than 2^8, writes P over S's first 64 columns and signals p_full.
-template <int D>
+// Softmax of one head (four warps, one query row per thread) for attn_tp_kernel and attn_db_kernel:
+// per key block it waits for S, masks the diagonal block, forms P = 2^(s c - m) as fp16 pairs,
+// rescales O when the running maximum grew by more than 2^8, writes P over S's first 64 columns
+// and signals p_full.  DB (attn_db_kernel): block j's scores are in the buffer at tS + 128 (j & 1),
+// completed on the barrier s_full + 8 (j & 1) (phase j / 2); P(j) is signalled on p_full + 8 (j & 1)
+// (a warp may run one block ahead of the others, so consecutive blocks use different barriers);
+// o_done completes after each P V product and o_final after the last: a rescale first waits for
+// the previous product, the final O for all of them.
+template <int D, bool DB = false>
 __device__ __forceinline__ void softmax_head_tm(const AttnParams& p, const Work& wk, int h, int quad, int lane,
                                                 uint32_t tS, uint32_t tO, uint32_t s_full, uint32_t p_full,
-                                                volatile int* abort_flag) {
+                                                volatile int* abort_flag, uint32_t o_done = 0, uint32_t o_final = 0) {
   const int qb = wk.qb, b = wk.b, nkv = qb + 1;
   const int r = quad * 32 + lane;
   const bool row_ok = qb * BQ + r < wk.len;  // inside its sequence
@@ -759,14 +507,16 @@ __device__ __forceinline__ void softmax_head_tm(const AttnParams& p, const Work&
   float m_used = -INFINITY, l = 0.f;
   bool ok = true;
   for (int j = 0; j < nkv; ++j) {
-    const bool w = mbar_wait(s_full, j & 1, p.err, abort_flag);
+    const uint32_t tSj = DB ? tS + 128u * (j & 1) : tS;
+    const bool w = DB ? mbar_wait(s_full + 8u * (j & 1), (j >> 1) & 1, p.err, abort_flag)
+                      : mbar_wait(s_full, j & 1, p.err, abort_flag);
     if (!__all_sync(0xffffffffu, w)) {
       ok = false;
       break;
     }
     tc_fence_after();
     float s[BKV];
-    tmem_ld128(tS + lane_off, s);
+    tmem_ld128(tSj + lane_off, s);
     if (j == qb) {  // diagonal block: key j*128+i visible iff i <= r
 #pragma unroll
       for (int i = 0; i < BKV; ++i)
@@ -806,7 +556,15 @@ __device__ __forceinline__ void softmax_head_tm(const AttnParams& p, const Work&
       }
     }
     l = l * alpha + rs;
-    if (grow && j > 0) {  // P(j-1) V_{j-1} has completed (it precedes S(j)): O is stable
+    if (DB && grow && j > 0) {  // O is stable once P(j-1) V_{j-1} has completed
+      const bool wo = mbar_wait(o_done, (j - 1) & 1, p.err, abort_flag);
+      if (!__all_sync(0xffffffffu, wo)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+    }
+    if (grow && j > 0) {  // (two heads: P(j-1) V_{j-1} precedes S(j), so O is stable)
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         float o[32];
@@ -816,13 +574,14 @@ __device__ __forceinline__ void softmax_head_tm(const AttnParams& p, const Work&
         tmem_st32(tO + lane_off + cc * 32, o);
       }
     }
-    tmem_st64(tS + lane_off, pk);  // key 2i (low half) and 2i+1 of P in column i
+    tmem_st64(tSj + lane_off, pk);  // key 2i (low half) and 2i+1 of P in column i
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(p_full);
+    if (lane == 0) mbar_arrive(DB ? p_full + 8u * (j & 1) : p_full);
   }
   if (ok) {
-    const bool w = mbar_wait(s_full, nkv & 1, p.err, abort_flag);  // the last P V product is done
+    const bool w = DB ? mbar_wait(o_final, 0, p.err, abort_flag)
+                      : mbar_wait(s_full, nkv & 1, p.err, abort_flag);  // the last P V product is done
     if (__all_sync(0xffffffffu, w)) {
       tc_fence_after();
       const float inv_l = 1.f / l;
@@ -863,7 +622,8 @@ template <int D>
 __global__ void __launch_bounds__(320, 1)
     attn_tp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
-  using G = GeoT<D>;
+  constexpr int NH = 2;
+  using G = GeoT<D, NH>;
   constexpr int NS = G::NS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -887,7 +647,7 @@ __global__ void __launch_bounds__(320, 1)
   pdl_wait();  // q, k, v (and cu_seqlens) are written by the kernels before
   pdl_trigger();
   Work wk;
-  if (!decode_work(p, p.nh >> 1, 2, wk)) return;  // uniform over the CTA, before any barrier or TMEM use
+  if (!decode_work(p, p.nh / NH, NH, wk)) return;  // uniform over the CTA, before any barrier or TMEM use
   const int qb = wk.qb, b = wk.b, h0 = wk.h;
   const int g = h0 / (p.nh / p.ng);  // both heads' kv group (an even number of heads per group)
   const int nkv = qb + 1;
@@ -899,7 +659,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(kv_full(i), 1);
       mbar_init(kv_empty(i), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NH; ++i) {
       mbar_init(s_full(i), 1);
       mbar_init(p_full(i), 4);
     }
@@ -913,7 +673,7 @@ __global__ void __launch_bounds__(320, 1)
     tma_prefetch(&tmV);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_alloc(smem_u32(tmem_slot), G::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -925,9 +685,9 @@ __global__ void __launch_bounds__(320, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(q_full, 2 * G::Q_BYTES);
+      mbar_arrive_expect_tx(q_full, NH * G::Q_BYTES);
 #pragma unroll
-      for (int t = 0; t < 2; ++t)
+      for (int t = 0; t < NH; ++t)
 #pragma unroll
         for (int a = 0; a < D / 64; ++a)
           tma_load_3d(sQa(t) + a * G::ATOM, &tmQ, q_full, a * 64, wk.q_row0, b * p.nh + h0 + t);
@@ -963,10 +723,11 @@ __global__ void __launch_bounds__(320, 1)
       bool ok = mbar_wait(q_full, 0, p.err, abort_flag) && mbar_wait(kv_full(0), use_parity(0), p.err, abort_flag);
       if (ok) {
         tc_fence_after();
-        issue_s(0, 0);
-        mma_commit(s_full(0));
-        issue_s(1, 0);
-        mma_commit(s_full(1));
+#pragma unroll
+        for (int t = 0; t < NH; ++t) {
+          issue_s(t, 0);
+          mma_commit(s_full(t));
+        }
         mma_commit(kv_empty(0));
       }
       for (int j = 0; ok && j < nkv; ++j) {
@@ -975,7 +736,7 @@ __global__ void __launch_bounds__(320, 1)
           ok = false;
           break;
         }
-        for (int t = 0; t < 2 && ok; ++t) {
+        for (int t = 0; t < NH && ok; ++t) {
           if (!mbar_wait(p_full(t), j & 1, p.err, abort_flag)) {
             ok = false;
             break;
@@ -1009,22 +770,187 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, 512);
+    tmem_dealloc(tmem_base, G::TMEM_COLS);
   }
 }
 
+// ------------------------------------------------------------------ one head, two score buffers
+// attn_db_kernel: one head per CTA (an odd number of heads per group, or too few two-head CTAs),
+// with two TMEM score buffers so that the tensor core computes S(j+1) while the softmax warps turn
+// S(j) into P(j), and one thread of warp 1 issues, after S(0) and S(1):
+//   per key block j: P(j) V_j (P from score buffer j % 2), then S(j+2) into the same buffer.
+// The MMAs run in issue order, so S(j+2) overwrites P(j) only after P(j) V_j has read it.  A
+// rescale of O in block j waits for P(j-1) V_{j-1} (o_done), which S(j) no longer implies.
+// Every parity wait sees its barrier at most one phase from the awaited one: S(j) completing
+// implies P(j-2) V_{j-2} completed, and S(j+2), P(j) V_j and a warp's block j+2 all wait for
+// block j's P from every softmax warp.
+//   TMEM: score buffers in columns [0, 128) and [128, 256), O in [256, 256 + d).
+//   Tiles enter the ring in the order the MMAs use them: K0, K1, then V_j, K_{j+2} per block.
 template <int D>
+__global__ void __launch_bounds__(192, 1)
+    attn_db_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+  using G = GeoT<D, 1>;
+  constexpr int NS = G::NS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + G::OFF_BAR);
+  // bars: q_full | kv_full[NS] | kv_empty[NS] | s_full[2] | p_full[2] | o_done | o_final | drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8 + 2 * NS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  const uint32_t q_full = bar0;
+  // tile n of the load sequence sits in ring slot n % NS, in that slot's (n / NS)-th use
+  auto kv_full = [&](int n) { return bar0 + 8u * (1 + n % NS); };
+  auto kv_empty = [&](int n) { return bar0 + 8u * (1 + NS + n % NS); };
+  auto use_parity = [](int n) { return static_cast<uint32_t>((n / NS) & 1); };
+  const uint32_t s_full = bar0 + 8u * (1 + 2 * NS);  // buffer b's barrier at s_full + 8 b
+  const uint32_t p_full = bar0 + 8u * (3 + 2 * NS);  // block j's at p_full + 8 (j & 1)
+  const uint32_t o_done = bar0 + 8u * (5 + 2 * NS);
+  const uint32_t o_final = bar0 + 8u * (6 + 2 * NS);
+  const uint32_t drain = bar0 + 8u * (7 + 2 * NS);
+  const uint32_t sQ = smem_u32(base + G::OFF_Q);
+  auto sKV = [&](int n) { return smem_u32(base + G::OFF_KV + (n % NS) * G::KV_BYTES); };
+
+  pdl_wait();  // q, k, v (and cu_seqlens) are written by the kernels before
+  pdl_trigger();
+  Work wk;
+  if (!decode_work(p, p.nh, 1, wk)) return;  // uniform over the CTA, before any barrier or TMEM use
+  const int qb = wk.qb, b = wk.b, h = wk.h;
+  const int g = h / (p.nh / p.ng);
+  const int nkv = qb + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(kv_full(i), 1);
+      mbar_init(kv_empty(i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(s_full + 8u * i, 1);
+      mbar_init(p_full + 8u * i, 4);
+    }
+    mbar_init(o_done, 1);
+    mbar_init(o_final, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(&tmQ);
+    tma_prefetch(&tmK);
+    tma_prefetch(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), G::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t tS = tmem_base, tO = tmem_base + 256u;  // score buffer b at tS + 128 b
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, G::Q_BYTES);
+#pragma unroll
+      for (int a = 0; a < D / 64; ++a) tma_load_3d(sQ + a * G::ATOM, &tmQ, q_full, a * 64, wk.q_row0, b * p.nh + h);
+      int n = 0;
+      // one tile (K or V of key block kb) into the next ring slot
+      auto load = [&](const CUtensorMap* map, int kb) {
+        if (!mbar_wait(kv_empty(n), use_parity(n) ^ 1u, p.err, abort_flag)) return false;
+        mbar_arrive_expect_tx(kv_full(n), G::KV_BYTES);
+#pragma unroll
+        for (int a = 0; a < D / 64; ++a)
+          tma_load_3d(sKV(n) + a * G::ATOM, map, kv_full(n), a * 64, wk.kv_row0 + kb * BKV, b * p.ng + g);
+        ++n;
+        return true;
+      };
+      bool ok = load(&tmK, 0) && (nkv < 2 || load(&tmK, 1));
+      for (int j = 0; ok && j < nkv; ++j) ok = load(&tmV, j) && (j + 2 >= nkv || load(&tmK, j + 2));
+      if (!ok) {  // let this CTA's own copies in flight land
+        mbar_wait_slow(q_full, 0, nullptr, nullptr, kDrainLimitNs);
+        for (int m = n - 1; m >= 0 && m >= n - NS; --m)
+          mbar_wait_slow(kv_full(m), use_parity(m), nullptr, nullptr, kDrainLimitNs);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int n = 0;  // next tile of the load sequence
+      auto issue_s = [&](int buf) {  // S into score buffer `buf` from the K tile n
+        const uint32_t ks = sKV(n);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * G::ATOM + (k & 3) * 32;
+          mma_bf16_ss(tS + 128u * buf, sw128_desc(sQ + off), sw128_desc(ks + off), G::IDESC_S, k > 0 ? 1u : 0u);
+        }
+        mma_commit(s_full + 8u * buf);
+        mma_commit(kv_empty(n));
+        ++n;
+      };
+      bool ok = mbar_wait(q_full, 0, p.err, abort_flag) && mbar_wait(kv_full(0), use_parity(0), p.err, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        if (nkv > 1) {
+          ok = mbar_wait(kv_full(n), use_parity(n), p.err, abort_flag);
+          if (ok) issue_s(1);
+        }
+      }
+      for (int j = 0; ok && j < nkv; ++j) {
+        const int buf = j & 1;
+        if (!mbar_wait(kv_full(n), use_parity(n), p.err, abort_flag) ||  // V_j
+            !mbar_wait(p_full + 8u * buf, (j >> 1) & 1, p.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t vs = sKV(n);
+#pragma unroll
+        for (int k = 0; k < BKV / 16; ++k)
+          mma_f16_ts(tO, tS + 128u * buf + 8u * k, sw128_desc_mn(vs + k * 2048, G::ATOM), G::IDESC_O,
+                     (j > 0 || k > 0) ? 1u : 0u);
+        mma_commit(o_done);
+        if (j + 1 == nkv) mma_commit(o_final);
+        mma_commit(kv_empty(n));
+        ++n;
+        if (j + 2 < nkv) {
+          if (!mbar_wait(kv_full(n), use_parity(n), p.err, abort_flag)) {  // K_{j+2}
+            ok = false;
+            break;
+          }
+          issue_s(buf);
+        }
+      }
+      mma_commit(drain);
+      mbar_wait_slow(drain, 0, nullptr, nullptr, ok ? kWaitLimitNs : kDrainLimitNs);
+    }
+  } else {
+    softmax_head_tm<D, true>(p, wk, h, warp & 3, lane, tS, tO, s_full, p_full, abort_flag, o_done, o_final);
+  }
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, G::TMEM_COLS);
+  }
+}
+
+template <int D, int NH>
 cudaError_t launch_tp(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnParams& p,
                       cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tp_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(GeoT<D>::SMEM));
+    cudaError_t e = cudaFuncSetAttribute(NH == 2 ? attn_tp_kernel<D> : attn_db_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(GeoT<D, NH>::SMEM));
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const unsigned grid = static_cast<unsigned>(p.num_qb) * (p.cu ? p.num_seqs : p.batch) * (p.nh / 2);
-  return launch_pdl(attn_tp_kernel<D>, dim3(grid), dim3(320), GeoT<D>::SMEM, stream, tmQ, tmK, tmV, p);
+  const unsigned grid = static_cast<unsigned>(p.num_qb) * (p.cu ? p.num_seqs : p.batch) * (p.nh / NH);
+  return launch_pdl(NH == 2 ? attn_tp_kernel<D> : attn_db_kernel<D>, dim3(grid), dim3(64 + 128 * NH),
+                    GeoT<D, NH>::SMEM, stream, tmQ, tmK, tmV, p);
 }
 
 template <int D, bool TG>
@@ -1041,33 +967,27 @@ cudaError_t launch_d2(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUte
   return launch_pdl(attn2_kernel<D, TG>, dim3(grid), dim3(320), Geo2<D, TG>::SMEM, stream, tmQ, tmK, tmV, p);
 }
 
-template <int D>
-cudaError_t launch_d(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnParams& p,
-                     cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(Geo<D>::SMEM));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  const unsigned grid = static_cast<unsigned>(p.num_qb) * (p.cu ? p.num_seqs : p.batch) * p.nh;
-  return launch_pdl(attn_kernel<D>, dim3(grid), dim3(192), Geo<D>::SMEM, stream, tmQ, tmK, tmV, p);
-}
+// Heads per CTA (set_attention_heads_mode): 0 automatic, 1 one head always, 2 two heads wherever
+// the form allows.
+std::atomic<int> g_heads_mode{0};
 
 }  // namespace
+
+void set_attention_heads_mode(int mode) { g_heads_mode.store(mode); }
 
 cudaError_t launch_attention(int head_dim, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                              const AttnParams& p, cudaStream_t stream) {
   if (p.num_qb <= 0) return cudaSuccess;
-  const bool paired = ((p.nh / p.ng) & 1) == 0;  // an even number of query heads per kv group
-  if (paired && head_dim == 64) return launch_tp<64>(tmQ, tmK, tmV, p, stream);
-  if (paired && head_dim == 128) return launch_tp<128>(tmQ, tmK, tmV, p, stream);
+  if (head_dim != 64 && head_dim != 128) return cudaErrorInvalidValue;
+  const int mode = g_heads_mode.load();
+  const bool even = ((p.nh / p.ng) & 1) == 0;  // an even number of query heads per kv group
   // d = 64 with an odd number of heads per group (MHA): two heads of two groups per CTA
-  if (head_dim == 64 && (p.nh & 1) == 0) return launch_d2<64, true>(tmQ, tmK, tmV, p, stream);
-  if (head_dim == 64) return launch_d<64>(tmQ, tmK, tmV, p, stream);
-  if (head_dim == 128) return launch_d<128>(tmQ, tmK, tmV, p, stream);
-  return cudaErrorInvalidValue;
+  if (mode != 1 && head_dim == 64 && !even && (p.nh & 1) == 0) return launch_d2<64, true>(tmQ, tmK, tmV, p, stream);
+  // two heads of one group per CTA when the two-head CTAs fill the SMs at least twice over
+  const long pair_ctas = static_cast<long>(p.num_qb) * (p.cu ? p.num_seqs : p.batch) * (p.nh / 2);
+  if (even && mode != 1 && (mode == 2 || pair_ctas >= 2L * num_sms()))
+    return head_dim == 64 ? launch_tp<64, 2>(tmQ, tmK, tmV, p, stream) : launch_tp<128, 2>(tmQ, tmK, tmV, p, stream);
+  return head_dim == 64 ? launch_tp<64, 1>(tmQ, tmK, tmV, p, stream) : launch_tp<128, 1>(tmQ, tmK, tmV, p, stream);
 }
 
 }  // namespace mt

@@ -175,6 +175,8 @@ size_t gemm_smem_bytes();
 
 cudaError_t launch_attention(int head_dim, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                              const AttnParams& p, cudaStream_t stream);
+// mt_attn_set_heads_per_cta's mode for every later launch_attention (0, 1 or 2; checked by the caller).
+void set_attention_heads_mode(int mode);
 
 // RoPE table rows written by a norm launch: the CTA of row r writes table row row0 + r when it is
 // below `rows` ((cos, sin) of s * theta_i, i < half).  The caller's norm launches must cover rows

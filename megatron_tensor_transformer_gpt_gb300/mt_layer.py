@@ -68,6 +68,7 @@ _SIGS = {
     "mt_last_error": ([], ctypes.c_char_p),
     "mt_layer_destroy": ([ctypes.c_void_p], None),
     "mt_gemm_set_pairing": ([ctypes.c_int], ctypes.c_int),
+    "mt_attn_set_heads_per_cta": ([ctypes.c_int], ctypes.c_int),
     "mt_gemm_set_tail_split": ([ctypes.c_int], ctypes.c_int),
     "mt_gemm_plan": ([ctypes.c_int] * 9 + [ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
     "mt_gemm_bf16_t": ([ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
@@ -284,6 +285,10 @@ def mt_gemm_bf16_t(A, a_layout, B, b_layout, C, M, N, K, stream):
 
 def mt_gemm_set_pairing(mode):
     _check(lib().mt_gemm_set_pairing(mode))
+
+
+def mt_attn_set_heads_per_cta(mode):
+    _check(lib().mt_attn_set_heads_per_cta(mode))
 
 
 def mt_gemm_set_tail_split(mode):

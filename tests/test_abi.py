@@ -101,6 +101,14 @@ def test_gemm_pairing_mode_is_checked(lib):
         assert lib.mt_gemm_set_pairing(mode) == ml.MT_OK
 
 
+def test_attention_heads_mode_is_checked(lib):
+    assert lib.mt_attn_set_heads_per_cta(3) == ml.MT_ERR_INVALID_ARG
+    assert lib.mt_attn_set_heads_per_cta(-1) == ml.MT_ERR_INVALID_ARG
+    assert "heads-per-CTA" in ml.mt_last_error()
+    for mode in (1, 2, 0):                 # 0 (automatic) is left in place
+        assert lib.mt_attn_set_heads_per_cta(mode) == ml.MT_OK
+
+
 # Llama-3-8B-shaped layer, 4096 tokens, on 152 SMs / 76 resident CTA pairs (epilogue codes:
 # 0 store, 1 residual, 2 QKV, 3 SwiGLU, 4 GeLU)
 LLAMA8B_GEMMS = {

@@ -108,6 +108,7 @@ EDGE = [
     small(batch=2, seq=384, heads=16, groups=2, ffn=1376),     # 8 heads per group
     small(hidden=264, heads=2, groups=2, ffn=520, seq=64),     # hidden and ffn not multiples of 64/128
     small(heads=6, groups=2, seq=300),                         # 3 heads per group: a CTA's two heads straddle groups
+    small(batch=2, seq=300, heads=8, groups=2, head_dim=128),  # GQA d=128, batch 2, three query blocks
 ]
 
 
@@ -122,6 +123,42 @@ def test_layer_matches_oracle_small(cfg, affine):
     dl.layer.status()
     assert_layer_close(to_f64(y), ol.layer_forward(cfg, inp)["y"], cfg.name)
     dl.close()
+
+
+# Attention forms (mt_attn_set_heads_per_cta): the automatic choice takes one head per CTA for all
+# of these small layers; mode 2 forces two heads of one group per CTA (and, for MHA at d = 64, two
+# heads of two groups).  Ragged sequences, batch > 1, an odd number of query blocks, MQA, GQA with
+# eight heads per group.
+ATTN_FORMS = [
+    small(),
+    small(batch=3, seq=200),
+    small(seq=129, heads=4, groups=1, head_dim=128),
+    small(batch=2, seq=300, heads=8, groups=2, head_dim=128),
+    small(batch=2, seq=384, heads=16, groups=2, ffn=1376),
+    small(groups=8, seq=300),                                  # MHA, d = 64
+    small(heads=6, groups=2, seq=300, head_dim=128),           # 3 heads per group
+]
+
+
+@pytest.mark.parametrize("cfg", ATTN_FORMS, ids=lambda c: f"b{c.batch}-s{c.seq}-{c.heads}x{c.groups}x{c.head_dim}")
+def test_attention_forms_match_oracle(cfg):
+    inp = synth.make_inputs(cfg, seed=8, affine="random", biases="random")
+    want = ol.layer_forward(cfg, inp)["y"]
+    ys = {}
+    try:
+        for mode in (1, 2):
+            ml.mt_attn_set_heads_per_cta(mode)
+            dl = DeviceLayer(cfg, inp)
+            y = dl.forward(to_dev(inp["x"]).reshape(cfg.tokens, cfg.hidden))
+            torch.cuda.synchronize()
+            dl.layer.status()
+            ys[mode] = y.clone()
+            assert_layer_close(to_f64(y), want, f"{cfg.name} heads-per-CTA mode {mode}")
+            dl.close()
+    finally:
+        ml.mt_attn_set_heads_per_cta(0)
+    if (cfg.heads // cfg.groups) % 2 == 0:  # one and two heads of one group: the same arithmetic
+        assert torch.equal(ys[1], ys[2])
 
 
 def test_gpt345m_full_layer():
