@@ -68,8 +68,9 @@ def _oracle_pieces(cfg, inp):
     return dict(xn=xn, q=q, k=k, v=v, o=o.reshape(T, nh * d))
 
 
-@pytest.mark.parametrize("cfg", [synth.CONFIGS["tiny"], small(batch=3, seq=200), small(head_dim=128, heads=4, groups=1)],
-                         ids=["tiny", "ragged_b3_s200", "mqa_d128"])
+@pytest.mark.parametrize("cfg", [synth.CONFIGS["tiny"], small(batch=3, seq=200), small(head_dim=128, heads=4, groups=1),
+                                 small(batch=2, seq=130, norm="layer", act="gelu_tanh", bias=True)],
+                         ids=["tiny", "ragged_b3_s200", "mqa_d128", "ln_gelu_b2_s130"])
 def test_intermediates_match_oracle(cfg):
     inp = synth.make_inputs(cfg, seed=21, affine="random")
     dl = DeviceLayer(cfg, inp)
@@ -93,6 +94,8 @@ def test_intermediates_match_oracle(cfg):
     assert_layer_close(reg("o", (T, nh * d)), ref["o"], "attention output")
     full = ol.layer_forward(cfg, inp)
     assert_layer_close(reg("h", (T, cfg.hidden)), full["h"], "h")
+    want_hn = ol.apply_norm(cfg, full["h"], ol._w(inp, "norm2_w"), ol._w(inp, "norm2_b"))
+    assert_layer_close(reg("hn", (T, cfg.hidden)), want_hn, "norm2")
     assert_layer_close(to_f64(y), full["y"], "y")
     dl.close()
 
@@ -343,10 +346,12 @@ def test_host_path_chunked_copies_match(cfg):
     dl.close()
 
 
-def test_launch_count_and_profile_mask():
-    """A dense forward launches seven kernels (the RoPE table rides on norm1); a slot mask brackets
-    only the selected slot."""
-    cfg = small()
+@pytest.mark.parametrize("norm", ["rms", "layer"])
+def test_launch_count_and_profile_mask(norm):
+    """A dense forward launches seven kernels (the RoPE table rides on norm1), with either norm; a
+    slot mask brackets only the selected slot."""
+    launches = 7
+    cfg = small(norm=norm)
     inp = synth.make_inputs(cfg, seed=5)
     dl = DeviceLayer(cfg, inp)
     x = to_dev(inp["x"]).reshape(cfg.tokens, cfg.hidden)
@@ -360,7 +365,7 @@ def test_launch_count_and_profile_mask():
     torch.cuda.synchronize()
     prof = ml.mt_layer_profile_read(dl.layer.handle)
     ml.mt_layer_profile_enable(dl.layer.handle, False)
-    assert ml.mt_layer_launch_count(dl.layer.handle) - n0 == 14
+    assert ml.mt_layer_launch_count(dl.layer.handle) - n0 == 2 * launches
     assert prof["gemm_fc1"][0] == 2 and prof["gemm_fc1"][1] > 0
     assert all(n == 0 for k, (n, _) in prof.items() if k != "gemm_fc1")
     with pytest.raises(ml.MtError):
