@@ -357,11 +357,18 @@ int mt_selftest_bounded_wait(int limit_us);
  * as kernel arguments), then the layer's kernels.  All calls share the one area, which keeps the
  * last call's contents: calls whose work overlaps on the GPU (other streams, other host threads)
  * race and corrupt each other's results.  Device-side timeouts are recorded in the area's error
- * word but cannot be read back through this entry point. */
+ * word (cleared at the start of each call), which mt_layer_forward_static_status reads. */
 #define MT_STATIC_AREA_BYTES (32u << 20)
 int mt_layer_forward_static(int hidden, int heads, int query_groups, int head_dim, int ffn, int norm, int act,
                             float rope_base, int tp_size, int tp_rank, float eps, const void* x, int seq, int batch,
                             const mt_weights* w, void* y_partial, void* cuda_stream);
+
+/* Outcome of the last mt_layer_forward_static call on this device: waits for the work queued on
+ * cuda_stream (the stream that call used), then reads the static area's error word with one
+ * device-to-host copy into host stack memory (no allocation).  MT_ERR_DEVICE_TIMEOUT when a kernel
+ * of that call gave up on a bounded barrier wait (its outputs are invalid), MT_OK otherwise.  The
+ * word is cleared by the next static call, not by this one. */
+int mt_layer_forward_static_status(void* cuda_stream);
 
 #ifdef __cplusplus
 }

@@ -1729,3 +1729,22 @@ extern "C" int mt_layer_forward_static(int hidden, int heads, int query_groups, 
   return rc ? rc : ok();
 }
 
+extern "C" int mt_layer_forward_static_status(void* cuda_stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  void* base = nullptr;
+  int rc = static_area(dev, &base);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  int code = 0;  // the copy to pageable memory returns once the stream's earlier work and the copy are done
+  e = cudaMemcpyAsync(&code, base, sizeof(int), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the static area's error word");
+  if (code != 0)
+    return fail(MT_ERR_DEVICE_TIMEOUT,
+                "a kernel of the last static call stopped waiting on a barrier (device code %d); its outputs are invalid",
+                code);
+  return ok();
+}
+

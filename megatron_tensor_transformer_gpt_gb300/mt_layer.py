@@ -104,6 +104,7 @@ _SIGS = {
                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_int,
                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                ctypes.c_void_p], ctypes.c_int),
+    "mt_layer_forward_static_status": ([ctypes.c_void_p], ctypes.c_int),
     "mt_layer_forward_static": ([ctypes.c_int] * 7 + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_float,
                                                       ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                                       ctypes.POINTER(MtWeights), ctypes.c_void_p, ctypes.c_void_p],
@@ -222,6 +223,10 @@ def mt_layer_profile_read(handle):
     launches, ms = (ctypes.c_int * n)(), (ctypes.c_double * n)()
     _check(lib().mt_layer_profile_read(handle, launches, ms))
     return {PROFILE_SLOTS[i]: (launches[i], ms[i]) for i in range(n)}
+
+
+def mt_layer_forward_static_status(stream):
+    _check(lib().mt_layer_forward_static_status(stream))
 
 
 def mt_layer_forward_static(hidden, heads, query_groups, head_dim, ffn, norm, act, rope_base, tp_size, tp_rank, eps,

@@ -51,6 +51,7 @@ def test_static_forward_matches_oracle_and_handle_on_two_calls(cfg):
     free0 = torch.cuda.mem_get_info()[0]
     for y in ys[1:]:
         _static_forward(cfg, dl, x, y)
+        ml.mt_layer_forward_static_status(torch.cuda.current_stream().cuda_stream)  # no timeout recorded
         torch.cuda.synchronize()
         assert torch.cuda.mem_get_info()[0] == free0, "a static call changed the device's free memory"
     for y in ys:
