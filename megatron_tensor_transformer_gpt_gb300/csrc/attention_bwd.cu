@@ -39,29 +39,44 @@ __global__ void head_slices_kernel(const bf16* __restrict__ src, size_t sp, size
   }
 }
 
-// D[(b * nh + h) * S + s] = sum_c dO[s b, h c] * O[s b, h c]  (both [S * B, nh * d] bf16), one warp
-// per (token, head).
+// The same copy, 16 bytes (8 columns) per thread, when C, the pitches and the slice offsets are
+// multiples of 8 elements (16-byte aligned rows): x indexes 8-column groups, y rows.
+__global__ void head_slices_vec_kernel(const bf16* __restrict__ src, size_t sp, size_t sb, size_t sh, int zdiv,
+                                       bf16* __restrict__ dst, size_t dp, int R, int C8) {
+  const int z = blockIdx.z;
+  const bf16* s = src + (z / zdiv) * sb + (z % zdiv) * sh;
+  bf16* d = dst + static_cast<size_t>(z) * R * dp;
+  const int c = blockIdx.x * blockDim.x + threadIdx.x, r = blockIdx.y * blockDim.y + threadIdx.y;
+  if (r < R && c < C8)
+    *reinterpret_cast<uint4*>(d + static_cast<size_t>(r) * dp + 8 * c) =
+        *reinterpret_cast<const uint4*>(s + static_cast<size_t>(r) * sp + 8 * c);
+}
+
+// D[(b * nh + h) * S + s] = sum_c dO[s b, h c] * O[s b, h c]  (both [S * B, nh * d] bf16, d = 64 or
+// 128): d / 8 lanes per (token, head), each taking 8 columns, so a warp covers 32 / (d / 8) rows.
 __global__ void row_dot_kernel(const bf16* __restrict__ dO, const bf16* __restrict__ O, float* __restrict__ Dsum,
                                int S, int B, int nh, int d) {
-  const size_t wid = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
+  const int L = d >> 3;  // lanes per row, a power of two dividing 32
+  const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const size_t rowi = tid / L;
+  const int sub = static_cast<int>(tid % L);
   const size_t rows = static_cast<size_t>(S) * B * nh;
-  if (wid >= rows) return;
-  const int h = static_cast<int>(wid % nh);
-  const size_t t = wid / nh;  // token s * B + b
-  const int b = static_cast<int>(t % B), s = static_cast<int>(t / B);
-  const size_t off = t * static_cast<size_t>(nh) * d + static_cast<size_t>(h) * d;
+  const int h = static_cast<int>(rowi % nh);
+  const size_t t = rowi / nh;  // token s * B + b
   float acc = 0.f;
-  for (int c = lane * 8; c < d; c += 256) {
+  if (rowi < rows) {
+    const size_t off = t * static_cast<size_t>(nh) * d + static_cast<size_t>(h) * d + sub * 8;
     float a[8], o[8];
-    unpack_bf16x8(*reinterpret_cast<const uint4*>(dO + off + c), a);
-    unpack_bf16x8(*reinterpret_cast<const uint4*>(O + off + c), o);
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(dO + off), a);
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(O + off), o);
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc += a[e] * o[e];
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) Dsum[(static_cast<size_t>(b) * nh + h) * S + s] = acc;
+  for (int o = L >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);  // inside the row's lanes
+  if (rowi < rows && sub == 0) {
+    const int b = static_cast<int>(t % B), s = static_cast<int>(t / B);
+    Dsum[(static_cast<size_t>(b) * nh + h) * S + s] = acc;
+  }
 }
 
 // Bounded wait shared by the roles below (records the error and raises the CTA's abort flag).
@@ -566,14 +581,22 @@ cudaError_t launch_bwd_d(const CUtensorMap* maps, const AttnBwdParams& p, cudaSt
 cudaError_t launch_head_slices(const bf16* src, size_t sp, size_t sb, size_t sh, int zdiv, int Z, bf16* dst, size_t dp,
                                int R, int C, cudaStream_t st) {
   if (Z <= 0 || R <= 0 || C <= 0) return cudaSuccess;
-  head_slices_kernel<<<dim3((C + 31) / 32, (R + 31) / 32, Z), dim3(32, 8), 0, st>>>(src, sp, sb, sh, zdiv, dst, dp, R, C);
+  const bool vec = C % 8 == 0 && sp % 8 == 0 && sb % 8 == 0 && sh % 8 == 0 && dp % 8 == 0 &&
+                   reinterpret_cast<uintptr_t>(src) % 16 == 0 && reinterpret_cast<uintptr_t>(dst) % 16 == 0;
+  if (vec)
+    head_slices_vec_kernel<<<dim3((C / 8 + 15) / 16, (R + 15) / 16, Z), dim3(16, 16), 0, st>>>(src, sp, sb, sh, zdiv,
+                                                                                              dst, dp, R, C / 8);
+  else
+    head_slices_kernel<<<dim3((C + 31) / 32, (R + 31) / 32, Z), dim3(32, 8), 0, st>>>(src, sp, sb, sh, zdiv, dst, dp, R,
+                                                                                     C);
   return cudaGetLastError();
 }
 
 cudaError_t launch_row_dot(const bf16* dO, const bf16* O, float* Dsum, int S, int B, int nh, int d, cudaStream_t st) {
-  const size_t warps = static_cast<size_t>(S) * B * nh;
-  if (warps == 0) return cudaSuccess;
-  row_dot_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, st>>>(dO, O, Dsum, S, B, nh, d);
+  if (d != 64 && d != 128) return cudaErrorInvalidValue;
+  const size_t threads = static_cast<size_t>(S) * B * nh * (d / 8);
+  if (threads == 0) return cudaSuccess;
+  row_dot_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, st>>>(dO, O, Dsum, S, B, nh, d);
   return cudaGetLastError();
 }
 

@@ -111,7 +111,8 @@ __device__ __forceinline__ float2 cta_sum2(float a, float b, float2* red) {
 }
 
 // One CTA per kNormBwdRows rows; each thread holds VPT 8-column vectors of a row in registers (x
-// and dy read once, 16 bytes at a time).  partial[blockIdx.x, :] = sum over the CTA's rows of
+// and dy read once, 16 bytes at a time); the next row's x and dy, and the current row's `add`, are
+// loaded while the current row is reduced, so the rows' load latencies overlap.  partial[blockIdx.x, :] = sum over the CTA's rows of
 // dy * xhat (and, LayerNorm, partial[gridDim.x + blockIdx.x, :] = sum of dy), folded over the CTAs
 // by the column-sum kernel into d gamma (d beta).
 template <int VPT, bool LN>
@@ -136,22 +137,37 @@ __global__ void __launch_bounds__(1024) norm_bwd_kernel(const bf16* __restrict__
     for (int e = 0; e < 8; ++e) pg[i][e] = pb[i][e] = 0.f;
   }
   const int r_end = min(T, static_cast<int>(blockIdx.x + 1) * kNormBwdRows);
-  for (int row = blockIdx.x * kNormBwdRows; row < r_end; ++row) {
+  // raw 16-byte vectors of x and dy of a row (zero past the row's end)
+  uint4 rx[VPT], rg[VPT];
+  auto fetch = [&](int row) {
     const size_t base = static_cast<size_t>(row) * nvec;
-    float xv[VPT][8], gv[VPT][8];
-    float s1 = 0.f, s2 = 0.f;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
       const int idx = i * blockDim.x + threadIdx.x;
       const bool in = idx < nvec;
-      unpack_bf16x8(in ? reinterpret_cast<const uint4*>(x)[base + idx] : make_uint4(0u, 0u, 0u, 0u), xv[i]);
-      unpack_bf16x8(in ? reinterpret_cast<const uint4*>(dy)[base + idx] : make_uint4(0u, 0u, 0u, 0u), gv[i]);
+      rx[i] = in ? reinterpret_cast<const uint4*>(x)[base + idx] : make_uint4(0u, 0u, 0u, 0u);
+      rg[i] = in ? reinterpret_cast<const uint4*>(dy)[base + idx] : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  if (static_cast<int>(blockIdx.x) * kNormBwdRows < r_end) fetch(blockIdx.x * kNormBwdRows);
+  for (int row = blockIdx.x * kNormBwdRows; row < r_end; ++row) {
+    const size_t base = static_cast<size_t>(row) * nvec;
+    float xv[VPT][8], gv[VPT][8];
+    uint4 rad[VPT];
+    float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int idx = i * blockDim.x + threadIdx.x;
+      unpack_bf16x8(rx[i], xv[i]);
+      unpack_bf16x8(rg[i], gv[i]);
+      rad[i] = (idx < nvec && add != nullptr) ? reinterpret_cast<const uint4*>(add)[base + idx] : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         s1 += xv[i][e];
         s2 += xv[i][e] * xv[i][e];
       }
     }
+    if (row + 1 < r_end) fetch(row + 1);
     float mean = 0.f, var;
     if (LN) {  // two-pass variance from the registers
       mean = cta_sum2(s1, 0.f, red).x * inv_h;
@@ -185,12 +201,7 @@ __global__ void __launch_bounds__(1024) norm_bwd_kernel(const bf16* __restrict__
       const int idx = i * blockDim.x + threadIdx.x;
       if (idx >= nvec) continue;
       float ad[8], o[8];
-      if (add != nullptr) {
-        unpack_bf16x8(reinterpret_cast<const uint4*>(add)[base + idx], ad);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) ad[e] = 0.f;
-      }
+      unpack_bf16x8(rad[i], ad);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float xh = (xv[i][e] - mean) * r;
