@@ -1201,10 +1201,12 @@ int mt_layer_forward_host(mt_layer* L, const void* x_host, int seq, int batch, c
   void* yd = region<void>(L, lay, kYStage);
   const size_t bytes = lay.size[kXStage];
   const int T = seq * batch;
-  // Row chunks at multiples of the 256-row GEMM tile, about 2048 rows or more each (two to four):
-  // smaller chunks cost the split GEMMs more than they hide (four chunks of a 4096-token layer
-  // measured slower than two).
-  const int n = T < 512 ? 1 : std::min(kMaxChunks, std::max(2, T / 2048));
+  // Row chunks at multiples of the 256-row GEMM tile, about 1024 rows or more each (two to four).
+  // The first input chunk's copy and the last output chunk's copy are not hidden, so smaller chunks
+  // hide more, while every QKV or fc2 chunk below one wave of tiles still costs a whole tile time.
+  // 4096 tokens on one box: two chunks 1.341-1.360 ms per step, four 1.292-1.314 ms, eight input
+  // chunks (with four output chunks) 1.367-1.379 ms.
+  const int n = T < 512 ? 1 : std::min(kMaxChunks, std::max(2, T / 1024));
   if (n > 1 && pinned(x_host) && pinned(y_host)) {
     // Overlap the copies with the layer: x arrives in n row chunks on the copy stream and norm1 + QKV
     // of chunk c run as soon as it is in; fc2 runs per chunk and each chunk of y is copied back while
