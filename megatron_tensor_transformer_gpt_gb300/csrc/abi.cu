@@ -973,12 +973,11 @@ int backward_device(mt_layer* L, const BwLayout& b, const void* x, const void* d
   count_launch(L);
   if ((e = mt::launch_row_dot(dO, o, dsum, S, B, nh, d, st)) != cudaSuccess) return cuda_fail(e, "rowsum(dO o O)");
   {
-    CUtensorMap m[8];
+    CUtensorMap m[6];
     const uint64_t Zq = zq, Zk = zk;
     if ((rc = map_3d(&m[0], q, d, S, Zq, d, sd, 128)) || (rc = map_3d(&m[1], dOh, d, S, Zq, d, sd, 128)) ||
-        (rc = map_3d(&m[2], k, d, S, Zk, d, sd, 64)) || (rc = map_3d(&m[3], Vh, d, S, Zk, d, sd, 64)) ||
-        (rc = map_3d(&m[4], k, d, S, Zk, d, sd, 128)) || (rc = map_3d(&m[5], Vh, d, S, Zk, d, sd, 128)) ||
-        (rc = map_3d(&m[6], q, d, S, Zq, d, sd, 64)) || (rc = map_3d(&m[7], dOh, d, S, Zq, d, sd, 64)))
+        (rc = map_3d(&m[2], k, d, S, Zk, d, sd, 128)) || (rc = map_3d(&m[3], Vh, d, S, Zk, d, sd, 128)) ||
+        (rc = map_3d(&m[4], q, d, S, Zq, d, sd, 64)) || (rc = map_3d(&m[5], dOh, d, S, Zq, d, sd, 64)))
       return rc;
     mt::AttnBwdParams ap{};
     ap.seq = S;

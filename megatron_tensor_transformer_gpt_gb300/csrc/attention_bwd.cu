@@ -4,14 +4,15 @@
 // scores S = Q K^T, P = softmax(S / sqrt(d)) and D_i = dO_i . O_i:
 //     dS = P o (dP - D) / sqrt(d),  dP = dO V^T,
 //     dV = P^T dO,  dK = dS^T Q,  dQ = dS K   (dK, dV summed over the query heads of a group).
-// Two kernels, each a producer warp (TMA), one MMA-issuing thread (tcgen05) and eight elementwise
-// warps: two per TMEM lane quadrant, one row per thread, each warp taking half of a step's 64
-// columns:
-//   attn_bwd_dq_kernel:   one CTA per (128 queries, head); steps over 64-key blocks j <= i:
+// Two kernels, each a producer warp (TMA), one MMA-issuing thread (tcgen05) and elementwise warps
+// (one row per thread, a TMEM lane quadrant per warp):
+//   attn_bwd_dq_kernel:   one CTA per (128 queries, head); steps over 128-key blocks j <= i with
+//                         sixteen elementwise warps (32 of a step's 128 columns each): Q in TMEM,
 //                         S and dP into TMEM, dS (bf16) into shared memory, dQ += dS K in TMEM.
 //   attn_bwd_dkdv_kernel: one CTA per (128 keys, kv group); steps over the group's heads and the
-//                         64-query blocks i >= j: S^T and dP^T into TMEM, P^T and dS^T into shared
-//                         memory, dV += P^T dO and dK += dS^T Q in TMEM.
+//                         64-query blocks i >= j with eight elementwise warps (32 of a step's 64
+//                         columns each): S^T and dP^T into TMEM, P^T and dS^T into shared memory,
+//                         dV += P^T dO and dK += dS^T Q in TMEM.
 // The caller provides head-major copies of dO and V (head_slices_kernel below); the second operands of the
 // gradient products (K for dQ, dO for dV, Q for dK) are the tiles already staged for the score
 // products, read as MN-major operands.
@@ -92,27 +93,50 @@ __device__ __forceinline__ void store_row_chunk(uint8_t* row, int r, int ch, con
 }
 
 // ------------------------------------------------------------------ dQ
+// One CTA per (128 queries, head), stepping over the 128-key blocks j <= i, so that every product
+// has N = 128 (N = d for dQ).  Q moves to tensor memory once, as the A operand of S, and the
+// elementwise warps write dS there too, as the A operand of dQ += dS K (two bf16 per 32-bit
+// column): the tensor core then reads only K, V and dO from shared memory, which holds dO, a
+// three-slot K ring and a two-slot V ring.  K_j feeds S_j (read K-major) and, one step later,
+// dQ += dS_j K_j (read MN-major), so its slot is released after that; V_j feeds dP_j only.  One
+// barrier per step (two in turn) completes when both K_j and V_j have landed.
+//   TMEM: S [0, 128), dP [128, 256), dQ [256, 256 + d), Q [384, 384 + d/2), dS [448, 512).
+//   Two issuing threads: warp 1 issues S_n and dP_n for every step, the last warp dQ += dS_n K_n once
+//   dS_n is written, so that neither's waits stall the other's products; a K slot is free once
+//   both have committed its last product.
+//   Sixteen elementwise warps, four per TMEM lane quadrant, each taking 32 of a step's 128 columns.
 template <int D>
 struct GeoQ {
-  static constexpr int QD_BYTES = 128 * D * 2;          // Q_i or dO_i: D/64 blocks of [128 x 64]
-  static constexpr int K_BYTES = 64 * D * 2;            // K_j or V_j: D/64 blocks of [64 x 64]
-  static constexpr int STAGE = 2 * K_BYTES;             // K, V of one key block
-  static constexpr int NSTG = 3;                        // key blocks in flight
-  static constexpr int DS_BYTES = 128 * 64 * 2;         // dS [128 queries x 64 keys]
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_DO = QD_BYTES;
-  static constexpr int OFF_ST = 2 * QD_BYTES;
-  static constexpr int OFF_DS = OFF_ST + NSTG * STAGE;
-  static constexpr int OFF_BAR = OFF_DS + 2 * DS_BYTES;
+  static constexpr int QD_BYTES = 128 * D * 2;      // Q_i or dO_i: D/64 blocks of [128 x 64]
+  static constexpr int KV_BYTES = 128 * D * 2;      // K_j or V_j: D/64 blocks of [128 x 64]
+  static constexpr int NK = 3, NV = 2;              // K and V ring slots
+  static constexpr int OFF_DO = 0;
+  static constexpr int OFF_QS = QD_BYTES;           // Q, on its way to tensor memory
+  static constexpr int OFF_K = OFF_QS + QD_BYTES;
+  static constexpr int OFF_V = OFF_K + NK * KV_BYTES;
+  static constexpr int OFF_BAR = OFF_V + NV * KV_BYTES;
   static constexpr size_t SMEM_USED = 1024 + OFF_BAR + 256;
   static constexpr size_t SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;  // one CTA per SM (TMEM)
-  static constexpr uint32_t IDESC_S = idesc_bf16(128, 64);
+  static constexpr int EW = 16;                     // elementwise warps
+  static constexpr int THREADS = 96 + 32 * EW;      // producer, S/dP issuer, elementwise, dQ issuer
+  static constexpr uint32_t IDESC_S = idesc_bf16(128, 128);
   static constexpr uint32_t IDESC_Q = idesc_bf16_bmn(128, D);  // B = K_j read MN-major
 };
 static_assert(GeoQ<128>::SMEM_USED <= 232448, "dQ tiles exceed the shared memory of a CTA");
 
+// Each thread writes 16 consecutive 32-bit columns of its own TMEM lane and waits for the write.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(GeoQ<D>::THREADS, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                        const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                        const AttnBwdParams p) {
@@ -120,21 +144,18 @@ __global__ void __launch_bounds__(320, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + G::OFF_BAR);
-  // bars: q_full | kv_full[3] | kv_empty[3] | s_full[2] | s_free[2] | ds_full[2] | ds_free[2] | done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  // bars: q_full | kv_full[2] | k_empty[3] | v_empty[2] | q_tm | s_full | s_free | ds_full | ds_free | done | sp_done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
-  const uint32_t q_full = bar0, done = bar0 + 8u * 15;
-  auto kv_full = [&](int i) { return bar0 + 8u * (1 + i); };
-  auto kv_empty = [&](int i) { return bar0 + 8u * (4 + i); };
-  auto s_full = [&](int i) { return bar0 + 8u * (7 + i); };
-  auto s_free = [&](int i) { return bar0 + 8u * (9 + i); };
-  auto ds_full = [&](int i) { return bar0 + 8u * (11 + i); };
-  auto ds_free = [&](int i) { return bar0 + 8u * (13 + i); };
-  const uint32_t sQ = smem_u32(base + G::OFF_Q), sDO = smem_u32(base + G::OFF_DO);
-  auto sK = [&](int st) { return smem_u32(base + G::OFF_ST + st * G::STAGE); };
-  auto sV = [&](int st) { return smem_u32(base + G::OFF_ST + st * G::STAGE + G::K_BYTES); };
-  auto sDS = [&](int i) { return smem_u32(base + G::OFF_DS + i * G::DS_BYTES); };
+  const uint32_t q_full = bar0, q_tm = bar0 + 8u * 8, s_full = bar0 + 8u * 9, s_free = bar0 + 8u * 10,
+                 ds_full = bar0 + 8u * 11, ds_free = bar0 + 8u * 12, done = bar0 + 8u * 13, sp_done = bar0 + 8u * 14;
+  auto kv_full = [&](int n) { return bar0 + 8u * (1 + (n & 1)); };
+  auto k_empty = [&](int n) { return bar0 + 8u * (3 + n % G::NK); };
+  auto v_empty = [&](int n) { return bar0 + 8u * (6 + n % G::NV); };
+  const uint32_t sDO = smem_u32(base + G::OFF_DO), sQS = smem_u32(base + G::OFF_QS);
+  auto sK = [&](int n) { return smem_u32(base + G::OFF_K + (n % G::NK) * G::KV_BYTES); };
+  auto sV = [&](int n) { return smem_u32(base + G::OFF_V + (n % G::NV) * G::KV_BYTES); };
 
   pdl_wait();
   pdl_trigger();
@@ -143,22 +164,22 @@ __global__ void __launch_bounds__(320, 1)
   const int zq = static_cast<int>(blockIdx.x) % per;                  // b * nh + h
   const int b = zq / p.nh, h = zq % p.nh;
   const int zk = b * p.ng + h / (p.nh / p.ng);
-  const int nst = min(2 * qb + 2, (p.seq + 63) / 64);  // 64-key blocks j with 64 j <= last query
+  const int nst = qb + 1;  // 128-key blocks j <= qb (keys past seq arrive as zeros and are masked)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < G::NSTG; ++i) {
-      mbar_init(kv_full(i), 1);
-      mbar_init(kv_empty(i), 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(s_full(i), 1);
-      mbar_init(s_free(i), 8);
-      mbar_init(ds_full(i), 8);
-      mbar_init(ds_free(i), 1);
-    }
+    mbar_init(kv_full(0), 1);
+    mbar_init(kv_full(1), 1);
+    for (int i = 0; i < G::NK; ++i) mbar_init(k_empty(i), 2);  // after S_n (warp 1) and dQ_n (last warp)
+    for (int i = 0; i < G::NV; ++i) mbar_init(v_empty(i), 1);
+    mbar_init(q_tm, D / 8);  // the warps that move Q: D/32 per lane quadrant
+    mbar_init(s_full, 1);
+    mbar_init(s_free, G::EW);
+    mbar_init(ds_full, G::EW);
+    mbar_init(ds_free, 1);
     mbar_init(done, 1);
+    mbar_init(sp_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -176,127 +197,163 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  auto tS = [&](int i) { return tmem_base + 64u * i; };
-  auto tP = [&](int i) { return tmem_base + 128u + 64u * i; };
-  const uint32_t tQ = tmem_base + 256u;
+  const uint32_t tS = tmem_base, tP = tmem_base + 128u, tQ = tmem_base + 256u, tQa = tmem_base + 384u,
+                 tDS = tmem_base + 448u;
 
   if (warp == 0) {
     if (lane == 0) {
       mbar_arrive_expect_tx(q_full, 2 * G::QD_BYTES);
 #pragma unroll
       for (int a = 0; a < D / 64; ++a) {
-        tma_load_3d(sQ + a * ATOM128, &tmQ, q_full, a * 64, qb * 128, zq);
+        tma_load_3d(sQS + a * ATOM128, &tmQ, q_full, a * 64, qb * 128, zq);
         tma_load_3d(sDO + a * ATOM128, &tmDO, q_full, a * 64, qb * 128, zq);
       }
       int issued = 0;
       bool ok = true;
       for (int n = 0; n < nst; ++n) {
-        const int st = n % G::NSTG;
-        if (!mbar_wait(kv_empty(st), ((n / G::NSTG) & 1) ^ 1u, p.err, abort_flag)) {
+        if (!mbar_wait(k_empty(n), ((n / G::NK) & 1) ^ 1u, p.err, abort_flag) ||
+            !mbar_wait(v_empty(n), ((n / G::NV) & 1) ^ 1u, p.err, abort_flag)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(kv_full(st), G::STAGE);
+        mbar_arrive_expect_tx(kv_full(n), 2 * G::KV_BYTES);
 #pragma unroll
         for (int a = 0; a < D / 64; ++a) {
-          tma_load_3d(sK(st) + a * ATOM64, &tmK, kv_full(st), a * 64, n * 64, zk);
-          tma_load_3d(sV(st) + a * ATOM64, &tmV, kv_full(st), a * 64, n * 64, zk);
+          tma_load_3d(sK(n) + a * ATOM128, &tmK, kv_full(n), a * 64, n * 128, zk);
+          tma_load_3d(sV(n) + a * ATOM128, &tmV, kv_full(n), a * 64, n * 128, zk);
         }
         ++issued;
       }
       if (!ok) {  // let this CTA's own copies in flight land
         mbar_wait_slow(q_full, 0, nullptr, nullptr, kDrainLimitNs);
-        for (int n = issued - 1; n >= 0 && n >= issued - G::NSTG; --n)
-          mbar_wait_slow(kv_full(n % G::NSTG), (n / G::NSTG) & 1, nullptr, nullptr, kDrainLimitNs);
+        for (int n = issued - 1; n >= 0 && n >= issued - 2; --n)
+          mbar_wait_slow(kv_full(n), (n >> 1) & 1, nullptr, nullptr, kDrainLimitNs);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      bool ok = mbar_wait(q_full, 0, p.err, abort_flag);
-      auto issue_dq = [&](int m) -> bool {  // dQ += dS(m) K_m, K_m read MN-major (d contiguous)
-        const int i = m & 1, st = m % G::NSTG;
-        if (!mbar_wait(ds_full(i), (m >> 1) & 1, p.err, abort_flag)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_bf16_ss(tQ, sw128_desc(sDS(i) + k * 32), sw128_desc_mn(sK(st) + k * 2048, ATOM64), G::IDESC_Q,
-                      (m > 0 || k > 0) ? 1u : 0u);
-        mma_commit(ds_free(i));
-        mma_commit(kv_empty(st));
-        return true;
-      };
+    if (lane == 0) {  // S_n = Q K_n^T (Q from tensor memory) and dP_n = dO V_n^T
+      bool ok = mbar_wait(q_full, 0, p.err, abort_flag) && mbar_wait(q_tm, 0, p.err, abort_flag);
       for (int n = 0; ok && n < nst; ++n) {
-        const int i = n & 1, st = n % G::NSTG;
-        const uint32_t ph = (n >> 1) & 1;
-        if (!mbar_wait(kv_full(st), (n / G::NSTG) & 1, p.err, abort_flag) ||
-            (n >= 2 && !mbar_wait(s_free(i), ph ^ 1u, p.err, abort_flag))) {
+        if (!mbar_wait(kv_full(n), (n >> 1) & 1, p.err, abort_flag) ||
+            (n >= 1 && !mbar_wait(s_free, (n - 1) & 1, p.err, abort_flag))) {
           ok = false;
           break;
         }
         tc_fence_after();
+        const uint32_t sk = sK(n), sv = sV(n);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {  // S = Q K^T and dP = dO V^T for keys 64 n ..
-          const uint32_t oq = (k >> 2) * ATOM128 + (k & 3) * 32, ok_ = (k >> 2) * ATOM64 + (k & 3) * 32;
-          mma_bf16_ss(tS(i), sw128_desc(sQ + oq), sw128_desc(sK(st) + ok_), G::IDESC_S, k > 0 ? 1u : 0u);
-          mma_bf16_ss(tP(i), sw128_desc(sDO + oq), sw128_desc(sV(st) + ok_), G::IDESC_S, k > 0 ? 1u : 0u);
+        for (int k = 0; k < D / 16; ++k)
+          mma_f16_ts(tS, tQa + 8u * k, sw128_desc(sk + (k >> 2) * ATOM128 + (k & 3) * 32), G::IDESC_S,
+                     k > 0 ? 1u : 0u);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * ATOM128 + (k & 3) * 32;
+          mma_bf16_ss(tP, sw128_desc(sDO + off), sw128_desc(sv + off), G::IDESC_S, k > 0 ? 1u : 0u);
         }
-        mma_commit(s_full(i));
-        if (n >= 1 && !issue_dq(n - 1)) ok = false;
+        mma_commit(s_full);
+        mma_commit(v_empty(n));
+        mma_commit(k_empty(n));
       }
-      if (ok && nst > 0) ok = issue_dq(nst - 1);
+      mma_commit(sp_done);
+      mbar_wait_slow(sp_done, 0, nullptr, nullptr, ok ? kWaitLimitNs : kDrainLimitNs);
+    }
+  } else if (warp == 2 + G::EW) {
+    if (lane == 0) {  // dQ += dS_m K_m, dS from tensor memory, K_m read MN-major
+      bool ok = true;
+      for (int m = 0; ok && m < nst; ++m) {
+        if (!mbar_wait(ds_full, m & 1, p.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sk = sK(m);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_f16_ts(tQ, tDS + 8u * k, sw128_desc_mn(sk + k * 2048, ATOM128), G::IDESC_Q, (m > 0 || k > 0) ? 1u : 0u);
+        mma_commit(ds_free);
+        mma_commit(k_empty(m));
+      }
       mma_commit(done);
       mbar_wait_slow(done, 0, nullptr, nullptr, ok ? kWaitLimitNs : kDrainLimitNs);
     }
   } else {
-    const int quad = warp & 3, half = (warp - 2) >> 2;  // columns [32 half, 32 half + 32) of a step
+    const int quad = warp & 3, c4 = (warp - 2) >> 2;  // columns [32 c4, 32 c4 + 32) of a step
     const int r = quad * 32 + lane;
     const int qi = qb * 128 + r;  // query row
     const bool row_ok = qi < p.seq;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const size_t rix = static_cast<size_t>(zq) * p.seq + qi;
-    const float lse = row_ok ? p.lse[rix] : 0.f;
+    // P / sqrt(d) = 2^(s c - lse + log2(1/sqrt(d))): the scale folds into the exponent; a row past
+    // seq gets P = 0 through lse = +inf
+    const float lse = row_ok ? p.lse[rix] - log2f(p.scale) : __int_as_float(0x7f800000);
     const float dsum = row_ok ? p.dsum[rix] : 0.f;
     bool ok = true;
-    for (int n = 0; n < nst; ++n) {
-      const int i = n & 1;
-      const uint32_t ph = (n >> 1) & 1;
-      if (!wait_all(s_full(i), ph, p.err, abort_flag)) {
+    if (c4 < D / 32) {  // Q into tensor memory: this warp's 32 elements as 16 columns of bf16 pairs
+      ok = wait_all(q_full, 0, p.err, abort_flag);
+      if (ok) {
+        const uint8_t* row = base + G::OFF_QS + (c4 >> 1) * ATOM128 + r * 128;
+        uint32_t w[16];
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          const uint4 v = *reinterpret_cast<const uint4*>(row + (((4 * (c4 & 1) + ch) ^ (r & 7)) << 4));
+          w[4 * ch] = v.x;
+          w[4 * ch + 1] = v.y;
+          w[4 * ch + 2] = v.z;
+          w[4 * ch + 3] = v.w;
+        }
+        tmem_st16(tQa + lane_off + 16 * c4, w);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(q_tm);
+      }
+    }
+    for (int n = 0; ok && n < nst; ++n) {
+      if (!wait_all(s_full, n & 1, p.err, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float s[32], dp[32];
-      tmem_ld32(tS(i) + lane_off + 32 * half, s);
-      tmem_ld32(tP(i) + lane_off + 32 * half, dp);
+      uint32_t su[32], du[32];
+      tmem_ld32_issue(tS + lane_off + 32 * c4, su);
+      tmem_ld32_issue(tP + lane_off + 32 * c4, du);
+      tmem_ld32_wait(su);
+      tmem_ld32_wait(du);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(s_free(i));
+      if (lane == 0) mbar_arrive(s_free);
+      uint32_t w[16];  // dS as bf16 pairs
+      if (n < qb) {  // below the diagonal block every key is visible
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const bool valid = row_ok && n * 64 + 32 * half + c <= qi;
-        const float pv = valid ? ex2_approx(s[c] * p.scale_log2 - lse) : 0.f;
-        s[c] = pv * (dp[c] - dsum) * p.scale;  // dS
+        for (int c = 0; c < 32; c += 2) {
+          const float p0 = ex2_approx(__uint_as_float(su[c]) * p.scale_log2 - lse);
+          const float p1 = ex2_approx(__uint_as_float(su[c + 1]) * p.scale_log2 - lse);
+          w[c >> 1] = pack_bf16x2(p0 * (__uint_as_float(du[c]) - dsum), p1 * (__uint_as_float(du[c + 1]) - dsum));
+        }
+      } else {
+        const int key0 = n * 128 + 32 * c4;
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const float p0 = key0 + c <= qi ? ex2_approx(__uint_as_float(su[c]) * p.scale_log2 - lse) : 0.f;
+          const float p1 = key0 + c + 1 <= qi ? ex2_approx(__uint_as_float(su[c + 1]) * p.scale_log2 - lse) : 0.f;
+          w[c >> 1] = pack_bf16x2(p0 * (__uint_as_float(du[c]) - dsum), p1 * (__uint_as_float(du[c + 1]) - dsum));
+        }
       }
-      if (n >= 2 && !wait_all(ds_free(i), ph ^ 1u, p.err, abort_flag)) {
+      if (n >= 1 && !wait_all(ds_free, (n - 1) & 1, p.err, abort_flag)) {
         ok = false;
         break;
       }
-      uint8_t* row = base + G::OFF_DS + i * G::DS_BYTES + r * 128;
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) store_row_chunk(row, r, 4 * half + ch, s + 8 * ch);
-      fence_proxy_async_smem();
+      tmem_st16(tDS + lane_off + 16 * c4, w);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(ds_full(i));
+      if (lane == 0) mbar_arrive(ds_full);
     }
     if (ok && wait_all(done, 0, p.err, abort_flag)) {
       tc_fence_after();
-#pragma unroll 1
-      for (int cc = half * (D / 64); cc < (half + 1) * (D / 64); ++cc) {
+      if (c4 < D / 32) {
         float v[32];
-        tmem_ld32(tQ + lane_off + cc * 32, v);
+        tmem_ld32(tQ + lane_off + 32 * c4, v);
         if (row_ok) {
-          float4* dst = reinterpret_cast<float4*>(p.dq + rix * D + cc * 32);
+          float4* dst = reinterpret_cast<float4*>(p.dq + rix * D + 32 * c4);
 #pragma unroll
           for (int g = 0; g < 8; ++g) dst[g] = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
         }
@@ -568,12 +625,12 @@ cudaError_t launch_bwd_d(const CUtensorMap* maps, const AttnBwdParams& p, cudaSt
     configured = true;
   }
   const unsigned nb = static_cast<unsigned>((p.seq + 127) / 128);
-  // maps: Q128, dO128, K64, V64 | K128, V128, Q64, dO64
-  cudaError_t e = launch_pdl(attn_bwd_dq_kernel<D>, dim3(nb * p.batch * p.nh), dim3(320), GeoQ<D>::SMEM, st,
-                             maps[0], maps[1], maps[2], maps[3], p);
+  // maps: Q, dO, K, V as 128-row boxes; Q, dO as 64-row boxes
+  cudaError_t e = launch_pdl(attn_bwd_dq_kernel<D>, dim3(nb * p.batch * p.nh), dim3(GeoQ<D>::THREADS), GeoQ<D>::SMEM,
+                             st, maps[0], maps[1], maps[2], maps[3], p);
   if (e != cudaSuccess) return e;
-  return launch_pdl(attn_bwd_dkdv_kernel<D>, dim3(nb * p.batch * p.ng), dim3(320), GeoKV<D>::SMEM, st, maps[4],
-                    maps[5], maps[6], maps[7], p);
+  return launch_pdl(attn_bwd_dkdv_kernel<D>, dim3(nb * p.batch * p.ng), dim3(320), GeoKV<D>::SMEM, st, maps[2],
+                    maps[3], maps[4], maps[5], p);
 }
 
 }  // namespace
