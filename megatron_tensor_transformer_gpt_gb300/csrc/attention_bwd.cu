@@ -4,15 +4,14 @@
 // scores S = Q K^T, P = softmax(S / sqrt(d)) and D_i = dO_i . O_i:
 //     dS = P o (dP - D) / sqrt(d),  dP = dO V^T,
 //     dV = P^T dO,  dK = dS^T Q,  dQ = dS K   (dK, dV summed over the query heads of a group).
-// Two kernels, each a producer warp (TMA), one MMA-issuing thread (tcgen05) and elementwise warps
-// (one row per thread, a TMEM lane quadrant per warp):
-//   attn_bwd_dq_kernel:   one CTA per (128 queries, head); steps over 128-key blocks j <= i with
-//                         sixteen elementwise warps (32 of a step's 128 columns each): Q in TMEM,
-//                         S and dP into TMEM, dS (bf16) into shared memory, dQ += dS K in TMEM.
+// Two kernels, each a producer warp (TMA), two MMA-issuing threads (tcgen05: one for the score
+// products, one for the gradient products, so that neither's waits stall the other) and sixteen
+// elementwise warps (one row per thread, four warps per TMEM lane quadrant):
+//   attn_bwd_dq_kernel:   one CTA per (128 queries, head); steps over 128-key blocks j <= i:
+//                         Q in TMEM, S and dP into TMEM, dS (bf16) into TMEM, dQ += dS K in TMEM.
 //   attn_bwd_dkdv_kernel: one CTA per (128 keys, kv group); steps over the group's heads and the
-//                         64-query blocks i >= j with eight elementwise warps (32 of a step's 64
-//                         columns each): S^T and dP^T into TMEM, P^T and dS^T into shared memory,
-//                         dV += P^T dO and dK += dS^T Q in TMEM.
+//                         64-query blocks i >= j: S^T and dP^T into TMEM, P^T and dS^T (bf16) into
+//                         TMEM, dV += P^T dO and dK += dS^T Q in TMEM.
 // The caller provides head-major copies of dO and V (head_slices_kernel below); the second operands of the
 // gradient products (K for dQ, dO for dV, Q for dK) are the tiles already staged for the score
 // products, read as MN-major operands.
@@ -84,12 +83,6 @@ __global__ void row_dot_kernel(const bf16* __restrict__ dO, const bf16* __restri
 __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, int* err, volatile int* abort_flag) {
   const bool ok = mbar_wait(bar, parity, err, abort_flag);
   return __all_sync(0xffffffffu, ok);
-}
-
-// Eight values of row r, as bf16 (one 16-byte chunk), into chunk ch of the row's 128 bytes in a
-// K-major tile with the 128-byte swizzle: chunk ch of row r sits at ((ch ^ (r & 7)) << 4).
-__device__ __forceinline__ void store_row_chunk(uint8_t* row, int r, int ch, const float* v8) {
-  *reinterpret_cast<uint4*>(row + ((ch ^ (r & 7)) << 4)) = pack_bf16x8(v8);
 }
 
 // ------------------------------------------------------------------ dQ
@@ -232,6 +225,9 @@ __global__ void __launch_bounds__(GeoQ<D>::THREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {  // S_n = Q K_n^T (Q from tensor memory) and dP_n = dO V_n^T
+      uint64_t ddo[D / 16];  // dO stays put: its descriptors are built once
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) ddo[k] = sw128_desc(sDO + (k >> 2) * ATOM128 + (k & 3) * 32);
       bool ok = mbar_wait(q_full, 0, p.err, abort_flag) && mbar_wait(q_tm, 0, p.err, abort_flag);
       for (int n = 0; ok && n < nst; ++n) {
         if (!mbar_wait(kv_full(n), (n >> 1) & 1, p.err, abort_flag) ||
@@ -240,16 +236,13 @@ __global__ void __launch_bounds__(GeoQ<D>::THREADS, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t sk = sK(n), sv = sV(n);
+        const uint64_t dk = sw128_desc(sK(n)), dv = sw128_desc(sV(n));
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_f16_ts(tS, tQa + 8u * k, sw128_desc(sk + (k >> 2) * ATOM128 + (k & 3) * 32), G::IDESC_S,
-                     k > 0 ? 1u : 0u);
+          mma_f16_ts(tS, tQa + 8u * k, desc_add(dk, (k >> 2) * ATOM128 + (k & 3) * 32), G::IDESC_S, k > 0 ? 1u : 0u);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * ATOM128 + (k & 3) * 32;
-          mma_bf16_ss(tP, sw128_desc(sDO + off), sw128_desc(sv + off), G::IDESC_S, k > 0 ? 1u : 0u);
-        }
+        for (int k = 0; k < D / 16; ++k)
+          mma_bf16_ss(tP, ddo[k], desc_add(dv, (k >> 2) * ATOM128 + (k & 3) * 32), G::IDESC_S, k > 0 ? 1u : 0u);
         mma_commit(s_full);
         mma_commit(v_empty(n));
         mma_commit(k_empty(n));
@@ -266,10 +259,10 @@ __global__ void __launch_bounds__(GeoQ<D>::THREADS, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t sk = sK(m);
+        const uint64_t dk = sw128_desc_mn(sK(m), ATOM128);
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_f16_ts(tQ, tDS + 8u * k, sw128_desc_mn(sk + k * 2048, ATOM128), G::IDESC_Q, (m > 0 || k > 0) ? 1u : 0u);
+          mma_f16_ts(tQ, tDS + 8u * k, desc_add(dk, k * 2048), G::IDESC_Q, (m > 0 || k > 0) ? 1u : 0u);
         mma_commit(ds_free);
         mma_commit(k_empty(m));
       }
@@ -369,48 +362,91 @@ __global__ void __launch_bounds__(GeoQ<D>::THREADS, 1)
 }
 
 // ------------------------------------------------------------------ dK, dV
+// One CTA per (128 keys, kv group), stepping over the group's heads and, per head, the 64-query
+// blocks i >= j.  K and V stay in shared memory (the A operands of S^T = K Q^T and dP^T = V dO^T);
+// a ring of Q and dO blocks feeds those products (read K-major) and the gradient products
+// dV += P^T dO and dK += dS^T Q (read MN-major).  S^T and dP^T are double-buffered in tensor
+// memory; the elementwise warps write P^T over S^T and dS^T over dP^T (bf16 pairs in the first 32
+// columns of each), the A operands of the gradient products, and the sums over the group's heads
+// happen in the dV and dK accumulators.
+//   TMEM: buffer b: S^T [128 b, 128 b + 64), dP^T [128 b + 64, 128 b + 128); dV [256, 256 + d),
+//         dK [384, 384 + d).
+//   Two issuing threads: warp 1 issues S^T_n and dP^T_n into buffer n % 2 once the gradient
+//   products of step n - 2 have read it, the last warp dV and dK once P^T_n and dS^T_n are written;
+//   a ring slot is free once both have committed its last product.
+//   Sixteen elementwise warps, four per TMEM lane quadrant, each taking 16 of a step's 64 columns;
+//   the four warps of a quadrant meet at a named barrier between reading S^T, dP^T and writing
+//   P^T, dS^T over them (a warp's P^T columns hold other warps' S^T columns).
 template <int D>
 struct GeoKV {
   static constexpr int KV_BYTES = 128 * D * 2;            // K_j or V_j: D/64 blocks of [128 x 64]
   static constexpr int QD_BYTES = 64 * D * 2;             // Q_i or dO_i: D/64 blocks of [64 x 64]
   static constexpr int STAGE = 2 * QD_BYTES;
-  static constexpr int NSTG = 4;                          // query blocks in flight
-  static constexpr int PT_BYTES = 128 * 64 * 2;           // P^T or dS^T [128 keys x 64 queries]
+  static constexpr int NSTG = D == 128 ? 5 : 8;           // query blocks in flight
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = KV_BYTES;
   static constexpr int OFF_ST = 2 * KV_BYTES;
-  static constexpr int OFF_PT = OFF_ST + NSTG * STAGE;
-  static constexpr int OFF_DST = OFF_PT + PT_BYTES;
-  static constexpr int OFF_BAR = OFF_DST + PT_BYTES;
+  static constexpr int OFF_BAR = OFF_ST + NSTG * STAGE;
   static constexpr size_t SMEM_USED = 1024 + OFF_BAR + 256;
   static constexpr size_t SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
+  static constexpr int EW = 16;
+  static constexpr int THREADS = 96 + 32 * EW;            // producer, S/dP issuer, elementwise, gradient issuer
   static constexpr uint32_t IDESC_S = idesc_bf16(128, 64);
   static constexpr uint32_t IDESC_G = idesc_bf16_bmn(128, D);  // B = dO_i or Q_i read MN-major
 };
 static_assert(GeoKV<128>::SMEM_USED <= 232448, "dK/dV tiles exceed the shared memory of a CTA");
 
+// 16 consecutive fp32 columns of the thread's TMEM lane, split into issue and wait (see tmem_ld32_issue).
+__device__ __forceinline__ void tmem_ld16_issue(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld16_wait(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
+}
+// Each thread writes 8 consecutive 32-bit columns of its own TMEM lane (no wait).
+__device__ __forceinline__ void tmem_st8_nowait(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Named barrier of the four elementwise warps that share TMEM lane quadrant q (ids 1-4).
+__device__ __forceinline__ void quad_sync(int q) {
+  asm volatile("bar.sync %0, 128;" ::"r"(1 + q) : "memory");
+}
+
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(GeoKV<D>::THREADS, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                          const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                          const AttnBwdParams p) {
   using G = GeoKV<D>;
+  constexpr int NS = G::NSTG;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + G::OFF_BAR);
-  // bars: kv_full | st_full[4] | st_empty[4] | s_full[2] | s_free[2] | pt_full | pt_free | done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  // bars: kv_full | st_full[NS] | st_empty[NS] | s_full[2] | pt_full[2] | g_done[2] | done | sp_done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 9 + 2 * NS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
-  const uint32_t kv_full = bar0, pt_full = bar0 + 8u * 13, pt_free = bar0 + 8u * 14, done = bar0 + 8u * 15;
-  auto st_full = [&](int i) { return bar0 + 8u * (1 + i); };
-  auto st_empty = [&](int i) { return bar0 + 8u * (5 + i); };
-  auto s_full = [&](int i) { return bar0 + 8u * (9 + i); };
-  auto s_free = [&](int i) { return bar0 + 8u * (11 + i); };
+  const uint32_t kv_full = bar0, done = bar0 + 8u * (7 + 2 * NS), sp_done = bar0 + 8u * (8 + 2 * NS);
+  // step n uses buffer n & 1; its barriers complete phase n / 2
+  auto s_full = [&](int n) { return bar0 + 8u * (1 + 2 * NS + (n & 1)); };
+  auto pt_full = [&](int n) { return bar0 + 8u * (3 + 2 * NS + (n & 1)); };
+  auto g_done = [&](int n) { return bar0 + 8u * (5 + 2 * NS + (n & 1)); };
+  auto st_full = [&](int n) { return bar0 + 8u * (1 + n % NS); };
+  auto st_empty = [&](int n) { return bar0 + 8u * (1 + NS + n % NS); };
   const uint32_t sK = smem_u32(base + G::OFF_K), sV = smem_u32(base + G::OFF_V);
-  auto sQ = [&](int st) { return smem_u32(base + G::OFF_ST + st * G::STAGE); };
-  auto sDO = [&](int st) { return smem_u32(base + G::OFF_ST + st * G::STAGE + G::QD_BYTES); };
-  const uint32_t sPT = smem_u32(base + G::OFF_PT), sDST = smem_u32(base + G::OFF_DST);
+  auto sQ = [&](int n) { return smem_u32(base + G::OFF_ST + (n % NS) * G::STAGE); };
+  auto sDO = [&](int n) { return smem_u32(base + G::OFF_ST + (n % NS) * G::STAGE + G::QD_BYTES); };
 
   pdl_wait();
   pdl_trigger();
@@ -427,17 +463,17 @@ __global__ void __launch_bounds__(320, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int i = 0; i < G::NSTG; ++i) {
+    for (int i = 0; i < NS; ++i) {
       mbar_init(st_full(i), 1);
-      mbar_init(st_empty(i), 1);
+      mbar_init(st_empty(i), 2);  // after S^T/dP^T (warp 1) and after dV/dK (last warp)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(s_full(i), 1);
-      mbar_init(s_free(i), 8);
+      mbar_init(pt_full(i), G::EW);
+      mbar_init(g_done(i), 1);
     }
-    mbar_init(pt_full, 8);
-    mbar_init(pt_free, 1);
     mbar_init(done, 1);
+    mbar_init(sp_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -455,9 +491,9 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  auto tS = [&](int i) { return tmem_base + 64u * i; };
-  auto tP = [&](int i) { return tmem_base + 128u + 64u * i; };
-  const uint32_t tV = tmem_base + 256u, tK = tmem_base + 256u + D;
+  auto tS = [&](int n) { return tmem_base + 128u * (n & 1); };        // S^T, then P^T
+  auto tP = [&](int n) { return tmem_base + 128u * (n & 1) + 64u; };  // dP^T, then dS^T
+  const uint32_t tV = tmem_base + 256u, tK = tmem_base + 384u;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -470,136 +506,188 @@ __global__ void __launch_bounds__(320, 1)
       int issued = 0;
       bool ok = true;
       for (int n = 0; n < nst; ++n) {
-        const int st = n % G::NSTG;
         const int zq = b * p.nh + g * rep + n / per_head;
         const int qi0 = (i0 + n % per_head) * 64;
-        if (!mbar_wait(st_empty(st), ((n / G::NSTG) & 1) ^ 1u, p.err, abort_flag)) {
+        if (!mbar_wait(st_empty(n), ((n / NS) & 1) ^ 1u, p.err, abort_flag)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(st_full(st), G::STAGE);
+        mbar_arrive_expect_tx(st_full(n), G::STAGE);
 #pragma unroll
         for (int a = 0; a < D / 64; ++a) {
-          tma_load_3d(sQ(st) + a * ATOM64, &tmQ, st_full(st), a * 64, qi0, zq);
-          tma_load_3d(sDO(st) + a * ATOM64, &tmDO, st_full(st), a * 64, qi0, zq);
+          tma_load_3d(sQ(n) + a * ATOM64, &tmQ, st_full(n), a * 64, qi0, zq);
+          tma_load_3d(sDO(n) + a * ATOM64, &tmDO, st_full(n), a * 64, qi0, zq);
         }
         ++issued;
       }
       if (!ok) {
         mbar_wait_slow(kv_full, 0, nullptr, nullptr, kDrainLimitNs);
-        for (int n = issued - 1; n >= 0 && n >= issued - G::NSTG; --n)
-          mbar_wait_slow(st_full(n % G::NSTG), (n / G::NSTG) & 1, nullptr, nullptr, kDrainLimitNs);
+        for (int n = issued - 1; n >= 0 && n >= issued - NS; --n)
+          mbar_wait_slow(st_full(n), (n / NS) & 1, nullptr, nullptr, kDrainLimitNs);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      bool ok = mbar_wait(kv_full, 0, p.err, abort_flag);
-      auto issue_grad = [&](int m) -> bool {  // dV += P^T dO, dK += dS^T Q for step m (dO, Q MN-major)
-        const int st = m % G::NSTG;
-        if (!mbar_wait(pt_full, m & 1, p.err, abort_flag)) return false;
-        tc_fence_after();
+    if (lane == 0) {  // S^T = K Q^T and dP^T = V dO^T for one 64-query block
+      uint64_t dk[D / 16], dv[D / 16];  // K and V stay put: their descriptors are built once
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          mma_bf16_ss(tV, sw128_desc(sPT + k * 32), sw128_desc_mn(sDO(st) + k * 2048, ATOM64), G::IDESC_G,
-                      (m > 0 || k > 0) ? 1u : 0u);
-          mma_bf16_ss(tK, sw128_desc(sDST + k * 32), sw128_desc_mn(sQ(st) + k * 2048, ATOM64), G::IDESC_G,
-                      (m > 0 || k > 0) ? 1u : 0u);
-        }
-        mma_commit(pt_free);
-        mma_commit(st_empty(st));
-        return true;
-      };
+      for (int k = 0; k < D / 16; ++k) {
+        dk[k] = sw128_desc(sK + (k >> 2) * ATOM128 + (k & 3) * 32);
+        dv[k] = sw128_desc(sV + (k >> 2) * ATOM128 + (k & 3) * 32);
+      }
+      bool ok = mbar_wait(kv_full, 0, p.err, abort_flag);
       for (int n = 0; ok && n < nst; ++n) {
-        const int i = n & 1, st = n % G::NSTG;
-        const uint32_t ph = (n >> 1) & 1;
-        if (!mbar_wait(st_full(st), (n / G::NSTG) & 1, p.err, abort_flag) ||
-            (n >= 2 && !mbar_wait(s_free(i), ph ^ 1u, p.err, abort_flag))) {
+        if (!mbar_wait(st_full(n), (n / NS) & 1, p.err, abort_flag) ||
+            (n >= 2 && !mbar_wait(g_done(n), ((n >> 1) - 1) & 1, p.err, abort_flag))) {
           ok = false;
           break;
         }
         tc_fence_after();
+        const uint64_t dq = sw128_desc(sQ(n)), ddo = sw128_desc(sDO(n));
+        const uint32_t ts = tS(n), tp = tP(n);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {  // S^T = K Q^T and dP^T = V dO^T for one 64-query block
-          const uint32_t okv = (k >> 2) * ATOM128 + (k & 3) * 32, oq = (k >> 2) * ATOM64 + (k & 3) * 32;
-          mma_bf16_ss(tS(i), sw128_desc(sK + okv), sw128_desc(sQ(st) + oq), G::IDESC_S, k > 0 ? 1u : 0u);
-          mma_bf16_ss(tP(i), sw128_desc(sV + okv), sw128_desc(sDO(st) + oq), G::IDESC_S, k > 0 ? 1u : 0u);
-        }
-        mma_commit(s_full(i));
-        if (n >= 1 && !issue_grad(n - 1)) ok = false;
+        for (int k = 0; k < D / 16; ++k)
+          mma_bf16_ss(ts, dk[k], desc_add(dq, (k >> 2) * ATOM64 + (k & 3) * 32), G::IDESC_S, k > 0 ? 1u : 0u);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          mma_bf16_ss(tp, dv[k], desc_add(ddo, (k >> 2) * ATOM64 + (k & 3) * 32), G::IDESC_S, k > 0 ? 1u : 0u);
+        mma_commit(s_full(n));
+        mma_commit(st_empty(n));
       }
-      if (ok && nst > 0) ok = issue_grad(nst - 1);
+      mma_commit(sp_done);
+      mbar_wait_slow(sp_done, 0, nullptr, nullptr, ok ? kWaitLimitNs : kDrainLimitNs);
+    }
+  } else if (warp == 2 + G::EW) {
+    if (lane == 0) {  // dV += P^T dO and dK += dS^T Q (P^T, dS^T from tensor memory; dO, Q MN-major)
+      bool ok = true;
+      for (int m = 0; ok && m < nst; ++m) {
+        if (!mbar_wait(pt_full(m), (m >> 1) & 1, p.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t dq = sw128_desc_mn(sQ(m), ATOM64), ddo = sw128_desc_mn(sDO(m), ATOM64);
+        const uint32_t ts = tS(m), tp = tP(m);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_f16_ts(tV, ts + 8u * k, desc_add(ddo, k * 2048), G::IDESC_G, (m > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_f16_ts(tK, tp + 8u * k, desc_add(dq, k * 2048), G::IDESC_G, (m > 0 || k > 0) ? 1u : 0u);
+        mma_commit(g_done(m));
+        mma_commit(st_empty(m));
+      }
       mma_commit(done);
       mbar_wait_slow(done, 0, nullptr, nullptr, ok ? kWaitLimitNs : kDrainLimitNs);
     }
   } else {
-    const int quad = warp & 3, half = (warp - 2) >> 2;  // query columns [32 half, 32 half + 32) of a step
+    const int quad = warp & 3, c4 = (warp - 2) >> 2;  // query columns [16 c4, 16 c4 + 16) of a step
     const int r = quad * 32 + lane;
     const int kj = kb * 128 + r;  // key row
     const bool row_ok = kj < p.seq;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    // the statistics of a step's columns come by 16-byte loads when rows are 16-byte aligned
+    const bool vec = (p.seq & 3) == 0 && (reinterpret_cast<uintptr_t>(p.lse) & 15) == 0 &&
+                     (reinterpret_cast<uintptr_t>(p.dsum) & 15) == 0;
+    // every warp of a quadrant passes the quadrant barrier once per step, also after a failed wait
+    // (it then skips the step's work), so that no warp is left at the barrier
     bool ok = true;
     for (int n = 0; n < nst; ++n) {
-      const int i = n & 1;
-      const uint32_t ph = (n >> 1) & 1;
+      if (!ok) {
+        quad_sync(quad);
+        continue;
+      }
       const int zq = b * p.nh + g * rep + n / per_head;
-      const int qc0 = (i0 + n % per_head) * 64 + 32 * half;  // this warp's first query column
-      // lane l holds the row statistics of query qc0 + l; column c reads them from lane c
-      const int ql = min(qc0 + lane, p.seq - 1);
-      const float lse_l = __ldg(p.lse + static_cast<size_t>(zq) * p.seq + ql);
-      const float dsum_l = __ldg(p.dsum + static_cast<size_t>(zq) * p.seq + ql);
-      if (!wait_all(s_full(i), ph, p.err, abort_flag)) {
+      const int qc0 = (i0 + n % per_head) * 64 + 16 * c4;  // this warp's first query column
+      // the 16 columns' row statistics, the same for every lane (one broadcast load each); columns
+      // past seq read the last row's (their P^T and dS^T multiply zero rows of dO and Q)
+      // dsum is kept as D / sqrt(d), so that dS^T = P^T (dP^T / sqrt(d) - D / sqrt(d)) is one FMA and a product
+      float lse[16], dsum[16];
+      const size_t s0 = static_cast<size_t>(zq) * p.seq;
+      if (vec && qc0 + 16 <= p.seq) {
+#pragma unroll
+        for (int c = 0; c < 16; c += 4) {
+          const float4 a = __ldg(reinterpret_cast<const float4*>(p.lse + s0 + qc0 + c));
+          const float4 d = __ldg(reinterpret_cast<const float4*>(p.dsum + s0 + qc0 + c));
+          lse[c] = a.x;
+          lse[c + 1] = a.y;
+          lse[c + 2] = a.z;
+          lse[c + 3] = a.w;
+          dsum[c] = d.x * p.scale;
+          dsum[c + 1] = d.y * p.scale;
+          dsum[c + 2] = d.z * p.scale;
+          dsum[c + 3] = d.w * p.scale;
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int q = min(qc0 + c, p.seq - 1);
+          lse[c] = __ldg(p.lse + s0 + q);
+          dsum[c] = __ldg(p.dsum + s0 + q) * p.scale;
+        }
+      }
+      if (!wait_all(s_full(n), (n >> 1) & 1, p.err, abort_flag)) {
         ok = false;
-        break;
+        quad_sync(quad);
+        continue;
       }
       tc_fence_after();
-      float s[32], dp[32];
-      tmem_ld32(tS(i) + lane_off + 32 * half, s);
-      tmem_ld32(tP(i) + lane_off + 32 * half, dp);
+      const uint32_t ts = tS(n) + lane_off, tp = tP(n) + lane_off;
+      uint32_t su[16], du[16];
+      tmem_ld16_issue(ts + 16 * c4, su);
+      tmem_ld16_issue(tp + 16 * c4, du);
+      tmem_ld16_wait(su);
+      tmem_ld16_wait(du);
+      tc_fence_before();
+      quad_sync(quad);  // the quadrant's four warps have read S^T and dP^T
+      tc_fence_after();
+      uint32_t wp[8], wd[8];  // P^T and dS^T as bf16 pairs
+      const bool below = qc0 >= kb * 128 + 127;  // every key of the block precedes every query of these columns
+#pragma unroll
+      for (int c = 0; c < 16; c += 2) {
+        float p0 = ex2_approx(__uint_as_float(su[c]) * p.scale_log2 - lse[c]);
+        float p1 = ex2_approx(__uint_as_float(su[c + 1]) * p.scale_log2 - lse[c + 1]);
+        if (!below) {
+          p0 = qc0 + c >= kj ? p0 : 0.f;
+          p1 = qc0 + c + 1 >= kj ? p1 : 0.f;
+        }
+        wp[c >> 1] = pack_bf16x2(p0, p1);
+        wd[c >> 1] = pack_bf16x2(p0 * fmaf(__uint_as_float(du[c]), p.scale, -dsum[c]),
+                                 p1 * fmaf(__uint_as_float(du[c + 1]), p.scale, -dsum[c + 1]));
+      }
+      tmem_st8_nowait(ts + 8 * c4, wp);
+      tmem_st8_nowait(tp + 8 * c4, wd);
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(s_free(i));
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const int qi = qc0 + c;
-        const float lse_c = __shfl_sync(0xffffffffu, lse_l, c);
-        const float dsum_c = __shfl_sync(0xffffffffu, dsum_l, c);
-        const bool valid = row_ok && qi < p.seq && qi >= kj;
-        const float pv = valid ? ex2_approx(s[c] * p.scale_log2 - lse_c) : 0.f;
-        s[c] = pv;                                    // P^T
-        dp[c] = pv * (dp[c] - dsum_c) * p.scale;      // dS^T
-      }
-      if (n >= 1 && !wait_all(pt_free, (n - 1) & 1, p.err, abort_flag)) {
-        ok = false;
-        break;
-      }
-      uint8_t* prow = base + G::OFF_PT + r * 128;
-      uint8_t* drow = base + G::OFF_DST + r * 128;
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        store_row_chunk(prow, r, 4 * half + ch, s + 8 * ch);
-        store_row_chunk(drow, r, 4 * half + ch, dp + 8 * ch);
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(pt_full);
+      if (lane == 0) mbar_arrive(pt_full(n));
     }
     if (ok && wait_all(done, 0, p.err, abort_flag)) {
       tc_fence_after();
       const size_t row = static_cast<size_t>(zk) * p.seq + kj;
-#pragma unroll 1
-      for (int cc = half * (D / 64); cc < (half + 1) * (D / 64); ++cc) {
-        float v[32], k32[32];
-        tmem_ld32(tV + lane_off + cc * 32, v);
-        tmem_ld32(tK + lane_off + cc * 32, k32);
-        if (row_ok) {
-          float4* dv = reinterpret_cast<float4*>(p.dv + row * D + cc * 32);
-          float4* dk = reinterpret_cast<float4*>(p.dk + row * D + cc * 32);
+      constexpr int W = D / 4;  // columns of dV and dK per warp
+      float v[W], k32[W];
+      if (W == 32) {
+        tmem_ld32(tV + lane_off + W * c4, v);
+        tmem_ld32(tK + lane_off + W * c4, k32);
+      } else {
+        uint32_t a[16], c[16];
+        tmem_ld16_issue(tV + lane_off + W * c4, a);
+        tmem_ld16_issue(tK + lane_off + W * c4, c);
+        tmem_ld16_wait(a);
+        tmem_ld16_wait(c);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            dv[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-            dk[q] = make_float4(k32[4 * q], k32[4 * q + 1], k32[4 * q + 2], k32[4 * q + 3]);
-          }
+        for (int i = 0; i < 16; ++i) {
+          v[i] = __uint_as_float(a[i]);
+          k32[i] = __uint_as_float(c[i]);
+        }
+      }
+      if (row_ok) {
+        float4* dv = reinterpret_cast<float4*>(p.dv + row * D + W * c4);
+        float4* dk = reinterpret_cast<float4*>(p.dk + row * D + W * c4);
+#pragma unroll
+        for (int q = 0; q < W / 4; ++q) {
+          dv[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          dk[q] = make_float4(k32[4 * q], k32[4 * q + 1], k32[4 * q + 2], k32[4 * q + 3]);
         }
       }
     }
@@ -629,8 +717,8 @@ cudaError_t launch_bwd_d(const CUtensorMap* maps, const AttnBwdParams& p, cudaSt
   cudaError_t e = launch_pdl(attn_bwd_dq_kernel<D>, dim3(nb * p.batch * p.nh), dim3(GeoQ<D>::THREADS), GeoQ<D>::SMEM,
                              st, maps[0], maps[1], maps[2], maps[3], p);
   if (e != cudaSuccess) return e;
-  return launch_pdl(attn_bwd_dkdv_kernel<D>, dim3(nb * p.batch * p.ng), dim3(320), GeoKV<D>::SMEM, st, maps[2],
-                    maps[3], maps[4], maps[5], p);
+  return launch_pdl(attn_bwd_dkdv_kernel<D>, dim3(nb * p.batch * p.ng), dim3(GeoKV<D>::THREADS), GeoKV<D>::SMEM, st,
+                    maps[2], maps[3], maps[4], maps[5], p);
 }
 
 }  // namespace
