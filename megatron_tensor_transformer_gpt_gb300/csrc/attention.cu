@@ -732,7 +732,10 @@ __global__ void __launch_bounds__(320, 1)
       }
       for (int j = 0; ok && j < nkv; ++j) {
         const int nv = 2 * j + 1, nk = 2 * j + 2;  // tiles V_j and K_{j+1}
-        if (!mbar_wait(kv_full(nv), use_parity(nv), p.err, abort_flag)) {
+        // both tiles' waits back to back, ahead of the block's MMAs: a wait stops the MMA stream, and a
+        // second wait right after the first costs far less than one between MMAs
+        if (!mbar_wait(kv_full(nv), use_parity(nv), p.err, abort_flag) ||
+            (j + 1 < nkv && !mbar_wait(kv_full(nk), use_parity(nk), p.err, abort_flag))) {
           ok = false;
           break;
         }
@@ -746,13 +749,7 @@ __global__ void __launch_bounds__(320, 1)
           for (int k = 0; k < BKV / 16; ++k)
             mma_f16_ts(tO(t), tS(t) + 8u * k, sw128_desc_mn(sKV(nv) + k * 2048, G::ATOM), G::IDESC_O,
                        (j > 0 || k > 0) ? 1u : 0u);
-          if (j + 1 < nkv) {
-            if (t == 0 && !mbar_wait(kv_full(nk), use_parity(nk), p.err, abort_flag)) {
-              ok = false;
-              break;
-            }
-            issue_s(t, nk);
-          }
+          if (j + 1 < nkv) issue_s(t, nk);
           mma_commit(s_full(t));
         }
         if (!ok) break;

@@ -24,6 +24,11 @@ namespace {
 constexpr int ATOM128 = 128 * 128;  // [128 rows x 64] bf16 block with the 128-byte swizzle, 16 KB
 constexpr int ATOM64 = 64 * 128;    // [64 rows x 64] block, 8 KB
 
+// `desc` advanced by `bytes` (a multiple of 16): the start-address field holds (address & 0x3FFFF) >> 4
+// and no shared-memory address of a CTA reaches 2^18, so the advance is a plain add that never
+// carries out of the field.  Lets a loop build each descriptor once and step it.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
 // ------------------------------------------------------------------ prep
 // Batched copy of the R x C slices src_z = src + (z / zdiv) * sb + (z % zdiv) * sh (row pitch sp) into
 // dst + z R dp (row pitch dp): the head-major copies of dO and V.

@@ -158,11 +158,6 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
-// `desc` advanced by `bytes` (a multiple of 16): the start-address field holds (address & 0x3FFFF) >> 4
-// and no shared-memory address of a CTA reaches 2^18, so the advance is a plain add that never
-// carries out of the field.  Lets a loop build each descriptor once and step it.
-__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
-
 // Shared-memory descriptor of an MN-major operand stored with the 128-byte swizzle: each 128-byte
 // row holds 64 consecutive M (or N) elements at one K index, 8-row K groups are 1024 B apart and
 // further 64-element M (N) blocks `mn_block_bytes` apart (the leading byte offset); advancing K by
