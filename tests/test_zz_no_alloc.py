@@ -71,3 +71,34 @@ def test_static_forward_rejects_workspace_beyond_the_area():
                                    ml.MtWeights(), x.data_ptr(), None)
     assert e.value.code == ml.MT_ERR_UNSUPPORTED
     assert "static area" in str(e.value)
+
+
+def test_static_forward_replays_from_a_cuda_graph():
+    """After its first call a static call is stream-ordered device work only (no allocation, no
+    host copy or synchronisation), so it can be captured in a CUDA graph under the global capture
+    mode, which rejects any of those; the replay equals an eager static call bit for bit."""
+    torch.cuda.set_device(0)
+    cfg = synth.LayerConfig("static_graph", batch=1, seq=256, hidden=512, heads=8, groups=2, head_dim=128, ffn=1024,
+                            rope_base=5e5, bias=True)
+    inp = synth.make_inputs(cfg, seed=33, affine="random", biases="random")
+    dl = DeviceLayer(cfg, inp)
+    x = to_dev(inp["x"]).reshape(cfg.tokens, cfg.hidden)
+    want = torch.full((cfg.tokens, cfg.hidden), float("nan"), dtype=torch.bfloat16, device="cuda")
+    _static_forward(cfg, dl, x, want)  # eager: the first call on the device happens outside the capture
+    torch.cuda.synchronize()
+    y = torch.full_like(want, float("nan"))
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side, capture_error_mode="global"):
+            _static_forward(cfg, dl, x, y)
+    torch.cuda.current_stream().wait_stream(side)
+    y.fill_(float("nan"))
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    ml.mt_layer_forward_static_status(torch.cuda.current_stream().cuda_stream)
+    assert torch.equal(want, y)
+    assert_layer_close(to_f64(y), ol.layer_forward(cfg, inp)["y"], "static forward replayed from a graph vs oracle")
+    dl.close()
