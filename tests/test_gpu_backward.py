@@ -48,6 +48,12 @@ CFGS = [
                       norm="layer", act="gelu_tanh", rope_base=0.0, bias=True),
     synth.LayerConfig("bw_mqa", batch=1, seq=200, hidden=512, heads=4, groups=1, head_dim=128, ffn=1024,
                       rope_base=5e5, bias=True),
+    # a sequence shorter than one 64-query block (the backward takes seq % 8 == 0), three samples
+    synth.LayerConfig("bw_short", batch=3, seq=24, hidden=256, heads=2, groups=2, head_dim=128, ffn=512,
+                      rope_base=1e4),
+    # three query heads per kv group (an odd count) and a ragged last 128-key block
+    synth.LayerConfig("bw_rep3", batch=1, seq=136, hidden=384, heads=6, groups=2, head_dim=64, ffn=768,
+                      rope_base=1e4, bias=True),
 ]
 
 
