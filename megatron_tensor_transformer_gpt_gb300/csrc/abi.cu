@@ -289,7 +289,9 @@ int map_qkv_out(CUtensorMap* m, const void* q, uint64_t d, uint64_t tokens, uint
 // Sets up the TMA output of a GEMM whose epilogue writes bf16 `out` (store, residual, GeLU, SwiGLU).
 int prepare_out(mt::GemmParams& p, int mode, CUtensorMap* to) {
   p.tma_out = (mode != mt::kEpiQkv && p.out != nullptr && p.out8 == nullptr && p.out32 == nullptr) ? 1 : 0;
-  return p.tma_out ? map_out(to, p.out, p.N, p.M, p.ldo) : MT_OK;
+  if (!p.tma_out) return MT_OK;
+  // a transposed store writes an [N, M] output: rows are the tile's columns
+  return p.c_trans ? map_out(to, p.out, p.M, p.N, p.ldo) : map_out(to, p.out, p.N, p.M, p.ldo);
 }
 
 // Row-major E4M3 (byte) matrix [rows, cols], pitch in bytes; box = 128 columns x box_rows.
@@ -791,7 +793,7 @@ int forward_device_fp8(mt_layer* L, const Layout& lay, const void* x, int S, int
 // stored [N, K] (b_mn = false) or [K, N] (b_mn = true), pitch ldb.  L may be null (no error word,
 // no launch count).
 int gemm_ab(mt_layer* L, const void* A, size_t lda, bool a_mn, const void* Bm, size_t ldb, bool b_mn, int M, int N,
-            int K, void* out, float* out32, size_t ldo, bool acc32, cudaStream_t st) {
+            int K, void* out, float* out32, size_t ldo, bool acc32, cudaStream_t st, bool c_trans = false) {
   CUtensorMap ta, tb, tb64;
   int rc = a_mn ? map_2d(&ta, A, M, K, lda, 64) : map_2d(&ta, A, K, M, lda, 128);
   if (!rc) rc = b_mn ? map_2d(&tb, Bm, N, K, ldb, 64) : map_2d(&tb, Bm, K, N, ldb, 128);
@@ -804,6 +806,7 @@ int gemm_ab(mt_layer* L, const void* A, size_t lda, bool a_mn, const void* Bm, s
   p.ldo = static_cast<int>(ldo);
   p.a_mn = a_mn ? 1 : 0;
   p.b_mn = b_mn ? 1 : 0;
+  p.c_trans = c_trans && out32 == nullptr ? 1 : 0;
   plan_gemm(p, mt::kEpiStore, 0, L, false);
   CUtensorMap to = ta;
   if ((rc = prepare_out(p, mt::kEpiStore, &to))) return rc;
@@ -869,14 +872,16 @@ int linear_bwd(mt_layer* L, const BwLayout& b, const void* dY, const void* X, co
                void* dW, void* db, void* dX, cudaStream_t st) {
   int rc;
   // Y [M, N] = X [M, K] W[N, K]^T:  dW = dY^T X  (both operands read MN-major, no transposes),
-  //                                  dX = dY W    (W read MN-major)
+  //                                  dX = dY W, formed as dX^T = W^T dY^T and stored transposed: W is
+  //                                  then an MN-major A and dY a K-major B, which the GEMM reads at full
+  //                                  rate (an MN-major B costs it 12-14 %)
   if (dW != nullptr && (rc = gemm_ab(L, dY, N, true, X, K, true, N, K, M, dW, nullptr, K, false, st))) return rc;
   if (db != nullptr) {
     count_launch(L);
     cudaError_t e = mt::launch_colsum(dY, false, N, M, N, bwr<float>(L, b, kBAcc), static_cast<bf16*>(db), st);
     if (e != cudaSuccess) return cuda_fail(e, "bias gradient");
   }
-  if (dX != nullptr && (rc = gemm_ab(L, dY, N, false, W, K, true, M, K, N, dX, nullptr, K, false, st))) return rc;
+  if (dX != nullptr && (rc = gemm_ab(L, W, K, true, dY, N, false, K, M, N, dX, nullptr, K, false, st, true))) return rc;
   return MT_OK;
 }
 

@@ -214,25 +214,45 @@ __device__ __forceinline__ void resid_box_load(EpiStore& es, int g, int col) {
   __syncwarp();
 }
 
+// p.c_trans: the tile is stored transposed, element (row, col) at out[col * ldo + row] (the output
+// tensor map then spans [N rows][M columns]); box row e holds output row col + e, whose 32 elements
+// are the warp's 32 rows, one 2-byte store per lane and e (a warp covers a whole 64-byte box row,
+// free of bank conflicts).
 __device__ __forceinline__ void store_chunk(const GemmParams& p, EpiStore& es, bf16* out_row, int col, bool valid,
                                             const float* v) {
+  const int lane = threadIdx.x & 31;
   if (!p.tma_out) {
-    if (valid) store_vec32(out_row, col, p.N, v);
+    if (!valid) return;
+    if (p.c_trans) {
+      bf16* dst = p.out + es.y0 + lane;
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        if (col + e < p.N) dst[static_cast<size_t>(col + e) * p.ldo] = __float2bfloat16_rn(v[e]);
+    } else {
+      store_vec32(out_row, col, p.N, v);
+    }
     return;
   }
-  const int lane = threadIdx.x & 31;
   uint8_t* box = es.stage + (es.n & 1) * EPI_BOX_BYTES;
   if (es.n >= 2) {
     if (lane == 0) cp_bulk_wait_read<1>();
     __syncwarp();
   }
-  const int sw = (lane >> 1) & 3;
+  if (p.c_trans) {
 #pragma unroll
-  for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(box + lane * 64 + ((c ^ sw) << 4)) = pack_bf16x8(v + 8 * c);
+    for (int e = 0; e < 32; ++e)
+      *reinterpret_cast<bf16*>(box + e * 64 + ((((lane >> 3) ^ (e >> 1)) & 3) << 4) + (lane & 7) * 2) =
+          __float2bfloat16_rn(v[e]);
+  } else {
+    const int sw = (lane >> 1) & 3;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(box + lane * 64 + ((c ^ sw) << 4)) = pack_bf16x8(v + 8 * c);
+  }
   fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) {
-    tma_store_2d(es.map, smem_u32(box), col, es.y0);
+    if (p.c_trans) tma_store_2d(es.map, smem_u32(box), es.y0, col);
+    else tma_store_2d(es.map, smem_u32(box), col, es.y0);
     cp_bulk_commit();
   }
   ++es.n;

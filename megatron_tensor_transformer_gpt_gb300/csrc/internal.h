@@ -77,6 +77,9 @@ struct GemmParams {
   // (boxes of 32 rows x 32 columns staged in shared memory and written by TMA) instead of per-thread
   // stores
   int tma_out;
+  // kEpiStore with bf16 output only: the tile is stored transposed, C[m][n] at out[n * ldo + m]
+  // (computing X^T = B A^T lets the MMA read both operands in their faster layouts)
+  int c_trans;
   // B is a weight that no kernel of the stream writes: the pair kernel issues the first stages' B
   // loads before it waits for the previous kernel (programmatic dependent launch)
   int b_static;
