@@ -817,7 +817,7 @@ int gemm_ab(mt_layer* L, const void* A, size_t lda, bool a_mn, const void* Bm, s
 
 enum BwRegion {
   kBQkv = 0, kBU, kBA, kBDa, kBDu, kBDhn, kBDh, kBDo, kBDq, kBDk, kBDv, kBDqkv, kBDxn, kBGrow, kBAcc,
-  kBLse, kBDsum, kBDoH, kBVh, kBNum
+  kBLse, kBDsum, kBDoH, kBVh, kBT, kBNum
 };
 
 struct BwLayout {
@@ -852,6 +852,9 @@ BwLayout bw_layout(const mt_layer* L, int S, int B) {
   b.size[kBDsum] = zq * S * 4;
   b.size[kBDoH] = zq * S * d * 2;
   b.size[kBVh] = zk * S * d * 2;
+  // the transposed operand of a weight gradient: the smaller of X and dY, at most H columns (every
+  // projection has H on one side)
+  b.size[kBT] = T * H * 2;
   size_t o = b.fwd.total;
   for (int r = 0; r < kBNum; ++r) {
     b.off[r] = o;
@@ -871,11 +874,22 @@ T* bwr(const mt_layer* L, const BwLayout& b, BwRegion r) {
 int linear_bwd(mt_layer* L, const BwLayout& b, const void* dY, const void* X, const void* W, int M, int N, int K,
                void* dW, void* db, void* dX, cudaStream_t st) {
   int rc;
-  // Y [M, N] = X [M, K] W[N, K]^T:  dW = dY^T X  (both operands read MN-major, no transposes),
-  //                                  dX = dY W, formed as dX^T = W^T dY^T and stored transposed: W is
-  //                                  then an MN-major A and dY a K-major B, which the GEMM reads at full
-  //                                  rate (an MN-major B costs it 12-14 %)
-  if (dW != nullptr && (rc = gemm_ab(L, dY, N, true, X, K, true, N, K, M, dW, nullptr, K, false, st))) return rc;
+  // Y [M, N] = X [M, K] W[N, K]^T.  The GEMM reads an MN-major A at full rate and loses 12-14 % on an
+  // MN-major B, so every product here takes its B K-major:
+  //   dW = dY^T X with X^T [K, M] (one transpose) as B, dY read as an MN-major A; or, when dY is the
+  //        narrower of the two, dW^T = X^T dY with dY^T [N, M] as B, stored transposed;
+  //   dX = dY W formed as dX^T = W^T dY^T: W an MN-major A, dY a K-major B, stored transposed.
+  if (dW != nullptr) {
+    bf16* tr = bwr<bf16>(L, b, kBT);
+    const bool tx = K <= N;  // transpose X (else dY)
+    count_launch(L);
+    cudaError_t e = tx ? mt::launch_transpose_bf16(static_cast<const bf16*>(X), K, tr, M, M, K, st)
+                       : mt::launch_transpose_bf16(static_cast<const bf16*>(dY), N, tr, M, M, N, st);
+    if (e != cudaSuccess) return cuda_fail(e, "weight-gradient operand transpose");
+    if ((rc = tx ? gemm_ab(L, dY, N, true, tr, M, false, N, K, M, dW, nullptr, K, false, st)
+                 : gemm_ab(L, X, K, true, tr, M, false, K, N, M, dW, nullptr, K, false, st, true)))
+      return rc;
+  }
   if (db != nullptr) {
     count_launch(L);
     cudaError_t e = mt::launch_colsum(dY, false, N, M, N, bwr<float>(L, b, kBAcc), static_cast<bf16*>(db), st);

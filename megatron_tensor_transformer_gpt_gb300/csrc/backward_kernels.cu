@@ -290,6 +290,32 @@ __global__ void rope_bwd_pack_kernel(const float* __restrict__ dq, const float* 
   }
 }
 
+// dst[C, R] = src[R, C]^T (bf16; pitches in elements; R and C multiples of 8), one 8 x 8 block per
+// thread: eight 16-byte row loads, a register transpose of the 16-bit halves (a byte permutation per
+// output pair), eight 16-byte stores.  Consecutive lanes take consecutive 8-row groups of src, so a
+// warp's stores fill 512 contiguous bytes of a dst row; its loads take 16 bytes of 32 rows, whose
+// neighbouring 16 bytes the warp of the next column group reads from L2.
+__global__ void __launch_bounds__(256) transpose_bf16_kernel(const uint4* __restrict__ src, size_t sp16,
+                                                             uint4* __restrict__ dst, size_t dp16, int rg, int cg) {
+  const size_t t = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= static_cast<size_t>(rg) * cg) return;
+  const int rb = static_cast<int>(t % rg), cb = static_cast<int>(t / rg);
+  uint4 r[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) r[i] = src[static_cast<size_t>(8 * rb + i) * sp16 + cb];
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(r);  // w[4 i + k]: elements 2k, 2k + 1 of row i
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;  // the high or the low halves of two words
+    uint4 o;
+    o.x = __byte_perm(w[0 * 4 + j / 2], w[1 * 4 + j / 2], sel);
+    o.y = __byte_perm(w[2 * 4 + j / 2], w[3 * 4 + j / 2], sel);
+    o.z = __byte_perm(w[4 * 4 + j / 2], w[5 * 4 + j / 2], sel);
+    o.w = __byte_perm(w[6 * 4 + j / 2], w[7 * 4 + j / 2], sel);
+    dst[static_cast<size_t>(8 * cb + j) * dp16 + rb] = o;
+  }
+}
+
 }  // namespace
 
 // Blocks of 256 threads for T x f / 8 vectors: one pass, at most 32 blocks per SM.
@@ -332,6 +358,16 @@ cudaError_t launch_colsum(const void* src, bool f32, size_t ld, int T, int N, fl
   if (f32) colsum_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(src), ld, T, N, acc);
   else colsum_kernel<bf16><<<grid, 256, 0, st>>>(static_cast<const bf16*>(src), ld, T, N, acc);
   f32_to_bf16_kernel<<<(N + 255) / 256, 256, 0, st>>>(acc, out, N);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_bf16(const bf16* src, size_t sp, bf16* dst, size_t dp, int R, int C, cudaStream_t st) {
+  if (R <= 0 || C <= 0) return cudaSuccess;
+  if (R % 8 || C % 8 || sp % 8 || dp % 8 || reinterpret_cast<uintptr_t>(src) % 16 || reinterpret_cast<uintptr_t>(dst) % 16)
+    return cudaErrorInvalidValue;
+  const size_t blocks = static_cast<size_t>(R / 8) * (C / 8);
+  transpose_bf16_kernel<<<static_cast<unsigned>((blocks + 255) / 256), 256, 0, st>>>(
+      reinterpret_cast<const uint4*>(src), sp / 8, reinterpret_cast<uint4*>(dst), dp / 8, R / 8, C / 8);
   return cudaGetLastError();
 }
 

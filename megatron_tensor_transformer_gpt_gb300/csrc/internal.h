@@ -209,6 +209,9 @@ int norm_bwd_blocks(int T);
 cudaError_t launch_norm_bwd(const bf16* dy, const bf16* x, const bf16* gamma, const bf16* add, bf16* out,
                             float* partial, int T, int H, float eps, bool layer_norm, cudaStream_t st);
 cudaError_t launch_colsum(const void* src, bool f32, size_t ld, int T, int N, float* acc, bf16* out, cudaStream_t st);
+// dst [C, R] (pitch dp) = src [R, C] (pitch sp)^T, bf16; R, C and the pitches multiples of 8, 16-byte
+// aligned pointers (cudaErrorInvalidValue otherwise).
+cudaError_t launch_transpose_bf16(const bf16* src, size_t sp, bf16* dst, size_t dp, int R, int C, cudaStream_t st);
 cudaError_t launch_rope_bwd_pack(const float* dq, const float* dk, const float* dv, const float2* rope, bf16* dqkv,
                                  int S, int B, int nh, int ng, int d, cudaStream_t st);
 
