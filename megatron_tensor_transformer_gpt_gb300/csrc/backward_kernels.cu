@@ -290,29 +290,36 @@ __global__ void rope_bwd_pack_kernel(const float* __restrict__ dq, const float* 
   }
 }
 
-// dst[C, R] = src[R, C]^T (bf16; pitches in elements; R and C multiples of 8), one 8 x 8 block per
-// thread: eight 16-byte row loads, a register transpose of the 16-bit halves (a byte permutation per
-// output pair), eight 16-byte stores.  Consecutive lanes take consecutive 8-row groups of src, so a
-// warp's stores fill 512 contiguous bytes of a dst row; its loads take 16 bytes of 32 rows, whose
-// neighbouring 16 bytes the warp of the next column group reads from L2.
-__global__ void __launch_bounds__(256) transpose_bf16_kernel(const uint4* __restrict__ src, size_t sp16,
-                                                             uint4* __restrict__ dst, size_t dp16, int rg, int cg) {
-  const size_t t = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (t >= static_cast<size_t>(rg) * cg) return;
-  const int rb = static_cast<int>(t % rg), cb = static_cast<int>(t / rg);
-  uint4 r[8];
+// dst[C, R] = src[R, C]^T (bf16; pitches in elements; R and C multiples of 8) through a 64 x 64 tile in
+// shared memory, every global load and store a 16-byte vector and coalesced (a warp moves 128
+// contiguous bytes of four rows).  Tile row r keeps its eight 16-byte chunks with chunk ch at
+// ch ^ (r / 8), so that the transposed reads (2-byte elements of one column from eight rows 8g ..
+// 8g + 7, g differing across a warp) fall in distinct banks.
+__global__ void __launch_bounds__(256) transpose_bf16_kernel(const bf16* __restrict__ src, size_t sp,
+                                                             bf16* __restrict__ dst, size_t dp, int R, int C) {
+  __shared__ uint4 tile[64 * 8];
+  const int tr = blockIdx.y * 64, tc = blockIdx.x * 64;  // tile origin in src (row, column)
+  const int t = threadIdx.x;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) r[i] = src[static_cast<size_t>(8 * rb + i) * sp16 + cb];
-  const uint32_t* w = reinterpret_cast<const uint32_t*>(r);  // w[4 i + k]: elements 2k, 2k + 1 of row i
+  for (int k = 0; k < 2; ++k) {
+    const int r = t / 8 + 32 * k, ch = t % 8;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (tr + r < R && tc + 8 * ch < C) v = *reinterpret_cast<const uint4*>(src + static_cast<size_t>(tr + r) * sp + tc + 8 * ch);
+    tile[r * 8 + ((ch ^ (r >> 3)) & 7)] = v;
+  }
+  __syncthreads();
+  const uint16_t* ts = reinterpret_cast<const uint16_t*>(tile);
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;  // the high or the low halves of two words
-    uint4 o;
-    o.x = __byte_perm(w[0 * 4 + j / 2], w[1 * 4 + j / 2], sel);
-    o.y = __byte_perm(w[2 * 4 + j / 2], w[3 * 4 + j / 2], sel);
-    o.z = __byte_perm(w[4 * 4 + j / 2], w[5 * 4 + j / 2], sel);
-    o.w = __byte_perm(w[6 * 4 + j / 2], w[7 * 4 + j / 2], sel);
-    dst[static_cast<size_t>(8 * cb + j) * dp16 + rb] = o;
+  for (int k = 0; k < 2; ++k) {
+    const int c = t / 8 + 32 * k, g = t % 8;  // dst row tc + c holds src rows tr + 8g .. tr + 8g + 7 here
+    if (tc + c >= C || tr + 8 * g >= R) continue;
+    const int phys = (((c >> 3) ^ g) & 7) * 8 + (c & 7);  // element c of a row of group g
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      w[q] = static_cast<uint32_t>(ts[(8 * g + 2 * q) * 64 + phys]) |
+             (static_cast<uint32_t>(ts[(8 * g + 2 * q + 1) * 64 + phys]) << 16);
+    *reinterpret_cast<uint4*>(dst + static_cast<size_t>(tc + c) * dp + tr + 8 * g) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -365,9 +372,7 @@ cudaError_t launch_transpose_bf16(const bf16* src, size_t sp, bf16* dst, size_t 
   if (R <= 0 || C <= 0) return cudaSuccess;
   if (R % 8 || C % 8 || sp % 8 || dp % 8 || reinterpret_cast<uintptr_t>(src) % 16 || reinterpret_cast<uintptr_t>(dst) % 16)
     return cudaErrorInvalidValue;
-  const size_t blocks = static_cast<size_t>(R / 8) * (C / 8);
-  transpose_bf16_kernel<<<static_cast<unsigned>((blocks + 255) / 256), 256, 0, st>>>(
-      reinterpret_cast<const uint4*>(src), sp / 8, reinterpret_cast<uint4*>(dst), dp / 8, R / 8, C / 8);
+  transpose_bf16_kernel<<<dim3((C + 63) / 64, (R + 63) / 64), 256, 0, st>>>(src, sp, dst, dp, R, C);
   return cudaGetLastError();
 }
 
