@@ -816,7 +816,7 @@ int gemm_ab(mt_layer* L, const void* A, size_t lda, bool a_mn, const void* Bm, s
 }
 
 enum BwRegion {
-  kBQkv = 0, kBU, kBA, kBDa, kBDu, kBDhn, kBDh, kBDo, kBDq, kBDk, kBDv, kBDqkv, kBDxn, kBGrow, kBAcc,
+  kBU = 0, kBA, kBDa, kBDu, kBDhn, kBDh, kBDo, kBDq, kBDk, kBDv, kBDqkv, kBDxn, kBGrow, kBAcc,
   kBLse, kBDsum, kBDoH, kBVh, kBT, kBNum
 };
 
@@ -831,7 +831,6 @@ BwLayout bw_layout(const mt_layer* L, int S, int B) {
   const size_t T = static_cast<size_t>(S) * B, H = L->hidden, d = L->head_dim;
   const size_t QKV = L->q_w + 2 * L->kv_w, f = L->f_r, f1 = L->f1_r, qw = L->q_w;
   const size_t maxc = std::max(std::max(QKV, f1), std::max(H, qw));
-  b.size[kBQkv] = T * QKV * 2;
   b.size[kBU] = T * f1 * 2;
   b.size[kBA] = T * f * 2;
   b.size[kBDa] = T * f * 2;
@@ -928,7 +927,7 @@ int backward_device(mt_layer* L, const BwLayout& b, const void* x, const void* d
   const bool swiglu = L->act == MT_ACT_SWIGLU;
   int rc;
   cudaError_t e;
-  // ---- forward recompute: xn, q, k (after RoPE), o, h (attention block), hn, plain qkv, u, a
+  // ---- forward recompute: xn, q, k (after RoPE), v, o, h (attention block), hn, u, a
   bf16* h = region<bf16>(L, lay, kH);
   if ((rc = run_attention_block(L, lay, x, S, B, w, h, mt::kEpiResid, st, nullptr, bwr<float>(L, b, kBLse))))
     return rc;
@@ -938,14 +937,9 @@ int backward_device(mt_layer* L, const BwLayout& b, const void* x, const void* d
   e = mt::launch_norm(L->norm == MT_NORM_LAYER, h, static_cast<const bf16*>(w->norm2_w),
                       static_cast<const bf16*>(w->norm2_b), hn, T, H, L->eps, st);
   if (e != cudaSuccess) return cuda_fail(e, "norm2 launch");
-  bf16 *qkv = bwr<bf16>(L, b, kBQkv), *u = bwr<bf16>(L, b, kBU), *a = bwr<bf16>(L, b, kBA);
+  bf16 *u = bwr<bf16>(L, b, kBU), *a = bwr<bf16>(L, b, kBA);
   {
-    mt::GemmParams p = gemm_params(T, QKV, H, false, L->d_err);
-    p.out = qkv;
-    p.ldo = QKV;
-    p.bias = static_cast<const bf16*>(w->b_qkv);
-    if ((rc = run_gemm(L, -1, mt::kEpiStore, xn, H, w->w_qkv, QKV, T, QKV, H, p, st))) return rc;
-    p = gemm_params(T, f1, H, false, L->d_err);
+    mt::GemmParams p = gemm_params(T, f1, H, false, L->d_err);
     p.out = u;
     p.ldo = f1;
     p.bias = static_cast<const bf16*>(w->b_fc1);
@@ -974,21 +968,14 @@ int backward_device(mt_layer* L, const BwLayout& b, const void* x, const void* d
   bf16 *dOh = bwr<bf16>(L, b, kBDoH), *Vh = bwr<bf16>(L, b, kBVh);
   const int zq = B * nh, zk = B * ng;
   const size_t sd = static_cast<size_t>(S) * d;
-  struct Slice {
-    const bf16* src;
-    size_t pitch, sb, sh;
-    int zdiv, Z;
-    bf16* dst;
-  } slices[] = {
-      {dO, static_cast<size_t>(B) * qw, static_cast<size_t>(qw), static_cast<size_t>(d), nh, zq, dOh},
-      {qkv + qw + kvw, static_cast<size_t>(B) * QKV, static_cast<size_t>(QKV), static_cast<size_t>(d), ng, zk, Vh},
-  };
-  for (const Slice& sl : slices) {
-    count_launch(L);
-    if ((e = mt::launch_head_slices(sl.src, sl.pitch, sl.sb, sl.sh, sl.zdiv, sl.Z, sl.dst, static_cast<size_t>(d), S,
-                                    d, st)) != cudaSuccess)
-      return cuda_fail(e, "attention backward operands");
-  }
+  // dO head-major; V from the forward's head-major fp16 copy (the bf16 dO pairs with a bf16 V)
+  count_launch(L);
+  if ((e = mt::launch_head_slices(dO, static_cast<size_t>(B) * qw, static_cast<size_t>(qw), static_cast<size_t>(d),
+                                  nh, zq, dOh, static_cast<size_t>(d), S, d, st)) != cudaSuccess)
+    return cuda_fail(e, "attention backward operands");
+  count_launch(L);
+  if ((e = mt::launch_f16_to_bf16(region<__half>(L, lay, kV), Vh, static_cast<size_t>(zk) * sd, st)) != cudaSuccess)
+    return cuda_fail(e, "attention backward operands");
   count_launch(L);
   if ((e = mt::launch_row_dot(dO, o, dsum, S, B, nh, d, st)) != cudaSuccess) return cuda_fail(e, "rowsum(dO o O)");
   {

@@ -323,6 +323,25 @@ __global__ void __launch_bounds__(256) transpose_bf16_kernel(const bf16* __restr
   }
 }
 
+// The attention backward's V operand in bf16 (its dP = dO V^T product pairs it with the bf16 dO) from
+// the forward's head-major fp16 V: fp16 -> fp32 is exact, then one round to nearest even.  n8
+// vectors of eight elements.
+__global__ void f16_to_bf16_kernel(const __half* __restrict__ src, bf16* __restrict__ dst, size_t n8) {
+  for (size_t v = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; v < n8;
+       v += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const uint4 u = reinterpret_cast<const uint4*>(src)[v];
+    const __half2* h = reinterpret_cast<const __half2*>(&u);
+    float f[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 x = __half22float2(h[e]);
+      f[2 * e] = x.x;
+      f[2 * e + 1] = x.y;
+    }
+    reinterpret_cast<uint4*>(dst)[v] = pack_bf16x8(f);
+  }
+}
+
 }  // namespace
 
 // Blocks of 256 threads for T x f / 8 vectors: one pass, at most 32 blocks per SM.
@@ -373,6 +392,12 @@ cudaError_t launch_transpose_bf16(const bf16* src, size_t sp, bf16* dst, size_t 
   if (R % 8 || C % 8 || sp % 8 || dp % 8 || reinterpret_cast<uintptr_t>(src) % 16 || reinterpret_cast<uintptr_t>(dst) % 16)
     return cudaErrorInvalidValue;
   transpose_bf16_kernel<<<dim3((C + 63) / 64, (R + 63) / 64), 256, 0, st>>>(src, sp, dst, dp, R, C);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_f16_to_bf16(const __half* src, bf16* dst, size_t n, cudaStream_t st) {
+  if (n % 8) return cudaErrorInvalidValue;
+  f16_to_bf16_kernel<<<act_grid(n / 8, 8), 256, 0, st>>>(src, dst, n / 8);
   return cudaGetLastError();
 }
 

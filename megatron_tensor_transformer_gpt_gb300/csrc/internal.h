@@ -209,6 +209,8 @@ int norm_bwd_blocks(int T);
 cudaError_t launch_norm_bwd(const bf16* dy, const bf16* x, const bf16* gamma, const bf16* add, bf16* out,
                             float* partial, int T, int H, float eps, bool layer_norm, cudaStream_t st);
 cudaError_t launch_colsum(const void* src, bool f32, size_t ld, int T, int N, float* acc, bf16* out, cudaStream_t st);
+// dst[i] = bf16(src[i]) for n elements, n a multiple of 8, 16-byte aligned pointers.
+cudaError_t launch_f16_to_bf16(const __half* src, bf16* dst, size_t n, cudaStream_t st);
 // dst [C, R] (pitch dp) = src [R, C] (pitch sp)^T, bf16; R, C and the pitches multiples of 8, 16-byte
 // aligned pointers (cudaErrorInvalidValue otherwise).
 cudaError_t launch_transpose_bf16(const bf16* src, size_t sp, bf16* dst, size_t dp, int R, int C, cudaStream_t st);
