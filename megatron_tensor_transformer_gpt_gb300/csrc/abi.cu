@@ -43,9 +43,11 @@ struct mt_layer {
   };
   std::vector<Rec> recs;
   std::vector<cudaEvent_t> pool;
-  // host-buffer forward: a copy stream and its events (created on first use)
+  // host-buffer forward: a copy stream and its events (created on first use); the backward also
+  // runs its dQ kernel there, between a fork and a join event
   cudaStream_t copy_stream;
   cudaEvent_t copy_ev[9];
+  cudaEvent_t fork_ev, join_ev;
   // K-split tails of the CTA-pair GEMM: partial sums (kKsSlots slots of 256 x 256 fp32) and
   // arrival counters (kept at zero between launches)
   float4* d_kws;
@@ -155,11 +157,15 @@ int ensure_copy_stream(mt_layer* L) {
   cudaStream_t s = nullptr;
   cudaError_t e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
   if (e != cudaSuccess) return cuda_fail(e, "creating the copy stream");
-  for (auto& ev : L->copy_ev) {
-    if (ev == nullptr && (e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess) {
-      cudaStreamDestroy(s);
-      return cuda_fail(e, "creating the copy events");
-    }
+  auto make = [&](cudaEvent_t& ev) {
+    if (ev == nullptr && e == cudaSuccess) e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+  };
+  for (auto& ev : L->copy_ev) make(ev);
+  make(L->fork_ev);
+  make(L->join_ev);
+  if (e != cudaSuccess) {
+    cudaStreamDestroy(s);
+    return cuda_fail(e, "creating the copy events");
   }
   L->copy_stream = s;
   return MT_OK;
@@ -999,9 +1005,18 @@ int backward_device(mt_layer* L, const BwLayout& b, const void* x, const void* d
     ap.dk = dk;
     ap.dv = dv;
     ap.err = L->d_err;
+    // dQ on the copy stream beside dK/dV: fork after D = rowsum(dO o O), join before the RoPE pack
+    if ((rc = ensure_copy_stream(L))) return rc;
+    cudaStream_t cs = L->copy_stream;
+    if ((e = cudaEventRecord(L->fork_ev, st)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(cs, L->fork_ev, 0)) != cudaSuccess)
+      return cuda_fail(e, "attention backward fork");
     count_launch(L);
     count_launch(L);
-    if ((e = mt::launch_attention_bwd(d, m, ap, st)) != cudaSuccess) return cuda_fail(e, "attention backward");
+    if ((e = mt::launch_attention_bwd(d, m, ap, st, cs)) != cudaSuccess) return cuda_fail(e, "attention backward");
+    if ((e = cudaEventRecord(L->join_ev, cs)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(st, L->join_ev, 0)) != cudaSuccess)
+      return cuda_fail(e, "attention backward join");
   }
   bf16* dqkv = bwr<bf16>(L, b, kBDqkv);
   const float2* rope = L->rope_base > 0.f ? region<float2>(L, lay, kRope) : nullptr;
@@ -1304,6 +1319,8 @@ void mt_layer_destroy(mt_layer* L) {
   for (auto e : L->pool) cudaEventDestroy(e);
   for (auto e : L->copy_ev)
     if (e) cudaEventDestroy(e);
+  if (L->fork_ev) cudaEventDestroy(L->fork_ev);
+  if (L->join_ev) cudaEventDestroy(L->join_ev);
   if (L->copy_stream) cudaStreamDestroy(L->copy_stream);
   if (L->done_ev) cudaEventDestroy(L->done_ev);
   delete L;

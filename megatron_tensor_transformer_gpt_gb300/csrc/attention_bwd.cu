@@ -706,7 +706,7 @@ __global__ void __launch_bounds__(GeoKV<D>::THREADS, 1)
 }
 
 template <int D>
-cudaError_t launch_bwd_d(const CUtensorMap* maps, const AttnBwdParams& p, cudaStream_t st) {
+cudaError_t launch_bwd_d(const CUtensorMap* maps, const AttnBwdParams& p, cudaStream_t st, cudaStream_t st_dq) {
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -718,12 +718,13 @@ cudaError_t launch_bwd_d(const CUtensorMap* maps, const AttnBwdParams& p, cudaSt
     configured = true;
   }
   const unsigned nb = static_cast<unsigned>((p.seq + 127) / 128);
-  // maps: Q, dO, K, V as 128-row boxes; Q, dO as 64-row boxes
-  cudaError_t e = launch_pdl(attn_bwd_dq_kernel<D>, dim3(nb * p.batch * p.nh), dim3(GeoQ<D>::THREADS), GeoQ<D>::SMEM,
-                             st, maps[0], maps[1], maps[2], maps[3], p);
+  // maps: Q, dO, K, V as 128-row boxes; Q, dO as 64-row boxes.  dK/dV first: its longest blocks
+  // (key block 0 sees every query block) set the critical path, so they start before any dQ block.
+  cudaError_t e = launch_pdl(attn_bwd_dkdv_kernel<D>, dim3(nb * p.batch * p.ng), dim3(GeoKV<D>::THREADS),
+                             GeoKV<D>::SMEM, st, maps[2], maps[3], maps[4], maps[5], p);
   if (e != cudaSuccess) return e;
-  return launch_pdl(attn_bwd_dkdv_kernel<D>, dim3(nb * p.batch * p.ng), dim3(GeoKV<D>::THREADS), GeoKV<D>::SMEM, st,
-                    maps[2], maps[3], maps[4], maps[5], p);
+  return launch_pdl(attn_bwd_dq_kernel<D>, dim3(nb * p.batch * p.nh), dim3(GeoQ<D>::THREADS), GeoQ<D>::SMEM, st_dq,
+                    maps[0], maps[1], maps[2], maps[3], p);
 }
 
 }  // namespace
@@ -750,10 +751,11 @@ cudaError_t launch_row_dot(const bf16* dO, const bf16* O, float* Dsum, int S, in
   return cudaGetLastError();
 }
 
-cudaError_t launch_attention_bwd(int head_dim, const CUtensorMap* maps, const AttnBwdParams& p, cudaStream_t st) {
+cudaError_t launch_attention_bwd(int head_dim, const CUtensorMap* maps, const AttnBwdParams& p, cudaStream_t st,
+                                 cudaStream_t st_dq) {
   if (p.seq <= 0) return cudaSuccess;
-  if (head_dim == 64) return launch_bwd_d<64>(maps, p, st);
-  if (head_dim == 128) return launch_bwd_d<128>(maps, p, st);
+  if (head_dim == 64) return launch_bwd_d<64>(maps, p, st, st_dq);
+  if (head_dim == 128) return launch_bwd_d<128>(maps, p, st, st_dq);
   return cudaErrorInvalidValue;
 }
 

@@ -159,10 +159,13 @@ int gemm_pair_slots();
 
 // Kernel launchers; return a cudaError_t from the launch.
 // fp8 = true: A and B are E4M3 (tensor maps of bytes, boxes 128 wide).
-// Attention backward: maps = {Q [.,128 rows], dO [.,128], K [.,64], V [.,64] for the dQ kernel;
-// K [.,128], V [.,128], Q [.,64], dO [.,64] for dK/dV} (bf16, 64-element inner boxes, head-major
-// [z][seq][d] tensors).
-cudaError_t launch_attention_bwd(int head_dim, const CUtensorMap* maps, const AttnBwdParams& p, cudaStream_t st);
+// Attention backward: maps = {Q, dO, K, V as 128-row boxes; Q, dO as 64-row boxes} (bf16,
+// 64-element inner boxes, head-major [z][seq][d] tensors).  The dK/dV kernel goes on `st`, then the
+// dQ kernel on `st_dq`; the two read the same inputs and write disjoint outputs, so on two streams
+// the dQ blocks fill the SMs that the causally uneven dK/dV blocks leave idle.  The caller orders
+// `st_dq` after the inputs' producers and joins it back (st_dq may be st).
+cudaError_t launch_attention_bwd(int head_dim, const CUtensorMap* maps, const AttnBwdParams& p, cudaStream_t st,
+                                 cudaStream_t st_dq);
 // Batched copy of R x C bf16 slices z = 0..Z-1 at src + (z / zdiv) sb + (z % zdiv) sh (row pitch sp)
 // into dst + z R dp (row pitch dp).
 cudaError_t launch_head_slices(const bf16* src, size_t sp, size_t sb, size_t sh, int zdiv, int Z, bf16* dst, size_t dp,
