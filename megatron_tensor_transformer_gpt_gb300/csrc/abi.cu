@@ -944,15 +944,15 @@ int backward_device(mt_layer* L, const BwLayout& b, const void* x, const void* d
                       static_cast<const bf16*>(w->norm2_b), hn, T, H, L->eps, st);
   if (e != cudaSuccess) return cuda_fail(e, "norm2 launch");
   bf16 *u = bwr<bf16>(L, b, kBU), *a = bwr<bf16>(L, b, kBA);
-  {
-    mt::GemmParams p = gemm_params(T, f1, H, false, L->d_err);
-    p.out = u;
-    p.ldo = f1;
+  {  // fc1 with the forward's activation epilogue, which also keeps the pre-activation u
+    mt::GemmParams p = gemm_params(T, f, H, swiglu, L->d_err);
+    p.out = a;
+    p.ldo = f;
     p.bias = static_cast<const bf16*>(w->b_fc1);
-    if ((rc = run_gemm(L, -1, mt::kEpiStore, hn, H, w->w_fc1, f1, T, f1, H, p, st))) return rc;
+    p.pre = u;
+    p.ldp = f1;
+    if ((rc = run_gemm(L, -1, swiglu ? mt::kEpiSwiglu : mt::kEpiGelu, hn, H, w->w_fc1, f1, T, f, H, p, st))) return rc;
   }
-  count_launch(L);
-  if ((e = mt::launch_act_fwd(u, a, T, f, swiglu, st)) != cudaSuccess) return cuda_fail(e, "activation");
 
   // ---- MLP
   bf16 *da = bwr<bf16>(L, b, kBDa), *du = bwr<bf16>(L, b, kBDu), *dhn = bwr<bf16>(L, b, kBDhn);

@@ -19,33 +19,6 @@ __device__ __forceinline__ float warp_sum_f(float v) {
 
 __device__ __forceinline__ float sigmoidf(float g) { return 1.0f / (1.0f + expf(-g)); }
 
-// SwiGLU / GeLU(tanh) forward from the stored fc1 output u: a = silu(u[:, :f]) u[:, f:] or gelu(u).
-__global__ void act_fwd_kernel(const bf16* __restrict__ u, bf16* __restrict__ a, size_t T, int f, int swiglu) {
-  // eight outputs (16 bytes) per thread and iteration; f is a multiple of 8
-  const int f8 = f >> 3;
-  const size_t n8 = T * f8;
-  for (size_t v = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; v < n8;
-       v += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const size_t t = v / f8;
-    const int c = static_cast<int>(v - t * f8) * 8;
-    float r[8];
-    if (swiglu) {
-      float g[8], up[8];
-      unpack_bf16x8(*reinterpret_cast<const uint4*>(u + t * 2 * f + c), g);
-      unpack_bf16x8(*reinterpret_cast<const uint4*>(u + t * 2 * f + f + c), up);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) r[e] = g[e] * sigmoidf(g[e]) * up[e];
-    } else {
-      float x[8];
-      unpack_bf16x8(*reinterpret_cast<const uint4*>(u + t * f + c), x);
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        r[e] = 0.5f * x[e] * (1.0f + tanhf(0.7978845608028654f * (x[e] + 0.044715f * x[e] * x[e] * x[e])));
-    }
-    *reinterpret_cast<uint4*>(a + t * f + c) = pack_bf16x8(r);
-  }
-}
-
 // Gradient through the activation: du from da = dL/da and the fc1 output u.
 //   SwiGLU: d gate = da up silu'(gate), d up = da silu(gate), silu'(g) = s (1 + g (1 - s)), s = sigmoid(g)
 //   GeLU(tanh): du = da gelu'(u)
@@ -350,12 +323,6 @@ static unsigned act_grid(size_t T, int f) {
   const size_t blocks = (n8 + 255) / 256;
   const size_t cap = static_cast<size_t>(num_sms()) * 32;
   return static_cast<unsigned>(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
-}
-
-cudaError_t launch_act_fwd(const bf16* u, bf16* a, size_t T, int f, bool swiglu, cudaStream_t st) {
-  if (f % 8) return cudaErrorInvalidValue;
-  act_fwd_kernel<<<act_grid(T, f), 256, 0, st>>>(u, a, T, f, swiglu ? 1 : 0);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_act_bwd(const bf16* u, const bf16* da, bf16* du, size_t T, int f, bool swiglu, cudaStream_t st) {

@@ -319,6 +319,11 @@ __device__ __forceinline__ void epilogue_tile_bf16(const GemmParams& p, uint32_t
           add_vec32(v, p.bias, col, p.N);
           add_vec32(w, p.bias + p.N, col, p.N);
         }
+        if (p.pre != nullptr) {
+          bf16* pre_row = p.pre + static_cast<size_t>(row) * p.ldp;
+          store_vec32(pre_row, col, p.N, v);
+          store_vec32(pre_row + p.N, col, p.N, w);
+        }
 #pragma unroll
         for (int e = 0; e < 32; ++e) v[e] = silu(v[e]) * w[e];
       }
@@ -388,6 +393,7 @@ __device__ __forceinline__ void epilogue_tile_bf16(const GemmParams& p, uint32_t
         if (p.bias != nullptr) add_vec32(v, p.bias, col, p.N);
         if (MODE == kEpiResid) add_loaded32(v, res);
         if (MODE == kEpiGelu) {
+          if (p.pre != nullptr) store_vec32(p.pre + static_cast<size_t>(row) * p.ldp, col, p.N, v);
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = gelu_tanh(v[e]);
         }

@@ -73,6 +73,10 @@ struct GemmParams {
   // kEpiStore only: fp32 output to out32 (pitch ldo) instead of bf16; acc32 = 1 adds to it
   float* out32;
   int acc32;
+  // SwiGLU / GeLU epilogue with bf16 output: when non-null, the pre-activation values (bias added,
+  // rounded to bf16) also go to pre (pitch ldp): SwiGLU as [gate N | up N], GeLU as N columns
+  bf16* pre;
+  int ldp;
   // bf16 output of the store / residual / GeLU / SwiGLU epilogues through the output tensor map
   // (boxes of 32 rows x 32 columns staged in shared memory and written by TMA) instead of per-thread
   // stores
@@ -204,7 +208,6 @@ cudaError_t launch_norm(bool layer_norm, const bf16* x, const bf16* g, const bf1
 cudaError_t launch_quantize_e4m3(const bf16* x, size_t n, uint8_t* q, float* slot, cudaStream_t stream);
 
 // ---- backward pass (backward_kernels.cu)
-cudaError_t launch_act_fwd(const bf16* u, bf16* a, size_t T, int f, bool swiglu, cudaStream_t st);
 cudaError_t launch_act_bwd(const bf16* u, const bf16* da, bf16* du, size_t T, int f, bool swiglu, cudaStream_t st);
 // dx of a norm (plus `add`), and per-CTA partial rows of d gamma (rows [0, norm_bwd_blocks(T)) of
 // `partial`, pitch H) and, for LayerNorm, of d beta (the next norm_bwd_blocks(T) rows).
