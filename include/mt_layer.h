@@ -236,8 +236,9 @@ const char* mt_last_error(void);
 
 void mt_layer_destroy(mt_layer* L);
 
-/* Per-kernel timing.  Kernel slots: 0 (reserved: the RoPE table, now written by the norm1 launch,
- * so it records nothing), 1 norm1 (with the RoPE table), 2 QKV GEMM, 3 attention,
+/* Per-kernel timing.  Kernel slots: 0 the attention backward (its dQ and dK/dV kernels, which run
+ * side by side on two streams, as one interval from before the first to after both; a launch
+ * count of 1 per backward), 1 norm1 (with the RoPE table), 2 QKV GEMM, 3 attention,
  * 4 output-projection GEMM, 5 norm2, 6 fc1 GEMM, 7 fc2 GEMM (MT_PROFILE_SLOTS).  slot_mask selects
  * the slots whose launches this handle brackets with a pair of CUDA events on their stream (bit s
  * for slot s; MT_PROFILE_ALL for every slot, 0 to stop); values outside 0..MT_PROFILE_ALL return

@@ -96,7 +96,7 @@ int done(mt_layer* L, cudaStream_t st) {
   return ok();
 }
 
-enum Slot { kSlotRope = 0, kSlotNorm1, kSlotQkv, kSlotAttn, kSlotO, kSlotNorm2, kSlotFc1, kSlotFc2 };
+enum Slot { kSlotAttnBwd = 0, kSlotNorm1, kSlotQkv, kSlotAttn, kSlotO, kSlotNorm2, kSlotFc1, kSlotFc2 };
 constexpr size_t kMaxRecords = 8192;
 
 cudaEvent_t pool_event(mt_layer* L) {
@@ -1011,7 +1011,7 @@ int backward_device(mt_layer* L, const BwLayout& b, const void* x, const void* d
     if ((e = cudaEventRecord(L->fork_ev, st)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(cs, L->fork_ev, 0)) != cudaSuccess)
       return cuda_fail(e, "attention backward fork");
-    count_launch(L);
+    Timed t(L, kSlotAttnBwd, st);  // both kernels: from the fork to the join
     count_launch(L);
     if ((e = mt::launch_attention_bwd(d, m, ap, st, cs)) != cudaSuccess) return cuda_fail(e, "attention backward");
     if ((e = cudaEventRecord(L->join_ev, cs)) != cudaSuccess ||

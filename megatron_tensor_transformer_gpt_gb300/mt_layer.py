@@ -111,7 +111,7 @@ _SIGS = {
                                 ctypes.c_int),
 }
 
-PROFILE_SLOTS = ("rope_table", "norm1", "gemm_qkv", "attention", "gemm_o", "norm2", "gemm_fc1", "gemm_fc2")
+PROFILE_SLOTS = ("attention_bwd", "norm1", "gemm_qkv", "attention", "gemm_o", "norm2", "gemm_fc1", "gemm_fc2")
 
 
 def lib() -> ctypes.CDLL:
