@@ -831,6 +831,19 @@ struct BwLayout {
   size_t off[kBNum], size[kBNum], total;
 };
 
+// Runs the dK/dV kernel of the attention backward cuts each (key block, kv group) into: doubled
+// while the grid has fewer CTAs than SMs and the shortest key block (the last, with the fewest
+// query blocks) still has a step for every run.  With few kv groups (one TP rank of a GQA layer)
+// the grid would otherwise leave most SMs idle; with enough CTAs a split only adds the partial
+// sums' traffic (Llama-3-8B shape, 256 CTAs: the same time with two runs).
+int kv_parts(const mt_layer* L, int S, int B) {
+  const int nb = (S + 127) / 128, shortest = (L->nh_r / L->ng_r) * ((S + 63) / 64 - 2 * (nb - 1));
+  const long ctas = static_cast<long>(nb) * B * L->ng_r;
+  int parts = 1;
+  while (2 * parts <= mt::kMaxKvParts && 2 * parts <= shortest && ctas * parts < mt::num_sms()) parts *= 2;
+  return parts;
+}
+
 BwLayout bw_layout(const mt_layer* L, int S, int B) {
   BwLayout b{};
   b.fwd = layout_for(L, S, B);
@@ -845,8 +858,9 @@ BwLayout bw_layout(const mt_layer* L, int S, int B) {
   b.size[kBDh] = T * H * 2;
   b.size[kBDo] = T * qw * 2;
   b.size[kBDq] = static_cast<size_t>(B) * L->nh_r * S * d * 4;
-  b.size[kBDk] = static_cast<size_t>(B) * L->ng_r * S * d * 4;
-  b.size[kBDv] = static_cast<size_t>(B) * L->ng_r * S * d * 4;
+  // dK and dV: room for the most partial runs the attention backward may cut a key block into
+  b.size[kBDk] = static_cast<size_t>(B) * L->ng_r * S * d * 4 * mt::kMaxKvParts;
+  b.size[kBDv] = static_cast<size_t>(B) * L->ng_r * S * d * 4 * mt::kMaxKvParts;
   b.size[kBDqkv] = T * QKV * 2;
   b.size[kBDxn] = T * H * 2;
   b.size[kBGrow] = 2 * static_cast<size_t>(mt::norm_bwd_blocks(static_cast<int>(T))) * H * 4;  // norm partials
@@ -974,6 +988,7 @@ int backward_device(mt_layer* L, const BwLayout& b, const void* x, const void* d
   bf16 *dOh = bwr<bf16>(L, b, kBDoH), *Vh = bwr<bf16>(L, b, kBVh);
   const int zq = B * nh, zk = B * ng;
   const size_t sd = static_cast<size_t>(S) * d;
+  int kvp = 1;  // partial dK/dV buffers the RoPE pack sums
   // dO head-major; V from the forward's head-major fp16 copy (the bf16 dO pairs with a bf16 V)
   count_launch(L);
   if ((e = mt::launch_head_slices(dO, static_cast<size_t>(B) * qw, static_cast<size_t>(qw), static_cast<size_t>(d),
@@ -1005,6 +1020,9 @@ int backward_device(mt_layer* L, const BwLayout& b, const void* x, const void* d
     ap.dk = dk;
     ap.dv = dv;
     ap.err = L->d_err;
+    ap.kv_parts = kv_parts(L, S, B);
+    ap.part_stride = static_cast<size_t>(zk) * sd;
+    kvp = ap.kv_parts;
     // dQ on the copy stream beside dK/dV: fork after D = rowsum(dO o O), join before the RoPE pack
     if ((rc = ensure_copy_stream(L))) return rc;
     cudaStream_t cs = L->copy_stream;
@@ -1021,7 +1039,8 @@ int backward_device(mt_layer* L, const BwLayout& b, const void* x, const void* d
   bf16* dqkv = bwr<bf16>(L, b, kBDqkv);
   const float2* rope = L->rope_base > 0.f ? region<float2>(L, lay, kRope) : nullptr;
   count_launch(L);
-  if ((e = mt::launch_rope_bwd_pack(dq, dk, dv, rope, dqkv, S, B, nh, ng, d, st)) != cudaSuccess)
+  if ((e = mt::launch_rope_bwd_pack(dq, dk, dv, kvp, static_cast<size_t>(zk) * sd, rope, dqkv, S, B, nh, ng, d,
+                                    st)) != cudaSuccess)
     return cuda_fail(e, "RoPE backward");
 
   // ---- QKV projection and the input norm

@@ -455,15 +455,19 @@ __global__ void __launch_bounds__(GeoKV<D>::THREADS, 1)
 
   pdl_wait();
   pdl_trigger();
-  const int per = p.batch * p.ng;
+  const int per = p.batch * p.ng * p.kv_parts;
   const int kb = static_cast<int>(blockIdx.x) / per;  // key block 0 has the most query blocks
-  const int zk = static_cast<int>(blockIdx.x) % per;  // b * ng + g
+  const int zk = static_cast<int>(blockIdx.x) % per / p.kv_parts;  // b * ng + g
+  const int part = static_cast<int>(blockIdx.x) % p.kv_parts;
   const int b = zk / p.ng, g = zk % p.ng;
   const int rep = p.nh / p.ng;
   const int nq64 = (p.seq + 63) / 64;
   const int i0 = 2 * kb;            // first 64-query block that sees a key of this block
   const int per_head = nq64 - i0;   // >= 1 for every launched key block
-  const int nst = rep * per_head;   // steps: (head of the group, query block)
+  // steps (head of the group, query block), flattened; this CTA takes the run [n0, n0 + nst), which
+  // is not empty (the launcher cuts at most as many runs as the shortest key block has steps)
+  const int n0 = part * (rep * per_head) / p.kv_parts;
+  const int nst = (part + 1) * (rep * per_head) / p.kv_parts - n0;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -511,8 +515,8 @@ __global__ void __launch_bounds__(GeoKV<D>::THREADS, 1)
       int issued = 0;
       bool ok = true;
       for (int n = 0; n < nst; ++n) {
-        const int zq = b * p.nh + g * rep + n / per_head;
-        const int qi0 = (i0 + n % per_head) * 64;
+        const int zq = b * p.nh + g * rep + (n0 + n) / per_head;
+        const int qi0 = (i0 + (n0 + n) % per_head) * 64;
         if (!mbar_wait(st_empty(n), ((n / NS) & 1) ^ 1u, p.err, abort_flag)) {
           ok = false;
           break;
@@ -601,8 +605,8 @@ __global__ void __launch_bounds__(GeoKV<D>::THREADS, 1)
         quad_sync(quad);
         continue;
       }
-      const int zq = b * p.nh + g * rep + n / per_head;
-      const int qc0 = (i0 + n % per_head) * 64 + 16 * c4;  // this warp's first query column
+      const int zq = b * p.nh + g * rep + (n0 + n) / per_head;
+      const int qc0 = (i0 + (n0 + n) % per_head) * 64 + 16 * c4;  // this warp's first query column
       // the 16 columns' row statistics, the same for every lane (one broadcast load each); columns
       // past seq read the last row's (their P^T and dS^T multiply zero rows of dO and Q)
       // dsum is kept as D / sqrt(d), so that dS^T = P^T (dP^T / sqrt(d) - D / sqrt(d)) is one FMA and a product
@@ -687,8 +691,9 @@ __global__ void __launch_bounds__(GeoKV<D>::THREADS, 1)
         }
       }
       if (row_ok) {
-        float4* dv = reinterpret_cast<float4*>(p.dv + row * D + W * c4);
-        float4* dk = reinterpret_cast<float4*>(p.dk + row * D + W * c4);
+        const size_t off = part * p.part_stride + row * D + W * c4;  // this run's partial sums
+        float4* dv = reinterpret_cast<float4*>(p.dv + off);
+        float4* dk = reinterpret_cast<float4*>(p.dk + off);
 #pragma unroll
         for (int q = 0; q < W / 4; ++q) {
           dv[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
@@ -720,7 +725,7 @@ cudaError_t launch_bwd_d(const CUtensorMap* maps, const AttnBwdParams& p, cudaSt
   const unsigned nb = static_cast<unsigned>((p.seq + 127) / 128);
   // maps: Q, dO, K, V as 128-row boxes; Q, dO as 64-row boxes.  dK/dV first: its longest blocks
   // (key block 0 sees every query block) set the critical path, so they start before any dQ block.
-  cudaError_t e = launch_pdl(attn_bwd_dkdv_kernel<D>, dim3(nb * p.batch * p.ng), dim3(GeoKV<D>::THREADS),
+  cudaError_t e = launch_pdl(attn_bwd_dkdv_kernel<D>, dim3(nb * p.batch * p.ng * p.kv_parts), dim3(GeoKV<D>::THREADS),
                              GeoKV<D>::SMEM, st, maps[2], maps[3], maps[4], maps[5], p);
   if (e != cudaSuccess) return e;
   return launch_pdl(attn_bwd_dq_kernel<D>, dim3(nb * p.batch * p.nh), dim3(GeoQ<D>::THREADS), GeoQ<D>::SMEM, st_dq,
@@ -754,6 +759,11 @@ cudaError_t launch_row_dot(const bf16* dO, const bf16* O, float* Dsum, int S, in
 cudaError_t launch_attention_bwd(int head_dim, const CUtensorMap* maps, const AttnBwdParams& p, cudaStream_t st,
                                  cudaStream_t st_dq) {
   if (p.seq <= 0) return cudaSuccess;
+  // every run of steps must be non-empty: the last key block has the fewest, (nh / ng) x (query
+  // blocks of 64 from its first on), and part_stride must keep whole rows of D floats
+  const int nb = (p.seq + 127) / 128, shortest = (p.nh / p.ng) * ((p.seq + 63) / 64 - 2 * (nb - 1));
+  if (p.kv_parts < 1 || p.kv_parts > kMaxKvParts || p.kv_parts > shortest || p.part_stride % head_dim != 0)
+    return cudaErrorInvalidValue;
   if (head_dim == 64) return launch_bwd_d<64>(maps, p, st, st_dq);
   if (head_dim == 128) return launch_bwd_d<128>(maps, p, st, st_dq);
   return cudaErrorInvalidValue;

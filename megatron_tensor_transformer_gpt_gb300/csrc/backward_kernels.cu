@@ -223,11 +223,31 @@ __global__ void f32_to_bf16_kernel(const float* __restrict__ a, bf16* __restrict
   if (i < n) b[i] = __float2bfloat16_rn(a[i]);
 }
 
+// Eight consecutive floats at src, summed over n buffers `stride` floats apart (in buffer order).
+__device__ __forceinline__ void load8_sum(const float* src, int n, size_t stride, float* g) {
+  *reinterpret_cast<float4*>(g) = *reinterpret_cast<const float4*>(src);
+  *reinterpret_cast<float4*>(g + 4) = *reinterpret_cast<const float4*>(src + 4);
+  for (int r = 1; r < n; ++r) {
+    const float4 a = *reinterpret_cast<const float4*>(src + r * stride);
+    const float4 c = *reinterpret_cast<const float4*>(src + r * stride + 4);
+    g[0] += a.x;
+    g[1] += a.y;
+    g[2] += a.z;
+    g[3] += a.w;
+    g[4] += c.x;
+    g[5] += c.y;
+    g[6] += c.z;
+    g[7] += c.w;
+  }
+}
+
 // dqkv[t, :] from the per-head fp32 gradients of q, k (after RoPE) and v: the rotation's transpose
-// (the opposite angle) on q and k, then [q heads | k groups | v groups] in the fused layout.
+// (the opposite angle) on q and k, then [q heads | k groups | v groups] in the fused layout; dk and dv
+// are summed over `parts` partial buffers first.
 __global__ void rope_bwd_pack_kernel(const float* __restrict__ dq, const float* __restrict__ dk,
-                                     const float* __restrict__ dv, const float2* __restrict__ rope,
-                                     bf16* __restrict__ dqkv, int S, int B, int nh, int ng, int d) {
+                                     const float* __restrict__ dv, int parts, size_t part_stride,
+                                     const float2* __restrict__ rope, bf16* __restrict__ dqkv, int S, int B, int nh,
+                                     int ng, int d) {
   const int t = blockIdx.x;  // token row s*B + b
   const int s = t / B, b = t - s * B;
   const int half = d / 2;
@@ -239,17 +259,15 @@ __global__ void rope_bwd_pack_kernel(const float* __restrict__ dq, const float* 
     if (head < nh) src = dq + ((static_cast<size_t>(b) * nh + head) * S + s) * d;
     else if (head < nh + ng) src = dk + ((static_cast<size_t>(b) * ng + head - nh) * S + s) * d;
     else src = dv + ((static_cast<size_t>(b) * ng + head - nh - ng) * S + s) * d;
+    const int np = head < nh ? 1 : parts;  // dk and dv: the sum of the partial buffers
     float g[8];
-    *reinterpret_cast<float4*>(g) = *reinterpret_cast<const float4*>(src + i);
-    *reinterpret_cast<float4*>(g + 4) = *reinterpret_cast<const float4*>(src + i + 4);
+    load8_sum(src + i, np, part_stride, g);
     if (rope != nullptr && head < nh + ng) {
       // forward: y1 = x1 c - x2 s, y2 = x2 c + x1 s  ->  dx1 = dy1 c + dy2 s, dx2 = dy2 c - dy1 s
       const bool first = i < half;
       const int p = first ? i : i - half;
-      const float* o_src = src + (first ? i + half : i - half);
       float o[8];
-      *reinterpret_cast<float4*>(o) = *reinterpret_cast<const float4*>(o_src);
-      *reinterpret_cast<float4*>(o + 4) = *reinterpret_cast<const float4*>(o_src + 4);
+      load8_sum(src + (first ? i + half : i - half), np, part_stride, o);
       const float4* cs4 = reinterpret_cast<const float4*>(rope + static_cast<size_t>(s) * half + p);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -368,11 +386,12 @@ cudaError_t launch_f16_to_bf16(const __half* src, bf16* dst, size_t n, cudaStrea
   return cudaGetLastError();
 }
 
-cudaError_t launch_rope_bwd_pack(const float* dq, const float* dk, const float* dv, const float2* rope, bf16* dqkv,
-                                 int S, int B, int nh, int ng, int d, cudaStream_t st) {
+cudaError_t launch_rope_bwd_pack(const float* dq, const float* dk, const float* dv, int parts, size_t part_stride,
+                                 const float2* rope, bf16* dqkv, int S, int B, int nh, int ng, int d, cudaStream_t st) {
+  if (parts < 1 || part_stride % 8 != 0) return cudaErrorInvalidValue;
   if (d % 16 != 0) return cudaErrorInvalidValue;  // eight-column vectors inside each half of a head
   const int threads = std::min(256, ((nh + 2 * ng) * d / 8 + 31) / 32 * 32);
-  rope_bwd_pack_kernel<<<S * B, threads, 0, st>>>(dq, dk, dv, rope, dqkv, S, B, nh, ng, d);
+  rope_bwd_pack_kernel<<<S * B, threads, 0, st>>>(dq, dk, dv, parts, part_stride, rope, dqkv, S, B, nh, ng, d);
   return cudaGetLastError();
 }
 

@@ -120,7 +120,13 @@ struct AttnBwdParams {
   const float* dsum;
   float *dq, *dk, *dv;
   int* err;
+  // dK/dV: the (head, query block) steps of every (key block, kv group) are cut into kv_parts
+  // (1..kMaxKvParts) equal runs on separate CTAs; run r writes its partial sums to dk and dv +
+  // r * part_stride floats, which the caller adds
+  int kv_parts;
+  size_t part_stride;
 };
+constexpr int kMaxKvParts = 4;
 
 // Sequence-parallel epilogue (see mt_sp_reduce_add_norm).
 constexpr int kMaxSpParts = 16;
@@ -220,8 +226,10 @@ cudaError_t launch_f16_to_bf16(const __half* src, bf16* dst, size_t n, cudaStrea
 // dst [C, R] (pitch dp) = src [R, C] (pitch sp)^T, bf16; R, C and the pitches multiples of 8, 16-byte
 // aligned pointers (cudaErrorInvalidValue otherwise).
 cudaError_t launch_transpose_bf16(const bf16* src, size_t sp, bf16* dst, size_t dp, int R, int C, cudaStream_t st);
-cudaError_t launch_rope_bwd_pack(const float* dq, const float* dk, const float* dv, const float2* rope, bf16* dqkv,
-                                 int S, int B, int nh, int ng, int d, cudaStream_t st);
+// dqkv [T, (nh + 2 ng) d] bf16 from head-major fp32 dq, dk, dv (dk and dv the sums of `parts`
+// partial buffers part_stride floats apart), with RoPE's rotation undone on the q and k heads.
+cudaError_t launch_rope_bwd_pack(const float* dq, const float* dk, const float* dv, int parts, size_t part_stride,
+                                 const float2* rope, bf16* dqkv, int S, int B, int nh, int ng, int d, cudaStream_t st);
 
 // Delayed-scaling update after an FP8 forward (state layout: see fp8_history_kernel).
 cudaError_t launch_fp8_history(float* state, int len, int pos, cudaStream_t stream);
