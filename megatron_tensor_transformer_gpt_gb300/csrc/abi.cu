@@ -911,6 +911,7 @@ int linear_bwd(mt_layer* L, const BwLayout& b, const void* dY, const void* X, co
   }
   if (db != nullptr) {
     count_launch(L);
+    count_launch(L);  // the column sums, then their conversion to bf16
     cudaError_t e = mt::launch_colsum(dY, false, N, M, N, bwr<float>(L, b, kBAcc), static_cast<bf16*>(db), st);
     if (e != cudaSuccess) return cuda_fail(e, "bias gradient");
   }
@@ -929,9 +930,11 @@ int norm_bwd(mt_layer* L, const BwLayout& b, const void* dy, const void* x, cons
                                       static_cast<bf16*>(out), part, T, H, L->eps, L->norm == MT_NORM_LAYER, st);
   if (e == cudaSuccess && dgamma != nullptr) {
     count_launch(L);
+    count_launch(L);  // the column sums, then their conversion to bf16
     e = mt::launch_colsum(part, true, H, nb, H, bwr<float>(L, b, kBAcc), static_cast<bf16*>(dgamma), st);
   }
   if (e == cudaSuccess && dbeta != nullptr && L->norm == MT_NORM_LAYER) {
+    count_launch(L);
     count_launch(L);
     e = mt::launch_colsum(part + static_cast<size_t>(nb) * H, true, H, nb, H, bwr<float>(L, b, kBAcc),
                           static_cast<bf16*>(dbeta), st);
