@@ -202,9 +202,10 @@ typedef struct { /* device pointers, shapes as in mt_weights; NULL = gradient no
 } mt_grads;
 
 /* Workspace the backward pass needs (a superset of the forward's: the forward intermediates, the
- * plain QKV and fc1 outputs, gradient scratch in bf16, fp32 dq/dk/dv in head-major order, the
- * per-row softmax statistics and head-major copies of dO and V).  No [seq, seq] matrix is stored:
- * the attention backward rebuilds the probabilities tile by tile. */
+ * pre-activation fc1 output, gradient scratch in bf16, fp32 dq in head-major order and up to four
+ * partial copies of fp32 dk/dv, the per-row softmax statistics, a head-major copy of dO and a bf16
+ * V).  No [seq, seq] matrix is stored: the attention backward rebuilds the probabilities tile by
+ * tile. */
 int mt_layer_backward_workspace_bytes(const mt_layer* L, int seq, int batch, size_t* bytes);
 
 /* dx [T, H] = dL/dx and the requested weight gradients, given x and dy = dL/dy [T, H].  Needs
