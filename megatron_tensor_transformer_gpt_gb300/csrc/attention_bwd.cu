@@ -9,10 +9,13 @@
 // elementwise warps (one row per thread, four warps per TMEM lane quadrant):
 //   attn_bwd_dq_kernel:   one CTA per (128 queries, head); steps over 128-key blocks j <= i:
 //                         Q in TMEM, S and dP into TMEM, dS (bf16) into TMEM, dQ += dS K in TMEM.
-//   attn_bwd_dkdv_kernel: one CTA per (128 keys, kv group); steps over the group's heads and the
-//                         64-query blocks i >= j: S^T and dP^T into TMEM, P^T and dS^T (bf16) into
-//                         TMEM, dV += P^T dO and dK += dS^T Q in TMEM.
-// The caller provides head-major copies of dO and V (head_slices_kernel below); the second operands of the
+//   attn_bwd_dkdv_kernel: one CTA per (128 keys, kv group, run); steps over the group's heads and
+//                         the 64-query blocks i >= j: S^T and dP^T into TMEM, P^T and dS^T (bf16) into
+//                         TMEM, dV += P^T dO and dK += dS^T Q in TMEM.  With kv_parts > 1 the steps of
+//                         a (key block, group) are cut into that many runs on separate CTAs, each
+//                         writing partial sums to its own dK/dV buffer (the caller adds them).
+// The two kernels share no output, so the caller may run them on two streams at once.
+// The caller provides head-major copies of dO and V (dO by head_slices_kernel below); the second operands of the
 // gradient products (K for dQ, dO for dV, Q for dK) are the tiles already staged for the score
 // products, read as MN-major operands.
 #include "common.cuh"
@@ -31,7 +34,7 @@ __device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) { re
 
 // ------------------------------------------------------------------ prep
 // Batched copy of the R x C slices src_z = src + (z / zdiv) * sb + (z % zdiv) * sh (row pitch sp) into
-// dst + z R dp (row pitch dp): the head-major copies of dO and V.
+// dst + z R dp (row pitch dp): the head-major copy of dO.
 __global__ void head_slices_kernel(const bf16* __restrict__ src, size_t sp, size_t sb, size_t sh, int zdiv,
                                    bf16* __restrict__ dst, size_t dp, int R, int C) {
   const int z = blockIdx.z;
