@@ -18,7 +18,11 @@
 using mt::bf16;
 
 // K-split tails of the CTA-pair GEMM: at most kKsTiles tail tiles and kKsSlots partial sums of
-// 256 x 256 fp32 per launch (a tail of r tiles cut into s K ranges stores r (s - 1) of them).
+// 256 x 256 fp32 per launch (a tail of r tiles cut into s K ranges stores r (s - 1) of them).  One
+// set: only the GEMMs of the caller's stream cut K (the backward's weight-gradient GEMMs, on a stream
+// of their own, cut their tails along N), so no two launches share it at once.  The range holding a
+// tail tile's first K blocks waits for the other ranges; their CTAs may start late while a
+// weight-gradient GEMM holds SMs, but that GEMM waits on nothing outside its own CTAs, so they start.
 constexpr int kKsSlots = 64, kKsTiles = 64;
 
 struct mt_layer {
@@ -48,6 +52,10 @@ struct mt_layer {
   cudaStream_t copy_stream;
   cudaEvent_t copy_ev[9];
   cudaEvent_t fork_ev, join_ev;
+  // the backward's weight-gradient GEMMs: a stream of their own (created on first use), forked from
+  // the caller's stream where each one's operands are ready and joined back at the end
+  cudaStream_t dw_stream;
+  cudaEvent_t dw_fork, dw_join;
   // K-split tails of the CTA-pair GEMM: partial sums (kKsSlots slots of 256 x 256 fp32) and
   // arrival counters (kept at zero between launches)
   float4* d_kws;
@@ -168,6 +176,21 @@ int ensure_copy_stream(mt_layer* L) {
     return cuda_fail(e, "creating the copy events");
   }
   L->copy_stream = s;
+  return MT_OK;
+}
+
+// The stream of the backward's weight-gradient GEMMs and its two events, created on first use.
+int ensure_dw_stream(mt_layer* L) {
+  if (L->dw_stream != nullptr) return MT_OK;
+  cudaStream_t s = nullptr;
+  cudaError_t e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
+  if (e == cudaSuccess && L->dw_fork == nullptr) e = cudaEventCreateWithFlags(&L->dw_fork, cudaEventDisableTiming);
+  if (e == cudaSuccess && L->dw_join == nullptr) e = cudaEventCreateWithFlags(&L->dw_join, cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    if (s != nullptr) cudaStreamDestroy(s);
+    return cuda_fail(e, "creating the weight-gradient stream");
+  }
+  L->dw_stream = s;
   return MT_OK;
 }
 
@@ -429,8 +452,8 @@ void plan_gemm_on(mt::GemmParams& p, int mode, int head_dim, bool ksplit_ok, boo
   p.epi_split = (p.K <= 2048 || p.num_units <= workers || (p.ksplit > 1 && p.K <= 4096)) ? 2 : 1;
 }
 
-void plan_gemm(mt::GemmParams& p, int mode, int head_dim, const mt_layer* L, bool fp8) {
-  const bool ksplit_ok = L != nullptr && L->d_kws != nullptr;
+void plan_gemm(mt::GemmParams& p, int mode, int head_dim, const mt_layer* L, bool fp8, bool cut_k = true) {
+  const bool ksplit_ok = cut_k && L != nullptr && L->d_kws != nullptr;
   const int sms = mt::num_sms();
   // the resident-pair query only where the pair kernel can be chosen (as the planner decides it)
   const int pair_slots = (g_pairing.load() != 1 && p.M > 128) ? mt::gemm_pair_slots() : std::max(1, sms / 2);
@@ -799,7 +822,8 @@ int forward_device_fp8(mt_layer* L, const Layout& lay, const void* x, int S, int
 // stored [N, K] (b_mn = false) or [K, N] (b_mn = true), pitch ldb.  L may be null (no error word,
 // no launch count).
 int gemm_ab(mt_layer* L, const void* A, size_t lda, bool a_mn, const void* Bm, size_t ldb, bool b_mn, int M, int N,
-            int K, void* out, float* out32, size_t ldo, bool acc32, cudaStream_t st, bool c_trans = false) {
+            int K, void* out, float* out32, size_t ldo, bool acc32, cudaStream_t st, bool c_trans = false,
+            bool cut_k = true) {
   CUtensorMap ta, tb, tb64;
   int rc = a_mn ? map_2d(&ta, A, M, K, lda, 64) : map_2d(&ta, A, K, M, lda, 128);
   if (!rc) rc = b_mn ? map_2d(&tb, Bm, N, K, ldb, 64) : map_2d(&tb, Bm, K, N, ldb, 128);
@@ -813,7 +837,7 @@ int gemm_ab(mt_layer* L, const void* A, size_t lda, bool a_mn, const void* Bm, s
   p.a_mn = a_mn ? 1 : 0;
   p.b_mn = b_mn ? 1 : 0;
   p.c_trans = c_trans && out32 == nullptr ? 1 : 0;
-  plan_gemm(p, mt::kEpiStore, 0, L, false);
+  plan_gemm(p, mt::kEpiStore, 0, L, false, cut_k);
   CUtensorMap to = ta;
   if ((rc = prepare_out(p, mt::kEpiStore, &to))) return rc;
   count_launch(L);
@@ -890,8 +914,10 @@ T* bwr(const mt_layer* L, const BwLayout& b, BwRegion r) {
 
 // Gradients of one linear Y = X W^T (+ b) given dY (all bf16, dense):
 //   dW [N, K] = dY^T X, db = column sums of dY, dX [M, K] = dY W (written to dx if not null).
+// The weight gradient (its operand transpose and GEMM) runs on `sw` once dY and X are ready on `st`
+// (sw may be st); the bias gradient and dX run on `st`.
 int linear_bwd(mt_layer* L, const BwLayout& b, const void* dY, const void* X, const void* W, int M, int N, int K,
-               void* dW, void* db, void* dX, cudaStream_t st) {
+               void* dW, void* db, void* dX, cudaStream_t st, cudaStream_t sw) {
   int rc;
   // Y [M, N] = X [M, K] W[N, K]^T.  The GEMM reads an MN-major A at full rate and loses 12-14 % on an
   // MN-major B, so every product here takes its B K-major:
@@ -899,14 +925,20 @@ int linear_bwd(mt_layer* L, const BwLayout& b, const void* dY, const void* X, co
   //        narrower of the two, dW^T = X^T dY with dY^T [N, M] as B, stored transposed;
   //   dX = dY W formed as dX^T = W^T dY^T: W an MN-major A, dY a K-major B, stored transposed.
   if (dW != nullptr) {
+    // the transpose buffer is used on `sw` only, so the weight gradients take it in turn
     bf16* tr = bwr<bf16>(L, b, kBT);
     const bool tx = K <= N;  // transpose X (else dY)
+    const bool cut_k = sw == st;  // a K-cut tail's waits assume no other kernel of the handle runs beside it
+    cudaError_t e = cudaSuccess;
+    if (sw != st && ((e = cudaEventRecord(L->dw_fork, st)) != cudaSuccess ||
+                     (e = cudaStreamWaitEvent(sw, L->dw_fork, 0)) != cudaSuccess))
+      return cuda_fail(e, "weight-gradient fork");
     count_launch(L);
-    cudaError_t e = tx ? mt::launch_transpose_bf16(static_cast<const bf16*>(X), K, tr, M, M, K, st)
-                       : mt::launch_transpose_bf16(static_cast<const bf16*>(dY), N, tr, M, M, N, st);
+    e = tx ? mt::launch_transpose_bf16(static_cast<const bf16*>(X), K, tr, M, M, K, sw)
+           : mt::launch_transpose_bf16(static_cast<const bf16*>(dY), N, tr, M, M, N, sw);
     if (e != cudaSuccess) return cuda_fail(e, "weight-gradient operand transpose");
-    if ((rc = tx ? gemm_ab(L, dY, N, true, tr, M, false, N, K, M, dW, nullptr, K, false, st)
-                 : gemm_ab(L, X, K, true, tr, M, false, K, N, M, dW, nullptr, K, false, st, true)))
+    if ((rc = tx ? gemm_ab(L, dY, N, true, tr, M, false, N, K, M, dW, nullptr, K, false, sw, false, cut_k)
+                 : gemm_ab(L, X, K, true, tr, M, false, K, N, M, dW, nullptr, K, false, sw, true, cut_k)))
       return rc;
   }
   if (db != nullptr) {
@@ -974,15 +1006,19 @@ int backward_device(mt_layer* L, const BwLayout& b, const void* x, const void* d
   // ---- MLP
   bf16 *da = bwr<bf16>(L, b, kBDa), *du = bwr<bf16>(L, b, kBDu), *dhn = bwr<bf16>(L, b, kBDhn);
   bf16* dh = bwr<bf16>(L, b, kBDh);
-  if ((rc = linear_bwd(L, b, dy, a, w->w_fc2, T, H, f, g->w_fc2, w->b_fc2 ? g->b_fc2 : nullptr, da, st))) return rc;
+  if ((rc = ensure_dw_stream(L))) return rc;
+  cudaStream_t sw = L->dw_stream;  // the weight gradients' GEMMs, beside the chain of dX
+  if ((rc = linear_bwd(L, b, dy, a, w->w_fc2, T, H, f, g->w_fc2, w->b_fc2 ? g->b_fc2 : nullptr, da, st, sw)))
+    return rc;
   count_launch(L);
   if ((e = mt::launch_act_bwd(u, da, du, T, f, swiglu, st)) != cudaSuccess) return cuda_fail(e, "activation backward");
-  if ((rc = linear_bwd(L, b, du, hn, w->w_fc1, T, f1, H, g->w_fc1, w->b_fc1 ? g->b_fc1 : nullptr, dhn, st))) return rc;
+  if ((rc = linear_bwd(L, b, du, hn, w->w_fc1, T, f1, H, g->w_fc1, w->b_fc1 ? g->b_fc1 : nullptr, dhn, st, sw)))
+    return rc;
   if ((rc = norm_bwd(L, b, dhn, h, w->norm2_w, dy, dh, g->norm2_w, g->norm2_b, T, st))) return rc;
 
   // ---- output projection
   bf16* dO = bwr<bf16>(L, b, kBDo);
-  if ((rc = linear_bwd(L, b, dh, o, w->w_o, T, H, qw, g->w_o, w->b_o ? g->b_o : nullptr, dO, st))) return rc;
+  if ((rc = linear_bwd(L, b, dh, o, w->w_o, T, H, qw, g->w_o, w->b_o ? g->b_o : nullptr, dO, st, sw))) return rc;
 
   // ---- attention, flash-style: P and dS are rebuilt tile by tile from the row log-sum-exp the
   //      forward recompute wrote; fp32 dQ, dK, dV
@@ -1048,9 +1084,12 @@ int backward_device(mt_layer* L, const BwLayout& b, const void* x, const void* d
 
   // ---- QKV projection and the input norm
   bf16* dxn = bwr<bf16>(L, b, kBDxn);
-  if ((rc = linear_bwd(L, b, dqkv, xn, w->w_qkv, T, QKV, H, g->w_qkv, w->b_qkv ? g->b_qkv : nullptr, dxn, st)))
+  if ((rc = linear_bwd(L, b, dqkv, xn, w->w_qkv, T, QKV, H, g->w_qkv, w->b_qkv ? g->b_qkv : nullptr, dxn, st, sw)))
     return rc;
-  return norm_bwd(L, b, dxn, x, w->norm1_w, dh, dx, g->norm1_w, g->norm1_b, T, st);
+  if ((rc = norm_bwd(L, b, dxn, x, w->norm1_w, dh, dx, g->norm1_w, g->norm1_b, T, st))) return rc;
+  if ((e = cudaEventRecord(L->dw_join, sw)) != cudaSuccess || (e = cudaStreamWaitEvent(st, L->dw_join, 0)) != cudaSuccess)
+    return cuda_fail(e, "weight-gradient join");
+  return MT_OK;
 }
 
 }  // namespace
@@ -1344,6 +1383,9 @@ void mt_layer_destroy(mt_layer* L) {
   if (L->fork_ev) cudaEventDestroy(L->fork_ev);
   if (L->join_ev) cudaEventDestroy(L->join_ev);
   if (L->copy_stream) cudaStreamDestroy(L->copy_stream);
+  if (L->dw_fork) cudaEventDestroy(L->dw_fork);
+  if (L->dw_join) cudaEventDestroy(L->dw_join);
+  if (L->dw_stream) cudaStreamDestroy(L->dw_stream);
   if (L->done_ev) cudaEventDestroy(L->done_ev);
   delete L;
 }
