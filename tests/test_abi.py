@@ -169,20 +169,23 @@ def test_gemm_plan_of_the_ksplit_test_layers(lib):
 
 
 def test_gemm_plan_of_the_backward_ksplit_layers(lib):
-    """The weight-gradient GEMMs of the GPU backward tests' K-split layers (dW [out, in] = dY^T X,
-    K = the 2048 or 2064 tokens) are single partial waves cut into 4 ranges of K, and so are the
-    Llama-3-8B-shaped layer's dW of QKV (tail 4 tiles); its output projection's dW (tail 28 tiles)
-    takes 2.  Planning does not depend on the operands' layout."""
-    ks = lambda M, N, K: ml.mt_gemm_plan(M, N, K, 0)["ksplit"]
+    """The backward's dX GEMMs (dX^T = W^T dY^T: M = the layer's input width, N = the tokens, K = its
+    output width) in the GPU backward tests' K-split layers: fc1's is a single partial wave cut into 4
+    ranges of K (the second layer with a ragged last K block, K = 2056); at the Llama-3-8B shape the
+    dX of the output projection, QKV and fc1 cut their 28-tile tails into 2.  The weight-gradient
+    GEMMs, which run beside them on a stream of their own, are planned without K ranges (as the
+    handle-less calls are) and cut their tails along N.  Planning does not depend on the operands'
+    layout."""
+    ks = lambda M, N, K, handle=True: ml.mt_gemm_plan(M, N, K, 0, with_handle=handle)
     for T in (2048, 2064):
-        assert ks(512, 1024, T) == 4     # dW_fc2 (hidden 512, ffn 1024)
-        assert ks(2048, 512, T) == 4     # dW_fc1, SwiGLU rows
-        assert ks(512, 512, T) == 4      # dW_o
-        assert ks(768, 512, T) == 4      # dW_qkv, 8 x 64 heads over 2 groups
-    assert ks(1000, 512, 2064) == 4      # dW_fc1, GeLU ffn 1000 of the ragged layer
-    assert ks(512, 1000, 2064) == 4      # dW_fc2
-    assert ks(6144, 4096, 4096) == 4     # Llama-3-8B dW_qkv
-    assert ks(4096, 4096, 4096) == 2     # Llama-3-8B dW_o
+        assert ks(512, T, 2048)["ksplit"] == 4       # dX_fc1 (SwiGLU rows 2048)
+    assert ks(512, 2064, 2056)["ksplit"] == 4        # dX_fc1, GeLU ffn 2056: a ragged last K block
+    assert ks(4096, 4096, 4096)["ksplit"] == 2       # Llama-3-8B dX_o
+    assert ks(4096, 4096, 6144)["ksplit"] == 2       # dX_qkv
+    assert ks(4096, 4096, 28672)["ksplit"] == 2      # dX_fc1
+    for M, N, K in ((512, 1024, 2048), (6144, 4096, 4096), (4096, 4096, 4096)):  # dW_fc2, dW_qkv, dW_o
+        plan = ks(M, N, K, handle=False)
+        assert plan["ksplit"] == 1 and plan["split"] == 2
 
 
 def _with_tail_split(mode, fn):

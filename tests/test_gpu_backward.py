@@ -29,15 +29,16 @@ def assert_grad_close(got, want, what):
     assert rel < 2e-2, f"{what}: relative Frobenius error {rel:.3e}"
 
 
-# Shapes whose weight-gradient GEMMs (dW = dY^T X: K = T tokens, both operands read MN-major) take
-# the layer handle's K-split tail: with K = 2048 or 2064 tokens every dW GEMM of these small layers
-# is a single partial wave, cut into 4 ranges of K (tests/test_abi.py pins the plan); the second
-# has a ragged last K block (T = 2064) and batch 2.
+# Shapes whose dX GEMMs take the layer handle's K-split tail with an MN-major A operand (dX^T = W^T
+# dY^T reads W MN-major): fc1's dX (M = hidden 512, N = the tokens, K = fc1's output width) is a
+# single partial wave cut into 4 ranges of K (tests/test_abi.py pins the plans); the second layer's
+# K = 2056 leaves a ragged last K block, with batch 2 and 2064 tokens.  (The weight gradients run
+# on a stream of their own and cut their tails along N.)
 KSPLIT_CFGS = [
     synth.LayerConfig("bw_ksplit", batch=1, seq=2048, hidden=512, heads=8, groups=2, head_dim=64, ffn=1024,
                       rope_base=1e4, bias=True),
     synth.LayerConfig("bw_ksplit_ragged", batch=2, seq=1032, hidden=512, heads=4, groups=1, head_dim=128,
-                      ffn=1000, norm="layer", act="gelu_tanh", rope_base=0.0, bias=True),
+                      ffn=2056, norm="layer", act="gelu_tanh", rope_base=0.0, bias=True),
 ]
 
 CFGS = [
