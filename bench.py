@@ -37,6 +37,8 @@ sys.path.insert(0, ROOT)
 import synth  # noqa: E402
 
 METRIC = "Layer fwd TFLOP/s & MFU vs GB300 bf16 dense peak; tokens/s per layer (1 GPU)"
+# --backward: the same layer's backward pass (forward recompute included in the time, not in the work)
+METRIC_BWD = "Layer bwd TFLOP/s (the backward's own algorithmic work) & MFU vs GB300 bf16 dense peak (1 GPU)"
 UNIT = "TFLOP/s"
 EXTRA_WORKLOADS = ("tiny", "gpt345m", "llama70b_tp8", "llama8b_32k")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -478,8 +480,8 @@ def run_native(args):
         cpu_extra = cpu_oracle_extras()
 
     out = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": total_ms / args.steps,
+        "metric": METRIC_BWD if args.backward else METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
         "step_ms": {"median": step_med, "p10": step_p10, "p90": step_p90,
                     "note": "CUDA-event time of each timed step; the slowest rank's statistic"},
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
