@@ -39,6 +39,8 @@ import synth  # noqa: E402
 METRIC = "Layer fwd TFLOP/s & MFU vs GB300 bf16 dense peak; tokens/s per layer (1 GPU)"
 # --backward: the same layer's backward pass (forward recompute included in the time, not in the work)
 METRIC_BWD = "Layer bwd TFLOP/s (the backward's own algorithmic work) & MFU vs GB300 bf16 dense peak (1 GPU)"
+# --train-step: forward then backward (the forward's and the backward's algorithmic work)
+METRIC_TRAIN = "Layer training step (fwd + bwd) TFLOP/s & MFU vs GB300 bf16 dense peak (1 GPU)"
 UNIT = "TFLOP/s"
 EXTRA_WORKLOADS = ("tiny", "gpt345m", "llama70b_tp8", "llama8b_32k")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -353,6 +355,8 @@ def run_native(args):
         # and dQ, dK, dV, dP plus the recomputed scores (2.5x the causal attention); the forward
         # recompute it also runs is not counted
         flops = 2.0 * cfg.gemm_flops() + 2.5 * cfg.attn_flops()
+        if args.train_step:  # forward and backward: the forward's work plus the backward's
+            flops += cfg.flops()
         rng = np.random.default_rng(rank + 100)
         dyb = torch.from_numpy(synth.f32_to_bf16_bits(rng.standard_normal((cfg.tokens, cfg.hidden), dtype=np.float32))
                                .view(np.int16)).view(torch.bfloat16).to(dev)
@@ -360,7 +364,13 @@ def run_native(args):
         grads = {k: (None if v is None else torch.empty_like(v)) for k, v in tens.items()}
 
     def step():
-        if args.backward:
+        if args.train_step == "saved":
+            layer.forward_train(x, cfg.seq, cfg.batch, w, y)
+            layer.backward_saved(x, dyb, cfg.seq, cfg.batch, w, dxb, grads)
+        elif args.train_step == "recompute":
+            layer.forward(x, cfg.seq, cfg.batch, w, y)
+            layer.backward(x, dyb, cfg.seq, cfg.batch, w, dxb, grads)
+        elif args.backward:
             layer.backward(x, dyb, cfg.seq, cfg.batch, w, dxb, grads)
         else:
             layer.forward(x, cfg.seq, cfg.batch, w, y)
@@ -480,7 +490,8 @@ def run_native(args):
         cpu_extra = cpu_oracle_extras()
 
     out = {
-        "metric": METRIC_BWD if args.backward else METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "metric": METRIC_TRAIN if args.train_step else METRIC_BWD if args.backward else METRIC, "value": value,
+        "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
         "step_ms": {"median": step_med, "p10": step_p10, "p90": step_p90,
                     "note": "CUDA-event time of each timed step; the slowest rank's statistic"},
@@ -566,12 +577,17 @@ def main():
                     help="skip the GPU-only timings of the other configurations")
     ap.add_argument("--backward", action="store_true",
                     help="time mt_layer_backward (forward recompute + gradients) instead of the forward")
+    ap.add_argument("--train-step", choices=("recompute", "saved"), default=None,
+                    help="time a training step: mt_layer_forward + mt_layer_backward (recompute) or "
+                         "mt_layer_forward_train + mt_layer_backward_saved (saved)")
     ap.add_argument("--fp8", action="store_true",
                     help="time the FP8 (E4M3) forward instead of the bf16 one (no host-buffer pass, no CPU baseline)")
     ap.add_argument("--quick", action="store_true",
                     help="profiling runs: no clock sampling, no host-buffer pass, no CPU baseline")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    if args.train_step:
+        args.backward = True  # the backward's buffers and its options (no host-buffer pass, no CPU baseline)
     if args.impl == "reference":
         run_reference(args)
     else:

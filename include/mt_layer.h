@@ -211,9 +211,24 @@ int mt_layer_backward_workspace_bytes(const mt_layer* L, int seq, int batch, siz
 /* dx [T, H] = dL/dx and the requested weight gradients, given x and dy = dL/dy [T, H].  Needs
  * tp_size == 1, seq % 8 == 0, hidden <= 8192 and a workspace of mt_layer_backward_workspace_bytes.  Asynchronous
  * on cuda_stream: the forward recomputed, then the GEMMs, elementwise kernels and the two
- * flash-attention backward kernels (dQ; dK and dV), all on the stream. */
+ * flash-attention backward kernels (dQ; dK and dV); the handle orders two streams of its own after
+ * cuda_stream (the dQ kernel, and the weight gradients beside the chain of dx) and joins them back
+ * into it before the call's work ends. */
 int mt_layer_backward(mt_layer* L, const void* x, const void* dy, int seq, int batch, const mt_weights* w, void* dx,
                       const mt_grads* g, void* cuda_stream);
+
+/* Training without the recompute (the level below activation checkpointing in the memory-saving
+ * ladder of "快速入门" §10.3, which stores the activations instead of recomputing them):
+ * mt_layer_forward_train computes y [T, H] exactly as mt_layer_forward (same kernels, the
+ * same bits) and leaves the intermediates the gradients need in the workspace (of
+ * mt_layer_backward_workspace_bytes); mt_layer_backward_saved then computes what mt_layer_backward
+ * computes from them, without recomputing the forward.  Between the two calls the workspace must
+ * not be used by another call of the handle, and x, seq, batch and the weights must be the same.
+ * Same requirements and errors as mt_layer_backward. */
+int mt_layer_forward_train(mt_layer* L, const void* x, int seq, int batch, const mt_weights* w, void* y,
+                           void* cuda_stream);
+int mt_layer_backward_saved(mt_layer* L, const void* x, const void* dy, int seq, int batch, const mt_weights* w,
+                            void* dx, const mt_grads* g, void* cuda_stream);
 
 /* Where an intermediate lives inside the workspace (for inspection in tests).  `which`:
  * 0 norm1 out [T,H]; 1 q [batch, nh_r, seq, d] after RoPE; 2 k [batch, ng_r, seq, d] after RoPE;

@@ -974,34 +974,46 @@ int norm_bwd(mt_layer* L, const BwLayout& b, const void* dy, const void* x, cons
   return e == cudaSuccess ? MT_OK : cuda_fail(e, "norm backward");
 }
 
-int backward_device(mt_layer* L, const BwLayout& b, const void* x, const void* dy, int S, int B, const mt_weights* w,
-                    void* dx, const mt_grads* g, cudaStream_t st) {
+// The forward intermediates the gradients need, written into the backward workspace: xn, q, k
+// (after RoPE), v, o, h (attention block, with each query row's log-sum-exp), hn, u (fc1's
+// pre-activation output) and a.  The full-recompute backward runs this first; the training forward
+// runs it (plus fc2) so that a later backward can skip it.
+int forward_saving(mt_layer* L, const BwLayout& b, const void* x, int S, int B, const mt_weights* w, cudaStream_t st) {
+  const Layout& lay = b.fwd;
+  const int T = S * B, H = L->hidden, f = L->f_r, f1 = L->f1_r;
+  const bool swiglu = L->act == MT_ACT_SWIGLU;
+  int rc;
+  bf16* h = region<bf16>(L, lay, kH);
+  if ((rc = run_attention_block(L, lay, x, S, B, w, h, mt::kEpiResid, st, nullptr, bwr<float>(L, b, kBLse))))
+    return rc;
+  bf16* hn = region<bf16>(L, lay, kHn);
+  count_launch(L);
+  cudaError_t e = mt::launch_norm(L->norm == MT_NORM_LAYER, h, static_cast<const bf16*>(w->norm2_w),
+                                  static_cast<const bf16*>(w->norm2_b), hn, T, H, L->eps, st);
+  if (e != cudaSuccess) return cuda_fail(e, "norm2 launch");
+  // fc1 with the forward's activation epilogue, which also keeps the pre-activation u
+  mt::GemmParams p = gemm_params(T, f, H, swiglu, L->d_err);
+  p.out = bwr<bf16>(L, b, kBA);
+  p.ldo = f;
+  p.bias = static_cast<const bf16*>(w->b_fc1);
+  p.pre = bwr<bf16>(L, b, kBU);
+  p.ldp = f1;
+  return run_gemm(L, -1, swiglu ? mt::kEpiSwiglu : mt::kEpiGelu, hn, H, w->w_fc1, f1, T, f, H, p, st);
+}
+
+// The gradients from the intermediates forward_saving left in the workspace.
+int backward_from_saved(mt_layer* L, const BwLayout& b, const void* x, const void* dy, int S, int B,
+                        const mt_weights* w, void* dx, const mt_grads* g, cudaStream_t st) {
   const Layout& lay = b.fwd;
   const int T = S * B, H = L->hidden, d = L->head_dim, nh = L->nh_r, ng = L->ng_r;
   const int qw = L->q_w, kvw = L->kv_w, QKV = qw + 2 * kvw, f = L->f_r, f1 = L->f1_r;
   const bool swiglu = L->act == MT_ACT_SWIGLU;
   int rc;
   cudaError_t e;
-  // ---- forward recompute: xn, q, k (after RoPE), v, o, h (attention block), hn, u, a
   bf16* h = region<bf16>(L, lay, kH);
-  if ((rc = run_attention_block(L, lay, x, S, B, w, h, mt::kEpiResid, st, nullptr, bwr<float>(L, b, kBLse))))
-    return rc;
   bf16 *xn = region<bf16>(L, lay, kXn), *hn = region<bf16>(L, lay, kHn), *o = region<bf16>(L, lay, kO);
   bf16 *q = region<bf16>(L, lay, kQ), *k = region<bf16>(L, lay, kK);
-  count_launch(L);
-  e = mt::launch_norm(L->norm == MT_NORM_LAYER, h, static_cast<const bf16*>(w->norm2_w),
-                      static_cast<const bf16*>(w->norm2_b), hn, T, H, L->eps, st);
-  if (e != cudaSuccess) return cuda_fail(e, "norm2 launch");
   bf16 *u = bwr<bf16>(L, b, kBU), *a = bwr<bf16>(L, b, kBA);
-  {  // fc1 with the forward's activation epilogue, which also keeps the pre-activation u
-    mt::GemmParams p = gemm_params(T, f, H, swiglu, L->d_err);
-    p.out = a;
-    p.ldo = f;
-    p.bias = static_cast<const bf16*>(w->b_fc1);
-    p.pre = u;
-    p.ldp = f1;
-    if ((rc = run_gemm(L, -1, swiglu ? mt::kEpiSwiglu : mt::kEpiGelu, hn, H, w->w_fc1, f1, T, f, H, p, st))) return rc;
-  }
 
   // ---- MLP
   bf16 *da = bwr<bf16>(L, b, kBDa), *du = bwr<bf16>(L, b, kBDu), *dhn = bwr<bf16>(L, b, kBDhn);
@@ -1092,6 +1104,13 @@ int backward_device(mt_layer* L, const BwLayout& b, const void* x, const void* d
   return MT_OK;
 }
 
+// Full activation recompute: the forward intermediates, then the gradients.
+int backward_device(mt_layer* L, const BwLayout& b, const void* x, const void* dy, int S, int B, const mt_weights* w,
+                    void* dx, const mt_grads* g, cudaStream_t st) {
+  const int rc = forward_saving(L, b, x, S, B, w, st);
+  return rc ? rc : backward_from_saved(L, b, x, dy, S, B, w, dx, g, st);
+}
+
 }  // namespace
 
 namespace mt {
@@ -1108,6 +1127,32 @@ int num_sms() {
 }  // namespace mt
 
 // ====================================================================== exported C ABI
+namespace {
+// The checks shared by the backward and training-forward entry points (g may be NULL for the
+// training forward, which takes y in place of dy and dx).
+int check_train_call(mt_layer* L, const void* x, const void* dy, int seq, int batch, const mt_weights* w,
+                     const void* dx, const mt_grads* g, bool need_grads, BwLayout* b) {
+  if (L == nullptr) return fail(MT_ERR_INVALID_ARG, "handle is NULL");
+  if (L->tp != 1) return fail(MT_ERR_UNSUPPORTED, "the backward pass is implemented for tp_size == 1");
+  if (x == nullptr || dy == nullptr || dx == nullptr || (need_grads && g == nullptr))
+    return fail(MT_ERR_INVALID_ARG, need_grads ? "x, dy, dx and grads must not be NULL" : "x and y must not be NULL");
+  if (!aligned16(x) || !aligned16(dy) || !aligned16(dx)) return fail(MT_ERR_INVALID_ARG, "x/dy/dx/y must be 16-byte aligned");
+  if (seq <= 0 || batch <= 0) return fail(MT_ERR_INVALID_ARG, "seq and batch must be positive");
+  if (seq % 8) return fail(MT_ERR_UNSUPPORTED, "the backward pass needs seq % 8 == 0");
+  if (L->hidden > 8192) return fail(MT_ERR_UNSUPPORTED, "the backward pass needs hidden <= 8192");
+  if (need_grads) {
+    const void* gp[] = {g->norm1_w, g->norm1_b, g->w_qkv, g->b_qkv, g->w_o, g->b_o,
+                        g->norm2_w, g->norm2_b, g->w_fc1, g->b_fc1, g->w_fc2, g->b_fc2};
+    for (const void* p : gp)
+      if (p != nullptr && !aligned16(p)) return fail(MT_ERR_INVALID_ARG, "gradient buffers must be 16-byte aligned");
+  }
+  *b = bw_layout(L, seq, batch);
+  if (L->ws == nullptr || L->ws_bytes < b->total)
+    return fail(MT_ERR_NO_WORKSPACE, "the backward pass needs a workspace of %zu bytes", b->total);
+  return check_weights(L, w, true, true);
+}
+}  // namespace
+
 extern "C" {
 
 int mt_layer_create(int hidden, int heads, int query_groups, int head_dim, int ffn, int norm, int act,
@@ -1592,24 +1637,38 @@ int mt_layer_backward_workspace_bytes(const mt_layer* L, int seq, int batch, siz
 
 int mt_layer_backward(mt_layer* L, const void* x, const void* dy, int seq, int batch, const mt_weights* w, void* dx,
                       const mt_grads* g, void* cuda_stream) {
-  if (L == nullptr) return fail(MT_ERR_INVALID_ARG, "handle is NULL");
-  if (L->tp != 1) return fail(MT_ERR_UNSUPPORTED, "the backward pass is implemented for tp_size == 1");
-  if (x == nullptr || dy == nullptr || dx == nullptr || g == nullptr)
-    return fail(MT_ERR_INVALID_ARG, "x, dy, dx and grads must not be NULL");
-  if (!aligned16(x) || !aligned16(dy) || !aligned16(dx)) return fail(MT_ERR_INVALID_ARG, "x/dy/dx must be 16-byte aligned");
-  if (seq <= 0 || batch <= 0) return fail(MT_ERR_INVALID_ARG, "seq and batch must be positive");
-  if (seq % 8) return fail(MT_ERR_UNSUPPORTED, "the backward pass needs seq % 8 == 0");
-  if (L->hidden > 8192) return fail(MT_ERR_UNSUPPORTED, "the backward pass needs hidden <= 8192");
-  const void* gp[] = {g->norm1_w, g->norm1_b, g->w_qkv, g->b_qkv, g->w_o, g->b_o,
-                      g->norm2_w, g->norm2_b, g->w_fc1, g->b_fc1, g->w_fc2, g->b_fc2};
-  for (const void* p : gp)
-    if (p != nullptr && !aligned16(p)) return fail(MT_ERR_INVALID_ARG, "gradient buffers must be 16-byte aligned");
-  const BwLayout b = bw_layout(L, seq, batch);
-  if (L->ws == nullptr || L->ws_bytes < b.total)
-    return fail(MT_ERR_NO_WORKSPACE, "the backward pass needs a workspace of %zu bytes", b.total);
-  int rc = check_weights(L, w, true, true);
+  BwLayout b;
+  int rc = check_train_call(L, x, dy, seq, batch, w, dx, g, true, &b);
   if (rc) return rc;
   rc = backward_device(L, b, x, dy, seq, batch, w, dx, g, static_cast<cudaStream_t>(cuda_stream));
+  return rc ? rc : done(L, static_cast<cudaStream_t>(cuda_stream));
+}
+
+int mt_layer_forward_train(mt_layer* L, const void* x, int seq, int batch, const mt_weights* w, void* y,
+                           void* cuda_stream) {
+  BwLayout b;
+  int rc = check_train_call(L, x, x, seq, batch, w, y, nullptr, false, &b);
+  if (rc) return rc;
+  const cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  if ((rc = forward_saving(L, b, x, seq, batch, w, st))) return rc;
+  // fc2 with the residual: y = h + a W_fc2^T + b_fc2, as the forward's last GEMM
+  const int T = seq * batch, H = L->hidden, f = L->f_r;
+  mt::GemmParams p = gemm_params(T, H, f, false, L->d_err);
+  p.out = static_cast<bf16*>(y);
+  p.ldo = H;
+  p.bias = static_cast<const bf16*>(w->b_fc2);
+  p.resid = region<bf16>(L, b.fwd, kH);
+  p.ldr = H;
+  if ((rc = run_gemm(L, kSlotFc2, mt::kEpiResid, bwr<bf16>(L, b, kBA), f, w->w_fc2, H, T, H, f, p, st))) return rc;
+  return done(L, st);
+}
+
+int mt_layer_backward_saved(mt_layer* L, const void* x, const void* dy, int seq, int batch, const mt_weights* w,
+                            void* dx, const mt_grads* g, void* cuda_stream) {
+  BwLayout b;
+  int rc = check_train_call(L, x, dy, seq, batch, w, dx, g, true, &b);
+  if (rc) return rc;
+  rc = backward_from_saved(L, b, x, dy, seq, batch, w, dx, g, static_cast<cudaStream_t>(cuda_stream));
   return rc ? rc : done(L, static_cast<cudaStream_t>(cuda_stream));
 }
 

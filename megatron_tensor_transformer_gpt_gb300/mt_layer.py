@@ -90,6 +90,11 @@ _SIGS = {
     "mt_layer_backward": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                            ctypes.POINTER(MtWeights), ctypes.c_void_p, ctypes.POINTER(MtGrads), ctypes.c_void_p],
                           ctypes.c_int),
+    "mt_layer_forward_train": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                ctypes.POINTER(MtWeights), ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "mt_layer_backward_saved": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                 ctypes.POINTER(MtWeights), ctypes.c_void_p, ctypes.POINTER(MtGrads),
+                                 ctypes.c_void_p], ctypes.c_int),
     "mt_layer_fp8_enable": ([ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
     "mt_layer_fp8_set_scales": ([ctypes.c_void_p, ctypes.POINTER(ctypes.c_float)], ctypes.c_int),
     "mt_layer_fp8_state": ([ctypes.c_void_p, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)],
@@ -255,6 +260,15 @@ def mt_layer_backward(handle, x, dy, seq, batch, weights: MtWeights, dx, grads: 
     _check(lib().mt_layer_backward(handle, x, dy, seq, batch, ctypes.byref(weights), dx, ctypes.byref(grads), stream))
 
 
+def mt_layer_forward_train(handle, x, seq, batch, weights: MtWeights, y, stream):
+    _check(lib().mt_layer_forward_train(handle, x, seq, batch, ctypes.byref(weights), y, stream))
+
+
+def mt_layer_backward_saved(handle, x, dy, seq, batch, weights: MtWeights, dx, grads: "MtGrads", stream):
+    _check(lib().mt_layer_backward_saved(handle, x, dy, seq, batch, ctypes.byref(weights), dx, ctypes.byref(grads),
+                                         stream))
+
+
 def mt_layer_fp8_enable(handle, amax_history_len=1024):
     _check(lib().mt_layer_fp8_enable(handle, int(amax_history_len)))
 
@@ -392,19 +406,39 @@ class Layer:
                                 out.data_ptr(), self._stream(stream))
         return out
 
-    def backward(self, x, dy, seq, batch, weights: MtWeights, dx, grads: Dict[str, "object"], stream=None):
-        """dx and the weight gradients into the given torch tensors (grads: name -> tensor or None)."""
+    def _backward_workspace(self, seq, batch, device):
         import torch
         need = mt_layer_backward_workspace_bytes(self.handle, seq, batch)
         if self._ws is None or self._ws.numel() < need:
-            self._ws = torch.empty(need, dtype=torch.uint8, device=x.device)
+            self._ws = torch.empty(need, dtype=torch.uint8, device=device)
             mt_layer_set_workspace(self.handle, self._ws.data_ptr(), self._ws.numel())
+
+    @staticmethod
+    def _grads(grads):
         g = MtGrads()
         for f in WEIGHT_FIELDS:
             t = grads.get(f)
             setattr(g, f, None if t is None else t.data_ptr())
-        mt_layer_backward(self.handle, x.data_ptr(), dy.data_ptr(), seq, batch, weights, dx.data_ptr(), g,
-                          self._stream(stream))
+        return g
+
+    def backward(self, x, dy, seq, batch, weights: MtWeights, dx, grads: Dict[str, "object"], stream=None):
+        """dx and the weight gradients into the given torch tensors (grads: name -> tensor or None)."""
+        self._backward_workspace(seq, batch, x.device)
+        mt_layer_backward(self.handle, x.data_ptr(), dy.data_ptr(), seq, batch, weights, dx.data_ptr(),
+                          self._grads(grads), self._stream(stream))
+        return dx
+
+    def forward_train(self, x, seq, batch, weights: MtWeights, y, stream=None):
+        """y as forward() computes it, keeping the intermediates for backward_saved()."""
+        self._backward_workspace(seq, batch, x.device)
+        mt_layer_forward_train(self.handle, x.data_ptr(), seq, batch, weights, y.data_ptr(), self._stream(stream))
+        return y
+
+    def backward_saved(self, x, dy, seq, batch, weights: MtWeights, dx, grads: Dict[str, "object"], stream=None):
+        """backward() without the recompute, from the intermediates of the last forward_train()."""
+        self._backward_workspace(seq, batch, x.device)
+        mt_layer_backward_saved(self.handle, x.data_ptr(), dy.data_ptr(), seq, batch, weights, dx.data_ptr(),
+                                self._grads(grads), self._stream(stream))
         return dx
 
     def forward_host(self, x_host, seq, batch, weights: MtWeights, y_host, stream=None):

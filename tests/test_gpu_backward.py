@@ -99,3 +99,42 @@ def test_backward_rejects_unsupported():
                              ml.MtGrads(), None)
     assert e.value.code == ml.MT_ERR_UNSUPPORTED
     layer.close()
+
+
+@pytest.mark.parametrize("cfg", [CFGS[1], CFGS[2], CFGS[5], KSPLIT_CFGS[1]], ids=lambda c: c.name)
+def test_forward_train_and_backward_saved_match_forward_and_backward(cfg):
+    """mt_layer_forward_train gives mt_layer_forward's y bit for bit, and mt_layer_backward_saved
+    after it gives mt_layer_backward's dx and weight-matrix gradients bit for bit (the same kernels on
+    the same intermediates); the norm-weight and bias gradients, whose column sums add per-CTA
+    partial rows atomically in no fixed order, agree within the gradient tolerance."""
+    inp = synth.make_inputs(cfg, seed=83, affine="random", biases="random")
+    T, H = cfg.tokens, cfg.hidden
+    dy = to_dev(synth.f32_to_bf16_bits(np.random.default_rng(84).standard_normal((T, H)).astype(np.float32)))
+    dl = DeviceLayer(cfg, inp)
+    x = to_dev(inp["x"]).reshape(T, H)
+
+    def run(saved):
+        y, dx = torch.empty_like(x), torch.empty_like(x)
+        grads = {k: (None if v is None else torch.empty_like(v)) for k, v in dl.tens.items()}
+        if saved:
+            dl.layer.forward_train(x, cfg.seq, cfg.batch, dl.w, y)
+            dl.layer.backward_saved(x, dy, cfg.seq, cfg.batch, dl.w, dx, grads)
+        else:
+            dl.layer.forward(x, cfg.seq, cfg.batch, dl.w, y)
+            dl.layer.backward(x, dy, cfg.seq, cfg.batch, dl.w, dx, grads)
+        torch.cuda.synchronize()
+        dl.layer.status()
+        return y, dx, grads
+
+    y0, dx0, g0 = run(False)
+    y1, dx1, g1 = run(True)
+    dl.close()
+    assert torch.equal(y0, y1), "forward_train's y differs from forward's"
+    assert torch.equal(dx0, dx1), "dx differs"
+    for name, t in g0.items():
+        if t is None:
+            assert g1[name] is None
+        elif name.startswith("w_"):
+            assert torch.equal(t, g1[name]), name
+        else:
+            assert_grad_close(to_f64(g1[name]), to_f64(t), name)
